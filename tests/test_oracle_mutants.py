@@ -1,0 +1,69 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+the pins of `test_oracle_pins.py` catch every one of them."""
+import os
+import types
+
+import pytest
+
+import test_oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "kvq_oracle.py")
+
+MUTANTS = {
+    "rope-sign": ("y[..., :half] = x1 * c - x2 * s", "y[..., :half] = x1 * c + x2 * s"),
+    "rope-freq-over-R": ("f = rope_inv_freq(theta, D, R)", "f = rope_inv_freq(theta, R, R)"),
+    "rope-interleaved-pairs": ("x1 = x[..., :half]\n    x2 = x[..., half:R]",
+                               "x1 = x[..., 0:R:2]\n    x2 = x[..., 1:R:2]"),
+    "norm-weight-dropped": ("y = y * np.asarray(w, dtype=np.float64)", "y = y * 1.0"),
+    "norm-eps-outside-sqrt": ("np.sqrt(ms + float(eps))", "(np.sqrt(ms) + float(eps))"),
+    "norm-no-mean": ("ms = np.mean(x * x, axis=-1, keepdims=True)",
+                     "ms = np.sum(x * x, axis=-1, keepdims=True)"),
+    "quant-divide-by-fp32-scale": ("safe = np.where(s == 0, np.float32(1), s)",
+                                   "safe = np.where(s == 0, np.float32(1), s32)"),
+    "quant-round-half-up": ("c = np.clip(np.rint(q), 0, 2 ** bits - 1)",
+                            "c = np.clip(np.floor(q + np.float32(0.5)), 0, 2 ** bits - 1)"),
+    "quant-levels-2^b": ("levels = np.float32(2 ** bits - 1)", "levels = np.float32(2 ** bits)"),
+    "quant-bias-max": ("bias = mn\n", "bias = mx\n"),
+    "pack-big-endian": ("words |= c[..., i] << np.uint64(i * bits)",
+                        "words |= c[..., per - 1 - i] << np.uint64(i * bits)"),
+    "window-off-by-one": ("max(0, p - window + 1)", "max(0, p - window)"),
+    "gqa-modulo-mapping": ("out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh * G:(kvh + 1) * G], K[:, kvh], V[:, kvh])",
+                           "out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh::n_kv_heads], K[:, kvh], V[:, kvh])"),
+    "softmax-unnormalised": ("return (p @ v_hat) / p.sum(axis=-1, keepdims=True)", "return (p @ v_hat)"),
+    "sdpa-scale-rsqrt-d": ("s = q_hat @ k_hat.T ", "s = q_hat @ k_hat.T / np.sqrt(q_hat.shape[-1]) "),
+    "dequant-no-bias": ("x = c * np.asarray(scales)[..., None] + np.asarray(biases)[..., None]",
+                        "x = c * np.asarray(scales)[..., None]"),
+    "v-norm-weighted": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
+                        "v_hat = rms_norm(k_raw if v_raw is None else v_raw, k_w, eps)"),
+    "bf16-7-bits": ("q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
+                    "q = np.ldexp(np.rint(np.ldexp(x, 7 - e)), e - 7)"),
+}
+
+PINS = [
+    P.pin_rn_bf16, P.pin_quant_ramp4, P.pin_quant_exact8, P.pin_quant_constant,
+    P.pin_quant_ties, P.pin_quant_bf16_scale_divides, P.pin_quant_group_independence,
+    lambda o: P.pin_quant_invariants(o, 4), lambda o: P.pin_quant_invariants(o, 8),
+    P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants,
+    P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,
+]
+
+
+def _mutant(old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    m = types.ModuleType("kvq_oracle_mutant")
+    exec(compile(src.replace(old, new), "kvq_oracle_mutant", "exec"), m.__dict__)
+    return m
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    m = _mutant(*MUTANTS[name])
+    caught = []
+    for pin in PINS:
+        try:
+            pin(m)
+        except Exception:          # an assertion or a crash both count as caught
+            caught.append(getattr(pin, "__name__", "pin"))
+    assert caught, f"no pin catches mutant {name}"

@@ -1,0 +1,433 @@
+"""Pins of the float64 oracle to facts outside itself.
+
+The pages print no worked example of the quantizer, the norms, RoPE or the
+attention read, so the oracle is pinned by hand-worked cases (derivations in
+the comments), closed forms, invariants and brute force on tiny inputs.  Each
+pin is a function of the oracle module `o`, so `test_oracle_mutants.py` can
+run the same pins against copies of the oracle with a planted mistake and
+check that some pin fails.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------
+# bf16 rounding
+# ----------------------------------------------------------------------------
+
+def pin_rn_bf16(o):
+    # bf16 has 8 significant bits: in [1, 2) the spacing is 2^-7.
+    assert o.rn_bf16(np.array([1.0 + 2 ** -8]))[0] == 1.0               # tie -> even (1.0)
+    assert o.rn_bf16(np.array([1.0 + 3 * 2 ** -8]))[0] == 1.0 + 2 ** -6  # tie -> even (up)
+    assert o.rn_bf16(np.array([1.0 + 2 ** -8 + 2 ** -30]))[0] == 1.0 + 2 ** -7
+    assert o.rn_bf16(np.array([-1.0 - 2 ** -8 - 2 ** -30]))[0] == -1.0 - 2 ** -7
+    # every float32 whose low 16 bits are zero is a fixed point
+    rng = np.random.default_rng(0)
+    u = (rng.integers(0, 2 ** 16, 5000).astype(np.uint32) << 16)
+    f = u.view(np.float32)
+    f = f[np.isfinite(f)].astype(np.float64)
+    assert np.array_equal(o.rn_bf16(f), f)
+    # agreement with rounding the float32 bit pattern for float32 inputs
+    x = rng.standard_normal(20000).astype(np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    ref = b.astype(np.uint32).view(np.float32).astype(np.float64)
+    assert np.array_equal(o.rn_bf16(x.astype(np.float64)), ref)
+
+
+def test_rn_bf16():
+    pin_rn_bf16(O)
+
+
+# ----------------------------------------------------------------------------
+# quantizer, hand-worked cases
+# ----------------------------------------------------------------------------
+
+def pin_quant_ramp4(o):
+    # x_i = (i mod 16) * 0.25: max - min = 3.75, 3.75 / 15 = 0.25 exactly, so
+    # scale 0.25, bias 0, codes i mod 16; word 0 holds codes 0..7 low nibble
+    # first: 0x76543210.
+    x = (np.arange(64) % 16) * 0.25
+    c, s, b = o.quantize(x[None], 4)
+    assert s[0, 0] == 0.25 and b[0, 0] == 0.0
+    assert np.array_equal(c[0], np.arange(64) % 16)
+    w = o.pack(c, 4)
+    assert w[0, 0] == 0x76543210 and w[0, 1] == 0xFEDCBA98
+
+
+def pin_quant_exact8(o):
+    # x_i = c_i / 64 with integer c_i in [0, 255] including 0 and 255:
+    # (255/64) / 255 = 1/64 exactly -> scale 1/64, bias 0, codes c_i.
+    rng = np.random.default_rng(1)
+    ci = rng.integers(0, 256, 64)
+    ci[3], ci[40] = 0, 255
+    c, s, b = o.quantize((ci / 64.0)[None], 8)
+    assert s[0, 0] == 1 / 64 and b[0, 0] == 0.0
+    assert np.array_equal(c[0], ci)
+    w = o.pack(np.array([[1, 2, 3, 4]]), 8)
+    assert w[0, 0] == 0x04030201
+
+
+def pin_quant_constant(o):
+    # a constant group: max == min -> scale 0, every code 0, bias = the value
+    c, s, b = o.quantize(np.full((1, 64), -1.375), 4)
+    assert s[0, 0] == 0.0 and b[0, 0] == -1.375 and not c.any()
+    assert np.all(o.dequantize(c, s, b) == -1.375)
+
+
+def pin_quant_ties(o):
+    # min 0, max 15 -> scale 1.  (x - 0) / 1 = 2.5 -> 2 and 3.5 -> 4 (half to even)
+    x = np.zeros(64)
+    x[1], x[2], x[3], x[4] = 15.0, 2.5, 3.5, 0.5
+    c, s, _ = o.quantize(x[None], 4)
+    assert s[0, 0] == 1.0
+    assert (c[0, 2], c[0, 3], c[0, 4], c[0, 1]) == (2, 4, 0, 15)
+
+
+def pin_quant_bf16_scale_divides(o):
+    # The stored bf16 scale is the divisor.  8-bit, min 0 max 1:
+    # 1/255 = 2^-8 * 1.0039..., i.e. 128.502 units of 2^-15 -> bf16 scale
+    # 129 * 2^-15 = 0.003936767578125.  1 / that = 254.0155 -> code 254
+    # (not 255), 0.5 / that = 127.0078 -> code 127.
+    x = np.zeros(64)
+    x[1], x[2] = 1.0, 0.5
+    c, s, _ = o.quantize(x[None], 8)
+    assert s[0, 0] == 129 * 2.0 ** -15
+    assert (c[0, 1], c[0, 2]) == (254, 127)
+    # 4-bit: 1/15 = 136.53 units of 2^-11 -> scale 137 * 2^-11; 1 / scale
+    # = 14.9489 -> code 15.
+    c, s, _ = o.quantize(x[None], 4)
+    assert s[0, 0] == 137 * 2.0 ** -11
+    assert c[0, 1] == 15 and c[0, 2] == 7      # 0.5 / s = 7.4745 -> 7
+
+
+def pin_quant_group_independence(o):
+    # groups of 64 along the row are quantized independently
+    rng = np.random.default_rng(2)
+    x = o.rn_bf16(rng.standard_normal((3, 256)))
+    c, s, b = o.quantize(x, 4)
+    for g in range(4):
+        cg, sg, bg = o.quantize(x[:, 64 * g:64 * (g + 1)], 4)
+        assert np.array_equal(c[:, 64 * g:64 * (g + 1)], cg)
+        assert np.array_equal(s[:, g], sg[:, 0]) and np.array_equal(b[:, g], bg[:, 0])
+
+
+@pytest.mark.parametrize("pin", [pin_quant_ramp4, pin_quant_exact8, pin_quant_constant,
+                                 pin_quant_ties, pin_quant_bf16_scale_divides,
+                                 pin_quant_group_independence])
+def test_quant_hand_cases(pin):
+    pin(O)
+
+
+def pin_quant_invariants(o, bits):
+    """Codes in range; bias = group min; dequant error <= scale/2 except at the
+    clamped top code; the chosen code is a nearest code by brute force; pack
+    and unpack are inverse."""
+    rng = np.random.default_rng(10 + bits)
+    x = o.rn_bf16(rng.standard_normal((200, 256)) * rng.uniform(0.01, 10, (200, 1)))
+    c, s, b = o.quantize(x, bits)
+    top = 2 ** bits - 1
+    assert c.min() >= 0 and c.max() <= top
+    g = x.reshape(200, 4, 64)
+    assert np.array_equal(b, g.min(-1))
+    # the scale is within half a bf16 ulp of (max - min) / top
+    s_exact = (g.max(-1) - g.min(-1)) / top
+    assert np.all(np.abs(s - s_exact) <= s_exact * 2.0 ** -8 * 1.0001)
+    xh = o.dequantize(c, s, b).reshape(200, 4, 64)
+    err = np.abs(xh - g)
+    slack = top * np.abs(s - s_exact)                  # clamp slack at the top code
+    cg = c.reshape(200, 4, 64)
+    bound = np.where(cg == top, s[..., None] / 2 + slack[..., None], s[..., None] / 2)
+    assert np.all(err <= bound * (1 + 1e-6) + 1e-12)
+    # brute force: no code reconstructs x more closely (up to fp32 rounding of
+    # the quotient)
+    codes = np.arange(top + 1)
+    recon = codes[None, None, None, :] * s[..., None, None] + b[..., None, None]
+    best = np.min(np.abs(recon - g[..., None]), axis=-1)
+    assert np.all(err <= best + s[..., None] * 1e-5 + 1e-12)
+    assert np.array_equal(o.unpack(o.pack(c, bits), bits), c)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quant_invariants(bits):
+    pin_quant_invariants(O, bits)
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm
+# ----------------------------------------------------------------------------
+
+def pin_rms_hand(o):
+    # x = [1, 2], w = 1, eps = 0: mean square 2.5, 1/sqrt(2.5) = 0.632455532...
+    # = 161.909 units of 2^-8 -> 162 * 2^-8 = 0.6328125; 2/sqrt(2.5) =
+    # 1.264911 = 161.909 units of 2^-7 -> 1.265625.
+    y = o.rms_norm(np.array([[1.0, 2.0]]), None, 0.0)
+    assert y[0, 0] == 0.6328125 and y[0, 1] == 1.265625
+    # the weight multiplies: w = [2, -0.5] -> [1.265625, -0.6328125]
+    y = o.rms_norm(np.array([[1.0, 2.0]]), np.array([2.0, -0.5]), 0.0)
+    assert y[0, 0] == 1.265625 and y[0, 1] == -0.6328125
+    # eps enters under the square root: x = [1, 1], eps = 3 -> 1/sqrt(4) = 0.5
+    y = o.rms_norm(np.array([[1.0, 1.0]]), None, 3.0)
+    assert np.all(y == 0.5)
+
+
+def pin_rms_invariants(o):
+    rng = np.random.default_rng(3)
+    x = o.rn_bf16(rng.standard_normal((50, 256)))
+    w = o.rn_bf16(1 + 0.1 * rng.standard_normal(256))
+    # scale invariance with eps = 0 (powers of two scale exactly)
+    assert np.array_equal(o.rms_norm(x * 8.0, w, 0.0), o.rms_norm(x, w, 0.0))
+    # a row of +-c gives sign * w
+    row = np.where(rng.random(256) < 0.5, -3.0, 3.0)[None]
+    assert np.array_equal(o.rms_norm(row, w, 0.0), np.sign(row) * w)
+    # the result has mean square ~1 (w = 1) up to bf16 rounding
+    y = o.rms_norm(x, None, 1e-6)
+    assert np.allclose(np.mean(y * y, -1), 1.0, rtol=1e-2)
+
+
+def test_rms_norm():
+    pin_rms_hand(O)
+    pin_rms_invariants(O)
+
+
+# ----------------------------------------------------------------------------
+# RoPE
+# ----------------------------------------------------------------------------
+
+def pin_rope_hand(o):
+    # D = R = 4, theta 1e4, pos 1: frequencies 1 and 1e4^(-1/2) = 0.01; pairs
+    # (0, 2) and (1, 3).  x = [1, 0, 0, 0] -> x0' = cos 1 = 0.540302 = 138.317
+    # units of 2^-8 -> 138/256 = 0.5390625; x2' = sin 1 = 0.841471 = 215.417
+    # units of 2^-8 -> 215/256 = 0.83984375.
+    y = o.rope(np.array([[[1.0, 0, 0, 0]]]), np.array([1]), 1e4, 4)
+    assert np.array_equal(y[0, 0], [138 / 256, 0.0, 215 / 256, 0.0])
+    # x = [0, 0, 1, 0] -> x0' = -sin 1 -> -0.83984375, x2' = cos 1
+    y = o.rope(np.array([[[0, 0, 1.0, 0]]]), np.array([1]), 1e4, 4)
+    assert np.array_equal(y[0, 0], [-215 / 256, 0.0, 138 / 256, 0.0])
+
+
+def _textbook_rope(x, pos, theta):
+    """Non-interleaved ("rotate half") RoPE as complex multiplication:
+    z_j = x_j + i x_{j+D/2} times exp(i pos theta^(-2j/D))."""
+    D = x.shape[-1]
+    h = D // 2
+    z = x[..., :h] + 1j * x[..., h:]
+    ang = np.asarray(pos, float)[:, None] * theta ** (-2.0 * np.arange(h) / D)
+    z = z * np.exp(1j * ang)[:, None, :]
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def pin_rope_invariants(o):
+    rng = np.random.default_rng(4)
+    x = o.rn_bf16(rng.standard_normal((6, 2, 256)))
+    pos = np.array([0, 1, 7, 511, 4096, 32768])
+    # pos 0 and R = 0 are the identity
+    assert np.array_equal(o.rope(x[:1], np.array([0]), 1e4, 256), x[:1])
+    assert np.array_equal(o.rope(x, pos, 1e4, 0), x)
+    # R = D is textbook RoPE (then rounded to bf16)
+    full = o.rope(x, pos, 1e4, 256)
+    assert np.array_equal(full, o.rn_bf16(_textbook_rope(x, pos, 1e4)))
+    # partial: the first R dims are textbook RoPE over an R-dim vector whose
+    # frequencies are those of the full D; dims >= R untouched
+    R = 64
+    part = o.rope(x, pos, 1e6, R)
+    assert np.array_equal(part[..., R:], x[..., R:])
+    theta_eff = 1e6 ** (R / 256)         # theta^(-2j/D) == (theta^(R/D))^(-2j/R)
+    ref = _textbook_rope(x[..., :R], pos, theta_eff)
+    assert np.allclose(part[..., :R], ref, atol=2 ** -6, rtol=2 ** -7)
+    # pair norms are preserved up to bf16 rounding
+    n0 = x[..., :32] ** 2 + x[..., 32:64] ** 2
+    n1 = part[..., :32] ** 2 + part[..., 32:64] ** 2
+    assert np.allclose(n0, n1, rtol=2e-2, atol=1e-3)
+    # relative position: q(m).k(n) depends on m - n only
+    q = x[:1, :1]
+    k = x[1:2, :1]
+    d1 = np.sum(o.rope(q, [100], 1e4, 256) * o.rope(k, [90], 1e4, 256))
+    d2 = np.sum(o.rope(q, [2010], 1e4, 256) * o.rope(k, [2000], 1e4, 256))
+    assert abs(d1 - d2) < 0.1
+
+
+def test_rope():
+    pin_rope_hand(O)
+    pin_rope_invariants(O)
+
+
+# ----------------------------------------------------------------------------
+# attention read
+# ----------------------------------------------------------------------------
+
+def _cache_with(o, k_hat, v_hat, bits=8):
+    c = o.OracleCache(k_hat.shape[1], k_hat.shape[2], bits)
+    c.append(np.arange(k_hat.shape[0]), k_hat, v_hat)
+    return c
+
+
+def pin_attention(o):
+    rng = np.random.default_rng(5)
+    n, H, D, Hq = 40, 2, 64, 8
+    kh = o.rn_bf16(rng.standard_normal((n, H, D)))
+    vh = o.rn_bf16(rng.standard_normal((n, H, D)))
+    cache = _cache_with(o, kh, vh)
+    q = o.rn_bf16(rng.standard_normal((Hq, D)))
+
+    def run(p, window, qq=q, c=cache):
+        return o.attend_cache(qq, p, window, H, c.k_hat, c.v_hat)
+
+    # one visible key (p = 0, or window 1): the output is that key's v_hat
+    assert np.allclose(run(0, 0), np.repeat(cache.v_hat(0, 0)[0], Hq // H, axis=0), atol=1e-12)
+    assert np.allclose(run(17, 1), np.repeat(cache.v_hat(17, 17)[0], Hq // H, axis=0), atol=1e-12)
+    # window >= p + 1 equals full causal
+    assert np.allclose(run(30, 31), run(30, 0), atol=1e-14)
+    assert np.allclose(run(30, 1000), run(30, 0), atol=1e-14)
+    # keys outside the window (and in the future) do not matter
+    kh2, vh2 = kh.copy(), vh.copy()
+    kh2[:20] += 3.0
+    vh2[:20] -= 5.0
+    kh2[31:] *= -1
+    c2 = _cache_with(o, kh2, vh2)
+    assert np.allclose(run(30, 11, c=c2), run(30, 11), atol=1e-14)
+    # GQA: q head h reads kv head h // (Hq / Hkv): heads 0-3 see kv head 0
+    out = run(25, 0)
+    only0 = o.attend(q[:4], cache.k_hat(0, 25)[:, 0], cache.v_hat(0, 25)[:, 0])
+    assert np.allclose(out[:4], only0, atol=1e-14)
+    # equal q heads give equal outputs
+    q3 = q.copy()
+    q3[1] = q3[0]
+    o3 = run(25, 0, qq=q3)
+    assert np.array_equal(o3[0], o3[1])
+    # closed form for two keys: out = v1 + sigmoid(s2 - s1) (v2 - v1)
+    K = cache.k_hat(10, 11)[:, 1]
+    V = cache.v_hat(10, 11)[:, 1]
+    s = q[4:] @ K.T
+    sig = 1.0 / (1.0 + np.exp(-(s[:, 1] - s[:, 0])))
+    closed = V[0][None] + sig[:, None] * (V[1] - V[0])[None]
+    assert np.allclose(run(11, 2)[4:], closed, atol=1e-12)
+    # equal logits -> the mean of the values
+    kk = np.zeros((2, 1, D)); kk[:] = kh[0, 0]
+    vv = vh[:2, :1]
+    c4 = _cache_with(o, kk, vv)
+    r = o.attend_cache(q[:1], 1, 0, 1, c4.k_hat, c4.v_hat)
+    assert np.allclose(r[0], c4.v_hat(0, 1)[:, 0].mean(0), atol=1e-12)
+    # scale 1.0 and max subtraction: huge logits stay finite and pick the argmax
+    big = run(39, 0, qq=q * 64.0)
+    assert np.all(np.isfinite(big))
+    # the output is a convex combination of the visible values
+    out = run(39, 8)
+    vis = cache.v_hat(32, 39)
+    for h in range(Hq):
+        lo, hi = vis[:, h // 4].min(0), vis[:, h // 4].max(0)
+        assert np.all(out[h] >= lo - 1e-12) and np.all(out[h] <= hi + 1e-12)
+
+
+def test_attention():
+    pin_attention(O)
+
+
+def pin_brute_force_attention(o):
+    """Tiny case summed term by term over explicit (key, dim) loops with the
+    softmax written as exp(s_j) / sum exp(s_i) without max subtraction."""
+    rng = np.random.default_rng(6)
+    n, D = 6, 64
+    kh = o.rn_bf16(rng.standard_normal((n, 1, D)) * 0.2)
+    vh = o.rn_bf16(rng.standard_normal((n, 1, D)))
+    cache = _cache_with(o, kh, vh, bits=4)
+    q = o.rn_bf16(rng.standard_normal((1, D)) * 0.2)
+    K = cache.k_hat(0, n - 1)[:, 0]
+    V = cache.v_hat(0, n - 1)[:, 0]
+    # K / V dequantized: codes * scale + bias, rebuilt here from unpacked
+    # packed words to tie the attention to the packed storage
+    words = cache.packed(np.arange(n))
+    kc = o.unpack(words[0], 4)[:, 0]
+    ks = o.bf16_to_f64(words[1])[:, 0]
+    kb = o.bf16_to_f64(words[2])[:, 0]
+    Kb = np.array([[kc[j, d] * ks[j, d // 64] + kb[j, d // 64] for d in range(D)] for j in range(n)])
+    assert np.array_equal(K, Kb)
+    e = [math.exp(sum(q[0, d] * K[j, d] for d in range(D))) for j in range(n)]
+    ref = [sum(e[j] * V[j, d] for j in range(n)) / sum(e) for d in range(D)]
+    got = o.attend_cache(q, n - 1, 0, 1, cache.k_hat, cache.v_hat)[0]
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_brute_force_attention():
+    pin_brute_force_attention(O)
+
+
+# ----------------------------------------------------------------------------
+# whole steps
+# ----------------------------------------------------------------------------
+
+def pin_keqv(o):
+    """K = V with w_k = 1 and no RoPE: the K and V caches are bit-identical
+    (kNorm with unit weight equals the un-scaled vNorm)."""
+    rng = np.random.default_rng(7)
+    layer = W.LayerSpec(4, 1, 128, 0, 0, 1e6, True)
+    k_raw = o.rn_bf16(rng.standard_normal((5, 1, 128)))
+    kh, vh = o.prep_kv(k_raw, None, np.ones(128), np.arange(5), 1e6, 0, layer.rms_eps)
+    assert np.array_equal(kh, vh)
+    c = o.OracleCache(1, 128, 4)
+    c.append(np.arange(5), kh, vh)
+    w = c.packed(np.arange(5))
+    assert all(np.array_equal(w[i], w[i + 3]) for i in range(3))
+    # v gets the un-scaled norm even when k carries a weight (hand case of
+    # pin_rms_hand: x = [1, 2] -> [0.6328125, 1.265625]; with w = [2, -0.5]
+    # the k side is [1.265625, -0.6328125])
+    kh1, vh1 = o.prep_kv(np.array([[[1.0, 2.0]]]), None, np.array([2.0, -0.5]),
+                         np.array([3]), 1e4, 0, 0.0)
+    assert np.array_equal(kh1[0, 0], [1.265625, -0.6328125])
+    assert np.array_equal(vh1[0, 0], [0.6328125, 1.265625])
+    # with a weight and RoPE the two differ
+    kh2, vh2 = o.prep_kv(k_raw, None, 1 + 0.1 * np.ones(128), np.arange(5), 1e6, 64, 1e-6)
+    assert not np.array_equal(kh2, vh2)
+
+
+def pin_prefill_matches_decode(o):
+    """A chunk of T tokens gives the same cache and outputs as T decode steps."""
+    rng = np.random.default_rng(8)
+    layer = W.LayerSpec(4, 2, 64, 5, 64, 1e4, False)
+    T = 7
+    qr = o.rn_bf16(rng.standard_normal((T, 4, 64)))
+    kr = o.rn_bf16(rng.standard_normal((T, 2, 64)))
+    vr = o.rn_bf16(rng.standard_normal((T, 2, 64)))
+    qw = o.rn_bf16(1 + 0.1 * rng.standard_normal(64))
+    kw = o.rn_bf16(1 + 0.1 * rng.standard_normal(64))
+    c1 = o.OracleCache(2, 64, 4)
+    _, _, _, outs = o.prefill_chunk(layer, c1, 0, qr, qw, kr, vr, kw)
+    c2 = o.OracleCache(2, 64, 4)
+    for t in range(T):
+        _, _, _, out = o.decode_step(layer, c2, t, qr[t], qw, kr[t], vr[t], kw)
+        assert np.allclose(out, outs[t], atol=1e-14)
+    for a, b in zip(c1.packed(np.arange(T)), c2.packed(np.arange(T))):
+        assert np.array_equal(a, b)
+
+
+def test_steps():
+    pin_keqv(O)
+    pin_prefill_matches_decode(O)
+
+
+# ----------------------------------------------------------------------------
+# the workload structure against the page's layer table
+# ----------------------------------------------------------------------------
+
+def test_stack_matches_e4b_layer_table():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4b_layers.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            rows.append(line.split())
+    assert len(rows) == W.N_LAYERS == 42
+    for layer, attn, cache, bits, group, keqv in rows:
+        i = int(layer)
+        assert W.stack_layer_kind(i) == attn
+        assert W.stack_cache_layer(i) == int(cache)
+        assert int(group) == W.GROUP == 64 and int(bits) in (4, 8)
+    assert sum(1 for r in rows if int(r[0]) == int(r[2])) == W.N_DONORS == 24

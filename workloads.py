@@ -1,0 +1,289 @@
+"""Seeded synthetic inputs for the quantized-KV attention path.
+
+This module is the one place both sides of every parity check draw their
+inputs from: the CUDA library (through its Python binding) and the float64
+oracle. It holds random number generation, the f32 -> bf16 bit conversion of
+generated values, and the shapes of the workloads. It holds none of the
+method's arithmetic (no norm, RoPE, quantizer or attention).
+
+Workload shapes follow the e4b layer table of the Gemma 4 pages
+(gemma4-e4b.ts, `LAYERS`: sliding layers with a 4- or 8-bit affine cache of
+group 64, one full layer in six, KV-shared layers 24..41 reading the last donor
+of their own type) and the parity notes of model.ts (full layers: head_dim 512,
+one KV head, K = V, partial rotary factor).
+
+Every stream of random numbers is keyed by (seed, purpose, layer, sequence) so
+any single sequence of any layer can be regenerated on its own.
+"""
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+GROUP = 64
+TILE_KEYS = 64          # cache capacities are kept a multiple of this
+
+
+# ----------------------------------------------------------------------------
+# random streams and bf16 bit patterns of generated values
+# ----------------------------------------------------------------------------
+
+def _rng(seed: int, *key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *key])))
+
+
+def bf16_bits_from_f32(a: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even of float32 values to bf16 bit patterns (uint16).
+
+    Generated values are finite, so no NaN handling is needed."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def normal_bf16(seed: int, key: tuple, shape, loc: float = 0.0, scale: float = 1.0) -> np.ndarray:
+    """bf16 bit patterns of N(loc, scale^2) draws from the stream `key`."""
+    g = _rng(seed, *key)
+    a = g.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        a = a * np.float32(scale)
+    if loc != 0.0:
+        a = a + np.float32(loc)
+    return bf16_bits_from_f32(a)
+
+
+# stream purposes
+P_Q, P_K, P_V, P_QW, P_KW, P_CACHE_K, P_CACHE_V, P_BITS, P_LEN = range(9)
+
+
+# ----------------------------------------------------------------------------
+# layer and workload descriptions
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class LayerSpec:
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    window: int            # 0 = full causal
+    rope_dims: int
+    rope_theta: float
+    k_eq_v: bool
+    rms_eps: float = 1e-6
+
+    @property
+    def group_ratio(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+
+SLIDING = LayerSpec(n_q_heads=8, n_kv_heads=2, head_dim=256, window=512,
+                    rope_dims=256, rope_theta=1e4, k_eq_v=False)
+FULL_KEQV = LayerSpec(n_q_heads=16, n_kv_heads=1, head_dim=512, window=0,
+                      rope_dims=128, rope_theta=1e6, k_eq_v=True)
+
+
+def round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+def ring_capacity(window: int, rows_per_call: int = 1) -> int:
+    """Slots a sliding-window ring needs so that appending `rows_per_call` rows
+    never overwrites a key an earlier query of the same call still sees."""
+    return round_up(window + rows_per_call - 1, TILE_KEYS)
+
+
+def linear_capacity(max_pos: int) -> int:
+    return round_up(max_pos + 1, TILE_KEYS)
+
+
+@dataclasses.dataclass
+class DecodeWorkload:
+    """One decode step of one layer: every sequence has `filled[s]` cached
+    tokens (positions 0..filled-1) and appends one token at position filled[s]."""
+    name: str
+    seed: int
+    layer: LayerSpec
+    filled: list            # per sequence
+    bits: list              # per sequence
+    layer_id: int = 0
+
+    @property
+    def n_seqs(self) -> int:
+        return len(self.filled)
+
+    def capacity(self, s: int) -> int:
+        if self.layer.window > 0:
+            return ring_capacity(self.layer.window)
+        return linear_capacity(self.filled[s])
+
+    def cached_positions(self, s: int) -> np.ndarray:
+        """Positions whose rows are still resident before the step's append
+        (older rows of a ring were overwritten and are never read)."""
+        lo = 0
+        if self.layer.window > 0:
+            lo = max(0, self.filled[s] - self.capacity(s) + 1)
+        return np.arange(lo, self.filled[s], dtype=np.int64)
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    """One prompt chunk: every sequence holds `filled[s]` cached tokens and
+    appends `chunk` new tokens at positions filled[s] .. filled[s]+chunk-1."""
+    name: str
+    seed: int
+    layer: LayerSpec
+    filled: list
+    chunk: list             # rows per sequence
+    bits: list
+    layer_id: int = 0
+
+    @property
+    def n_seqs(self) -> int:
+        return len(self.filled)
+
+    def capacity(self, s: int) -> int:
+        if self.layer.window > 0:
+            return ring_capacity(self.layer.window, max(self.chunk))
+        return linear_capacity(self.filled[s] + self.chunk[s] - 1)
+
+    def cached_positions(self, s: int) -> np.ndarray:
+        lo = 0
+        if self.layer.window > 0:
+            lo = max(0, self.filled[s] - self.capacity(s) + self.chunk[s])
+        return np.arange(lo, self.filled[s], dtype=np.int64)
+
+
+def layer_inputs(seed: int, layer_id: int, layer: LayerSpec, n_rows_q: int, n_rows_kv: int,
+                 seq: int | None = None):
+    """Norm weights (~1+N(0, 0.1)) and raw q/k/v rows (~N(0,1)) as bf16 bits.
+
+    Returns dict with q [n_rows_q, Hq, D], k [n_rows_kv, Hkv, D], v (or None
+    when K = V), q_w [D], k_w [D]."""
+    D = layer.head_dim
+    sk = () if seq is None else (seq,)
+    out = {
+        "q_w": normal_bf16(seed, (P_QW, layer_id), (D,), loc=1.0, scale=0.1),
+        "k_w": normal_bf16(seed, (P_KW, layer_id), (D,), loc=1.0, scale=0.1),
+        "q": normal_bf16(seed, (P_Q, layer_id, *sk), (n_rows_q, layer.n_q_heads, D)),
+        "k": normal_bf16(seed, (P_K, layer_id, *sk), (n_rows_kv, layer.n_kv_heads, D)),
+        "v": None,
+    }
+    if not layer.k_eq_v:
+        out["v"] = normal_bf16(seed, (P_V, layer_id, *sk), (n_rows_kv, layer.n_kv_heads, D))
+    return out
+
+
+def cache_rows(seed: int, layer_id: int, seq: int, layer: LayerSpec, positions: np.ndarray):
+    """Raw k (and v) rows [n, Hkv, D] for the listed cached positions of one
+    sequence, as bf16 bits.  The stream is keyed by sequence, so a row's values
+    depend only on (seed, layer, sequence, position-index-from-0)."""
+    n_all = int(positions[-1]) + 1 if len(positions) else 0
+    first = int(positions[0]) if len(positions) else 0
+    D, H = layer.head_dim, layer.n_kv_heads
+    # Draw only the rows from `first` onward: each stream is generated in
+    # fixed blocks of 256 positions so that any suffix can be drawn alone.
+    def draw(purpose):
+        blocks = []
+        b0, b1 = first // 256, (n_all + 255) // 256
+        for b in range(b0, b1):
+            blocks.append(normal_bf16(seed, (purpose, layer_id, seq, b), (256, H, D)))
+        if not blocks:
+            return np.zeros((0, H, D), np.uint16)
+        a = np.concatenate(blocks, axis=0)
+        return a[first - b0 * 256: n_all - b0 * 256]
+    k = draw(P_CACHE_K)
+    v = None if layer.k_eq_v else draw(P_CACHE_V)
+    return k, v
+
+
+# ----------------------------------------------------------------------------
+# the five measured workloads
+# ----------------------------------------------------------------------------
+
+def workload_tiny_decode() -> DecodeWorkload:
+    """Tiny sliding-window decode: 1 sequence, 8 q / 2 kv heads, head_dim 256,
+    128 cached tokens, window 512, 4-bit, full RoPE theta 1e4."""
+    return DecodeWorkload("tiny-sliding-decode-b1", 1001, SLIDING, filled=[128], bits=[4])
+
+
+def workload_sliding_decode_b16() -> DecodeWorkload:
+    """Sliding decode, 16 sequences at 4096 cached tokens, window 512;
+    sequences 0..7 use a 4-bit cache and 8..15 an 8-bit cache."""
+    return DecodeWorkload("sliding-decode-b16-4k-w512", 1002, SLIDING,
+                          filled=[4096] * 16, bits=[4] * 8 + [8] * 8)
+
+
+def workload_full_keqv_decode() -> DecodeWorkload:
+    """Full-attention K = V decode: 8 sequences at 32768 cached tokens,
+    16 q / 1 kv head, head_dim 512, 128 of 512 dims rotated, theta 1e6, 4-bit."""
+    return DecodeWorkload("full-keqv-decode-b8-32k", 1003, FULL_KEQV,
+                          filled=[32768] * 8, bits=[4] * 8)
+
+
+def workload_prefill_chunk() -> PrefillWorkload:
+    """Prompt chunk: 4 sequences append 512 tokens each onto 8192 cached
+    tokens of an 8-bit cache; 8 q / 2 kv heads, head_dim 256, window 1024."""
+    layer = dataclasses.replace(SLIDING, window=1024)
+    return PrefillWorkload("prefill-chunk-b4x512-8k-w1024", 1004, layer,
+                           filled=[8192] * 4, chunk=[512] * 4, bits=[8] * 4)
+
+
+N_LAYERS = 42
+N_DONORS = 24
+
+
+def stack_layer_kind(i: int) -> str:
+    """5 sliding : 1 full, full at layers 5, 11, 17, ... (gemma4-e4b.ts LAYERS)."""
+    return "full" if i % 6 == 5 else "sliding"
+
+
+def stack_cache_layer(i: int) -> int:
+    """The layer whose cache layer i reads: itself for donors 0..23, else the
+    last donor of the same attention type (22 sliding, 23 full)."""
+    if i < N_DONORS:
+        return i
+    want = stack_layer_kind(i)
+    return max(j for j in range(N_DONORS) if stack_layer_kind(j) == want)
+
+
+@dataclasses.dataclass
+class StackWorkload:
+    """Decode step over the 42-layer stack for ragged sequences."""
+    name: str
+    seed: int
+    lengths: list          # cached tokens per sequence; new token at this position
+    donor_bits: dict       # donor layer -> 4 or 8
+
+    @property
+    def n_seqs(self) -> int:
+        return len(self.lengths)
+
+    def layer(self, i: int) -> LayerSpec:
+        return FULL_KEQV if stack_layer_kind(i) == "full" else SLIDING
+
+    def decode_view(self, i: int) -> DecodeWorkload:
+        """The per-layer decode workload of (donor) layer i."""
+        d = stack_cache_layer(i)
+        return DecodeWorkload(f"{self.name}-layer{d}", self.seed, self.layer(d),
+                              filled=list(self.lengths), bits=[self.donor_bits[d]] * self.n_seqs,
+                              layer_id=d)
+
+
+def workload_stack_decode(n_seqs: int = 64, lo: int = 1024, hi: int = 32768) -> StackWorkload:
+    """Mixed decode step over the 42-layer stack pattern for ragged sequences
+    with lengths uniform in [lo, hi]; per-donor KV bits 4 or 8 from the seed."""
+    seed = 1005
+    g = _rng(seed, P_LEN)
+    lengths = [int(x) for x in g.integers(lo, hi + 1, size=n_seqs)]
+    gb = _rng(seed, P_BITS)
+    bits = {d: int(gb.choice([4, 8])) for d in range(N_DONORS)}
+    return StackWorkload("stack42-mixed-decode-64-ragged", seed, lengths, bits)
+
+
+WORKLOADS = {
+    "tiny": workload_tiny_decode,
+    "sliding16": workload_sliding_decode_b16,
+    "full32k": workload_full_keqv_decode,
+    "prefill": workload_prefill_chunk,
+    "stack42": workload_stack_decode,
+}
