@@ -1,0 +1,198 @@
+/*
+ * kvq -- attention over a group-wise affine-quantized KV cache, for one
+ * NVIDIA GB300 GPU (sm_103a).  C ABI of libkvq.so.
+ *
+ * The operations are those of one attention layer of the Gemma 4 serving
+ * graph shown on the pages of the @mlx-bun/inference package:
+ *   - model.ts, "Parity notes" header: SDPA scale 1.0 (q and k are
+ *     normalized instead); full-attention layers use K = V (one projection,
+ *     v gets an un-scaled RMS norm); proportional RoPE rotates only
+ *     partial_rotary_factor * head_dim dims.
+ *   - model.ts, attentionTraining: q/k/v reshaped per head, qNorm / kNorm /
+ *     vNorm, RoPE at the cache offset, cache.appendWindow(k, v), then
+ *     read.attend(q, 1.0).
+ *   - gemma4-e4b.ts, Gemma4Layer / LAYERS: each cache is affine quantized
+ *     with {bits: 4 | 8, groupSize: 64}; KV-shared layers attend the cache of
+ *     the last donor of their type without appending.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates nothing and keeps no reference after the call
+ *     returns.  `kvq_layer` is read on the host during the call.
+ *   - Alignment: k_raw, v_raw and q_raw 16 bytes (read with 128-bit loads);
+ *     the workspace 256 bytes; the kvq_seq_cache array 8 bytes; every other
+ *     pointer its element size.  The six arrays a kvq_seq_cache points to are
+ *     16-byte aligned (copied with the tensor memory accelerator).
+ *   - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously; no call synchronizes the device.
+ *   - Arguments are checked on the host first; a bad argument returns a
+ *     status other than KVQ_OK and enqueues nothing.  kvq_last_error()
+ *     returns a message for the calling thread's last failure.
+ *   - Per-sequence fields that live in device memory (kvq_seq_cache) are
+ *     checked by the kernels.  A sequence whose cache descriptor is invalid
+ *     (bits not 4/8, capacity not a positive multiple of 64, a misaligned
+ *     pointer, or a capacity too small for the window) is skipped: nothing of
+ *     it is written by kv_quant_append, and its attention outputs are NaN.
+ *
+ * Cache layout (per sequence of one layer)
+ *   k_codes, v_codes  uint32 [n_kv_heads][capacity][head_dim*bits/32]
+ *       element e of a row lives in word e*bits/32 at bit (e*bits) % 32,
+ *       element 0 in the low bits (little-endian packing).
+ *   k_scales, k_biases, v_scales, v_biases  bf16 [n_kv_heads][capacity][head_dim/64]
+ *   Position p is stored in slot p % capacity: a full-attention cache uses a
+ *   capacity above its largest position (linear), a sliding-window cache a
+ *   ring of at least `window` slots (window + rows_per_call - 1 for prompt
+ *   chunks).
+ *
+ * Quantization of one 64-element group of a prepped bf16 row (IEEE fp32):
+ *   scale = bf16_rne((max - min) / (2^bits - 1));  bias = min;
+ *   code  = clamp(rint_half_even((x - bias) / scale), 0, 2^bits - 1),
+ *   all codes 0 when scale == 0.  The pages name the affine {bits, groupSize}
+ *   scheme and its (codes, scales, biases) triple but print no formula; this
+ *   is the plain min/max affine reading.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_EINVAL = 1,        /* bad argument (null/misaligned pointer, size out of range) */
+  KVQ_EUNSUPPORTED = 2,  /* shape this build does not implement (head_dim, group, ratio) */
+  KVQ_ECUDA = 3,         /* a CUDA launch failed; kvq_last_error() has the CUDA message */
+  KVQ_EWORKSPACE = 4     /* workspace smaller than the matching *_workspace_bytes() */
+} kvq_status;
+
+/* One sequence's cache of one layer.  An array of these lives in DEVICE
+ * memory (kernels read the pointers from it). */
+typedef struct {
+  uint32_t* k_codes;
+  uint32_t* v_codes;
+  uint16_t* k_scales;
+  uint16_t* k_biases;
+  uint16_t* v_scales;
+  uint16_t* v_biases;
+  int32_t bits;        /* 4 or 8; may differ between sequences */
+  int32_t capacity;    /* slots, a positive multiple of 64 */
+} kvq_seq_cache;
+
+/* One attention layer (host memory). */
+typedef struct {
+  int32_t n_q_heads;   /* q heads; a multiple of n_kv_heads */
+  int32_t n_kv_heads;  /* kv heads; q head h reads kv head h / (n_q_heads / n_kv_heads) */
+  int32_t head_dim;    /* 64, 128, 256 or 512 */
+  int32_t group_size;  /* must be 64 */
+  int32_t window;      /* 0 = full causal; W > 0: a query at p sees keys p-W+1 .. p */
+  int32_t rope_dims;   /* even, 0..head_dim: dims 0..rope_dims-1 are rotated in pairs
+                          (j, j + rope_dims/2) at angle pos * rope_theta^(-2j/head_dim) */
+  double rope_theta;   /* > 0 */
+  float rms_eps;       /* >= 0; RMSNorm: x / sqrt(mean(x^2) + eps) * w */
+  int32_t k_eq_v;      /* 1: V is the un-scaled RMS norm of the raw k rows (no v input) */
+} kvq_layer;
+
+/*
+ * kv_quant_append -- prep and quantize-append new K/V rows (the cache's
+ * appendWindow in model.ts attentionTraining).
+ *
+ * For each new row t of sequence s at position p = start_pos[s] + (t - row_offsets[s]):
+ *   k_hat = RoPE_p(bf16(RMSNorm(k_raw[t], k_norm_w)))       (rounded to bf16 after each)
+ *   v_hat = bf16(RMSNorm(v_raw[t] or k_raw[t] if k_eq_v, no weight))
+ * then each is quantized per 64-group and written at slot p % capacity of
+ * every kv head.  When a sequence appends more rows than its capacity, only
+ * the newest `capacity` rows are written (older ones would be overwritten).
+ *
+ *   seqs          device kvq_seq_cache[n_seqs]
+ *   row_offsets   device int32[n_seqs + 1], non-decreasing, row_offsets[0] = 0,
+ *                 row_offsets[n_seqs] = n_rows (rows of sequence s are
+ *                 row_offsets[s] .. row_offsets[s+1]-1)
+ *   start_pos     device int32[n_seqs], position of each sequence's first new row,
+ *                 0 <= p < 2^24
+ *   n_rows        host copy of row_offsets[n_seqs]
+ *   k_raw         device bf16 [n_rows][n_kv_heads][head_dim]
+ *   v_raw         device bf16 [n_rows][n_kv_heads][head_dim]; NULL iff k_eq_v
+ *   k_norm_w      device bf16 [head_dim]
+ *   kv_prepped    NULL, or device bf16 [2][n_rows][n_kv_heads][head_dim] that
+ *                 receives k_hat and v_hat (for inspection)
+ */
+kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                           const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                           const uint16_t* k_raw, const uint16_t* v_raw, const uint16_t* k_norm_w,
+                           uint16_t* kv_prepped, void* stream);
+
+/*
+ * attn_decode -- one query token per sequence attends its cache
+ * (read.attend(q, 1.0) of model.ts attentionTraining in the decode phase).
+ * Call it after kv_quant_append has stored the token's own K/V row (the new
+ * row is read back quantized); a KV-shared layer calls it on its donor's
+ * caches without appending.
+ *
+ * For sequence s with query position p = pos[s] and each q head h:
+ *   q_hat = RoPE_p(bf16(RMSNorm(q_raw[s][h], q_norm_w)))
+ *   out[s][h] = sum_j softmax_j(q_hat . k_hat_j) v_hat_j,  scale 1.0,
+ * over keys j = max(0, p-window+1) .. p (0 .. p when window == 0), with
+ * k_hat_j, v_hat_j dequantized (code * scale + bias) from the cache.
+ *
+ *   seqs        device kvq_seq_cache[n_seqs]
+ *   pos         device int32[n_seqs], 0 <= pos < 2^24; the cache must hold
+ *               every visible key (ring capacity >= window, linear capacity > pos)
+ *   max_pos     host upper bound of pos[] (sizes the split over the cache length)
+ *   q_raw       device bf16 [n_seqs][n_q_heads][head_dim]
+ *   q_norm_w    device bf16 [head_dim]
+ *   out         device [n_seqs][n_q_heads][head_dim], fp32 if out_is_f32 else bf16
+ *   q_prepped   NULL, or device bf16 [n_seqs][n_q_heads][head_dim] receiving q_hat
+ *   workspace   device scratch of at least attn_decode_workspace_bytes(...) bytes;
+ *               its first 4 bytes receive a device status word (0 = clean;
+ *               bit 1: a bounded wait gave up; bit 2: a sequence was skipped)
+ */
+kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                       const int32_t* pos, int32_t max_pos,
+                       const uint16_t* q_raw, const uint16_t* q_norm_w,
+                       void* out, int32_t out_is_f32, uint16_t* q_prepped,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos);
+
+/*
+ * attn_prefill_chunk -- a chunk of new query rows per sequence attends the
+ * cache after kv_quant_append stored the chunk's K/V rows (the "window" phase
+ * of the pages: prompt chunks and verify windows).  Row t of sequence s sits
+ * at position p = start_pos[s] + (t - row_offsets[s]) and sees keys
+ * max(0, p-window+1) .. p (0 .. p when window == 0), including the rows of
+ * its own chunk up to itself.  Same arithmetic as attn_decode per row.
+ *
+ *   row_offsets, start_pos, n_rows   as for kv_quant_append
+ *   max_rows_per_seq                 host upper bound of rows per sequence
+ *   q_raw                            device bf16 [n_rows][n_q_heads][head_dim]
+ *   out                              device [n_rows][n_q_heads][head_dim]
+ *   q_prepped                        NULL or device bf16 [n_rows][n_q_heads][head_dim]
+ *   A ring cache needs capacity >= window + rows_of_the_sequence - 1.
+ */
+kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                              int32_t max_rows_per_seq,
+                              const uint16_t* q_raw, const uint16_t* q_norm_w,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
+                                    int32_t max_rows_per_seq);
+
+/* Static message for a status code. */
+const char* kvq_status_string(kvq_status status);
+/* Message of the calling thread's most recent failing call ("" if none). */
+const char* kvq_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

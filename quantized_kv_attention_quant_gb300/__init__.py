@@ -1,0 +1,160 @@
+"""Python binding of libkvq.so: attention over a group-wise affine-quantized
+KV cache on one GB300 GPU (sm_103a).
+
+The functions below carry the C ABI's names (include/kvq.h) and only marshal
+arguments: every step of the computation runs in the library's CUDA kernels.
+Tensor arguments may be torch tensors (their data pointers are passed) or raw
+integer device addresses.  A failing call raises KvqError.  Importing this
+package without a built library raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kvq.h")
+
+KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECUDA, KVQ_EWORKSPACE = range(5)
+
+
+class KvqLayer(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("rope_dims", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_float),
+                ("k_eq_v", ctypes.c_int32)]
+
+
+class KvqSeqCache(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("k_scales", ctypes.c_void_p), ("k_biases", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p), ("v_biases", ctypes.c_void_p),
+                ("bits", ctypes.c_int32), ("capacity", ctypes.c_int32)]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"kvq status {status}: {message}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run "
+                          "`python -m quantized_kv_attention_quant_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lay = ctypes.POINTER(KvqLayer)
+    lib.kv_quant_append.argtypes = [lay, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.kv_quant_append.restype = ctypes.c_int
+    lib.attn_decode.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
+    lib.attn_decode.restype = ctypes.c_int
+    lib.attn_decode_workspace_bytes.argtypes = [lay, i32, i32]
+    lib.attn_decode_workspace_bytes.restype = sz
+    lib.attn_prefill_chunk.argtypes = [lay, vp, i32, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, sz, vp]
+    lib.attn_prefill_chunk.restype = ctypes.c_int
+    lib.attn_prefill_workspace_bytes.argtypes = [lay, i32, i32, i32]
+    lib.attn_prefill_workspace_bytes.restype = sz
+    lib.kvq_status_string.argtypes = [ctypes.c_int]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    lib.kvq_last_error.argtypes = []
+    lib.kvq_last_error.restype = ctypes.c_char_p
+    lib.kvq_version.argtypes = []
+    lib.kvq_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def header_functions() -> list:
+    """Names of the functions include/kvq.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{]*\)\s*;", text)) - {"if", "while"})
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, ctypes.Array):
+        return ctypes.addressof(x)
+    raise TypeError(f"cannot pass {type(x)} as a device pointer")
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != KVQ_OK:
+        raise KvqError(status, lib.kvq_last_error().decode())
+
+
+def layer(n_q_heads, n_kv_heads, head_dim, window, rope_dims, rope_theta, rms_eps=1e-6,
+          k_eq_v=False, group_size=64) -> KvqLayer:
+    return KvqLayer(n_q_heads, n_kv_heads, head_dim, group_size, window, rope_dims,
+                    float(rope_theta), float(rms_eps), int(bool(k_eq_v)))
+
+
+def kv_quant_append(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_rows, k_raw, v_raw,
+                    k_norm_w, kv_prepped=None, stream=None):
+    _check(lib.kv_quant_append(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(row_offsets),
+                               _ptr(start_pos), n_rows, _ptr(k_raw), _ptr(v_raw), _ptr(k_norm_w),
+                               _ptr(kv_prepped), _stream(stream)))
+
+
+def attn_decode(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, out, out_is_f32,
+                q_prepped, workspace, workspace_bytes, stream=None):
+    _check(lib.attn_decode(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(pos), max_pos, _ptr(q_raw),
+                           _ptr(q_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
+                           _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def attn_decode_workspace_bytes(layer: KvqLayer, n_seqs, max_pos) -> int:
+    return lib.attn_decode_workspace_bytes(ctypes.byref(layer), n_seqs, max_pos)
+
+
+def attn_prefill_chunk(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_rows_per_seq,
+                       q_raw, q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes,
+                       stream=None):
+    _check(lib.attn_prefill_chunk(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(row_offsets),
+                                  _ptr(start_pos), n_rows, max_rows_per_seq, _ptr(q_raw),
+                                  _ptr(q_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
+                                  _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def attn_prefill_workspace_bytes(layer: KvqLayer, n_seqs, n_rows, max_rows_per_seq) -> int:
+    return lib.attn_prefill_workspace_bytes(ctypes.byref(layer), n_seqs, n_rows, max_rows_per_seq)
+
+
+def kvq_status_string(status: int) -> str:
+    return lib.kvq_status_string(status).decode()
+
+
+def kvq_last_error() -> str:
+    return lib.kvq_last_error().decode()
+
+
+def kvq_version() -> int:
+    return lib.kvq_version()
+
+
+from .cache import LayerCaches  # noqa: E402,F401  (torch device memory for caches)

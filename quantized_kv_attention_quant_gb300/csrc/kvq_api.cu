@@ -1,0 +1,247 @@
+// C ABI of libkvq.so: argument checks, rotary frequency tables, launches.
+// The operations and their page citations are documented in include/kvq.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+// theta^(-2j/D) (libm pow, float64) split into three floats that sum to it
+// exactly, cached per (theta, D, rope_dims).
+const kvq::RopeFreqs& rope_freqs(double theta, int D, int R) {
+  static std::mutex mu;
+  static std::map<std::tuple<double, int, int>, kvq::RopeFreqs> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(theta, D, R);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  kvq::RopeFreqs f;
+  std::memset(&f, 0, sizeof f);
+  for (int j = 0; j < R / 2; ++j) {
+    const double v = std::pow(theta, -(2.0 * j) / D);
+    const float f1 = (float)v;
+    const double r1 = v - (double)f1;      // exact
+    const float f2 = (float)r1;
+    const double r2 = r1 - (double)f2;     // exact
+    f.f[j][0] = f1;
+    f.f[j][1] = f2;
+    f.f[j][2] = (float)r2;
+  }
+  return cache.emplace(key, f).first->second;
+}
+
+int num_sms_current() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
+  if (!L) return fail(KVQ_EINVAL, "layer is NULL");
+  if (L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->n_q_heads % L->n_kv_heads)
+    return fail(KVQ_EINVAL, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                L->n_q_heads, L->n_kv_heads);
+  const int G = L->n_q_heads / L->n_kv_heads;
+  if (G > kvq::kMaxG)
+    return fail(KVQ_EUNSUPPORTED, "n_q_heads / n_kv_heads = %d exceeds %d", G, kvq::kMaxG);
+  if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 256 && L->head_dim != 512)
+    return fail(KVQ_EUNSUPPORTED, "head_dim %d not in {64, 128, 256, 512}", L->head_dim);
+  if (L->group_size != 64) return fail(KVQ_EUNSUPPORTED, "group_size %d != 64", L->group_size);
+  if (L->window < 0) return fail(KVQ_EINVAL, "window %d < 0", L->window);
+  if (L->rope_dims < 0 || L->rope_dims > L->head_dim || (L->rope_dims & 1))
+    return fail(KVQ_EINVAL, "rope_dims %d must be even and in [0, head_dim]", L->rope_dims);
+  if (!(L->rope_theta > 0.0) || !std::isfinite(L->rope_theta))
+    return fail(KVQ_EINVAL, "rope_theta must be positive and finite");
+  if (!(L->rms_eps >= 0.f) || !std::isfinite(L->rms_eps)) return fail(KVQ_EINVAL, "rms_eps must be >= 0");
+  if (L->k_eq_v != 0 && L->k_eq_v != 1) return fail(KVQ_EINVAL, "k_eq_v must be 0 or 1");
+  out->n_q = L->n_q_heads;
+  out->n_kv = L->n_kv_heads;
+  out->D = L->head_dim;
+  out->G = G;
+  out->window = L->window;
+  out->rope_dims = L->rope_dims;
+  out->k_eq_v = L->k_eq_v;
+  out->eps = L->rms_eps;
+  return KVQ_OK;
+}
+
+// A non-NULL pointer aligned to `al` bytes (16 for tensors read with 128-bit
+// loads, the element size otherwise, 8 for the descriptor array).
+#define REQUIRE_PTR(p, name, al)                                                         \
+  do {                                                                                   \
+    if (!(p)) return fail(KVQ_EINVAL, "%s is NULL", name);                               \
+    if (!aligned(p, al)) return fail(KVQ_EINVAL, "%s is not %d-byte aligned", name, al); \
+  } while (0)
+
+kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                            const int32_t* row_offsets, const int32_t* pos, int32_t n_rows, int32_t max_keys,
+                            const uint16_t* q_raw, const uint16_t* q_norm_w, void* out, int32_t out_is_f32,
+                            uint16_t* q_prepped, void* workspace, size_t workspace_bytes, void* stream) {
+  kvq::LayerArgs L;
+  kvq_status st = check_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if (n_seqs < 0 || n_rows < 0) return fail(KVQ_EINVAL, "negative n_seqs or n_rows");
+  if (n_rows == 0) return KVQ_OK;
+  if (n_seqs == 0) return fail(KVQ_EINVAL, "n_rows > 0 with n_seqs == 0");
+  if (max_keys < 1 || max_keys > (1 << 24)) return fail(KVQ_EINVAL, "max position out of range");
+  REQUIRE_PTR(seqs, "seqs", 8);
+  REQUIRE_PTR(pos, "pos/start_pos", 4);
+  REQUIRE_PTR(q_raw, "q_raw", 16);
+  REQUIRE_PTR(q_norm_w, "q_norm_w", 2);
+  REQUIRE_PTR(out, "out", out_is_f32 ? 4 : 2);
+  REQUIRE_PTR(workspace, "workspace", 256);
+  if (row_offsets) REQUIRE_PTR(row_offsets, "row_offsets", 4);
+  if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
+  if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
+  const int splits = kvq::decode_pick_splits(L, n_rows, max_keys, num_sms_current());
+  const size_t need = kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
+  if (workspace_bytes < need)
+    return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  kvq::DecodeArgs a;
+  a.L = L;
+  a.seqs = seqs;
+  a.n_seqs = n_seqs;
+  a.n_rows = n_rows;
+  a.row_offsets = row_offsets;
+  a.pos = pos;
+  a.q_raw = q_raw;
+  a.q_w = q_norm_w;
+  a.out = out;
+  a.out_f32 = out_is_f32;
+  a.q_prepped = q_prepped;
+  a.splits = splits;
+  a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, splits);
+  const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
+  cudaError_t e = kvq::launch_decode(a, f, num_sms_current(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                           const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                           const uint16_t* k_raw, const uint16_t* v_raw, const uint16_t* k_norm_w,
+                           uint16_t* kv_prepped, void* stream) {
+  kvq::LayerArgs L;
+  kvq_status st = check_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if (n_seqs < 0 || n_rows < 0) return fail(KVQ_EINVAL, "negative n_seqs or n_rows");
+  if (n_rows == 0) return KVQ_OK;
+  if (n_seqs == 0) return fail(KVQ_EINVAL, "n_rows > 0 with n_seqs == 0");
+  REQUIRE_PTR(seqs, "seqs", 8);
+  REQUIRE_PTR(row_offsets, "row_offsets", 4);
+  REQUIRE_PTR(start_pos, "start_pos", 4);
+  REQUIRE_PTR(k_raw, "k_raw", 16);
+  REQUIRE_PTR(k_norm_w, "k_norm_w", 2);
+  if (L.k_eq_v) {
+    if (v_raw) return fail(KVQ_EINVAL, "v_raw must be NULL when k_eq_v = 1");
+  } else {
+    REQUIRE_PTR(v_raw, "v_raw", 16);
+  }
+  if (kv_prepped && !aligned(kv_prepped, 2)) return fail(KVQ_EINVAL, "kv_prepped is not 2-byte aligned");
+  kvq::AppendArgs a;
+  a.L = L;
+  a.seqs = seqs;
+  a.n_seqs = n_seqs;
+  a.row_offsets = row_offsets;
+  a.start_pos = start_pos;
+  a.n_rows = n_rows;
+  a.k_raw = k_raw;
+  a.v_raw = v_raw;
+  a.k_w = k_norm_w;
+  a.prepped = kv_prepped;
+  const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
+  cudaError_t e = kvq::launch_append(a, f, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_quant_append launch");
+  return KVQ_OK;
+}
+
+kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                       const int32_t* pos, int32_t max_pos, const uint16_t* q_raw, const uint16_t* q_norm_w,
+                       void* out, int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, q_raw, q_norm_w, out,
+                          out_is_f32, q_prepped, workspace, workspace_bytes, stream);
+}
+
+size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos) {
+  kvq::LayerArgs L;
+  if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || max_pos < 0) return 0;
+  const int splits = kvq::decode_pick_splits(L, n_seqs, max_pos + 1, num_sms_current());
+  return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, splits);
+}
+
+kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                              int32_t max_rows_per_seq, const uint16_t* q_raw, const uint16_t* q_norm_w,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (n_rows > 0 && !row_offsets) return fail(KVQ_EINVAL, "row_offsets is NULL");
+  if (max_rows_per_seq < 1 && n_rows > 0) return fail(KVQ_EINVAL, "max_rows_per_seq < 1");
+  // each row reads at most window keys (full layers: the caller's positions)
+  const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
+  return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, q_raw, q_norm_w,
+                          out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
+}
+
+size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
+                                    int32_t max_rows_per_seq) {
+  kvq::LayerArgs L;
+  if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || n_rows < 0 || max_rows_per_seq < 0) return 0;
+  const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
+  const int splits = kvq::decode_pick_splits(L, n_rows, max_keys, num_sms_current());
+  return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
+}
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_EINVAL: return "invalid argument";
+    case KVQ_EUNSUPPORTED: return "unsupported shape";
+    case KVQ_ECUDA: return "CUDA error";
+    case KVQ_EWORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* kvq_last_error(void) { return g_last_error.c_str(); }
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

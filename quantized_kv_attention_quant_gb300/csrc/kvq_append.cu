@@ -1,0 +1,217 @@
+// kv_quant_append: prep (norm, RoPE) and group-quantize new K/V rows into the
+// affine cache (model.ts attentionTraining: kNorm, vNorm, RoPE at the cache
+// offset, then cache.appendWindow(k, v); gemma4-e4b.ts Gemma4Layer.kv:
+// {bits, groupSize 64}).
+//
+// One warp handles one (row, kv head, K-or-V) item: 32 lanes x D/32
+// contiguous elements, loaded with 16-byte vector loads; a 64-element group
+// spans 64/(D/32) lanes and is reduced with shuffles.  Output words are
+// written coalesced at slot pos % capacity.
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 4;
+
+template <int D>
+struct AppendSmem {
+  float normed[kWarpsPerBlock][D];
+  float4 cs[kWarpsPerBlock][D / 2];     // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
+};
+
+__device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row) {
+  int lo = 0, hi = n_seqs - 1;          // largest s with off[s] <= row
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Quantize this lane's E prepped values (one slice of a 64-group), pack the
+// codes little-endian and store them, the group's scale and its bias.
+template <int D, int BITS>
+__device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], const kvq_seq_cache& c,
+                                               int kind, int head, int pos, int lane) {
+  constexpr int E = D / 32;
+  constexpr int LPG = 64 / E;
+  constexpr int NG = D / 64;
+  constexpr int TOP = (1 << BITS) - 1;
+  float v[E];
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < E; ++i) { v[i] = bf16_to_f(y[i]); mn = fminf(mn, v[i]); mx = fmaxf(mx, v[i]); }
+#pragma unroll
+  for (int m = 1; m < LPG; m <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+  }
+  // scale = bf16((max - min) / (2^bits - 1)), two IEEE fp32 roundings
+  const uint16_t sb = f_to_bf16_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)TOP));
+  const float sf = bf16_to_f(sb);
+  uint32_t code[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    int q = 0;
+    if (sf != 0.f) {
+      q = __float2int_rn(__fdiv_rn(__fsub_rn(v[i], mn), sf));   // half to even
+      q = min(max(q, 0), TOP);
+    }
+    code[i] = uint32_t(q);
+  }
+  const int slot = pos % c.capacity;
+  const size_t rowi = (size_t)head * c.capacity + slot;
+  uint32_t* codes = kind == 0 ? c.k_codes : c.v_codes;
+  constexpr int WPR = D * BITS / 32;       // words per row
+  constexpr int LB = E * BITS;             // bits per lane
+  if constexpr (LB >= 32) {
+    constexpr int NW = LB / 32, PER = 32 / BITS;
+    uint32_t* dst = codes + rowi * WPR + lane * NW;
+#pragma unroll
+    for (int wi = 0; wi < NW; ++wi) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) w |= code[wi * PER + i] << (i * BITS);
+      dst[wi] = w;
+    }
+  } else {
+    constexpr int LPW = 32 / LB;           // lanes sharing one word
+    uint32_t part = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) part |= code[i] << (i * BITS);
+    part <<= (lane % LPW) * LB;
+#pragma unroll
+    for (int m = 1; m < LPW; m <<= 1) part |= __shfl_xor_sync(0xffffffffu, part, m);
+    if (lane % LPW == 0) codes[rowi * WPR + lane / LPW] = part;
+  }
+  if (lane % LPG == 0) {
+    const int g = lane / LPG;
+    uint16_t* sc = kind == 0 ? c.k_scales : c.v_scales;
+    uint16_t* bi = kind == 0 ? c.k_biases : c.v_biases;
+    sc[rowi * NG + g] = sb;
+    bi[rowi * NG + g] = f_to_bf16_rn(mn);            // mn is a bf16 value: exact
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+append_kernel(const AppendArgs a, const RopeFreqs freqs) {
+  constexpr int E = D / 32;              // elements per lane
+  constexpr int LPG = 64 / E;            // lanes per quantization group
+  __shared__ AppendSmem<D> sm;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = a.L.n_kv;
+  const long item = (long)blockIdx.x * kWarpsPerBlock + warp;
+  const int kind = int(item & 1);        // 0: K, 1: V
+  const long rh = item >> 1;
+  if (rh >= (long)a.n_rows * Hkv) return;
+  const int row = int(rh / Hkv), head = int(rh % Hkv);
+
+  const int s = find_seq(a.row_offsets, a.n_seqs, row);
+  const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
+  const int t_in = row - off0, rows_s = off1 - off0;
+  const int pos = __ldg(a.start_pos + s) + t_in;
+  const kvq_seq_cache c = a.seqs[s];
+  const bool ok = (c.bits == 4 || c.bits == 8) && c.capacity > 0 && (c.capacity % kTileKeys) == 0 &&
+                  c.k_codes && c.v_codes && c.k_scales && c.k_biases && c.v_scales && c.v_biases &&
+                  aligned16(c.k_codes) && aligned16(c.v_codes) && aligned16(c.k_scales) &&
+                  aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases) &&
+                  pos >= 0 && pos < (1 << 24);
+  if (!ok) return;
+  if (t_in < rows_s - c.capacity) return;   // overwritten by a newer row of this call
+
+  // ---- load the raw row ----
+  const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
+  src += ((size_t)row * Hkv + head) * D + lane * E;
+  float x[E];
+  if constexpr (E >= 8) {
+#pragma unroll
+    for (int v = 0; v < E / 8; ++v) {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { x[8 * v + 2 * i] = bf16lo_to_f(w[i]); x[8 * v + 2 * i + 1] = bf16hi_to_f(w[i]); }
+    }
+  } else if constexpr (E == 4) {
+    uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+    x[0] = bf16lo_to_f(u.x); x[1] = bf16hi_to_f(u.x); x[2] = bf16lo_to_f(u.y); x[3] = bf16hi_to_f(u.y);
+  } else {
+    uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+    x[0] = bf16lo_to_f(u); x[1] = bf16hi_to_f(u);
+  }
+
+  // ---- RMSNorm (weight on K only) ----
+  ff ss = {0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
+  ss = ff_warp_sum(ss);
+  const ff inv = rms_inv(ss, D, a.L.eps);
+  uint16_t y[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + lane * E + i)) : 1.f;
+    y[i] = norm_scale_bf16(x[i], w, inv);
+  }
+
+  // ---- RoPE on K ----
+  const int R = a.L.rope_dims;
+  if (kind == 0 && R > 0) {
+    const int half = R >> 1;
+#pragma unroll
+    for (int i = 0; i < E; ++i) sm.normed[warp][lane * E + i] = bf16_to_f(y[i]);
+    for (int j = lane; j < half; j += 32) {
+      ff cc, sn;
+      rope_cos_sin(pos, freqs.f[j][0], freqs.f[j][1], freqs.f[j][2], cc, sn);
+      sm.cs[warp][j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int e = lane * E + i;
+      if (e < R) {
+        const int j = e < half ? e : e - half;
+        const float4 t = sm.cs[warp][j];
+        const ff cc = {t.x, t.y};
+        if (e < half) {      // x_j cos - x_{j+h} sin
+          y[i] = rot_bf16(sm.normed[warp][e], sm.normed[warp][e + half], cc, ff{t.z, t.w});
+        } else {             // x_{j+h} cos + x_j sin
+          y[i] = rot_bf16(sm.normed[warp][e], sm.normed[warp][j], cc, ff{-t.z, -t.w});
+        }
+      }
+    }
+  }
+
+  if (a.prepped) {
+    uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) dst[i] = y[i];
+  }
+
+  // ---- quantize the 64-element group, pack, store ----
+  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, lane);
+  else quantize_store<D, 8>(y, c, kind, head, pos, lane);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st) {
+  const long items = (long)a.n_rows * a.L.n_kv * 2;
+  if (items == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((items + kWarpsPerBlock - 1) / kWarpsPerBlock));
+  const dim3 block(kWarpsPerBlock * 32);
+  switch (a.L.D) {
+    case 64: append_kernel<64><<<grid, block, 0, st>>>(a, f); break;
+    case 128: append_kernel<128><<<grid, block, 0, st>>>(a, f); break;
+    case 256: append_kernel<256><<<grid, block, 0, st>>>(a, f); break;
+    case 512: append_kernel<512><<<grid, block, 0, st>>>(a, f); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

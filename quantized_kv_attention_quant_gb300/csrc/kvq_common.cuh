@@ -1,0 +1,336 @@
+// Device helpers shared by the kvq kernels (sm_103a).
+//
+// Precision contract of the "prep" steps (q/k RMSNorm, un-scaled v norm,
+// RoPE): each prepped element is the bf16 value nearest to the exact real
+// result (ties to even).  The arithmetic runs in float-float pairs of fp32
+// (~2^-44 relative), which GB300 executes at full fp32 rate, instead of in
+// fp64 (a small fraction of that rate on this part).
+//
+// Model code this implements (pages of the @mlx-bun/inference package):
+//   model.ts, "Parity notes" header: SDPA scale 1.0 because q and k are
+//     normalized; K = V full layers with un-scaled v norm; proportional RoPE
+//     rotating only partial_rotary_factor * dims dims.
+//   model.ts, attentionTraining: qNorm/kNorm/vNorm per head, RoPE at the
+//     cache offset, appendWindow(k, v), then read.attend(q, 1.0).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "rope_consts.h"
+
+namespace kvq {
+
+// ----------------------------------------------------------------------------
+// bf16 bit helpers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+__device__ __forceinline__ float bf16lo_to_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// IEEE round-to-nearest-even fp32 -> bf16 (finite inputs).
+__device__ __forceinline__ uint16_t f_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ----------------------------------------------------------------------------
+// float-float arithmetic.  The _rn intrinsics keep the compiler from fusing
+// or reordering the error-free transformations.
+// ----------------------------------------------------------------------------
+struct ff { float hi, lo; };
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float bp = __fsub_rn(s, a);
+  float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+  return {s, e};
+}
+// requires |a| >= |b| (or a == 0)
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float e = __fsub_rn(b, __fsub_rn(s, a));
+  return {s, e};
+}
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  float p = __fmul_rn(a, b);
+  float e = __fmaf_rn(a, b, -p);
+  return {p, e};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return fast_two_sum(s.hi, e);
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+  ff p = two_prod(a.hi, b);
+  float e = __fmaf_rn(a.lo, b, p.lo);
+  return fast_two_sum(p.hi, e);
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  ff p = two_prod(a.hi, b.hi);
+  float e = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo));
+  return fast_two_sum(p.hi, e);
+}
+
+// Correctly rounded bf16 of the real number hi + lo, where (hi, lo) is
+// normalised (|lo| <= ulp(hi)/2, as fast_two_sum leaves it).  hi is the fp32
+// nearest to hi + lo, so hi + lo lies on the same side of every bf16 rounding
+// boundary as hi, except when hi sits exactly on a boundary; then lo decides.
+__device__ __forceinline__ uint16_t ff_to_bf16_rn(ff v) {
+  uint32_t u = __float_as_uint(v.hi);
+  uint32_t low = u & 0xFFFFu;
+  uint32_t top = u >> 16;
+  if (low > 0x8000u) return uint16_t(top + 1);
+  if (low < 0x8000u) return uint16_t(top);
+  if (v.lo == 0.f) return uint16_t(top + (top & 1u));
+  bool away = (v.lo > 0.f) == (v.hi > 0.f);   // true magnitude above the tie
+  return uint16_t(away ? top + 1 : top);
+}
+
+// ----------------------------------------------------------------------------
+// RMSNorm pieces (reading: y = x / sqrt(mean(x^2) + eps) * w, rounded once)
+// ----------------------------------------------------------------------------
+// Accumulate x^2 (exact in fp32 for bf16 x) into a float-float sum.
+__device__ __forceinline__ void ff_acc_sq(ff& acc, float x) {
+  float sq = __fmul_rn(x, x);
+  ff s = two_sum(acc.hi, sq);
+  acc = fast_two_sum(s.hi, __fadd_rn(s.lo, acc.lo));
+}
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int m) {
+  return {__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
+}
+// Full-warp float-float sum.
+__device__ __forceinline__ ff ff_warp_sum(ff v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = ff_add(v, ff_shfl_xor(v, m));
+  return v;
+}
+// 1 / sqrt(ss / D + eps) as a float-float, from the float-float sum of
+// squares.  One fp64 square root and division per row (IEEE, correctly
+// rounded), then split into a float pair.
+__device__ __forceinline__ ff rms_inv(ff ss, int D, float eps) {
+  double r = ((double)ss.hi + (double)ss.lo) / (double)D + (double)eps;
+  double inv = 1.0 / sqrt(r);
+  float hi = (float)inv;
+  float lo = (float)(inv - (double)hi);
+  return {hi, lo};
+}
+// x * w * inv, correctly rounded to bf16; x and w are bf16 values so x*w is
+// exact in fp32.
+__device__ __forceinline__ uint16_t norm_scale_bf16(float x, float w, ff inv) {
+  float xw = __fmul_rn(x, w);
+  return ff_to_bf16_rn(ff_mul_f(inv, xw));
+}
+
+// ----------------------------------------------------------------------------
+// Rotary angles.  For position p (integer < 2^24) and frequency f given as an
+// exact sum f1 + f2 + f3 of floats (the float64 theta^(-2j/D) split three
+// ways), returns cos and sin of p*f as float-float pairs accurate to ~2^-45
+// absolute, without fp64 arithmetic:
+//   1. p*f1, p*f2 exactly by two_prod (p*f3 is below 2^-33 and rounded once);
+//   2. k = rint(p*f * 2/pi); r = p*f - k*pi/2 with pi/2 as a three-float
+//      Cody-Waite split, every product exact by two_prod; the leading
+//      difference is exact (Sterbenz), the small terms are summed float-float;
+//   3. k2 = rint(r * 128/pi); r -= k2*pi/128 the same way, |r| <= ~pi/256;
+//   4. cos/sin of r by Taylor series (r^2/2 and r carried float-float);
+//   5. rotate by the table entry (cos, sin)((64k + k2) * pi/128).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void ff_accum(ff& acc, float t) {
+  ff s = two_sum(acc.hi, t);
+  acc = fast_two_sum(s.hi, __fadd_rn(s.lo, acc.lo));
+}
+
+__device__ __forceinline__ void rope_cos_sin(int p, float f1, float f2, float f3, ff& c, ff& s) {
+  const float P = (float)p;
+  ff a1 = two_prod(P, f1);
+  ff a2 = two_prod(P, f2);
+  float a3 = __fmul_rn(P, f3);
+  // first reduction by pi/2
+  float k = rintf(__fmul_rn(a1.hi, KVQ_TWO_OVER_PI));
+  ff b1 = two_prod(k, KVQ_PIO2_1);
+  ff b2 = two_prod(k, KVQ_PIO2_2);
+  float b3 = __fmul_rn(k, KVQ_PIO2_3);
+  ff r = {__fsub_rn(a1.hi, b1.hi), 0.f};      // exact
+  r = fast_two_sum(r.hi, 0.f);
+  ff_accum(r, a1.lo);
+  ff_accum(r, -b1.lo);
+  ff_accum(r, a2.hi);
+  ff_accum(r, -b2.hi);
+  ff_accum(r, a2.lo);
+  ff_accum(r, -b2.lo);
+  ff_accum(r, __fsub_rn(a3, b3));
+  // second reduction by pi/128
+  float k2 = rintf(__fmul_rn(r.hi, KVQ_128_OVER_PI));
+  ff c1 = two_prod(k2, KVQ_PIO128_1);
+  ff c2 = two_prod(k2, KVQ_PIO128_2);
+  float c3 = __fmul_rn(k2, KVQ_PIO128_3);
+  ff t = two_sum(r.hi, -c1.hi);
+  ff rr = fast_two_sum(t.hi, t.lo);
+  ff_accum(rr, r.lo);
+  ff_accum(rr, -c1.lo);
+  ff_accum(rr, -c2.hi);
+  ff_accum(rr, -c2.lo);
+  ff_accum(rr, -c3);
+  // table index: the angle removed is (64 k + k2) * pi/128
+  int ki = (int)k;
+  int idx = ((ki & 3) * 64 + (int)k2) & 255;
+  // Taylor series of sin / cos at |rr| <= ~0.0123
+  float x = rr.hi;
+  ff x2 = two_prod(x, x);
+  x2.lo = __fmaf_rn(2.f * x, rr.lo, x2.lo);
+  x2 = fast_two_sum(x2.hi, x2.lo);
+  float z = x2.hi;
+  // sin r = r - r^3/6 + r^5/120 - r^7/5040
+  float ps = __fmul_rn(z, __fmaf_rn(z, __fmaf_rn(z, -1.f / 5040.f, 1.f / 120.f), -1.f / 6.f));
+  ff sr = fast_two_sum(x, __fmaf_rn(x, ps, rr.lo));
+  // cos r = 1 - r^2/2 + r^4/24 - r^6/720
+  float pc = __fmul_rn(__fmul_rn(z, z), __fmaf_rn(z, -1.f / 720.f, 1.f / 24.f));
+  ff half = {__fmul_rn(x2.hi, 0.5f), __fmul_rn(x2.lo, 0.5f)};
+  ff cr = two_sum(1.f, -half.hi);
+  cr = fast_two_sum(cr.hi, __fadd_rn(cr.lo, __fsub_rn(pc, half.lo)));
+  // rotate by the table angle
+  float4 tb = __ldg(&kvq_rope_table[idx]);
+  ff tc = {tb.x, tb.y}, ts = {tb.z, tb.w};
+  c = ff_add(ff_mul(tc, cr), ff_neg(ff_mul(ts, sr)));
+  s = ff_add(ff_mul(ts, cr), ff_mul(tc, sr));
+}
+
+// x*c - y*s, correctly rounded to bf16 (x, y bf16 values; c, s float-float).
+__device__ __forceinline__ uint16_t rot_bf16(float x, float y, ff c, ff s) {
+  ff a = ff_mul_f(c, x);
+  ff b = ff_mul_f(s, y);
+  return ff_to_bf16_rn(ff_add(a, ff_neg(b)));
+}
+
+// ----------------------------------------------------------------------------
+// Bounded waits.  Every wait in these kernels gives up after kWaitLimitNs of
+// wall-clock time (read from %globaltimer), records the fact in a status word
+// and lets the kernel run to its end, so a lost arrival can never hang the GPU.
+// ----------------------------------------------------------------------------
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+enum : uint32_t { KVQ_DEV_OK = 0, KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BADSEQ = 2 };
+
+__device__ __forceinline__ void flag_error(uint32_t* status, uint32_t code) {
+  if (status) atomicOr(status, 1u << code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Returns false if the phase did not complete within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// Programmatic dependent launch controls (no-ops without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// Warp-level tensor-core MMA, m16n8k16, f16 inputs, fp32 accumulate.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+               "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+               "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+               : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+// ----------------------------------------------------------------------------
+// Code -> f16 conversion (exact: integers <= 255 are f16 values).
+// 0x6400 is f16 1024; OR-ing a value v < 1024 into its mantissa gives 1024+v.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t orv) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(orv));  // (x & mask) | orv
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+constexpr uint32_t kMagic = 0x64006400u;        // (1024, 1024)
+constexpr uint32_t kSixteenth = 0x2C002C00u;    // (1/16, 1/16)
+constexpr uint32_t kNeg64 = 0xD400D400u;        // (-64, -64)
+
+// low nibbles of each 16-bit half -> (c, c)
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x) { return h2_sub(lop3_and_or(x, 0x000F000Fu, kMagic), kMagic); }
+// bits 4..7 of each 16-bit half -> (c, c)
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x) { return h2_fma(lop3_and_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64); }
+// low bytes of each 16-bit half -> (c, c)
+__device__ __forceinline__ uint32_t byte_lo(uint32_t x) { return h2_sub(lop3_and_or(x, 0x00FF00FFu, kMagic), kMagic); }
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace kvq

@@ -1,0 +1,630 @@
+// attn_decode: one query token per sequence attends its quantized cache
+// (model.ts attentionTraining, decode phase: qNorm, RoPE at the cache offset,
+// read.attend(q, 1.0); "Parity notes": SDPA scale 1.0, GQA over n_kv heads).
+//
+// Three launches on the caller's stream:
+//   1. qprep_kernel   (n_kv, n_seqs): q RMSNorm + RoPE for the G q heads of a kv
+//      head, written as ready-made mma.sync A fragments plus per-group sums.
+//   2. decode_kernel  (splits, n_kv, n_seqs), programmatic dependent launch:
+//      split-K ("flash decoding") over the visible keys.  Warp NW is a TMA
+//      producer streaming 64-key tiles (packed codes row by row into padded
+//      shared rows, scales and biases) through an mbarrier ring; warps
+//      0..NW-1 compute
+//        QK: warp w takes 64/NW keys, all G heads (M = 16 rows), full head_dim;
+//            codes enter the tensor cores exactly as f16 integers, per 64-dim
+//            group: S += scale * (q . codes) + bias * sum(q)
+//        softmax: online, tile max exchanged through shared memory
+//        PV: warp w owns head_dim group w; v_hat = code*scale + bias in f16,
+//            P (f16) from shared memory via ldmatrix.
+//      Each split writes its (m, l, o) partial.
+//   3. combine_kernel (n_q, n_seqs): merges the split partials.
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+#include <algorithm>
+
+namespace kvq {
+
+namespace {
+
+template <int D>
+struct Dec {
+  static constexpr int NG = D / 64;          // 64-dim groups = consumer warps
+  static constexpr int NW = NG;
+  static constexpr int KPW = 64 / NW;        // keys per consumer warp in QK
+  static constexpr int NTQ = KPW / 8;        // QK n-tiles per warp
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D == 256 ? 2 : 4);
+  // registers per thread that still fit MIN_BLOCKS CTAs in the 64K register file
+  static constexpr int MAX_REGS_RAW = 65536 / (THREADS * MIN_BLOCKS) / 8 * 8;
+  static constexpr int MAX_REGS = MAX_REGS_RAW > 248 ? 248 : MAX_REGS_RAW;
+};
+
+constexpr int kMaxStages = 8;
+
+__host__ __device__ constexpr int row_bytes(int D, int bits) { return D * bits / 8; }
+__host__ __device__ constexpr int row_stride(int D, int bits) { return D * bits / 8 + 16; }
+__host__ __device__ constexpr int sb_bytes(int D) { return 64 * (D / 64) * 2; }
+__host__ __device__ constexpr int stage_bytes(int D, int bits) { return 2 * 64 * row_stride(D, bits) + 4 * sb_bytes(D); }
+__host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
+// control block: 16 mbarriers, max-exchange [2][NW][16], l-exchange [NW][16], qsum [16][NG]
+__host__ __device__ constexpr int ctrl_bytes(int D) { return align128(128 + (3 * (D / 64) * 16 + 16 * (D / 64)) * 4); }
+__host__ __device__ constexpr int stage0_off(int D) { return ctrl_bytes(D) + 2 * 16 * 64 * 2; }
+
+__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__device__ __forceinline__ bool seq_ok(const kvq_seq_cache& c) {
+  return (c.bits == 4 || c.bits == 8) && c.capacity > 0 && (c.capacity % kTileKeys) == 0 &&
+         aligned16(c.k_codes) && aligned16(c.v_codes) && aligned16(c.k_scales) &&
+         aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases) &&
+         c.k_codes && c.v_codes && c.k_scales && c.k_biases && c.v_scales && c.v_biases;
+}
+
+// Dims (relative to the thread's 16-dim slice 16*t4 of a group) that feed A
+// fragment registers a0, a1, a4, a5 of k-step ks.  They mirror how the code
+// words are split into f16 pairs for the B fragment (nibbles (i, i+4) of a
+// 4-bit word, bytes (i, i+2) of an 8-bit word).
+__device__ __forceinline__ void qk_dims(int bits, int ks, int (&d)[4]) {
+  if (bits == 4) {
+    const int base = (ks < 2 ? 0 : 8) + (ks & 1) * 2;
+    d[0] = base; d[1] = base + 4; d[2] = base + 1; d[3] = base + 5;
+  } else {
+    const int base = 4 * ks;
+    d[0] = base; d[1] = base + 2; d[2] = base + 1; d[3] = base + 3;
+  }
+}
+
+struct RowInfo { int s, p, newest; };
+
+__device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
+  if (a.row_offsets == nullptr) {
+    const int p = a.pos[row];
+    return {row, p, p};
+  }
+  int lo = 0, hi = a.n_seqs - 1;           // largest s with row_offsets[s] <= row
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.row_offsets + mid) <= row) lo = mid; else hi = mid - 1;
+  }
+  const int o0 = __ldg(a.row_offsets + lo), o1 = __ldg(a.row_offsets + lo + 1);
+  const int p0 = __ldg(a.pos + lo);
+  return {lo, p0 + (row - o0), p0 + (o1 - o0) - 1};
+}
+
+__device__ __forceinline__ uint32_t bf16_pair_to_h2(uint16_t lo, uint16_t hi) {
+  return pack_h2(bf16_to_f(lo), bf16_to_f(hi));
+}
+
+// ----------------------------------------------------------------------------
+// 1. q prep
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(512)
+qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
+  constexpr int E = D / 32, NG = D / 64, LPG = 64 / E;
+  __shared__ uint16_t q16[kMaxG][D];
+  __shared__ uint16_t qn[kMaxG][D];
+  __shared__ float4 cs[D / 2];
+  pdl_launch();
+  const int row = blockIdx.x, kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
+  const RowInfo ri = row_info(a, row);
+  const int p = ri.p;
+  const int bits = a.seqs[ri.s].bits;
+  const int pc = min(max(p, 0), (1 << 24) - 1);
+  for (int j = threadIdx.x; j < half; j += blockDim.x) {
+    ff cc, sn;
+    rope_cos_sin(pc, freqs.f[j][0], freqs.f[j][1], freqs.f[j][2], cc, sn);
+    cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+  }
+  // blockDim is 32 * G: warp w preps q head kvh * G + w
+  const int hq = kvh * G + warp;
+  float* qsum = a.ws.qsum + ((size_t)row * a.L.n_kv + kvh) * 16 * NG;
+  const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + lane * E;
+  float x[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) x[i] = bf16_to_f(src[i]);
+  ff ss = {0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
+  ss = ff_warp_sum(ss);
+  const ff inv = rms_inv(ss, D, a.L.eps);
+  uint16_t y[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[lane * E + i]), inv);
+    qn[warp][lane * E + i] = y[i];
+  }
+  __syncthreads();                       // cs[] and qn[] complete
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int e = lane * E + i;
+    if (e < R) {
+      const int j = e < half ? e : e - half;
+      const float4 t = cs[j];
+      const ff cc = {t.x, t.y};
+      y[i] = e < half ? rot_bf16(bf16_to_f(qn[warp][e]), bf16_to_f(qn[warp][e + half]), cc, ff{t.z, t.w})
+                      : rot_bf16(bf16_to_f(qn[warp][e]), bf16_to_f(qn[warp][j]), cc, ff{-t.z, -t.w});
+    }
+  }
+  float gs = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) { q16[warp][lane * E + i] = y[i]; gs += bf16_to_f(y[i]); }
+#pragma unroll
+  for (int m = 1; m < LPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
+  if (lane % LPG == 0) qsum[warp * NG + lane / LPG] = gs;
+  if (a.q_prepped) {
+    uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) dst[i] = y[i];
+  }
+  // zero rows G..15
+  for (int i = threadIdx.x; i < (kMaxG - G) * D; i += blockDim.x) q16[G + i / D][i % D] = 0;
+  for (int i = threadIdx.x; i < (kMaxG - G) * NG; i += blockDim.x) qsum[G * NG + i] = 0.f;
+  __syncthreads();
+  // A fragments: [NG][4 ks][32 lanes] x 4 registers
+  uint32_t* frag = reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
+  for (int idx = threadIdx.x; idx < NG * 4 * 32 * 4; idx += blockDim.x) {
+    const int reg = idx & 3, ln = (idx >> 2) & 31, ks = (idx >> 7) & 3, g = idx >> 9;
+    const int t4 = ln & 3, r = (ln >> 2) + ((reg & 1) ? 8 : 0);
+    int d[4];
+    qk_dims(bits, ks, d);
+    const int base = g * 64 + 16 * t4;
+    const int d0 = base + ((reg & 2) ? d[2] : d[0]);
+    const int d1 = base + ((reg & 2) ? d[3] : d[1]);
+    frag[idx] = bf16_pair_to_h2(q16[r][d0], q16[r][d1]);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// 2. split-K attention over the quantized cache
+// ----------------------------------------------------------------------------
+struct TileRange {
+  int t_begin, n_my, lo, hi;
+};
+
+template <int D, int BITS>
+__device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
+                                            const int nst, const TileRange tr, const int row, const int kvh,
+                                            const int split) {
+  using C = Dec<D>;
+  constexpr int NG = C::NG, NW = C::NW, KPW = C::KPW, NTQ = C::NTQ;
+  constexpr int RB = row_bytes(D, BITS), RS = row_stride(D, BITS), SB = sb_bytes(D);
+  constexpr int STB = stage_bytes(D, BITS);
+  constexpr float L2E = 1.4426950408889634f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  float* red = reinterpret_cast<float*>(smem + 128);        // [2][NW][16]
+  float* lred = red + 2 * NW * 16;                          // [NW][16]
+  float* qs_sm = lred + NW * 16;                            // [16][NG]
+  uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
+  uint8_t* stages = smem + stage0_off(D);
+  const int cap = c.capacity;
+
+  if (warp == NW) {
+    // ------------------------------ producer ------------------------------
+    const uint32_t tile_tx = 2 * 64 * RB + 4 * SB;
+    const size_t head_row0 = (size_t)kvh * cap;
+    int issued = 0;
+    for (int it = 0; it < tr.n_my; ++it) {
+      const int st = it % nst;
+      if (it >= nst && !mbar_wait(&empty[st], ((it / nst) & 1) ^ 1)) {
+        flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
+        break;
+      }
+      const int slot0 = ((tr.t_begin + it) * kTileKeys) % cap;
+      uint8_t* sb = stages + st * STB;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], tile_tx);
+      __syncwarp();
+      const size_t r0 = head_row0 + slot0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        bulk_g2s(sb + r * RS, reinterpret_cast<const uint8_t*>(c.k_codes) + (r0 + r) * RB, RB, &full[st]);
+        bulk_g2s(sb + (64 + r) * RS, reinterpret_cast<const uint8_t*>(c.v_codes) + (r0 + r) * RB, RB, &full[st]);
+      }
+      if (lane < 4) {
+        const uint16_t* src = lane == 0 ? c.k_scales : lane == 1 ? c.k_biases : lane == 2 ? c.v_scales : c.v_biases;
+        bulk_g2s(sb + 2 * 64 * RS + lane * SB, src + r0 * NG, SB, &full[st]);
+      }
+      ++issued;
+    }
+    // Every issued copy must land before this CTA may exit.
+    for (int it = max(0, issued - nst); it < issued; ++it)
+      if (!mbar_wait(&full[it % nst], (it / nst) & 1)) flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
+    return;
+  }
+
+  // ------------------------------ consumers ------------------------------
+  const int t4 = lane & 3, rq = lane >> 2;
+  pdl_wait();                                   // q fragments come from qprep_kernel
+  uint32_t qa[NG][4][4];
+  {
+    const uint4* src = a.ws.qfrag + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32;
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint4 v = src[(g * 4 + ks) * 32 + lane];
+        qa[g][ks][0] = v.x; qa[g][ks][1] = v.y; qa[g][ks][2] = v.z; qa[g][ks][3] = v.w;
+      }
+    const float* qsg = a.ws.qsum + ((size_t)row * a.L.n_kv + kvh) * 16 * NG;
+    for (int i = threadIdx.x; i < 16 * NG; i += NW * 32) qs_sm[i] = qsg[i];
+  }
+  named_bar(1, NW * 32);
+
+  float oacc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  bool dead = false;
+  const int g_pv = warp;                        // PV group of this warp
+
+  for (int it = 0; it < tr.n_my; ++it) {
+    const int st = it % nst, buf = it & 1;
+    if (!dead && !mbar_wait(&full[st], (it / nst) & 1)) {
+      dead = true;
+      flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
+    }
+    const uint8_t* Ks = stages + st * STB;
+    const uint8_t* Vs = Ks + 64 * RS;
+    const uint16_t* sks = reinterpret_cast<const uint16_t*>(Ks + 2 * 64 * RS);
+    const uint16_t* skb = sks + 64 * NG;
+    const uint16_t* svs = skb + 64 * NG;
+    const uint16_t* svb = svs + 64 * NG;
+    const int tpos0 = (tr.t_begin + it) * kTileKeys;
+
+    // ---- QK ----
+    float S[NTQ][4];
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < NTQ; ++nt) {
+      const int kb8 = warp * KPW + nt * 8;
+      const int kB = kb8 + rq, kC = kb8 + 2 * t4;
+      S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+      const uint8_t* krow = Ks + kB * RS + t4 * (BITS * 2);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        float acc[4];
+        if constexpr (BITS == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(krow + g * 32);
+          mma_f16_zc(acc, qa[g][0], nib_lo(w.x), nib_hi(w.x));
+          mma_f16(acc, qa[g][1], nib_lo(w.x >> 8), nib_hi(w.x >> 8));
+          mma_f16(acc, qa[g][2], nib_lo(w.y), nib_hi(w.y));
+          mma_f16(acc, qa[g][3], nib_lo(w.y >> 8), nib_hi(w.y >> 8));
+        } else {
+          const uint4 w = *reinterpret_cast<const uint4*>(krow + g * 64);
+          mma_f16_zc(acc, qa[g][0], byte_lo(w.x), byte_lo(w.x >> 8));
+          mma_f16(acc, qa[g][1], byte_lo(w.y), byte_lo(w.y >> 8));
+          mma_f16(acc, qa[g][2], byte_lo(w.z), byte_lo(w.z >> 8));
+          mma_f16(acc, qa[g][3], byte_lo(w.w), byte_lo(w.w >> 8));
+        }
+        const float s0 = bf16_to_f(sks[kC * NG + g]), s1 = bf16_to_f(sks[(kC + 1) * NG + g]);
+        const float b0 = bf16_to_f(skb[kC * NG + g]), b1 = bf16_to_f(skb[(kC + 1) * NG + g]);
+        const float qr = qs_sm[rq * NG + g], qr8 = qs_sm[(rq + 8) * NG + g];
+        S[nt][0] = fmaf(s0, acc[0], fmaf(b0, qr, S[nt][0]));
+        S[nt][1] = fmaf(s1, acc[1], fmaf(b1, qr, S[nt][1]));
+        S[nt][2] = fmaf(s0, acc[2], fmaf(b0, qr8, S[nt][2]));
+        S[nt][3] = fmaf(s1, acc[3], fmaf(b1, qr8, S[nt][3]));
+      }
+      const int kp = tpos0 + kC;
+      const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 1 >= tr.lo && kp + 1 <= tr.hi;
+      if (!v0) { S[nt][0] = -INFINITY; S[nt][2] = -INFINITY; }
+      if (!v1) { S[nt][1] = -INFINITY; S[nt][3] = -INFINITY; }
+      tmax[0] = fmaxf(tmax[0], fmaxf(S[nt][0], S[nt][1]));
+      tmax[1] = fmaxf(tmax[1], fmaxf(S[nt][2], S[nt][3]));
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+      tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], m));
+      tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], m));
+    }
+    float* redb = red + buf * NW * 16;
+    if (t4 == 0) { redb[warp * 16 + rq] = tmax[0]; redb[warp * 16 + rq + 8] = tmax[1]; }
+    named_bar(1, NW * 32);
+
+    // ---- softmax update ----
+    float m_new[2], alpha[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mt = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) mt = fmaxf(mt, redb[w * 16 + rq + 8 * h]);
+      m_new[h] = fmaxf(m_run[h], mt);
+      alpha[h] = m_new[h] == -INFINITY ? 1.f : exp2f((m_run[h] - m_new[h]) * L2E);
+    }
+    uint8_t* Pb = Pbuf + buf * (16 * 64 * 2);
+    float lsum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < NTQ; ++nt) {
+      const int kC = warp * KPW + nt * 8 + 2 * t4;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float p0 = 0.f, p1 = 0.f;
+        if (m_new[h] != -INFINITY) {
+          p0 = exp2f((S[nt][2 * h] - m_new[h]) * L2E);
+          p1 = exp2f((S[nt][2 * h + 1] - m_new[h]) * L2E);
+        }
+        const __half2 ph = __floats2half2_rn(p0, p1);
+        const float2 pf = __half22float2(ph);
+        lsum[h] += pf.x + pf.y;
+        const int row = rq + 8 * h;
+        const int chunk = (kC >> 3) ^ (row & 7);
+        *reinterpret_cast<__half2*>(Pb + row * 128 + chunk * 16 + (kC & 7) * 2) = ph;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) { l_run[h] = l_run[h] * alpha[h] + lsum[h]; m_run[h] = m_new[h]; }
+    named_bar(1, NW * 32);
+
+    // ---- PV for this warp's 64-dim group ----
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
+      oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      {
+        const int mtx = lane >> 3, i = lane & 7;
+        const int row = (mtx & 1) * 8 + i;
+        const int chunk = (kk * 2 + (mtx >> 1)) ^ (row & 7);
+        ldmatrix_x4(pa, Pb + row * 128 + chunk * 16);
+      }
+      const int ka = kk * 16 + 2 * t4;           // keys ka, ka+1, ka+8, ka+9
+      const uint32_t sAB = bf16_pair_to_h2(svs[ka * NG + g_pv], svs[(ka + 1) * NG + g_pv]);
+      const uint32_t sCD = bf16_pair_to_h2(svs[(ka + 8) * NG + g_pv], svs[(ka + 9) * NG + g_pv]);
+      const uint32_t bAB = bf16_pair_to_h2(svb[ka * NG + g_pv], svb[(ka + 1) * NG + g_pv]);
+      const uint32_t bCD = bf16_pair_to_h2(svb[(ka + 8) * NG + g_pv], svb[(ka + 9) * NG + g_pv]);
+      if constexpr (BITS == 4) {
+        const uint8_t* vb = Vs + g_pv * 32 + rq * 4;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vb + ka * RS);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + (ka + 1) * RS);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vb + (ka + 8) * RS);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vb + (ka + 9) * RS);
+        const uint32_t xab = prmt(wa, wb, 0x5410), yab = prmt(wa, wb, 0x7632);
+        const uint32_t xcd = prmt(wc, wd, 0x5410), ycd = prmt(wc, wd, 0x7632);
+        const uint32_t src_ab[4] = {xab, xab >> 8, yab, yab >> 8};
+        const uint32_t src_cd[4] = {xcd, xcd >> 8, ycd, ycd >> 8};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo_ab = h2_fma(nib_lo(src_ab[q]), sAB, bAB), lo_cd = h2_fma(nib_lo(src_cd[q]), sCD, bCD);
+          const uint32_t hi_ab = h2_fma(nib_hi(src_ab[q]), sAB, bAB), hi_cd = h2_fma(nib_hi(src_cd[q]), sCD, bCD);
+          mma_f16(oacc[2 * q], pa, lo_ab, lo_cd);
+          mma_f16(oacc[2 * q + 1], pa, hi_ab, hi_cd);
+        }
+      } else {
+        const uint8_t* vb = Vs + g_pv * 64 + rq * 8;
+        const uint2 wa = *reinterpret_cast<const uint2*>(vb + ka * RS);
+        const uint2 wb = *reinterpret_cast<const uint2*>(vb + (ka + 1) * RS);
+        const uint2 wc = *reinterpret_cast<const uint2*>(vb + (ka + 8) * RS);
+        const uint2 wd = *reinterpret_cast<const uint2*>(vb + (ka + 9) * RS);
+        const uint32_t src_ab[4] = {prmt(wa.x, wb.x, 0x5410), prmt(wa.x, wb.x, 0x7632),
+                                    prmt(wa.y, wb.y, 0x5410), prmt(wa.y, wb.y, 0x7632)};
+        const uint32_t src_cd[4] = {prmt(wc.x, wd.x, 0x5410), prmt(wc.x, wd.x, 0x7632),
+                                    prmt(wc.y, wd.y, 0x5410), prmt(wc.y, wd.y, 0x7632)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t e_ab = h2_fma(byte_lo(src_ab[q]), sAB, bAB), e_cd = h2_fma(byte_lo(src_cd[q]), sCD, bCD);
+          const uint32_t o_ab = h2_fma(byte_lo(src_ab[q] >> 8), sAB, bAB), o_cd = h2_fma(byte_lo(src_cd[q] >> 8), sCD, bCD);
+          mma_f16(oacc[2 * q], pa, e_ab, e_cd);
+          mma_f16(oacc[2 * q + 1], pa, o_ab, o_cd);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+  pdl_launch();
+
+  // ---- write this split's partial (m, l, o) ----
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+  }
+  if (t4 == 0) { lred[warp * 16 + rq] = l_run[0]; lred[warp * 16 + rq + 8] = l_run[1]; }
+  named_bar(1, NW * 32);
+  const int G = a.L.G;
+  const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
+  float* po = a.ws.part_o + pidx * 16 * D;
+  float* ml = a.ws.part_ml + pidx * 32;
+  if (warp == 0) {
+    // every consumer warp holds the same running max; warp 0 writes it
+    if (t4 == 0) { ml[rq] = m_run[0]; ml[rq + 8] = m_run[1]; }
+    if (lane < 16) {
+      float l = 0.f;
+      for (int w = 0; w < NW; ++w) l += lred[w * 16 + lane];
+      ml[16 + lane] = l;
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const int d0 = g_pv * 64 + 8 * (2 * t4) + nt, d1 = d0 + 8;
+    if (rq < G) { po[rq * D + d0] = oacc[nt][0]; po[rq * D + d1] = oacc[nt][1]; }
+    if (rq + 8 < G) { po[(rq + 8) * D + d0] = oacc[nt][2]; po[(rq + 8) * D + d1] = oacc[nt][3]; }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(Dec<D>::THREADS) __maxnreg__(Dec<D>::MAX_REGS)
+decode_kernel(const DecodeArgs a, const int smem_total) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int row = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
+  const RowInfo ri = row_info(a, row);
+  const kvq_seq_cache c = a.seqs[ri.s];
+  const int p = ri.p;
+  const int W = a.L.window;
+  const int lo = W > 0 ? max(0, p - W + 1) : 0, hi = p;
+  // every key from lo up to the newest cached position must own its slot
+  const bool ok = seq_ok(c) && p >= 0 && ri.newest < (1 << 24) && p <= ri.newest &&
+                  (ri.newest - lo + 1) <= c.capacity;
+  const int t_lo = lo / kTileKeys, t_hi = hi / kTileKeys;
+  const int ntiles = t_hi - t_lo + 1;
+  const int chunk = (ntiles + a.splits - 1) / a.splits;
+  const int t_begin = t_lo + split * chunk;
+  const int n_my = ok ? max(0, min(chunk, t_hi + 1 - t_begin)) : 0;
+  if (n_my == 0) {
+    // nothing to read: an empty partial (m = -inf), or NaN for a bad sequence
+    if (!ok && split == 0 && kvh == 0 && threadIdx.x == 0) flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+    const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
+    if (threadIdx.x < 16) {
+      a.ws.part_ml[pidx * 32 + threadIdx.x] = ok ? -INFINITY : __int_as_float(0x7fc00000);
+      a.ws.part_ml[pidx * 32 + 16 + threadIdx.x] = 0.f;
+    }
+    pdl_launch();
+    return;
+  }
+  const int bits = c.bits;
+  const int nst = min(kMaxStages, (smem_total - stage0_off(D)) / stage_bytes(D, bits));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
+      mbar_init(reinterpret_cast<uint64_t*>(smem) + kMaxStages + i, Dec<D>::NW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const TileRange tr{t_begin, n_my, lo, hi};
+  if (bits == 4) decode_body<D, 4>(a, c, smem, nst, tr, row, kvh, split);
+  else decode_body<D, 8>(a, c, smem, nst, tr, row, kvh, split);
+}
+
+// ----------------------------------------------------------------------------
+// 3. merge split partials
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128)
+combine_kernel(const DecodeArgs a) {
+  pdl_wait();
+  const int row = blockIdx.x, hq = blockIdx.y;
+  const int G = a.L.G, kvh = hq / G, r = hq % G;
+  const size_t base = ((size_t)row * a.L.n_kv + kvh) * a.splits;
+  float M = -INFINITY;
+  bool nan = false;
+  for (int i = 0; i < a.splits; ++i) {
+    const float m = a.ws.part_ml[(base + i) * 32 + r];
+    nan |= m != m;
+    M = fmaxf(M, m);
+  }
+  float L = 0.f;
+  for (int i = 0; i < a.splits; ++i) {
+    const float m = a.ws.part_ml[(base + i) * 32 + r];
+    if (m != -INFINITY) L += exp2f((m - M) * 1.4426950408889634f) * a.ws.part_ml[(base + i) * 32 + 16 + r];
+  }
+  const float invL = nan ? __int_as_float(0x7fc00000) : 1.f / L;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.f;
+    for (int i = 0; i < a.splits; ++i) {
+      const float m = a.ws.part_ml[(base + i) * 32 + r];
+      if (m != -INFINITY && m == m)
+        acc += exp2f((m - M) * 1.4426950408889634f) * a.ws.part_o[((base + i) * 16 + r) * D + d];
+    }
+    const float o = acc * invL;
+    const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
+    if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
+    else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
+  }
+}
+
+template <int D>
+int decode_smem_bytes() {
+  // D = 512: one CTA per SM with the largest shared carve-out; smaller head
+  // dims leave room for several CTAs per SM.
+  return D >= 512 ? 227 * 1024 : (D == 256 ? 110 * 1024 : 56 * 1024);
+}
+
+template <int D>
+cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
+  static_assert(D % 64 == 0, "");
+  cudaError_t e;
+  const int smem = decode_smem_bytes<D>();
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  qprep_kernel<D><<<dim3(a.n_rows, a.L.n_kv), dim3(32 * a.L.G), 0, st>>>(a, f);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_rows, a.L.n_kv, a.splits);
+  cfg.blockDim = dim3(Dec<D>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, smem);
+  if (e != cudaSuccess) return e;
+
+  cfg.gridDim = dim3(a.n_rows, a.L.n_q);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
+  return e;
+}
+
+}  // namespace
+
+size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits) {
+  const size_t NG = D / 64, B = (size_t)n_rows * n_kv;
+  size_t off = 256;
+  off += B * NG * 4 * 32 * 16;                 // qfrag
+  off += B * 16 * NG * 4;                      // qsum
+  off = (off + 255) & ~size_t(255);
+  off += B * splits * 16 * (size_t)D * 4;      // part_o
+  off += B * splits * 32 * 4;                  // part_ml
+  return off;
+}
+
+DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
+  const size_t NG = D / 64, B = (size_t)n_rows * n_kv;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  DecodeWs w;
+  w.status = reinterpret_cast<uint32_t*>(p);
+  size_t off = 256;
+  w.qfrag = reinterpret_cast<uint4*>(p + off);
+  off += B * NG * 4 * 32 * 16;
+  w.qsum = reinterpret_cast<float*>(p + off);
+  off += B * 16 * NG * 4;
+  off = (off + 255) & ~size_t(255);
+  w.part_o = reinterpret_cast<float*>(p + off);
+  off += B * splits * 16 * (size_t)D * 4;
+  w.part_ml = reinterpret_cast<float*>(p + off);
+  return w;
+}
+
+int decode_pick_splits(const LayerArgs& L, int n_rows, int max_keys, int num_sms) {
+  const long keys = L.window > 0 ? std::min<long>((long)max_keys, L.window) : (long)max_keys;
+  const int tiles = int(keys / kTileKeys) + 2;
+  const int per_sm = L.D >= 512 ? 1 : (L.D == 256 ? 2 : 4);
+  const long base = (long)n_rows * L.n_kv;
+  long want = ((long)num_sms * per_sm + base - 1) / std::max<long>(base, 1);
+  want = std::min<long>(want, std::max(1, tiles / 2));
+  return int(std::max<long>(1, std::min<long>(want, 256)));
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int /*num_sms*/, cudaStream_t st) {
+  if (a.n_rows == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.ws.status, 0, 4, st);
+  if (e != cudaSuccess) return e;
+  switch (a.L.D) {
+    case 64: return launch_decode_t<64>(a, f, st);
+    case 128: return launch_decode_t<128>(a, f, st);
+    case 256: return launch_decode_t<256>(a, f, st);
+    case 512: return launch_decode_t<512>(a, f, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,74 @@
+// Internal launch interfaces between the C ABI (kvq_api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kMaxRopeHalf = 256;   // head_dim <= 512
+constexpr int kTileKeys = 64;       // keys per pipeline tile; capacities are multiples of it
+constexpr int kMaxG = 16;           // q heads per kv head handled by one MMA row block
+
+// theta^(-2j/D) for j < rope_dims/2, each as an exact sum of three floats.
+struct RopeFreqs {
+  float f[kMaxRopeHalf][3];
+};
+
+struct LayerArgs {
+  int n_q, n_kv, D, G, window, rope_dims, k_eq_v;
+  float eps;
+};
+
+struct AppendArgs {
+  LayerArgs L;
+  const kvq_seq_cache* seqs;
+  int n_seqs;
+  const int32_t* row_offsets;
+  const int32_t* start_pos;
+  int n_rows;
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  const uint16_t* k_w;
+  uint16_t* prepped;
+};
+
+// Workspace of the attention calls, carved from the caller's buffer.
+struct DecodeWs {
+  uint32_t* status;     // 1 word (padded to 256 B)
+  uint4* qfrag;         // [n_rows][n_kv][NG][4][32] x uint4
+  float* qsum;          // [n_rows][n_kv][16][NG]
+  float* part_o;        // [n_rows][n_kv][splits][16][D]
+  float* part_ml;       // [n_rows][n_kv][splits][2][16]  (m, l)
+};
+
+// Query rows of an attention call.  Decode: row i is sequence i at position
+// pos[i] (row_offsets == nullptr).  Prompt chunk: row i belongs to the
+// sequence s with row_offsets[s] <= i < row_offsets[s+1] and sits at position
+// pos[s] + (i - row_offsets[s]); the sequence's newest cached position is its
+// last row's.
+struct DecodeArgs {
+  LayerArgs L;
+  const kvq_seq_cache* seqs;
+  int n_seqs;
+  int n_rows;
+  const int32_t* row_offsets;
+  const int32_t* pos;
+  const uint16_t* q_raw;
+  const uint16_t* q_w;
+  void* out;
+  int out_f32;
+  uint16_t* q_prepped;
+  int splits;
+  DecodeWs ws;
+};
+
+size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits);
+DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits);
+int decode_pick_splits(const LayerArgs& L, int n_rows, int max_keys, int num_sms);
+
+cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
+
+}  // namespace kvq

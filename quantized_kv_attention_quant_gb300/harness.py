@@ -1,0 +1,215 @@
+"""Runs the library on the seeded workloads of `workloads`: allocates the
+caches in device memory, fills every cached position through kv_quant_append,
+uploads each step's inputs and runs steps.  The tests and bench.py drive the
+GPU path through these classes; the arithmetic happens only in libkvq.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads as W
+
+from . import (attn_decode, attn_decode_workspace_bytes, attn_prefill_chunk,
+               attn_prefill_workspace_bytes, kv_quant_append, layer as make_layer)
+from .cache import LayerCaches
+
+
+def kvq_layer(spec: W.LayerSpec):
+    return make_layer(spec.n_q_heads, spec.n_kv_heads, spec.head_dim, spec.window, spec.rope_dims,
+                      spec.rope_theta, spec.rms_eps, spec.k_eq_v)
+
+
+def dev_bits(a: np.ndarray, device) -> torch.Tensor:
+    """Upload bf16 bit patterns (uint16) as an int16 device tensor."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device)
+
+
+def dev_i32(values, device) -> torch.Tensor:
+    return torch.tensor(np.asarray(values, dtype=np.int32), device=device)
+
+
+def fill_caches(caches: LayerCaches, spec: W.LayerSpec, seed: int, layer_id: int, positions_of,
+                k_w: torch.Tensor, device, max_rows_per_call: int = 1 << 20, keep_prepped=False):
+    """Append the raw rows of every cached position of every sequence.
+
+    positions_of(s) -> int array of the positions resident before the step.
+    Returns {s: prepped [2, n, Hkv, D] uint16} when keep_prepped, else {}."""
+    lay = kvq_layer(spec)
+    desc_size = 56
+    kept = {}
+    s = 0
+    n = caches.n_seqs
+    while s < n:
+        # group sequences into one call up to max_rows_per_call rows
+        group, rows = [], 0
+        while s < n:
+            pos = positions_of(s)
+            if group and rows + len(pos) > max_rows_per_call:
+                break
+            group.append((s, pos))
+            rows += len(pos)
+            s += 1
+        if rows == 0:
+            continue
+        ks, vs, offs, starts = [], [], [0], []
+        for si, pos in group:
+            k, v = W.cache_rows(seed, layer_id, si, spec, pos)
+            ks.append(k)
+            if v is not None:
+                vs.append(v)
+            offs.append(offs[-1] + len(pos))
+            starts.append(int(pos[0]) if len(pos) else 0)
+        k_raw = dev_bits(np.concatenate(ks), device)
+        v_raw = dev_bits(np.concatenate(vs), device) if vs else None
+        prepped = None
+        if keep_prepped:
+            prepped = torch.empty((2, rows, spec.n_kv_heads, spec.head_dim), dtype=torch.int16, device=device)
+        first = group[0][0]
+        # the descriptor array of this group starts at sequence `first`
+        kv_quant_append(lay, caches.desc.data_ptr() + first * desc_size, len(group), dev_i32(offs, device),
+                        dev_i32(starts, device), rows, k_raw, v_raw, k_w, prepped)
+        if keep_prepped:
+            host = prepped.cpu().numpy().view(np.uint16)
+            for j, (si, _) in enumerate(group):
+                kept[si] = host[:, offs[j]:offs[j + 1]]
+        del k_raw, v_raw
+    return kept
+
+
+class DecodeCase:
+    """One decode step of one layer (DecodeWorkload): every sequence appends its
+    new token's K/V row, then attends with one query token."""
+
+    def __init__(self, wl: W.DecodeWorkload, device="cuda", keep_prepped=False, out_f32=True,
+                 caches: LayerCaches | None = None, fill=True):
+        self.wl, self.spec, self.device = wl, wl.layer, device
+        spec, n = wl.layer, wl.n_seqs
+        self.lay = kvq_layer(spec)
+        inp = W.layer_inputs(wl.seed, wl.layer_id, spec, n, n)
+        self.host_inputs = inp
+        self.q_w = dev_bits(inp["q_w"], device)
+        self.k_w = dev_bits(inp["k_w"], device)
+        self.q = dev_bits(inp["q"], device)
+        self.k = dev_bits(inp["k"], device)
+        self.v = dev_bits(inp["v"], device) if inp["v"] is not None else None
+        self.caches = caches or LayerCaches(spec.n_kv_heads, spec.head_dim, wl.bits,
+                                            [wl.capacity(s) for s in range(n)], device)
+        self.fill_prepped = {}
+        if fill:
+            self.fill_prepped = fill_caches(self.caches, spec, wl.seed, wl.layer_id, wl.cached_positions,
+                                            self.k_w, device, keep_prepped=keep_prepped)
+        self.pos = dev_i32(wl.filled, device)
+        self.offs = dev_i32(np.arange(n + 1), device)
+        self.max_pos = int(max(wl.filled))
+        self.ws_bytes = attn_decode_workspace_bytes(self.lay, n, self.max_pos)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.out_f32 = out_f32
+        self.out = torch.empty((n, spec.n_q_heads, spec.head_dim),
+                               dtype=torch.float32 if out_f32 else torch.int16, device=device)
+        self.keep_prepped = keep_prepped
+        self.q_prepped = torch.empty_like(self.q) if keep_prepped else None
+        self.kv_prepped = (torch.empty((2, n, spec.n_kv_heads, spec.head_dim), dtype=torch.int16, device=device)
+                           if keep_prepped else None)
+
+    def append(self, stream=None):
+        kv_quant_append(self.lay, self.caches.desc, self.wl.n_seqs, self.offs, self.pos, self.wl.n_seqs,
+                        self.k, self.v, self.k_w, self.kv_prepped, stream)
+
+    def attend(self, stream=None, caches: LayerCaches | None = None):
+        c = caches or self.caches
+        attn_decode(self.lay, c.desc, self.wl.n_seqs, self.pos, self.max_pos, self.q, self.q_w, self.out,
+                    self.out_f32, self.q_prepped, self.ws, self.ws_bytes, stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.attend(stream)
+
+    def status_word(self) -> int:
+        return int(self.ws[:4].cpu().numpy().view(np.uint32)[0])
+
+
+class PrefillCase:
+    """One prompt chunk of one layer (PrefillWorkload): every sequence appends
+    its chunk's K/V rows, then all chunk rows attend."""
+
+    def __init__(self, wl: W.PrefillWorkload, device="cuda", keep_prepped=False, out_f32=True, fill=True):
+        self.wl, self.spec, self.device = wl, wl.layer, device
+        spec, n = wl.layer, wl.n_seqs
+        self.lay = kvq_layer(spec)
+        rows = int(sum(wl.chunk))
+        self.n_rows = rows
+        self.host_inputs = []
+        qs, ks, vs = [], [], []
+        for s in range(n):
+            inp = W.layer_inputs(wl.seed, wl.layer_id, spec, wl.chunk[s], wl.chunk[s], seq=s)
+            self.host_inputs.append(inp)
+            qs.append(inp["q"]); ks.append(inp["k"])
+            if inp["v"] is not None:
+                vs.append(inp["v"])
+        w = self.host_inputs[0] if n else W.layer_inputs(wl.seed, wl.layer_id, spec, 0, 0)
+        self.q_w = dev_bits(w["q_w"], device)
+        self.k_w = dev_bits(w["k_w"], device)
+        self.q = dev_bits(np.concatenate(qs), device)
+        self.k = dev_bits(np.concatenate(ks), device)
+        self.v = dev_bits(np.concatenate(vs), device) if vs else None
+        self.caches = LayerCaches(spec.n_kv_heads, spec.head_dim, wl.bits,
+                                  [wl.capacity(s) for s in range(n)], device)
+        self.fill_prepped = {}
+        if fill:
+            self.fill_prepped = fill_caches(self.caches, spec, wl.seed, wl.layer_id, wl.cached_positions,
+                                            self.k_w, device, keep_prepped=keep_prepped)
+        self.offs = dev_i32(np.concatenate([[0], np.cumsum(wl.chunk)]), device)
+        self.start = dev_i32(wl.filled, device)
+        self.max_rows = int(max(wl.chunk))
+        self.ws_bytes = attn_prefill_workspace_bytes(self.lay, n, rows, self.max_rows)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.out_f32 = out_f32
+        self.out = torch.empty((rows, spec.n_q_heads, spec.head_dim),
+                               dtype=torch.float32 if out_f32 else torch.int16, device=device)
+        self.q_prepped = torch.empty_like(self.q) if keep_prepped else None
+        self.kv_prepped = (torch.empty((2, rows, spec.n_kv_heads, spec.head_dim), dtype=torch.int16, device=device)
+                           if keep_prepped else None)
+
+    def append(self, stream=None):
+        kv_quant_append(self.lay, self.caches.desc, self.wl.n_seqs, self.offs, self.start, self.n_rows,
+                        self.k, self.v, self.k_w, self.kv_prepped, stream)
+
+    def attend(self, stream=None):
+        attn_prefill_chunk(self.lay, self.caches.desc, self.wl.n_seqs, self.offs, self.start, self.n_rows,
+                           self.max_rows, self.q, self.q_w, self.out, self.out_f32, self.q_prepped, self.ws,
+                           self.ws_bytes, stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.attend(stream)
+
+    def status_word(self) -> int:
+        return int(self.ws[:4].cpu().numpy().view(np.uint32)[0])
+
+
+class StackCase:
+    """Decode step over the 42-layer stack (StackWorkload): donors 0..23 append
+    and attend their own caches; layers 24..41 attend their donor's cache."""
+
+    def __init__(self, wl: W.StackWorkload, device="cuda", out_f32=True):
+        self.wl = wl
+        self.layers = []
+        self.donor_case = {}
+        for i in range(W.N_LAYERS):
+            d = W.stack_cache_layer(i)
+            view = wl.decode_view(i)
+            if i < W.N_DONORS:
+                case = DecodeCase(view, device, out_f32=out_f32)
+                self.donor_case[i] = case
+            else:
+                # a sharer: its own q inputs, the donor's caches, no append
+                sv = W.DecodeWorkload(view.name, wl.seed, view.layer, view.filled, view.bits, layer_id=i)
+                case = DecodeCase(sv, device, out_f32=out_f32, caches=self.donor_case[d].caches, fill=False)
+            self.layers.append((i, d, case))
+
+    def step(self, stream=None):
+        for i, d, case in self.layers:
+            if i < W.N_DONORS:
+                case.append(stream)
+            case.attend(stream)

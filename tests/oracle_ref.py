@@ -1,0 +1,95 @@
+"""Expected values of the workloads, computed by the float64 oracle from the
+seeded inputs of `workloads` (never from anything the GPU produced)."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle as O
+import workloads as W
+
+
+def oracle_layer(spec: W.LayerSpec) -> W.LayerSpec:
+    """The layer as the library sees it: rms_eps is passed as a float32."""
+    return dataclasses.replace(spec, rms_eps=float(np.float32(spec.rms_eps)))
+
+
+def ring_slots(positions, capacity):
+    return np.asarray(positions, dtype=np.int64) % capacity
+
+
+@dataclasses.dataclass
+class SeqExpect:
+    cache: O.OracleCache
+    fill_positions: np.ndarray
+    fill_k_hat: np.ndarray
+    fill_v_hat: np.ndarray
+    resident: np.ndarray          # positions resident in the cache after the step
+    q_hat: np.ndarray             # [rows, Hq, D]
+    k_hat: np.ndarray             # new rows [rows, Hkv, D]
+    v_hat: np.ndarray
+    out: dict                     # row -> [Hq, D]
+
+
+def _fill(wl, spec, s, bits):
+    L = oracle_layer(spec)
+    pos = wl.cached_positions(s)
+    cache = O.OracleCache(spec.n_kv_heads, spec.head_dim, bits)
+    k_raw, v_raw = W.cache_rows(wl.seed, wl.layer_id, s, spec, pos)
+    inp = W.layer_inputs(wl.seed, wl.layer_id, spec, 0, 0)
+    k_w = O.bf16_to_f64(inp["k_w"])
+    if len(pos):
+        kh, vh = O.prep_kv(O.bf16_to_f64(k_raw), None if v_raw is None else O.bf16_to_f64(v_raw), k_w,
+                           pos, L.rope_theta, L.rope_dims, L.rms_eps)
+        cache.append(pos, kh, vh)
+    else:
+        kh = vh = np.zeros((0, spec.n_kv_heads, spec.head_dim))
+    return L, cache, pos, kh, vh
+
+
+def expect_decode(wl: W.DecodeWorkload, s: int) -> SeqExpect:
+    spec = wl.layer
+    L, cache, pos, kh, vh = _fill(wl, spec, s, wl.bits[s])
+    inp = W.layer_inputs(wl.seed, wl.layer_id, spec, wl.n_seqs, wl.n_seqs)
+    f = O.bf16_to_f64
+    p = wl.filled[s]
+    q_hat, k_new, v_new, out = O.decode_step(L, cache, p, f(inp["q"][s]), f(inp["q_w"]), f(inp["k"][s]),
+                                             None if inp["v"] is None else f(inp["v"][s]), f(inp["k_w"]))
+    cap = wl.capacity(s)
+    lo = max(0, p - cap + 1)
+    return SeqExpect(cache, pos, kh, vh, np.arange(lo, p + 1), q_hat[None], k_new[None], v_new[None], {0: out})
+
+
+def expect_prefill(wl: W.PrefillWorkload, s: int, rows=None) -> SeqExpect:
+    spec = wl.layer
+    L, cache, pos, kh, vh = _fill(wl, spec, s, wl.bits[s])
+    inp = W.layer_inputs(wl.seed, wl.layer_id, spec, wl.chunk[s], wl.chunk[s], seq=s)
+    f = O.bf16_to_f64
+    start = wl.filled[s]
+    q_hat, k_new, v_new, outs = O.prefill_chunk(L, cache, start, f(inp["q"]), f(inp["q_w"]), f(inp["k"]),
+                                                None if inp["v"] is None else f(inp["v"]), f(inp["k_w"]),
+                                                rows=rows)
+    cap = wl.capacity(s)
+    newest = start + wl.chunk[s] - 1
+    lo = max(0, newest - cap + 1)
+    return SeqExpect(cache, pos, kh, vh, np.arange(lo, newest + 1), q_hat, k_new, v_new, outs)
+
+
+def compare_cache(gpu_rows: dict, cache: O.OracleCache, positions) -> int:
+    """Number of mismatching words/scales/biases between the GPU cache rows
+    (gathered at the positions' slots) and the oracle's packed rows."""
+    kw, ks, kb, vw, vs, vb = cache.packed(positions)
+    # oracle arrays are [n, H, ...]; GPU rows are [H, n, ...]
+    pairs = [("k_codes", kw), ("k_scales", ks), ("k_biases", kb),
+             ("v_codes", vw), ("v_scales", vs), ("v_biases", vb)]
+    bad = 0
+    for name, want in pairs:
+        got = np.swapaxes(gpu_rows[name], 0, 1)
+        bad += int(np.count_nonzero(got != want))
+    return bad
+
+
+def attn_errors(got: np.ndarray, want: np.ndarray):
+    d = np.abs(np.asarray(got, dtype=np.float64) - want)
+    return float(d.max()), float(d.mean())

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/kvq.h declares, and rejects bad arguments with the documented status
+before enqueueing any GPU work (no compute call is made here)."""
+import ctypes
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def m():
+    from quantized_kv_attention_quant_gb300 import build
+    build.build()
+    import quantized_kv_attention_quant_gb300 as pkg
+    return pkg
+
+
+def test_exports_every_declared_function(m):
+    names = m.header_functions()
+    assert set(names) >= {"kv_quant_append", "attn_decode", "attn_prefill_chunk",
+                          "attn_decode_workspace_bytes", "attn_prefill_workspace_bytes",
+                          "kvq_status_string", "kvq_last_error", "kvq_version"}
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"libkvq.so does not export {n}"
+
+
+def test_status_strings_and_version(m):
+    assert m.kvq_status_string(0) == "ok"
+    for st in range(1, 5):
+        assert m.kvq_status_string(st) not in ("ok", "unknown status")
+    assert m.kvq_status_string(99) == "unknown status"
+    assert m.kvq_version() >= 100
+
+
+def test_struct_layout_matches_header(m):
+    assert ctypes.sizeof(m.KvqSeqCache) == 56
+    assert m.KvqSeqCache.bits.offset == 48 and m.KvqSeqCache.capacity.offset == 52
+    assert m.KvqLayer.rope_theta.offset == 24 and ctypes.sizeof(m.KvqLayer) == 40
+
+
+GOOD = dict(n_q_heads=8, n_kv_heads=2, head_dim=256, window=512, rope_dims=256, rope_theta=1e4)
+P = 1 << 20          # a fake, aligned "device address": never dereferenced (calls fail on the host)
+
+
+def _layer(m, **kw):
+    d = dict(GOOD)
+    d.update(kw)
+    return m.layer(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_q_heads=6, n_kv_heads=4), 1),       # not a multiple
+    (dict(n_q_heads=0), 1),
+    (dict(n_q_heads=34, n_kv_heads=2), 2),      # ratio 17 > 16
+    (dict(head_dim=96), 2),
+    (dict(head_dim=1024), 2),
+    (dict(window=-1), 1),
+    (dict(rope_dims=3), 1),
+    (dict(rope_dims=512), 1),
+    (dict(rope_theta=0.0), 1),
+    (dict(rope_theta=float("inf")), 1),
+])
+def test_bad_layer(m, kw, status):
+    lay = _layer(m, **kw)
+    st = m.lib.kv_quant_append(ctypes.byref(lay), P, 1, P, P, 1, P, P, P, None, None)
+    assert st == status
+    assert m.kvq_last_error()
+    assert m.attn_decode_workspace_bytes(lay, 1, 10) == 0
+
+
+def test_bad_group_and_eps(m):
+    lay = _layer(m)
+    lay.group_size = 32
+    assert m.lib.attn_decode(ctypes.byref(lay), P, 1, P, 10, P, P, P, 1, None, P, 1 << 30, None) == 2
+    lay = _layer(m, rms_eps=-1.0)
+    assert m.lib.attn_decode(ctypes.byref(lay), P, 1, P, 10, P, P, P, 1, None, P, 1 << 30, None) == 1
+    assert m.lib.attn_decode(None, P, 1, P, 10, P, P, P, 1, None, P, 1 << 30, None) == 1
+
+
+def test_bad_pointers_append(m):
+    lay = _layer(m)
+    f = m.lib.kv_quant_append
+    L = ctypes.byref(lay)
+    assert f(L, None, 1, P, P, 1, P, P, P, None, None) == 1            # seqs NULL
+    assert f(L, P + 4, 1, P, P, 1, P, P, P, None, None) == 1           # seqs misaligned
+    assert f(L, P, 1, P, P, 1, P + 8, P, P, None, None) == 1           # k_raw not 16-aligned
+    assert f(L, P, 1, P, P, 1, P, None, P, None, None) == 1            # v_raw missing
+    keqv = _layer(m, k_eq_v=True)
+    assert f(ctypes.byref(keqv), P, 1, P, P, 1, P, P, P, None, None) == 1   # v_raw given with K = V
+    assert f(L, P, 1, P, P, 1, P, P, P, P + 1, None) == 1              # kv_prepped odd address
+    assert f(L, P, -1, P, P, 1, P, P, P, None, None) == 1
+    assert f(L, P, 0, P, P, 1, P, P, P, None, None) == 1               # rows without sequences
+    assert f(L, P, 1, P, P, 0, P, P, P, None, None) == 0               # nothing to do
+
+
+def test_bad_pointers_decode(m):
+    lay = _layer(m)
+    f = m.lib.attn_decode
+    L = ctypes.byref(lay)
+    big = 1 << 40
+    assert f(L, P, 1, P, 10, P + 8, P, P, 1, None, P, big, None) == 1     # q_raw misaligned
+    assert f(L, P, 1, None, 10, P, P, P, 1, None, P, big, None) == 1      # pos NULL
+    assert f(L, P, 1, P, 10, P, P, P + 2, 1, None, P, big, None) == 1     # f32 out misaligned
+    assert f(L, P, 1, P, 10, P, P, P, 2, None, P, big, None) == 1         # out_is_f32 not 0/1
+    assert f(L, P, 1, P, 10, P, P, P, 1, None, P + 16, big, None) == 1    # workspace not 256-aligned
+    assert f(L, P, 1, P, -1, P, P, P, 1, None, P, big, None) == 1         # max_pos < 0
+    need = m.attn_decode_workspace_bytes(lay, 1, 10)
+    assert need > 0
+    assert f(L, P, 1, P, 10, P, P, P, 1, None, P, need - 1, None) == 4    # workspace too small
+    assert f(L, P, 0, P, 10, P, P, P, 1, None, P, 0, None) == 0           # no sequences: no work
+
+
+def test_bad_pointers_prefill(m):
+    lay = _layer(m)
+    f = m.lib.attn_prefill_chunk
+    L = ctypes.byref(lay)
+    assert f(L, P, 1, None, P, 4, 4, P, P, P, 1, None, P, 1 << 40, None) == 1   # row_offsets NULL
+    assert f(L, P, 1, P, P, 4, 0, P, P, P, 1, None, P, 1 << 40, None) == 1      # max_rows < 1
+    need = m.attn_prefill_workspace_bytes(lay, 1, 4, 4)
+    assert need > 0
+    assert f(L, P, 1, P, P, 4, 4, P, P, P, 1, None, P, need - 1, None) == 4
+
+
+def test_workspace_grows_with_rows(m):
+    lay = _layer(m)
+    assert m.attn_prefill_workspace_bytes(lay, 1, 64, 64) < m.attn_prefill_workspace_bytes(lay, 1, 512, 512)
+    full = _layer(m, window=0, head_dim=512, n_q_heads=16, n_kv_heads=1, rope_dims=128)
+    assert m.attn_decode_workspace_bytes(full, 8, 32768) > 0

@@ -1,0 +1,208 @@
+"""GPU path vs the float64 oracle, element by element, through the C ABI.
+
+Bars (from the statement of the method): the prepped bf16 rows and the packed
+codes / scales / biases bit-exact; attention outputs (fp32) within max-abs
+1e-2 and mean-abs 1e-3 of the oracle.  Sizes span several 64-key tiles with a
+ragged tail; the edge cases cover the first token, window 1, window larger
+than the history, ring wrap-around, rope_dims 0 / partial / full, GQA ratios
+1..16, head_dim 64..512, 4- and 8-bit caches mixed across sequences.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from oracle_ref import attn_errors, compare_cache, expect_decode, expect_prefill, ring_slots
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_kv_attention_quant_gb300 as m
+    from quantized_kv_attention_quant_gb300 import harness
+    return m, harness
+
+
+def _spec(n_q, n_kv, D, window, rope_dims, theta=1e4, k_eq_v=False):
+    return W.LayerSpec(n_q, n_kv, D, window, rope_dims, theta, k_eq_v)
+
+
+def check_decode(harness, wl, seqs=None, check_fill=True):
+    case = harness.DecodeCase(wl, keep_prepped=True)
+    case.step()
+    torch.cuda.synchronize()
+    assert case.status_word() == 0
+    out = case.out.cpu().numpy()
+    qp = case.q_prepped.cpu().numpy().view(np.uint16)
+    kvp = case.kv_prepped.cpu().numpy().view(np.uint16)
+    worst = (0.0, 0.0)
+    for s in (range(wl.n_seqs) if seqs is None else seqs):
+        e = expect_decode(wl, s)
+        if check_fill and len(e.fill_positions):
+            got = case.fill_prepped[s]
+            assert np.array_equal(got[0], O.f64_to_bf16(e.fill_k_hat)), f"seq {s}: fill k prep"
+            assert np.array_equal(got[1], O.f64_to_bf16(e.fill_v_hat)), f"seq {s}: fill v prep"
+        assert np.array_equal(qp[s], O.f64_to_bf16(e.q_hat[0])), f"seq {s}: q prep"
+        assert np.array_equal(kvp[0, s], O.f64_to_bf16(e.k_hat[0])), f"seq {s}: k prep"
+        assert np.array_equal(kvp[1, s], O.f64_to_bf16(e.v_hat[0])), f"seq {s}: v prep"
+        rows = case.caches.host_rows(s, ring_slots(e.resident, wl.capacity(s)))
+        assert compare_cache(rows, e.cache, e.resident) == 0, f"seq {s}: cache bytes"
+        mx, mean = attn_errors(out[s], e.out[0])
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, f"seq {s}: max {mx} mean {mean}"
+        worst = (max(worst[0], mx), max(worst[1], mean))
+    return case, worst
+
+
+DECODE_CASES = {
+    # name: (spec, filled per seq, bits per seq)
+    "sliding-ring-wrap": (_spec(8, 2, 256, 100, 256), [300, 99, 5], [4, 8, 4]),
+    "full-keqv-partial-rope": (_spec(16, 1, 512, 0, 128, 1e6, True), [0, 1, 63, 64, 65, 700], [4, 8, 4, 8, 4, 8]),
+    "window-1": (_spec(8, 2, 256, 1, 256), [0, 37, 200], [4, 8, 8]),
+    "window-over-history": (_spec(8, 2, 256, 4096, 256), [200, 1], [8, 4]),
+    "mha-no-rope-d128": (_spec(4, 4, 128, 0, 0), [129, 3], [4, 8]),
+    "d64-full-rope": (_spec(2, 1, 64, 0, 64), [80, 64], [8, 4]),
+    "gqa8-d256": (_spec(8, 1, 256, 0, 64, 1e6), [190], [4]),
+    "gqa1-d512-window": (_spec(2, 2, 512, 64, 512), [130, 64], [8, 4]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_CASES))
+def test_decode_small(kvq, name):
+    _, harness = kvq
+    spec, filled, bits = DECODE_CASES[name]
+    wl = W.DecodeWorkload(name, 77, spec, filled=filled, bits=bits)
+    _, worst = check_decode(harness, wl)
+    print(name, "worst", worst)
+
+
+def test_decode_bf16_output_is_rounded_f32(kvq):
+    _, harness = kvq
+    spec, filled, bits = DECODE_CASES["sliding-ring-wrap"]
+    wl = W.DecodeWorkload("bf16out", 78, spec, filled=filled, bits=bits)
+    a = harness.DecodeCase(wl)
+    a.step()
+    b = harness.DecodeCase(wl, out_f32=False)
+    b.step()
+    torch.cuda.synchronize()
+    f32 = a.out.cpu().numpy()
+    bf = b.out.cpu().numpy().view(np.uint16)
+    want = O.f64_to_bf16(O.rn_bf16(f32.astype(np.float64)))
+    assert np.array_equal(bf, want)
+
+
+def check_prefill(harness, wl, seqs=None, rows=None, nan_rows=None):
+    case = harness.PrefillCase(wl, keep_prepped=True)
+    case.step()
+    torch.cuda.synchronize()
+    out = case.out.cpu().numpy()
+    qp = case.q_prepped.cpu().numpy().view(np.uint16)
+    kvp = case.kv_prepped.cpu().numpy().view(np.uint16)
+    offs = np.concatenate([[0], np.cumsum(wl.chunk)])
+    worst = (0.0, 0.0)
+    for s in (range(wl.n_seqs) if seqs is None else seqs):
+        e = expect_prefill(wl, s, rows=rows)
+        r0, r1 = offs[s], offs[s + 1]
+        assert np.array_equal(qp[r0:r1], O.f64_to_bf16(e.q_hat)), f"seq {s}: q prep"
+        assert np.array_equal(kvp[0, r0:r1], O.f64_to_bf16(e.k_hat)), f"seq {s}: k prep"
+        assert np.array_equal(kvp[1, r0:r1], O.f64_to_bf16(e.v_hat)), f"seq {s}: v prep"
+        cache_rows = case.caches.host_rows(s, ring_slots(e.resident, wl.capacity(s)))
+        assert compare_cache(cache_rows, e.cache, e.resident) == 0, f"seq {s}: cache bytes"
+        for t, want in e.out.items():
+            got = out[r0 + t]
+            if nan_rows is not None and t in nan_rows.get(s, ()):
+                assert np.all(np.isnan(got)), f"seq {s} row {t}: expected NaN"
+                continue
+            mx, mean = attn_errors(got, want)
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, f"seq {s} row {t}: max {mx} mean {mean}"
+            worst = (max(worst[0], mx), max(worst[1], mean))
+    return case, worst
+
+
+def test_prefill_small_sliding(kvq):
+    _, harness = kvq
+    spec = _spec(8, 2, 256, 64, 256)
+    wl = W.PrefillWorkload("prefill-sliding", 79, spec, filled=[150, 0], chunk=[100, 37], bits=[8, 4])
+    _, worst = check_prefill(harness, wl)
+    print("worst", worst)
+
+
+def test_prefill_small_full_keqv(kvq):
+    _, harness = kvq
+    spec = _spec(16, 1, 512, 0, 128, 1e6, True)
+    wl = W.PrefillWorkload("prefill-full", 80, spec, filled=[130, 5], chunk=[70, 9], bits=[4, 8])
+    check_prefill(harness, wl)
+
+
+def test_prefill_rows_beyond_ring_are_nan(kvq):
+    """A chunk longer than its ring keeps only the newest `capacity` rows; rows
+    whose window reaches an overwritten key are reported as NaN."""
+    _, harness = kvq
+    spec = _spec(4, 1, 128, 64, 128)
+    wl = W.PrefillWorkload("prefill-overflow", 81, spec, filled=[10], chunk=[300], bits=[4])
+    cap = wl.capacity(0)                      # ring for chunk 300 = 384 slots: no overflow
+    assert cap >= 300 + 64 - 1
+    wl2 = dataclasses.replace(wl)
+    wl2.capacity = lambda s: 192              # force a too-small ring
+    wl2.cached_positions = lambda s: np.arange(0, 10)
+    newest = 10 + 300 - 1
+    valid_from = newest - 192 + 1 + 63 - 10   # row index whose window start fits
+    nan_rows = {0: set(range(0, valid_from))}
+    check_prefill(harness, wl2, rows=[0, valid_from - 1, valid_from, 299], nan_rows=nan_rows)
+
+
+def test_bad_descriptor_is_skipped(kvq):
+    """A descriptor with an unsupported width or a misaligned pointer is
+    skipped by the kernels: nothing written, NaN outputs, status bit set."""
+    m, harness = kvq
+    spec = _spec(8, 2, 256, 0, 256)
+    wl = W.DecodeWorkload("bad", 82, spec, filled=[70, 70], bits=[4, 4])
+    case = harness.DecodeCase(wl)
+    torch.cuda.synchronize()
+    raw = case.caches.desc.cpu().numpy().copy()
+    before = case.caches.seqs[1]["k_codes"].clone()
+    bad = raw.copy()
+    bad[56 + 48:56 + 52] = np.frombuffer(np.int32(5).tobytes(), np.uint8)      # bits = 5
+    case.caches.desc.copy_(torch.from_numpy(bad))
+    case.step()
+    torch.cuda.synchronize()
+    out = case.out.cpu().numpy()
+    assert np.all(np.isnan(out[1])) and np.all(np.isfinite(out[0]))
+    assert case.status_word() & (1 << 2)
+    assert torch.equal(before, case.caches.seqs[1]["k_codes"])
+    # misaligned scale pointer (still inside its allocation)
+    mis = raw.copy()
+    p = int(np.frombuffer(mis[56 + 16:56 + 24].tobytes(), np.uint64)[0]) + 2
+    mis[56 + 16:56 + 24] = np.frombuffer(np.uint64(p).tobytes(), np.uint8)
+    case.caches.desc.copy_(torch.from_numpy(mis))
+    case.attend()
+    torch.cuda.synchronize()
+    assert np.all(np.isnan(case.out.cpu().numpy()[1]))
+
+
+# ----------------------------------------------------------------------------
+# the measured workloads at full size (sampled sequences where the oracle
+# would take long)
+# ----------------------------------------------------------------------------
+
+def test_workload_tiny(kvq):
+    check_decode(kvq[1], W.workload_tiny_decode())
+
+
+def test_workload_sliding16(kvq):
+    check_decode(kvq[1], W.workload_sliding_decode_b16(), seqs=[0, 7, 8, 15])
+
+
+def test_workload_full32k(kvq):
+    check_decode(kvq[1], W.workload_full_keqv_decode(), seqs=[3], check_fill=False)
+
+
+def test_workload_prefill(kvq):
+    check_prefill(kvq[1], W.workload_prefill_chunk(), seqs=[2], rows=[0, 1, 255, 511])
