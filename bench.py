@@ -1,0 +1,452 @@
+"""Benchmark of the quantized-KV attention path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input.
+The default workload is the 42-layer mixed decode step: 64 ragged sequences
+(lengths uniform in [1024, 32768]), the 5 sliding : 1 full layer pattern of
+the e4b layer table, per-donor 4/8-bit caches, KV-shared layers 24..41.  Per
+step: 24 quantize-appends (q/k/v prep, quantize, pack) and 42 attention reads
+(split-K decode, combine), 64 decode tokens.  Other workloads (--workload):
+tiny, sliding16, full32k, prefill.
+
+The timed region replays a CUDA graph holding K steps (inputs resident in
+HBM); `e2e` repeats K steps through the Python binding with inputs copied
+from pinned host memory and outputs copied back every step.  The reference
+arm (--impl reference) times the float64 CPU oracle on a bounded sample.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def rb_pair(D: int, bits: int) -> int:
+    """Bytes of one cached key+value row: packed codes plus bf16 scale and
+    bias per 64-group, for K and for V."""
+    return 2 * (D * bits // 8 + (D // 64) * 4)
+
+
+def visible_keys(p: int, window: int) -> int:
+    return p + 1 if window <= 0 else min(p + 1, window)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
+
+    def find(d, keys):
+        if isinstance(d, dict):
+            for k, v in d.items():
+                if k in keys and isinstance(v, (int, float)):
+                    return float(v)
+                r = find(v, keys)
+                if r is not None:
+                    return r
+        return None
+    hbm = find(mp, {"hbm_gbs", "hbm_GBps", "hbm_copy_gbs"})
+    bf = find(mp, {"bf16_tflops_sustained"}) or find(mp, {"bf16_tflops"})
+    return {"hbm_gbs": hbm or FALLBACK_HBM_GBS, "bf16_tflops": bf or FALLBACK_BF16_TFLOPS,
+            "source": "measured" if hbm else "fallback"}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_kv_attention_quant_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas of independent work)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def dist_barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def dist_max(value: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (timing metadata only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def build_workload(name: str, rank: int, device):
+    from quantized_kv_attention_quant_gb300 import harness
+    if name == "stack42":
+        wl = W.workload_stack_decode()
+        if rank:
+            wl = W.StackWorkload(wl.name, wl.seed + 100 * rank, wl.lengths, wl.donor_bits)
+        case = harness.StackCase(wl, device=device, out_f32=False)
+        calls = []           # (kind, case) in step order, for e2e and accounting
+        for i, d, c in case.layers:
+            calls.append((i < W.N_DONORS, c))
+        full_bytes = 0
+        kv_bytes = 0
+        for i, d, c in case.layers:
+            spec = c.spec
+            by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
+                     for p, b in zip(c.wl.filled, c.wl.bits)) * spec.n_kv_heads
+            kv_bytes += by
+            if spec.window == 0:
+                full_bytes += by
+        info = {"tokens": wl.n_seqs, "kv_bytes": kv_bytes, "dominant_bytes": full_bytes,
+                "dominant": "decode_kernel<512> (full-attention layers)",
+                "launches": 24 + 42 * 3, "config": {
+                    "workload": "42-layer mixed decode step, 64 ragged sequences (lengths U[1024,32768]), "
+                                "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64",
+                    "n_seqs": wl.n_seqs, "layers": 42, "kv_donor_layers": 24}}
+        return case, calls, info
+    if name in ("tiny", "sliding16", "full32k"):
+        wl = W.WORKLOADS[name]()
+        case = harness.DecodeCase(wl, device=device, out_f32=False)
+        spec = wl.layer
+        by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
+                 for p, b in zip(wl.filled, wl.bits)) * spec.n_kv_heads
+        info = {"tokens": wl.n_seqs, "kv_bytes": by, "dominant_bytes": by,
+                "dominant": f"decode_kernel<{spec.head_dim}>", "launches": 1 + 3,
+                "config": {"workload": wl.name, "n_seqs": wl.n_seqs}}
+        return case, [(True, case)], info
+    if name == "prefill":
+        wl = W.workload_prefill_chunk()
+        case = harness.PrefillCase(wl, device=device, out_f32=False)
+        spec = wl.layer
+        rows = sum(wl.chunk)
+        flops = 0
+        for s in range(wl.n_seqs):
+            for t in range(wl.chunk[s]):
+                flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
+        info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
+                "dominant": f"decode_kernel<{spec.head_dim}> (prompt rows)", "launches": 1 + 3,
+                "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
+        return case, [(True, case)], info
+    raise SystemExit(f"unknown workload {name}")
+
+
+def step_calls(calls, stream=None):
+    for donor, c in calls:
+        if donor:
+            c.append(stream)
+        c.attend(stream)
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    case, calls, info = build_workload(args.workload, rank, device)
+    torch.cuda.synchronize()
+
+    # warm-up, eager (first calls also set kernel attributes)
+    for _ in range(args.warmup):
+        step_calls(calls)
+    torch.cuda.synchronize()
+
+    # capture K steps into one graph, with timing events around each attention
+    # call of the dominant kernel
+    stream = torch.cuda.Stream(device=device)
+    K = args.steps
+    full_calls = [c for _, c in calls if c.spec.window == 0] if args.workload == "stack42" else [c for _, c in calls]
+    try:
+        ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in full_calls] for _ in range(K)]
+        have_inner = True
+    except TypeError:
+        ev, have_inner = None, False
+    graph = torch.cuda.CUDAGraph()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step_calls(calls)                      # one more warm-up on the capture stream
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(K):
+            j = 0
+            for donor, c in calls:
+                if donor:
+                    c.append()
+                inner = have_inner and c in full_calls
+                if inner:
+                    ev[k][j][0].record()
+                c.attend()
+                if inner:
+                    ev[k][j][1].record()
+                    j += 1
+    torch.cuda.synchronize()
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        dist_barrier(world, device)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world, device)
+    ms_total = t0.elapsed_time(t1)
+    ms_total = dist_max(ms_total, world, device)
+    ms_step = ms_total / K
+    tokens_per_step = info["tokens"] * world
+    value = tokens_per_step / (ms_step / 1e3)
+
+    # dominant-kernel duration from the events inside the graph
+    dom_ms = None
+    if have_inner:
+        dom_ms = sum(a.elapsed_time(b) for row in ev for a, b in row) / K
+    status_ok = all(c.status_word() == 0 for _, c in calls)
+
+    # e2e through the binding with host buffers
+    e2e = run_e2e(calls, K, device, info, world)
+
+    peaks = load_peaks()
+    roof = None
+    if args.workload == "prefill":
+        if dom_ms:
+            achieved = info["flops"] / (dom_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                    "peak_source": peaks["source"] + " bf16 (f16 runs at the bf16 rate)",
+                    "kernel": info["dominant"]}
+    elif dom_ms:
+        achieved = info["dominant_bytes"] / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic_for("decode_kernel_512" if "512" in info["dominant"] else info["dominant"],
+                                       args.workload),
+                "peak_source": peaks["source"], "kernel": info["dominant"],
+                "launch_ms": dom_ms / max(1, len(full_calls))}
+    step_gbs = info["kv_bytes"] / (ms_step / 1e3) / 1e9 if info["kv_bytes"] else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.workload, steps=1, warmup=0)
+
+    cfg = dict(info["config"])
+    cfg.update({"l2": "inputs larger than L2" if info["kv_bytes"] > 129e6 else
+                "inputs smaller than L2 (launch-bound case)",
+                "kv_bytes_per_step": info["kv_bytes"], "step_kv_gbs": step_gbs,
+                "graph": f"{K} steps captured in one CUDA graph", "device_status_clean": status_ok})
+    line = {"metric": "decode-attention tokens/s" if args.workload != "prefill" else "prefill tokens/s",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic (seeded N(0,1) bf16 inputs, norm weights 1+N(0,0.1))",
+            "config": cfg, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": info["launches"] * K, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(calls, K, device, info, world):
+    """K steps through the binding; every step copies its q/k/v inputs from
+    pinned host memory and its outputs back."""
+    import torch
+    host_in, host_out = [], []
+    for donor, c in calls:
+        ins = [c.q] + ([c.k] + ([c.v] if c.v is not None else []) if donor else [])
+        host_in.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins])
+        host_out.append(torch.empty(c.out.shape, dtype=c.out.dtype, pin_memory=True))
+    bi = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    bo = sum(t.numel() * t.element_size() for t in host_out)
+    s = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist_barrier(world, device)
+    t0.record(s)
+    for _ in range(K):
+        for (donor, c), hs in zip(calls, host_in):
+            devs = [c.q] + ([c.k] + ([c.v] if c.v is not None else []) if donor else [])
+            for d, h in zip(devs, hs):
+                d.copy_(h, non_blocking=True)
+        step_calls(calls)
+        for (donor, c), h in zip(calls, host_out):
+            h.copy_(c.out, non_blocking=True)
+    t1.record(s)
+    torch.cuda.synchronize()
+    dist_barrier(world, device)
+    ms = dist_max(t0.elapsed_time(t1), world, device) / K
+    return {"value": info["tokens"] * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+CPU_SAMPLE_SEQS = 2
+
+
+def run_cpu_baseline(workload: str, steps: int, warmup: int):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.join(ROOT, "oracle", "timing.py"), workload, str(steps), str(warmup),
+           str(CPU_SAMPLE_SEQS)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT, timeout=1800)
+    if r.returncode != 0:
+        return {"error": r.stderr[-500:]}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": res["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": res["sample"], "ms_per_step": res["ms_per_step"]}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    res = run_cpu_baseline(args.workload, steps=args.steps, warmup=args.warmup)
+    line = {"impl": "reference", "metric": "decode-attention tokens/s" if args.workload != "prefill"
+            else "prefill tokens/s", "value": res.get("value"), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.get("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, same generators as the GPU arm)",
+            "config": {"workload": args.workload, "sample": res.get("sample")},
+            "cpu_baseline": res,
+            "e2e": {"value": res.get("value"), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="stack42",
+                    choices=["stack42", "tiny", "sliding16", "full32k", "prefill"])
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

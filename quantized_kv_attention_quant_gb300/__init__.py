@@ -44,7 +44,7 @@ class KvqError(RuntimeError):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run "
-                          "`python -m quantized_kv_attention_quant_gb300.build` (needs nvcc)")
+                          "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     lay = ctypes.POINTER(KvqLayer)

@@ -5,11 +5,15 @@
 // Three launches on the caller's stream:
 //   1. qprep_kernel   (n_kv, n_seqs): q RMSNorm + RoPE for the G q heads of a kv
 //      head, written as ready-made mma.sync A fragments plus per-group sums.
-//   2. decode_kernel  (splits, n_kv, n_seqs), programmatic dependent launch:
-//      split-K ("flash decoding") over the visible keys.  Warp NW is a TMA
-//      producer streaming 64-key tiles (packed codes row by row into padded
-//      shared rows, scales and biases) through an mbarrier ring; warps
-//      0..NW-1 compute
+//   2. decode_kernel  (rows, n_kv, splits), programmatic dependent launch:
+//      split-K ("flash decoding") over the visible keys.  64-key tiles (packed
+//      codes row by row into padded shared rows, scales and biases) stream
+//      through a ring of stages filled by TMA bulk copies and tracked by
+//      mbarriers.  There is no producer warp (a 9th warp would share a
+//      register sub-partition with two consumers and cap them at 168
+//      registers): once a tile's max-exchange barrier shows every warp is done
+//      with the previous tile, the warps refill that stage themselves.
+//      Warps 0..NW-1 compute
 //        QK: warp w takes 64/NW keys, all G heads (M = 16 rows), full head_dim;
 //            codes enter the tensor cores exactly as f16 integers, per 64-dim
 //            group: S += scale * (q . codes) + bias * sum(q)
@@ -33,11 +37,8 @@ struct Dec {
   static constexpr int NW = NG;
   static constexpr int KPW = 64 / NW;        // keys per consumer warp in QK
   static constexpr int NTQ = KPW / 8;        // QK n-tiles per warp
-  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int THREADS = NW * 32;      // no dedicated producer warp
   static constexpr int MIN_BLOCKS = D >= 512 ? 1 : (D == 256 ? 2 : 4);
-  // registers per thread that still fit MIN_BLOCKS CTAs in the 64K register file
-  static constexpr int MAX_REGS_RAW = 65536 / (THREADS * MIN_BLOCKS) / 8 * 8;
-  static constexpr int MAX_REGS = MAX_REGS_RAW > 248 ? 248 : MAX_REGS_RAW;
 };
 
 constexpr int kMaxStages = 8;
@@ -195,47 +196,38 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   constexpr float L2E = 1.4426950408889634f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
   float* red = reinterpret_cast<float*>(smem + 128);        // [2][NW][16]
   float* lred = red + 2 * NW * 16;                          // [NW][16]
   float* qs_sm = lred + NW * 16;                            // [16][NG]
   uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
   uint8_t* stages = smem + stage0_off(D);
   const int cap = c.capacity;
+  const size_t head_row0 = (size_t)kvh * cap;
 
-  if (warp == NW) {
-    // ------------------------------ producer ------------------------------
-    const uint32_t tile_tx = 2 * 64 * RB + 4 * SB;
-    const size_t head_row0 = (size_t)kvh * cap;
-    int issued = 0;
-    for (int it = 0; it < tr.n_my; ++it) {
-      const int st = it % nst;
-      if (it >= nst && !mbar_wait(&empty[st], ((it / nst) & 1) ^ 1)) {
-        flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
-        break;
+  // Issue tile `it` into its stage: 128 code rows and 4 scale/bias blocks,
+  // spread over all threads of the CTA (one or two copies each).
+  auto issue = [&](int it) {
+    const int st = it % nst;
+    uint8_t* sb = stages + st * STB;
+    const size_t r0 = head_row0 + ((tr.t_begin + it) * kTileKeys) % cap;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&full[st], 2 * 64 * RB + 4 * SB);
+    fence_proxy_async();        // order this CTA's earlier generic reads of the stage before the copies
+    for (int j = threadIdx.x; j < 2 * 64 + 4; j += NW * 32) {
+      if (j < 64) {
+        bulk_g2s(sb + j * RS, reinterpret_cast<const uint8_t*>(c.k_codes) + (r0 + j) * RB, RB, &full[st]);
+      } else if (j < 128) {
+        const int r = j - 64;
+        bulk_g2s(sb + j * RS, reinterpret_cast<const uint8_t*>(c.v_codes) + (r0 + r) * RB, RB, &full[st]);
+      } else {
+        const int q = j - 128;
+        const uint16_t* src = q == 0 ? c.k_scales : q == 1 ? c.k_biases : q == 2 ? c.v_scales : c.v_biases;
+        bulk_g2s(sb + 2 * 64 * RS + q * SB, src + r0 * NG, SB, &full[st]);
       }
-      const int slot0 = ((tr.t_begin + it) * kTileKeys) % cap;
-      uint8_t* sb = stages + st * STB;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], tile_tx);
-      __syncwarp();
-      const size_t r0 = head_row0 + slot0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        bulk_g2s(sb + r * RS, reinterpret_cast<const uint8_t*>(c.k_codes) + (r0 + r) * RB, RB, &full[st]);
-        bulk_g2s(sb + (64 + r) * RS, reinterpret_cast<const uint8_t*>(c.v_codes) + (r0 + r) * RB, RB, &full[st]);
-      }
-      if (lane < 4) {
-        const uint16_t* src = lane == 0 ? c.k_scales : lane == 1 ? c.k_biases : lane == 2 ? c.v_scales : c.v_biases;
-        bulk_g2s(sb + 2 * 64 * RS + lane * SB, src + r0 * NG, SB, &full[st]);
-      }
-      ++issued;
     }
-    // Every issued copy must land before this CTA may exit.
-    for (int it = max(0, issued - nst); it < issued; ++it)
-      if (!mbar_wait(&full[it % nst], (it / nst) & 1)) flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
-    return;
-  }
+  };
+  // prologue: fill every stage (the cache was written before this launch)
+  for (int it = 0; it < min(nst, tr.n_my); ++it) issue(it);
+  int issued = min(nst, tr.n_my);
 
   // ------------------------------ consumers ------------------------------
   const int t4 = lane & 3, rq = lane >> 2;
@@ -324,6 +316,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     float* redb = red + buf * NW * 16;
     if (t4 == 0) { redb[warp * 16 + rq] = tmax[0]; redb[warp * 16 + rq + 8] = tmax[1]; }
     named_bar(1, NW * 32);
+    // every warp has finished tile it-1: its stage takes tile it-1+nst
+    if (it >= 1 && issued < tr.n_my) {
+      issue(issued);
+      ++issued;
+    }
 
     // ---- softmax update ----
     float m_new[2], alpha[2];
@@ -415,10 +412,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
   }
   pdl_launch();
+  // a timed-out wait may leave copies in flight: they must land before exit
+  if (dead && threadIdx.x == 0)
+    for (int it = max(0, issued - nst); it < issued; ++it) mbar_wait(&full[it % nst], (it / nst) & 1);
 
   // ---- write this split's partial (m, l, o) ----
 #pragma unroll
@@ -450,7 +448,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
 }
 
 template <int D>
-__global__ void __launch_bounds__(Dec<D>::THREADS) __maxnreg__(Dec<D>::MAX_REGS)
+__global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
 decode_kernel(const DecodeArgs a, const int smem_total) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int row = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
@@ -481,10 +479,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
   const int bits = c.bits;
   const int nst = min(kMaxStages, (smem_total - stage0_off(D)) / stage_bytes(D, bits));
   if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
-      mbar_init(reinterpret_cast<uint64_t*>(smem) + kMaxStages + i, Dec<D>::NW);
-    }
+    for (int i = 0; i < nst; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
     fence_mbar_init();
   }
   __syncthreads();

@@ -8,8 +8,8 @@ import pytest
 
 @pytest.fixture(scope="module")
 def m():
-    from quantized_kv_attention_quant_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import quantized_kv_attention_quant_gb300 as pkg
     return pkg
 

@@ -35,9 +35,9 @@ def _rng(seed: int, *key: int) -> np.random.Generator:
 def bf16_bits_from_f32(a: np.ndarray) -> np.ndarray:
     """Round-to-nearest-even of float32 values to bf16 bit patterns (uint16).
 
-    Generated values are finite, so no NaN handling is needed."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    Generated values are finite, so the uint32 sum below cannot wrap."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return u.astype(np.uint16)
 
 
