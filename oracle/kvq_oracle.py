@@ -37,6 +37,8 @@ Readings taken where the pages are silent:
   R-window: a query at position p sees keys max(0, p-W+1) .. p (W keys).
   R-round: bf16 rounding after the norm and after RoPE (the pages keep the
           normed and roped tensors as separate bf16 arrays).
+  R-zero: a group whose minimum (maximum) is a zero stores +0 as its bias;
+          zeros elsewhere keep their IEEE sign.
 
 Values are carried as float64 arrays holding bf16-representable numbers.
 """
@@ -161,8 +163,10 @@ def quantize(x: np.ndarray, bits: int):
     if D % GROUP:
         raise ValueError("head_dim must be a multiple of 64")
     g = x.reshape(*x.shape[:-1], D // GROUP, GROUP).astype(np.float32)   # exact
-    mn = g.min(axis=-1)
-    mx = g.max(axis=-1)
+    # a zero minimum / maximum is taken as +0 (reading R-zero: the sign of a
+    # zero extremum is otherwise unspecified)
+    mn = g.min(axis=-1) + np.float32(0)
+    mx = g.max(axis=-1) + np.float32(0)
     levels = np.float32(2 ** bits - 1)
     s32 = (mx - mn) / levels                                     # two fp32 roundings
     s = rn_bf16(s32.astype(np.float64)).astype(np.float32)       # stored bf16 scale

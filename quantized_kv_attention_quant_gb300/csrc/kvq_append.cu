@@ -51,6 +51,9 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], cons
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
   }
+  // a zero minimum or maximum is taken as +0 (min/max of -0 and +0 is unordered)
+  mn = __fadd_rn(mn, 0.f);
+  mx = __fadd_rn(mx, 0.f);
   // scale = bf16((max - min) / (2^bits - 1)), two IEEE fp32 roundings
   const uint16_t sb = f_to_bf16_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)TOP));
   const float sf = bf16_to_f(sb);
@@ -123,7 +126,9 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
                   aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases) &&
                   pos >= 0 && pos < (1 << 24);
   if (!ok) return;
-  if (t_in < rows_s - c.capacity) return;   // overwritten by a newer row of this call
+  // a row whose slot a newer row of this call overwrites is prepped (for
+  // kv_prepped) but not stored
+  const bool store = t_in >= rows_s - c.capacity;
 
   // ---- load the raw row ----
   const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
@@ -193,6 +198,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
   }
 
   // ---- quantize the 64-element group, pack, store ----
+  if (!store) return;
   if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, lane);
   else quantize_store<D, 8>(y, c, kind, head, pos, lane);
 }

@@ -121,6 +121,8 @@ __device__ __forceinline__ ff rms_inv(ff ss, int D, float eps) {
 // exact in fp32.
 __device__ __forceinline__ uint16_t norm_scale_bf16(float x, float w, ff inv) {
   float xw = __fmul_rn(x, w);
+  // exact zero keeps its IEEE sign (inv > 0); the float-float sums would drop it
+  if (xw == 0.f) return uint16_t(__float_as_uint(xw) >> 16);
   return ff_to_bf16_rn(ff_mul_f(inv, xw));
 }
 
@@ -199,6 +201,8 @@ __device__ __forceinline__ void rope_cos_sin(int p, float f1, float f2, float f3
 
 // x*c - y*s, correctly rounded to bf16 (x, y bf16 values; c, s float-float).
 __device__ __forceinline__ uint16_t rot_bf16(float x, float y, ff c, ff s) {
+  if (x == 0.f && y == 0.f)   // signed zero as IEEE arithmetic gives it
+    return uint16_t(__float_as_uint(__fsub_rn(__fmul_rn(x, c.hi), __fmul_rn(y, s.hi))) >> 16);
   ff a = ff_mul_f(c, x);
   ff b = ff_mul_f(s, y);
   return ff_to_bf16_rn(ff_add(a, ff_neg(b)));

@@ -5,6 +5,10 @@ GPU path through these classes; the arithmetic happens only in libkvq.so.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import multiprocessing as mp
+import os
+
 import numpy as np
 import torch
 
@@ -27,6 +31,19 @@ def dev_bits(a: np.ndarray, device) -> torch.Tensor:
 
 def dev_i32(values, device) -> torch.Tensor:
     return torch.tensor(np.asarray(values, dtype=np.int32), device=device)
+
+
+_POOL = None
+
+
+def _gen_pool():
+    """Worker processes for drawing cache rows (spawned, so safe to start after
+    CUDA is initialised in this process)."""
+    global _POOL
+    if _POOL is None:
+        n = max(1, min(16, (os.cpu_count() or 2) - 1))
+        _POOL = cf.ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"))
+    return _POOL
 
 
 def fill_caches(caches: LayerCaches, spec: W.LayerSpec, seed: int, layer_id: int, positions_of,
@@ -53,8 +70,12 @@ def fill_caches(caches: LayerCaches, spec: W.LayerSpec, seed: int, layer_id: int
         if rows == 0:
             continue
         ks, vs, offs, starts = [], [], [0], []
-        for si, pos in group:
-            k, v = W.cache_rows(seed, layer_id, si, spec, pos)
+        jobs = [(seed, layer_id, si, spec, pos) for si, pos in group]
+        if rows >= 65536 and len(group) > 1:
+            results = list(_gen_pool().map(W.cache_rows_job, jobs))
+        else:
+            results = [W.cache_rows_job(j) for j in jobs]
+        for (si, pos), (k, v) in zip(group, results):
             ks.append(k)
             if v is not None:
                 vs.append(v)

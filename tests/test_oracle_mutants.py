@@ -36,13 +36,14 @@ MUTANTS = {
                         "x = c * np.asarray(scales)[..., None]"),
     "v-norm-weighted": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
                         "v_hat = rms_norm(k_raw if v_raw is None else v_raw, k_w, eps)"),
+    "quant-signed-zero-bias": ("    mn = g.min(axis=-1) + np.float32(0)\n", "    mn = g.min(axis=-1)\n"),
     "bf16-7-bits": ("q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
                     "q = np.ldexp(np.rint(np.ldexp(x, 7 - e)), e - 7)"),
 }
 
 PINS = [
     P.pin_rn_bf16, P.pin_quant_ramp4, P.pin_quant_exact8, P.pin_quant_constant,
-    P.pin_quant_ties, P.pin_quant_bf16_scale_divides, P.pin_quant_group_independence,
+    P.pin_quant_ties, P.pin_quant_negative_zero, P.pin_quant_bf16_scale_divides, P.pin_quant_group_independence,
     lambda o: P.pin_quant_invariants(o, 4), lambda o: P.pin_quant_invariants(o, 8),
     P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants,
     P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,

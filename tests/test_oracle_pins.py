@@ -83,6 +83,20 @@ def pin_quant_constant(o):
     assert np.all(o.dequantize(c, s, b) == -1.375)
 
 
+def pin_quant_negative_zero(o):
+    # reading R-zero: a -0 group minimum is stored as +0; the codes are as for +0
+    x = np.full(64, -0.0)           # every zero is -0, so the raw minimum is -0
+    x[5] = 15.0
+    x[1:5] = 1.0
+    c, s, b = o.quantize(x[None], 4)
+    assert s[0, 0] == 1.0 and b[0, 0] == 0.0 and not np.signbit(b[0, 0])
+    assert o.f64_to_bf16(b)[0, 0] == 0x0000
+    assert c[0, 0] == 0 and c[0, 1] == 1 and c[0, 5] == 15
+    # the norm keeps the sign of a zero input (IEEE division)
+    y = o.rms_norm(np.array([[-0.0, 2.0]]), None, 0.0)
+    assert np.signbit(y[0, 0]) and y[0, 0] == 0.0
+
+
 def pin_quant_ties(o):
     # min 0, max 15 -> scale 1.  (x - 0) / 1 = 2.5 -> 2 and 3.5 -> 4 (half to even)
     x = np.zeros(64)
@@ -121,7 +135,7 @@ def pin_quant_group_independence(o):
 
 
 @pytest.mark.parametrize("pin", [pin_quant_ramp4, pin_quant_exact8, pin_quant_constant,
-                                 pin_quant_ties, pin_quant_bf16_scale_divides,
+                                 pin_quant_ties, pin_quant_negative_zero, pin_quant_bf16_scale_divides,
                                  pin_quant_group_independence])
 def test_quant_hand_cases(pin):
     pin(O)

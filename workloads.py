@@ -196,6 +196,11 @@ def cache_rows(seed: int, layer_id: int, seq: int, layer: LayerSpec, positions: 
     return k, v
 
 
+def cache_rows_job(args):
+    """cache_rows(*args), for process pools (this module imports no torch)."""
+    return cache_rows(*args)
+
+
 # ----------------------------------------------------------------------------
 # the five measured workloads
 # ----------------------------------------------------------------------------
