@@ -297,12 +297,13 @@ def run_gpu(args):
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    replay_stream = torch.cuda.current_stream()     # graph.replay() launches here
     with ClockSampler(local) as clk:
         dist_barrier(world, device)
         torch.cuda.synchronize()
-        t0.record(stream)
+        t0.record(replay_stream)
         graph.replay()
-        t1.record(stream)
+        t1.record(replay_stream)
         torch.cuda.synchronize()
         dist_barrier(world, device)
     ms_total = t0.elapsed_time(t1)
