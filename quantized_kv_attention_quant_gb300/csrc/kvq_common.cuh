@@ -325,6 +325,10 @@ __device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
                       *reinterpret_cast<__half2*>(&c));
   return *reinterpret_cast<uint32_t*>(&r);
 }
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 constexpr uint32_t kMagic = 0x64006400u;        // (1024, 1024)
 constexpr uint32_t kSixteenth = 0x2C002C00u;    // (1/16, 1/16)
 constexpr uint32_t kNeg64 = 0xD400D400u;        // (-64, -64)

@@ -48,8 +48,9 @@ __host__ __device__ constexpr int row_stride(int D, int bits) { return D * bits 
 __host__ __device__ constexpr int sb_bytes(int D) { return 64 * (D / 64) * 2; }
 __host__ __device__ constexpr int stage_bytes(int D, int bits) { return 2 * 64 * row_stride(D, bits) + 4 * sb_bytes(D); }
 __host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
-// control block: 16 mbarriers, max-exchange [2][NW][16], l-exchange [NW][16], qsum [16][NG]
-__host__ __device__ constexpr int ctrl_bytes(int D) { return align128(128 + (3 * (D / 64) * 16 + 16 * (D / 64)) * 4); }
+// control block: mbarriers, max-exchange [2][NW][16], l-exchange [NW][16] (floats),
+// V scale/bias f16 pairs [2][2][NG][32] (words)
+__host__ __device__ constexpr int ctrl_bytes(int D) { return align128(128 + (3 * (D / 64) * 16) * 4 + 2 * 2 * (D / 64) * 32 * 4); }
 __host__ __device__ constexpr int stage0_off(int D) { return ctrl_bytes(D) + 2 * 16 * 64 * 2; }
 
 __device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -106,6 +107,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   __shared__ uint16_t q16[kMaxG][D];
   __shared__ uint16_t qn[kMaxG][D];
   __shared__ float4 cs[D / 2];
+  __shared__ float qs[kMaxG][8];         // per-group sums of the f16 q values
   pdl_launch();
   const int row = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,7 +123,6 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   }
   // blockDim is 32 * G: warp w preps q head kvh * G + w
   const int hq = kvh * G + warp;
-  float* qsum = a.ws.qsum + ((size_t)row * a.L.n_kv + kvh) * 16 * NG;
   const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + lane * E;
   float x[E];
 #pragma unroll
@@ -151,10 +152,13 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   }
   float gs = 0.f;
 #pragma unroll
-  for (int i = 0; i < E; ++i) { q16[warp][lane * E + i] = y[i]; gs += bf16_to_f(y[i]); }
+  for (int i = 0; i < E; ++i) {
+    q16[warp][lane * E + i] = y[i];
+    gs += __half2float(__float2half_rn(bf16_to_f(y[i])));   // the f16 value the MMA multiplies
+  }
 #pragma unroll
   for (int m = 1; m < LPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
-  if (lane % LPG == 0) qsum[warp * NG + lane / LPG] = gs;
+  if (lane % LPG == 0) qs[warp][lane / LPG] = gs;
   if (a.q_prepped) {
     uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + lane * E;
 #pragma unroll
@@ -162,8 +166,25 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   }
   // zero rows G..15
   for (int i = threadIdx.x; i < (kMaxG - G) * D; i += blockDim.x) q16[G + i / D][i % D] = 0;
-  for (int i = threadIdx.x; i < (kMaxG - G) * NG; i += blockDim.x) qsum[G * NG + i] = 0.f;
+  for (int i = threadIdx.x; i < kMaxG * 8; i += blockDim.x) {
+    const int r = i / 8, g = i % 8;
+    if (r >= G || g >= NG) qs[r][g] = 0.f;
+  }
   __syncthreads();
+  // bias-term A fragment: rows = q heads, k = group (hi part) | 8 + group (lo part)
+  if (threadIdx.x < 128) {
+    const int ln = threadIdx.x >> 2, reg = threadIdx.x & 3;
+    const int t4 = ln & 3, r = (ln >> 2) + ((reg & 1) ? 8 : 0);
+    const bool lo_part = reg & 2;
+    float v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float x = qs[r][2 * t4 + e];
+      const float hi = __half2float(__float2half_rn(x));
+      v[e] = lo_part ? x - hi : hi;
+    }
+    reinterpret_cast<uint32_t*>(a.ws.qbias)[((size_t)row * a.L.n_kv + kvh) * 128 + ln * 4 + reg] = pack_h2(v[0], v[1]);
+  }
   // A fragments: [NG][4 ks][32 lanes] x 4 registers
   uint32_t* frag = reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
   for (int idx = threadIdx.x; idx < NG * 4 * 32 * 4; idx += blockDim.x) {
@@ -185,6 +206,30 @@ struct TileRange {
   int t_begin, n_my, lo, hi;
 };
 
+// Load NG consecutive bf16 values (16 B for NG = 8) as raw words.
+template <int NG>
+__device__ __forceinline__ void load_bf16_row(const uint16_t* p, uint32_t (&w)[(NG + 1) / 2]) {
+  if constexpr (NG == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (NG == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x; w[1] = v.y;
+  } else if constexpr (NG == 2) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else {
+    w[0] = *p;
+  }
+}
+template <int NG>
+__device__ __forceinline__ float bf16_word_at(const uint32_t (&w)[(NG + 1) / 2], int g) {
+  return (g & 1) ? bf16hi_to_f(w[g >> 1]) : bf16lo_to_f(w[g >> 1]);
+}
+
+// log2 of the power of two the PV A operand (P * scale) is multiplied by, so
+// that it stays clear of the f16 subnormal range; divided out at the end.
+template <int BITS> struct PvPrescale { static constexpr int log2 = BITS == 4 ? 2 : 6; };
+
 template <int D, int BITS>
 __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
                                             const int nst, const TileRange tr, const int row, const int kvh,
@@ -194,11 +239,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   constexpr int RB = row_bytes(D, BITS), RS = row_stride(D, BITS), SB = sb_bytes(D);
   constexpr int STB = stage_bytes(D, BITS);
   constexpr float L2E = 1.4426950408889634f;
+  constexpr float PRESCALE = float(1 << PvPrescale<BITS>::log2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t4 = lane & 3, rq = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 128);        // [2][NW][16]
+  float* red = reinterpret_cast<float*>(smem + 128);        // [2][NW][16] tile max exchange
   float* lred = red + 2 * NW * 16;                          // [NW][16]
-  float* qs_sm = lred + NW * 16;                            // [16][NG]
+  uint32_t* vsb = reinterpret_cast<uint32_t*>(lred + NW * 16);  // [2][2][NG][32] f16 pairs of V scale/bias
   uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
   uint8_t* stages = smem + stage0_off(D);
   const int cap = c.capacity;
@@ -229,12 +276,14 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   for (int it = 0; it < min(nst, tr.n_my); ++it) issue(it);
   int issued = min(nst, tr.n_my);
 
-  // ------------------------------ consumers ------------------------------
-  const int t4 = lane & 3, rq = lane >> 2;
   pdl_wait();                                   // q fragments come from qprep_kernel
+  // QK A fragments (q heads x permuted head_dim) and the bias-term A fragment
+  // (per-group q sums as f16 hi | lo parts)
   uint32_t qa[NG][4][4];
+  uint32_t qb[4];
   {
-    const uint4* src = a.ws.qfrag + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32;
+    const size_t rk = (size_t)row * a.L.n_kv + kvh;
+    const uint4* src = a.ws.qfrag + rk * NG * 4 * 32;
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
@@ -242,14 +291,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const uint4 v = src[(g * 4 + ks) * 32 + lane];
         qa[g][ks][0] = v.x; qa[g][ks][1] = v.y; qa[g][ks][2] = v.z; qa[g][ks][3] = v.w;
       }
-    const float* qsg = a.ws.qsum + ((size_t)row * a.L.n_kv + kvh) * 16 * NG;
-    for (int i = threadIdx.x; i < 16 * NG; i += NW * 32) qs_sm[i] = qsg[i];
+    const uint4 v = a.ws.qbias[rk * 32 + lane];
+    qb[0] = v.x; qb[1] = v.y; qb[2] = v.z; qb[3] = v.w;
   }
-  named_bar(1, NW * 32);
 
-  float oacc[8][4];
+  float oacc[8][4];      // PV accumulator of this warp's group: 16 rows x 64 dims (permuted)
+  float cb[4];           // sum_j P_j * bias_j of this warp's group (column 0 is used)
 #pragma unroll
   for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  cb[0] = cb[1] = cb[2] = cb[3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   bool dead = false;
   const int g_pv = warp;                        // PV group of this warp
@@ -268,14 +318,48 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     const uint16_t* svb = svs + 64 * NG;
     const int tpos0 = (tr.t_begin + it) * kTileKeys;
 
-    // ---- QK ----
+    // ---- V scale/bias of this tile as f16 pairs (scale pre-multiplied by
+    // PRESCALE), zero for keys outside the window ----
+    {
+      uint32_t* vs16 = vsb + buf * 2 * NG * 32;
+      uint32_t* vb16 = vs16 + NG * 32;
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int idx = threadIdx.x + rep * NW * 32;          // NG * 64 entries = 2 per thread
+        const int which = idx / (NG * 32);                    // 0: scale, 1: bias
+        const int rem = idx % (NG * 32);
+        const int g = rem / 32, pr = rem % 32;
+        const int k0 = 2 * pr;
+        const bool v0 = tpos0 + k0 >= tr.lo && tpos0 + k0 <= tr.hi;
+        const bool v1 = tpos0 + k0 + 1 >= tr.lo && tpos0 + k0 + 1 <= tr.hi;
+        const uint16_t* srcp = which == 0 ? svs : svb;
+        const float mul = which == 0 ? PRESCALE : 1.f;
+        const float x0 = v0 ? bf16_to_f(srcp[k0 * NG + g]) * mul : 0.f;
+        const float x1 = v1 ? bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul : 0.f;
+        (which == 0 ? vs16 : vb16)[g * 32 + pr] = pack_h2(x0, x1);
+      }
+    }
+
+    // ---- QK: this warp's KPW keys, all q heads, full head_dim ----
     float S[NTQ][4];
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
       const int kb8 = warp * KPW + nt * 8;
       const int kB = kb8 + rq, kC = kb8 + 2 * t4;
-      S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+      // bias term: sum_g qsum[h][g] * bias[key][g] as one MMA (k = group for
+      // the hi part, 8 + group for the lo part)
+      {
+        uint32_t bb = 0;
+        if (2 * t4 < NG) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(skb + kB * NG + 2 * t4);
+          bb = pack_h2(bf16lo_to_f(w), 2 * t4 + 1 < NG ? bf16hi_to_f(w) : 0.f);
+        }
+        mma_f16_zc(S[nt], qb, bb, bb);
+      }
+      uint32_t sw0[(NG + 1) / 2], sw1[(NG + 1) / 2];
+      load_bf16_row<NG>(sks + kC * NG, sw0);
+      load_bf16_row<NG>(sks + (kC + 1) * NG, sw1);
       const uint8_t* krow = Ks + kB * RS + t4 * (BITS * 2);
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
@@ -293,13 +377,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
           mma_f16(acc, qa[g][2], byte_lo(w.z), byte_lo(w.z >> 8));
           mma_f16(acc, qa[g][3], byte_lo(w.w), byte_lo(w.w >> 8));
         }
-        const float s0 = bf16_to_f(sks[kC * NG + g]), s1 = bf16_to_f(sks[(kC + 1) * NG + g]);
-        const float b0 = bf16_to_f(skb[kC * NG + g]), b1 = bf16_to_f(skb[(kC + 1) * NG + g]);
-        const float qr = qs_sm[rq * NG + g], qr8 = qs_sm[(rq + 8) * NG + g];
-        S[nt][0] = fmaf(s0, acc[0], fmaf(b0, qr, S[nt][0]));
-        S[nt][1] = fmaf(s1, acc[1], fmaf(b1, qr, S[nt][1]));
-        S[nt][2] = fmaf(s0, acc[2], fmaf(b0, qr8, S[nt][2]));
-        S[nt][3] = fmaf(s1, acc[3], fmaf(b1, qr8, S[nt][3]));
+        const float s0 = bf16_word_at<NG>(sw0, g), s1 = bf16_word_at<NG>(sw1, g);
+        S[nt][0] = fmaf(s0, acc[0], S[nt][0]);
+        S[nt][1] = fmaf(s1, acc[1], S[nt][1]);
+        S[nt][2] = fmaf(s0, acc[2], S[nt][2]);
+        S[nt][3] = fmaf(s1, acc[3], S[nt][3]);
       }
       const int kp = tpos0 + kC;
       const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 1 >= tr.lo && kp + 1 <= tr.hi;
@@ -347,68 +429,70 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const __half2 ph = __floats2half2_rn(p0, p1);
         const float2 pf = __half22float2(ph);
         lsum[h] += pf.x + pf.y;
-        const int row = rq + 8 * h;
-        const int chunk = (kC >> 3) ^ (row & 7);
-        *reinterpret_cast<__half2*>(Pb + row * 128 + chunk * 16 + (kC & 7) * 2) = ph;
+        const int prow = rq + 8 * h;
+        const int chunk = (kC >> 3) ^ (prow & 7);
+        *reinterpret_cast<__half2*>(Pb + prow * 128 + chunk * 16 + (kC & 7) * 2) = ph;
       }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) { l_run[h] = l_run[h] * alpha[h] + lsum[h]; m_run[h] = m_new[h]; }
     named_bar(1, NW * 32);
 
-    // ---- PV for this warp's 64-dim group ----
+    // ---- PV for this warp's 64-dim group: O += (P * scale) codes + P bias ----
+    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
-      oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
+      for (int nt = 0; nt < 8; ++nt) {
+        oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
+        oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
+      }
+      cb[0] *= alpha[0]; cb[1] *= alpha[0]; cb[2] *= alpha[1]; cb[3] *= alpha[1];
     }
+    const uint32_t* vs16 = vsb + buf * 2 * NG * 32 + g_pv * 32;
+    const uint32_t* vb16 = vs16 + NG * 32;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
       {
         const int mtx = lane >> 3, i = lane & 7;
-        const int row = (mtx & 1) * 8 + i;
-        const int chunk = (kk * 2 + (mtx >> 1)) ^ (row & 7);
-        ldmatrix_x4(pa, Pb + row * 128 + chunk * 16);
+        const int prow = (mtx & 1) * 8 + i;
+        const int chunk = (kk * 2 + (mtx >> 1)) ^ (prow & 7);
+        ldmatrix_x4(pa, Pb + prow * 128 + chunk * 16);
       }
       const int ka = kk * 16 + 2 * t4;           // keys ka, ka+1, ka+8, ka+9
-      const uint32_t sAB = bf16_pair_to_h2(svs[ka * NG + g_pv], svs[(ka + 1) * NG + g_pv]);
-      const uint32_t sCD = bf16_pair_to_h2(svs[(ka + 8) * NG + g_pv], svs[(ka + 9) * NG + g_pv]);
-      const uint32_t bAB = bf16_pair_to_h2(svb[ka * NG + g_pv], svb[(ka + 1) * NG + g_pv]);
-      const uint32_t bCD = bf16_pair_to_h2(svb[(ka + 8) * NG + g_pv], svb[(ka + 9) * NG + g_pv]);
+      const uint32_t sAB = vs16[kk * 8 + t4], sCD = vs16[kk * 8 + 4 + t4];
+      // bias column: only B column 0 (lanes 0..3) is non-zero
+      const uint32_t bAB = rq == 0 ? vb16[kk * 8 + t4] : 0u, bCD = rq == 0 ? vb16[kk * 8 + 4 + t4] : 0u;
+      mma_f16(cb, pa, bAB, bCD);
+      const uint32_t ps[4] = {h2_mul(pa[0], sAB), h2_mul(pa[1], sAB), h2_mul(pa[2], sCD), h2_mul(pa[3], sCD)};
       if constexpr (BITS == 4) {
-        const uint8_t* vb = Vs + g_pv * 32 + rq * 4;
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vb + ka * RS);
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vb + (ka + 1) * RS);
-        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vb + (ka + 8) * RS);
-        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vb + (ka + 9) * RS);
+        const uint8_t* vrow = Vs + g_pv * 32 + rq * 4;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vrow + ka * RS);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vrow + (ka + 1) * RS);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vrow + (ka + 8) * RS);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vrow + (ka + 9) * RS);
         const uint32_t xab = prmt(wa, wb, 0x5410), yab = prmt(wa, wb, 0x7632);
         const uint32_t xcd = prmt(wc, wd, 0x5410), ycd = prmt(wc, wd, 0x7632);
         const uint32_t src_ab[4] = {xab, xab >> 8, yab, yab >> 8};
         const uint32_t src_cd[4] = {xcd, xcd >> 8, ycd, ycd >> 8};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t lo_ab = h2_fma(nib_lo(src_ab[q]), sAB, bAB), lo_cd = h2_fma(nib_lo(src_cd[q]), sCD, bCD);
-          const uint32_t hi_ab = h2_fma(nib_hi(src_ab[q]), sAB, bAB), hi_cd = h2_fma(nib_hi(src_cd[q]), sCD, bCD);
-          mma_f16(oacc[2 * q], pa, lo_ab, lo_cd);
-          mma_f16(oacc[2 * q + 1], pa, hi_ab, hi_cd);
+          mma_f16(oacc[2 * q], ps, nib_lo(src_ab[q]), nib_lo(src_cd[q]));
+          mma_f16(oacc[2 * q + 1], ps, nib_hi(src_ab[q]), nib_hi(src_cd[q]));
         }
       } else {
-        const uint8_t* vb = Vs + g_pv * 64 + rq * 8;
-        const uint2 wa = *reinterpret_cast<const uint2*>(vb + ka * RS);
-        const uint2 wb = *reinterpret_cast<const uint2*>(vb + (ka + 1) * RS);
-        const uint2 wc = *reinterpret_cast<const uint2*>(vb + (ka + 8) * RS);
-        const uint2 wd = *reinterpret_cast<const uint2*>(vb + (ka + 9) * RS);
+        const uint8_t* vrow = Vs + g_pv * 64 + rq * 8;
+        const uint2 wa = *reinterpret_cast<const uint2*>(vrow + ka * RS);
+        const uint2 wb = *reinterpret_cast<const uint2*>(vrow + (ka + 1) * RS);
+        const uint2 wc = *reinterpret_cast<const uint2*>(vrow + (ka + 8) * RS);
+        const uint2 wd = *reinterpret_cast<const uint2*>(vrow + (ka + 9) * RS);
         const uint32_t src_ab[4] = {prmt(wa.x, wb.x, 0x5410), prmt(wa.x, wb.x, 0x7632),
                                     prmt(wa.y, wb.y, 0x5410), prmt(wa.y, wb.y, 0x7632)};
         const uint32_t src_cd[4] = {prmt(wc.x, wd.x, 0x5410), prmt(wc.x, wd.x, 0x7632),
                                     prmt(wc.y, wd.y, 0x5410), prmt(wc.y, wd.y, 0x7632)};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t e_ab = h2_fma(byte_lo(src_ab[q]), sAB, bAB), e_cd = h2_fma(byte_lo(src_cd[q]), sCD, bCD);
-          const uint32_t o_ab = h2_fma(byte_lo(src_ab[q] >> 8), sAB, bAB), o_cd = h2_fma(byte_lo(src_cd[q] >> 8), sCD, bCD);
-          mma_f16(oacc[2 * q], pa, e_ab, e_cd);
-          mma_f16(oacc[2 * q + 1], pa, o_ab, o_cd);
+          mma_f16(oacc[2 * q], ps, byte_lo(src_ab[q]), byte_lo(src_cd[q]));
+          mma_f16(oacc[2 * q + 1], ps, byte_lo(src_ab[q] >> 8), byte_lo(src_cd[q] >> 8));
         }
       }
     }
@@ -425,13 +509,16 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
   if (t4 == 0) { lred[warp * 16 + rq] = l_run[0]; lred[warp * 16 + rq + 8] = l_run[1]; }
+  // bias column 0 lives in lanes with t4 == 0 (c0: row rq, c2: row rq + 8)
+  const float bias_r = __shfl_sync(0xffffffffu, cb[0], lane & ~3);
+  const float bias_r8 = __shfl_sync(0xffffffffu, cb[2], lane & ~3);
   named_bar(1, NW * 32);
   const int G = a.L.G;
   const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
   float* po = a.ws.part_o + pidx * 16 * D;
   float* ml = a.ws.part_ml + pidx * 32;
   if (warp == 0) {
-    // every consumer warp holds the same running max; warp 0 writes it
+    // every warp holds the same running max; warp 0 writes it
     if (t4 == 0) { ml[rq] = m_run[0]; ml[rq + 8] = m_run[1]; }
     if (lane < 16) {
       float l = 0.f;
@@ -439,11 +526,18 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       ml[16 + lane] = l;
     }
   }
+  constexpr float UNSCALE = 1.f / PRESCALE;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int d0 = g_pv * 64 + 8 * (2 * t4) + nt, d1 = d0 + 8;
-    if (rq < G) { po[rq * D + d0] = oacc[nt][0]; po[rq * D + d1] = oacc[nt][1]; }
-    if (rq + 8 < G) { po[(rq + 8) * D + d0] = oacc[nt][2]; po[(rq + 8) * D + d1] = oacc[nt][3]; }
+    if (rq < G) {
+      po[rq * D + d0] = fmaf(oacc[nt][0], UNSCALE, bias_r);
+      po[rq * D + d1] = fmaf(oacc[nt][1], UNSCALE, bias_r);
+    }
+    if (rq + 8 < G) {
+      po[(rq + 8) * D + d0] = fmaf(oacc[nt][2], UNSCALE, bias_r8);
+      po[(rq + 8) * D + d1] = fmaf(oacc[nt][3], UNSCALE, bias_r8);
+    }
   }
 }
 
@@ -575,7 +669,7 @@ size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits) {
   const size_t NG = D / 64, B = (size_t)n_rows * n_kv;
   size_t off = 256;
   off += B * NG * 4 * 32 * 16;                 // qfrag
-  off += B * 16 * NG * 4;                      // qsum
+  off += B * 32 * 16;                          // qbias
   off = (off + 255) & ~size_t(255);
   off += B * splits * 16 * (size_t)D * 4;      // part_o
   off += B * splits * 32 * 4;                  // part_ml
@@ -590,8 +684,8 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
   size_t off = 256;
   w.qfrag = reinterpret_cast<uint4*>(p + off);
   off += B * NG * 4 * 32 * 16;
-  w.qsum = reinterpret_cast<float*>(p + off);
-  off += B * 16 * NG * 4;
+  w.qbias = reinterpret_cast<uint4*>(p + off);
+  off += B * 32 * 16;
   off = (off + 255) & ~size_t(255);
   w.part_o = reinterpret_cast<float*>(p + off);
   off += B * splits * 16 * (size_t)D * 4;
