@@ -351,9 +351,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       // the hi part, 8 + group for the lo part)
       {
         uint32_t bb = 0;
-        if (2 * t4 < NG) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(skb + kB * NG + 2 * t4);
-          bb = pack_h2(bf16lo_to_f(w), 2 * t4 + 1 < NG ? bf16hi_to_f(w) : 0.f);
+        if constexpr (NG == 1) {       // one group: a single bf16 (2-byte aligned only)
+          if (t4 == 0) bb = pack_h2(bf16_to_f(skb[kB]), 0.f);
+        } else {
+          if (2 * t4 < NG) {           // an aligned pair of groups 2*t4, 2*t4+1
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(skb + kB * NG + 2 * t4);
+            bb = pack_h2(bf16lo_to_f(w), bf16hi_to_f(w));
+          }
         }
         mma_f16_zc(S[nt], qb, bb, bb);
       }
