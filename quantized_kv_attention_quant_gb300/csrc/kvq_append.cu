@@ -105,7 +105,6 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 append_kernel(const AppendArgs a, const RopeFreqs freqs) {
   constexpr int E = D / 32;              // elements per lane
-  constexpr int LPG = 64 / E;            // lanes per quantization group
   __shared__ AppendSmem<D> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = a.L.n_kv;
