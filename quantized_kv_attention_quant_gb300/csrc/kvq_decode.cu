@@ -535,6 +535,10 @@ decode_kernel(const DecodeArgs a, const RopeFreqs freqs, const int smem_total) {
       a.ws.part_ml[pidx * 32 + 16 + threadIdx.x] = 0.f;
     }
     pdl_launch();
+    // q_prepped covers every row, also one whose attention is NaN
+    if (split == 0 && a.q_prepped != nullptr)
+      prep_q_block<D>(a, freqs, row, kvh, p, smem + ctrl_bytes(D),
+                      reinterpret_cast<float*>(smem + off_qsum()), true);
     return;
   }
   const int bits = c.bits;
