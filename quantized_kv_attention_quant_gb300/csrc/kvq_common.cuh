@@ -107,15 +107,23 @@ __device__ __forceinline__ ff ff_warp_sum(ff v) {
   for (int m = 16; m >= 1; m >>= 1) v = ff_add(v, ff_shfl_xor(v, m));
   return v;
 }
-// 1 / sqrt(ss / D + eps) as a float-float, from the float-float sum of
-// squares.  One fp64 square root and division per row (IEEE, correctly
-// rounded), then split into a float pair.
+// 1 / sqrt(ss / D + eps) as a float-float (~2^-45 relative), in fp32 only
+// (fp64 sqrt + divide cost ~1500 cycles of latency on this part):
+//   r = ss/D + eps (float-float; /D is exact for a power of two);
+//   y0 = 1/sqrt(r.hi), IEEE-rounded sqrt and division (|rel. error| <= 2^-23);
+//   one Newton step y = y0 + y0 (1 - r y0^2) / 2 with r y0^2 formed exactly
+//   (two_prod; 1 - p.hi is exact by Sterbenz since p.hi ~ 1); the step's
+//   error is 1.5 (2^-23)^2 ~ 2^-45.
 __device__ __forceinline__ ff rms_inv(ff ss, int D, float eps) {
-  double r = ((double)ss.hi + (double)ss.lo) / (double)D + (double)eps;
-  double inv = 1.0 / sqrt(r);
-  float hi = (float)inv;
-  float lo = (float)(inv - (double)hi);
-  return {hi, lo};
+  const float invD = 1.0f / (float)D;                    // D is a power of two
+  ff r = two_sum(__fmul_rn(ss.hi, invD), eps);
+  r = fast_two_sum(r.hi, __fadd_rn(r.lo, __fmul_rn(ss.lo, invD)));
+  const float y0 = __fdiv_rn(1.0f, __fsqrt_rn(r.hi));
+  const ff t = two_prod(y0, y0);                         // y0^2 exactly
+  const ff p = two_prod(r.hi, t.hi);                     // r.hi * t.hi exactly
+  const float small = __fmaf_rn(r.hi, t.lo, __fmul_rn(r.lo, t.hi));
+  const float e = __fsub_rn(__fsub_rn(__fsub_rn(1.0f, p.hi), p.lo), small);
+  return fast_two_sum(y0, __fmul_rn(__fmul_rn(y0, e), 0.5f));
 }
 // x * w * inv, correctly rounded to bf16; x and w are bf16 values so x*w is
 // exact in fp32.

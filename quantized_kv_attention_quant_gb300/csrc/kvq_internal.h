@@ -37,6 +37,8 @@ struct AppendArgs {
 // Workspace of the attention calls, carved from the caller's buffer.
 struct DecodeWs {
   uint32_t* status;     // 1 word (padded to 256 B)
+  uint4* qfrag;         // [n_rows][n_kv][NG][4][32] x uint4
+  uint4* qbias;         // [n_rows][n_kv][32] x uint4: A fragment of the QK bias term
   float* part_o;        // [n_rows][n_kv][splits][16][D]
   float* part_ml;       // [n_rows][n_kv][splits][2][16]  (m, l)
 };
