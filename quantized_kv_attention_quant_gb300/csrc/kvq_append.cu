@@ -20,6 +20,7 @@ template <int D>
 struct AppendSmem {
   float normed[kWarpsPerBlock][D];
   float4 cs[kWarpsPerBlock][D / 2];     // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
+  float freq[D / 2][3];                 // rotary frequency triples
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row) {
@@ -106,6 +107,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 append_kernel(const AppendArgs a, const RopeFreqs freqs) {
   constexpr int E = D / 32;              // elements per lane
   __shared__ AppendSmem<D> sm;
+  stage_freqs(freqs.f, a.L.rope_dims >> 1, sm.freq);
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = a.L.n_kv;
   const long item = (long)blockIdx.x * kWarpsPerBlock + warp;
@@ -170,7 +173,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
     for (int i = 0; i < E; ++i) sm.normed[warp][lane * E + i] = bf16_to_f(y[i]);
     for (int j = lane; j < half; j += 32) {
       ff cc, sn;
-      rope_cos_sin(pos, freqs.f[j][0], freqs.f[j][1], freqs.f[j][2], cc, sn);
+      rope_cos_sin(pos, sm.freq[j][0], sm.freq[j][1], sm.freq[j][2], cc, sn);
       sm.cs[warp][j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
     }
     __syncwarp();

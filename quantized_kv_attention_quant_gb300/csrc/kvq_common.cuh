@@ -207,6 +207,18 @@ __device__ __forceinline__ void rope_cos_sin(int p, float f1, float f2, float f3
   s = ff_add(ff_mul(ts, cr), ff_mul(tc, sr));
 }
 
+// Copy rope_dims/2 frequency triples from the kernel-parameter table into
+// shared memory.  Every read of the parameter block is warp-uniform (a lane
+// index into it would serialise on the constant cache); call from all threads
+// of the block, followed by a block barrier.
+__device__ __forceinline__ void stage_freqs(const float (*f)[3], int half, float (*dst)[3]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int j = warp; j < half; j += nw) {
+    const float a = f[j][0], b = f[j][1], c = f[j][2];
+    if (lane == 0) { dst[j][0] = a; dst[j][1] = b; dst[j][2] = c; }
+  }
+}
+
 // x*c - y*s, correctly rounded to bf16 (x, y bf16 values; c, s float-float).
 __device__ __forceinline__ uint16_t rot_bf16(float x, float y, ff c, ff s) {
   if (x == 0.f && y == 0.f)   // signed zero as IEEE arithmetic gives it

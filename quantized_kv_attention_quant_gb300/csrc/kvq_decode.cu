@@ -108,7 +108,10 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   __shared__ uint16_t qn[kMaxG][D];
   __shared__ float4 cs[D / 2];
   __shared__ float qs[kMaxG][8];         // per-group sums of the f16 q values
+  __shared__ float freq[D / 2][3];
   pdl_launch();
+  stage_freqs(freqs.f, a.L.rope_dims >> 1, freq);
+  __syncthreads();
   const int row = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
@@ -118,7 +121,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
   const int pc = min(max(p, 0), (1 << 24) - 1);
   for (int j = threadIdx.x; j < half; j += blockDim.x) {
     ff cc, sn;
-    rope_cos_sin(pc, freqs.f[j][0], freqs.f[j][1], freqs.f[j][2], cc, sn);
+    rope_cos_sin(pc, freq[j][0], freq[j][1], freq[j][2], cc, sn);
     cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
   }
   // blockDim is 32 * G: warp w preps q head kvh * G + w
