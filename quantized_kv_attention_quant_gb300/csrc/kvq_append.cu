@@ -3,10 +3,11 @@
 // offset, then cache.appendWindow(k, v); gemma4-e4b.ts Gemma4Layer.kv:
 // {bits, groupSize 64}).
 //
-// One warp handles one (row, kv head, K-or-V) item: 32 lanes x D/32
-// contiguous elements, loaded with 16-byte vector loads; a 64-element group
-// spans 64/(D/32) lanes and is reduced with shuffles.  Output words are
-// written coalesced at slot pos % capacity.
+// One block handles one (row, kv head, K-or-V) item with max(32, D/4)
+// threads of 4 (or 2) contiguous elements each, so the long float-float
+// chains of the prep are spread thin: a decode step appends only a handful of
+// rows, and its latency is the critical path of one block.  A 64-element
+// quantization group spans 16 threads and is reduced with shuffles.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 
@@ -14,13 +15,20 @@ namespace kvq {
 
 namespace {
 
-constexpr int kWarpsPerBlock = 4;
+template <int D>
+struct App {
+  static constexpr int THREADS = D / 4 >= 32 ? D / 4 : 32;
+  static constexpr int E = D / THREADS;            // elements per thread
+  static constexpr int NWARP = THREADS / 32;
+  static constexpr int TPG = 64 / E;               // threads per quantization group
+};
 
 template <int D>
 struct AppendSmem {
-  float normed[kWarpsPerBlock][D];
-  float4 cs[kWarpsPerBlock][D / 2];     // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
+  uint16_t normed[D];
+  float4 cs[D / 2];                     // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
   float freq[D / 2][3];                 // rotary frequency triples
+  ff red[App<D>::NWARP];
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row) {
@@ -34,13 +42,26 @@ __device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row)
 
 __device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Quantize this lane's E prepped values (one slice of a 64-group), pack the
+// rint(fl32(d / s)) for s > 0, bit-identical to the IEEE quotient rounded
+// half to even, without an IEEE division per element.  q1 = d * rcp(s)
+// (both correctly rounded) is within |d/s| * 2^-23 of d/s and fl32(d/s) within
+// |d/s| * 2^-24; for |d/s| <= 256 the two differ by < 5e-5, so their rints
+// agree unless q1 lies within 1e-4 of a half-integer, in which case the
+// quotient is formed exactly.
+__device__ __forceinline__ int quant_code(float d, float s, float rcp) {
+  const float q1 = __fmul_rn(d, rcp);
+  const float f = q1 - floorf(q1);
+  if (fabsf(f - 0.5f) > 1e-4f) return __float2int_rn(q1);
+  return __float2int_rn(__fdiv_rn(d, s));
+}
+
+// Quantize this thread's E prepped values (one slice of a 64-group), pack the
 // codes little-endian and store them, the group's scale and its bias.
 template <int D, int BITS>
-__device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], const kvq_seq_cache& c,
-                                               int kind, int head, int pos, int lane) {
-  constexpr int E = D / 32;
-  constexpr int LPG = 64 / E;
+__device__ __forceinline__ void quantize_store(const uint16_t (&y)[App<D>::E], const kvq_seq_cache& c,
+                                               int kind, int head, int pos, int t) {
+  constexpr int E = App<D>::E;
+  constexpr int TPG = App<D>::TPG;
   constexpr int NG = D / 64;
   constexpr int TOP = (1 << BITS) - 1;
   float v[E];
@@ -48,7 +69,7 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], cons
 #pragma unroll
   for (int i = 0; i < E; ++i) { v[i] = bf16_to_f(y[i]); mn = fminf(mn, v[i]); mx = fmaxf(mx, v[i]); }
 #pragma unroll
-  for (int m = 1; m < LPG; m <<= 1) {
+  for (int m = 1; m < TPG; m <<= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
   }
@@ -58,24 +79,22 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], cons
   // scale = bf16((max - min) / (2^bits - 1)), two IEEE fp32 roundings
   const uint16_t sb = f_to_bf16_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)TOP));
   const float sf = bf16_to_f(sb);
+  const float rcp = sf != 0.f ? __frcp_rn(sf) : 0.f;
   uint32_t code[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     int q = 0;
-    if (sf != 0.f) {
-      q = __float2int_rn(__fdiv_rn(__fsub_rn(v[i], mn), sf));   // half to even
-      q = min(max(q, 0), TOP);
-    }
+    if (sf != 0.f) q = min(max(quant_code(__fsub_rn(v[i], mn), sf, rcp), 0), TOP);
     code[i] = uint32_t(q);
   }
   const int slot = pos % c.capacity;
   const size_t rowi = (size_t)head * c.capacity + slot;
   uint32_t* codes = kind == 0 ? c.k_codes : c.v_codes;
   constexpr int WPR = D * BITS / 32;       // words per row
-  constexpr int LB = E * BITS;             // bits per lane
+  constexpr int LB = E * BITS;             // bits per thread
   if constexpr (LB >= 32) {
     constexpr int NW = LB / 32, PER = 32 / BITS;
-    uint32_t* dst = codes + rowi * WPR + lane * NW;
+    uint32_t* dst = codes + rowi * WPR + t * NW;
 #pragma unroll
     for (int wi = 0; wi < NW; ++wi) {
       uint32_t w = 0;
@@ -84,17 +103,17 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], cons
       dst[wi] = w;
     }
   } else {
-    constexpr int LPW = 32 / LB;           // lanes sharing one word
+    constexpr int TPW = 32 / LB;           // threads sharing one word
     uint32_t part = 0;
 #pragma unroll
     for (int i = 0; i < E; ++i) part |= code[i] << (i * BITS);
-    part <<= (lane % LPW) * LB;
+    part <<= (t % TPW) * LB;
 #pragma unroll
-    for (int m = 1; m < LPW; m <<= 1) part |= __shfl_xor_sync(0xffffffffu, part, m);
-    if (lane % LPW == 0) codes[rowi * WPR + lane / LPW] = part;
+    for (int m = 1; m < TPW; m <<= 1) part |= __shfl_xor_sync(0xffffffffu, part, m);
+    if (t % TPW == 0) codes[rowi * WPR + t / TPW] = part;
   }
-  if (lane % LPG == 0) {
-    const int g = lane / LPG;
+  if (t % TPG == 0) {
+    const int g = t / TPG;
     uint16_t* sc = kind == 0 ? c.k_scales : c.v_scales;
     uint16_t* bi = kind == 0 ? c.k_biases : c.v_biases;
     sc[rowi * NG + g] = sb;
@@ -103,19 +122,19 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[D / 32], cons
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(App<D>::THREADS)
 append_kernel(const AppendArgs a, const RopeFreqs freqs) {
-  constexpr int E = D / 32;              // elements per lane
+  using A = App<D>;
+  constexpr int E = A::E;
   __shared__ AppendSmem<D> sm;
-  stage_freqs(freqs.f, a.L.rope_dims >> 1, sm.freq);
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int R = a.L.rope_dims, half = R >> 1;
   const int Hkv = a.L.n_kv;
-  const long item = (long)blockIdx.x * kWarpsPerBlock + warp;
+  const long item = blockIdx.x;
   const int kind = int(item & 1);        // 0: K, 1: V
   const long rh = item >> 1;
-  if (rh >= (long)a.n_rows * Hkv) return;
   const int row = int(rh / Hkv), head = int(rh % Hkv);
+  if (kind == 0 && R > 0) stage_freqs(freqs.f, half, sm.freq);
 
   const int s = find_seq(a.row_offsets, a.n_seqs, row);
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
@@ -127,28 +146,20 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
                   aligned16(c.k_codes) && aligned16(c.v_codes) && aligned16(c.k_scales) &&
                   aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases) &&
                   pos >= 0 && pos < (1 << 24);
-  if (!ok) return;
+  if (!ok) return;                       // uniform over the block
   // a row whose slot a newer row of this call overwrites is prepped (for
   // kv_prepped) but not stored
   const bool store = t_in >= rows_s - c.capacity;
 
   // ---- load the raw row ----
   const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
-  src += ((size_t)row * Hkv + head) * D + lane * E;
+  src += ((size_t)row * Hkv + head) * D + t * E;
   float x[E];
-  if constexpr (E >= 8) {
-#pragma unroll
-    for (int v = 0; v < E / 8; ++v) {
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + v);
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { x[8 * v + 2 * i] = bf16lo_to_f(w[i]); x[8 * v + 2 * i + 1] = bf16hi_to_f(w[i]); }
-    }
-  } else if constexpr (E == 4) {
-    uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+  if constexpr (E == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
     x[0] = bf16lo_to_f(u.x); x[1] = bf16hi_to_f(u.x); x[2] = bf16lo_to_f(u.y); x[3] = bf16hi_to_f(u.y);
   } else {
-    uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+    const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
     x[0] = bf16lo_to_f(u); x[1] = bf16hi_to_f(u);
   }
 
@@ -157,52 +168,57 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
 #pragma unroll
   for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
   ss = ff_warp_sum(ss);
+  if constexpr (A::NWARP > 1) {
+    if (lane == 0) sm.red[warp] = ss;
+    __syncthreads();
+    ss = sm.red[0];
+#pragma unroll
+    for (int w = 1; w < A::NWARP; ++w) ss = ff_add(ss, sm.red[w]);
+  }
   const ff inv = rms_inv(ss, D, a.L.eps);
   uint16_t y[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + lane * E + i)) : 1.f;
+    const float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + t * E + i)) : 1.f;
     y[i] = norm_scale_bf16(x[i], w, inv);
   }
 
   // ---- RoPE on K ----
-  const int R = a.L.rope_dims;
   if (kind == 0 && R > 0) {
-    const int half = R >> 1;
 #pragma unroll
-    for (int i = 0; i < E; ++i) sm.normed[warp][lane * E + i] = bf16_to_f(y[i]);
-    for (int j = lane; j < half; j += 32) {
+    for (int i = 0; i < E; ++i) sm.normed[t * E + i] = y[i];
+    __syncthreads();                     // freq[] staged, normed[] complete
+    for (int j = t; j < half; j += A::THREADS) {
       ff cc, sn;
       rope_cos_sin(pos, sm.freq[j][0], sm.freq[j][1], sm.freq[j][2], cc, sn);
-      sm.cs[warp][j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+      sm.cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
     }
-    __syncwarp();
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-      const int e = lane * E + i;
+      const int e = t * E + i;
       if (e < R) {
         const int j = e < half ? e : e - half;
-        const float4 t = sm.cs[warp][j];
-        const ff cc = {t.x, t.y};
-        if (e < half) {      // x_j cos - x_{j+h} sin
-          y[i] = rot_bf16(sm.normed[warp][e], sm.normed[warp][e + half], cc, ff{t.z, t.w});
-        } else {             // x_{j+h} cos + x_j sin
-          y[i] = rot_bf16(sm.normed[warp][e], sm.normed[warp][j], cc, ff{-t.z, -t.w});
-        }
+        const float4 cv = sm.cs[j];
+        const ff cc = {cv.x, cv.y};
+        if (e < half)        // x_j cos - x_{j+h} sin
+          y[i] = rot_bf16(bf16_to_f(sm.normed[e]), bf16_to_f(sm.normed[e + half]), cc, ff{cv.z, cv.w});
+        else                 // x_{j+h} cos + x_j sin
+          y[i] = rot_bf16(bf16_to_f(sm.normed[e]), bf16_to_f(sm.normed[j]), cc, ff{-cv.z, -cv.w});
       }
     }
   }
 
   if (a.prepped) {
-    uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + lane * E;
+    uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + t * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) dst[i] = y[i];
   }
 
   // ---- quantize the 64-element group, pack, store ----
   if (!store) return;
-  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, lane);
-  else quantize_store<D, 8>(y, c, kind, head, pos, lane);
+  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, t);
+  else quantize_store<D, 8>(y, c, kind, head, pos, t);
 }
 
 }  // namespace
@@ -210,13 +226,13 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st) {
   const long items = (long)a.n_rows * a.L.n_kv * 2;
   if (items == 0) return cudaSuccess;
-  const dim3 grid((unsigned)((items + kWarpsPerBlock - 1) / kWarpsPerBlock));
-  const dim3 block(kWarpsPerBlock * 32);
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)items);
   switch (a.L.D) {
-    case 64: append_kernel<64><<<grid, block, 0, st>>>(a, f); break;
-    case 128: append_kernel<128><<<grid, block, 0, st>>>(a, f); break;
-    case 256: append_kernel<256><<<grid, block, 0, st>>>(a, f); break;
-    case 512: append_kernel<512><<<grid, block, 0, st>>>(a, f); break;
+    case 64: append_kernel<64><<<grid, App<64>::THREADS, 0, st>>>(a, f); break;
+    case 128: append_kernel<128><<<grid, App<128>::THREADS, 0, st>>>(a, f); break;
+    case 256: append_kernel<256><<<grid, App<256>::THREADS, 0, st>>>(a, f); break;
+    case 512: append_kernel<512><<<grid, App<512>::THREADS, 0, st>>>(a, f); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -98,107 +98,134 @@ __device__ __forceinline__ uint32_t bf16_pair_to_h2(uint16_t lo, uint16_t hi) {
 }
 
 // ----------------------------------------------------------------------------
-// 1. q prep
+// 1. q prep: one block per (row, kv head, q head slot h < 16), max(32, D/4)
+// threads of 4 (or 2) elements.  Writes q_hat (bf16), the head's words of the
+// QK A fragments and of the bias-term A fragment (rows >= G are zeros).
+// Each 32-bit fragment word holds two dims of ONE row, so blocks of different
+// heads write disjoint words.
 // ----------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(512)
+struct Qp {
+  static constexpr int THREADS = D / 4 >= 32 ? D / 4 : 32;
+  static constexpr int E = D / THREADS;
+  static constexpr int NWARP = THREADS / 32;
+  static constexpr int TPG = 64 / E;
+};
+
+template <int D>
+__global__ void __launch_bounds__(Qp<D>::THREADS)
 qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
-  constexpr int E = D / 32, NG = D / 64, LPG = 64 / E;
-  __shared__ uint16_t q16[kMaxG][D];
-  __shared__ uint16_t qn[kMaxG][D];
+  using Q = Qp<D>;
+  constexpr int E = Q::E, NG = D / 64;
+  __shared__ uint16_t qn[D];               // normed, then q_hat
   __shared__ float4 cs[D / 2];
-  __shared__ float qs[kMaxG][8];         // per-group sums of the f16 q values
   __shared__ float freq[D / 2][3];
+  __shared__ ff red[Q::NWARP];
+  __shared__ float qs[8];                  // per-group sums of the f16 q values
   pdl_launch();
-  stage_freqs(freqs.f, a.L.rope_dims >> 1, freq);
-  __syncthreads();
-  const int row = blockIdx.x, kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x, kvh = blockIdx.y, h = blockIdx.z;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
   const RowInfo ri = row_info(a, row);
-  const int p = ri.p;
   const int bits = a.seqs[ri.s].bits;
-  const int pc = min(max(p, 0), (1 << 24) - 1);
-  for (int j = threadIdx.x; j < half; j += blockDim.x) {
-    ff cc, sn;
-    rope_cos_sin(pc, freq[j][0], freq[j][1], freq[j][2], cc, sn);
-    cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+  uint32_t* frag = reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
+  uint32_t* qb = reinterpret_cast<uint32_t*>(a.ws.qbias) + ((size_t)row * a.L.n_kv + kvh) * 128;
+  // this row's fragment words: lanes with lane/4 == h % 8, register 0/2 (h < 8) or 1/3
+  const int rq = h & 7, reg_lo = h < 8 ? 0 : 1;
+  if (h >= G) {
+    for (int i = t; i < NG * 4 * 4 * 2; i += Q::THREADS) {
+      const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
+      frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] = 0u;
+    }
+    if (t < 8) qb[(rq * 4 + (t & 3)) * 4 + reg_lo + 2 * (t >> 2)] = 0u;
+    return;
   }
-  // blockDim is 32 * G: warp w preps q head kvh * G + w
-  const int hq = kvh * G + warp;
-  const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + lane * E;
+  if (R > 0) stage_freqs(freqs.f, half, freq);
+  const int hq = kvh * G + h;
+  const int pc = min(max(ri.p, 0), (1 << 24) - 1);
+  const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + t * E;
   float x[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) x[i] = bf16_to_f(src[i]);
+  if constexpr (E == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    x[0] = bf16lo_to_f(u.x); x[1] = bf16hi_to_f(u.x); x[2] = bf16lo_to_f(u.y); x[3] = bf16hi_to_f(u.y);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+    x[0] = bf16lo_to_f(u); x[1] = bf16hi_to_f(u);
+  }
   ff ss = {0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
   ss = ff_warp_sum(ss);
+  if constexpr (Q::NWARP > 1) {
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    ss = red[0];
+#pragma unroll
+    for (int w = 1; w < Q::NWARP; ++w) ss = ff_add(ss, red[w]);
+  }
   const ff inv = rms_inv(ss, D, a.L.eps);
   uint16_t y[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[lane * E + i]), inv);
-    qn[warp][lane * E + i] = y[i];
+    y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[t * E + i]), inv);
+    qn[t * E + i] = y[i];
   }
-  __syncthreads();                       // cs[] and qn[] complete
-#pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const int e = lane * E + i;
-    if (e < R) {
-      const int j = e < half ? e : e - half;
-      const float4 t = cs[j];
-      const ff cc = {t.x, t.y};
-      y[i] = e < half ? rot_bf16(bf16_to_f(qn[warp][e]), bf16_to_f(qn[warp][e + half]), cc, ff{t.z, t.w})
-                      : rot_bf16(bf16_to_f(qn[warp][e]), bf16_to_f(qn[warp][j]), cc, ff{-t.z, -t.w});
+  __syncthreads();                         // freq[] staged, qn[] complete
+  if (R > 0) {
+    for (int j = t; j < half; j += Q::THREADS) {
+      ff cc, sn;
+      rope_cos_sin(pc, freq[j][0], freq[j][1], freq[j][2], cc, sn);
+      cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
     }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int e = t * E + i;
+      if (e < R) {
+        const int j = e < half ? e : e - half;
+        const float4 cv = cs[j];
+        const ff cc = {cv.x, cv.y};
+        y[i] = e < half ? rot_bf16(bf16_to_f(qn[e]), bf16_to_f(qn[e + half]), cc, ff{cv.z, cv.w})
+                        : rot_bf16(bf16_to_f(qn[e]), bf16_to_f(qn[j]), cc, ff{-cv.z, -cv.w});
+      }
+    }
+    __syncthreads();                       // every read of the normed row is done
+#pragma unroll
+    for (int i = 0; i < E; ++i) qn[t * E + i] = y[i];
   }
   float gs = 0.f;
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    q16[warp][lane * E + i] = y[i];
-    gs += __half2float(__float2half_rn(bf16_to_f(y[i])));   // the f16 value the MMA multiplies
-  }
+  for (int i = 0; i < E; ++i) gs += __half2float(__float2half_rn(bf16_to_f(y[i])));   // the f16 value the MMA multiplies
 #pragma unroll
-  for (int m = 1; m < LPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
-  if (lane % LPG == 0) qs[warp][lane / LPG] = gs;
+  for (int m = 1; m < Q::TPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
+  if (t % Q::TPG == 0) qs[t / Q::TPG] = gs;
   if (a.q_prepped) {
-    uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + lane * E;
+    uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + t * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) dst[i] = y[i];
   }
-  // zero rows G..15
-  for (int i = threadIdx.x; i < (kMaxG - G) * D; i += blockDim.x) q16[G + i / D][i % D] = 0;
-  for (int i = threadIdx.x; i < kMaxG * 8; i += blockDim.x) {
-    const int r = i / 8, g = i % 8;
-    if (r >= G || g >= NG) qs[r][g] = 0.f;
-  }
-  __syncthreads();
-  // bias-term A fragment: rows = q heads, k = group (hi part) | 8 + group (lo part)
-  if (threadIdx.x < 128) {
-    const int ln = threadIdx.x >> 2, reg = threadIdx.x & 3;
-    const int t4 = ln & 3, r = (ln >> 2) + ((reg & 1) ? 8 : 0);
-    const bool lo_part = reg & 2;
-    float v[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float x = qs[r][2 * t4 + e];
-      const float hi = __half2float(__float2half_rn(x));
-      v[e] = lo_part ? x - hi : hi;
-    }
-    reinterpret_cast<uint32_t*>(a.ws.qbias)[((size_t)row * a.L.n_kv + kvh) * 128 + ln * 4 + reg] = pack_h2(v[0], v[1]);
-  }
-  // A fragments: [NG][4 ks][32 lanes] x 4 registers
-  uint32_t* frag = reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
-  for (int idx = threadIdx.x; idx < NG * 4 * 32 * 4; idx += blockDim.x) {
-    const int reg = idx & 3, ln = (idx >> 2) & 31, ks = (idx >> 7) & 3, g = idx >> 9;
-    const int t4 = ln & 3, r = (ln >> 2) + ((reg & 1) ? 8 : 0);
+  __syncthreads();                         // q_hat and the group sums complete
+  // QK A fragment words of row h: for each (group, k-step, t4) two words
+  for (int i = t; i < NG * 4 * 4 * 2; i += Q::THREADS) {
+    const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
     int d[4];
     qk_dims(bits, ks, d);
     const int base = g * 64 + 16 * t4;
-    const int d0 = base + ((reg & 2) ? d[2] : d[0]);
-    const int d1 = base + ((reg & 2) ? d[3] : d[1]);
-    frag[idx] = bf16_pair_to_h2(q16[r][d0], q16[r][d1]);
+    const int d0 = base + (pair ? d[2] : d[0]), d1 = base + (pair ? d[3] : d[1]);
+    frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] = bf16_pair_to_h2(qn[d0], qn[d1]);
+  }
+  // bias-term A fragment words of row h: k = group (hi part) | 8 + group (lo part)
+  if (t < 8) {
+    const int t4 = t & 3, lo_part = t >> 2;
+    float v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int g = 2 * t4 + e;
+      const float xs = g < NG ? qs[g] : 0.f;
+      const float hi = __half2float(__float2half_rn(xs));
+      v[e] = lo_part ? xs - hi : hi;
+    }
+    qb[(rq * 4 + t4) * 4 + reg_lo + 2 * lo_part] = pack_h2(v[0], v[1]);
   }
 }
 
@@ -593,7 +620,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
 // 3. merge split partials: out = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
 // ----------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(D)
 combine_kernel(const DecodeArgs a) {
   __shared__ float wsm[256];
   __shared__ float inv_l;
@@ -625,25 +652,24 @@ combine_kernel(const DecodeArgs a) {
     if (threadIdx.x == 0) inv_l = nan ? __int_as_float(0x7fc00000) : 1.f / L;
   }
   __syncthreads();
-  const float il = inv_l;
-  const float* po = a.ws.part_o + (base * 16 + r) * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    int i = 0;
-    for (; i + 4 <= S; i += 4) {
-      const float o0 = po[(size_t)(i + 0) * 16 * D + d], o1 = po[(size_t)(i + 1) * 16 * D + d];
-      const float o2 = po[(size_t)(i + 2) * 16 * D + d], o3 = po[(size_t)(i + 3) * 16 * D + d];
-      acc = fmaf(wsm[i], o0, acc);
-      acc = fmaf(wsm[i + 1], o1, acc);
-      acc = fmaf(wsm[i + 2], o2, acc);
-      acc = fmaf(wsm[i + 3], o3, acc);
-    }
-    for (; i < S; ++i) acc = fmaf(wsm[i], po[(size_t)i * 16 * D + d], acc);
-    const float o = acc * il;
-    const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
-    if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
-    else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
+  const int d = threadIdx.x;               // one output dim per thread
+  const float* po = a.ws.part_o + (base * 16 + r) * D + d;
+  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+  int i = 0;
+  for (; i + 8 <= S; i += 8) {
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = po[(size_t)(i + k) * 16 * D];
+    acc0 = fmaf(wsm[i], o[0], acc0); acc1 = fmaf(wsm[i + 1], o[1], acc1);
+    acc2 = fmaf(wsm[i + 2], o[2], acc2); acc3 = fmaf(wsm[i + 3], o[3], acc3);
+    acc0 = fmaf(wsm[i + 4], o[4], acc0); acc1 = fmaf(wsm[i + 5], o[5], acc1);
+    acc2 = fmaf(wsm[i + 6], o[6], acc2); acc3 = fmaf(wsm[i + 7], o[7], acc3);
   }
+  for (; i < S; ++i) acc0 = fmaf(wsm[i], po[(size_t)i * 16 * D], acc0);
+  const float o = ((acc0 + acc1) + (acc2 + acc3)) * inv_l;
+  const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
+  if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
+  else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
 }
 
 template <int D>
@@ -667,7 +693,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  qprep_kernel<D><<<dim3(a.n_rows, a.L.n_kv), dim3(32 * a.L.G), 0, st>>>(a, f);
+  qprep_kernel<D><<<dim3(a.n_rows, a.L.n_kv, kMaxG), dim3(Qp<D>::THREADS), 0, st>>>(a, f);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   cudaLaunchAttribute attr[1];
@@ -684,7 +710,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   if (e != cudaSuccess) return e;
 
   cfg.gridDim = dim3(a.n_rows, a.L.n_q);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(D);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
   return e;
