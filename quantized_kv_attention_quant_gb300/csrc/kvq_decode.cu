@@ -656,16 +656,18 @@ combine_kernel(const DecodeArgs a) {
   const float* po = a.ws.part_o + (base * 16 + r) * D + d;
   float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
   int i = 0;
+  // a split with no keys wrote no o partial (its weight is 0): never touch it
   for (; i + 8 <= S; i += 8) {
     float o[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o[k] = po[(size_t)(i + k) * 16 * D];
+    for (int k = 0; k < 8; ++k) o[k] = wsm[i + k] != 0.f ? po[(size_t)(i + k) * 16 * D] : 0.f;
     acc0 = fmaf(wsm[i], o[0], acc0); acc1 = fmaf(wsm[i + 1], o[1], acc1);
     acc2 = fmaf(wsm[i + 2], o[2], acc2); acc3 = fmaf(wsm[i + 3], o[3], acc3);
     acc0 = fmaf(wsm[i + 4], o[4], acc0); acc1 = fmaf(wsm[i + 5], o[5], acc1);
     acc2 = fmaf(wsm[i + 6], o[6], acc2); acc3 = fmaf(wsm[i + 7], o[7], acc3);
   }
-  for (; i < S; ++i) acc0 = fmaf(wsm[i], po[(size_t)i * 16 * D], acc0);
+  for (; i < S; ++i)
+    if (wsm[i] != 0.f) acc0 = fmaf(wsm[i], po[(size_t)i * 16 * D], acc0);
   const float o = ((acc0 + acc1) + (acc2 + acc3)) * inv_l;
   const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
