@@ -206,3 +206,19 @@ def test_workload_full32k(kvq):
 
 def test_workload_prefill(kvq):
     check_prefill(kvq[1], W.workload_prefill_chunk(), seqs=[2], rows=[0, 1, 255, 511])
+
+
+def test_workspace_contents_do_not_matter(kvq):
+    """The workspace is scratch: NaN garbage left in it by earlier use must not
+    reach the output (splits that read no keys write no o partial)."""
+    _, harness = kvq
+    spec, filled, bits = DECODE_CASES["sliding-ring-wrap"]
+    wl = W.DecodeWorkload("ws-garbage", 83, spec, filled=filled, bits=bits)
+    case = harness.DecodeCase(wl)
+    case.step()
+    torch.cuda.synchronize()
+    ref = case.out.cpu().numpy().copy()
+    case.ws.fill_(0xFF)                      # NaN bit patterns everywhere
+    case.attend()
+    torch.cuda.synchronize()
+    assert np.array_equal(case.out.cpu().numpy(), ref)
