@@ -184,6 +184,36 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
                                     int32_t max_rows_per_seq);
 
+/*
+ * attn_decode_static -- attn_decode without a caller-provided workspace, for
+ * callers that cannot allocate device memory: code that only receives input
+ * and output pointers from a host framework that owns every allocation (a
+ * plugin or kernel-library slot with no allocator handle), or a serving loop
+ * that reserves all device memory up front and forbids allocation
+ * afterwards.  The pages have no counterpart of this call: it exists only
+ * because the workspace of attn_decode must otherwise come from the caller.
+ *
+ * Same arguments and results as attn_decode, minus workspace and
+ * workspace_bytes.  The scratch is a static device array of
+ * KVQ_STATIC_SCRATCH_BYTES bytes inside libkvq.so; every GPU that loads the
+ * library holds it until the process exits.  The call allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ *   - A call whose attn_decode_workspace_bytes(layer, n_seqs, max_pos) exceeds
+ *     KVQ_STATIC_SCRATCH_BYTES returns KVQ_EWORKSPACE and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind (the
+ *     status word at its start is cleared by each call).  Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads on
+ *     one device) race on it: serialise them.
+ */
+#define KVQ_STATIC_SCRATCH_BYTES (16u << 20)
+kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* pos, int32_t max_pos,
+                              const uint16_t* q_raw, const uint16_t* q_norm_w,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped, void* stream);
+
 /* Static message for a status code. */
 const char* kvq_status_string(kvq_status status);
 /* Message of the calling thread's most recent failing call ("" if none). */

@@ -52,6 +52,8 @@ def _load():
     lib.kv_quant_append.restype = ctypes.c_int
     lib.attn_decode.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
     lib.attn_decode.restype = ctypes.c_int
+    lib.attn_decode_static.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
+    lib.attn_decode_static.restype = ctypes.c_int
     lib.attn_decode_workspace_bytes.argtypes = [lay, i32, i32]
     lib.attn_decode_workspace_bytes.restype = sz
     lib.attn_prefill_chunk.argtypes = [lay, vp, i32, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, sz, vp]
@@ -74,6 +76,7 @@ def header_functions() -> list:
     """Names of the functions include/kvq.h declares."""
     text = open(HEADER_PATH).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(ln for ln in text.splitlines() if not ln.lstrip().startswith("#"))
     return sorted(set(re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{]*\)\s*;", text)) - {"if", "while"})
 
 
@@ -126,6 +129,18 @@ def attn_decode(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, ou
     _check(lib.attn_decode(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(pos), max_pos, _ptr(q_raw),
                            _ptr(q_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
                            _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def attn_decode_static(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, out, out_is_f32,
+                       q_prepped=None, stream=None):
+    """attn_decode with the library's static scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/kvq.h)."""
+    _check(lib.attn_decode_static(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(pos), max_pos, _ptr(q_raw),
+                                  _ptr(q_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
+                                  _stream(stream)))
+
+
+KVQ_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def attn_decode_workspace_bytes(layer: KvqLayer, n_seqs, max_pos) -> int:

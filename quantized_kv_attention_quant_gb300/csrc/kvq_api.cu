@@ -231,6 +231,72 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
   return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
 }
 
+// ---------------------------------------------------------------------------
+// attn_decode_static: attn_decode for callers that cannot allocate device
+// memory.  Its scratch is this file-scope array, which every GPU that loads
+// the library holds until the process exits.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+static __device__ __align__(256) uint8_t g_static_scratch[KVQ_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device.  Returns nullptr (and sets the error message) on failure.
+void* static_scratch_address(int* dev_out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "attn_decode_static: cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) {
+    fail(KVQ_EUNSUPPORTED, "attn_decode_static: device ordinal %d >= 64", dev);
+    return nullptr;
+  }
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cuda_fail(e, "attn_decode_static: cudaGetSymbolAddress");
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* pos, int32_t max_pos, const uint16_t* q_raw,
+                              const uint16_t* q_norm_w, void* out, int32_t out_is_f32, uint16_t* q_prepped,
+                              void* stream) {
+  if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
+  kvq::LayerArgs L;
+  kvq_status st = check_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if (n_seqs < 0) return fail(KVQ_EINVAL, "negative n_seqs");
+  const size_t need = attn_decode_workspace_bytes(layer, n_seqs, max_pos);
+  if (need > (size_t)KVQ_STATIC_SCRATCH_BYTES)
+    return fail(KVQ_EWORKSPACE,
+                "attn_decode_static: this call needs %zu bytes of scratch, more than the %zu-byte "
+                "static buffer; use attn_decode with a caller-provided workspace",
+                need, (size_t)KVQ_STATIC_SCRATCH_BYTES);
+  int dev = 0;
+  void* scratch = static_scratch_address(&dev);
+  if (!scratch) return KVQ_ECUDA;
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, q_raw, q_norm_w, out,
+                          out_is_f32, q_prepped, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
+}
+
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
     case KVQ_OK: return "ok";
