@@ -81,9 +81,11 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, workload: str):
+def traffic_for(kernel: str, workload: str, algorithmic_per_launch: float):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel sources."""
+    was taken on the current kernel sources.  An entry may instead give the
+    traffic/algorithmic ratio measured on a smaller case of the same kernel
+    (`scaled_from`), applied to this workload's algorithmic bytes."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -93,7 +95,11 @@ def traffic_for(kernel: str, workload: str):
     e = t.get(kernel, {}).get(workload)
     if not e or e.get("source_hash") != source_hash():
         return None
-    return float(e["dram_bytes_per_launch"])
+    if e.get("dram_bytes_per_launch") is not None:
+        return float(e["dram_bytes_per_launch"])
+    if e.get("traffic_over_algorithmic") is not None:
+        return float(e["traffic_over_algorithmic"]) * algorithmic_per_launch
+    return None
 
 
 # ----------------------------------------------------------------------------
@@ -335,7 +341,7 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic_for("decode_kernel_512" if "512" in info["dominant"] else info["dominant"],
-                                       args.workload),
+                                       args.workload, info["dominant_bytes"] / max(1, len(full_calls))),
                 "peak_source": peaks["source"], "kernel": info["dominant"],
                 "launch_ms": dom_ms / max(1, len(full_calls))}
     step_gbs = info["kv_bytes"] / (ms_step / 1e3) / 1e9 if info["kv_bytes"] else None

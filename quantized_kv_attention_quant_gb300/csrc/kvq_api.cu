@@ -109,6 +109,7 @@ kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
 
 kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
                             const int32_t* row_offsets, const int32_t* pos, int32_t n_rows, int32_t max_keys,
+                            bool fixed_chunks,
                             const uint16_t* q_raw, const uint16_t* q_norm_w, void* out, int32_t out_is_f32,
                             uint16_t* q_prepped, void* workspace, size_t workspace_bytes, void* stream) {
   kvq::LayerArgs L;
@@ -127,7 +128,8 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   if (row_offsets) REQUIRE_PTR(row_offsets, "row_offsets", 4);
   if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
   if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
-  const int splits = kvq::decode_pick_splits(L, n_rows, max_keys, num_sms_current());
+  const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
+  const int splits = plan.splits;
   const size_t need = kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
   if (workspace_bytes < need)
     return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
@@ -144,6 +146,7 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   a.out_f32 = out_is_f32;
   a.q_prepped = q_prepped;
   a.splits = splits;
+  a.chunk_tiles = plan.chunk_tiles;
   a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, splits);
   const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
   cudaError_t e = kvq::launch_decode(a, f, num_sms_current(), static_cast<cudaStream_t>(stream));
@@ -198,15 +201,15 @@ kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_
                        void* out, int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
                        size_t workspace_bytes, void* stream) {
   if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
-  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, q_raw, q_norm_w, out,
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
 size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos) {
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || max_pos < 0) return 0;
-  const int splits = kvq::decode_pick_splits(L, n_seqs, max_pos + 1, num_sms_current());
-  return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, splits);
+  const kvq::DecodePlan plan = kvq::decode_plan(L, n_seqs, max_pos + 1, num_sms_current(), true);
+  return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, plan.splits);
 }
 
 kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
@@ -218,8 +221,8 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
   if (max_rows_per_seq < 1 && n_rows > 0) return fail(KVQ_EINVAL, "max_rows_per_seq < 1");
   // each row reads at most window keys (full layers: the caller's positions)
   const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
-  return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, q_raw, q_norm_w,
-                          out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
+  return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, false, q_raw,
+                          q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
@@ -227,8 +230,8 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || n_rows < 0 || max_rows_per_seq < 0) return 0;
   const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
-  const int splits = kvq::decode_pick_splits(L, n_rows, max_keys, num_sms_current());
-  return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
+  const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), false);
+  return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan.splits);
 }
 
 // ---------------------------------------------------------------------------
@@ -293,7 +296,7 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
   int dev = 0;
   void* scratch = static_scratch_address(&dev);
   if (!scratch) return KVQ_ECUDA;
-  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, q_raw, q_norm_w, out,
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
 }
 

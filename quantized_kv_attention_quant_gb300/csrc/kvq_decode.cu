@@ -590,7 +590,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
                   (ri.newest - lo + 1) <= c.capacity;
   const int t_lo = lo / kTileKeys, t_hi = hi / kTileKeys;
   const int ntiles = t_hi - t_lo + 1;
-  const int chunk = (ntiles + a.splits - 1) / a.splits;
+  const int chunk = a.chunk_tiles > 0 ? a.chunk_tiles : (ntiles + a.splits - 1) / a.splits;
   const int t_begin = t_lo + split * chunk;
   const int n_my = ok ? max(0, min(chunk, t_hi + 1 - t_begin)) : 0;
   if (n_my == 0) {
@@ -748,14 +748,28 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
   return w;
 }
 
-int decode_pick_splits(const LayerArgs& L, int n_rows, int max_keys, int num_sms) {
+DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks) {
   const long keys = L.window > 0 ? std::min<long>((long)max_keys, L.window) : (long)max_keys;
-  const int tiles = int(keys / kTileKeys) + 2;
+  const int tiles = int(keys / kTileKeys) + 2;              // tiles one row can touch
   const int per_sm = L.D >= 512 ? 1 : (L.D == 256 ? 2 : 4);
-  const long base = (long)n_rows * L.n_kv;
-  long want = ((long)num_sms * per_sm + base - 1) / std::max<long>(base, 1);
-  want = std::min<long>(want, std::max(1, tiles / 2));
-  return int(std::max<long>(1, std::min<long>(want, 256)));
+  const long base = std::max<long>((long)n_rows * L.n_kv, 1);
+  const long wave = ((long)num_sms * per_sm + base - 1) / base;    // splits for one full wave
+  DecodePlan plan;
+  if (fixed_chunks) {
+    // every split takes the same number of tiles: rows shorter than the
+    // longest use fewer splits and their surplus CTAs exit at once, so ragged
+    // batches balance through the block scheduler
+    long splits = std::max<long>(wave, (tiles + kChunkTiles - 1) / kChunkTiles);
+    splits = std::max<long>(1, std::min<long>(splits, 256));
+    const int chunk = int((tiles + splits - 1) / splits);
+    plan.chunk_tiles = chunk;
+    plan.splits = (tiles + chunk - 1) / chunk;
+  } else {
+    long splits = std::min<long>(wave, std::max(1, tiles / 2));
+    plan.splits = int(std::max<long>(1, std::min<long>(splits, 256)));
+    plan.chunk_tiles = 0;                                   // per row: ceil(row tiles / splits)
+  }
+  return plan;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int /*num_sms*/, cudaStream_t st) {

@@ -61,12 +61,15 @@ struct DecodeArgs {
   int out_f32;
   uint16_t* q_prepped;
   int splits;
+  int chunk_tiles;      // > 0: every split covers this many tiles; 0: ceil(row tiles / splits)
   DecodeWs ws;
 };
 
 size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits);
 DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits);
-int decode_pick_splits(const LayerArgs& L, int n_rows, int max_keys, int num_sms);
+constexpr int kChunkTiles = 32;   // target tiles per split when the longest row is known
+struct DecodePlan { int splits, chunk_tiles; };
+DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks);
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
