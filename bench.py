@@ -193,6 +193,14 @@ def dist_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(tokens_per_rank_step: float, ms_local: float, steps: int, world: int, device):
+    """(tokens/s of the whole job, ms per step): every rank processes its own
+    sequences (weak scaling); the job takes as long as the slowest rank."""
+    ms = dist_max(ms_local, world, device)
+    ms_step = ms / steps
+    return tokens_per_rank_step * world / (ms_step / 1e3), ms_step
+
+
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
@@ -312,11 +320,7 @@ def run_gpu(args):
         t1.record(replay_stream)
         torch.cuda.synchronize()
         dist_barrier(world, device)
-    ms_total = t0.elapsed_time(t1)
-    ms_total = dist_max(ms_total, world, device)
-    ms_step = ms_total / K
-    tokens_per_step = info["tokens"] * world
-    value = tokens_per_step / (ms_step / 1e3)
+    value, ms_step = whole_job_rate(info["tokens"], t0.elapsed_time(t1), K, world, device)
 
     # dominant-kernel duration from the events inside the graph
     dom_ms = None
