@@ -323,42 +323,32 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
 }
 
 // ----------------------------------------------------------------------------
-// Code -> f16 conversion (exact: integers <= 255 are f16 values).
-// 0x6400 is f16 1024; OR-ing a value v < 1024 into its mantissa gives 1024+v.
+// Code -> f16 conversion with one logic op per pair.  A 16-bit half whose
+// exponent field is zero is an f16 subnormal: bits m (m < 1024) in its
+// mantissa are the exact value m * 2^-24.  So masking a packed word leaves
+// two codes as exact f16 values scaled by 2^-24 (codes taken from bits 4..7
+// come out scaled by 2^-20, i.e. 16 times larger).  The tensor cores multiply
+// f16 subnormals exactly; the power of two is divided out of the fp32 result.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t orv) {
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(orv));  // (x & mask) | orv
-  return r;
-}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
-                      *reinterpret_cast<__half2*>(&c));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
 __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
-constexpr uint32_t kMagic = 0x64006400u;        // (1024, 1024)
-constexpr uint32_t kSixteenth = 0x2C002C00u;    // (1/16, 1/16)
-constexpr uint32_t kNeg64 = 0xD400D400u;        // (-64, -64)
+constexpr float kTwo24 = 16777216.f;            // 2^24
 
-// low nibbles of each 16-bit half -> (c, c)
-__device__ __forceinline__ uint32_t nib_lo(uint32_t x) { return h2_sub(lop3_and_or(x, 0x000F000Fu, kMagic), kMagic); }
-// bits 4..7 of each 16-bit half -> (c, c)
-__device__ __forceinline__ uint32_t nib_hi(uint32_t x) { return h2_fma(lop3_and_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64); }
-// low bytes of each 16-bit half -> (c, c)
-__device__ __forceinline__ uint32_t byte_lo(uint32_t x) { return h2_sub(lop3_and_or(x, 0x00FF00FFu, kMagic), kMagic); }
+// bits 0..3 of each 16-bit half -> (c, c) * 2^-24
+__device__ __forceinline__ uint32_t sub_n0(uint32_t x) { return x & 0x000F000Fu; }
+// bits 4..7 of each 16-bit half -> (c, c) * 2^-20
+__device__ __forceinline__ uint32_t sub_n1(uint32_t x) { return x & 0x00F000F0u; }
+// bits 0..7 of each 16-bit half -> (c, c) * 2^-24
+__device__ __forceinline__ uint32_t sub_b0(uint32_t x) { return x & 0x00FF00FFu; }
+// bytes 1 and 3 of x moved to bytes 0 and 2, zeros above -> (c, c) * 2^-24
+__device__ __forceinline__ uint32_t sub_b1(uint32_t x) { return prmt(x, 0u, 0x4341u); }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);

@@ -43,12 +43,17 @@ struct Dec {
 
 constexpr int kMaxStages = 8;
 
+// Shared-memory stage of one 64-key tile.  The K (then V) code rows arrive as
+// 8 chunks of 8 consecutive keys, each chunk one bulk copy of 8 rows followed
+// by 32 bytes of padding; chunk c starts 32*c bytes (mod 128) into the bank
+// space, so rows of different chunks fall on different banks.  Then the four
+// 64 x (D/64) bf16 blocks: K scales, K biases, V scales, V biases.
 __host__ __device__ constexpr int row_bytes(int D, int bits) { return D * bits / 8; }
-__host__ __device__ constexpr int row_stride(int D, int bits) { return D * bits / 8 + 16; }
+__host__ __device__ constexpr int chunk_stride(int D, int bits) { return 8 * row_bytes(D, bits) + 32; }
 __host__ __device__ constexpr int sb_bytes(int D) { return 64 * (D / 64) * 2; }
-__host__ __device__ constexpr int stage_bytes(int D, int bits) { return 2 * 64 * row_stride(D, bits) + 4 * sb_bytes(D); }
+__host__ __device__ constexpr int stage_bytes(int D, int bits) { return 16 * chunk_stride(D, bits) + 4 * sb_bytes(D); }
 __host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
-// control block: mbarriers, max-exchange [2][NW][16], l-exchange [NW][16] (floats),
+// control block: mbarriers, max-exchange [2][16][NW], l-exchange [16][NW] (floats),
 // V scale/bias f16 pairs [2][2][NG][32] (words)
 __host__ __device__ constexpr int ctrl_bytes(int D) { return align128(128 + (3 * (D / 64) * 16) * 4 + 2 * 2 * (D / 64) * 32 * 4); }
 __host__ __device__ constexpr int stage0_off(int D) { return ctrl_bytes(D) + 2 * 16 * 64 * 2; }
@@ -91,10 +96,6 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
   const int o0 = __ldg(a.row_offsets + lo), o1 = __ldg(a.row_offsets + lo + 1);
   const int p0 = __ldg(a.pos + lo);
   return {lo, p0 + (row - o0), p0 + (o1 - o0) - 1};
-}
-
-__device__ __forceinline__ uint32_t bf16_pair_to_h2(uint16_t lo, uint16_t hi) {
-  return pack_h2(bf16_to_f(lo), bf16_to_f(hi));
 }
 
 // ----------------------------------------------------------------------------
@@ -212,7 +213,11 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
     qk_dims(bits, ks, d);
     const int base = g * 64 + 16 * t4;
     const int d0 = base + (pair ? d[2] : d[0]), d1 = base + (pair ? d[3] : d[1]);
-    frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] = bf16_pair_to_h2(qn[d0], qn[d1]);
+    // with 4-bit codes the second k-half of every step multiplies codes read
+    // from bits 4..7 (16 times too large as f16 subnormals): q/16 there
+    const float f = (bits == 4 && pair) ? 0.0625f : 1.f;
+    frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] =
+        pack_h2(bf16_to_f(qn[d0]) * f, bf16_to_f(qn[d1]) * f);
   }
   // bias-term A fragment words of row h: k = group (hi part) | 8 + group (lo part)
   if (t < 8) {
@@ -260,51 +265,88 @@ __device__ __forceinline__ float bf16_word_at(const uint32_t (&w)[(NG + 1) / 2],
 // that it stays clear of the f16 subnormal range; divided out at the end.
 template <int BITS> struct PvPrescale { static constexpr int log2 = BITS == 4 ? 2 : 6; };
 
+// Key mapping inside a tile (keys 8c + s: chunk c, slot s).
+//   QK n-tile j (0..7) holds the keys of slot j, column n = chunk n; its B
+//   fragment rows therefore sit in eight different chunks.
+//   PV k-step kk (0..3) holds slots 2kk and 2kk+1; MMA k index
+//   2*t + b + 8*a (t < 4, a, b < 2) is key 8*(t + 4a) + 2kk + b, and P is
+//   stored in this order (column = 16*kk + k index).
+__device__ __forceinline__ int pv_col(int key) {
+  const int c = key >> 3, s = key & 7;
+  return (s >> 1) * 16 + 2 * (c & 3) + (s & 1) + 8 * (c >> 2);
+}
+
+template <int NW>
+__device__ __forceinline__ float max_over_warps(const float* p) {
+  float m;
+  if constexpr (NW >= 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if constexpr (NW == 8) {
+      const float4 u = *reinterpret_cast<const float4*>(p + 4);
+      m = fmaxf(m, fmaxf(fmaxf(u.x, u.y), fmaxf(u.z, u.w)));
+    }
+  } else if constexpr (NW == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    m = fmaxf(v.x, v.y);
+  } else {
+    m = p[0];
+  }
+  return m;
+}
+
 template <int D, int BITS>
 __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
                                             const int nst, const TileRange tr, const int row, const int kvh,
                                             const int split) {
   using C = Dec<D>;
-  constexpr int NG = C::NG, NW = C::NW, KPW = C::KPW, NTQ = C::NTQ;
-  constexpr int RB = row_bytes(D, BITS), RS = row_stride(D, BITS), SB = sb_bytes(D);
+  constexpr int NG = C::NG, NW = C::NW, NTQ = C::NTQ;
+  constexpr int RB = row_bytes(D, BITS), CS = chunk_stride(D, BITS), SB = sb_bytes(D);
   constexpr int STB = stage_bytes(D, BITS);
+  constexpr uint32_t TX = 2 * 64 * RB + 4 * SB;
   constexpr float L2E = 1.4426950408889634f;
   constexpr float PRESCALE = float(1 << PvPrescale<BITS>::log2);
+  constexpr int GB = NG < 4 ? NG : 4;           // groups whose MMA chains run interleaved
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3, rq = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 128);        // [2][NW][16] tile max exchange
-  float* lred = red + 2 * NW * 16;                          // [NW][16]
+  float* red = reinterpret_cast<float*>(smem + 128);        // [2][16][NW] tile max exchange
+  float* lred = red + 2 * NW * 16;                          // [16][NW]
   uint32_t* vsb = reinterpret_cast<uint32_t*>(lred + NW * 16);  // [2][2][NG][32] f16 pairs of V scale/bias
   uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
   uint8_t* stages = smem + stage0_off(D);
-  const int cap = c.capacity;
-  const size_t head_row0 = (size_t)kvh * cap;
+  const int cap_tiles = c.capacity / kTileKeys;
+  const size_t head_row0 = (size_t)kvh * c.capacity;
 
-  // Issue tile `it` into its stage: 128 code rows and 4 scale/bias blocks,
-  // spread over all threads of the CTA (one or two copies each).
-  auto issue = [&](int it) {
-    const int st = it % nst;
+  // Copies of one tile: 8 K chunks, 8 V chunks, 4 scale/bias blocks, spread
+  // over the warps (copy j is issued by lane j / NW of warp j % NW).
+  const int my_copy = lane * NW + warp;
+  auto issue = [&](int st, int slot_tile) {
     uint8_t* sb = stages + st * STB;
-    const size_t r0 = head_row0 + ((tr.t_begin + it) * kTileKeys) % cap;
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(&full[st], 2 * 64 * RB + 4 * SB);
-    fence_proxy_async();        // order this CTA's earlier generic reads of the stage before the copies
-    for (int j = threadIdx.x; j < 2 * 64 + 4; j += NW * 32) {
-      if (j < 64) {
-        bulk_g2s(sb + j * RS, reinterpret_cast<const uint8_t*>(c.k_codes) + (r0 + j) * RB, RB, &full[st]);
-      } else if (j < 128) {
-        const int r = j - 64;
-        bulk_g2s(sb + j * RS, reinterpret_cast<const uint8_t*>(c.v_codes) + (r0 + r) * RB, RB, &full[st]);
+    const size_t r0 = head_row0 + (size_t)slot_tile * kTileKeys;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&full[st], TX);
+    if (my_copy < 20) {
+      fence_proxy_async();      // this CTA's earlier generic reads of the stage come first
+      if (my_copy < 16) {
+        const int ch = my_copy & 7;
+        const uint32_t* src = my_copy < 8 ? c.k_codes : c.v_codes;
+        bulk_g2s(sb + my_copy * CS, reinterpret_cast<const uint8_t*>(src) + (r0 + 8 * ch) * RB, 8 * RB, &full[st]);
       } else {
-        const int q = j - 128;
+        const int q = my_copy - 16;
         const uint16_t* src = q == 0 ? c.k_scales : q == 1 ? c.k_biases : q == 2 ? c.v_scales : c.v_biases;
-        bulk_g2s(sb + 2 * 64 * RS + q * SB, src + r0 * NG, SB, &full[st]);
+        bulk_g2s(sb + 16 * CS + q * SB, src + r0 * NG, SB, &full[st]);
       }
     }
   };
   // prologue: fill every stage (the cache was written before this launch)
-  for (int it = 0; it < min(nst, tr.n_my); ++it) issue(it);
   int issued = min(nst, tr.n_my);
+  int issue_st = 0;
+  int issue_slot = tr.t_begin % cap_tiles;
+  for (int i = 0; i < issued; ++i) {
+    issue(issue_st, issue_slot);
+    if (++issue_st == nst) issue_st = 0;
+    if (++issue_slot == cap_tiles) issue_slot = 0;
+  }
 
   pdl_wait();                                   // q fragments come from qprep_kernel
   // QK A fragments (q heads x permuted head_dim) and the bias-term A fragment
@@ -325,7 +367,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     qb[0] = v.x; qb[1] = v.y; qb[2] = v.z; qb[3] = v.w;
   }
 
-  float oacc[8][4];      // PV accumulator of this warp's group: 16 rows x 64 dims (permuted)
+  float oacc[8][4];      // PV accumulator of this warp's group: 16 rows x 64 dims (permuted), 2^-24 units
   float cb[4];           // sum_j P_j * bias_j of this warp's group (column 0 is used)
 #pragma unroll
   for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
@@ -333,53 +375,58 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   bool dead = false;
   const int g_pv = warp;                        // PV group of this warp
+  int st = 0, phase = 0;
 
   for (int it = 0; it < tr.n_my; ++it) {
-    const int st = it % nst, buf = it & 1;
-    if (!dead && !mbar_wait(&full[st], (it / nst) & 1)) {
+    const int buf = it & 1;
+    if (!dead && !mbar_wait(&full[st], phase)) {
       dead = true;
       flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
     }
     const uint8_t* Ks = stages + st * STB;
-    const uint8_t* Vs = Ks + 64 * RS;
-    const uint16_t* sks = reinterpret_cast<const uint16_t*>(Ks + 2 * 64 * RS);
+    const uint8_t* Vs = Ks + 8 * CS;
+    const uint16_t* sks = reinterpret_cast<const uint16_t*>(Ks + 16 * CS);
     const uint16_t* skb = sks + 64 * NG;
     const uint16_t* svs = skb + 64 * NG;
     const uint16_t* svb = svs + 64 * NG;
     const int tpos0 = (tr.t_begin + it) * kTileKeys;
+    const bool inner = tpos0 >= tr.lo && tpos0 + kTileKeys - 1 <= tr.hi;   // no masked key
 
-    // ---- V scale/bias of this tile as f16 pairs (scale pre-multiplied by
-    // PRESCALE), zero for keys outside the window ----
+    // ---- V scale/bias of this tile as f16 pairs of consecutive keys (scale
+    // pre-multiplied by PRESCALE), zero for keys outside the window ----
     {
       uint32_t* vs16 = vsb + buf * 2 * NG * 32;
-      uint32_t* vb16 = vs16 + NG * 32;
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
-        const int idx = threadIdx.x + rep * NW * 32;          // NG * 64 entries = 2 per thread
+        const int idx = threadIdx.x + rep * NW * 32;          // 2 * NG * 32 entries = 2 per thread
         const int which = idx / (NG * 32);                    // 0: scale, 1: bias
         const int rem = idx % (NG * 32);
         const int g = rem / 32, pr = rem % 32;
         const int k0 = 2 * pr;
-        const bool v0 = tpos0 + k0 >= tr.lo && tpos0 + k0 <= tr.hi;
-        const bool v1 = tpos0 + k0 + 1 >= tr.lo && tpos0 + k0 + 1 <= tr.hi;
         const uint16_t* srcp = which == 0 ? svs : svb;
         const float mul = which == 0 ? PRESCALE : 1.f;
-        const float x0 = v0 ? bf16_to_f(srcp[k0 * NG + g]) * mul : 0.f;
-        const float x1 = v1 ? bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul : 0.f;
-        (which == 0 ? vs16 : vb16)[g * 32 + pr] = pack_h2(x0, x1);
+        float x0 = bf16_to_f(srcp[k0 * NG + g]) * mul;
+        float x1 = bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul;
+        if (!inner) {
+          if (tpos0 + k0 < tr.lo || tpos0 + k0 > tr.hi) x0 = 0.f;
+          if (tpos0 + k0 + 1 < tr.lo || tpos0 + k0 + 1 > tr.hi) x1 = 0.f;
+        }
+        vs16[which * NG * 32 + g * 32 + pr] = pack_h2(x0, x1);
       }
     }
 
-    // ---- QK: this warp's KPW keys, all q heads, full head_dim ----
+    // ---- QK: this warp's NTQ n-tiles (keys of slot j, one per chunk), all q
+    // heads, full head_dim ----
     float S[NTQ][4];
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
-      const int kb8 = warp * KPW + nt * 8;
-      const int kB = kb8 + rq, kC = kb8 + 2 * t4;
+      const int j = warp * NTQ + nt;
       // bias term: sum_g qsum[h][g] * bias[key][g] as one MMA (k = group for
-      // the hi part, 8 + group for the lo part)
+      // the hi part, 8 + group for the lo part); B column rq is key 8*rq + j
+      float Sb[4];
       {
+        const int kB = 8 * rq + j;
         uint32_t bb = 0;
         if constexpr (NG == 1) {       // one group: a single bf16 (2-byte aligned only)
           if (t4 == 0) bb = pack_h2(bf16_to_f(skb[kB]), 0.f);
@@ -389,38 +436,66 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
             bb = pack_h2(bf16lo_to_f(w), bf16hi_to_f(w));
           }
         }
-        mma_f16_zc(S[nt], qb, bb, bb);
+        mma_f16_zc(Sb, qb, bb, bb);
       }
+      // S columns 2*t4 and 2*t4+1 are keys 16*t4 + j and 16*t4 + 8 + j
+      const int kc0 = 16 * t4 + j;
       uint32_t sw0[(NG + 1) / 2], sw1[(NG + 1) / 2];
-      load_bf16_row<NG>(sks + kC * NG, sw0);
-      load_bf16_row<NG>(sks + (kC + 1) * NG, sw1);
-      const uint8_t* krow = Ks + kB * RS + t4 * (BITS * 2);
+      load_bf16_row<NG>(sks + kc0 * NG, sw0);
+      load_bf16_row<NG>(sks + (kc0 + 8) * NG, sw1);
+      const uint8_t* krow = Ks + rq * CS + j * RB + t4 * (BITS * 2);
+      float T[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        float acc[4];
+      for (int g0 = 0; g0 < NG; g0 += GB) {
+        float acc[GB][4];
         if constexpr (BITS == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(krow + g * 32);
-          mma_f16_zc(acc, qa[g][0], nib_lo(w.x), nib_hi(w.x));
-          mma_f16(acc, qa[g][1], nib_lo(w.x >> 8), nib_hi(w.x >> 8));
-          mma_f16(acc, qa[g][2], nib_lo(w.y), nib_hi(w.y));
-          mma_f16(acc, qa[g][3], nib_lo(w.y >> 8), nib_hi(w.y >> 8));
+          uint2 w[GB];
+#pragma unroll
+          for (int u = 0; u < GB; ++u) w[u] = *reinterpret_cast<const uint2*>(krow + (g0 + u) * 32);
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16_zc(acc[u], qa[g0 + u][0], sub_n0(w[u].x), sub_n1(w[u].x));
+#pragma unroll
+          for (int u = 0; u < GB; ++u) {
+            const uint32_t x = w[u].x >> 8;
+            mma_f16(acc[u], qa[g0 + u][1], sub_n0(x), sub_n1(x));
+          }
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16(acc[u], qa[g0 + u][2], sub_n0(w[u].y), sub_n1(w[u].y));
+#pragma unroll
+          for (int u = 0; u < GB; ++u) {
+            const uint32_t y = w[u].y >> 8;
+            mma_f16(acc[u], qa[g0 + u][3], sub_n0(y), sub_n1(y));
+          }
         } else {
-          const uint4 w = *reinterpret_cast<const uint4*>(krow + g * 64);
-          mma_f16_zc(acc, qa[g][0], byte_lo(w.x), byte_lo(w.x >> 8));
-          mma_f16(acc, qa[g][1], byte_lo(w.y), byte_lo(w.y >> 8));
-          mma_f16(acc, qa[g][2], byte_lo(w.z), byte_lo(w.z >> 8));
-          mma_f16(acc, qa[g][3], byte_lo(w.w), byte_lo(w.w >> 8));
+          uint4 w[GB];
+#pragma unroll
+          for (int u = 0; u < GB; ++u) w[u] = *reinterpret_cast<const uint4*>(krow + (g0 + u) * 64);
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16_zc(acc[u], qa[g0 + u][0], sub_b0(w[u].x), sub_b1(w[u].x));
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16(acc[u], qa[g0 + u][1], sub_b0(w[u].y), sub_b1(w[u].y));
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16(acc[u], qa[g0 + u][2], sub_b0(w[u].z), sub_b1(w[u].z));
+#pragma unroll
+          for (int u = 0; u < GB; ++u) mma_f16(acc[u], qa[g0 + u][3], sub_b0(w[u].w), sub_b1(w[u].w));
         }
-        const float s0 = bf16_word_at<NG>(sw0, g), s1 = bf16_word_at<NG>(sw1, g);
-        S[nt][0] = fmaf(s0, acc[0], S[nt][0]);
-        S[nt][1] = fmaf(s1, acc[1], S[nt][1]);
-        S[nt][2] = fmaf(s0, acc[2], S[nt][2]);
-        S[nt][3] = fmaf(s1, acc[3], S[nt][3]);
+#pragma unroll
+        for (int u = 0; u < GB; ++u) {
+          const float s0 = bf16_word_at<NG>(sw0, g0 + u), s1 = bf16_word_at<NG>(sw1, g0 + u);
+          T[0] = fmaf(s0, acc[u][0], T[0]);
+          T[1] = fmaf(s1, acc[u][1], T[1]);
+          T[2] = fmaf(s0, acc[u][2], T[2]);
+          T[3] = fmaf(s1, acc[u][3], T[3]);
+        }
       }
-      const int kp = tpos0 + kC;
-      const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 1 >= tr.lo && kp + 1 <= tr.hi;
-      if (!v0) { S[nt][0] = -INFINITY; S[nt][2] = -INFINITY; }
-      if (!v1) { S[nt][1] = -INFINITY; S[nt][3] = -INFINITY; }
+      // the code products are in units of 2^-24
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S[nt][e] = fmaf(T[e], kTwo24, Sb[e]);
+      if (!inner) {
+        const int kp = tpos0 + kc0;
+        if (kp < tr.lo || kp > tr.hi) { S[nt][0] = -INFINITY; S[nt][2] = -INFINITY; }
+        if (kp + 8 < tr.lo || kp + 8 > tr.hi) { S[nt][1] = -INFINITY; S[nt][3] = -INFINITY; }
+      }
       tmax[0] = fmaxf(tmax[0], fmaxf(S[nt][0], S[nt][1]));
       tmax[1] = fmaxf(tmax[1], fmaxf(S[nt][2], S[nt][3]));
     }
@@ -430,11 +505,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], m));
     }
     float* redb = red + buf * NW * 16;
-    if (t4 == 0) { redb[warp * 16 + rq] = tmax[0]; redb[warp * 16 + rq + 8] = tmax[1]; }
+    if (t4 == 0) { redb[rq * NW + warp] = tmax[0]; redb[(rq + 8) * NW + warp] = tmax[1]; }
     named_bar(1, NW * 32);
-    // every warp has finished tile it-1: its stage takes tile it-1+nst
+    // every warp has finished tile it-1: its stage takes the next tile
     if (it >= 1 && issued < tr.n_my) {
-      issue(issued);
+      issue(issue_st, issue_slot);
+      if (++issue_st == nst) issue_st = 0;
+      if (++issue_slot == cap_tiles) issue_slot = 0;
       ++issued;
     }
 
@@ -442,9 +519,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     float m_new[2], alpha[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float mt = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) mt = fmaxf(mt, redb[w * 16 + rq + 8 * h]);
+      const float mt = max_over_warps<NW>(redb + (rq + 8 * h) * NW);
       m_new[h] = fmaxf(m_run[h], mt);
       alpha[h] = m_new[h] == -INFINITY ? 1.f : exp2f((m_run[h] - m_new[h]) * L2E);
     }
@@ -452,7 +527,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     float lsum[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
-      const int kC = warp * KPW + nt * 8 + 2 * t4;
+      const int j = warp * NTQ + nt;
+      const int col0 = pv_col(16 * t4 + j), col1 = pv_col(16 * t4 + 8 + j);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float p0 = 0.f, p1 = 0.f;
@@ -460,12 +536,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
           p0 = exp2f((S[nt][2 * h] - m_new[h]) * L2E);
           p1 = exp2f((S[nt][2 * h + 1] - m_new[h]) * L2E);
         }
-        const __half2 ph = __floats2half2_rn(p0, p1);
-        const float2 pf = __half22float2(ph);
-        lsum[h] += pf.x + pf.y;
+        const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
+        lsum[h] += __half2float(h0) + __half2float(h1);
         const int prow = rq + 8 * h;
-        const int chunk = (kC >> 3) ^ (prow & 7);
-        *reinterpret_cast<__half2*>(Pb + prow * 128 + chunk * 16 + (kC & 7) * 2) = ph;
+        uint8_t* prw = Pb + prow * 128;
+        *reinterpret_cast<__half*>(prw + (((col0 >> 3) ^ (prow & 7)) << 4) + (col0 & 7) * 2) = h0;
+        *reinterpret_cast<__half*>(prw + (((col1 >> 3) ^ (prow & 7)) << 4) + (col1 & 7) * 2) = h1;
       }
     }
 #pragma unroll
@@ -483,6 +559,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     }
     const uint32_t* vs16 = vsb + buf * 2 * NG * 32 + g_pv * 32;
     const uint32_t* vb16 = vs16 + NG * 32;
+    // this lane's B rows: k = 2*t4 (+1) -> chunk t4, k = 2*t4 + 8 (+1) -> chunk t4 + 4
+    const uint8_t* vlo = Vs + t4 * CS + (BITS == 4 ? g_pv * 32 + rq * 4 : g_pv * 64 + rq * 8);
+    const uint8_t* vhi = vlo + 4 * CS;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
@@ -492,49 +571,46 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const int chunk = (kk * 2 + (mtx >> 1)) ^ (prow & 7);
         ldmatrix_x4(pa, Pb + prow * 128 + chunk * 16);
       }
-      const int ka = kk * 16 + 2 * t4;           // keys ka, ka+1, ka+8, ka+9
-      const uint32_t sAB = vs16[kk * 8 + t4], sCD = vs16[kk * 8 + 4 + t4];
+      // key pairs (8*t4 + 2kk, +1) and (8*(t4+4) + 2kk, +1)
+      const uint32_t sAB = vs16[4 * t4 + kk], sCD = vs16[16 + 4 * t4 + kk];
       // bias column: only B column 0 (lanes 0..3) is non-zero
-      const uint32_t bAB = rq == 0 ? vb16[kk * 8 + t4] : 0u, bCD = rq == 0 ? vb16[kk * 8 + 4 + t4] : 0u;
+      const uint32_t bAB = rq == 0 ? vb16[4 * t4 + kk] : 0u, bCD = rq == 0 ? vb16[16 + 4 * t4 + kk] : 0u;
       mma_f16(cb, pa, bAB, bCD);
       const uint32_t ps[4] = {h2_mul(pa[0], sAB), h2_mul(pa[1], sAB), h2_mul(pa[2], sCD), h2_mul(pa[3], sCD)};
       if constexpr (BITS == 4) {
-        const uint8_t* vrow = Vs + g_pv * 32 + rq * 4;
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vrow + ka * RS);
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vrow + (ka + 1) * RS);
-        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vrow + (ka + 8) * RS);
-        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vrow + (ka + 9) * RS);
-        const uint32_t xab = prmt(wa, wb, 0x5410), yab = prmt(wa, wb, 0x7632);
-        const uint32_t xcd = prmt(wc, wd, 0x5410), ycd = prmt(wc, wd, 0x7632);
-        const uint32_t src_ab[4] = {xab, xab >> 8, yab, yab >> 8};
-        const uint32_t src_cd[4] = {xcd, xcd >> 8, ycd, ycd >> 8};
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vlo + (2 * kk) * RB);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vlo + (2 * kk + 1) * RB);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vhi + (2 * kk) * RB);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vhi + (2 * kk + 1) * RB);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          mma_f16(oacc[2 * q], ps, nib_lo(src_ab[q]), nib_lo(src_cd[q]));
-          mma_f16(oacc[2 * q + 1], ps, nib_hi(src_ab[q]), nib_hi(src_cd[q]));
+          // byte q of both keys into the low byte of each half
+          const uint32_t sel = (uint32_t)(q | (q << 4) | ((4 + q) << 8) | ((4 + q) << 12));
+          const uint32_t xab = prmt(wa, wb, sel), xcd = prmt(wc, wd, sel);
+          mma_f16(oacc[2 * q], ps, sub_n0(xab), sub_n0(xcd));
+          mma_f16(oacc[2 * q + 1], ps, sub_n1(xab), sub_n1(xcd));
         }
       } else {
-        const uint8_t* vrow = Vs + g_pv * 64 + rq * 8;
-        const uint2 wa = *reinterpret_cast<const uint2*>(vrow + ka * RS);
-        const uint2 wb = *reinterpret_cast<const uint2*>(vrow + (ka + 1) * RS);
-        const uint2 wc = *reinterpret_cast<const uint2*>(vrow + (ka + 8) * RS);
-        const uint2 wd = *reinterpret_cast<const uint2*>(vrow + (ka + 9) * RS);
-        const uint32_t src_ab[4] = {prmt(wa.x, wb.x, 0x5410), prmt(wa.x, wb.x, 0x7632),
-                                    prmt(wa.y, wb.y, 0x5410), prmt(wa.y, wb.y, 0x7632)};
-        const uint32_t src_cd[4] = {prmt(wc.x, wd.x, 0x5410), prmt(wc.x, wd.x, 0x7632),
-                                    prmt(wc.y, wd.y, 0x5410), prmt(wc.y, wd.y, 0x7632)};
+        const uint2 wa = *reinterpret_cast<const uint2*>(vlo + (2 * kk) * RB);
+        const uint2 wb = *reinterpret_cast<const uint2*>(vlo + (2 * kk + 1) * RB);
+        const uint2 wc = *reinterpret_cast<const uint2*>(vhi + (2 * kk) * RB);
+        const uint2 wd = *reinterpret_cast<const uint2*>(vhi + (2 * kk + 1) * RB);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mma_f16(oacc[2 * q], ps, byte_lo(src_ab[q]), byte_lo(src_cd[q]));
-          mma_f16(oacc[2 * q + 1], ps, byte_lo(src_ab[q] >> 8), byte_lo(src_cd[q] >> 8));
+        for (int q = 0; q < 8; ++q) {
+          const int bq = q & 3;
+          const uint32_t sel = (uint32_t)(bq | ((4 + bq) << 8));
+          const uint32_t xab = prmt(q < 4 ? wa.x : wa.y, q < 4 ? wb.x : wb.y, sel) & 0x00FF00FFu;
+          const uint32_t xcd = prmt(q < 4 ? wc.x : wc.y, q < 4 ? wd.x : wd.y, sel) & 0x00FF00FFu;
+          mma_f16(oacc[q], ps, xab, xcd);
         }
       }
     }
+    if (++st == nst) { st = 0; phase ^= 1; }
   }
   pdl_launch();
   // a timed-out wait may leave copies in flight: they must land before exit
   if (dead && threadIdx.x == 0)
-    for (int it = max(0, issued - nst); it < issued; ++it) mbar_wait(&full[it % nst], (it / nst) & 1);
+    for (int i = max(0, issued - nst); i < issued; ++i) mbar_wait(&full[i % nst], (i / nst) & 1);
 
   // ---- write this split's partial (m, l, o) ----
 #pragma unroll
@@ -542,7 +618,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
-  if (t4 == 0) { lred[warp * 16 + rq] = l_run[0]; lred[warp * 16 + rq + 8] = l_run[1]; }
+  if (t4 == 0) { lred[rq * NW + warp] = l_run[0]; lred[(rq + 8) * NW + warp] = l_run[1]; }
   // bias column 0 lives in lanes with t4 == 0 (c0: row rq, c2: row rq + 8)
   const float bias_r = __shfl_sync(0xffffffffu, cb[0], lane & ~3);
   const float bias_r8 = __shfl_sync(0xffffffffu, cb[2], lane & ~3);
@@ -556,21 +632,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     if (t4 == 0) { ml[rq] = m_run[0]; ml[rq + 8] = m_run[1]; }
     if (lane < 16) {
       float l = 0.f;
-      for (int w = 0; w < NW; ++w) l += lred[w * 16 + lane];
+      for (int w = 0; w < NW; ++w) l += lred[lane * NW + w];
       ml[16 + lane] = l;
     }
   }
-  constexpr float UNSCALE = 1.f / PRESCALE;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
+    // codes were 2^-24 units (2^-20 for 4-bit codes from bits 4..7: odd nt)
+    const float uns = (BITS == 4 && (nt & 1) ? kTwo24 / 16.f : kTwo24) / PRESCALE;
     const int d0 = g_pv * 64 + 8 * (2 * t4) + nt, d1 = d0 + 8;
     if (rq < G) {
-      po[rq * D + d0] = fmaf(oacc[nt][0], UNSCALE, bias_r);
-      po[rq * D + d1] = fmaf(oacc[nt][1], UNSCALE, bias_r);
+      po[rq * D + d0] = fmaf(oacc[nt][0], uns, bias_r);
+      po[rq * D + d1] = fmaf(oacc[nt][1], uns, bias_r);
     }
     if (rq + 8 < G) {
-      po[(rq + 8) * D + d0] = fmaf(oacc[nt][2], UNSCALE, bias_r8);
-      po[(rq + 8) * D + d1] = fmaf(oacc[nt][3], UNSCALE, bias_r8);
+      po[(rq + 8) * D + d0] = fmaf(oacc[nt][2], uns, bias_r8);
+      po[(rq + 8) * D + d1] = fmaf(oacc[nt][3], uns, bias_r8);
     }
   }
 }
@@ -749,8 +826,11 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
 }
 
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks) {
-  const long keys = L.window > 0 ? std::min<long>((long)max_keys, L.window) : (long)max_keys;
-  const int tiles = int(keys / kTileKeys) + 2;              // tiles one row can touch
+  // tiles one row can touch: keys 0..max_keys-1 when causal, else a window
+  // of at most `window` keys starting anywhere inside a tile
+  const long full_tiles = ((long)std::max(max_keys, 1) - 1) / kTileKeys + 1;
+  const int tiles = int(L.window > 0 ? std::min<long>(full_tiles, (L.window + kTileKeys - 2) / kTileKeys + 1)
+                                     : full_tiles);
   const int per_sm = L.D >= 512 ? 1 : (L.D == 256 ? 2 : 4);
   const long base = std::max<long>((long)n_rows * L.n_kv, 1);
   const long wave = ((long)num_sms * per_sm + base - 1) / base;    // splits for one full wave
