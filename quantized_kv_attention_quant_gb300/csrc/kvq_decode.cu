@@ -306,7 +306,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   constexpr uint32_t TX = 2 * 64 * RB + 4 * SB;
   constexpr float L2E = 1.4426950408889634f;
   constexpr float PRESCALE = float(1 << PvPrescale<BITS>::log2);
-  constexpr int GB = NG < 4 ? NG : 4;           // groups whose MMA chains run interleaved
+  constexpr int GB = NG < 8 ? NG : 8;           // groups whose MMA chains run interleaved
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3, rq = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -375,50 +375,50 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   bool dead = false;
   const int g_pv = warp;                        // PV group of this warp
-  int st = 0, phase = 0;
-
-  for (int it = 0; it < tr.n_my; ++it) {
-    const int buf = it & 1;
-    if (!dead && !mbar_wait(&full[st], phase)) {
+  // Tiles flow through a two-deep software pipeline: while PV of tile i runs,
+  // the same warp already computes QK of tile i+1, so the tensor cores always
+  // have two independent streams of MMAs from every warp.
+  int cons_st = 0, cons_phase = 0;               // stage / parity of the next tile to wait for
+  auto wait_next = [&]() -> int {
+    const int stg = cons_st;
+    if (!dead && !mbar_wait(&full[stg], cons_phase)) {
       dead = true;
       flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
     }
-    const uint8_t* Ks = stages + st * STB;
-    const uint8_t* Vs = Ks + 8 * CS;
-    const uint16_t* sks = reinterpret_cast<const uint16_t*>(Ks + 16 * CS);
-    const uint16_t* skb = sks + 64 * NG;
-    const uint16_t* svs = skb + 64 * NG;
+    if (++cons_st == nst) { cons_st = 0; cons_phase ^= 1; }
+    return stg;
+  };
+
+  // V scale/bias of tile `ti` as f16 pairs of consecutive keys (scale
+  // pre-multiplied by PRESCALE), zero for keys outside the window
+  auto build_vsb = [&](const uint8_t* stage, int ti, int bf) {
+    const uint16_t* svs = reinterpret_cast<const uint16_t*>(stage + 16 * CS) + 2 * 64 * NG;
     const uint16_t* svb = svs + 64 * NG;
-    const int tpos0 = (tr.t_begin + it) * kTileKeys;
-    const bool inner = tpos0 >= tr.lo && tpos0 + kTileKeys - 1 <= tr.hi;   // no masked key
-
-    // ---- V scale/bias of this tile as f16 pairs of consecutive keys (scale
-    // pre-multiplied by PRESCALE), zero for keys outside the window ----
-    {
-      uint32_t* vs16 = vsb + buf * 2 * NG * 32;
+    const int tpos0 = (tr.t_begin + ti) * kTileKeys;
+    uint32_t* vs16 = vsb + bf * 2 * NG * 32;
 #pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int idx = threadIdx.x + rep * NW * 32;          // 2 * NG * 32 entries = 2 per thread
-        const int which = idx / (NG * 32);                    // 0: scale, 1: bias
-        const int rem = idx % (NG * 32);
-        const int g = rem / 32, pr = rem % 32;
-        const int k0 = 2 * pr;
-        const uint16_t* srcp = which == 0 ? svs : svb;
-        const float mul = which == 0 ? PRESCALE : 1.f;
-        float x0 = bf16_to_f(srcp[k0 * NG + g]) * mul;
-        float x1 = bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul;
-        if (!inner) {
-          if (tpos0 + k0 < tr.lo || tpos0 + k0 > tr.hi) x0 = 0.f;
-          if (tpos0 + k0 + 1 < tr.lo || tpos0 + k0 + 1 > tr.hi) x1 = 0.f;
-        }
-        vs16[which * NG * 32 + g * 32 + pr] = pack_h2(x0, x1);
-      }
+    for (int rep = 0; rep < 2; ++rep) {
+      const int idx = threadIdx.x + rep * NW * 32;          // 2 * NG * 32 entries = 2 per thread
+      const int which = idx / (NG * 32);                    // 0: scale, 1: bias
+      const int rem = idx % (NG * 32);
+      const int g = rem / 32, pr = rem % 32;
+      const int k0 = 2 * pr;
+      const uint16_t* srcp = which == 0 ? svs : svb;
+      const float mul = which == 0 ? PRESCALE : 1.f;
+      const int kp = tpos0 + k0;
+      const float x0 = (kp >= tr.lo && kp <= tr.hi) ? bf16_to_f(srcp[k0 * NG + g]) * mul : 0.f;
+      const float x1 = (kp + 1 >= tr.lo && kp + 1 <= tr.hi) ? bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul : 0.f;
+      vs16[which * NG * 32 + g * 32 + pr] = pack_h2(x0, x1);
     }
+  };
 
-    // ---- QK: this warp's NTQ n-tiles (keys of slot j, one per chunk), all q
-    // heads, full head_dim ----
-    float S[NTQ][4];
-    float tmax[2] = {-INFINITY, -INFINITY};
+  // QK of tile `ti`: this warp's NTQ n-tiles (keys of slot j, one per chunk),
+  // all q heads, full head_dim; masked keys get -inf.  Returns the row maxima.
+  auto qk = [&](const uint8_t* stage, int ti, float (&S)[NTQ][4], float (&tmax)[2]) {
+    const uint16_t* sks = reinterpret_cast<const uint16_t*>(stage + 16 * CS);
+    const uint16_t* skb = sks + 64 * NG;
+    const int tpos0 = (tr.t_begin + ti) * kTileKeys;
+    tmax[0] = tmax[1] = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
       const int j = warp * NTQ + nt;
@@ -429,7 +429,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const int kB = 8 * rq + j;
         uint32_t bb = 0;
         if constexpr (NG == 1) {       // one group: a single bf16 (2-byte aligned only)
-          if (t4 == 0) bb = pack_h2(bf16_to_f(skb[kB]), 0.f);
+          bb = t4 == 0 ? pack_h2(bf16_to_f(skb[kB]), 0.f) : 0u;
         } else {
           if (2 * t4 < NG) {           // an aligned pair of groups 2*t4, 2*t4+1
             const uint32_t w = *reinterpret_cast<const uint32_t*>(skb + kB * NG + 2 * t4);
@@ -443,7 +443,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       uint32_t sw0[(NG + 1) / 2], sw1[(NG + 1) / 2];
       load_bf16_row<NG>(sks + kc0 * NG, sw0);
       load_bf16_row<NG>(sks + (kc0 + 8) * NG, sw1);
-      const uint8_t* krow = Ks + rq * CS + j * RB + t4 * (BITS * 2);
+      const uint8_t* krow = stage + rq * CS + j * RB + t4 * (BITS * 2);
       float T[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int g0 = 0; g0 < NG; g0 += GB) {
@@ -489,13 +489,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         }
       }
       // the code products are in units of 2^-24
-#pragma unroll
-      for (int e = 0; e < 4; ++e) S[nt][e] = fmaf(T[e], kTwo24, Sb[e]);
-      if (!inner) {
-        const int kp = tpos0 + kc0;
-        if (kp < tr.lo || kp > tr.hi) { S[nt][0] = -INFINITY; S[nt][2] = -INFINITY; }
-        if (kp + 8 < tr.lo || kp + 8 > tr.hi) { S[nt][1] = -INFINITY; S[nt][3] = -INFINITY; }
-      }
+      const int kp = tpos0 + kc0;
+      const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 8 >= tr.lo && kp + 8 <= tr.hi;
+      S[nt][0] = v0 ? fmaf(T[0], kTwo24, Sb[0]) : -INFINITY;
+      S[nt][1] = v1 ? fmaf(T[1], kTwo24, Sb[1]) : -INFINITY;
+      S[nt][2] = v0 ? fmaf(T[2], kTwo24, Sb[2]) : -INFINITY;
+      S[nt][3] = v1 ? fmaf(T[3], kTwo24, Sb[3]) : -INFINITY;
       tmax[0] = fmaxf(tmax[0], fmaxf(S[nt][0], S[nt][1]));
       tmax[1] = fmaxf(tmax[1], fmaxf(S[nt][2], S[nt][3]));
     }
@@ -504,26 +503,25 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], m));
       tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], m));
     }
-    float* redb = red + buf * NW * 16;
-    if (t4 == 0) { redb[rq * NW + warp] = tmax[0]; redb[(rq + 8) * NW + warp] = tmax[1]; }
-    named_bar(1, NW * 32);
-    // every warp has finished tile it-1: its stage takes the next tile
-    if (it >= 1 && issued < tr.n_my) {
-      issue(issue_st, issue_slot);
-      if (++issue_st == nst) issue_st = 0;
-      if (++issue_slot == cap_tiles) issue_slot = 0;
-      ++issued;
-    }
+  };
 
-    // ---- softmax update ----
-    float m_new[2], alpha[2];
+  auto post_max = [&](const float (&tmax)[2], int bf) {
+    float* redb = red + bf * NW * 16;
+    if (t4 == 0) { redb[rq * NW + warp] = tmax[0]; redb[(rq + 8) * NW + warp] = tmax[1]; }
+  };
+
+  // after the max exchange: new running max, P (f16) of this warp's keys into
+  // the P buffer, running sums; returns the rescale factors of the old state
+  auto softmax = [&](const float (&S)[NTQ][4], int bf, float (&alpha)[2]) {
+    const float* redb = red + bf * NW * 16;
+    float m_new[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const float mt = max_over_warps<NW>(redb + (rq + 8 * h) * NW);
       m_new[h] = fmaxf(m_run[h], mt);
       alpha[h] = m_new[h] == -INFINITY ? 1.f : exp2f((m_run[h] - m_new[h]) * L2E);
     }
-    uint8_t* Pb = Pbuf + buf * (16 * 64 * 2);
+    uint8_t* Pb = Pbuf + bf * (16 * 64 * 2);
     float lsum[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
@@ -546,9 +544,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) { l_run[h] = l_run[h] * alpha[h] + lsum[h]; m_run[h] = m_new[h]; }
-    named_bar(1, NW * 32);
+  };
 
-    // ---- PV for this warp's 64-dim group: O += (P * scale) codes + P bias ----
+  auto rescale = [&](const float (&alpha)[2]) {
     if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
@@ -557,10 +555,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       }
       cb[0] *= alpha[0]; cb[1] *= alpha[0]; cb[2] *= alpha[1]; cb[3] *= alpha[1];
     }
-    const uint32_t* vs16 = vsb + buf * 2 * NG * 32 + g_pv * 32;
+  };
+
+  // PV of one tile for this warp's 64-dim group: O += (P * scale) codes + P bias
+  auto pv = [&](const uint8_t* stage, int bf) {
+    const uint8_t* Pb = Pbuf + bf * (16 * 64 * 2);
+    const uint32_t* vs16 = vsb + bf * 2 * NG * 32 + g_pv * 32;
     const uint32_t* vb16 = vs16 + NG * 32;
     // this lane's B rows: k = 2*t4 (+1) -> chunk t4, k = 2*t4 + 8 (+1) -> chunk t4 + 4
-    const uint8_t* vlo = Vs + t4 * CS + (BITS == 4 ? g_pv * 32 + rq * 4 : g_pv * 64 + rq * 8);
+    const uint8_t* vlo = stage + 8 * CS + t4 * CS + (BITS == 4 ? g_pv * 32 + rq * 4 : g_pv * 64 + rq * 8);
     const uint8_t* vhi = vlo + 4 * CS;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
@@ -605,8 +608,47 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         }
       }
     }
-    if (++st == nst) { st = 0; phase ^= 1; }
+  };
+
+  auto refill = [&]() {
+    if (issued < tr.n_my) {
+      issue(issue_st, issue_slot);
+      if (++issue_st == nst) issue_st = 0;
+      if (++issue_slot == cap_tiles) issue_slot = 0;
+      ++issued;
+    }
+  };
+
+  // ---- pipeline prologue: scores and P of tile 0 ----
+  float S[NTQ][4], tmax[2], alpha[2];
+  int cur_st = wait_next();
+  {
+    const uint8_t* stage = stages + cur_st * STB;
+    build_vsb(stage, 0, 0);
+    qk(stage, 0, S, tmax);
+    post_max(tmax, 0);
+    named_bar(1, NW * 32);
+    softmax(S, 0, alpha);
+    named_bar(1, NW * 32);
   }
+  // ---- steady state: QK(it+1) alongside PV(it) ----
+  for (int it = 0; it + 1 < tr.n_my; ++it) {
+    const int bf = it & 1;
+    const int nxt_st = wait_next();
+    const uint8_t* nstage = stages + nxt_st * STB;
+    build_vsb(nstage, it + 1, bf ^ 1);
+    qk(nstage, it + 1, S, tmax);
+    pv(stages + cur_st * STB, bf);
+    post_max(tmax, bf ^ 1);
+    named_bar(1, NW * 32);
+    // every warp is done with tile it: its stage takes the next tile
+    refill();
+    softmax(S, bf ^ 1, alpha);
+    rescale(alpha);
+    named_bar(1, NW * 32);
+    cur_st = nxt_st;
+  }
+  pv(stages + cur_st * STB, (tr.n_my - 1) & 1);
   pdl_launch();
   // a timed-out wait may leave copies in flight: they must land before exit
   if (dead && threadIdx.x == 0)
