@@ -43,20 +43,26 @@ struct Dec {
 
 constexpr int kMaxStages = 8;
 
-// Shared-memory stage of one 64-key tile.  The K (then V) code rows arrive as
-// 8 chunks of 8 consecutive keys, each chunk one bulk copy of 8 rows followed
-// by 32 bytes of padding; chunk c starts 32*c bytes (mod 128) into the bank
-// space, so rows of different chunks fall on different banks.  Then the four
-// 64 x (D/64) bf16 blocks: K scales, K biases, V scales, V biases.
+// Shared memory holds a ring of stages; a stage is one 64-key tile, a K slot
+// followed by a V slot.  A slot's code rows arrive as 4 chunks of 16
+// consecutive keys, each chunk one bulk copy of 16 rows followed by 32 bytes
+// of padding (chunk c starts 32*c bytes, mod 128, into the bank space, so rows
+// of different chunks fall on different banks), then the 64 x (D/64) bf16
+// scale block and the bias block.
 __host__ __device__ constexpr int row_bytes(int D, int bits) { return D * bits / 8; }
-__host__ __device__ constexpr int chunk_stride(int D, int bits) { return 8 * row_bytes(D, bits) + 32; }
+__host__ __device__ constexpr int chunk_stride(int D, int bits) { return 16 * row_bytes(D, bits) + 32; }
 __host__ __device__ constexpr int sb_bytes(int D) { return 64 * (D / 64) * 2; }
-__host__ __device__ constexpr int stage_bytes(int D, int bits) { return 16 * chunk_stride(D, bits) + 4 * sb_bytes(D); }
+__host__ __device__ constexpr int slot_bytes(int D, int bits) { return 4 * chunk_stride(D, bits) + 2 * sb_bytes(D); }
 __host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
-// control block: mbarriers, max-exchange [2][16][NW], l-exchange [16][NW] (floats),
-// V scale/bias f16 pairs [2][2][NG][32] (words)
-__host__ __device__ constexpr int ctrl_bytes(int D) { return align128(128 + (3 * (D / 64) * 16) * 4 + 2 * 2 * (D / 64) * 32 * 4); }
-__host__ __device__ constexpr int stage0_off(int D) { return ctrl_bytes(D) + 2 * 16 * 64 * 2; }
+// control block: kMaxStages mbarriers (16 reserved), max-exchange
+// [2][16][NW] and l-exchange [16][NW] (floats)
+__host__ __device__ constexpr int ctrl_bytes(int D) { return align128(16 * 8 + (3 * (D / 64) * 16) * 4); }
+__host__ __device__ constexpr int slot0_off(int D) { return ctrl_bytes(D) + 2 * 16 * 64 * 2; }
+// stages for a given dynamic shared-memory size
+__host__ __device__ constexpr int ring_slots(int D, int bits, int smem) {
+  return (smem - slot0_off(D)) / (2 * slot_bytes(D, bits)) < kMaxStages
+             ? (smem - slot0_off(D)) / (2 * slot_bytes(D, bits)) : kMaxStages;
+}
 
 __device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -265,15 +271,15 @@ __device__ __forceinline__ float bf16_word_at(const uint32_t (&w)[(NG + 1) / 2],
 // that it stays clear of the f16 subnormal range; divided out at the end.
 template <int BITS> struct PvPrescale { static constexpr int log2 = BITS == 4 ? 2 : 6; };
 
-// Key mapping inside a tile (keys 8c + s: chunk c, slot s).
-//   QK n-tile j (0..7) holds the keys of slot j, column n = chunk n; its B
-//   fragment rows therefore sit in eight different chunks.
-//   PV k-step kk (0..3) holds slots 2kk and 2kk+1; MMA k index
-//   2*t + b + 8*a (t < 4, a, b < 2) is key 8*(t + 4a) + 2kk + b, and P is
-//   stored in this order (column = 16*kk + k index).
+// Key mapping inside a tile (key 16c + s: chunk c < 4, slot s < 16).
+//   QK n-tile j (0..7): column n is key 16*(n & 3) + 2j + (n >> 2), so the
+//   eight B fragment rows sit in four chunks, two per chunk.
+//   PV k-step kk (0..3): MMA k index 2t + b + 8a (t < 4, a, b < 2) is key
+//   16t + 4kk + 2a + b, and P is stored in this order (column = 16*kk + k).
+__device__ __forceinline__ int qk_key(int n, int j) { return 16 * (n & 3) + 2 * j + (n >> 2); }
 __device__ __forceinline__ int pv_col(int key) {
-  const int c = key >> 3, s = key & 7;
-  return (s >> 1) * 16 + 2 * (c & 3) + (s & 1) + 8 * (c >> 2);
+  const int c = key >> 4, s = key & 15;
+  return (s >> 2) * 16 + 2 * c + (s & 1) + 8 * ((s >> 1) & 1);
 }
 
 template <int NW>
@@ -301,52 +307,55 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
                                             const int split) {
   using C = Dec<D>;
   constexpr int NG = C::NG, NW = C::NW, NTQ = C::NTQ;
+  static_assert(NW == NG, "one PV warp per 64-dim group");
   constexpr int RB = row_bytes(D, BITS), CS = chunk_stride(D, BITS), SB = sb_bytes(D);
-  constexpr int STB = stage_bytes(D, BITS);
-  constexpr uint32_t TX = 2 * 64 * RB + 4 * SB;
+  constexpr int SLB = slot_bytes(D, BITS);
+  constexpr uint32_t TX = 64 * RB + 2 * SB;     // bytes of one slot
   constexpr float L2E = 1.4426950408889634f;
   constexpr float PRESCALE = float(1 << PvPrescale<BITS>::log2);
   constexpr int GB = NG < 8 ? NG : 8;           // groups whose MMA chains run interleaved
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3, rq = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 128);        // [2][16][NW] tile max exchange
+  float* red = reinterpret_cast<float*>(smem + 16 * 8);     // [2][16][NW] tile max exchange
   float* lred = red + 2 * NW * 16;                          // [16][NW]
-  uint32_t* vsb = reinterpret_cast<uint32_t*>(lred + NW * 16);  // [2][2][NG][32] f16 pairs of V scale/bias
   uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
-  uint8_t* stages = smem + stage0_off(D);
+  uint8_t* stages = smem + slot0_off(D);                    // stage i: K slot, then V slot
   const int cap_tiles = c.capacity / kTileKeys;
   const size_t head_row0 = (size_t)kvh * c.capacity;
 
-  // Copies of one tile: 8 K chunks, 8 V chunks, 4 scale/bias blocks, spread
-  // over the warps (copy j is issued by lane j / NW of warp j % NW).
+  // Copies of one stage: per side 4 code chunks, the scale block and the bias
+  // block; K copies by copy ids 0..5, V copies by 6..11 (copy id j is lane
+  // j / NW of warp j % NW).  A stage is refilled only after a block barrier
+  // that follows every read of its previous contents.
   const int my_copy = lane * NW + warp;
   auto issue = [&](int st, int slot_tile) {
-    uint8_t* sb = stages + st * STB;
-    const size_t r0 = head_row0 + (size_t)slot_tile * kTileKeys;
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(&full[st], TX);
-    if (my_copy < 20) {
-      fence_proxy_async();      // this CTA's earlier generic reads of the stage come first
-      if (my_copy < 16) {
-        const int ch = my_copy & 7;
-        const uint32_t* src = my_copy < 8 ? c.k_codes : c.v_codes;
-        bulk_g2s(sb + my_copy * CS, reinterpret_cast<const uint8_t*>(src) + (r0 + 8 * ch) * RB, 8 * RB, &full[st]);
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&full[st], 2 * TX);
+    if (my_copy < 12) {
+      const bool v_side = my_copy >= 6;
+      const int j = my_copy - (v_side ? 6 : 0);
+      uint8_t* sl = stages + (2 * st + (v_side ? 1 : 0)) * SLB;
+      const size_t r0 = head_row0 + (size_t)slot_tile * kTileKeys;
+      if (j < 4) {
+        const uint32_t* src = v_side ? c.v_codes : c.k_codes;
+        bulk_g2s(sl + j * CS, reinterpret_cast<const uint8_t*>(src) + (r0 + 16 * j) * RB, 16 * RB, &full[st]);
       } else {
-        const int q = my_copy - 16;
-        const uint16_t* src = q == 0 ? c.k_scales : q == 1 ? c.k_biases : q == 2 ? c.v_scales : c.v_biases;
-        bulk_g2s(sb + 16 * CS + q * SB, src + r0 * NG, SB, &full[st]);
+        const uint16_t* src = j == 4 ? (v_side ? c.v_scales : c.k_scales) : (v_side ? c.v_biases : c.k_biases);
+        bulk_g2s(sl + 4 * CS + (j - 4) * SB, src + r0 * NG, SB, &full[st]);
       }
     }
   };
-  // prologue: fill every stage (the cache was written before this launch)
-  int issued = min(nst, tr.n_my);
-  int issue_st = 0;
-  int issue_slot = tr.t_begin % cap_tiles;
-  for (int i = 0; i < issued; ++i) {
-    issue(issue_st, issue_slot);
-    if (++issue_st == nst) issue_st = 0;
-    if (++issue_slot == cap_tiles) issue_slot = 0;
-  }
+  int issued = 0, issue_st = 0, issue_slot = tr.t_begin % cap_tiles;
+  auto refill = [&]() {
+    if (issued < tr.n_my) {
+      issue(issue_st, issue_slot);
+      if (++issue_st == nst) issue_st = 0;
+      if (++issue_slot == cap_tiles) issue_slot = 0;
+      ++issued;
+    }
+  };
+  // prologue: fill the ring (the cache was written before this launch)
+  for (int i = 0; i < nst; ++i) refill();
 
   pdl_wait();                                   // q fragments come from qprep_kernel
   // QK A fragments (q heads x permuted head_dim) and the bias-term A fragment
@@ -354,8 +363,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   uint32_t qa[NG][4][4];
   uint32_t qb[4];
   {
-    const size_t rk = (size_t)row * a.L.n_kv + kvh;
-    const uint4* src = a.ws.qfrag + rk * NG * 4 * 32;
+    const size_t rkv = (size_t)row * a.L.n_kv + kvh;
+    const uint4* src = a.ws.qfrag + rkv * NG * 4 * 32;
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
@@ -363,7 +372,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const uint4 v = src[(g * 4 + ks) * 32 + lane];
         qa[g][ks][0] = v.x; qa[g][ks][1] = v.y; qa[g][ks][2] = v.z; qa[g][ks][3] = v.w;
       }
-    const uint4 v = a.ws.qbias[rk * 32 + lane];
+    const uint4 v = a.ws.qbias[rkv * 32 + lane];
     qb[0] = v.x; qb[1] = v.y; qb[2] = v.z; qb[3] = v.w;
   }
 
@@ -375,47 +384,45 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   bool dead = false;
   const int g_pv = warp;                        // PV group of this warp
+
   // Tiles flow through a two-deep software pipeline: while PV of tile i runs,
   // the same warp already computes QK of tile i+1, so the tensor cores always
   // have two independent streams of MMAs from every warp.
-  int cons_st = 0, cons_phase = 0;               // stage / parity of the next tile to wait for
-  auto wait_next = [&]() -> int {
+  int cons_st = 0, cons_phase = 0;
+  auto wait_stage = [&]() -> const uint8_t* {
     const int stg = cons_st;
     if (!dead && !mbar_wait(&full[stg], cons_phase)) {
       dead = true;
       flag_error(a.ws.status, KVQ_DEV_TIMEOUT);
     }
     if (++cons_st == nst) { cons_st = 0; cons_phase ^= 1; }
-    return stg;
+    return stages + 2 * stg * SLB;
   };
 
-  // V scale/bias of tile `ti` as f16 pairs of consecutive keys (scale
-  // pre-multiplied by PRESCALE), zero for keys outside the window
-  auto build_vsb = [&](const uint8_t* stage, int ti, int bf) {
-    const uint16_t* svs = reinterpret_cast<const uint16_t*>(stage + 16 * CS) + 2 * 64 * NG;
+  // V scale/bias of tile `ti`, this warp's group, as f16 pairs of consecutive
+  // keys (scale pre-multiplied by PRESCALE), zero for keys outside the window.
+  // Lane l forms pair l (keys 2l, 2l+1); PV lane (rq, t4) needs pairs
+  // 8*t4 + m (m < 8), fetched by shuffles: sv[m], bv[m].
+  auto build_vsb = [&](const uint8_t* vslot, int ti, uint32_t (&sv)[8], uint32_t (&bv)[8]) {
+    const uint16_t* svs = reinterpret_cast<const uint16_t*>(vslot + 4 * CS);
     const uint16_t* svb = svs + 64 * NG;
-    const int tpos0 = (tr.t_begin + ti) * kTileKeys;
-    uint32_t* vs16 = vsb + bf * 2 * NG * 32;
+    const int kp = (tr.t_begin + ti) * kTileKeys + 2 * lane;
+    const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 1 >= tr.lo && kp + 1 <= tr.hi;
+    const int i0 = 2 * lane * NG + g_pv;
+    const float s0 = v0 ? bf16_to_f(svs[i0]) * PRESCALE : 0.f, s1 = v1 ? bf16_to_f(svs[i0 + NG]) * PRESCALE : 0.f;
+    const float b0 = v0 ? bf16_to_f(svb[i0]) : 0.f, b1 = v1 ? bf16_to_f(svb[i0 + NG]) : 0.f;
+    const uint32_t sp = pack_h2(s0, s1), bp = pack_h2(b0, b1);
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int idx = threadIdx.x + rep * NW * 32;          // 2 * NG * 32 entries = 2 per thread
-      const int which = idx / (NG * 32);                    // 0: scale, 1: bias
-      const int rem = idx % (NG * 32);
-      const int g = rem / 32, pr = rem % 32;
-      const int k0 = 2 * pr;
-      const uint16_t* srcp = which == 0 ? svs : svb;
-      const float mul = which == 0 ? PRESCALE : 1.f;
-      const int kp = tpos0 + k0;
-      const float x0 = (kp >= tr.lo && kp <= tr.hi) ? bf16_to_f(srcp[k0 * NG + g]) * mul : 0.f;
-      const float x1 = (kp + 1 >= tr.lo && kp + 1 <= tr.hi) ? bf16_to_f(srcp[(k0 + 1) * NG + g]) * mul : 0.f;
-      vs16[which * NG * 32 + g * 32 + pr] = pack_h2(x0, x1);
+    for (int m = 0; m < 8; ++m) {
+      sv[m] = __shfl_sync(0xffffffffu, sp, 8 * t4 + m);
+      bv[m] = __shfl_sync(0xffffffffu, bp, 8 * t4 + m);
     }
   };
 
   // QK of tile `ti`: this warp's NTQ n-tiles (keys of slot j, one per chunk),
   // all q heads, full head_dim; masked keys get -inf.  Returns the row maxima.
   auto qk = [&](const uint8_t* stage, int ti, float (&S)[NTQ][4], float (&tmax)[2]) {
-    const uint16_t* sks = reinterpret_cast<const uint16_t*>(stage + 16 * CS);
+    const uint16_t* sks = reinterpret_cast<const uint16_t*>(stage + 4 * CS);
     const uint16_t* skb = sks + 64 * NG;
     const int tpos0 = (tr.t_begin + ti) * kTileKeys;
     tmax[0] = tmax[1] = -INFINITY;
@@ -423,10 +430,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     for (int nt = 0; nt < NTQ; ++nt) {
       const int j = warp * NTQ + nt;
       // bias term: sum_g qsum[h][g] * bias[key][g] as one MMA (k = group for
-      // the hi part, 8 + group for the lo part); B column rq is key 8*rq + j
+      // the hi part, 8 + group for the lo part); B column rq is key qk_key(rq, j)
       float Sb[4];
+      const int kB = qk_key(rq, j);
       {
-        const int kB = 8 * rq + j;
         uint32_t bb = 0;
         if constexpr (NG == 1) {       // one group: a single bf16 (2-byte aligned only)
           bb = t4 == 0 ? pack_h2(bf16_to_f(skb[kB]), 0.f) : 0u;
@@ -438,12 +445,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         }
         mma_f16_zc(Sb, qb, bb, bb);
       }
-      // S columns 2*t4 and 2*t4+1 are keys 16*t4 + j and 16*t4 + 8 + j
-      const int kc0 = 16 * t4 + j;
+      // S columns 2*t4 and 2*t4+1
+      const int kc0 = qk_key(2 * t4, j), kc1 = qk_key(2 * t4 + 1, j);
       uint32_t sw0[(NG + 1) / 2], sw1[(NG + 1) / 2];
       load_bf16_row<NG>(sks + kc0 * NG, sw0);
-      load_bf16_row<NG>(sks + (kc0 + 8) * NG, sw1);
-      const uint8_t* krow = stage + rq * CS + j * RB + t4 * (BITS * 2);
+      load_bf16_row<NG>(sks + kc1 * NG, sw1);
+      const uint8_t* krow = stage + (kB >> 4) * CS + (kB & 15) * RB + t4 * (BITS * 2);
       float T[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int g0 = 0; g0 < NG; g0 += GB) {
@@ -489,8 +496,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         }
       }
       // the code products are in units of 2^-24
-      const int kp = tpos0 + kc0;
-      const bool v0 = kp >= tr.lo && kp <= tr.hi, v1 = kp + 8 >= tr.lo && kp + 8 <= tr.hi;
+      const int kp0 = tpos0 + kc0, kp1 = tpos0 + kc1;
+      const bool v0 = kp0 >= tr.lo && kp0 <= tr.hi, v1 = kp1 >= tr.lo && kp1 <= tr.hi;
       S[nt][0] = v0 ? fmaf(T[0], kTwo24, Sb[0]) : -INFINITY;
       S[nt][1] = v1 ? fmaf(T[1], kTwo24, Sb[1]) : -INFINITY;
       S[nt][2] = v0 ? fmaf(T[2], kTwo24, Sb[2]) : -INFINITY;
@@ -526,7 +533,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
       const int j = warp * NTQ + nt;
-      const int col0 = pv_col(16 * t4 + j), col1 = pv_col(16 * t4 + 8 + j);
+      const int col0 = pv_col(qk_key(2 * t4, j)), col1 = pv_col(qk_key(2 * t4 + 1, j));
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float p0 = 0.f, p1 = 0.f;
@@ -558,13 +565,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   };
 
   // PV of one tile for this warp's 64-dim group: O += (P * scale) codes + P bias
-  auto pv = [&](const uint8_t* stage, int bf) {
+  auto pv = [&](const uint8_t* vslot, int bf, const uint32_t (&sv)[8], const uint32_t (&bv)[8]) {
     const uint8_t* Pb = Pbuf + bf * (16 * 64 * 2);
-    const uint32_t* vs16 = vsb + bf * 2 * NG * 32 + g_pv * 32;
-    const uint32_t* vb16 = vs16 + NG * 32;
-    // this lane's B rows: k = 2*t4 (+1) -> chunk t4, k = 2*t4 + 8 (+1) -> chunk t4 + 4
-    const uint8_t* vlo = stage + 8 * CS + t4 * CS + (BITS == 4 ? g_pv * 32 + rq * 4 : g_pv * 64 + rq * 8);
-    const uint8_t* vhi = vlo + 4 * CS;
+    // this lane's B rows (k = 2*t4 + b + 8a) are keys 16*t4 + 4kk + 2a + b: all in chunk t4
+    const uint8_t* vrow = vslot + t4 * CS + (BITS == 4 ? g_pv * 32 + rq * 4 : g_pv * 64 + rq * 8);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
@@ -574,17 +578,18 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         const int chunk = (kk * 2 + (mtx >> 1)) ^ (prow & 7);
         ldmatrix_x4(pa, Pb + prow * 128 + chunk * 16);
       }
-      // key pairs (8*t4 + 2kk, +1) and (8*(t4+4) + 2kk, +1)
-      const uint32_t sAB = vs16[4 * t4 + kk], sCD = vs16[16 + 4 * t4 + kk];
+      // key pairs (16*t4 + 4kk, +1) and (16*t4 + 4kk + 2, +3): pairs 8*t4 + 2kk, +1
+      const uint32_t sAB = sv[2 * kk], sCD = sv[2 * kk + 1];
       // bias column: only B column 0 (lanes 0..3) is non-zero
-      const uint32_t bAB = rq == 0 ? vb16[4 * t4 + kk] : 0u, bCD = rq == 0 ? vb16[16 + 4 * t4 + kk] : 0u;
+      const uint32_t bAB = rq == 0 ? bv[2 * kk] : 0u, bCD = rq == 0 ? bv[2 * kk + 1] : 0u;
       mma_f16(cb, pa, bAB, bCD);
       const uint32_t ps[4] = {h2_mul(pa[0], sAB), h2_mul(pa[1], sAB), h2_mul(pa[2], sCD), h2_mul(pa[3], sCD)};
+      const uint8_t* vk = vrow + 4 * kk * RB;
       if constexpr (BITS == 4) {
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vlo + (2 * kk) * RB);
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vlo + (2 * kk + 1) * RB);
-        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vhi + (2 * kk) * RB);
-        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vhi + (2 * kk + 1) * RB);
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vk);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vk + RB);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vk + 2 * RB);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vk + 3 * RB);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           // byte q of both keys into the low byte of each half
@@ -594,10 +599,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
           mma_f16(oacc[2 * q + 1], ps, sub_n1(xab), sub_n1(xcd));
         }
       } else {
-        const uint2 wa = *reinterpret_cast<const uint2*>(vlo + (2 * kk) * RB);
-        const uint2 wb = *reinterpret_cast<const uint2*>(vlo + (2 * kk + 1) * RB);
-        const uint2 wc = *reinterpret_cast<const uint2*>(vhi + (2 * kk) * RB);
-        const uint2 wd = *reinterpret_cast<const uint2*>(vhi + (2 * kk + 1) * RB);
+        const uint2 wa = *reinterpret_cast<const uint2*>(vk);
+        const uint2 wb = *reinterpret_cast<const uint2*>(vk + RB);
+        const uint2 wc = *reinterpret_cast<const uint2*>(vk + 2 * RB);
+        const uint2 wd = *reinterpret_cast<const uint2*>(vk + 3 * RB);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int bq = q & 3;
@@ -610,22 +615,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     }
   };
 
-  auto refill = [&]() {
-    if (issued < tr.n_my) {
-      issue(issue_st, issue_slot);
-      if (++issue_st == nst) issue_st = 0;
-      if (++issue_slot == cap_tiles) issue_slot = 0;
-      ++issued;
-    }
-  };
-
   // ---- pipeline prologue: scores and P of tile 0 ----
   float S[NTQ][4], tmax[2], alpha[2];
-  int cur_st = wait_next();
+  const uint8_t* cur = wait_stage();
   {
-    const uint8_t* stage = stages + cur_st * STB;
-    build_vsb(stage, 0, 0);
-    qk(stage, 0, S, tmax);
+    qk(cur, 0, S, tmax);
     post_max(tmax, 0);
     named_bar(1, NW * 32);
     softmax(S, 0, alpha);
@@ -634,21 +628,24 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   // ---- steady state: QK(it+1) alongside PV(it) ----
   for (int it = 0; it + 1 < tr.n_my; ++it) {
     const int bf = it & 1;
-    const int nxt_st = wait_next();
-    const uint8_t* nstage = stages + nxt_st * STB;
-    build_vsb(nstage, it + 1, bf ^ 1);
-    qk(nstage, it + 1, S, tmax);
-    pv(stages + cur_st * STB, bf);
+    const uint8_t* nxt = wait_stage();
+    uint32_t sv[8], bv[8];
+    build_vsb(cur + SLB, it, sv, bv);
+    qk(nxt, it + 1, S, tmax);
+    pv(cur + SLB, bf, sv, bv);
     post_max(tmax, bf ^ 1);
     named_bar(1, NW * 32);
-    // every warp is done with tile it: its stage takes the next tile
-    refill();
+    refill();                                   // every warp is done with tile it
     softmax(S, bf ^ 1, alpha);
     rescale(alpha);
     named_bar(1, NW * 32);
-    cur_st = nxt_st;
+    cur = nxt;
   }
-  pv(stages + cur_st * STB, (tr.n_my - 1) & 1);
+  {
+    uint32_t sv[8], bv[8];
+    build_vsb(cur + SLB, tr.n_my - 1, sv, bv);
+    pv(cur + SLB, (tr.n_my - 1) & 1, sv, bv);
+  }
   pdl_launch();
   // a timed-out wait may leave copies in flight: they must land before exit
   if (dead && threadIdx.x == 0)
@@ -724,9 +721,11 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
     return;
   }
   const int bits = c.bits;
-  const int nst = min(kMaxStages, (smem_total - stage0_off(D)) / stage_bytes(D, bits));
+  const int nst = ring_slots(D, bits, smem_total);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -794,7 +793,7 @@ combine_kernel(const DecodeArgs a) {
 }
 
 template <int D>
-int decode_smem_bytes() {
+constexpr int decode_smem_bytes() {
   // D = 512: one CTA per SM with the largest shared carve-out; smaller head
   // dims leave room for several CTAs per SM.
   return D >= 512 ? 227 * 1024 : (D == 256 ? 110 * 1024 : 56 * 1024);
@@ -803,6 +802,8 @@ int decode_smem_bytes() {
 template <int D>
 cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
   static_assert(D % 64 == 0, "");
+  static_assert(ring_slots(D, 8, decode_smem_bytes<D>()) >= 2 && ring_slots(D, 4, decode_smem_bytes<D>()) >= 2,
+                "the pipeline needs at least two stages");
   cudaError_t e;
   const int smem = decode_smem_bytes<D>();
   static bool attr_set[64] = {};
