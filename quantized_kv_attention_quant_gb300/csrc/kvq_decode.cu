@@ -517,19 +517,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     if (t4 == 0) { redb[rq * NW + warp] = tmax[0]; redb[(rq + 8) * NW + warp] = tmax[1]; }
   };
 
-  // after the max exchange: new running max, P (f16) of this warp's keys into
-  // the P buffer, running sums; returns the rescale factors of the old state
-  auto softmax = [&](const float (&S)[NTQ][4], int bf, float (&alpha)[2]) {
-    const float* redb = red + bf * NW * 16;
-    float m_new[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mt = max_over_warps<NW>(redb + (rq + 8 * h) * NW);
-      m_new[h] = fmaxf(m_run[h], mt);
-      alpha[h] = m_new[h] == -INFINITY ? 1.f : exp2f((m_run[h] - m_new[h]) * L2E);
-    }
+  // P (f16) = e^(S - ref) of this warp's keys into the P buffer; returns the
+  // row sums of the stored (rounded) values
+  auto store_p = [&](const float (&S)[NTQ][4], int bf, const float (&ref)[2], float (&lsum)[2]) {
     uint8_t* Pb = Pbuf + bf * (16 * 64 * 2);
-    float lsum[2] = {0.f, 0.f};
+    lsum[0] = lsum[1] = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NTQ; ++nt) {
       const int j = warp * NTQ + nt;
@@ -537,9 +529,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float p0 = 0.f, p1 = 0.f;
-        if (m_new[h] != -INFINITY) {
-          p0 = exp2f((S[nt][2 * h] - m_new[h]) * L2E);
-          p1 = exp2f((S[nt][2 * h + 1] - m_new[h]) * L2E);
+        if (ref[h] != -INFINITY) {
+          p0 = exp2f((S[nt][2 * h] - ref[h]) * L2E);
+          p1 = exp2f((S[nt][2 * h + 1] - ref[h]) * L2E);
         }
         const __half h0 = __float2half_rn(p0), h1 = __float2half_rn(p1);
         lsum[h] += __half2float(h0) + __half2float(h1);
@@ -549,6 +541,26 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
         *reinterpret_cast<__half*>(prw + (((col1 >> 3) ^ (prow & 7)) << 4) + (col1 & 7) * 2) = h1;
       }
     }
+  };
+
+  // after the max exchange: the tile's row maxima (every warp reads the same
+  // values, so anything derived from them is uniform over the block)
+  auto tile_max = [&](int bf, float (&mt)[2]) {
+    const float* redb = red + bf * NW * 16;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) mt[h] = max_over_warps<NW>(redb + (rq + 8 * h) * NW);
+  };
+
+  // exact online-softmax step: new running max, P against it, running sums;
+  // returns the rescale factors of the old state
+  auto softmax = [&](const float (&S)[NTQ][4], int bf, const float (&mt)[2], float (&alpha)[2]) {
+    float m_new[2], lsum[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m_new[h] = fmaxf(m_run[h], mt[h]);
+      alpha[h] = m_new[h] == -INFINITY ? 1.f : exp2f((m_run[h] - m_new[h]) * L2E);
+    }
+    store_p(S, bf, m_new, lsum);
 #pragma unroll
     for (int h = 0; h < 2; ++h) { l_run[h] = l_run[h] * alpha[h] + lsum[h]; m_run[h] = m_new[h]; }
   };
@@ -616,29 +628,44 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   };
 
   // ---- pipeline prologue: scores and P of tile 0 ----
-  float S[NTQ][4], tmax[2], alpha[2];
+  float S[NTQ][4], tmax[2], alpha[2], mt[2];
   const uint8_t* cur = wait_stage();
   {
     qk(cur, 0, S, tmax);
     post_max(tmax, 0);
     named_bar(1, NW * 32);
-    softmax(S, 0, alpha);
+    tile_max(0, mt);
+    softmax(S, 0, mt, alpha);
     named_bar(1, NW * 32);
   }
   // ---- steady state: QK(it+1) alongside PV(it) ----
+  // P of tile it+1 is formed before the max exchange against the running max
+  // (the same in every warp).  Scores up to kSlack above it keep P <= e^8,
+  // well inside f16 even after the V scale is folded in; then the exchange
+  // barrier also publishes P and nothing is rescaled.  A tile that exceeds the
+  // running max by more has P redone against its own maximum.
+  constexpr float kSlack = 8.f;
   for (int it = 0; it + 1 < tr.n_my; ++it) {
     const int bf = it & 1;
     const uint8_t* nxt = wait_stage();
     uint32_t sv[8], bv[8];
     build_vsb(cur + SLB, it, sv, bv);
     qk(nxt, it + 1, S, tmax);
+    float lsum[2];
+    store_p(S, bf ^ 1, m_run, lsum);
     pv(cur + SLB, bf, sv, bv);
     post_max(tmax, bf ^ 1);
     named_bar(1, NW * 32);
     refill();                                   // every warp is done with tile it
-    softmax(S, bf ^ 1, alpha);
-    rescale(alpha);
-    named_bar(1, NW * 32);
+    tile_max(bf ^ 1, mt);
+    if (__any_sync(0xffffffffu, mt[0] > m_run[0] + kSlack || mt[1] > m_run[1] + kSlack)) {
+      softmax(S, bf ^ 1, mt, alpha);
+      rescale(alpha);
+      named_bar(1, NW * 32);
+    } else {
+      l_run[0] += lsum[0];
+      l_run[1] += lsum[1];
+    }
     cur = nxt;
   }
   {
