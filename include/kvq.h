@@ -165,7 +165,13 @@ size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32
  * of the pages: prompt chunks and verify windows).  Row t of sequence s sits
  * at position p = start_pos[s] + (t - row_offsets[s]) and sees keys
  * max(0, p-window+1) .. p (0 .. p when window == 0), including the rows of
- * its own chunk up to itself.  Same arithmetic as attn_decode per row.
+ * its own chunk up to itself.  With head_dim <= 256 and G dividing 128 the
+ * rows run on the tcgen05 tensor cores, 128 (token, head) rows per block:
+ * QK as on attn_decode (exact codes, fp32 per-group scale), PV on v_hat =
+ * scale * code + bias rounded once to f16.  Other shapes use the attn_decode
+ * kernels row by row.
+ *
+ *   max_rows_per_seq must be >= the rows of every sequence (it sizes the grid).
  *
  *   row_offsets, start_pos, n_rows   as for kv_quant_append
  *   max_rows_per_seq                 host upper bound of rows per sequence

@@ -109,7 +109,7 @@ kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
 
 kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
                             const int32_t* row_offsets, const int32_t* pos, int32_t n_rows, int32_t max_keys,
-                            bool fixed_chunks,
+                            bool fixed_chunks, int32_t max_rows_per_seq,
                             const uint16_t* q_raw, const uint16_t* q_norm_w, void* out, int32_t out_is_f32,
                             uint16_t* q_prepped, void* workspace, size_t workspace_bytes, void* stream) {
   kvq::LayerArgs L;
@@ -128,9 +128,12 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   if (row_offsets) REQUIRE_PTR(row_offsets, "row_offsets", 4);
   if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
   if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
-  const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
+  // prompt chunks whose head shape fits the tensor-core kernel take it
+  const bool tc = row_offsets != nullptr && kvq::prefill_tc_supported(L);
+  const kvq::DecodePlan plan = tc ? kvq::DecodePlan{1, 0}
+                                  : kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
   const int splits = plan.splits;
-  const size_t need = kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
+  const size_t need = tc ? kvq::prefill_tc_ws_bytes(n_rows, L) : kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
   if (workspace_bytes < need)
     return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
   kvq::DecodeArgs a;
@@ -147,9 +150,15 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   a.q_prepped = q_prepped;
   a.splits = splits;
   a.chunk_tiles = plan.chunk_tiles;
-  a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, splits);
   const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
-  cudaError_t e = kvq::launch_decode(a, f, num_sms_current(), static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (tc) {
+    a.ws = kvq::prefill_tc_ws_carve(workspace, n_rows, L);
+    e = kvq::launch_prefill_tc(a, f, max_rows_per_seq, static_cast<cudaStream_t>(stream));
+  } else {
+    a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, splits);
+    e = kvq::launch_decode(a, f, num_sms_current(), static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return KVQ_OK;
 }
@@ -201,7 +210,7 @@ kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_
                        void* out, int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
                        size_t workspace_bytes, void* stream) {
   if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
-  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, q_raw, q_norm_w, out,
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, 0, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
@@ -221,14 +230,15 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
   if (max_rows_per_seq < 1 && n_rows > 0) return fail(KVQ_EINVAL, "max_rows_per_seq < 1");
   // each row reads at most window keys (full layers: the caller's positions)
   const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
-  return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, false, q_raw,
-                          q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
+  return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, false, max_rows_per_seq,
+                          q_raw, q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
                                     int32_t max_rows_per_seq) {
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || n_rows < 0 || max_rows_per_seq < 0) return 0;
+  if (kvq::prefill_tc_supported(L)) return kvq::prefill_tc_ws_bytes(n_rows, L);
   const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
   const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), false);
   return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan.splits);
@@ -296,7 +306,7 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
   int dev = 0;
   void* scratch = static_scratch_address(&dev);
   if (!scratch) return KVQ_ECUDA;
-  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, q_raw, q_norm_w, out,
+  return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, 0, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
 }
 

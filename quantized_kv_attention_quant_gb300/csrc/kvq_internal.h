@@ -41,6 +41,9 @@ struct DecodeWs {
   uint4* qbias;         // [n_rows][n_kv][32] x uint4: A fragment of the QK bias term
   float* part_o;        // [n_rows][n_kv][splits][16][D]
   float* part_ml;       // [n_rows][n_kv][splits][2][16]  (m, l)
+  // prompt-chunk tensor-core path only
+  uint16_t* q16;        // [n_rows][n_q][D] q_hat as f16
+  float* qsum;          // [n_rows][n_q][D/64] per-group sums of those f16 values
 };
 
 // Query rows of an attention call.  Decode: row i is sequence i at position
@@ -70,6 +73,12 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits);
 constexpr int kChunkTiles = 32;   // target tiles per split when the longest row is known
 struct DecodePlan { int splits, chunk_tiles; };
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks);
+
+// Prompt chunks on the tensor cores (tcgen05): head_dim <= 256 and G | 128.
+bool prefill_tc_supported(const LayerArgs& L);
+size_t prefill_tc_ws_bytes(int n_rows, const LayerArgs& L);
+DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L);
+cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st);
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
