@@ -667,7 +667,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  qprep_kernel<D, false><<<dim3(a.n_rows, a.L.n_kv, kMaxG), dim3(Qp<D>::THREADS), 0, st>>>(a, f);
+  int hpb = 1, nblk = 1;
+  qprep_shape<D>(a.L.n_q, hpb, nblk);
+  qprep_kernel<D, false><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH), 0, st>>>(a, f, hpb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   cudaLaunchAttribute attr[1];

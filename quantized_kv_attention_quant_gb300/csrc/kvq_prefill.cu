@@ -3,14 +3,17 @@
 // qNorm, RoPE at the cache offset, read.attend(q, 1.0) under the causal +
 // sliding-window mask; "Parity notes": SDPA scale 1.0, GQA).
 //
-// One CTA of 128 threads takes 128 query rows that share a kv head: 128/G
-// consecutive tokens of one sequence times its G q heads (thread r = token
-// r / G, head r % G).  It walks the keys its rows can see in 64-key tiles:
+// One CTA takes 128 query rows that share a kv head: 128/G consecutive tokens
+// of one sequence times its G q heads (row r = token r / G, head r % G), with
+// two threads per row (warps w and w + 4 reach the same tensor-memory lanes;
+// each takes half of the row's keys and output dims).  It walks the keys its
+// rows can see in 64-key tiles:
 //   1. TMA bulk copies bring the tile's packed codes and bf16 scale/bias
 //      blocks into a staging area (prefetched one tile ahead).
 //   2. All threads turn the K codes into f16 integers (exact) and the V codes
-//      into v_hat = scale * code + bias rounded once to f16 (written
-//      transposed with stmatrix so that keys run along the MMA's K).
+//      into v_hat = scale * code + bias, one f16 fma (written transposed with
+//      stmatrix so that keys run along the MMA's K).  V is converted while QK
+//      runs and the next tile's K while PV runs.
 //   3. One thread issues QK as one MMA chain per 64-dim group into tensor
 //      memory (M = 128 rows, N = 64 keys): S = sum_g scale_g * (q_g . codes_g)
 //      + sum_g bias_g * sum(q_g) keeps the QK product exact up to fp32
@@ -35,7 +38,8 @@ namespace kvq {
 
 namespace {
 
-constexpr int kRows = 128;   // MMA rows per CTA = threads per CTA
+constexpr int kRows = 128;      // MMA rows per CTA
+constexpr int kThreads = 256;   // two threads per row: warps w and w + 4 share tensor-memory lanes
 
 template <int D>
 struct Pf {
@@ -49,20 +53,23 @@ struct Pf {
   static constexpr int P_OFF = V_OFF + D * 128;         // [128 rows x 128 B]: P as f16
   static constexpr int S_OFF = P_OFF + 16384;           // staging: K codes, V codes, 4 scale/bias blocks
   static constexpr int STAGE = 2 * 64 * RB8 + 4 * SB;
-  static constexpr int T_OFF = S_OFF + STAGE;           // K scale, K bias as f32 [2][64][NG]
-  static constexpr int C_OFF = T_OFF + 2 * 64 * NG * 4; // 3 mbarriers and the tensor-memory address
+  static constexpr int T_OFF = S_OFF + STAGE;           // K scale, K bias as f32 [2][NG][64]
+  static constexpr int X_OFF = T_OFF + 2 * 64 * NG * 4; // row exchange between the two halves [2][128] f32
+  static constexpr int C_OFF = X_OFF + 2 * 128 * 4;     // 3 mbarriers and the tensor-memory address
   static constexpr int BYTES = C_OFF + 64 + 1024;       // + room to align the base
   static constexpr int TMEM_COLS = 2 * D;               // group products (NG x 64) then the output (D)
 };
 
+__device__ __forceinline__ uint32_t h2_fma_u(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 __device__ __forceinline__ uint32_t h2_sub_u(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 constexpr uint32_t kF16_1024 = 0x64006400u;            // (1024, 1024): OR-ing v < 1024 into the mantissa gives 1024 + v
 
-// exact float value of an integer code 0..255
-__device__ __forceinline__ float code_f(uint32_t c) { return __int_as_float(0x4B000000u | c) - 8388608.f; }
 
 template <int D, int BITS>
 __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, const kvq_seq_cache& c,
@@ -79,8 +86,9 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   uint64_t* bar_s = bar_tma + 1;
   uint64_t* bar_o = bar_tma + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P::C_OFF + 24);
-  float* skf = reinterpret_cast<float*>(sm + P::T_OFF);   // [64][NG]
-  float* bkf = skf + 64 * NG;
+  float* xr = reinterpret_cast<float*>(sm + P::X_OFF);    // [2][128] row exchange
+  float* skf = reinterpret_cast<float*>(sm + P::T_OFF);   // [NG][64] K scale as f32
+  float* bkf = skf + 64 * NG;                             // [NG][64] K bias as f32
   uint8_t* stg = sm + P::S_OFF;
   const uint8_t* stg_k = stg;
   const uint8_t* stg_v = stg + 64 * RB;
@@ -90,8 +98,9 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const uint16_t* stg_vb = stg_vs + 64 * NG;
   const uint32_t base = smem_u32(sm);
 
-  // ---- this thread's row and the CTA's key range ----
-  const int r = tid, tq = r / G, h = r % G;
+  // ---- this thread's row (half hf of its keys and output dims) and the CTA's key range ----
+  const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
+  const int tq = r / G, h = r % G;
   const int t = t0 + tq;
   const bool row_valid = t < rows_s;
   const int newest = start + rows_s - 1;
@@ -110,6 +119,8 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const size_t head_row0 = (size_t)kvh * cap;
   const int hq = kvh * G + h;
   const size_t grow = (size_t)__ldg(a.row_offsets + s) + t;     // global query row
+  const int kk0 = 32 * hf;                                // this thread's keys of a tile
+  const int dd0 = (D / 2) * hf;                           // this thread's output dims
 
   // 16-byte stores when the output allows them (the API asks only for element alignment)
   const bool out_vec = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
@@ -134,14 +145,14 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       o[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
   };
-  auto write_nan_row = [&]() {
+  auto write_nan_half = [&]() {
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __int_as_float(0x7fc00000);
-    for (int d0 = 0; d0 < D; d0 += 16) write_row(v, d0);
+    for (int d0 = dd0; d0 < dd0 + D / 2; d0 += 16) write_row(v, d0);
   };
   if (n_tiles == 0) {                                     // uniform over the CTA
-    if (row_valid) write_nan_row();
+    if (row_valid) write_nan_half();
     return;
   }
 
@@ -172,12 +183,13 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const uint32_t tmem = *tslot;
   if (tid == 0) issue_tile(0);
 
-  // Q rows as f16.  With 4-bit codes the K conversion yields the dims of each
-  // 8-dim chunk in the order 0 4 1 5 2 6 3 7; Q uses the same order.
+  // Q rows as f16 (each thread half of its row's chunks).  With 4-bit codes
+  // the K conversion yields the dims of each 8-dim chunk in the order
+  // 0 4 1 5 2 6 3 7; Q uses the same order.
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.ws.q16 + (grow * a.L.n_q + hq) * D);
 #pragma unroll 4
-    for (int ch = 0; ch < D / 8; ++ch) {
+    for (int ch = hf * (D / 16); ch < (hf + 1) * (D / 16); ++ch) {
       uint4 v = row_valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
       if (BITS == 4)
         v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
@@ -189,7 +201,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
 #pragma unroll
   for (int g = 0; g < NG; ++g) qsum[g] = row_valid ? a.ws.qsum[(grow * a.L.n_q + hq) * NG + g] : 0.f;
 
-  float m_ref = -INFINITY, l_sum = 0.f;
+  float m_ref = -INFINITY, l_part = 0.f;
   int ph_tma = 0, ph_s = 0, ph_o = 0;
   bool dead = false;
   auto wait = [&](uint64_t* bar, int& ph) {
@@ -199,20 +211,14 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     }
     ph ^= 1;
   };
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   constexpr uint32_t ID_QK = tc::idesc_f16_f32(128, 64);
   constexpr uint32_t ID_PV = tc::idesc_f16_f32(128, D);
 
-  for (int ti = 0; ti < n_tiles; ++ti) {
-    const int tpos0 = (tile_lo + ti) * kTileKeys;
-    wait(bar_tma, ph_tma);                                // codes of tile ti are in the staging area
-    if (ti > 0) {                                         // PV of tile ti-1 done: K, V and P buffers are free
-      wait(bar_o, ph_o);
-      tc::fence_after_sync();
-    }
-    // ---- K codes -> f16 integers, K scale/bias -> f32 ----
-#pragma unroll 4
-    for (int i = tid; i < 64 * D / 8; i += kRows) {
+  // K codes of the staged tile -> f16 integers; K scale/bias -> f32 tables
+  auto convert_k = [&]() {
+#pragma unroll 2
+    for (int i = tid; i < 64 * D / 8; i += kThreads) {
       const int key = i / (D / 8), ch = i % (D / 8);
       uint4 o;
       if constexpr (BITS == 4) {
@@ -230,13 +236,16 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       }
       *reinterpret_cast<uint4*>(sm + P::K_OFF + (ch >> 3) * 8192 + tc::sw128_off(key, ch & 7)) = o;
     }
-    for (int i = tid; i < 64 * NG; i += kRows) {
-      skf[i] = bf16_to_f(stg_ks[i]);
-      bkf[i] = bf16_to_f(stg_kb[i]);
+    for (int i = tid; i < 64 * NG; i += kThreads) {       // [key][g] -> [g][key]
+      const int key = i / NG, g = i % NG;
+      skf[g * 64 + key] = bf16_to_f(stg_ks[i]);
+      bkf[g * 64 + key] = bf16_to_f(stg_kb[i]);
     }
-    // ---- V: v_hat = scale * code + bias as f16, stored transposed (row = dim,
-    // 64 keys per row); keys outside the CTA's range are zero ----
-    for (int task = warp; task < 8 * (D / 32); task += kRows / 32) {
+  };
+  // V of the staged tile: v_hat = scale * code + bias (one f16 fma), stored
+  // transposed (row = dim, 64 keys per row); keys outside the CTA's range are zero
+  auto convert_v = [&](int tpos0) {
+    for (int task = warp; task < 8 * (D / 32); task += kThreads / 32) {
       const int kb = task & 7, db = task >> 3;
       const int key = 8 * kb + (lane >> 2);
       const int g = db >> 1;
@@ -244,29 +253,43 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       const bool in = kp >= k_lo && kp <= k_hi;
       const float sc = in ? bf16_to_f(stg_vs[key * NG + g]) : 0.f;
       const float bi = in ? bf16_to_f(stg_vb[key * NG + g]) : 0.f;
+      const uint32_t s2 = pack_h2(sc, sc), b2 = pack_h2(bi, bi);
+      // each lane loads its key's dims 32 db + 8 (lane & 3) .. +7 (one load per
+      // lane); the pair a fragment needs comes from a neighbour by shuffle
       uint32_t rr[4];
+      if constexpr (BITS == 4) {
+        const uint32_t mine = *reinterpret_cast<const uint32_t*>(stg_v + key * RB + 16 * db + 4 * (lane & 3));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int d0 = 32 * db + 8 * j + 2 * (lane & 3);
-        uint32_t c0, c1;
-        if constexpr (BITS == 4) {
-          const uint32_t b = stg_v[key * RB + (d0 >> 1)];
-          c0 = b & 15u;
-          c1 = b >> 4;
-        } else {
-          const uint32_t b = *reinterpret_cast<const uint16_t*>(stg_v + key * RB + d0);
-          c0 = b & 255u;
-          c1 = b >> 8;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w = __shfl_sync(0xffffffffu, mine, (lane & ~3) + j);   // dims 32 db + 8 j .. +7
+          const uint32_t b = (w >> (8 * (lane & 3))) & 0xFFu;                   // dims + 2 (lane & 3), +1
+          const uint32_t cp = (b & 0xFu) | ((b & 0xF0u) << 12) | kF16_1024;
+          rr[j] = h2_fma_u(h2_sub_u(cp, kF16_1024), s2, b2);
         }
-        rr[j] = pack_h2(fmaf(sc, code_f(c0), bi), fmaf(sc, code_f(c1), bi));
+      } else {
+        const uint2 mine = *reinterpret_cast<const uint2*>(stg_v + key * RB + 32 * db + 8 * (lane & 3));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t wx = __shfl_sync(0xffffffffu, mine.x, (lane & ~3) + j);
+          const uint32_t wy = __shfl_sync(0xffffffffu, mine.y, (lane & ~3) + j);
+          const uint32_t w = (lane & 2) ? wy : wx;
+          const uint32_t cp = prmt(w >> (16 * (lane & 1)), 0x64646464u, 0x4140u);
+          rr[j] = h2_fma_u(h2_sub_u(cp, kF16_1024), s2, b2);
+        }
       }
       const int dim = 32 * db + 8 * (lane >> 3) + (lane & 7);
       tc::stmatrix_x4_trans(base + P::V_OFF + tc::sw128_off(dim, kb), rr[0], rr[1], rr[2], rr[3]);
     }
+  };
+
+  // prologue: K of tile 0
+  wait(bar_tma, ph_tma);
+  convert_k();
+  for (int ti = 0; ti < n_tiles; ++ti) {
+    const int tpos0 = (tile_lo + ti) * kTileKeys;
     fence_proxy_async();
-    __syncthreads();                                      // operands of tile ti written; staging free
+    __syncthreads();                                      // K(ti) and Q written
     if (tid == 0) {
-      if (ti + 1 < n_tiles) issue_tile(ti + 1);
       tc::fence_after_sync();
 #pragma unroll
       for (int g = 0; g < NG; ++g)
@@ -276,35 +299,57 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
                       tc::desc_kmajor_sw128(base + P::K_OFF + g * 8192 + 32 * k, 1024), ID_QK, k > 0);
       tc::commit(bar_s);
     }
+    // V(ti) while QK(ti) runs; its buffer is free once PV(ti-1) is done
+    if (ti > 0) {
+      wait(bar_o, ph_o);
+      tc::fence_after_sync();
+    }
+    convert_v(tpos0);
+    fence_proxy_async();
+    __syncthreads();                                      // staging read completely: prefetch the next tile
+    if (tid == 0 && ti + 1 < n_tiles) issue_tile(ti + 1);
     wait(bar_s, ph_s);
     tc::fence_after_sync();
 
-    // ---- scores of this thread's row ----
-    float S[64];
+    // ---- scores of this thread's 32 keys ----
+    float S[32];
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      float b = 0.f;
+    for (int q4 = 0; q4 < 8; ++q4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int g = 0; g < NG; ++g) b = fmaf(bkf[j * NG + g], qsum[g], b);
-      S[j] = b;
+      for (int g = 0; g < NG; ++g) {
+        const float4 b4 = *reinterpret_cast<const float4*>(bkf + g * 64 + kk0 + 4 * q4);
+        acc.x = fmaf(b4.x, qsum[g], acc.x); acc.y = fmaf(b4.y, qsum[g], acc.y);
+        acc.z = fmaf(b4.z, qsum[g], acc.z); acc.w = fmaf(b4.w, qsum[g], acc.w);
+      }
+      S[4 * q4] = acc.x; S[4 * q4 + 1] = acc.y; S[4 * q4 + 2] = acc.z; S[4 * q4 + 3] = acc.w;
     }
 #pragma unroll
-    for (int g = 0; g < NG; ++g)
+    for (int g = 0; g < NG; ++g) {
+      float v[2][16];
+      tc::ld_x16(lane_base + g * 64 + kk0, v[0]);
+      tc::ld_x16(lane_base + g * 64 + kk0 + 16, v[1]);
+      tc::wait_ld();
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float v[16];
-        tc::ld_x16(lane_base + g * 64 + 16 * c4, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) S[16 * c4 + i] = fmaf(skf[(16 * c4 + i) * NG + g], v[i], S[16 * c4 + i]);
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(skf + g * 64 + kk0 + 4 * q4);
+        const float* vv = &v[q4 >> 2][4 * (q4 & 3)];
+        S[4 * q4] = fmaf(s4.x, vv[0], S[4 * q4]);
+        S[4 * q4 + 1] = fmaf(s4.y, vv[1], S[4 * q4 + 1]);
+        S[4 * q4 + 2] = fmaf(s4.z, vv[2], S[4 * q4 + 2]);
+        S[4 * q4 + 3] = fmaf(s4.w, vv[3], S[4 * q4 + 3]);
       }
+    }
     float mt = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const int kp = tpos0 + j;
+    for (int j = 0; j < 32; ++j) {
+      const int kp = tpos0 + kk0 + j;
       S[j] = (row_live && kp >= lo_r && kp <= p_r) ? S[j] : -INFINITY;
       mt = fmaxf(mt, S[j]);
     }
+    xr[hf * 128 + r] = mt;
+    __syncthreads();                                      // row maxima of both halves
+    mt = fmaxf(mt, xr[(hf ^ 1) * 128 + r]);
     // a new reference for this row; its output row is rescaled unless it had
     // no visible key before (tensor-memory loads and stores are warp-wide:
     // the whole warp takes part, with factor 1 for rows that keep theirs)
@@ -312,23 +357,23 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     const bool rescale_o = renew && m_ref != -INFINITY;
     const float alpha = rescale_o ? exp2f((m_ref - mt) * L2E) : 1.f;
     if (renew) {
-      l_sum *= alpha;
+      l_part *= alpha;
       m_ref = mt;
     }
     if (__any_sync(0xffffffffu, rescale_o)) {
-      for (int cc = 0; cc < D / 16; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         float v[16];
-        tc::ld_x16(lane_base + D + 16 * cc, v);
+        tc::ld_x16(lane_base + D + dd0 + 16 * cc, v);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] *= alpha;
-        tc::st_x16(lane_base + D + 16 * cc, v);
+        tc::st_x16(lane_base + D + dd0 + 16 * cc, v);
       }
       tc::wait_st();
     }
     // ---- P = e^(S - ref) as f16 ----
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
+    for (int ch = 0; ch < 4; ++ch) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -340,10 +385,10 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
         }
         const __half2 hp = __floats2half2_rn(p0, p1);
         const float2 pf = __half22float2(hp);
-        l_sum += pf.x + pf.y;
+        l_part += pf.x + pf.y;
         w[e] = *reinterpret_cast<const uint32_t*>(&hp);
       }
-      *reinterpret_cast<uint4*>(sm + P::P_OFF + tc::sw128_off(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(sm + P::P_OFF + tc::sw128_off(r, 4 * hf + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async();
     tc::fence_before_sync();
@@ -356,28 +401,35 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
                     tc::desc_kmajor_sw128(base + P::V_OFF + 32 * k, 1024), ID_PV, ti > 0 || k > 0);
       tc::commit(bar_o);
     }
+    // K(ti+1) while PV(ti) runs (QK(ti) is done, its tables were read above)
+    if (ti + 1 < n_tiles) {
+      wait(bar_tma, ph_tma);
+      convert_k();
+    }
   }
   wait(bar_o, ph_o);                                      // the last PV
   tc::fence_after_sync();
 
-  // ---- output row: O / l (the loads are warp-wide; only live rows write) ----
-  const float inv = 1.f / l_sum;
-  for (int cc = 0; cc < D / 16; ++cc) {
+  // ---- output: O / l, each thread half of its row's dims ----
+  xr[hf * 128 + r] = l_part;
+  __syncthreads();
+  const float inv = 1.f / (l_part + xr[(hf ^ 1) * 128 + r]);
+  for (int cc = 0; cc < D / 32; ++cc) {
     float v[16];
-    tc::ld_x16(lane_base + D + 16 * cc, v);
+    tc::ld_x16(lane_base + D + dd0 + 16 * cc, v);
     tc::wait_ld();
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] *= inv;
-    if (row_live) write_row(v, 16 * cc);
+    if (row_live) write_row(v, dd0 + 16 * cc);
   }
-  if (row_nan) write_nan_row();
+  if (row_nan) write_nan_half();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kRows, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -394,7 +446,7 @@ prefill_tc_kernel(const DecodeArgs a) {
   if (!ok) {
     if (qb == 0 && kvh == 0 && threadIdx.x == 0) flag_error(a.ws.status, KVQ_DEV_BADSEQ);
     const int r = threadIdx.x, t = t0 + r / G;
-    if (t < rows_s) {
+    if (r < kRows && t < rows_s) {
       const size_t oi = (((size_t)off0 + t) * a.L.n_q + kvh * G + r % G) * D;
       for (int d = 0; d < D; ++d) {
         if (a.out_f32) reinterpret_cast<float*>(a.out)[oi + d] = __int_as_float(0x7fc00000);
@@ -427,12 +479,14 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
   }
   const int per_sm = 512 / Pf<D>::TMEM_COLS;
   const int launch_smem = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);
-  qprep_kernel<D, true><<<dim3(a.n_rows, a.L.n_kv, a.L.G), dim3(Qp<D>::THREADS), 0, st>>>(a, f);
+  int hpb = 1, nblk = 1;
+  qprep_shape<D>(a.L.n_q, hpb, nblk);
+  qprep_kernel<D, true><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH), 0, st>>>(a, f, hpb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int TQ = kRows / a.L.G;
   if (a.n_seqs > 65535 || a.L.n_kv > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, a.L.n_kv);
-  prefill_tc_kernel<D><<<grid, kRows, launch_smem, st>>>(a);
+  prefill_tc_kernel<D><<<grid, kThreads, launch_smem, st>>>(a);
   return cudaGetLastError();
 }
 

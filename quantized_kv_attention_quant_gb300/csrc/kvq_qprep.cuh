@@ -49,149 +49,190 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
 }
 
 // ----------------------------------------------------------------------------
-// 1. q prep: one block per (row, kv head, q head slot h < 16), max(32, D/4)
-// threads of 4 (or 2) elements.  Writes q_hat (bf16), the head's words of the
-// QK A fragments and of the bias-term A fragment (rows >= G are zeros).
-// Each 32-bit fragment word holds two dims of ONE row, so blocks of different
-// heads write disjoint words.
+// q prep: one block per (row, block of heads).  The block first evaluates
+// the row's RoPE angles once for all its heads (the float-float sine/cosine
+// is the costly part), then each head's TH threads of E elements RMS-normalise
+// and rotate it.  Outputs:
+//   ROWS = false (decode): the mma.sync A fragments of every head slot of the
+//     row's kv heads (slots >= G are zeros) and the bias-term fragment; each
+//     32-bit fragment word holds two dims of ONE head, so heads write
+//     disjoint words.
+//   ROWS = true (prompt chunk): q_hat as f16 rows and per-group sums of
+//     those f16 values.
+// Both write q_hat (bf16) to q_prepped when it is given.
 // ----------------------------------------------------------------------------
 template <int D>
 struct Qp {
-  static constexpr int THREADS = D / 4 >= 32 ? D / 4 : 32;
-  static constexpr int E = D / THREADS;
-  static constexpr int NWARP = THREADS / 32;
-  static constexpr int TPG = 64 / E;
+  static constexpr int TH = D >= 512 ? D / 8 : (D / 4 >= 32 ? D / 4 : 32);   // threads per head
+  static constexpr int E = D / TH;                                            // elements per thread
+  static constexpr int HW = TH / 32;                                          // warps per head
+  static constexpr int TPG = 64 / E;                                          // threads per 64-dim group
+  static constexpr int HPB = 1024 / TH;                                       // most heads per block
 };
 
-// ROWS = false: decode (mma.sync fragments, grid z = 16 head slots);
-// ROWS = true: prompt chunk (q_hat as f16 rows and per-group sums of those
-// f16 values, grid z = G heads).
+// heads per block and blocks per row for n_q heads
+template <int D>
+inline void qprep_shape(int n_q, int& hpb, int& nblk) {
+  hpb = n_q < Qp<D>::HPB ? n_q : Qp<D>::HPB;
+  nblk = (n_q + hpb - 1) / hpb;
+}
+
 template <int D, bool ROWS>
-__global__ void __launch_bounds__(Qp<D>::THREADS)
-qprep_kernel(const DecodeArgs a, const RopeFreqs freqs) {
+__global__ void __launch_bounds__(1024)
+qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   using Q = Qp<D>;
-  constexpr int E = Q::E, NG = D / 64;
-  __shared__ uint16_t qn[D];               // normed, then q_hat
-  __shared__ float4 cs[D / 2];
+  constexpr int E = Q::E, NG = D / 64, TH = Q::TH;
+  __shared__ uint16_t qn[Q::HPB * D];      // normed, then q_hat, per head of the block
+  __shared__ float4 cs[D / 2];             // (cos.hi, cos.lo, sin.hi, sin.lo) per rotated pair
   __shared__ float freq[D / 2][3];
-  __shared__ ff red[Q::NWARP];
-  __shared__ float qs[8];                  // per-group sums of the f16 q values
+  __shared__ ff red[Q::HPB][Q::HW];
+  __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
   pdl_launch();
-  const int row = blockIdx.x, kvh = blockIdx.y, h = blockIdx.z;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, hl = tid / TH, tt = tid % TH, lane = tid & 31;
+  const int hq = blockIdx.y * hpb + hl;                   // q head of this thread
+  const bool active = hl < hpb && hq < a.L.n_q;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
   const RowInfo ri = row_info(a, row);
   const int bits = a.seqs[ri.s].bits;
-  uint32_t* frag = ROWS ? nullptr : reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
-  uint32_t* qb = ROWS ? nullptr : reinterpret_cast<uint32_t*>(a.ws.qbias) + ((size_t)row * a.L.n_kv + kvh) * 128;
-  // this row's fragment words: lanes with lane/4 == h % 8, register 0/2 (h < 8) or 1/3
-  const int rq = h & 7, reg_lo = h < 8 ? 0 : 1;
-  if (ROWS && h >= G) return;
-  if (!ROWS && h >= G) {
-    for (int i = t; i < NG * 4 * 4 * 2; i += Q::THREADS) {
-      const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
-      frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] = 0u;
-    }
-    if (t < 8) qb[(rq * 4 + (t & 3)) * 4 + reg_lo + 2 * (t >> 2)] = 0u;
-    return;
-  }
-  if (R > 0) stage_freqs(freqs.f, half, freq);
-  const int hq = kvh * G + h;
   const int pc = min(max(ri.p, 0), (1 << 24) - 1);
-  const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + t * E;
-  float x[E];
-  if constexpr (E == 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(src);
-    x[0] = bf16lo_to_f(u.x); x[1] = bf16hi_to_f(u.x); x[2] = bf16lo_to_f(u.y); x[3] = bf16hi_to_f(u.y);
-  } else {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
-    x[0] = bf16lo_to_f(u); x[1] = bf16hi_to_f(u);
-  }
-  ff ss = {0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
-  ss = ff_warp_sum(ss);
-  if constexpr (Q::NWARP > 1) {
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    ss = red[0];
-#pragma unroll
-    for (int w = 1; w < Q::NWARP; ++w) ss = ff_add(ss, red[w]);
-  }
-  const ff inv = rms_inv(ss, D, a.L.eps);
-  uint16_t y[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) {
-    y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[t * E + i]), inv);
-    qn[t * E + i] = y[i];
-  }
-  __syncthreads();                         // freq[] staged, qn[] complete
+
+  // ---- the row's rotation angles, once for all heads ----
   if (R > 0) {
-    for (int j = t; j < half; j += Q::THREADS) {
+    stage_freqs(freqs.f, half, freq);
+    __syncthreads();
+    for (int j = tid; j < half; j += blockDim.x) {
       ff cc, sn;
       rope_cos_sin(pc, freq[j][0], freq[j][1], freq[j][2], cc, sn);
       cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
     }
+  }
+
+  // ---- RMSNorm of this thread's E elements ----
+  uint16_t y[E];
+  ff ss = {0.f, 0.f};
+  float x[E];
+  if (active) {
+    const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + tt * E;
+#pragma unroll
+    for (int v = 0; v < E; v += 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(src + v);
+      x[v] = bf16lo_to_f(u);
+      x[v + 1] = bf16hi_to_f(u);
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = 0.f;
+  }
+  ss = ff_warp_sum(ss);
+  if constexpr (Q::HW > 1) {
+    if (lane == 0 && hl < Q::HPB) red[hl][(tt >> 5)] = ss;
     __syncthreads();
+    if (hl < Q::HPB) {
+      ss = red[hl][0];
+#pragma unroll
+      for (int w = 1; w < Q::HW; ++w) ss = ff_add(ss, red[hl][w]);
+    }
+  }
+  uint16_t* qh = qn + (hl < Q::HPB ? hl : 0) * D;
+  if (active) {
+    const ff inv = rms_inv(ss, D, a.L.eps);
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-      const int e = t * E + i;
+      y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[tt * E + i]), inv);
+      qh[tt * E + i] = y[i];
+    }
+  }
+  __syncthreads();                         // angles and normed rows complete
+
+  // ---- RoPE ----
+  if (R > 0 && active) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int e = tt * E + i;
       if (e < R) {
         const int j = e < half ? e : e - half;
         const float4 cv = cs[j];
         const ff cc = {cv.x, cv.y};
-        y[i] = e < half ? rot_bf16(bf16_to_f(qn[e]), bf16_to_f(qn[e + half]), cc, ff{cv.z, cv.w})
-                        : rot_bf16(bf16_to_f(qn[e]), bf16_to_f(qn[j]), cc, ff{-cv.z, -cv.w});
+        y[i] = e < half ? rot_bf16(bf16_to_f(qh[e]), bf16_to_f(qh[e + half]), cc, ff{cv.z, cv.w})
+                        : rot_bf16(bf16_to_f(qh[e]), bf16_to_f(qh[j]), cc, ff{-cv.z, -cv.w});
       }
     }
-    __syncthreads();                       // every read of the normed row is done
-#pragma unroll
-    for (int i = 0; i < E; ++i) qn[t * E + i] = y[i];
   }
+  __syncthreads();                         // every read of the normed rows is done
   float gs = 0.f;
+  if (active) {
 #pragma unroll
-  for (int i = 0; i < E; ++i) gs += __half2float(__float2half_rn(bf16_to_f(y[i])));   // the f16 value the MMA multiplies
+    for (int i = 0; i < E; ++i) {
+      qh[tt * E + i] = y[i];
+      gs += __half2float(__float2half_rn(bf16_to_f(y[i])));   // the f16 value the MMA multiplies
+    }
+  }
 #pragma unroll
   for (int m = 1; m < Q::TPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
-  if (t % Q::TPG == 0) qs[t / Q::TPG] = gs;
-  if (a.q_prepped) {
-    uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + t * E;
+  if (active) {
+    if (tt % Q::TPG == 0) qs[hl][tt / Q::TPG] = gs;
+    if (a.q_prepped) {
+      uint16_t* dst = a.q_prepped + ((size_t)row * a.L.n_q + hq) * D + tt * E;
 #pragma unroll
-    for (int i = 0; i < E; ++i) dst[i] = y[i];
+      for (int i = 0; i < E; ++i) dst[i] = y[i];
+    }
   }
   if constexpr (ROWS) {
-    __half* dst = reinterpret_cast<__half*>(a.ws.q16) + ((size_t)row * a.L.n_q + hq) * D + t * E;
+    if (active) {
+      __half* dst = reinterpret_cast<__half*>(a.ws.q16) + ((size_t)row * a.L.n_q + hq) * D + tt * E;
 #pragma unroll
-    for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(bf16_to_f(y[i]));
-    if (t % Q::TPG == 0) a.ws.qsum[((size_t)row * a.L.n_q + hq) * NG + t / Q::TPG] = gs;
+      for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(bf16_to_f(y[i]));
+      if (tt % Q::TPG == 0) a.ws.qsum[((size_t)row * a.L.n_q + hq) * NG + tt / Q::TPG] = gs;
+    }
     return;
   }
   __syncthreads();                         // q_hat and the group sums complete
-  // QK A fragment words of row h: for each (group, k-step, t4) two words
-  for (int i = t; i < NG * 4 * 4 * 2; i += Q::THREADS) {
-    const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
-    int d[4];
-    qk_dims(bits, ks, d);
-    const int base = g * 64 + 16 * t4;
-    const int d0 = base + (pair ? d[2] : d[0]), d1 = base + (pair ? d[3] : d[1]);
-    // with 4-bit codes the second k-half of every step multiplies codes read
-    // from bits 4..7 (16 times too large as f16 subnormals): q/16 there
-    const float f = (bits == 4 && pair) ? 0.0625f : 1.f;
-    frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] =
-        pack_h2(bf16_to_f(qn[d0]) * f, bf16_to_f(qn[d1]) * f);
-  }
-  // bias-term A fragment words of row h: k = group (hi part) | 8 + group (lo part)
-  if (t < 8) {
-    const int t4 = t & 3, lo_part = t >> 2;
-    float v[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int g = 2 * t4 + e;
-      const float xs = g < NG ? qs[g] : 0.f;
-      const float hi = __half2float(__float2half_rn(xs));
-      v[e] = lo_part ? xs - hi : hi;
+  if (!active) return;
+  const int kvh = hq / G, h = hq % G;
+  uint32_t* frag = reinterpret_cast<uint32_t*>(a.ws.qfrag) + ((size_t)row * a.L.n_kv + kvh) * NG * 4 * 32 * 4;
+  uint32_t* qb = reinterpret_cast<uint32_t*>(a.ws.qbias) + ((size_t)row * a.L.n_kv + kvh) * 128;
+  // fragment words of head slot h: lanes with lane/4 == h % 8, register 0/2 (h < 8) or 1/3
+  {
+    const int rq = h & 7, reg_lo = h < 8 ? 0 : 1;
+    for (int i = tt; i < NG * 4 * 4 * 2; i += TH) {
+      const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
+      int d[4];
+      qk_dims(bits, ks, d);
+      const int base = g * 64 + 16 * t4;
+      const int d0 = base + (pair ? d[2] : d[0]), d1 = base + (pair ? d[3] : d[1]);
+      // with 4-bit codes the second k-half of every step multiplies codes read
+      // from bits 4..7 (16 times too large as f16 subnormals): q/16 there
+      const float f = (bits == 4 && pair) ? 0.0625f : 1.f;
+      frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] =
+          pack_h2(bf16_to_f(qh[d0]) * f, bf16_to_f(qh[d1]) * f);
     }
-    qb[(rq * 4 + t4) * 4 + reg_lo + 2 * lo_part] = pack_h2(v[0], v[1]);
+    // bias-term A fragment words of slot h: k = group (hi part) | 8 + group (lo part)
+    if (tt < 8) {
+      const int t4 = tt & 3, lo_part = tt >> 2;
+      float v[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int g = 2 * t4 + e;
+        const float xs = g < NG ? qs[hl][g] : 0.f;
+        const float hi = __half2float(__float2half_rn(xs));
+        v[e] = lo_part ? xs - hi : hi;
+      }
+      qb[(rq * 4 + t4) * 4 + reg_lo + 2 * lo_part] = pack_h2(v[0], v[1]);
+    }
+  }
+  // the last q head of a kv head also zero-fills the unused slots G .. 15
+  if (h == G - 1) {
+    for (int hz = G; hz < kMaxG; ++hz) {
+      const int rq = hz & 7, reg_lo = hz < 8 ? 0 : 1;
+      for (int i = tt; i < NG * 4 * 4 * 2; i += TH) {
+        const int pair = i & 1, t4 = (i >> 1) & 3, ks = (i >> 3) & 3, g = i >> 5;
+        frag[((g * 4 + ks) * 32 + rq * 4 + t4) * 4 + reg_lo + 2 * pair] = 0u;
+      }
+      if (tt < 8) qb[(rq * 4 + (tt & 3)) * 4 + reg_lo + 2 * (tt >> 2)] = 0u;
+    }
   }
 }
 
