@@ -3,13 +3,16 @@
 // offset, then cache.appendWindow(k, v); gemma4-e4b.ts Gemma4Layer.kv:
 // {bits, groupSize 64}).
 //
-// One block handles one (row, kv head, K-or-V) item with max(32, D/4)
-// threads of 4 (or 2) contiguous elements each, so the long float-float
-// chains of the prep are spread thin: a decode step appends only a handful of
-// rows, and its latency is the critical path of one block.  A 64-element
-// quantization group spans 16 threads and is reduced with shuffles.
+// One block handles one row (token) and a block of its (kv head, K-or-V)
+// items, TH threads of E contiguous elements per item: the row's RoPE angles
+// (the costly float-float sine/cosine) are evaluated once for all its K
+// heads, and the float-float norm chains of the items run side by side.  A
+// 64-element quantization group spans 64/E threads and is reduced with
+// shuffles.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
+
+#include <type_traits>
 
 namespace kvq {
 
@@ -17,18 +20,11 @@ namespace {
 
 template <int D>
 struct App {
-  static constexpr int THREADS = D / 4 >= 32 ? D / 4 : 32;
-  static constexpr int E = D / THREADS;            // elements per thread
-  static constexpr int NWARP = THREADS / 32;
+  static constexpr int TH = D >= 512 ? D / 8 : (D / 4 >= 32 ? D / 4 : 32);   // threads per item
+  static constexpr int E = D / TH;                 // elements per thread
+  static constexpr int HW = TH / 32;               // warps per item
   static constexpr int TPG = 64 / E;               // threads per quantization group
-};
-
-template <int D>
-struct AppendSmem {
-  uint16_t normed[D];
-  float4 cs[D / 2];                     // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
-  float freq[D / 2][3];                 // rotary frequency triples
-  ff red[App<D>::NWARP];
+  static constexpr int IPB = 1024 / TH;            // most items per block
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row) {
@@ -122,19 +118,22 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[App<D>::E], c
 }
 
 template <int D>
-__global__ void __launch_bounds__(App<D>::THREADS)
-append_kernel(const AppendArgs a, const RopeFreqs freqs) {
+__global__ void __launch_bounds__(1024)
+append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   using A = App<D>;
-  constexpr int E = A::E;
-  __shared__ AppendSmem<D> sm;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  constexpr int E = A::E, TH = A::TH;
+  __shared__ uint16_t normed[A::IPB * D];
+  __shared__ float4 cs[D / 2];            // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
+  __shared__ float freq[D / 2][3];        // rotary frequency triples
+  __shared__ ff red[A::IPB][A::HW];
+  const int tid = threadIdx.x, il = tid / TH, tt = tid % TH, lane = tid & 31;
   const int R = a.L.rope_dims, half = R >> 1;
   const int Hkv = a.L.n_kv;
-  const long item = blockIdx.x;
-  const int kind = int(item & 1);        // 0: K, 1: V
-  const long rh = item >> 1;
-  const int row = int(rh / Hkv), head = int(rh % Hkv);
-  if (kind == 0 && R > 0) stage_freqs(freqs.f, half, sm.freq);
+  const int row = blockIdx.x;
+  const int item = blockIdx.y * ipb + il;
+  const bool active = item < 2 * Hkv;
+  const int kind = item & 1;             // 0: K, 1: V
+  const int head = item >> 1;
 
   const int s = find_seq(a.row_offsets, a.n_seqs, row);
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
@@ -151,16 +150,31 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
   // kv_prepped) but not stored
   const bool store = t_in >= rows_s - c.capacity;
 
+  // ---- the row's rotation angles, once for all K heads ----
+  if (R > 0) {
+    stage_freqs(freqs.f, half, freq);
+    __syncthreads();
+    for (int j = tid; j < half; j += blockDim.x) {
+      ff cc, sn;
+      rope_cos_sin(pos, freq[j][0], freq[j][1], freq[j][2], cc, sn);
+      cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+    }
+  }
+
   // ---- load the raw row ----
-  const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
-  src += ((size_t)row * Hkv + head) * D + t * E;
   float x[E];
-  if constexpr (E == 4) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-    x[0] = bf16lo_to_f(u.x); x[1] = bf16hi_to_f(u.x); x[2] = bf16lo_to_f(u.y); x[3] = bf16hi_to_f(u.y);
+  if (active) {
+    const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
+    src += ((size_t)row * Hkv + head) * D + tt * E;
+#pragma unroll
+    for (int v = 0; v < E; v += 2) {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src + v));
+      x[v] = bf16lo_to_f(u);
+      x[v + 1] = bf16hi_to_f(u);
+    }
   } else {
-    const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
-    x[0] = bf16lo_to_f(u); x[1] = bf16hi_to_f(u);
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = 0.f;
   }
 
   // ---- RMSNorm (weight on K only) ----
@@ -168,71 +182,73 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs) {
 #pragma unroll
   for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
   ss = ff_warp_sum(ss);
-  if constexpr (A::NWARP > 1) {
-    if (lane == 0) sm.red[warp] = ss;
+  if constexpr (A::HW > 1) {
+    if (lane == 0) red[il][tt >> 5] = ss;
     __syncthreads();
-    ss = sm.red[0];
+    ss = red[il][0];
 #pragma unroll
-    for (int w = 1; w < A::NWARP; ++w) ss = ff_add(ss, sm.red[w]);
+    for (int w = 1; w < A::HW; ++w) ss = ff_add(ss, red[il][w]);
   }
   const ff inv = rms_inv(ss, D, a.L.eps);
   uint16_t y[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    const float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + t * E + i)) : 1.f;
+    const float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + tt * E + i)) : 1.f;
     y[i] = norm_scale_bf16(x[i], w, inv);
   }
 
   // ---- RoPE on K ----
-  if (kind == 0 && R > 0) {
+  if (R > 0) {
+    uint16_t* nr = normed + il * D;
 #pragma unroll
-    for (int i = 0; i < E; ++i) sm.normed[t * E + i] = y[i];
-    __syncthreads();                     // freq[] staged, normed[] complete
-    for (int j = t; j < half; j += A::THREADS) {
-      ff cc, sn;
-      rope_cos_sin(pos, sm.freq[j][0], sm.freq[j][1], sm.freq[j][2], cc, sn);
-      sm.cs[j] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
-    }
-    __syncthreads();
+    for (int i = 0; i < E; ++i) nr[tt * E + i] = y[i];
+    __syncthreads();                     // angles and normed rows complete
+    if (active && kind == 0) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const int e = t * E + i;
-      if (e < R) {
-        const int j = e < half ? e : e - half;
-        const float4 cv = sm.cs[j];
-        const ff cc = {cv.x, cv.y};
-        if (e < half)        // x_j cos - x_{j+h} sin
-          y[i] = rot_bf16(bf16_to_f(sm.normed[e]), bf16_to_f(sm.normed[e + half]), cc, ff{cv.z, cv.w});
-        else                 // x_{j+h} cos + x_j sin
-          y[i] = rot_bf16(bf16_to_f(sm.normed[e]), bf16_to_f(sm.normed[j]), cc, ff{-cv.z, -cv.w});
+      for (int i = 0; i < E; ++i) {
+        const int e = tt * E + i;
+        if (e < R) {
+          const int j = e < half ? e : e - half;
+          const float4 cv = cs[j];
+          const ff cc = {cv.x, cv.y};
+          if (e < half)        // x_j cos - x_{j+h} sin
+            y[i] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w});
+          else                 // x_{j+h} cos + x_j sin
+            y[i] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
+        }
       }
     }
   }
+  if (!active) return;
 
   if (a.prepped) {
-    uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + t * E;
+    uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + tt * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) dst[i] = y[i];
   }
 
   // ---- quantize the 64-element group, pack, store ----
   if (!store) return;
-  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, t);
-  else quantize_store<D, 8>(y, c, kind, head, pos, t);
+  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, tt);
+  else quantize_store<D, 8>(y, c, kind, head, pos, tt);
 }
 
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st) {
-  const long items = (long)a.n_rows * a.L.n_kv * 2;
-  if (items == 0) return cudaSuccess;
-  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)items);
+  if (a.n_rows == 0) return cudaSuccess;
+  auto go = [&](auto tag) {
+    constexpr int D = decltype(tag)::value;
+    const int items = 2 * a.L.n_kv;
+    const int ipb = items < App<D>::IPB ? items : App<D>::IPB;
+    const dim3 grid((unsigned)a.n_rows, (unsigned)((items + ipb - 1) / ipb));
+    append_kernel<D><<<grid, ipb * App<D>::TH, 0, st>>>(a, f, ipb);
+  };
   switch (a.L.D) {
-    case 64: append_kernel<64><<<grid, App<64>::THREADS, 0, st>>>(a, f); break;
-    case 128: append_kernel<128><<<grid, App<128>::THREADS, 0, st>>>(a, f); break;
-    case 256: append_kernel<256><<<grid, App<256>::THREADS, 0, st>>>(a, f); break;
-    case 512: append_kernel<512><<<grid, App<512>::THREADS, 0, st>>>(a, f); break;
+    case 64: go(std::integral_constant<int, 64>{}); break;
+    case 128: go(std::integral_constant<int, 128>{}); break;
+    case 256: go(std::integral_constant<int, 256>{}); break;
+    case 512: go(std::integral_constant<int, 512>{}); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
