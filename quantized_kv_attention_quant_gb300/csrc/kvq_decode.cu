@@ -563,7 +563,10 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
   const int n_my = ok ? max(0, min(chunk, t_hi + 1 - t_begin)) : 0;
   if (n_my == 0) {
     // nothing to read: an empty partial (m = -inf), or NaN for a bad sequence
-    if (!ok && split == 0 && kvh == 0 && threadIdx.x == 0) flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+    if (!ok && split == 0 && kvh == 0 && threadIdx.x == 0) {
+      pdl_wait();                                   // after q prep has cleared the status word
+      flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+    }
     const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
     if (threadIdx.x < 16) {
       a.ws.part_ml[pidx * 32 + threadIdx.x] = ok ? -INFINITY : __int_as_float(0x7fc00000);
@@ -730,7 +733,7 @@ DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms
                                      : full_tiles);
   const int per_sm = L.D >= 512 ? 1 : (L.D == 256 ? 2 : 4);
   const long base = std::max<long>((long)n_rows * L.n_kv, 1);
-  const long wave = ((long)num_sms * per_sm + base - 1) / base;    // splits for one full wave
+  const long wave = std::max<long>(1, ((long)num_sms * per_sm) / base);   // splits that still fit one wave
   DecodePlan plan;
   if (fixed_chunks) {
     // every split takes the same number of tiles: rows shorter than the
@@ -751,8 +754,7 @@ DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms
 
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int /*num_sms*/, cudaStream_t st) {
   if (a.n_rows == 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(a.ws.status, 0, 4, st);
-  if (e != cudaSuccess) return e;
+  // the status word is cleared by q prep, the first kernel of the call
   switch (a.L.D) {
     case 64: return launch_decode_t<64>(a, f, st);
     case 128: return launch_decode_t<128>(a, f, st);

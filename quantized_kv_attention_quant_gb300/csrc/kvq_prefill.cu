@@ -518,8 +518,7 @@ DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L) {
 
 cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st) {
   if (a.n_rows == 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(a.ws.status, 0, 4, st);
-  if (e != cudaSuccess) return e;
+  // the status word is cleared by q prep, the first kernel of the call
   switch (a.L.D) {
     case 64: return launch_prefill_t<64>(a, f, max_rows_per_seq, st);
     case 128: return launch_prefill_t<128>(a, f, max_rows_per_seq, st);

@@ -87,9 +87,12 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   __shared__ float freq[D / 2][3];
   __shared__ ff red[Q::HPB][Q::HW];
   __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
-  pdl_launch();
   const int row = blockIdx.x;
   const int tid = threadIdx.x, hl = tid / TH, tt = tid % TH, lane = tid & 31;
+  // the first kernel of an attention call clears its status word; the later
+  // kernels flag errors only once this grid is complete
+  if (row == 0 && blockIdx.y == 0 && tid == 0) *a.ws.status = 0u;
+  pdl_launch();
   const int hq = blockIdx.y * hpb + hl;                   // q head of this thread
   const bool active = hl < hpb && hq < a.L.n_q;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
