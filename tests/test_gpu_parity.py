@@ -222,3 +222,17 @@ def test_workspace_contents_do_not_matter(kvq):
     case.attend()
     torch.cuda.synchronize()
     assert np.array_equal(case.out.cpu().numpy(), ref)
+
+
+def test_verify_windows(kvq):
+    """Short windows of 2..64 query rows per sequence (speculative verify):
+    the same call as a prompt chunk, on the tensor-core path (D256, G 4) and
+    on the row path (D512, G 16)."""
+    _, harness = kvq
+    spec = _spec(8, 2, 256, 512, 256)
+    wl = W.PrefillWorkload("verify-sliding", 84, spec, filled=[100, 700, 5, 1030], chunk=[2, 7, 33, 64],
+                           bits=[4, 8, 8, 4])
+    check_prefill(harness, wl)
+    spec = _spec(16, 1, 512, 0, 128, 1e6, True)
+    wl = W.PrefillWorkload("verify-full", 85, spec, filled=[90, 3], chunk=[5, 17], bits=[8, 4])
+    check_prefill(harness, wl)
