@@ -20,7 +20,7 @@ namespace {
 
 template <int D>
 struct App {
-  static constexpr int TH = D >= 512 ? D / 8 : (D / 4 >= 32 ? D / 4 : 32);   // threads per item
+  static constexpr int TH = D / 4 >= 32 ? D / 4 : 32;                         // threads per item
   static constexpr int E = D / TH;                 // elements per thread
   static constexpr int HW = TH / 32;               // warps per item
   static constexpr int TPG = 64 / E;               // threads per quantization group

@@ -63,7 +63,7 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
 // ----------------------------------------------------------------------------
 template <int D>
 struct Qp {
-  static constexpr int TH = D >= 512 ? D / 8 : (D / 4 >= 32 ? D / 4 : 32);   // threads per head
+  static constexpr int TH = D / 4 >= 32 ? D / 4 : 32;                         // threads per head
   static constexpr int E = D / TH;                                            // elements per thread
   static constexpr int HW = TH / 32;                                          // warps per head
   static constexpr int TPG = 64 / E;                                          // threads per 64-dim group
