@@ -146,6 +146,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   float* lred = red + 2 * NW * 16;                          // [16][NW]
   uint8_t* Pbuf = smem + ctrl_bytes(D);                     // [2][16][64] f16, swizzled
   uint8_t* stages = smem + slot0_off(D);                    // stage i: K slot, then V slot
+  uint8_t* const slots_base = stages;
   const int cap_tiles = c.capacity / kTileKeys;
   const size_t head_row0 = (size_t)kvh * c.capacity;
 
@@ -527,19 +528,26 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
       ml[16 + lane] = l;
     }
   }
+  // the o partial goes through shared memory (the stages are free: every warp
+  // passed the barrier above after its last read) so that the global stores
+  // are whole 16-byte pieces of rows; rows padded by 4 floats against bank
+  // conflicts
+  constexpr int PS = D + 4;
+  float* ps = reinterpret_cast<float*>(slots_base);
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     // codes were 2^-24 units (2^-20 for 4-bit codes from bits 4..7: odd nt)
     const float uns = (BITS == 4 && (nt & 1) ? kTwo24 / 16.f : kTwo24) / PRESCALE;
     const int d0 = g_pv * 64 + 8 * (2 * t4) + nt, d1 = d0 + 8;
-    if (rq < G) {
-      po[rq * D + d0] = fmaf(oacc[nt][0], uns, bias_r);
-      po[rq * D + d1] = fmaf(oacc[nt][1], uns, bias_r);
-    }
-    if (rq + 8 < G) {
-      po[(rq + 8) * D + d0] = fmaf(oacc[nt][2], uns, bias_r8);
-      po[(rq + 8) * D + d1] = fmaf(oacc[nt][3], uns, bias_r8);
-    }
+    ps[rq * PS + d0] = fmaf(oacc[nt][0], uns, bias_r);
+    ps[rq * PS + d1] = fmaf(oacc[nt][1], uns, bias_r);
+    ps[(rq + 8) * PS + d0] = fmaf(oacc[nt][2], uns, bias_r8);
+    ps[(rq + 8) * PS + d1] = fmaf(oacc[nt][3], uns, bias_r8);
+  }
+  named_bar(1, NW * 32);
+  for (int i = threadIdx.x; i < G * (D / 4); i += NW * 32) {
+    const int r = i / (D / 4), c4 = i % (D / 4);
+    *reinterpret_cast<float4*>(po + r * D + 4 * c4) = *reinterpret_cast<const float4*>(ps + r * PS + 4 * c4);
   }
 }
 
