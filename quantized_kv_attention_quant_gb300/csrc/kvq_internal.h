@@ -70,7 +70,7 @@ struct DecodeArgs {
 
 size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits);
 DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits);
-constexpr int kChunkTiles = 32;   // target tiles per split when the longest row is known
+constexpr int kChunkTiles = 48;   // target tiles per split when the longest row is known
 struct DecodePlan { int splits, chunk_tiles; };
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks);
 
