@@ -283,31 +283,49 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=device)
     K = args.steps
     full_calls = [c for _, c in calls if c.spec.window == 0] if args.workload == "stack42" else [c for _, c in calls]
+    def ev_pair():
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
     try:
-        ev = [[(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in full_calls] for _ in range(K)]
+        ev = [[ev_pair() for _ in full_calls] for _ in range(K)]
+        # every other call too, for the step breakdown (appends, other attention calls)
+        ev_app = [[ev_pair() for donor, _ in calls if donor] for _ in range(K)]
+        ev_oth = [[ev_pair() for _, c in calls if c not in full_calls] for _ in range(K)]
         have_inner = True
     except TypeError:
-        ev, have_inner = None, False
+        ev, ev_app, ev_oth, have_inner = None, None, None, False
     graph = torch.cuda.CUDAGraph()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         step_calls(calls)                      # one more warm-up on the capture stream
     torch.cuda.synchronize()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(K):
-            j = 0
-            for donor, c in calls:
-                if donor:
-                    c.append()
-                inner = have_inner and c in full_calls
-                if inner:
-                    ev[k][j][0].record()
-                c.attend()
-                if inner:
-                    ev[k][j][1].record()
-                    j += 1
-    torch.cuda.synchronize()
+    def capture(g, all_events):
+        # all_events: time every call (the events break the launch overlap
+        # between calls, so that graph is replayed apart from the timed one)
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(K):
+                j = ja = jo = 0
+                for donor, c in calls:
+                    if donor:
+                        if all_events:
+                            ev_app[k][ja][0].record()
+                        c.append()
+                        if all_events:
+                            ev_app[k][ja][1].record()
+                            ja += 1
+                    inner = have_inner and c in full_calls
+                    pair = ev[k][j] if inner else (ev_oth[k][jo] if all_events else None)
+                    if pair:
+                        pair[0].record()
+                    c.attend()
+                    if pair:
+                        pair[1].record()
+                        if inner:
+                            j += 1
+                        else:
+                            jo += 1
+        torch.cuda.synchronize()
+    capture(graph, False)
 
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -324,8 +342,18 @@ def run_gpu(args):
 
     # dominant-kernel duration from the events inside the graph
     dom_ms = None
+    breakdown = None
     if have_inner:
         dom_ms = sum(a.elapsed_time(b) for row in ev for a, b in row) / K
+        # per-call breakdown from a separate replay with events around every call
+        graph_bd = torch.cuda.CUDAGraph()
+        capture(graph_bd, True)
+        graph_bd.replay()
+        torch.cuda.synchronize()
+        breakdown = {"dominant_calls_ms": sum(a.elapsed_time(b) for row in ev for a, b in row) / K,
+                     "other_attention_calls_ms": sum(a.elapsed_time(b) for row in ev_oth for a, b in row) / K,
+                     "append_calls_ms": sum(a.elapsed_time(b) for row in ev_app for a, b in row) / K}
+        del graph_bd
     status_ok = all(c.status_word() == 0 for _, c in calls)
 
     # e2e through the binding with host buffers
@@ -359,6 +387,9 @@ def run_gpu(args):
                 "inputs smaller than L2 (launch-bound case)",
                 "kv_bytes_per_step": info["kv_bytes"], "step_kv_gbs": step_gbs,
                 "graph": f"{K} steps captured in one CUDA graph", "device_status_clean": status_ok})
+    if breakdown:
+        cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in breakdown.items()}
+        cfg["step_breakdown_note"] = "separate replay with events around every call (they slow it down)"
     line = {"metric": "decode-attention tokens/s" if args.workload != "prefill" else "prefill tokens/s",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
