@@ -189,6 +189,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.ws.q16 + (grow * a.L.n_q + hq) * D);
 #pragma unroll 4
+#pragma unroll 1
     for (int ch = hf * (D / 16); ch < (hf + 1) * (D / 16); ++ch) {
       uint4 v = row_valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
       if (BITS == 4)
@@ -217,7 +218,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
 
   // K codes of the staged tile -> f16 integers; K scale/bias -> f32 tables
   auto convert_k = [&]() {
-#pragma unroll 2
+#pragma unroll 1
     for (int i = tid; i < 64 * D / 8; i += kThreads) {
       const int key = i / (D / 8), ch = i % (D / 8);
       uint4 o;
@@ -341,11 +342,18 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       }
     }
     float mt = -INFINITY;
+    // keys outside a row's window: only where the 32 keys are not all visible
+    // to every row of the warp (interior tiles skip the masks)
+    if (__all_sync(0xffffffffu, row_live && tpos0 + kk0 >= lo_r && tpos0 + kk0 + 31 <= p_r)) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int kp = tpos0 + kk0 + j;
-      S[j] = (row_live && kp >= lo_r && kp <= p_r) ? S[j] : -INFINITY;
-      mt = fmaxf(mt, S[j]);
+      for (int j = 0; j < 32; ++j) mt = fmaxf(mt, S[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int kp = tpos0 + kk0 + j;
+        S[j] = (row_live && kp >= lo_r && kp <= p_r) ? S[j] : -INFINITY;
+        mt = fmaxf(mt, S[j]);
+      }
     }
     xr[hf * 128 + r] = mt;
     __syncthreads();                                      // row maxima of both halves

@@ -236,3 +236,38 @@ def test_verify_windows(kvq):
     spec = _spec(16, 1, 512, 0, 128, 1e6, True)
     wl = W.PrefillWorkload("verify-full", 85, spec, filled=[90, 3], chunk=[5, 17], bits=[8, 4])
     check_prefill(harness, wl)
+
+
+PREFILL_TC_CASES = {
+    # name: (spec, filled per seq, chunk per seq, bits per seq) -- tensor-core path shapes
+    "g1-d64": (_spec(2, 2, 64, 0, 64), [70, 3], [130, 9], [8, 4]),
+    "g2-d128-window": (_spec(4, 2, 128, 96, 64, 1e6), [200, 0], [70, 45], [4, 8]),
+    "g8-d256": (_spec(8, 1, 256, 0, 256), [31, 140], [40, 17], [8, 4]),
+    "g16-d128-norope": (_spec(16, 1, 128, 0, 0), [64, 5], [24, 8], [4, 8]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_TC_CASES))
+def test_prefill_tc_shapes(kvq, name):
+    """The tensor-core prompt kernel across G (rows = 128/G tokens x G heads)
+    and head_dim, full and windowed, with and without RoPE."""
+    _, harness = kvq
+    spec, filled, chunk, bits = PREFILL_TC_CASES[name]
+    wl = W.PrefillWorkload(name, 86, spec, filled=filled, chunk=chunk, bits=bits)
+    _, worst = check_prefill(harness, wl)
+    print(name, "worst", worst)
+
+
+def test_prefill_bf16_output_is_rounded_f32(kvq):
+    _, harness = kvq
+    spec = _spec(8, 2, 256, 64, 256)
+    wl = W.PrefillWorkload("prefill-bf16", 87, spec, filled=[150, 0], chunk=[100, 37], bits=[8, 4])
+    a = harness.PrefillCase(wl)
+    a.step()
+    b = harness.PrefillCase(wl, out_f32=False)
+    b.step()
+    torch.cuda.synchronize()
+    f32 = a.out.cpu().numpy()
+    bf = b.out.cpu().numpy().view(np.uint16)
+    want = O.f64_to_bf16(O.rn_bf16(f32.astype(np.float64)))
+    assert np.array_equal(bf, want)
