@@ -130,10 +130,10 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
   // prompt chunks whose head shape fits the tensor-core kernel take it
   const bool tc = row_offsets != nullptr && kvq::prefill_tc_supported(L);
-  const kvq::DecodePlan plan = tc ? kvq::DecodePlan{1, 0}
+  const kvq::DecodePlan plan = tc ? kvq::DecodePlan{1, 0, 0}
                                   : kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
   const int splits = plan.splits;
-  const size_t need = tc ? kvq::prefill_tc_ws_bytes(n_rows, L) : kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, splits);
+  const size_t need = tc ? kvq::prefill_tc_ws_bytes(n_rows, L) : kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan);
   if (workspace_bytes < need)
     return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
   kvq::DecodeArgs a;
@@ -150,13 +150,14 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
   a.q_prepped = q_prepped;
   a.splits = splits;
   a.chunk_tiles = plan.chunk_tiles;
+  a.sk_ctas = plan.sk_ctas;
   const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
   cudaError_t e;
   if (tc) {
     a.ws = kvq::prefill_tc_ws_carve(workspace, n_rows, L);
     e = kvq::launch_prefill_tc(a, f, max_rows_per_seq, static_cast<cudaStream_t>(stream));
   } else {
-    a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, splits);
+    a.ws = kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, plan);
     e = kvq::launch_decode(a, f, num_sms_current(), static_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -218,7 +219,7 @@ size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || max_pos < 0) return 0;
   const kvq::DecodePlan plan = kvq::decode_plan(L, n_seqs, max_pos + 1, num_sms_current(), true);
-  return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, plan.splits);
+  return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, plan);
 }
 
 kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
@@ -241,7 +242,7 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
   if (kvq::prefill_tc_supported(L)) return kvq::prefill_tc_ws_bytes(n_rows, L);
   const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
   const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), false);
-  return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan.splits);
+  return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan);
 }
 
 // ---------------------------------------------------------------------------

@@ -126,10 +126,14 @@ __device__ __forceinline__ float max_over_warps(const float* p) {
   return m;
 }
 
+// One run of consecutive tiles of one (row, kv head): the ring prologue, the
+// pipelined loop and the epilogue, which writes the run's (m, l, o) partial
+// to po / ml, or, when the run is the whole row (final_out), the normalised
+// output.  Returns true when a bounded wait gave up.
 template <int D, int BITS>
-__device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
+__device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
                                             const int nst, const TileRange tr, const int row, const int kvh,
-                                            const int split) {
+                                            float* po, float* ml, const bool final_out) {
   using C = Dec<D>;
   constexpr int NG = C::NG, NW = C::NW, NTQ = C::NTQ;
   static_assert(NW == NG, "one PV warp per 64-dim group");
@@ -514,18 +518,17 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
   // bias column 0 lives in lanes with t4 == 0 (c0: row rq, c2: row rq + 8)
   const float bias_r = __shfl_sync(0xffffffffu, cb[0], lane & ~3);
   const float bias_r8 = __shfl_sync(0xffffffffu, cb[2], lane & ~3);
-  named_bar(1, NW * 32);
+  const bool any_dead = __syncthreads_or(dead);
   const int G = a.L.G;
-  const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
-  float* po = a.ws.part_o + pidx * 16 * D;
-  float* ml = a.ws.part_ml + pidx * 32;
+  float* lfin = red;                            // [16] row sums (final output); the max exchange is done
   if (warp == 0) {
     // every warp holds the same running max; warp 0 writes it
-    if (t4 == 0) { ml[rq] = m_run[0]; ml[rq + 8] = m_run[1]; }
+    if (!final_out && t4 == 0) { ml[rq] = m_run[0]; ml[rq + 8] = m_run[1]; }
     if (lane < 16) {
       float l = 0.f;
       for (int w = 0; w < NW; ++w) l += lred[lane * NW + w];
-      ml[16 + lane] = l;
+      if (final_out) lfin[lane] = l;
+      else ml[16 + lane] = l;
     }
   }
   // the o partial goes through shared memory (the stages are free: every warp
@@ -545,56 +548,212 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const kvq_seq_c
     ps[(rq + 8) * PS + d1] = fmaf(oacc[nt][3], uns, bias_r8);
   }
   named_bar(1, NW * 32);
-  for (int i = threadIdx.x; i < G * (D / 4); i += NW * 32) {
-    const int r = i / (D / 4), c4 = i % (D / 4);
-    *reinterpret_cast<float4*>(po + r * D + 4 * c4) = *reinterpret_cast<const float4*>(ps + r * PS + 4 * c4);
+  if (!final_out) {
+    for (int i = threadIdx.x; i < G * (D / 4); i += NW * 32) {
+      const int r = i / (D / 4), c4 = i % (D / 4);
+      *reinterpret_cast<float4*>(po + r * D + 4 * c4) = *reinterpret_cast<const float4*>(ps + r * PS + 4 * c4);
+    }
+  } else {
+    // the whole row in this run: out = o / l, as the merge of one partial
+    const size_t ob = ((size_t)row * a.L.n_q + (size_t)kvh * G) * D;
+    for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+      const int r = i / D, d = i % D;
+      const float o = ps[r * PS + d] * (1.f / lfin[r]);
+      if (a.out_f32) reinterpret_cast<float*>(a.out)[ob + i] = o;
+      else reinterpret_cast<uint16_t*>(a.out)[ob + i] = f_to_bf16_rn(o);
+    }
   }
+  return any_dead;
 }
 
-template <int D>
+// Visible keys of a row and whether its cache can serve them: every key from
+// lo up to the newest cached position must own its slot.
+struct RowWin {
+  int lo, hi, tiles;     // tiles = 0 for a sequence the kernels skip
+  bool ok;
+};
+__device__ __forceinline__ RowWin row_window(const DecodeArgs& a, const RowInfo& ri, const kvq_seq_cache& c) {
+  const int p = ri.p, W = a.L.window;
+  const int lo = W > 0 ? max(0, p - W + 1) : 0, hi = p;
+  const bool ok = seq_ok(c) && p >= 0 && ri.newest < (1 << 24) && p <= ri.newest &&
+                  (ri.newest - lo + 1) <= c.capacity;
+  return {lo, hi, ok ? hi / kTileKeys - lo / kTileKeys + 1 : 0, ok};
+}
+
+// Stream-K schedule (a.sk_ctas > 0, decode rows only): the tiles of all
+// (row, kv head) units, concatenated in unit order (u = row * n_kv + kvh),
+// are cut into nc equal ranges, range c = [c*T/nc, (c+1)*T/nc) for CTA c.  A
+// CTA walks its range unit by unit; a unit that lies wholly inside the range
+// is written as final output, every other piece as a partial in slot 0 (the
+// range's first piece) or 1 (its last piece) of the CTA.  With equal rows
+// and at least as many CTAs as units, nc is a multiple of the unit count so
+// that no range crosses a unit boundary.  Every CTA computes the same plan
+// from the rows' positions; CTA 0 also stores it for the merge kernel:
+// plan[0] = T, plan[1] = nc, plan[2 + r] = tiles of rows < r (per kv head).
+// The walk's state lives in shared memory (it is read only between pieces):
+struct SkWalk {
+  long long b, e, pos;   // the CTA's range and the next tile to run
+  long long next;        // end of the current piece
+  int r, kvh;            // unit of tile `pos`
+};
+
+__device__ __forceinline__ long long sk_range_start(long long c, long long T, long long nc) { return c * T / nc; }
+// shared memory of the plan, at the end of the dynamic allocation: the row
+// prefix [n_rows + 1], three control ints, then the walk (8-byte aligned)
+__host__ __device__ constexpr int sk_plan_bytes(int n_rows) {
+  return (((n_rows + 5) & ~1) * 4 + (int)sizeof(SkWalk) + 127) & ~127;
+}
+
+template <int D, bool SK>
 __global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
 decode_kernel(const DecodeArgs a, const int smem_total) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int row = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
-  const RowInfo ri = row_info(a, row);
-  const kvq_seq_cache c = a.seqs[ri.s];
-  const int p = ri.p;
-  const int W = a.L.window;
-  const int lo = W > 0 ? max(0, p - W + 1) : 0, hi = p;
-  // every key from lo up to the newest cached position must own its slot
-  const bool ok = seq_ok(c) && p >= 0 && ri.newest < (1 << 24) && p <= ri.newest &&
-                  (ri.newest - lo + 1) <= c.capacity;
-  const int t_lo = lo / kTileKeys, t_hi = hi / kTileKeys;
-  const int ntiles = t_hi - t_lo + 1;
-  const int chunk = a.chunk_tiles > 0 ? a.chunk_tiles : (ntiles + a.splits - 1) / a.splits;
-  const int t_begin = t_lo + split * chunk;
-  const int n_my = ok ? max(0, min(chunk, t_hi + 1 - t_begin)) : 0;
-  if (n_my == 0) {
-    // nothing to read: an empty partial (m = -inf), or NaN for a bad sequence
-    if (!ok && split == 0 && kvh == 0 && threadIdx.x == 0) {
-      pdl_wait();                                   // after q prep has cleared the status word
-      flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+  constexpr bool sk = SK;
+  const int ring_smem = sk ? smem_total - sk_plan_bytes(a.n_rows) : smem_total;
+  const int n_kv = a.L.n_kv;
+  int row, kvh;
+  kvq_seq_cache c;
+  TileRange tr;
+  float* po;
+  float* ml;
+  bool final_out = false;
+  int* pr = reinterpret_cast<int*>(smem + ring_smem);        // [n_rows + 1] row tile prefix (stream-K)
+  SkWalk* wk = reinterpret_cast<SkWalk*>(pr + ((a.n_rows + 5) & ~1));
+  if constexpr (!SK) {
+    row = blockIdx.x; kvh = blockIdx.y;
+    const int split = blockIdx.z;
+    const RowInfo ri = row_info(a, row);
+    c = a.seqs[ri.s];
+    const RowWin rw = row_window(a, ri, c);
+    const int t_lo = rw.lo / kTileKeys;
+    const int chunk = a.chunk_tiles > 0 ? a.chunk_tiles : (rw.tiles + a.splits - 1) / a.splits;
+    const int t_begin = t_lo + split * chunk;
+    const int n_my = rw.ok ? max(0, min(chunk, t_lo + rw.tiles - t_begin)) : 0;
+    const size_t pidx = ((size_t)row * n_kv + kvh) * a.splits + split;
+    if (n_my == 0) {
+      // nothing to read: an empty partial (m = -inf), or NaN for a bad sequence
+      if (!rw.ok && split == 0 && kvh == 0 && threadIdx.x == 0) {
+        pdl_wait();                                   // after q prep has cleared the status word
+        flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+      }
+      if (threadIdx.x < 16) {
+        a.ws.part_ml[pidx * 32 + threadIdx.x] = rw.ok ? -INFINITY : __int_as_float(0x7fc00000);
+        a.ws.part_ml[pidx * 32 + 16 + threadIdx.x] = 0.f;
+      }
+      pdl_launch();
+      return;
     }
-    const size_t pidx = ((size_t)row * a.L.n_kv + kvh) * a.splits + split;
-    if (threadIdx.x < 16) {
-      a.ws.part_ml[pidx * 32 + threadIdx.x] = ok ? -INFINITY : __int_as_float(0x7fc00000);
-      a.ws.part_ml[pidx * 32 + 16 + threadIdx.x] = 0.f;
+    tr = TileRange{t_begin, n_my, rw.lo, rw.hi};
+    po = a.ws.part_o + pidx * 16 * D;
+    ml = a.ws.part_ml + pidx * 32;
+  } else {
+    // ---- the plan: tiles per row, prefix over rows ----
+    const int n_rows = a.n_rows, tid = threadIdx.x, NT = blockDim.x;
+    int* ctl = pr + a.n_rows + 1;                            // min tiles, max tiles, any bad row
+    if (tid == 0) { ctl[0] = 0x7fffffff; ctl[1] = 0; ctl[2] = 0; }
+    __syncthreads();
+    int mn = 0x7fffffff, mx = 0, bad = 0;
+    for (int r = tid; r < n_rows; r += NT) {
+      const RowWin rw = row_window(a, row_info(a, r), a.seqs[r]);
+      pr[r + 1] = rw.tiles;
+      mn = min(mn, rw.tiles); mx = max(mx, rw.tiles); bad |= !rw.ok;
     }
-    pdl_launch();
-    return;
+    atomicMin(ctl, mn); atomicMax(ctl + 1, mx);
+    if (bad) atomicOr(ctl + 2, 1);
+    __syncthreads();
+    if (tid < 32) {                                          // inclusive scan, lane l takes a block of rows
+      const int per = (n_rows + 31) / 32, r0 = min(n_rows, tid * per), r1 = min(n_rows, r0 + per);
+      int sum = 0;
+      for (int r = r0; r < r1; ++r) sum += pr[r + 1];
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      int run = incl - sum;
+      for (int r = r0; r < r1; ++r) { run += pr[r + 1]; pr[r + 1] = run; }
+      if (tid == 0) pr[0] = 0;
+    }
+    __syncthreads();
+    const long long T = (long long)n_kv * pr[n_rows];
+    const long long U = (long long)n_rows * n_kv;
+    long long nc = a.sk_ctas;
+    if (ctl[0] == ctl[1] && ctl[0] > 0 && U <= nc) {
+      // equal rows: a whole number of ranges per unit, none below kSkMinTiles
+      nc = U * max(1LL, min(nc / U, (long long)ctl[0] / kSkMinTiles));
+    } else {
+      nc = min(nc, max(1LL, T / kSkMinTiles));
+    }
+    if (blockIdx.x == 0) {
+      long long* plan = a.ws.plan;
+      for (int r = tid; r <= n_rows; r += NT) plan[2 + r] = pr[r];
+      if (tid == 0) { plan[0] = T; plan[1] = nc; }
+      if (ctl[2] && tid == 0) {
+        pdl_wait();                                          // after q prep has cleared the status word
+        flag_error(a.ws.status, KVQ_DEV_BADSEQ);
+      }
+    }
+    const long long cta = blockIdx.x;
+    const long long b = sk_range_start(cta, T, nc), e = sk_range_start(cta + 1, T, nc);
+    if (cta >= nc || b >= e) { pdl_launch(); return; }
+    if (tid == 0) {
+      // the row holding tile b: the largest r with n_kv * pr[r] <= b (it has tiles)
+      int lo_r = 0, hi_r = n_rows - 1;
+      while (lo_r < hi_r) {
+        const int mid = (lo_r + hi_r + 1) >> 1;
+        if ((long long)n_kv * pr[mid] <= b) lo_r = mid; else hi_r = mid - 1;
+      }
+      wk->b = b; wk->e = e; wk->pos = b;
+      wk->r = lo_r;
+      wk->kvh = (int)((b - (long long)n_kv * pr[lo_r]) / (pr[lo_r + 1] - pr[lo_r]));
+    }
+    __syncthreads();
   }
-  const int bits = c.bits;
-  const int nst = ring_slots(D, bits, smem_total);
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
+  // stream-K: the piece of the walk's current unit (every thread reads the
+  // walk; thread 0 records where the piece ends)
+  auto sk_piece = [&]() {
+    const int t = pr[wk->r + 1] - pr[wk->r];
+    const long long pu = (long long)n_kv * pr[wk->r] + (long long)wk->kvh * t;
+    const int s0 = (int)(wk->pos - pu), s1 = (int)(min(wk->e, pu + t) - pu);
+    row = wk->r; kvh = wk->kvh;
+    const RowInfo ri = row_info(a, row);
+    c = a.seqs[ri.s];
+    const RowWin rw = row_window(a, ri, c);
+    tr = TileRange{rw.lo / kTileKeys + s0, s1 - s0, rw.lo, rw.hi};
+    final_out = s0 == 0 && s1 == t;
+    const size_t pidx = (size_t)blockIdx.x * 2 + (pu > wk->b ? 1 : 0);
+    po = a.ws.part_o + pidx * 16 * D;
+    ml = a.ws.part_ml + pidx * 32;
+    if (threadIdx.x == 0) wk->next = pu + s1;
+  };
+  if constexpr (SK) sk_piece();
+  for (;;) {
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kMaxStages; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem) + i, 1);
+      fence_mbar_init();
     }
-    fence_mbar_init();
+    __syncthreads();
+    const int nst = ring_slots(D, c.bits, ring_smem);
+    const bool dead = c.bits == 4 ? decode_body<D, 4>(a, c, smem, nst, tr, row, kvh, po, ml, final_out)
+                                  : decode_body<D, 8>(a, c, smem, nst, tr, row, kvh, po, ml, final_out);
+    if (!SK || dead) break;
+    // every thread is past its reads of the walk (decode_body has block
+    // barriers); thread 0 moves it to the next unit with tiles
+    if (threadIdx.x == 0) {
+      wk->pos = wk->next;
+      if (wk->pos < wk->e && ++wk->kvh == n_kv) {
+        wk->kvh = 0;
+        do { ++wk->r; } while (pr[wk->r + 1] == pr[wk->r]);
+      }
+    }
+    // every read of the ring and of the staged partial is done, and the
+    // generic-proxy writes are ordered before the next bulk copies
+    fence_proxy_async();
+    __syncthreads();
+    if (wk->pos >= wk->e) break;
+    sk_piece();
   }
-  __syncthreads();
-  const TileRange tr{t_begin, n_my, lo, hi};
-  if (bits == 4) decode_body<D, 4>(a, c, smem, nst, tr, row, kvh, split);
-  else decode_body<D, 8>(a, c, smem, nst, tr, row, kvh, split);
 }
 
 // ----------------------------------------------------------------------------
@@ -655,6 +814,75 @@ combine_kernel(const DecodeArgs a) {
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
 }
 
+// Stream-K merge: one block per (row, q head) of a unit whose tiles were
+// split between CTAs c_first .. c_last (a unit inside one CTA was written
+// by the attention kernel).  CTA c's piece of the unit is its slot 0 unless
+// the unit starts after c's range start (slot 1).
+__device__ __forceinline__ long long sk_cta_of(long long x, long long T, long long nc) {
+  return ((x + 1) * nc - 1) / T;                 // the largest c with c*T/nc <= x
+}
+
+template <int D>
+__global__ void __launch_bounds__(D)
+combine_sk_kernel(const DecodeArgs a) {
+  __shared__ float wsm[1024];
+  __shared__ int pid[1024];
+  __shared__ float inv_l;
+  pdl_wait();
+  const int row = blockIdx.x, hq = blockIdx.y;
+  const int G = a.L.G, kvh = hq / G, r = hq % G, n_kv = a.L.n_kv;
+  const long long* plan = a.ws.plan;
+  const long long T = plan[0], nc = plan[1];
+  const long long p0 = plan[2 + row], t = plan[3 + row] - p0;
+  const size_t oi = ((size_t)row * a.L.n_q + hq) * D + threadIdx.x;
+  if (t == 0) {                                  // a skipped sequence
+    if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = __int_as_float(0x7fc00000);
+    else reinterpret_cast<uint16_t*>(a.out)[oi] = 0x7fc0u;
+    return;
+  }
+  const long long pu = n_kv * p0 + kvh * t;
+  const long long c0 = sk_cta_of(pu, T, nc), c1 = sk_cta_of(pu + t - 1, T, nc);
+  if (c0 == c1) return;
+  const int S = (int)(c1 - c0 + 1);              // <= nc <= 1024
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    const long long cc = c0 + i;
+    pid[i] = (int)(cc * 2 + (pu > cc * T / nc ? 1 : 0));
+  }
+  __syncthreads();
+  auto piece = [&](int i) -> size_t { return (size_t)pid[i]; };
+  if (threadIdx.x < 32) {
+    float M = -INFINITY;
+    for (int i = threadIdx.x; i < S; i += 32) M = fmaxf(M, a.ws.part_ml[piece(i) * 32 + r]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int i = threadIdx.x; i < S; i += 32) {
+      const size_t pi = piece(i);
+      const float m = a.ws.part_ml[pi * 32 + r];
+      const float w = m == -INFINITY ? 0.f : exp2f((m - M) * 1.4426950408889634f);
+      wsm[i] = w;
+      L += w * a.ws.part_ml[pi * 32 + 16 + r];
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (threadIdx.x == 0) inv_l = 1.f / L;
+  }
+  __syncthreads();
+  const int d = threadIdx.x;
+  float acc0 = 0.f, acc1 = 0.f;
+  int i = 0;
+  for (; i + 2 <= S; i += 2) {
+    const float o0 = a.ws.part_o[(piece(i) * 16 + r) * D + d];
+    const float o1 = a.ws.part_o[(piece(i + 1) * 16 + r) * D + d];
+    acc0 = fmaf(wsm[i], o0, acc0);
+    acc1 = fmaf(wsm[i + 1], o1, acc1);
+  }
+  if (i < S) acc0 = fmaf(wsm[i], a.ws.part_o[(piece(i) * 16 + r) * D + d], acc0);
+  const float o = (acc0 + acc1) * inv_l;
+  if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
+  else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
+}
+
 template <int D>
 constexpr int decode_smem_bytes() {
   // D = 512: one CTA per SM with the largest shared carve-out; smaller head
@@ -667,6 +895,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   static_assert(D % 64 == 0, "");
   static_assert(ring_slots(D, 8, decode_smem_bytes<D>()) >= 2 && ring_slots(D, 4, decode_smem_bytes<D>()) >= 2,
                 "the pipeline needs at least two stages");
+  static_assert(ring_slots(D, 8, decode_smem_bytes<D>() - sk_plan_bytes(kSkMaxRows)) >= 2,
+                "the stream-K plan leaves two stages");
   cudaError_t e;
   const int smem = decode_smem_bytes<D>();
   static bool attr_set[64] = {};
@@ -674,7 +904,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -687,37 +919,42 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_rows, a.L.n_kv, a.splits);
+  cfg.gridDim = a.sk_ctas > 0 ? dim3(a.sk_ctas) : dim3(a.n_rows, a.L.n_kv, a.splits);
   cfg.blockDim = dim3(Dec<D>::THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, smem);
+  e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true>, a, smem)
+                    : cudaLaunchKernelEx(&cfg, decode_kernel<D, false>, a, smem);
   if (e != cudaSuccess) return e;
 
   cfg.gridDim = dim3(a.n_rows, a.L.n_q);
   cfg.blockDim = dim3(D);
   cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
+  e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D>, a) : cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
   return e;
 }
 
 }  // namespace
 
-size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits) {
+size_t decode_ws_bytes(int n_rows, int n_kv, int D, const DecodePlan& plan) {
   const size_t NG = D / 64, B = (size_t)n_rows * n_kv;
+  // partial pieces: per (row, kv head, split), or two per stream-K CTA
+  const size_t pieces = plan.sk_ctas > 0 ? (size_t)plan.sk_ctas * 2 : B * plan.splits;
   size_t off = 256;
   off += B * NG * 4 * 32 * 16;                 // qfrag
   off += B * 32 * 16;                          // qbias
   off = (off + 255) & ~size_t(255);
-  off += B * splits * 16 * (size_t)D * 4;      // part_o
-  off += B * splits * 32 * 4;                  // part_ml
+  off += pieces * 16 * (size_t)D * 4;          // part_o
+  off += pieces * 32 * 4;                      // part_ml
+  off += ((size_t)n_rows + 3) * 8;             // plan
   return off;
 }
 
-DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
+DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, const DecodePlan& plan) {
   const size_t NG = D / 64, B = (size_t)n_rows * n_kv;
+  const size_t pieces = plan.sk_ctas > 0 ? (size_t)plan.sk_ctas * 2 : B * plan.splits;
   uint8_t* p = static_cast<uint8_t*>(base);
   DecodeWs w = {};
   w.status = reinterpret_cast<uint32_t*>(p);
@@ -728,8 +965,10 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits) {
   off += B * 32 * 16;
   off = (off + 255) & ~size_t(255);
   w.part_o = reinterpret_cast<float*>(p + off);
-  off += B * splits * 16 * (size_t)D * 4;
+  off += pieces * 16 * (size_t)D * 4;
   w.part_ml = reinterpret_cast<float*>(p + off);
+  off += pieces * 32 * 4;
+  w.plan = reinterpret_cast<long long*>(p + off);
   return w;
 }
 
@@ -743,7 +982,13 @@ DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms
   const long base = std::max<long>((long)n_rows * L.n_kv, 1);
   const long wave = std::max<long>(1, ((long)num_sms * per_sm) / base);   // splits that still fit one wave
   DecodePlan plan;
-  if (fixed_chunks) {
+  plan.sk_ctas = 0;
+  if (fixed_chunks && n_rows <= kSkMaxRows && tiles > kChunkTiles) {
+    // long rows: stream-K over one wave of CTAs
+    plan.sk_ctas = std::max(1, std::min(1024, num_sms * per_sm));
+    plan.splits = 1;
+    plan.chunk_tiles = 0;
+  } else if (fixed_chunks) {
     // every split takes the same number of tiles: rows shorter than the
     // longest use fewer splits and their surplus CTAs exit at once, so ragged
     // batches balance through the block scheduler

@@ -41,6 +41,8 @@ struct DecodeWs {
   uint4* qbias;         // [n_rows][n_kv][32] x uint4: A fragment of the QK bias term
   float* part_o;        // [n_rows][n_kv][splits][16][D]
   float* part_ml;       // [n_rows][n_kv][splits][2][16]  (m, l)
+                        // stream-K: part_o / part_ml hold [ctas][2] pieces instead
+  long long* plan;      // stream-K: T, nc, then the row tile prefix [n_rows + 1]
   // prompt-chunk tensor-core path only
   uint16_t* q16;        // [n_rows][n_q][D] q_hat as f16
   float* qsum;          // [n_rows][n_q][D/64] per-group sums of those f16 values
@@ -65,13 +67,18 @@ struct DecodeArgs {
   uint16_t* q_prepped;
   int splits;
   int chunk_tiles;      // > 0: every split covers this many tiles; 0: ceil(row tiles / splits)
+  int sk_ctas;          // > 0: stream-K schedule over this many CTAs (splits / chunk_tiles unused)
   DecodeWs ws;
 };
 
-size_t decode_ws_bytes(int n_rows, int n_kv, int D, int splits);
-DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, int splits);
 constexpr int kChunkTiles = 48;   // target tiles per split when the longest row is known
-struct DecodePlan { int splits, chunk_tiles; };
+// Stream-K decode: used for decode calls whose longest row spans several
+// chunks and whose row count fits the plan held in shared memory.
+constexpr int kSkMaxRows = 1024;
+constexpr int kSkMinTiles = 16;   // shortest range per CTA
+struct DecodePlan { int splits, chunk_tiles, sk_ctas; };
+size_t decode_ws_bytes(int n_rows, int n_kv, int D, const DecodePlan& plan);
+DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, const DecodePlan& plan);
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks);
 
 // Prompt chunks on the tensor cores (tcgen05): head_dim <= 256 and G | 128.

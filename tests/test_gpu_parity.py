@@ -83,6 +83,50 @@ def test_decode_small(kvq, name):
     print(name, "worst", worst)
 
 
+# Batches whose longest row spans more than one 48-tile chunk take the
+# stream-K schedule: equal tile ranges per CTA across (row, kv head) units,
+# rows inside one range written directly, the others merged from pieces.
+STREAM_K_CASES = {
+    "sk-ragged-d512-keqv": (_spec(16, 1, 512, 0, 128, 1e6, True),
+                            [3100, 20, 500, 4000, 64, 3500, 0, 700], [4, 8, 8, 4, 4, 8, 4, 8]),
+    "sk-ragged-d256-full": (_spec(8, 2, 256, 0, 256), [3300, 100, 2000, 3999, 63], [8, 4, 4, 8, 8]),
+    "sk-equal-rows-d512": (_spec(16, 1, 512, 0, 128, 1e6, True), [3500] * 4, [4, 8, 4, 8]),
+    "sk-gqa8-d128": (_spec(8, 1, 128, 0, 128), [5000, 3072, 3073, 17], [8, 4, 8, 4]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(STREAM_K_CASES))
+def test_decode_stream_k(kvq, name):
+    _, harness = kvq
+    spec, filled, bits = STREAM_K_CASES[name]
+    wl = W.DecodeWorkload(name, 78, spec, filled=filled, bits=bits)
+    _, worst = check_decode(harness, wl, check_fill=False)
+    print(name, "worst", worst)
+
+
+def test_stream_k_bad_descriptor_is_nan(kvq):
+    """A skipped sequence inside a stream-K batch: NaN rows, status bit set,
+    the other rows unaffected."""
+    _, harness = kvq
+    spec = _spec(16, 1, 512, 0, 128, 1e6, True)
+    wl = W.DecodeWorkload("sk-bad", 83, spec, filled=[3200, 3300, 100], bits=[8, 4, 8])
+    case = harness.DecodeCase(wl)
+    case.step()
+    torch.cuda.synchronize()
+    good = case.out.cpu().numpy().copy()
+    raw = case.caches.desc.cpu().numpy().copy()
+    bad = raw.copy()
+    bad[56 + 48:56 + 52] = np.frombuffer(np.int32(5).tobytes(), np.uint8)      # seq 1: bits = 5
+    case.caches.desc.copy_(torch.from_numpy(bad))
+    case.attend()
+    torch.cuda.synchronize()
+    out = case.out.cpu().numpy()
+    assert np.all(np.isnan(out[1]))
+    # the other rows' tiles are split at other points now: equal up to rounding
+    assert np.allclose(out[0], good[0], atol=1e-4) and np.allclose(out[2], good[2], atol=1e-4)
+    assert case.status_word() & (1 << 2)
+
+
 def test_decode_bf16_output_is_rounded_f32(kvq):
     _, harness = kvq
     spec, filled, bits = DECODE_CASES["sliding-ring-wrap"]
