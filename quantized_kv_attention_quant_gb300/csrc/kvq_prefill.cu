@@ -5,8 +5,9 @@
 //
 // One CTA takes 128 query rows that share a kv head: 128/G consecutive tokens
 // of one sequence times its G q heads (row r = token r / G, head r % G), with
-// two threads per row (warps w and w + 4 reach the same tensor-memory lanes;
-// each takes half of the row's keys and output dims).  It walks the keys its
+// kNQ threads per row (warps w, w + 4, w + 8, ... reach the same
+// tensor-memory lanes; each takes a 1/kNQ share of the row's keys and output
+// dims).  It walks the keys its
 // rows can see in 64-key tiles:
 //   1. TMA bulk copies bring the tile's packed codes and bf16 scale/bias
 //      blocks into a staging area (prefetched one tile ahead).
@@ -39,7 +40,9 @@ namespace kvq {
 namespace {
 
 constexpr int kRows = 128;      // MMA rows per CTA
-constexpr int kThreads = 256;   // two threads per row: warps w and w + 4 share tensor-memory lanes
+constexpr int kNQ = 4;                  // threads per row: warps w + 4i share tensor-memory lanes
+constexpr int kThreads = kRows * kNQ;
+constexpr int kKPT = 64 / kNQ;          // keys of a tile per thread
 
 template <int D>
 struct Pf {
@@ -54,8 +57,8 @@ struct Pf {
   static constexpr int S_OFF = P_OFF + 16384;           // staging: K codes, V codes, 4 scale/bias blocks
   static constexpr int STAGE = 2 * 64 * RB8 + 4 * SB;
   static constexpr int T_OFF = S_OFF + STAGE;           // K scale, K bias as f32 [2][NG][64]
-  static constexpr int X_OFF = T_OFF + 2 * 64 * NG * 4; // row exchange between the two halves [2][128] f32
-  static constexpr int C_OFF = X_OFF + 2 * 128 * 4;     // 3 mbarriers and the tensor-memory address
+  static constexpr int X_OFF = T_OFF + 2 * 64 * NG * 4; // row exchange between a row's threads [kNQ][128] f32
+  static constexpr int C_OFF = X_OFF + kNQ * 128 * 4;   // 3 mbarriers and the tensor-memory address
   static constexpr int BYTES = C_OFF + 64 + 1024;       // + room to align the base
   static constexpr int TMEM_COLS = 2 * D;               // group products (NG x 64) then the output (D)
 };
@@ -86,7 +89,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   uint64_t* bar_s = bar_tma + 1;
   uint64_t* bar_o = bar_tma + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P::C_OFF + 24);
-  float* xr = reinterpret_cast<float*>(sm + P::X_OFF);    // [2][128] row exchange
+  float* xr = reinterpret_cast<float*>(sm + P::X_OFF);    // [kNQ][128] row exchange
   float* skf = reinterpret_cast<float*>(sm + P::T_OFF);   // [NG][64] K scale as f32
   float* bkf = skf + 64 * NG;                             // [NG][64] K bias as f32
   uint8_t* stg = sm + P::S_OFF;
@@ -98,8 +101,9 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const uint16_t* stg_vb = stg_vs + 64 * NG;
   const uint32_t base = smem_u32(sm);
 
-  // ---- this thread's row (half hf of its keys and output dims) and the CTA's key range ----
+  // ---- this thread's row (share hf of its keys and output dims) and the CTA's key range ----
   const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
+  constexpr int DPT = D / kNQ;                            // output dims per thread
   const int tq = r / G, h = r % G;
   const int t = t0 + tq;
   const bool row_valid = t < rows_s;
@@ -119,8 +123,8 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const size_t head_row0 = (size_t)kvh * cap;
   const int hq = kvh * G + h;
   const size_t grow = (size_t)__ldg(a.row_offsets + s) + t;     // global query row
-  const int kk0 = 32 * hf;                                // this thread's keys of a tile
-  const int dd0 = (D / 2) * hf;                           // this thread's output dims
+  const int kk0 = kKPT * hf;                              // this thread's keys of a tile
+  const int dd0 = DPT * hf;                               // this thread's output dims
 
   // 16-byte stores when the output allows them (the API asks only for element alignment)
   const bool out_vec = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
@@ -149,7 +153,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __int_as_float(0x7fc00000);
-    for (int d0 = dd0; d0 < dd0 + D / 2; d0 += 16) write_row(v, d0);
+    for (int d0 = dd0; d0 < dd0 + DPT; d0 += 16) write_row(v, d0);
   };
   if (n_tiles == 0) {                                     // uniform over the CTA
     if (row_valid) write_nan_half();
@@ -183,14 +187,14 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   const uint32_t tmem = *tslot;
   if (tid == 0) issue_tile(0);
 
-  // Q rows as f16 (each thread half of its row's chunks).  With 4-bit codes
+  // Q rows as f16 (each thread a 1/kNQ share of its row's chunks).  With 4-bit codes
   // the K conversion yields the dims of each 8-dim chunk in the order
   // 0 4 1 5 2 6 3 7; Q uses the same order.
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.ws.q16 + (grow * a.L.n_q + hq) * D);
 #pragma unroll 4
 #pragma unroll 1
-    for (int ch = hf * (D / 16); ch < (hf + 1) * (D / 16); ++ch) {
+    for (int ch = hf * (D / 8 / kNQ); ch < (hf + 1) * (D / 8 / kNQ); ++ch) {
       uint4 v = row_valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
       if (BITS == 4)
         v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
@@ -312,10 +316,10 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     wait(bar_s, ph_s);
     tc::fence_after_sync();
 
-    // ---- scores of this thread's 32 keys ----
-    float S[32];
+    // ---- scores of this thread's kKPT keys ----
+    float S[kKPT];
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
+    for (int q4 = 0; q4 < kKPT / 4; ++q4) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
@@ -327,12 +331,12 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     }
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      float v[2][16];
-      tc::ld_x16(lane_base + g * 64 + kk0, v[0]);
-      tc::ld_x16(lane_base + g * 64 + kk0 + 16, v[1]);
+      float v[kKPT / 16][16];
+#pragma unroll
+      for (int u = 0; u < kKPT / 16; ++u) tc::ld_x16(lane_base + g * 64 + kk0 + 16 * u, v[u]);
       tc::wait_ld();
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
+      for (int q4 = 0; q4 < kKPT / 4; ++q4) {
         const float4 s4 = *reinterpret_cast<const float4*>(skf + g * 64 + kk0 + 4 * q4);
         const float* vv = &v[q4 >> 2][4 * (q4 & 3)];
         S[4 * q4] = fmaf(s4.x, vv[0], S[4 * q4]);
@@ -342,22 +346,23 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       }
     }
     float mt = -INFINITY;
-    // keys outside a row's window: only where the 32 keys are not all visible
-    // to every row of the warp (interior tiles skip the masks)
-    if (__all_sync(0xffffffffu, row_live && tpos0 + kk0 >= lo_r && tpos0 + kk0 + 31 <= p_r)) {
+    // keys outside a row's window: only where the thread's keys are not all
+    // visible to every row of the warp (interior tiles skip the masks)
+    if (__all_sync(0xffffffffu, row_live && tpos0 + kk0 >= lo_r && tpos0 + kk0 + kKPT - 1 <= p_r)) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mt = fmaxf(mt, S[j]);
+      for (int j = 0; j < kKPT; ++j) mt = fmaxf(mt, S[j]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < kKPT; ++j) {
         const int kp = tpos0 + kk0 + j;
         S[j] = (row_live && kp >= lo_r && kp <= p_r) ? S[j] : -INFINITY;
         mt = fmaxf(mt, S[j]);
       }
     }
     xr[hf * 128 + r] = mt;
-    __syncthreads();                                      // row maxima of both halves
-    mt = fmaxf(mt, xr[(hf ^ 1) * 128 + r]);
+    __syncthreads();                                      // row maxima of every share
+#pragma unroll
+    for (int i = 1; i < kNQ; ++i) mt = fmaxf(mt, xr[((hf + i) % kNQ) * 128 + r]);
     // a new reference for this row; its output row is rescaled unless it had
     // no visible key before (tensor-memory loads and stores are warp-wide:
     // the whole warp takes part, with factor 1 for rows that keep theirs)
@@ -369,7 +374,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
       m_ref = mt;
     }
     if (__any_sync(0xffffffffu, rescale_o)) {
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < DPT / 16; ++cc) {
         float v[16];
         tc::ld_x16(lane_base + D + dd0 + 16 * cc, v);
         tc::wait_ld();
@@ -381,7 +386,7 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
     }
     // ---- P = e^(S - ref) as f16 ----
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 0; ch < kKPT / 8; ++ch) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -396,7 +401,8 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
         l_part += pf.x + pf.y;
         w[e] = *reinterpret_cast<const uint32_t*>(&hp);
       }
-      *reinterpret_cast<uint4*>(sm + P::P_OFF + tc::sw128_off(r, 4 * hf + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(sm + P::P_OFF + tc::sw128_off(r, (kKPT / 8) * hf + ch)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async();
     tc::fence_before_sync();
@@ -418,11 +424,14 @@ __device__ __forceinline__ void prefill_body(const DecodeArgs& a, uint8_t* sm, c
   wait(bar_o, ph_o);                                      // the last PV
   tc::fence_after_sync();
 
-  // ---- output: O / l, each thread half of its row's dims ----
+  // ---- output: O / l, each thread a 1/kNQ share of its row's dims ----
   xr[hf * 128 + r] = l_part;
   __syncthreads();
-  const float inv = 1.f / (l_part + xr[(hf ^ 1) * 128 + r]);
-  for (int cc = 0; cc < D / 32; ++cc) {
+  float l_row = l_part;
+#pragma unroll
+  for (int i = 1; i < kNQ; ++i) l_row += xr[((hf + i) % kNQ) * 128 + r];
+  const float inv = 1.f / l_row;
+  for (int cc = 0; cc < DPT / 16; ++cc) {
     float v[16];
     tc::ld_x16(lane_base + D + dd0 + 16 * cc, v);
     tc::wait_ld();
