@@ -28,6 +28,8 @@ struct App {
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* off, int n_seqs, int row) {
+  // one row per sequence (decode steps) needs one round trip: off[row] == row
+  if (row < n_seqs && __ldg(off + row) == row && __ldg(off + row + 1) > row) return row;
   int lo = 0, hi = n_seqs - 1;          // largest s with off[s] <= row
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -135,6 +137,25 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   const int kind = item & 1;             // 0: K, 1: V
   const int head = item >> 1;
 
+  // the raw row and the norm weight first: their latency overlaps the
+  // sequence lookup and the angles
+  float x[E], wk[E];
+  if (active) {
+    const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
+    src += ((size_t)row * Hkv + head) * D + tt * E;
+#pragma unroll
+    for (int v = 0; v < E; v += 2) {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src + v));
+      x[v] = bf16lo_to_f(u);
+      x[v + 1] = bf16hi_to_f(u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < E; ++i) wk[i] = kind == 0 ? bf16_to_f(__ldg(a.k_w + tt * E + i)) : 1.f;
+
   const int s = find_seq(a.row_offsets, a.n_seqs, row);
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
   const int t_in = row - off0, rows_s = off1 - off0;
@@ -161,22 +182,6 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
     }
   }
 
-  // ---- load the raw row ----
-  float x[E];
-  if (active) {
-    const uint16_t* src = (kind == 0 || a.L.k_eq_v) ? a.k_raw : a.v_raw;
-    src += ((size_t)row * Hkv + head) * D + tt * E;
-#pragma unroll
-    for (int v = 0; v < E; v += 2) {
-      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src + v));
-      x[v] = bf16lo_to_f(u);
-      x[v + 1] = bf16hi_to_f(u);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < E; ++i) x[i] = 0.f;
-  }
-
   // ---- RMSNorm (weight on K only) ----
   ff ss = {0.f, 0.f};
 #pragma unroll
@@ -192,10 +197,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   const ff inv = rms_inv(ss, D, a.L.eps);
   uint16_t y[E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const float w = kind == 0 ? bf16_to_f(__ldg(a.k_w + tt * E + i)) : 1.f;
-    y[i] = norm_scale_bf16(x[i], w, inv);
-  }
+  for (int i = 0; i < E; ++i) y[i] = norm_scale_bf16(x[i], wk[i], inv);
 
   // ---- RoPE on K ----
   if (R > 0) {

@@ -96,6 +96,23 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   const int hq = blockIdx.y * hpb + hl;                   // q head of this thread
   const bool active = hl < hpb && hq < a.L.n_q;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
+  // the raw row and the norm weight first: their latency overlaps the row
+  // lookup and the angles
+  float x[E], wq[E];
+  if (active) {
+    const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + tt * E;
+#pragma unroll
+    for (int v = 0; v < E; v += 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(src + v);
+      x[v] = bf16lo_to_f(u);
+      x[v + 1] = bf16hi_to_f(u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < E; ++i) wq[i] = bf16_to_f(a.q_w[tt * E + i]);
   const RowInfo ri = row_info(a, row);
   const int bits = a.seqs[ri.s].bits;
   const int pc = min(max(ri.p, 0), (1 << 24) - 1);
@@ -114,21 +131,8 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   // ---- RMSNorm of this thread's E elements ----
   uint16_t y[E];
   ff ss = {0.f, 0.f};
-  float x[E];
-  if (active) {
-    const uint16_t* src = a.q_raw + ((size_t)row * a.L.n_q + hq) * D + tt * E;
 #pragma unroll
-    for (int v = 0; v < E; v += 2) {
-      const uint32_t u = *reinterpret_cast<const uint32_t*>(src + v);
-      x[v] = bf16lo_to_f(u);
-      x[v + 1] = bf16hi_to_f(u);
-    }
-#pragma unroll
-    for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < E; ++i) x[i] = 0.f;
-  }
+  for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
   ss = ff_warp_sum(ss);
   if constexpr (Q::HW > 1) {
     if (lane == 0 && hl < Q::HPB) red[hl][(tt >> 5)] = ss;
@@ -144,7 +148,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
     const ff inv = rms_inv(ss, D, a.L.eps);
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-      y[i] = norm_scale_bf16(x[i], bf16_to_f(a.q_w[tt * E + i]), inv);
+      y[i] = norm_scale_bf16(x[i], wq[i], inv);
       qh[tt * E + i] = y[i];
     }
   }
