@@ -126,7 +126,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   constexpr int E = A::E, TH = A::TH;
   __shared__ uint16_t normed[A::IPB * D];
   __shared__ float4 cs[D / 2];            // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
-  __shared__ float freq[D / 2][3];        // rotary frequency triples
+  __shared__ __align__(16) float freq[D / 2][3];   // rotary frequency triples
   __shared__ ff red[A::IPB][A::HW];
   const int tid = threadIdx.x, il = tid / TH, tt = tid % TH, lane = tid & 31;
   const int R = a.L.rope_dims, half = R >> 1;

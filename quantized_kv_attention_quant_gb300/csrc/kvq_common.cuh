@@ -208,14 +208,21 @@ __device__ __forceinline__ void rope_cos_sin(int p, float f1, float f2, float f3
 }
 
 // Copy rope_dims/2 frequency triples from the kernel-parameter table into
-// shared memory.  Every read of the parameter block is warp-uniform (a lane
-// index into it would serialise on the constant cache); call from all threads
-// of the block, followed by a block barrier.
+// shared memory (16-byte aligned on both sides), 16 bytes per read.  Every
+// read of the parameter block is warp-uniform (a lane index into it would
+// serialise on the constant cache) and four are in flight at a time; call
+// from all threads of the block, followed by a block barrier.
 __device__ __forceinline__ void stage_freqs(const float (*f)[3], int half, float (*dst)[3]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int j = warp; j < half; j += nw) {
-    const float a = f[j][0], b = f[j][1], c = f[j][2];
-    if (lane == 0) { dst[j][0] = a; dst[j][1] = b; dst[j][2] = c; }
+  const float4* src4 = reinterpret_cast<const float4*>(&f[0][0]);
+  float4* dst4 = reinterpret_cast<float4*>(&dst[0][0]);
+  // up to 3 floats past 3*half: still inside the 256-triple table and inside
+  // dst, which holds D/2 triples (3*D/2 is a multiple of 4)
+  const int n4 = (3 * half + 3) / 4;
+#pragma unroll 4
+  for (int k = warp; k < n4; k += nw) {
+    const float4 v = src4[k];
+    if (lane == 0) dst4[k] = v;
   }
 }
 

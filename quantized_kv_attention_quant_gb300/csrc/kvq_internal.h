@@ -12,7 +12,7 @@ constexpr int kTileKeys = 64;       // keys per pipeline tile; capacities are mu
 constexpr int kMaxG = 16;           // q heads per kv head handled by one MMA row block
 
 // theta^(-2j/D) for j < rope_dims/2, each as an exact sum of three floats.
-struct RopeFreqs {
+struct alignas(16) RopeFreqs {
   float f[kMaxRopeHalf][3];
 };
 

@@ -84,7 +84,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   constexpr int E = Q::E, NG = D / 64, TH = Q::TH;
   __shared__ uint16_t qn[Q::HPB * D];      // normed, then q_hat, per head of the block
   __shared__ float4 cs[D / 2];             // (cos.hi, cos.lo, sin.hi, sin.lo) per rotated pair
-  __shared__ float freq[D / 2][3];
+  __shared__ __align__(16) float freq[D / 2][3];
   __shared__ ff red[Q::HPB][Q::HW];
   __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
   const int row = blockIdx.x;
