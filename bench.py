@@ -241,6 +241,26 @@ def build_workload(name: str, rank: int, device):
                 "dominant": f"decode_kernel<{spec.head_dim}>", "launches": 1 + 3,
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs}}
         return case, [(True, case)], info
+    if name == "mixed":
+        dwl, pwl = W.workload_mixed_step()
+        case = harness.MixedCase([dwl, pwl], device=device, out_f32=False)
+        spec = dwl.layer
+        dec_by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
+                     for p, b in zip(dwl.filled, dwl.bits)) * spec.n_kv_heads
+        # the window group reads each sequence's keys once: the window before
+        # its first row through its last row
+        win_by = sum(min(pwl.filled[s] + pwl.chunk[s], spec.window + pwl.chunk[s] - 1) *
+                     rb_pair(spec.head_dim, pwl.bits[s]) for s in range(pwl.n_seqs)) * spec.n_kv_heads
+        info = {"tokens": dwl.n_seqs + int(sum(pwl.chunk)), "kv_bytes": dec_by + win_by,
+                "dominant_bytes": dec_by + win_by,
+                "dominant": "attn_mixed call (decode group: decode_kernel<256>; window group: prefill_tc_kernel<256>)",
+                "launches": 2 + 3 + 2, "mixed": True,
+                "config": {"workload": "mixed step of one sliding layer (8q/2kv D256 W512): decode group of "
+                                       f"{dwl.n_seqs} sequences (lengths U[1024,8192]) + window group of 2 prompt "
+                                       "chunks of 256 rows, one attn_mixed call",
+                           "n_seqs": dwl.n_seqs + pwl.n_seqs, "decode_rows": dwl.n_seqs,
+                           "window_rows": int(sum(pwl.chunk))}}
+        return case, [(True, case)], info
     if name == "prefill":
         wl = W.workload_prefill_chunk()
         case = harness.PrefillCase(wl, device=device, out_f32=False)
@@ -255,6 +275,9 @@ def build_workload(name: str, rank: int, device):
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     raise SystemExit(f"unknown workload {name}")
+
+
+METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)"}
 
 
 def step_calls(calls, stream=None):
@@ -339,6 +362,30 @@ def run_gpu(args):
         torch.cuda.synchronize()
         dist_barrier(world, device)
     value, ms_step = whole_job_rate(info["tokens"], t0.elapsed_time(t1), K, world, device)
+    serial_ms = None
+    if info.get("mixed"):
+        # the same steps with every group as its own call on one stream
+        # (with the same timing events around the attention calls as the
+        # timed graph, so that both graphs have the same structure)
+        g_ser = torch.cuda.CUDAGraph()
+        ev_ser = [ev_pair() for _ in range(K)] if have_inner else None
+        with torch.cuda.graph(g_ser, stream=stream):
+            for k in range(K):
+                for _, c in calls:
+                    c.append()
+                    if ev_ser:
+                        ev_ser[k][0].record()
+                    c.attend_serial()
+                    if ev_ser:
+                        ev_ser[k][1].record()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(replay_stream)
+        g_ser.replay()
+        a1.record(replay_stream)
+        torch.cuda.synchronize()
+        serial_ms = a0.elapsed_time(a1) / K
+        del g_ser
 
     # dominant-kernel duration from the events inside the graph
     dom_ms = None
@@ -354,7 +401,8 @@ def run_gpu(args):
                      "other_attention_calls_ms": sum(a.elapsed_time(b) for row in ev_oth for a, b in row) / K,
                      "append_calls_ms": sum(a.elapsed_time(b) for row in ev_app for a, b in row) / K}
         del graph_bd
-    status_ok = all(c.status_word() == 0 for _, c in calls)
+    status_ok = all(all(w == 0 for w in (c.status_words() if hasattr(c, "status_words") else [c.status_word()]))
+                    for _, c in calls)
 
     # e2e through the binding with host buffers
     e2e = run_e2e(calls, K, device, info, world)
@@ -387,10 +435,12 @@ def run_gpu(args):
                 "inputs smaller than L2 (launch-bound case)",
                 "kv_bytes_per_step": info["kv_bytes"], "step_kv_gbs": step_gbs,
                 "graph": f"{K} steps captured in one CUDA graph", "device_status_clean": status_ok})
+    if serial_ms is not None:
+        cfg["separate_calls_ms_per_step"] = serial_ms
     if breakdown:
         cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in breakdown.items()}
         cfg["step_breakdown_note"] = "separate replay with events around every call (they slow it down)"
-    line = {"metric": "decode-attention tokens/s" if args.workload != "prefill" else "prefill tokens/s",
+    line = {"metric": METRIC.get(args.workload, "decode-attention tokens/s"),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic (seeded N(0,1) bf16 inputs, norm weights 1+N(0,0.1))",
@@ -398,6 +448,17 @@ def run_gpu(args):
             "gpu_launches": info["launches"] * K, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def call_inputs(donor, c):
+    """Device inputs a call reads each step (q; plus k/v rows when it appends)."""
+    if hasattr(c, "inputs"):
+        return c.inputs()
+    return [c.q] + ([c.k] + ([c.v] if c.v is not None else []) if donor else [])
+
+
+def call_outputs(c):
+    return c.outputs() if hasattr(c, "outputs") else [c.out]
 
 
 def run_e2e(calls, K, device, info, world):
@@ -413,11 +474,10 @@ def run_e2e(calls, K, device, info, world):
     import torch
     host_in, host_out = [], []
     for donor, c in calls:
-        ins = [c.q] + ([c.k] + ([c.v] if c.v is not None else []) if donor else [])
-        host_in.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins])
-        host_out.append(torch.empty(c.out.shape, dtype=c.out.dtype, pin_memory=True))
+        host_in.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in call_inputs(donor, c)])
+        host_out.append([torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in call_outputs(c)])
     bi = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
-    bo = sum(t.numel() * t.element_size() for t in host_out)
+    bo = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
     cap = torch.cuda.Stream(device)
     cin, cout = torch.cuda.Stream(device), torch.cuda.Stream(device)
     n = len(calls)
@@ -436,8 +496,7 @@ def run_e2e(calls, K, device, info, world):
                 for L, ((donor, c), hs) in enumerate(zip(calls, host_in)):
                     if done[L] is not None:
                         cin.wait_event(done[L])
-                    devs = [c.q] + ([c.k] + ([c.v] if c.v is not None else []) if donor else [])
-                    for d, h in zip(devs, hs):
+                    for d, h in zip(call_inputs(donor, c), hs):
                         d.copy_(h, non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(cin)
@@ -454,7 +513,8 @@ def run_e2e(calls, K, device, info, world):
                 done[L] = ev
                 cout.wait_event(ev)
                 with torch.cuda.stream(cout):
-                    host_out[L].copy_(c.out, non_blocking=True)
+                    for h, d in zip(host_out[L], call_outputs(c)):
+                        h.copy_(d, non_blocking=True)
                     ev2 = torch.cuda.Event()
                     ev2.record(cout)
                 read[L] = ev2
@@ -515,8 +575,8 @@ def run_reference(args):
     if rank != 0:
         return
     res = run_cpu_baseline(args.workload, steps=args.steps, warmup=args.warmup)
-    line = {"impl": "reference", "metric": "decode-attention tokens/s" if args.workload != "prefill"
-            else "prefill tokens/s", "value": res.get("value"), "unit": "tokens/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": METRIC.get(args.workload, "decode-attention tokens/s"),
+            "value": res.get("value"), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.get("ms_per_step"),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, same generators as the GPU arm)",
@@ -533,7 +593,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
-                    choices=["stack42", "tiny", "sliding16", "full32k", "prefill"])
+                    choices=["stack42", "tiny", "sliding16", "full32k", "prefill", "mixed"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -191,6 +191,50 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
                                     int32_t max_rows_per_seq);
 
 /*
+ * attn_mixed -- several groups of query rows of one layer in one call, each
+ * in its own phase, as in the mixed forward of the pages (serving-blocks.ts,
+ * `#mixed`, and the Gemma `#mixed` scope: every group's attention reads its
+ * own caches and positions in its own phase, decode or window, and a verify
+ * group reads a window).  A decode group is exactly the attn_decode call its
+ * fields describe, a window group (prompt chunk or verify window) the
+ * attn_prefill_chunk call.  The groups run concurrently on the GPU.
+ *
+ *   groups      host array of n_groups descriptors (below), 0 <= n_groups <=
+ *               KVQ_MAX_MIXED_GROUPS
+ *   q_norm_w, out_is_f32, stream   as for attn_decode, shared by every group
+ *
+ * Every group is checked before anything is enqueued: on any failing group
+ * the call returns that status and enqueues nothing.  Work enqueued on
+ * `stream` before the call is complete before any group starts; work
+ * enqueued on `stream` after it waits for every group.  Groups must not share
+ * workspace, out or q_prepped memory (overlapping workspaces are rejected
+ * with KVQ_EINVAL).  The groups run on streams and events the library
+ * creates once per device on the first call with two or more groups: make
+ * that call before any stream capture.  Calls that overlap on one device
+ * (several host threads) must be serialised.
+ */
+#define KVQ_MAX_MIXED_GROUPS 8
+enum { KVQ_PHASE_DECODE = 0, KVQ_PHASE_WINDOW = 1 };
+typedef struct {
+  int32_t phase;                 /* KVQ_PHASE_DECODE or KVQ_PHASE_WINDOW */
+  const kvq_seq_cache* seqs;     /* device kvq_seq_cache[n_seqs] */
+  int32_t n_seqs;
+  const int32_t* row_offsets;    /* window: device int32[n_seqs + 1]; decode: ignored */
+  const int32_t* pos;            /* device int32[n_seqs]: decode positions, or window start positions */
+  int32_t n_rows;                /* window: rows of the group; decode: ignored (one row per sequence) */
+  int32_t max_pos;               /* decode: host upper bound of pos[]; window: ignored */
+  int32_t max_rows_per_seq;      /* window: host upper bound of rows per sequence; decode: ignored */
+  const uint16_t* q_raw;         /* device bf16 [rows][n_q_heads][head_dim] */
+  void* out;                     /* device [rows][n_q_heads][head_dim], fp32 if out_is_f32 else bf16 */
+  uint16_t* q_prepped;           /* NULL or device bf16 [rows][n_q_heads][head_dim] */
+  void* workspace;               /* attn_decode_workspace_bytes / attn_prefill_workspace_bytes of the group */
+  size_t workspace_bytes;
+} kvq_attn_group;
+
+kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
+                      const uint16_t* q_norm_w, int32_t out_is_f32, void* stream);
+
+/*
  * attn_decode_static -- attn_decode without a caller-provided workspace, for
  * callers that cannot allocate device memory: code that only receives input
  * and output pointers from a host framework that owns every allocation (a

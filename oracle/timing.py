@@ -114,6 +114,23 @@ def build(workload: str, nseq: int):
                                        None if inp["v"] is None else f(inp["v"]), f(inp["k_w"]),
                                        rows=range(rows))[3]
         return [Chunk()], rows, f"sequence 0: its whole chunk appended, attention of its first {rows} rows"
+    if workload == "mixed":
+        dwl, pwl = W.workload_mixed_step()
+        n = min(nseq, dwl.n_seqs)
+        idx = sorted(np.random.default_rng(7).choice(dwl.n_seqs, size=n, replace=False).tolist())
+        units = [SeqLayer(dwl, s) for s in idx]
+        s, spec, rows = 0, pwl.layer, 16
+        state = SeqLayer(W.DecodeWorkload(pwl.name, pwl.seed, spec, pwl.filled, pwl.bits), s)
+        inp = W.layer_inputs(pwl.seed, pwl.layer_id, spec, pwl.chunk[s], pwl.chunk[s], seq=s)
+
+        class WindowRows:
+            def decode(self_inner):
+                return O.prefill_chunk(spec, state.cache, pwl.filled[s], f(inp["q"]), f(inp["q_w"]), f(inp["k"]),
+                                       None if inp["v"] is None else f(inp["v"]), f(inp["k_w"]),
+                                       rows=range(rows))[3]
+        units.append(WindowRows())
+        return units, n + rows, (f"decode group: {n} of {dwl.n_seqs} sequences (indices {idx}); window group: "
+                                 f"sequence 0, its chunk appended, attention of its first {rows} rows")
     raise SystemExit(f"unknown workload {workload}")
 
 

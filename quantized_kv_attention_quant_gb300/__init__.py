@@ -35,6 +35,18 @@ class KvqSeqCache(ctypes.Structure):
                 ("bits", ctypes.c_int32), ("capacity", ctypes.c_int32)]
 
 
+KVQ_MAX_MIXED_GROUPS = 8
+KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW = 0, 1
+
+
+class KvqAttnGroup(ctypes.Structure):
+    _fields_ = [("phase", ctypes.c_int32), ("seqs", ctypes.c_void_p), ("n_seqs", ctypes.c_int32),
+                ("row_offsets", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("n_rows", ctypes.c_int32),
+                ("max_pos", ctypes.c_int32), ("max_rows_per_seq", ctypes.c_int32),
+                ("q_raw", ctypes.c_void_p), ("out", ctypes.c_void_p), ("q_prepped", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class KvqError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"kvq status {status}: {message}")
@@ -60,6 +72,8 @@ def _load():
     lib.attn_prefill_chunk.restype = ctypes.c_int
     lib.attn_prefill_workspace_bytes.argtypes = [lay, i32, i32, i32]
     lib.attn_prefill_workspace_bytes.restype = sz
+    lib.attn_mixed.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
+    lib.attn_mixed.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_last_error.argtypes = []
@@ -158,6 +172,20 @@ def attn_prefill_chunk(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_
 
 def attn_prefill_workspace_bytes(layer: KvqLayer, n_seqs, n_rows, max_rows_per_seq) -> int:
     return lib.attn_prefill_workspace_bytes(ctypes.byref(layer), n_seqs, n_rows, max_rows_per_seq)
+
+
+def attn_group(phase, seqs, n_seqs, row_offsets, pos, n_rows, max_pos, max_rows_per_seq, q_raw, out,
+               q_prepped, workspace, workspace_bytes) -> KvqAttnGroup:
+    """One group of attn_mixed (see include/kvq.h for the fields)."""
+    return KvqAttnGroup(int(phase), _ptr(seqs), int(n_seqs), _ptr(row_offsets), _ptr(pos), int(n_rows),
+                        int(max_pos), int(max_rows_per_seq), _ptr(q_raw), _ptr(out), _ptr(q_prepped),
+                        _ptr(workspace), int(workspace_bytes))
+
+
+def attn_mixed(layer: KvqLayer, groups, q_norm_w, out_is_f32, stream=None):
+    arr = (KvqAttnGroup * max(1, len(groups)))(*groups)
+    _check(lib.attn_mixed(ctypes.byref(layer), arr, len(groups), _ptr(q_norm_w), int(out_is_f32),
+                          _stream(stream)))
 
 
 def kvq_status_string(status: int) -> str:

@@ -14,8 +14,9 @@ import torch
 
 import workloads as W
 
-from . import (attn_decode, attn_decode_workspace_bytes, attn_prefill_chunk,
-               attn_prefill_workspace_bytes, kv_quant_append, layer as make_layer)
+from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_workspace_bytes, attn_group,
+               attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, kv_quant_append,
+               layer as make_layer)
 from .cache import LayerCaches
 
 
@@ -207,6 +208,60 @@ class PrefillCase:
 
     def status_word(self) -> int:
         return int(self.ws[:4].cpu().numpy().view(np.uint32)[0])
+
+
+class MixedCase:
+    """Groups of one layer in one attn_mixed call: DecodeWorkload groups (one
+    query row per sequence) and PrefillWorkload groups (prompt chunks or
+    verify windows), each with its own caches, positions and bits.  The groups
+    must share the layer spec, seed and layer id (hence the q norm weight)."""
+
+    def __init__(self, workloads, device="cuda", keep_prepped=False, out_f32=True):
+        self.cases = []
+        for wl in workloads:
+            if isinstance(wl, W.DecodeWorkload):
+                self.cases.append(DecodeCase(wl, device, keep_prepped=keep_prepped, out_f32=out_f32))
+            else:
+                self.cases.append(PrefillCase(wl, device, keep_prepped=keep_prepped, out_f32=out_f32))
+        first = self.cases[0]
+        self.spec, self.lay, self.q_w, self.out_f32 = first.spec, first.lay, first.q_w, out_f32
+        for c in self.cases[1:]:
+            assert c.wl.seed == first.wl.seed and c.wl.layer_id == first.wl.layer_id and c.spec == first.spec
+
+    def groups(self):
+        gs = []
+        for c in self.cases:
+            if isinstance(c, DecodeCase):
+                gs.append(attn_group(KVQ_PHASE_DECODE, c.caches.desc, c.wl.n_seqs, None, c.pos, 0, c.max_pos, 0,
+                                     c.q, c.out, c.q_prepped, c.ws, c.ws_bytes))
+            else:
+                gs.append(attn_group(KVQ_PHASE_WINDOW, c.caches.desc, c.wl.n_seqs, c.offs, c.start, c.n_rows, 0,
+                                     c.max_rows, c.q, c.out, c.q_prepped, c.ws, c.ws_bytes))
+        return gs
+
+    def append(self, stream=None):
+        for c in self.cases:
+            c.append(stream)
+
+    def attend(self, stream=None):
+        attn_mixed(self.lay, self.groups(), self.q_w, self.out_f32, stream)
+
+    def attend_serial(self, stream=None):
+        for c in self.cases:
+            c.attend(stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.attend(stream)
+
+    def inputs(self):
+        return [t for c in self.cases for t in (c.q, c.k) + ((c.v,) if c.v is not None else ())]
+
+    def outputs(self):
+        return [c.out for c in self.cases]
+
+    def status_words(self):
+        return [c.status_word() for c in self.cases]
 
 
 class StackCase:

@@ -127,3 +127,35 @@ def test_workspace_grows_with_rows(m):
     assert m.attn_prefill_workspace_bytes(lay, 1, 64, 64) < m.attn_prefill_workspace_bytes(lay, 1, 512, 512)
     full = _layer(m, window=0, head_dim=512, n_q_heads=16, n_kv_heads=1, rope_dims=128)
     assert m.attn_decode_workspace_bytes(full, 8, 32768) > 0
+
+
+def test_bad_mixed_groups(m):
+    """attn_mixed checks every group before enqueueing anything."""
+    lay = _layer(m)
+    L = ctypes.byref(lay)
+    big = 1 << 40
+    dec = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, 10, 0, P, P, None, P, big)
+    win = m.attn_group(m.KVQ_PHASE_WINDOW, P, 1, P, P, 4, 0, 4, P, P, None, P + (1 << 30), big)
+    f = m.lib.attn_mixed
+
+    def call(groups, n=None):
+        arr = (m.KvqAttnGroup * max(1, len(groups)))(*groups)
+        return f(L, arr, len(groups) if n is None else n, P, 1, None)
+
+    assert call([], 0) == 0                                       # nothing to do
+    assert call([dec] * 9) == 1                                   # more than KVQ_MAX_MIXED_GROUPS
+    assert f(L, None, 1, P, 1, None) == 1                         # groups NULL
+    bad_phase = m.attn_group(7, P, 1, None, P, 0, 10, 0, P, P, None, P, big)
+    assert call([dec, bad_phase]) == 1
+    assert "group 1" in m.kvq_last_error()
+    bad_pos = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, -1, 0, P, P, None, P, big)
+    assert call([bad_pos]) == 1
+    no_offsets = m.attn_group(m.KVQ_PHASE_WINDOW, P, 1, None, P, 4, 0, 4, P, P, None, P, big)
+    assert call([dec, no_offsets]) == 1
+    misaligned = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, 10, 0, P + 8, P, None, P, big)
+    assert call([win, misaligned]) == 1                           # q_raw of group 1 misaligned
+    small = m.attn_group(m.KVQ_PHASE_WINDOW, P, 1, P, P, 4, 0, 4, P, P, None, P,
+                         m.attn_prefill_workspace_bytes(lay, 1, 4, 4) - 1)
+    assert call([dec, small]) == 4                                # workspace too small
+    assert call([dec, dec]) == 1                                  # the same workspace twice
+    assert "share workspace" in m.kvq_last_error()

@@ -39,6 +39,12 @@ def check_decode(harness, wl, seqs=None, check_fill=True):
     case = harness.DecodeCase(wl, keep_prepped=True)
     case.step()
     torch.cuda.synchronize()
+    return case, verify_decode(case, wl, seqs, check_fill)
+
+
+def verify_decode(case, wl, seqs=None, check_fill=True):
+    """The stepped case against the oracle: prepped rows and cache bytes
+    bit-exact, outputs within the tolerance.  Returns the worst errors."""
     assert case.status_word() == 0
     out = case.out.cpu().numpy()
     qp = case.q_prepped.cpu().numpy().view(np.uint16)
@@ -58,7 +64,7 @@ def check_decode(harness, wl, seqs=None, check_fill=True):
         mx, mean = attn_errors(out[s], e.out[0])
         assert mx <= MAX_ABS and mean <= MEAN_ABS, f"seq {s}: max {mx} mean {mean}"
         worst = (max(worst[0], mx), max(worst[1], mean))
-    return case, worst
+    return worst
 
 
 DECODE_CASES = {
@@ -146,6 +152,10 @@ def check_prefill(harness, wl, seqs=None, rows=None, nan_rows=None):
     case = harness.PrefillCase(wl, keep_prepped=True)
     case.step()
     torch.cuda.synchronize()
+    return case, verify_prefill(case, wl, seqs, rows, nan_rows)
+
+
+def verify_prefill(case, wl, seqs=None, rows=None, nan_rows=None):
     out = case.out.cpu().numpy()
     qp = case.q_prepped.cpu().numpy().view(np.uint16)
     kvp = case.kv_prepped.cpu().numpy().view(np.uint16)
@@ -167,7 +177,7 @@ def check_prefill(harness, wl, seqs=None, rows=None, nan_rows=None):
             mx, mean = attn_errors(got, want)
             assert mx <= MAX_ABS and mean <= MEAN_ABS, f"seq {s} row {t}: max {mx} mean {mean}"
             worst = (max(worst[0], mx), max(worst[1], mean))
-    return case, worst
+    return worst
 
 
 def test_prefill_small_sliding(kvq):
@@ -315,3 +325,61 @@ def test_prefill_bf16_output_is_rounded_f32(kvq):
     bf = b.out.cpu().numpy().view(np.uint16)
     want = O.f64_to_bf16(O.rn_bf16(f32.astype(np.float64)))
     assert np.array_equal(bf, want)
+
+
+# ----------------------------------------------------------------------------
+# mixed steps: decode groups and prompt / verify-window groups of one layer in
+# one attn_mixed call, each group checked against the oracle on its own
+# ----------------------------------------------------------------------------
+
+MIXED_CASES = {
+    "sliding-decode-and-chunk": (_spec(8, 2, 256, 512, 256), [
+        ("decode", [700, 40, 1500, 3], [4, 8, 8, 4]),
+        ("window", [300, 0], [37, 130], [8, 4]),
+    ]),
+    "full-keqv-two-decode-one-verify": (_spec(16, 1, 512, 0, 128, 1e6, True), [
+        ("decode", [3500, 10, 900], [8, 4, 4]),
+        ("window", [200, 65], [5, 64], [4, 8]),
+        ("decode", [64, 4000], [8, 8]),
+    ]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MIXED_CASES))
+def test_mixed_groups(kvq, name):
+    _, harness = kvq
+    spec, groups = MIXED_CASES[name]
+    wls = []
+    for i, g in enumerate(groups):
+        if g[0] == "decode":
+            wls.append(W.DecodeWorkload(f"{name}-{i}", 91, spec, filled=g[1], bits=g[2]))
+        else:
+            wls.append(W.PrefillWorkload(f"{name}-{i}", 91, spec, filled=g[1], chunk=g[2], bits=g[3]))
+    case = harness.MixedCase(wls, keep_prepped=True)
+    case.step()
+    torch.cuda.synchronize()
+    for c, wl in zip(case.cases, wls):
+        if isinstance(wl, W.DecodeWorkload):
+            worst = verify_decode(c, wl, check_fill=False)
+        else:
+            assert c.status_word() == 0
+            worst = verify_prefill(c, wl)
+        print(name, wl.name, "worst", worst)
+
+
+def test_mixed_equals_separate_calls(kvq):
+    """The groups of one attn_mixed call give the same bytes as the separate
+    attn_decode / attn_prefill_chunk calls."""
+    _, harness = kvq
+    spec = _spec(8, 2, 256, 512, 256)
+    wls = [W.DecodeWorkload("eq-d", 92, spec, filled=[900, 33], bits=[4, 8]),
+           W.PrefillWorkload("eq-w", 92, spec, filled=[128], chunk=[70], bits=[8])]
+    case = harness.MixedCase(wls)
+    case.append()
+    case.attend()
+    torch.cuda.synchronize()
+    mixed = [c.out.clone() for c in case.cases]
+    case.attend_serial()
+    torch.cuda.synchronize()
+    for a, c in zip(mixed, case.cases):
+        assert torch.equal(a, c.out)

@@ -285,6 +285,23 @@ def workload_stack_decode(n_seqs: int = 64, lo: int = 1024, hi: int = 32768) -> 
     return StackWorkload("stack42-mixed-decode-64-ragged", seed, lengths, bits)
 
 
+def workload_mixed_step(n_decode: int = 48, lo: int = 1024, hi: int = 8192):
+    """A mixed step of one sliding layer (the 42-layer stack's sliding shape):
+    a decode group of n_decode sequences with lengths uniform in [lo, hi] and
+    per-sequence bits from the seed, and a window group of two prompt chunks
+    of 256 rows onto 4096 and 6000 cached tokens (8- and 4-bit).  Both groups
+    share the seed and layer id, hence the norm weights."""
+    seed = 1006
+    g = _rng(seed, P_LEN)
+    lengths = [int(x) for x in g.integers(lo, hi + 1, size=n_decode)]
+    gb = _rng(seed, P_BITS)
+    bits = [int(gb.choice([4, 8])) for _ in range(n_decode)]
+    dec = DecodeWorkload("mixed-decode-48-ragged", seed, SLIDING, filled=lengths, bits=bits)
+    win = PrefillWorkload("mixed-window-2x256", seed, SLIDING, filled=[4096, 6000], chunk=[256, 256],
+                          bits=[8, 4])
+    return dec, win
+
+
 WORKLOADS = {
     "tiny": workload_tiny_decode,
     "sliding16": workload_sliding_decode_b16,
