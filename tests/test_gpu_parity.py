@@ -110,6 +110,21 @@ def test_decode_stream_k(kvq, name):
     print(name, "worst", worst)
 
 
+def test_many_rows_take_fixed_chunks(kvq):
+    """Over 1024 rows per call the decode falls back from stream-K to fixed
+    48-tile chunks; rows longer than one chunk still merge correctly."""
+    _, harness = kvq
+    spec = _spec(2, 1, 64, 0, 64)
+    rng = np.random.default_rng(84)
+    filled = [int(x) for x in rng.integers(0, 200, size=1030)]
+    for s, n in ((3, 3100), (517, 5000), (1029, 3072)):
+        filled[s] = n
+    bits = [int(b) for b in rng.choice([4, 8], size=1030)]
+    wl = W.DecodeWorkload("many-rows", 84, spec, filled=filled, bits=bits)
+    _, worst = check_decode(harness, wl, seqs=[0, 3, 4, 517, 700, 1029], check_fill=False)
+    print("many-rows worst", worst)
+
+
 def test_stream_k_bad_descriptor_is_nan(kvq):
     """A skipped sequence inside a stream-K batch: NaN rows, status bit set,
     the other rows unaffected."""
