@@ -3,14 +3,19 @@
 // read.attend(q, 1.0); "Parity notes": SDPA scale 1.0, GQA over n_kv heads).
 //
 // Three launches on the caller's stream:
-//   1. qprep_kernel   (n_kv, n_seqs): q RMSNorm + RoPE for the G q heads of a kv
-//      head, written as ready-made mma.sync A fragments plus per-group sums.
-//   2. decode_kernel  (rows, n_kv, splits), programmatic dependent launch:
-//      split-K ("flash decoding") over the visible keys.  64-key tiles (packed
-//      codes row by row into padded shared rows, scales and biases) stream
-//      through a ring of stages filled by TMA bulk copies and tracked by
-//      mbarriers.  There is no producer warp (a 9th warp would share a
-//      register sub-partition with two consumers and cap them at 168
+//   1. qprep_kernel   (rows, blocks of q heads): q RMSNorm + RoPE, written as
+//      ready-made mma.sync A fragments plus per-group sums.
+//   2. decode_kernel  programmatic dependent launch: split-K ("flash
+//      decoding") over the visible keys, in one of two schedules:
+//        fixed chunks (rows of at most 48 tiles): grid (rows, n_kv, splits),
+//          split z takes tiles [z*chunk, (z+1)*chunk) of its row;
+//        stream-K (longer rows): grid of one wave of CTAs, each taking an
+//          equal range of the tiles of all (row, kv head) units in a row and
+//          walking it unit by unit (see decode_kernel).
+//      64-key tiles (packed codes row by row into padded shared rows, scales
+//      and biases) stream through a ring of stages filled by TMA bulk copies
+//      and tracked by mbarriers.  There is no producer warp (a 9th warp would
+//      share a register sub-partition with two consumers and cap them at 168
 //      registers): once a tile's max-exchange barrier shows every warp is done
 //      with the previous tile, the warps refill that stage themselves.
 //      Warps 0..NW-1 compute
@@ -18,10 +23,11 @@
 //            codes enter the tensor cores exactly as f16 integers, per 64-dim
 //            group: S += scale * (q . codes) + bias * sum(q)
 //        softmax: online, tile max exchanged through shared memory
-//        PV: warp w owns head_dim group w; v_hat = code*scale + bias in f16,
-//            P (f16) from shared memory via ldmatrix.
-//      Each split writes its (m, l, o) partial.
-//   3. combine_kernel (n_q, n_seqs): merges the split partials.
+//        PV: warp w owns head_dim group w; A = P * scale (f16), B = exact
+//            codes, plus one MMA for sum(P * bias).
+//      Each run of tiles writes its (m, l, o) partial, or the output itself
+//      when it covers its whole row.
+//   3. combine_kernel / combine_sk_kernel (rows, n_q): merge the partials.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "kvq_qprep.cuh"
