@@ -17,8 +17,9 @@
  *
  * Conventions for every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
- *     library allocates nothing and keeps no reference after the call
- *     returns.  `kvq_layer` is read on the host during the call.
+ *     library allocates no memory and keeps no reference after the call
+ *     returns (attn_mixed creates its streams and events once per device).
+ *     `kvq_layer` is read on the host during the call.
  *   - Alignment: k_raw, v_raw and q_raw 16 bytes (read with 128-bit loads);
  *     the workspace 256 bytes; the kvq_seq_cache array 8 bytes; every other
  *     pointer its element size.  The six arrays a kvq_seq_cache points to are
