@@ -127,10 +127,22 @@ __device__ __forceinline__ ff rms_inv(ff ss, int D, float eps) {
 }
 // x * w * inv, correctly rounded to bf16; x and w are bf16 values so x*w is
 // exact in fp32.
+//
+// Fast path, bit-identical to the float-float result: p = fl(inv.hi * xw).
+// The float-float product's leading float hi' differs from p by at most
+// 1.5 ulp(p) (|p - inv.hi*xw| <= ulp/2, |inv.lo*xw| <= 2^-24 |p| < ulp(p)),
+// i.e. by at most 3 steps of the fp32 bit pattern even where a binade
+// boundary halves the ulp.  bf16 rounding of a float looks only at its low 16
+// bits (ties at exactly 0x8000), so when p's low half is more than 4 steps
+// from 0x8000, hi' and p round alike (a carry across the 16-bit boundary
+// keeps the rounded value: p = top|0xFFFF and top+1|0x0002 both give top+1).
 __device__ __forceinline__ uint16_t norm_scale_bf16(float x, float w, ff inv) {
   float xw = __fmul_rn(x, w);
   // exact zero keeps its IEEE sign (inv > 0); the float-float sums would drop it
   if (xw == 0.f) return uint16_t(__float_as_uint(xw) >> 16);
+  const uint32_t u = __float_as_uint(__fmul_rn(inv.hi, xw));
+  const uint32_t low = u & 0xFFFFu;
+  if (low - 0x7FFCu > 8u) return uint16_t((u >> 16) + (low > 0x8000u ? 1u : 0u));
   return ff_to_bf16_rn(ff_mul_f(inv, xw));
 }
 
@@ -227,9 +239,29 @@ __device__ __forceinline__ void stage_freqs(const float (*f)[3], int half, float
 }
 
 // x*c - y*s, correctly rounded to bf16 (x, y bf16 values; c, s float-float).
+//
+// Fast path: r = fl(x*c.hi - fl(y*s.hi)) (one fma).  Against the exact value
+// it drops x*c.lo and y*s.lo (each <= 2^-24 of its product) and rounds twice
+// (<= 2^-24 of |y*s.hi| and of |r|), so |r - exact| <= 2^-22 B with
+// B = |x*c.hi| + |y*s.hi|; the float-float result lies within 2^-44 B of the
+// exact value.  bf16 rounding midpoints sit where the fp32 low half is 0x8000
+// (mid-binade), so when r is a normal float whose distance to the nearest
+// one, |low - 0x8000| * ulp(r), exceeds 2^-21 B, the exact value, the
+// float-float result and r all round to the same bf16.
 __device__ __forceinline__ uint16_t rot_bf16(float x, float y, ff c, ff s) {
   if (x == 0.f && y == 0.f)   // signed zero as IEEE arithmetic gives it
     return uint16_t(__float_as_uint(__fsub_rn(__fmul_rn(x, c.hi), __fmul_rn(y, s.hi))) >> 16);
+  const float ys = __fmul_rn(y, s.hi);
+  const float r = __fmaf_rn(x, c.hi, -ys);
+  const uint32_t u = __float_as_uint(r);
+  const uint32_t ex = u & 0x7F800000u;
+  if (ex >= (24u << 23) && ex < 0x7F800000u) {
+    const uint32_t low = u & 0xFFFFu;
+    const float steps = (float)(low > 0x8000u ? low - 0x8000u : 0x8000u - low);
+    const float ulp = __uint_as_float(ex - (23u << 23));               // 2^(e - 23)
+    const float bound = __fmul_rn(__fadd_rn(fabsf(__fmul_rn(x, c.hi)), fabsf(ys)), 4.76837158203125e-7f);  // 2^-21
+    if (__fmul_rn(steps, ulp) > bound) return uint16_t((u >> 16) + (low > 0x8000u ? 1u : 0u));
+  }
   ff a = ff_mul_f(c, x);
   ff b = ff_mul_f(s, y);
   return ff_to_bf16_rn(ff_add(a, ff_neg(b)));
