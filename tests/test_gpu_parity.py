@@ -110,6 +110,23 @@ def test_decode_stream_k(kvq, name):
     print(name, "worst", worst)
 
 
+def test_stream_k_bf16_output_is_rounded_f32(kvq):
+    """bf16 outputs of the stream-K schedule (rows finished inside one CTA are
+    written by the attention kernel, the others by the merge) are exactly the
+    rounded fp32 outputs."""
+    _, harness = kvq
+    spec, filled, bits = STREAM_K_CASES["sk-ragged-d512-keqv"]
+    wl = W.DecodeWorkload("sk-bf16", 79, spec, filled=filled, bits=bits)
+    a = harness.DecodeCase(wl)
+    a.step()
+    b = harness.DecodeCase(wl, out_f32=False)
+    b.step()
+    torch.cuda.synchronize()
+    f32 = a.out.cpu().numpy()
+    bf = b.out.cpu().numpy().view(np.uint16)
+    assert np.array_equal(bf, O.f64_to_bf16(O.rn_bf16(f32.astype(np.float64))))
+
+
 def test_many_rows_take_fixed_chunks(kvq):
     """Over 1024 rows per call the decode falls back from stream-K to fixed
     48-tile chunks; rows longer than one chunk still merge correctly."""
