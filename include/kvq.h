@@ -265,6 +265,21 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
                               const uint16_t* q_raw, const uint16_t* q_norm_w,
                               void* out, int32_t out_is_f32, uint16_t* q_prepped, void* stream);
 
+/*
+ * kvq_selftest_wait_timeout -- exercises the failure detection of the
+ * attention kernels without faulting the GPU.  Every wait of the kernels (on
+ * the mbarriers their bulk copies complete) gives up after a bounded time,
+ * sets a status bit and lets the kernel finish, so that a lost completion
+ * never hangs the device.  This call launches one small kernel whose wait,
+ * on an mbarrier that nothing completes, runs out after limit_ns; it then
+ * ORs bit 1 (the "bounded wait gave up" bit of the attention status word)
+ * into *status.  Nothing else is touched and no copy is in flight.
+ *
+ *   status     device uint32 (4-byte aligned), typically cleared beforehand
+ *   limit_ns   1e3 .. 1e9
+ */
+kvq_status kvq_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, void* stream);
+
 /* Static message for a status code. */
 const char* kvq_status_string(kvq_status status);
 /* Message of the calling thread's most recent failing call ("" if none). */

@@ -74,6 +74,8 @@ def _load():
     lib.attn_prefill_workspace_bytes.restype = sz
     lib.attn_mixed.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
     lib.attn_mixed.restype = ctypes.c_int
+    lib.kvq_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.kvq_selftest_wait_timeout.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_last_error.argtypes = []
@@ -186,6 +188,12 @@ def attn_mixed(layer: KvqLayer, groups, q_norm_w, out_is_f32, stream=None):
     arr = (KvqAttnGroup * max(1, len(groups)))(*groups)
     _check(lib.attn_mixed(ctypes.byref(layer), arr, len(groups), _ptr(q_norm_w), int(out_is_f32),
                           _stream(stream)))
+
+
+def kvq_selftest_wait_timeout(status, limit_ns, stream=None):
+    """Run the kernels' bounded wait on an mbarrier nothing completes (see
+    include/kvq.h); bit 1 of the device uint32 `status` is set when it gives up."""
+    _check(lib.kvq_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)))
 
 
 def kvq_status_string(status: int) -> str:

@@ -467,6 +467,15 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
                           out_is_f32, q_prepped, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
 }
 
+kvq_status kvq_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, void* stream) {
+  if (!status || !aligned(status, 4)) return fail(KVQ_EINVAL, "status is NULL or not 4-byte aligned");
+  if (limit_ns < 1000u || limit_ns > 1000000000u)
+    return fail(KVQ_EINVAL, "limit_ns %llu not in [1e3, 1e9]", (unsigned long long)limit_ns);
+  const cudaError_t e = kvq::launch_wait_selftest(status, limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_selftest_wait_timeout launch");
+  return KVQ_OK;
+}
+
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
     case KVQ_OK: return "ok";

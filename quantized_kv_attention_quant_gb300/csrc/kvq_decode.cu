@@ -978,6 +978,26 @@ DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, const DecodePl
   return w;
 }
 
+namespace {
+// The attention kernels' bounded wait, alone: an mbarrier expecting one
+// arrival that never comes.  No copy is in flight, so returning is safe.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_for(&bar, 0, limit_ns);
+  if (!ok && threadIdx.x == 0) flag_error(status, KVQ_DEV_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks) {
   // tiles one row can touch: keys 0..max_keys-1 when causal, else a window
   // of at most `window` keys starting anywhere inside a tile

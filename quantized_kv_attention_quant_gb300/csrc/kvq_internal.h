@@ -88,6 +88,9 @@ DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L);
 cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st);
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
+// One CTA whose bounded wait on an mbarrier that nothing completes gives up
+// after limit_ns and flags the timeout bit in *status.
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
 
 }  // namespace kvq

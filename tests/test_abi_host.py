@@ -159,3 +159,11 @@ def test_bad_mixed_groups(m):
     assert call([dec, small]) == 4                                # workspace too small
     assert call([dec, dec]) == 1                                  # the same workspace twice
     assert "share workspace" in m.kvq_last_error()
+
+
+def test_bad_selftest_arguments(m):
+    f = m.lib.kvq_selftest_wait_timeout
+    assert f(None, 1000000, None) == 1            # status NULL
+    assert f(P + 2, 1000000, None) == 1           # status misaligned
+    assert f(P, 10, None) == 1                    # limit below 1 us
+    assert f(P, 2000000000, None) == 1            # limit above 1 s

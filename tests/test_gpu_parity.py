@@ -165,6 +165,19 @@ def test_stream_k_bad_descriptor_is_nan(kvq):
     assert case.status_word() & (1 << 2)
 
 
+def test_bounded_wait_gives_up(kvq):
+    """Failure detection without a fault: the kernels' bounded wait on an
+    mbarrier that nothing completes gives up, sets the timeout bit, and the
+    context stays usable for the next call."""
+    m, harness = kvq
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.kvq_selftest_wait_timeout(status, 5_000_000)        # 5 ms
+    torch.cuda.synchronize()
+    assert int(status.item()) & (1 << 1)
+    spec, filled, bits = DECODE_CASES["window-1"]
+    check_decode(harness, W.DecodeWorkload("after-timeout", 77, spec, filled=filled, bits=bits))
+
+
 def test_decode_bf16_output_is_rounded_f32(kvq):
     _, harness = kvq
     spec, filled, bits = DECODE_CASES["sliding-ring-wrap"]
