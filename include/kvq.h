@@ -194,9 +194,9 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
 /*
  * attn_mixed -- several groups of query rows of one layer in one call, each
  * in its own phase, as in the mixed forward of the pages (serving-blocks.ts,
- * `#mixed`, and the Gemma `#mixed` scope: every group's attention reads its
- * own caches and positions in its own phase, decode or window, and a verify
- * group reads a window).  A decode group is exactly the attn_decode call its
+ * `#mixed`, and the Gemma `#mixed` scope: each group attends over its own
+ * caches at its own positions, in decode or window mode, a verify group in
+ * window mode).  A decode group is exactly the attn_decode call its
  * fields describe, a window group (prompt chunk or verify window) the
  * attn_prefill_chunk call.  The groups run concurrently on the GPU.
  *

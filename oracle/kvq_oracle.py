@@ -10,12 +10,12 @@ the section of that file):
 
 * q / k RMSNorm per head over head_dim with a learned weight, and an
   un-scaled RMSNorm (no weight) of v -- model.ts, `attentionTraining`
-  (`qNorm`, `kNorm`, `vNorm`) and the header's "Parity notes" (K = V layers:
-  "V = same projection as K, with un-scaled RMS norm").
-* RoPE at the cache position, rotating only `rope_dims` of head_dim
-  ("ProportionalRoPE rotates only partial_rotary_factor*dims dims", model.ts
-  "Parity notes"; offset = cache offset, `cache.ropePositions` in
-  `attentionTraining`).
+  (`qNorm`, `kNorm`, `vNorm`) and the header's "Parity notes" (on K = V
+  layers V comes from the K projection and is normalised without a weight).
+* RoPE at the cache position, rotating only `rope_dims` of head_dim (the
+  proportional RoPE of model.ts "Parity notes" turns just a
+  partial_rotary_factor share of the dims; offset = cache offset,
+  `cache.ropePositions` in `attentionTraining`).
 * quantize-append of the new K/V rows into a `{bits, groupSize}` affine cache
   (gemma4-e4b.ts, `Gemma4Layer.kv` and the `LAYERS` table: bits 4 or 8, group
   64; the (codes, scales, biases) triple of MLX affine storage, trainable.ts,
@@ -23,10 +23,10 @@ the section of that file):
   used is scale = (max - min) / (2^bits - 1), bias = min,
   code = round-half-even((x - bias) / scale) clamped, in IEEE fp32, with codes
   packed little-endian into uint32 words.
-* GQA softmax attention with SDPA scale 1.0 ("SDPA scale is 1.0", model.ts
-  "Parity notes"; `read.attend(q, 1.0)` in `attentionTraining`) under a causal
-  mask, windowed on sliding layers (model.ts header: sliding layers compose a
-  RotatingKVCache whose reads own the window; `cacheLayers`).
+* GQA softmax attention with SDPA scale 1.0 (model.ts "Parity notes" and
+  `read.attend(q, 1.0)` in `attentionTraining`) under a causal mask, windowed
+  on sliding layers (model.ts, `cacheLayers`: a sliding layer's cache is a
+  ring sized to its window, and reading it applies the window mask).
 
 Readings taken where the pages are silent:
   R-norm: y = rn_bf16(x / sqrt(mean(x^2) + eps) * w); w = 1 for v.

@@ -213,7 +213,7 @@ class PrefillCase:
 class MixedCase:
     """Groups of one layer in one attn_mixed call: DecodeWorkload groups (one
     query row per sequence) and PrefillWorkload groups (prompt chunks or
-    verify windows), each with its own caches, positions and bits.  The groups
+    verify windows), each group with its own caches, bit widths and positions.  The groups
     must share the layer spec, seed and layer id (hence the q norm weight)."""
 
     def __init__(self, workloads, device="cuda", keep_prepped=False, out_f32=True):

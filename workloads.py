@@ -243,8 +243,9 @@ def stack_layer_kind(i: int) -> str:
 
 
 def stack_cache_layer(i: int) -> int:
-    """The layer whose cache layer i reads: itself for donors 0..23, else the
-    last donor of the same attention type (22 sliding, 23 full)."""
+    """Index of the layer owning the cache that layer i attends: i itself for
+    the donors 0..23; for a sharer, the highest-numbered donor of its own
+    attention type (22 when sliding, 23 when full)."""
     if i < N_DONORS:
         return i
     want = stack_layer_kind(i)
