@@ -93,3 +93,32 @@ def compare_cache(gpu_rows: dict, cache: O.OracleCache, positions) -> int:
 def attn_errors(got: np.ndarray, want: np.ndarray):
     d = np.abs(np.asarray(got, dtype=np.float64) - want)
     return float(d.max()), float(d.mean())
+
+
+# the hand-designed quantizer edge rows of `workloads.quantizer_edge_rows`
+EDGE_SPEC = W.LayerSpec(n_q_heads=2, n_kv_heads=1, head_dim=W.EDGE_HEAD_DIM, window=0, rope_dims=0,
+                        rope_theta=1e4, k_eq_v=False, rms_eps=0.0)
+EDGE_BITS = (4, 8)           # one sequence per bit width, the same rows in each
+
+
+def edge_inputs(seed: int = 1008):
+    """(names, k rows, v rows, q rows, weights) as bf16 bit patterns: K rows are
+    the designed rows, V rows the same in reverse order, q rows N(0, 1) draws;
+    the q and k norm weights are 1."""
+    names, k = W.quantizer_edge_rows()
+    v = k[::-1].copy()
+    q = W.normal_bf16(seed, (W.P_Q, 0), (len(names), EDGE_SPEC.n_q_heads, EDGE_SPEC.head_dim))
+    w = np.full(EDGE_SPEC.head_dim, 0x3F80, np.uint16)          # bf16 1.0
+    return names, k, v, q, w
+
+
+def expect_edge(bits: int) -> SeqExpect:
+    """The designed rows as one prompt chunk at position 0 of an empty cache
+    with `bits`-bit codes; every row attends."""
+    names, k, v, q, w = edge_inputs()
+    f = O.bf16_to_f64
+    cache = O.OracleCache(1, EDGE_SPEC.head_dim, bits)
+    q_hat, k_hat, v_hat, outs = O.prefill_chunk(oracle_layer(EDGE_SPEC), cache, 0, f(q), f(w), f(k), f(v), f(w))
+    n = len(names)
+    empty = np.zeros((0, 1, EDGE_SPEC.head_dim))
+    return SeqExpect(cache, np.arange(0), empty, empty, np.arange(n), q_hat, k_hat, v_hat, outs)

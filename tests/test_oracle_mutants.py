@@ -3,6 +3,7 @@ the pins of `test_oracle_pins.py` catch every one of them."""
 import os
 import types
 
+import numpy as np
 import pytest
 
 import test_oracle_pins as P
@@ -37,13 +38,40 @@ MUTANTS = {
     "v-norm-weighted": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
                         "v_hat = rms_norm(k_raw if v_raw is None else v_raw, k_w, eps)"),
     "quant-signed-zero-bias": ("    mn = g.min(axis=-1) + np.float32(0)\n", "    mn = g.min(axis=-1)\n"),
+    "norm-double-rounding": ("y = y * np.asarray(w, dtype=np.float64)",
+                             "y = rn_bf16(y) * np.asarray(w, dtype=np.float64)"),
+    "prefill-positions-from-zero": ("pos = np.arange(start, start + T)", "pos = np.arange(T)"),
+    "quant-quotient-in-f64": ("q = (g - bias[..., None]) / safe[..., None]",
+                              "q = (g.astype(np.float64) - bias[..., None]) / safe[..., None]"),
+    "bf16-no-subnormal-spacing": ("    e = np.maximum(e, -125)\n", "\n"),
+    "bf16-no-overflow": ("return np.where(np.abs(q) >= 2.0 ** 128, np.copysign(np.inf, x), q)", "return q"),
+    "softmax-max-over-heads": ("m = s.max(axis=-1, keepdims=True)", "m = s.max()"),
+    "norm-one-plus-weight": ("y = y * np.asarray(w, dtype=np.float64)",
+                             "y = y * (1.0 + np.asarray(w, dtype=np.float64))"),
+    "rope-position-plus-one": ("a = np.asarray(pos, dtype=np.float64)[:, None] * f[None, :]",
+                               "a = (np.asarray(pos, dtype=np.float64)[:, None] + 1) * f[None, :]"),
+    "rope-partial-ignored": ("    R = int(rope_dims)\n", "    R = D if int(rope_dims) else 0\n"),
+    "rope-exponent-j-over-D": ("math.pow(theta, -(2.0 * j) / head_dim)", "math.pow(theta, -(1.0 * j) / head_dim)"),
+    "query-excludes-itself": ("return lo, p\n", "return lo, max(lo, p - 1)\n"),
+    "window-ignores-full-layer": ("lo = 0 if window <= 0 else max(0, p - window + 1)",
+                                  "lo = max(0, p - window + 1)"),
+    "prefill-not-causal": ("outs[t] = attend_cache(q_hat[t], start + t,",
+                           "outs[t] = attend_cache(q_hat[t], start + T - 1,"),
+    "decode-q-norm-uses-k-weight": ("q_hat = prep_q(q_raw[None], q_w, pos,", "q_hat = prep_q(q_raw[None], k_w, pos,"),
+    "keqv-v-from-roped-k": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
+                            "v_hat = prep_v(k_hat if v_raw is None else v_raw, eps)"),
+    "quant-scale-truncated": ("s = rn_bf16(s32.astype(np.float64)).astype(np.float32)",
+                              "s = (s32.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)"),
+    "dequant-bias-before-scale": ("x = c * np.asarray(scales)[..., None] + np.asarray(biases)[..., None]",
+                                  "x = (c + np.asarray(biases)[..., None]) * np.asarray(scales)[..., None]"),
     "bf16-7-bits": ("q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
                     "q = np.ldexp(np.rint(np.ldexp(x, 7 - e)), e - 7)"),
 }
 
 PINS = [
     P.pin_rn_bf16, P.pin_quant_ramp4, P.pin_quant_exact8, P.pin_quant_constant,
-    P.pin_quant_ties, P.pin_quant_negative_zero, P.pin_quant_bf16_scale_divides, P.pin_quant_group_independence,
+    P.pin_quant_ties, P.pin_quant_negative_zero, P.pin_quant_bf16_scale_divides, P.pin_quant_fp32_quotient,
+    P.pin_quant_group_independence,
     lambda o: P.pin_quant_invariants(o, 4), lambda o: P.pin_quant_invariants(o, 8),
     P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants,
     P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,
@@ -64,7 +92,8 @@ def test_mutant_is_caught(name):
     caught = []
     for pin in PINS:
         try:
-            pin(m)
+            with np.errstate(all="ignore"):
+                pin(m)
         except Exception:          # an assertion or a crash both count as caught
             caught.append(getattr(pin, "__name__", "pin"))
     assert caught, f"no pin catches mutant {name}"

@@ -41,6 +41,22 @@ def pin_rn_bf16(o):
     b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
     ref = b.astype(np.uint32).view(np.float32).astype(np.float64)
     assert np.array_equal(o.rn_bf16(x.astype(np.float64)), ref)
+    # the same over random bit patterns of every finite float32, subnormals
+    # (bf16 spacing 2^-133 there) and values that round up to infinity
+    # included; the largest float32, (2 - 2^-23) * 2^127, rounds to 2^128 = inf
+    u = rng.integers(0, 2 ** 32, 200000, dtype=np.uint64).astype(np.uint32)
+    u = u[(u & 0x7F800000) != 0x7F800000]
+    u = np.concatenate([u, np.array([0x00000001, 0x807FFFFF, 0x00008000, 0x00018000,
+                                     0x7F7FFFFF, 0xFF7F8000, 0x7F7F7FFF], dtype=np.uint32)])
+    x = u.view(np.float32)
+    b = u.astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    ref = b.astype(np.uint32).view(np.float32).astype(np.float64)
+    got = o.rn_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+    assert np.isinf(o.rn_bf16(np.array([3.4028234663852886e38])))[0]
+    assert o.rn_bf16(np.array([2.0 ** -140]))[0] == 0.0          # below half of 2^-133
+    assert o.rn_bf16(np.array([3 * 2.0 ** -134]))[0] == 2.0 ** -132   # tie -> even
 
 
 def test_rn_bf16():
@@ -123,6 +139,28 @@ def pin_quant_bf16_scale_divides(o):
     assert c[0, 1] == 15 and c[0, 2] == 7      # 0.5 / s = 7.4745 -> 7
 
 
+def pin_quant_fp32_quotient(o):
+    # The quotient (x - bias) / scale is taken in fp32, after an fp32
+    # subtraction.  4-bit, min -2^-30, max 1: fl32(1 + 2^-30) = 1 (fp32 keeps
+    # 24 bits), 1/15 = 136.53 units of 2^-11 -> scale 137 * 2^-11.  The probe
+    # x = 137 * 2^-12 is half a scale; fl32(x + 2^-30) = x (the fp32 spacing
+    # at x is 2^-28), so the quotient is exactly 0.5 and rounds to the even
+    # code 0, where the exact quotient 0.5 + 2^-30 / scale would give 1.  The
+    # maximum gives 1 / scale = 14.95 -> 15; the zeros give ~2^-26 -> 0.
+    x = np.zeros(64)
+    x[0], x[1], x[2] = -2.0 ** -30, 1.0, 137 * 2.0 ** -12
+    c, s, b = o.quantize(x[None], 4)
+    assert s[0, 0] == 137 * 2.0 ** -11 and b[0, 0] == -2.0 ** -30
+    assert (c[0, 0], c[0, 1], c[0, 2], c[0, 3]) == (0, 15, 0, 0)
+    # 8-bit, min -2^-36: scale 129 * 2^-15 as in the bf16-scale case; the
+    # probe 129 * 2^-16 is half a scale and 2^-36 is below half the fp32
+    # spacing there (2^-32): code 0.  The maximum: 1 / scale = 254.02 -> 254.
+    x[0], x[2] = -2.0 ** -36, 129 * 2.0 ** -16
+    c, s, b = o.quantize(x[None], 8)
+    assert s[0, 0] == 129 * 2.0 ** -15 and b[0, 0] == -2.0 ** -36
+    assert (c[0, 0], c[0, 1], c[0, 2]) == (0, 254, 0)
+
+
 def pin_quant_group_independence(o):
     # groups of 64 along the row are quantized independently
     rng = np.random.default_rng(2)
@@ -136,7 +174,7 @@ def pin_quant_group_independence(o):
 
 @pytest.mark.parametrize("pin", [pin_quant_ramp4, pin_quant_exact8, pin_quant_constant,
                                  pin_quant_ties, pin_quant_negative_zero, pin_quant_bf16_scale_divides,
-                                 pin_quant_group_independence])
+                                 pin_quant_fp32_quotient, pin_quant_group_independence])
 def test_quant_hand_cases(pin):
     pin(O)
 
@@ -188,6 +226,12 @@ def pin_rms_hand(o):
     # the weight multiplies: w = [2, -0.5] -> [1.265625, -0.6328125]
     y = o.rms_norm(np.array([[1.0, 2.0]]), np.array([2.0, -0.5]), 0.0)
     assert y[0, 0] == 1.265625 and y[0, 1] == -0.6328125
+    # one rounding, after the weight: w = 65/64.  1/sqrt(2.5) * 65/64 =
+    # 0.642338 = 164.44 units of 2^-8 -> 164/256; 2/sqrt(2.5) * 65/64 =
+    # 1.284675 = 164.44 units of 2^-7 -> 164/128.  (Rounding before the weight
+    # would give 162/256 * 65/64 = 164.53 units -> 165.)
+    y = o.rms_norm(np.array([[1.0, 2.0]]), np.array([65 / 64, 65 / 64]), 0.0)
+    assert y[0, 0] == 164 / 256 and y[0, 1] == 164 / 128
     # eps enters under the square root: x = [1, 1], eps = 3 -> 1/sqrt(4) = 0.5
     y = o.rms_norm(np.array([[1.0, 1.0]]), None, 3.0)
     assert np.all(y == 0.5)
@@ -333,6 +377,19 @@ def pin_attention(o):
     # scale 1.0 and max subtraction: huge logits stay finite and pick the argmax
     big = run(39, 0, qq=q * 64.0)
     assert np.all(np.isfinite(big))
+    # the max is taken per query head: q heads 0 and 1 (both on kv head 0) of
+    # logits near +2000 and with the opposite sign stay finite, and head 0
+    # returns the value of its largest-logit key (the next logit trails by
+    # hundreds, so the other weights are below e^-100)
+    kd = cache.k_hat(0, 39)[:, 0]
+    qa = np.zeros((Hq, D))
+    qa[0], qa[1] = 32.0 * kd[7], -32.0 * kd[7]
+    r = run(39, 0, qq=qa)
+    assert np.all(np.isfinite(r))
+    s0 = np.sort(qa[0] @ kd.T)
+    assert s0[-1] - s0[-2] > 100
+    top = int(np.argmax(qa[0] @ kd.T))
+    assert np.allclose(r[0], cache.v_hat(top, top)[0, 0], atol=1e-12)
     # the output is a convex combination of the visible values
     out = run(39, 8)
     vis = cache.v_hat(32, 39)
@@ -419,6 +476,15 @@ def pin_prefill_matches_decode(o):
         _, _, _, out = o.decode_step(layer, c2, t, qr[t], qw, kr[t], vr[t], kw)
         assert np.allclose(out, outs[t], atol=1e-14)
     for a, b in zip(c1.packed(np.arange(T)), c2.packed(np.arange(T))):
+        assert np.array_equal(a, b)
+    # a second chunk continues at position T: its rows are placed, rotated and
+    # masked at T .. 2T-1, as T more decode steps would do
+    qr2, kr2, vr2 = qr[::-1].copy(), kr[::-1].copy(), vr[::-1].copy()
+    _, _, _, outs2 = o.prefill_chunk(layer, c1, T, qr2, qw, kr2, vr2, kw)
+    for t in range(T):
+        _, _, _, out = o.decode_step(layer, c2, T + t, qr2[t], qw, kr2[t], vr2[t], kw)
+        assert np.allclose(out, outs2[t], atol=1e-14)
+    for a, b in zip(c1.packed(np.arange(2 * T)), c2.packed(np.arange(2 * T))):
         assert np.array_equal(a, b)
 
 

@@ -310,3 +310,100 @@ WORKLOADS = {
     "prefill": workload_prefill_chunk,
     "stack42": workload_stack_decode,
 }
+
+
+# ----------------------------------------------------------------------------
+# hand-designed rows for the quantizer's edge groups
+# ----------------------------------------------------------------------------
+
+# Each entry: name -> {element index: value} of one 64-element group (the rest
+# of the group is +0 unless `fill` says otherwise).  The values are exact bf16
+# numbers chosen so that the group hits one edge of the affine quantizer.
+EDGE_GROUPS = {
+    # min -2^-30, max 1, probe 137*2^-12 = half the 4-bit bf16 scale
+    # 137*2^-11: the probe sits on a code midpoint only after the fp32
+    # subtraction x - min has dropped the 2^-30
+    "fp32-quotient-tie-4": ({0: -2.0 ** -30, 1: 1.0, 2: 137 * 2.0 ** -12}, 0.0),
+    # the same for 8 bits: bf16 scale 129*2^-15, probe 129*2^-16, min -2^-36
+    "fp32-quotient-tie-8": ({0: -2.0 ** -36, 1: 1.0, 2: 129 * 2.0 ** -16}, 0.0),
+    # exact half-code values on a scale-1/8 (4-bit) grid
+    "ties-grid-4": ({1: 15 / 8, 2: 2.5 / 8, 3: 3.5 / 8, 4: 0.5 / 8, 5: 1.5 / 8, 6: 14.5 / 8}, 0.0),
+    # exact half-code values on a scale-1/64 (8-bit) grid
+    "ties-grid-8": ({1: 255 / 64, 2: 2.5 / 64, 3: 3.5 / 64, 4: 100.5 / 64, 5: 126.5 / 64}, 0.0),
+    # a constant group (scale 0)
+    "constant": ({}, 0.5),
+    # every zero a -0, so the raw group minimum is -0
+    "negative-zero-min": ({1: 1 / 8, 2: 1 / 8, 3: 1 / 8, 4: 1 / 8, 5: 15 / 8}, -0.0),
+    # min 0, max 1: the bf16 scale differs from (max - min) / (2^b - 1)
+    "bf16-scale-divides": ({1: 1.0, 2: 0.5}, 0.0),
+    # a range of one bf16 step above 1
+    "nearly-constant": ({63: 1.0078125}, 1.0),
+    # an all-negative group
+    "all-negative": ({0: -2.0, 1: -0.015625, 2: -1.0, 3: -0.75}, -0.5),
+}
+
+EDGE_HEAD_DIM = 128      # one designed group followed by one balancing group
+EDGE_TINY = 2.0 ** -20   # elements below this are left out of the balance
+
+
+def _bf16_floor(x: float) -> float:
+    """The largest bf16 value <= x, for x > 0 (8 significant bits)."""
+    m, e = np.frexp(x)                       # x = m * 2^e, m in [0.5, 1)
+    return float(np.ldexp(np.floor(np.ldexp(m, 8)), e - 8))
+
+
+def _balance_group(sum_sq, seed: int) -> np.ndarray:
+    """64 bf16 values whose squares sum to exactly `sum_sq` (a Fraction >= 0),
+    taken greedily (largest bf16 square that still fits), with seeded signs
+    and order.  Raises if 64 values do not suffice."""
+    from fractions import Fraction
+    rest = Fraction(sum_sq)
+    # values are kept on the grid 2^-k with 2^-2k dividing sum_sq, so every
+    # remainder stays a whole number of grid squares and the loop ends
+    u = rest.denominator.bit_length() - 1          # sum_sq is a multiple of 2^-u
+    k = (u + 1) // 2
+    grid = 2.0 ** -k
+    vals = []
+    while rest > 0:
+        if len(vals) == GROUP:
+            raise ValueError("balancing group needs more than 64 values")
+        v = _bf16_floor(float(rest) ** 0.5)
+        v = float(np.floor(v / grid)) * grid
+        while Fraction(v) ** 2 > rest:          # float sqrt may round up
+            v = float(np.floor(_bf16_floor(np.nextafter(v, 0.0)) / grid)) * grid
+        vals.append(v)
+        rest -= Fraction(v) ** 2
+    out = np.zeros(GROUP)
+    out[:len(vals)] = vals
+    g = _rng(seed, P_CACHE_K, 99)
+    out *= np.where(g.random(GROUP) < 0.5, -1.0, 1.0)
+    return out[g.permutation(GROUP)]
+
+
+def quantizer_edge_rows(seed: int = 1007):
+    """Rows [n, 1, EDGE_HEAD_DIM] (bf16 bit patterns) whose first group is one
+    of EDGE_GROUPS and whose second group makes the squares of the row's
+    elements (those of magnitude >= EDGE_TINY) sum to exactly EDGE_HEAD_DIM.
+    The row's mean square is then 1 (up to the left-out tiny elements, which
+    move it by less than 2^-40 relative), so an RMSNorm without weight and with
+    eps 0 leaves every element as it is and the quantizer sees the designed
+    group.  Returns (names, bits)."""
+    from fractions import Fraction
+    names = list(EDGE_GROUPS)
+    rows = np.zeros((len(names), 1, EDGE_HEAD_DIM))
+    for i, name in enumerate(names):
+        at, fill = EDGE_GROUPS[name]
+        grp = np.full(GROUP, fill)
+        for j, v in at.items():
+            grp[j] = v
+        big = sum(Fraction(float(v)) ** 2 for v in grp if abs(v) >= EDGE_TINY)
+        rows[i, 0, :GROUP] = grp
+        rows[i, 0, GROUP:] = _balance_group(Fraction(EDGE_HEAD_DIM) - big, seed + i)
+    f32 = rows.astype(np.float32)
+    if not np.array_equal(f32.astype(np.float64), rows, equal_nan=False):
+        raise ValueError("edge row value not exact in float32")
+    bits = bf16_bits_from_f32(f32)
+    back = (bits.astype(np.uint32) << 16).view(np.float32)
+    if not np.array_equal(back, f32) or not np.array_equal(np.signbit(back), np.signbit(f32)):
+        raise ValueError("edge row value not exact in bf16")
+    return names, bits
