@@ -14,7 +14,8 @@ import pytest
 
 import oracle as O
 import workloads as W
-from oracle_ref import attn_errors, compare_cache, expect_decode, expect_prefill, ring_slots
+from oracle_ref import (EDGE_BITS, EDGE_SPEC, attn_errors, compare_cache, edge_inputs, expect_decode,
+                        expect_edge, expect_prefill, ring_slots)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -284,6 +285,65 @@ def test_bad_descriptor_is_skipped(kvq):
     case.attend()
     torch.cuda.synchronize()
     assert np.all(np.isnan(case.out.cpu().numpy()[1]))
+
+
+def test_quantizer_edge_rows(kvq):
+    """Hand-designed groups (an fp32-quotient midpoint, exact ties, a constant
+    group, a -0 minimum, a bf16 scale that is not (max - min) / (2^b - 1), a
+    nearly constant and an all-negative group) appended as one prompt chunk
+    into a 4-bit and an 8-bit cache: prepped rows and cache bytes bit-exact
+    with the oracle, the designed codes read back from the GPU cache, then the
+    prompt path (every row) and the decode path (the last row) within the
+    tolerance."""
+    m, harness = kvq
+    from quantized_kv_attention_quant_gb300.cache import LayerCaches
+    names, k, v, q, w = edge_inputs()
+    n, D, dev = len(names), EDGE_SPEC.head_dim, "cuda"
+    ns = len(EDGE_BITS)
+    lay = harness.kvq_layer(EDGE_SPEC)
+    caches = LayerCaches(1, D, list(EDGE_BITS), [W.TILE_KEYS] * ns, dev)
+    w_d = harness.dev_bits(w, dev)
+    k_d = harness.dev_bits(np.concatenate([k] * ns), dev)
+    v_d = harness.dev_bits(np.concatenate([v] * ns), dev)
+    q_d = harness.dev_bits(np.concatenate([q] * ns), dev)
+    offs = harness.dev_i32(np.arange(ns + 1) * n, dev)
+    start = harness.dev_i32([0] * ns, dev)
+    kvp = torch.empty((2, ns * n, 1, D), dtype=torch.int16, device=dev)
+    m.kv_quant_append(lay, caches.desc, ns, offs, start, ns * n, k_d, v_d, w_d, kvp)
+    ws_bytes = m.attn_prefill_workspace_bytes(lay, ns, ns * n, n)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((ns * n, EDGE_SPEC.n_q_heads, D), dtype=torch.float32, device=dev)
+    m.attn_prefill_chunk(lay, caches.desc, ns, offs, start, ns * n, n, q_d, w_d, out, 1, None, ws, ws_bytes)
+    pos = harness.dev_i32([n - 1] * ns, dev)
+    q_last = harness.dev_bits(np.stack([q[n - 1]] * ns), dev)
+    wsd_bytes = m.attn_decode_workspace_bytes(lay, ns, n - 1)
+    wsd = torch.empty(wsd_bytes, dtype=torch.uint8, device=dev)
+    out_d = torch.empty((ns, EDGE_SPEC.n_q_heads, D), dtype=torch.float32, device=dev)
+    m.attn_decode(lay, caches.desc, ns, pos, n - 1, q_last, w_d, out_d, 1, None, wsd, wsd_bytes)
+    torch.cuda.synchronize()
+    assert int(ws[:4].cpu().numpy().view(np.uint32)[0]) == 0
+    assert int(wsd[:4].cpu().numpy().view(np.uint32)[0]) == 0
+    got_kv = kvp.cpu().numpy().view(np.uint16)
+    got = out.cpu().numpy()
+    got_d = out_d.cpu().numpy()
+    for s, bits in enumerate(EDGE_BITS):
+        e = expect_edge(bits)
+        r = slice(s * n, (s + 1) * n)
+        assert np.array_equal(got_kv[0, r], k) and np.array_equal(got_kv[1, r], v), f"{bits}-bit: prep"
+        assert np.array_equal(got_kv[0, r], O.f64_to_bf16(e.k_hat)), f"{bits}-bit: k prep"
+        rows = caches.host_rows(s, np.arange(n))
+        assert compare_cache(rows, e.cache, np.arange(n)) == 0, f"{bits}-bit: cache bytes"
+        # the designed codes, unpacked from the GPU's own words
+        tie = names.index(f"fp32-quotient-tie-{bits}")
+        c = O.unpack(rows["k_codes"][0, tie], bits)
+        assert (c[0], c[1], c[2]) == ((0, 15, 0) if bits == 4 else (0, 254, 0))
+        assert rows["k_biases"][0, names.index("negative-zero-min"), 0] == 0x0000
+        assert rows["k_scales"][0, names.index("constant"), 0] == 0
+        for t in range(n):
+            mx, mean = attn_errors(got[s * n + t], e.out[t])
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{bits}-bit row {t} ({names[t]}): max {mx} mean {mean}"
+        mx, mean = attn_errors(got_d[s], e.out[n - 1])
+        assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{bits}-bit decode: max {mx} mean {mean}"
 
 
 # ----------------------------------------------------------------------------
