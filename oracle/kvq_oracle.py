@@ -32,6 +32,9 @@ Readings taken where the pages are silent:
   R-norm: y = rn_bf16(x / sqrt(mean(x^2) + eps) * w); w = 1 for v.
   R-rope: rotate-half pairs (j, j + R/2) for j < R/2 with frequency
           theta^(-2j/D) over the FULL head_dim D; dims >= R pass through.
+          The frequency is taken as its float64 value and the angle is that
+          value times the integer position without rounding (positions
+          below 2^24).
   R-quant: the stored bf16 scale is the divisor; a constant group has scale
           0 and all codes 0.
   R-window: a query at position p sees keys max(0, p-W+1) .. p (W keys).
@@ -106,6 +109,27 @@ def rope_inv_freq(theta: float, head_dim: int, rope_dims: int) -> np.ndarray:
                     dtype=np.float64)
 
 
+def rope_angle(pos: np.ndarray, f: np.ndarray):
+    """The angles pos * f [T, half] for integer positions 0 <= pos < 2^24 and
+    the float64 frequencies f, as hi + lo equal to the exact product (reading
+    R-rope: the frequency is the float64 value of theta^(-2j/D), the angle that
+    value times the position, unrounded).  f is split into a 26-bit head and a
+    tail (Veltkamp), so pos * head and pos * tail are exact in float64; hi is
+    their rounded sum and lo its rounding error (Knuth's two-sum)."""
+    p = np.asarray(pos, dtype=np.float64)[:, None]
+    if np.any(p < 0) or np.any(p >= 2.0 ** 24) or np.any(p != np.floor(p)):
+        raise ValueError("positions must be integers in [0, 2^24)")
+    f = np.asarray(f, dtype=np.float64)[None, :]
+    t = 134217729.0 * f                       # 2^27 + 1
+    head = t - (t - f)
+    tail = f - head
+    p1, p2 = p * head, p * tail               # both exact
+    hi = p1 + p2
+    b = hi - p1
+    lo = (p1 - (hi - b)) + (p2 - b)
+    return hi, lo
+
+
 def rope(x: np.ndarray, pos: np.ndarray, theta: float, rope_dims: int) -> np.ndarray:
     """Rotary embedding of rows x [..., T, H, D] at positions pos [T].
 
@@ -118,9 +142,10 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float, rope_dims: int) -> np.nda
         return x.copy()
     half = R // 2
     f = rope_inv_freq(theta, D, R)
-    a = np.asarray(pos, dtype=np.float64)[:, None] * f[None, :]       # [T, half]
-    c = np.cos(a)[:, None, :]
-    s = np.sin(a)[:, None, :]
+    hi, lo = rope_angle(pos, f)                                       # [T, half]
+    # cos and sin of hi + lo by the angle-addition formulas
+    c = (np.cos(hi) * np.cos(lo) - np.sin(hi) * np.sin(lo))[:, None, :]
+    s = (np.sin(hi) * np.cos(lo) + np.cos(hi) * np.sin(lo))[:, None, :]
     y = x.copy()
     x1 = x[..., :half]
     x2 = x[..., half:R]
@@ -257,58 +282,73 @@ class OracleCache:
     """Quantized K/V history of one sequence of one layer, indexed by position.
 
     The GPU library stores position j at slot j % capacity; this model keeps
-    every position it was given, densely, so that any window can be read back
-    and any ring layout rebuilt from it."""
+    every position it was given, densely from the lowest one (`base`), so that
+    any window can be read back and any ring layout rebuilt from it."""
 
     def __init__(self, n_kv_heads: int, head_dim: int, bits: int):
         self.H, self.D, self.bits = n_kv_heads, head_dim, bits
         G = head_dim // GROUP
+        self.base = 0
         self.kc = np.zeros((0, n_kv_heads, head_dim), np.uint32)
         self.vc = np.zeros((0, n_kv_heads, head_dim), np.uint32)
         self.ks = np.zeros((0, n_kv_heads, G)); self.kb = np.zeros((0, n_kv_heads, G))
         self.vs = np.zeros((0, n_kv_heads, G)); self.vb = np.zeros((0, n_kv_heads, G))
         self.valid = np.zeros(0, bool)
 
-    def _grow(self, n):
-        if n <= len(self.valid):
-            return
-        def ext(a):
-            z = np.zeros((n - a.shape[0],) + a.shape[1:], a.dtype)
-            return np.concatenate([a, z])
-        self.kc, self.vc = ext(self.kc), ext(self.vc)
-        self.ks, self.kb, self.vs, self.vb = ext(self.ks), ext(self.kb), ext(self.vs), ext(self.vb)
-        self.valid = ext(self.valid)
+    def _arrays(self):
+        return ["kc", "vc", "ks", "kb", "vs", "vb", "valid"]
+
+    def _cover(self, lo, hi):
+        """Extend the arrays to hold positions lo .. hi."""
+        if len(self.valid) == 0:
+            self.base = lo
+        if lo < self.base:
+            for name in self._arrays():
+                a = getattr(self, name)
+                z = np.zeros((self.base - lo,) + a.shape[1:], a.dtype)
+                setattr(self, name, np.concatenate([z, a]))
+            self.base = lo
+        n = hi - self.base + 1
+        if n > len(self.valid):
+            for name in self._arrays():
+                a = getattr(self, name)
+                z = np.zeros((n - a.shape[0],) + a.shape[1:], a.dtype)
+                setattr(self, name, np.concatenate([a, z]))
 
     def append(self, positions, k_hat, v_hat):
         """Quantize and store prepped rows k_hat / v_hat [T, Hkv, D]."""
         pos = np.asarray(positions, dtype=np.int64)
         if len(pos) == 0:
             return
-        self._grow(int(pos.max()) + 1)
+        self._cover(int(pos.min()), int(pos.max()))
+        i = pos - self.base
         kc, ks, kb = quantize(k_hat, self.bits)
         vc, vs, vb = quantize(v_hat, self.bits)
-        self.kc[pos], self.ks[pos], self.kb[pos] = kc, ks, kb
-        self.vc[pos], self.vs[pos], self.vb[pos] = vc, vs, vb
-        self.valid[pos] = True
+        self.kc[i], self.ks[i], self.kb[i] = kc, ks, kb
+        self.vc[i], self.vs[i], self.vb[i] = vc, vs, vb
+        self.valid[i] = True
 
-    def _check(self, lo, hi):
-        if not self.valid[lo:hi + 1].all():
+    def _index(self, lo, hi):
+        """Array slice of positions lo .. hi, all of which must be cached."""
+        a, b = lo - self.base, hi - self.base + 1
+        if a < 0 or b > len(self.valid) or not self.valid[a:b].all():
             raise KeyError(f"positions {lo}..{hi} not all cached")
+        return slice(a, b)
 
     def k_hat(self, lo, hi):
-        self._check(lo, hi)
-        return dequantize(self.kc[lo:hi + 1], self.ks[lo:hi + 1], self.kb[lo:hi + 1])
+        i = self._index(lo, hi)
+        return dequantize(self.kc[i], self.ks[i], self.kb[i])
 
     def v_hat(self, lo, hi):
-        self._check(lo, hi)
-        return dequantize(self.vc[lo:hi + 1], self.vs[lo:hi + 1], self.vb[lo:hi + 1])
+        i = self._index(lo, hi)
+        return dequantize(self.vc[i], self.vs[i], self.vb[i])
 
     def packed(self, positions):
         """Packed words and bf16 bit patterns of the listed positions:
         (k_words [n, H, D*b/32], k_scales [n, H, D/64], k_biases, v_words,
         v_scales, v_biases)."""
-        p = np.asarray(positions, dtype=np.int64)
-        if not self.valid[p].all():
+        p = np.asarray(positions, dtype=np.int64) - self.base
+        if len(p) and (p.min() < 0 or p.max() >= len(self.valid) or not self.valid[p].all()):
             raise KeyError("position not cached")
         return (pack(self.kc[p], self.bits), f64_to_bf16(self.ks[p]), f64_to_bf16(self.kb[p]),
                 pack(self.vc[p], self.bits), f64_to_bf16(self.vs[p]), f64_to_bf16(self.vb[p]))

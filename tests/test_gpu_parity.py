@@ -287,6 +287,26 @@ def test_bad_descriptor_is_skipped(kvq):
     assert np.all(np.isnan(case.out.cpu().numpy()[1]))
 
 
+def test_largest_positions(kvq):
+    """Positions up to 2^24 - 1, the largest the calls accept, on window
+    layers (the ring holds only the window, so the caches stay small): decode
+    at D256 with full RoPE and at D512 with partial RoPE and K = V, and a
+    prompt chunk ending at 2^24 - 2.  Some positions put cos or sin of a
+    rotary angle next to zero, where the angle has to be formed without
+    rounding to give the right bf16 row."""
+    _, harness = kvq
+    P = 2 ** 24 - 1
+    wl = W.DecodeWorkload("pos-max-d256", 87, _spec(8, 2, 256, 64, 256),
+                          filled=[P, P - 1, 11039086, 14207257, 2 ** 23], bits=[4, 8, 8, 4, 8])
+    check_decode(harness, wl)
+    wl = W.DecodeWorkload("pos-max-d512-keqv", 88, _spec(16, 1, 512, 64, 128, 1e6, True),
+                          filled=[P, 11311958, 10761476], bits=[8, 4, 8])
+    check_decode(harness, wl)
+    wl = W.PrefillWorkload("pos-max-chunk", 89, _spec(8, 2, 256, 64, 256),
+                           filled=[P - 40, 11039080], chunk=[40, 17], bits=[8, 4])
+    check_prefill(harness, wl)
+
+
 def test_quantizer_edge_rows(kvq):
     """Hand-designed groups (an fp32-quotient midpoint, exact ties, a constant
     group, a -0 minimum, a bf16 scale that is not (max - min) / (2^b - 1), a

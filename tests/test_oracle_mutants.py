@@ -48,8 +48,10 @@ MUTANTS = {
     "softmax-max-over-heads": ("m = s.max(axis=-1, keepdims=True)", "m = s.max()"),
     "norm-one-plus-weight": ("y = y * np.asarray(w, dtype=np.float64)",
                              "y = y * (1.0 + np.asarray(w, dtype=np.float64))"),
-    "rope-position-plus-one": ("a = np.asarray(pos, dtype=np.float64)[:, None] * f[None, :]",
-                               "a = (np.asarray(pos, dtype=np.float64)[:, None] + 1) * f[None, :]"),
+    "rope-position-plus-one": ("    p = np.asarray(pos, dtype=np.float64)[:, None]\n",
+                               "    p = np.asarray(pos, dtype=np.float64)[:, None] + 1\n"),
+    "rope-angle-rounded-to-f64": ("hi, lo = rope_angle(pos, f)",
+                                  "hi, lo = np.asarray(pos, dtype=np.float64)[:, None] * f[None, :], 0.0"),
     "rope-partial-ignored": ("    R = int(rope_dims)\n", "    R = D if int(rope_dims) else 0\n"),
     "rope-exponent-j-over-D": ("math.pow(theta, -(2.0 * j) / head_dim)", "math.pow(theta, -(1.0 * j) / head_dim)"),
     "query-excludes-itself": ("return lo, p\n", "return lo, max(lo, p - 1)\n"),
@@ -73,7 +75,7 @@ PINS = [
     P.pin_quant_ties, P.pin_quant_negative_zero, P.pin_quant_bf16_scale_divides, P.pin_quant_fp32_quotient,
     P.pin_quant_group_independence,
     lambda o: P.pin_quant_invariants(o, 4), lambda o: P.pin_quant_invariants(o, 8),
-    P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants,
+    P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants, P.pin_rope_large_positions,
     P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,
 ]
 

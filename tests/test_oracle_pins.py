@@ -313,9 +313,52 @@ def pin_rope_invariants(o):
     assert abs(d1 - d2) < 0.1
 
 
+def _mp_bf16(mpmath, v):
+    """A high-precision value rounded to the nearest bf16 (8 significant
+    bits), in mpmath; refuses values within 1e-9 units of a tie."""
+    if v == 0:
+        return 0.0
+    _, e = mpmath.frexp(v)                    # v = m * 2^e, |m| in [0.5, 1)
+    units = mpmath.ldexp(v, 8 - int(e))
+    r = mpmath.nint(units)
+    assert abs(abs(units - r) - 0.5) > 1e-9, "too close to a bf16 tie"
+    return float(mpmath.ldexp(r, int(e) - 8))
+
+
+# (theta, head_dim, position, pair index j): cos or sin of the angle lies near
+# zero, where rounding the product position * frequency to float64 (an error
+# up to 2^-29 at these positions) moves the bf16 result by one unit
+ROPE_NEAR_ZERO = [(1e4, 256, 11039086, 13), (1e4, 256, 14207257, 8),
+                  (1e6, 512, 11311958, 5), (1e6, 512, 10761476, 17)]
+
+
+def pin_rope_large_positions(o):
+    """Unit vectors rotated at positions up to 2^24 - 1 against cos and sin of
+    position * f evaluated by mpmath at 200 bits, f the float64 frequency
+    theta^(-2j/D), each rounded to bf16."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 200
+    cases = list(ROPE_NEAR_ZERO)
+    rng = np.random.default_rng(9)
+    for p in [2 ** 24 - 1, 2 ** 23 + 1, int(rng.integers(2 ** 20, 2 ** 24))]:
+        cases += [(1e4, 256, p, j) for j in range(0, 128, 7)]
+    for theta, D, p, j in cases:
+        x = np.zeros((2, 1, D))
+        x[0, 0, j] = 1.0             # -> (cos a, sin a) at (j, j + D/2)
+        x[1, 0, j + D // 2] = 1.0    # -> (-sin a, cos a)
+        y = o.rope(x, np.array([p, p]), theta, D)
+        a = mpmath.mpf(p) * mpmath.mpf(math.pow(theta, -(2.0 * j) / D))
+        c, s = _mp_bf16(mpmath, mpmath.cos(a)), _mp_bf16(mpmath, mpmath.sin(a))
+        assert (y[0, 0, j], y[0, 0, j + D // 2]) == (c, s), (theta, D, p, j)
+        assert (y[1, 0, j], y[1, 0, j + D // 2]) == (-s, c), (theta, D, p, j)
+    with pytest.raises(ValueError):
+        o.rope(np.zeros((1, 1, 64)), np.array([2 ** 24]), 1e4, 64)
+
+
 def test_rope():
     pin_rope_hand(O)
     pin_rope_invariants(O)
+    pin_rope_large_positions(O)
 
 
 # ----------------------------------------------------------------------------
