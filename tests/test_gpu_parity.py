@@ -78,6 +78,8 @@ DECODE_CASES = {
     "d64-full-rope": (_spec(2, 1, 64, 0, 64), [80, 64], [8, 4]),
     "gqa8-d256": (_spec(8, 1, 256, 0, 64, 1e6), [190], [4]),
     "gqa1-d512-window": (_spec(2, 2, 512, 64, 512), [130, 64], [8, 4]),
+    # G = 3 (not a power of two), a large eps and a single rotated pair
+    "gqa3-eps-half-rope2": (W.LayerSpec(6, 2, 256, 0, 2, 1e4, False, rms_eps=0.5), [100, 7], [4, 8]),
 }
 
 
@@ -414,6 +416,15 @@ def test_verify_windows(kvq):
     check_prefill(harness, wl)
     spec = _spec(16, 1, 512, 0, 128, 1e6, True)
     wl = W.PrefillWorkload("verify-full", 85, spec, filled=[90, 3], chunk=[5, 17], bits=[8, 4])
+    check_prefill(harness, wl)
+
+
+def test_prefill_row_path_gqa3(kvq):
+    """A GQA ratio that does not divide the tensor-core kernel's 128 rows
+    (G = 3) takes the row path for a prompt chunk on a window layer."""
+    _, harness = kvq
+    spec = W.LayerSpec(6, 2, 128, 48, 128, 1e4, False)
+    wl = W.PrefillWorkload("gqa3-rows", 90, spec, filled=[30, 0], chunk=[20, 9], bits=[8, 4])
     check_prefill(harness, wl)
 
 
