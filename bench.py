@@ -72,12 +72,27 @@ def load_peaks():
             "source": "measured" if hbm else "fallback"}
 
 
-def source_hash() -> str:
+# The sources that make up one kernel: its translation unit and every header
+# of this repository it includes (the launch plan and the launch live in the
+# same .cu).  A traffic figure stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "decode_kernel_512": ["quantized_kv_attention_quant_gb300/csrc/kvq_decode.cu",
+                          "quantized_kv_attention_quant_gb300/csrc/kvq_common.cuh",
+                          "quantized_kv_attention_quant_gb300/csrc/rope_consts.h",
+                          "quantized_kv_attention_quant_gb300/csrc/kvq_internal.h",
+                          "quantized_kv_attention_quant_gb300/csrc/kvq_qprep.cuh",
+                          "include/kvq.h"],
+}
+
+
+def source_hash(kernel: str) -> str | None:
+    files = KERNEL_SOURCES.get(kernel)
+    if not files:
+        return None
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "quantized_kv_attention_quant_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in files:
+        h.update(f.encode() + b"\0")
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -93,7 +108,7 @@ def traffic_for(kernel: str, workload: str, algorithmic_per_launch: float):
     except (OSError, ValueError):
         return None
     e = t.get(kernel, {}).get(workload)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") is None or e.get("source_hash") != source_hash(kernel):
         return None
     if e.get("dram_bytes_per_launch") is not None:
         return float(e["dram_bytes_per_launch"])
