@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -85,14 +86,27 @@ KERNEL_SOURCES = {
 }
 
 
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|/\*.*?\*/|//[^\n]*', re.S)
+
+
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed
+    (string and character literals kept as they are)."""
+    def keep(m):
+        t = m.group(0)
+        return t if t[0] in "\"'" else " "
+    return " ".join(_C_TOKENS.sub(keep, text).split())
+
+
 def source_hash(kernel: str) -> str | None:
+    """Hash of the code (comments and layout aside) of a kernel's sources."""
     files = KERNEL_SOURCES.get(kernel)
     if not files:
         return None
     h = hashlib.sha256()
     for f in files:
         h.update(f.encode() + b"\0")
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, f), encoding="utf-8").read()).encode() + b"\0")
     return h.hexdigest()[:16]
 
 

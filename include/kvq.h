@@ -143,7 +143,8 @@ kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, in
  *   seqs        device kvq_seq_cache[n_seqs]
  *   pos         device int32[n_seqs], 0 <= pos < 2^24; the cache must hold
  *               every visible key (ring capacity >= window, linear capacity > pos)
- *   max_pos     host upper bound of pos[] (sizes the split over the cache length)
+ *   max_pos     host upper bound of pos[] (sizes the split over the cache length),
+ *               0 <= max_pos < 2^24, else KVQ_EINVAL (and a workspace size of 0)
  *   q_raw       device bf16 [n_seqs][n_q_heads][head_dim]
  *   q_norm_w    device bf16 [head_dim]
  *   out         device [n_seqs][n_q_heads][head_dim], fp32 if out_is_f32 else bf16
@@ -223,7 +224,7 @@ typedef struct {
   const int32_t* row_offsets;    /* window: device int32[n_seqs + 1]; decode: ignored */
   const int32_t* pos;            /* device int32[n_seqs]: decode positions, or window start positions */
   int32_t n_rows;                /* window: rows of the group; decode: ignored (one row per sequence) */
-  int32_t max_pos;               /* decode: host upper bound of pos[]; window: ignored */
+  int32_t max_pos;               /* decode: host upper bound of pos[], below 2^24; window: ignored */
   int32_t max_rows_per_seq;      /* window: host upper bound of rows per sequence; decode: ignored */
   const uint16_t* q_raw;         /* device bf16 [rows][n_q_heads][head_dim] */
   void* out;                     /* device [rows][n_q_heads][head_dim], fp32 if out_is_f32 else bf16 */

@@ -32,6 +32,9 @@ kvq_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
+// Positions are below 2^24 (exact in fp32); checked before max_pos + 1 is formed.
+bool max_pos_ok(int32_t max_pos) { return max_pos >= 0 && max_pos < (1 << 24); }
+
 // theta^(-2j/D) (libm pow, float64) split into three floats that sum to it
 // exactly, cached per (theta, D, rope_dims).
 const kvq::RopeFreqs& rope_freqs(double theta, int D, int R) {
@@ -239,14 +242,14 @@ kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_
                        const int32_t* pos, int32_t max_pos, const uint16_t* q_raw, const uint16_t* q_norm_w,
                        void* out, int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
                        size_t workspace_bytes, void* stream) {
-  if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
+  if (!max_pos_ok(max_pos)) return fail(KVQ_EINVAL, "max_pos %d not in [0, 2^24)", max_pos);
   return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, 0, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
 size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos) {
   kvq::LayerArgs L;
-  if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || max_pos < 0) return 0;
+  if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || !max_pos_ok(max_pos)) return 0;
   const kvq::DecodePlan plan = kvq::decode_plan(L, n_seqs, max_pos + 1, num_sms_current(), true);
   return kvq::decode_ws_bytes(n_seqs, L.n_kv, L.D, plan);
 }
@@ -333,7 +336,7 @@ kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int3
     const kvq_attn_group& g = groups[i];
     kvq_status st;
     if (g.phase == KVQ_PHASE_DECODE) {
-      if (g.max_pos < 0) return fail(KVQ_EINVAL, "group %d: max_pos %d < 0", i, g.max_pos);
+      if (!max_pos_ok(g.max_pos)) return fail(KVQ_EINVAL, "group %d: max_pos %d not in [0, 2^24)", i, g.max_pos);
       st = attention_prepare(layer, g.seqs, g.n_seqs, nullptr, g.pos, g.n_seqs, g.max_pos + 1, true, 0, g.q_raw,
                              q_norm_w, g.out, out_is_f32, g.q_prepped, g.workspace, g.workspace_bytes, &p[i]);
     } else if (g.phase == KVQ_PHASE_WINDOW) {
@@ -449,7 +452,7 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
                               const int32_t* pos, int32_t max_pos, const uint16_t* q_raw,
                               const uint16_t* q_norm_w, void* out, int32_t out_is_f32, uint16_t* q_prepped,
                               void* stream) {
-  if (max_pos < 0) return fail(KVQ_EINVAL, "max_pos %d < 0", max_pos);
+  if (!max_pos_ok(max_pos)) return fail(KVQ_EINVAL, "max_pos %d not in [0, 2^24)", max_pos);
   kvq::LayerArgs L;
   kvq_status st = check_layer(layer, &L);
   if (st != KVQ_OK) return st;

@@ -105,6 +105,12 @@ def test_bad_pointers_decode(m):
     assert f(L, P, 1, P, 10, P, P, P, 2, None, P, big, None) == 1         # out_is_f32 not 0/1
     assert f(L, P, 1, P, 10, P, P, P, 1, None, P + 16, big, None) == 1    # workspace not 256-aligned
     assert f(L, P, 1, P, -1, P, P, P, 1, None, P, big, None) == 1         # max_pos < 0
+    assert f(L, P, 1, P, 1 << 24, P, P, P, 1, None, P, big, None) == 1    # max_pos >= 2^24
+    assert f(L, P, 1, P, 2 ** 31 - 1, P, P, P, 1, None, P, big, None) == 1
+    assert m.attn_decode_workspace_bytes(lay, 1, 1 << 24) == 0
+    assert m.attn_decode_workspace_bytes(lay, 1, 2 ** 31 - 1) == 0
+    assert m.attn_decode_workspace_bytes(lay, 1, (1 << 24) - 1) > 0
+    assert m.lib.attn_decode_static(L, P, 1, P, 2 ** 31 - 1, P, P, P, 1, None, None) == 1
     need = m.attn_decode_workspace_bytes(lay, 1, 10)
     assert need > 0
     assert f(L, P, 1, P, 10, P, P, P, 1, None, P, need - 1, None) == 4    # workspace too small
@@ -150,6 +156,8 @@ def test_bad_mixed_groups(m):
     assert "group 1" in m.kvq_last_error()
     bad_pos = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, -1, 0, P, P, None, P, big)
     assert call([bad_pos]) == 1
+    far_pos = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, 2 ** 31 - 1, 0, P, P, None, P, big)
+    assert call([win, far_pos]) == 1 and "group 1" in m.kvq_last_error()
     no_offsets = m.attn_group(m.KVQ_PHASE_WINDOW, P, 1, None, P, 4, 0, 4, P, P, None, P, big)
     assert call([dec, no_offsets]) == 1
     misaligned = m.attn_group(m.KVQ_PHASE_DECODE, P, 1, None, P, 0, 10, 0, P + 8, P, None, P, big)
