@@ -32,8 +32,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-import numpy as np  # noqa: E402
-
 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
