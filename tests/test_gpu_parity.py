@@ -419,6 +419,22 @@ def test_verify_windows(kvq):
     check_prefill(harness, wl)
 
 
+def test_prefill_empty_sequences(kvq):
+    """Sequences with no new rows inside a prompt call (first, middle and
+    last), on the tensor-core path and on the row path, and a call with no
+    rows at all: the other sequences' rows, caches and outputs are as the
+    oracle has them."""
+    _, harness = kvq
+    wl = W.PrefillWorkload("empty-seqs-tc", 91, _spec(8, 2, 256, 64, 256), filled=[10, 100, 0, 7],
+                           chunk=[0, 12, 0, 5], bits=[4, 8, 8, 4])
+    check_prefill(harness, wl)
+    wl = W.PrefillWorkload("empty-seqs-rows", 92, _spec(16, 1, 512, 0, 128, 1e6, True), filled=[30, 5, 64],
+                           chunk=[3, 0, 0], bits=[8, 4, 8])
+    check_prefill(harness, wl)
+    wl = W.PrefillWorkload("no-rows", 93, _spec(8, 2, 256, 64, 256), filled=[10, 3], chunk=[0, 0], bits=[4, 8])
+    check_prefill(harness, wl)
+
+
 def test_prefill_row_path_gqa3(kvq):
     """A GQA ratio that does not divide the tensor-core kernel's 128 rows
     (G = 3) takes the row path for a prompt chunk on a window layer."""
