@@ -66,6 +66,21 @@ MUTANTS = {
                               "s = (s32.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)"),
     "dequant-bias-before-scale": ("x = c * np.asarray(scales)[..., None] + np.asarray(biases)[..., None]",
                                   "x = (c + np.asarray(biases)[..., None]) * np.asarray(scales)[..., None]"),
+    "norm-over-heads": ("ms = np.mean(x * x, axis=-1, keepdims=True)", "ms = np.mean(x * x, axis=-2, keepdims=True)"),
+    "rope-cos-sin-swapped": ("c = (np.cos(hi) * np.cos(lo) - np.sin(hi) * np.sin(lo))[:, None, :]\n"
+                             "    s = (np.sin(hi) * np.cos(lo) + np.cos(hi) * np.sin(lo))[:, None, :]",
+                             "s = (np.cos(hi) * np.cos(lo) - np.sin(hi) * np.sin(lo))[:, None, :]\n"
+                             "    c = (np.sin(hi) * np.cos(lo) + np.cos(hi) * np.sin(lo))[:, None, :]"),
+    "rope-angle-error-sign": ("    lo = (p1 - (hi - b)) + (p2 - b)\n", "    lo = -((p1 - (hi - b)) + (p2 - b))\n"),
+    "quant-levels-minus-one": ("s32 = (mx - mn) / levels", "s32 = (mx - mn) / (levels - 1)"),
+    "unpack-big-endian": ("parts = [(w >> np.uint64(i * bits)) & mask for i in range(per)]",
+                          "parts = [(w >> np.uint64((per - 1 - i) * bits)) & mask for i in range(per)]"),
+    "attend-values-reversed": ("return (p @ v_hat) / p.sum(axis=-1, keepdims=True)",
+                               "return (p @ v_hat[::-1]) / p.sum(axis=-1, keepdims=True)"),
+    "decode-attends-before-append": ("    cache.append(pos, k_hat, v_hat)\n    q_hat = prep_q(q_raw[None], q_w, pos,",
+                                     "    q_hat = prep_q(q_raw[None], q_w, pos,"),
+    "prefill-window-grows-in-chunk": ("outs[t] = attend_cache(q_hat[t], start + t, layer.window,",
+                                      "outs[t] = attend_cache(q_hat[t], start + t, layer.window + t,"),
     "bf16-7-bits": ("q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
                     "q = np.ldexp(np.rint(np.ldexp(x, 7 - e)), e - 7)"),
 }
