@@ -2,6 +2,9 @@
 include/kvq.h declares, and rejects bad arguments with the documented status
 before enqueueing any GPU work (no compute call is made here)."""
 import ctypes
+import os
+import shutil
+import subprocess
 
 import pytest
 
@@ -175,3 +178,22 @@ def test_bad_selftest_arguments(m):
     assert f(P + 2, 1000000, None) == 1           # status misaligned
     assert f(P, 10, None) == 1                    # limit below 1 us
     assert f(P, 2000000000, None) == 1            # limit above 1 s
+
+
+def test_plain_c_program(m, tmp_path):
+    """include/kvq.h compiles as pedantic C11 and a C program links libkvq.so,
+    resolves every declared function and gets the documented host-side
+    results (tests/c_abi_check.c)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    libdir = os.path.dirname(m.LIB_PATH)
+    exe = str(tmp_path / "c_abi_check")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I" + os.path.join(root, "include"), os.path.join(here, "c_abi_check.c"),
+                    "-L" + libdir, "-lkvq", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout[-2000:]
+    assert r.stdout.strip().endswith("all checks passed")
