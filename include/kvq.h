@@ -118,7 +118,8 @@ typedef struct {
  *   n_rows        host copy of row_offsets[n_seqs]
  *   k_raw         device bf16 [n_rows][n_kv_heads][head_dim]
  *   v_raw         device bf16 [n_rows][n_kv_heads][head_dim]; NULL iff k_eq_v
- *   k_norm_w      device bf16 [head_dim]
+ *   k_norm_w      device bf16 [head_dim]; |w| <= 256 keeps the attention
+ *                 calls' f16 operands (k biases) finite
  *   kv_prepped    NULL, or device bf16 [2][n_rows][n_kv_heads][head_dim] that
  *                 receives k_hat and v_hat (for inspection)
  */
@@ -146,7 +147,8 @@ kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, in
  *   max_pos     host upper bound of pos[] (sizes the split over the cache length),
  *               0 <= max_pos < 2^24, else KVQ_EINVAL (and a workspace size of 0)
  *   q_raw       device bf16 [n_seqs][n_q_heads][head_dim]
- *   q_norm_w    device bf16 [head_dim]
+ *   q_norm_w    device bf16 [head_dim]; q_hat and its per-group sums enter the
+ *               MMAs as f16, finite for |w| <= 256 (|q_hat| <= sqrt(head_dim) |w|)
  *   out         device [n_seqs][n_q_heads][head_dim], fp32 if out_is_f32 else bf16
  *   q_prepped   NULL, or device bf16 [n_seqs][n_q_heads][head_dim] receiving q_hat
  *   workspace   device scratch of at least attn_decode_workspace_bytes(...) bytes;
