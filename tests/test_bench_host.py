@@ -29,7 +29,8 @@ def test_peaks_fallback_and_measured(tmp_path, monkeypatch):
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
         {"gb300": {"hbm_gbs": 7100.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1750.0}}))
     p = bench.load_peaks()
-    assert p == {"hbm_gbs": 7100.0, "bf16_tflops": 1750.0, "source": "measured"}
+    # the burst bf16 figure (kernels are timed inside sub-millisecond steps)
+    assert p == {"hbm_gbs": 7100.0, "bf16_tflops": 2000.0, "source": "measured"}
 
 
 def test_clock_summary():
