@@ -1,0 +1,76 @@
+"""Property checks of the oracle's quantizer over generated bf16 groups
+(hypothesis; CPU only).  Groups are drawn as bf16 bit patterns, so tiny and
+large magnitudes, negative zeros, repeated values and constant groups all
+occur; magnitudes are bounded by 2^64, far above what the weightless RMS norm
+of the method can produce (at most sqrt(head_dim) times the norm weight)."""
+import numpy as np
+import pytest
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings  # noqa: E402
+from hypothesis import strategies as st  # noqa: E402
+
+import oracle as O  # noqa: E402
+
+
+def _bf16_values(bits_list):
+    b = np.array(bits_list, dtype=np.uint16)
+    return O.bf16_to_f64(b)
+
+
+# finite bf16 bit patterns with exponent field below 127 + 64 (|x| < 2^64)
+finite_bf16 = st.integers(0, 0xFFFF).filter(lambda u: ((u >> 7) & 0xFF) < 127 + 64)
+groups = st.lists(finite_bf16, min_size=64, max_size=64)
+
+
+@settings(max_examples=400, deadline=None, derandomize=True)
+@given(groups, st.sampled_from([4, 8]))
+def test_quantizer_properties(bits_list, bits):
+    x = _bf16_values(bits_list)[None]
+    c, s, b = O.quantize(x, bits)
+    c, s, b = c[0], float(s[0, 0]), float(b[0, 0])
+    top = 2 ** bits - 1
+    g = x[0]
+    # codes in range; bias is the group minimum (a zero minimum stored as +0)
+    assert c.min() >= 0 and c.max() <= top
+    assert b == g.min() and not (b == 0 and np.signbit(b))
+    # the scale is the bf16 value nearest (max - min) / (2^b - 1), up to the
+    # fp32 rounding of the difference and the quotient
+    rng = g.max() - g.min()
+    if rng == 0:
+        assert s == 0 and not c.any()
+        return
+    # monotone in x; the minimum takes code 0
+    order = np.argsort(g, kind="stable")
+    assert np.all(np.diff(c[order].astype(np.int64)) >= 0)
+    assert c[np.argmin(g)] == 0
+    if rng / top < 2.0 ** -126:
+        # a range below bf16's normal range: the scale is the nearest bf16
+        # subnormal (spacing 2^-133), possibly 0 -- then every code is 0
+        assert abs(s - rng / top) <= 2.0 ** -134 * (1 + 2.0 ** -20)
+        if s == 0:
+            assert not c.any()
+        return
+    # the scale is the bf16 value nearest (max - min) / (2^b - 1), up to the
+    # fp32 rounding of the difference and the quotient
+    assert abs(s - rng / top) <= (rng / top) * (2.0 ** -8 + 2.0 ** -22)
+    # the maximum takes the top code (or one below it when the bf16 scale
+    # rounded up)
+    assert c[np.argmax(g)] >= top - (1 if bits == 8 else 0)
+    # dequantized error: half a scale, plus the clamp slack at the top code
+    err = np.abs(c * s + b - g)
+    slack = top * abs(s - rng / top)
+    assert np.all(err <= s / 2 * (1 + 2.0 ** -20) + np.where(c == top, slack, 0) + 2.0 ** -60 * abs(b))
+    # pack and unpack are inverse
+    assert np.array_equal(O.unpack(O.pack(c[None], bits), bits)[0], c)
+
+
+@settings(max_examples=100, deadline=None, derandomize=True)
+@given(st.lists(groups, min_size=2, max_size=4), st.sampled_from([4, 8]))
+def test_groups_are_independent(gs, bits):
+    x = np.concatenate([_bf16_values(g) for g in gs])[None]
+    c, s, b = O.quantize(x, bits)
+    for i, g in enumerate(gs):
+        ci, si, bi = O.quantize(_bf16_values(g)[None], bits)
+        assert np.array_equal(c[0, 64 * i:64 * (i + 1)], ci[0])
+        assert s[0, i] == si[0, 0] and b[0, i] == bi[0, 0]
