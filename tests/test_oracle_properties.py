@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 hyp = pytest.importorskip("hypothesis")
-from hypothesis import given, settings  # noqa: E402
+from hypothesis import example, given, settings  # noqa: E402
 from hypothesis import strategies as st  # noqa: E402
 
 import oracle as O  # noqa: E402
@@ -74,3 +74,40 @@ def test_groups_are_independent(gs, bits):
         ci, si, bi = O.quantize(_bf16_values(g)[None], bits)
         assert np.array_equal(c[0, 64 * i:64 * (i + 1)], ci[0])
         assert s[0, i] == si[0, 0] and b[0, i] == bi[0, 0]
+
+
+def _bf16_neighbours(r: float):
+    """The bf16 values just below and above the bf16 value r (finite, r != 0)."""
+    u = int(np.array([r], dtype=np.float32).view(np.uint32)[0]) >> 16
+    def val(v):
+        return float(np.array([v << 16], dtype=np.uint32).view(np.float32)[0])
+    a, b = val(u - 1), val(u + 1)          # one unit of the magnitude, either way
+    return (min(a, b), max(a, b))
+
+
+@settings(max_examples=2000, deadline=None, derandomize=True)
+@given(st.floats(min_value=-2.0 ** 100, max_value=2.0 ** 100, allow_nan=False, allow_infinity=False,
+                 width=64).filter(lambda v: v == 0 or abs(v) >= 2.0 ** -120))
+@example(1.0 + 2.0 ** -8)                 # tie -> 1.0 (even)
+@example(1.0 + 3 * 2.0 ** -8)             # tie -> 1 + 2^-6 (even)
+@example(-(1.0 + 2.0 ** -8))
+@example((1.0 + 2.0 ** -8) * 2.0 ** -119)
+@example(1.0 + 2.0 ** -8 + 2.0 ** -52)    # just above a tie
+@example(255.5 * 2.0 ** 40)               # tie at the top of a binade -> next binade
+def test_rn_bf16_is_nearest_ties_to_even(x):
+    """rn_bf16 on arbitrary float64 values (the norm and rotation outputs are
+    float64 before their bf16 rounding), checked against the definition: the
+    result is a bf16 value, no neighbouring bf16 value is closer (exact
+    arithmetic), and a tie goes to the even mantissa."""
+    from fractions import Fraction
+    r = float(O.rn_bf16(np.array([x]))[0])
+    bits = int(np.array([r], dtype=np.float32).view(np.uint32)[0])
+    assert float(np.float32(r)) == r and bits & 0xFFFF == 0
+    if x == 0:
+        assert r == 0
+        return
+    lo, hi = _bf16_neighbours(r)
+    d = abs(Fraction(x) - Fraction(r))
+    assert d <= abs(Fraction(x) - Fraction(lo)) and d <= abs(Fraction(x) - Fraction(hi))
+    if d == abs(Fraction(x) - Fraction(lo)) or d == abs(Fraction(x) - Fraction(hi)):
+        assert (bits >> 16) & 1 == 0, "a tie must round to the even mantissa"
