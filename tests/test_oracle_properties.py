@@ -111,3 +111,64 @@ def test_rn_bf16_is_nearest_ties_to_even(x):
     assert d <= abs(Fraction(x) - Fraction(lo)) and d <= abs(Fraction(x) - Fraction(hi))
     if d == abs(Fraction(x) - Fraction(lo)) or d == abs(Fraction(x) - Fraction(hi)):
         assert (bits >> 16) & 1 == 0, "a tie must round to the even mantissa"
+
+
+def _mp_round_bf16(mpmath, v):
+    """(nearest bf16 of the high-precision value v, distance of v from a bf16
+    tie in units of the bf16 spacing)."""
+    if v == 0:
+        return 0.0, 1.0
+    _, e = mpmath.frexp(v)
+    e = max(int(e), -125)
+    units = mpmath.ldexp(v, 8 - e)
+    n = mpmath.nint(units)
+    return float(mpmath.ldexp(n, e - 8)), float(abs(abs(units - mpmath.floor(units)) - 0.5))
+
+
+# bf16 values of magnitude 2^-20 .. 2^8: sign, exponent field and mantissa drawn directly
+elem_bf16 = st.tuples(st.integers(0, 1), st.integers(127 - 20, 127 + 7), st.integers(0, 127)).map(
+    lambda t: (t[0] << 15) | (t[1] << 7) | t[2])
+row_bf16 = st.lists(elem_bf16, min_size=64, max_size=64)
+weight_bf16 = st.lists(st.integers(0x3F00, 0x4000), min_size=64, max_size=64)     # 0.5 .. 2
+
+
+@settings(max_examples=60, deadline=None, derandomize=True)
+@given(row_bf16, weight_bf16, st.sampled_from([0.0, 1e-6, 0.5]))
+def test_rms_norm_is_the_correctly_rounded_definition(xb, wb, eps):
+    """RMSNorm against mpmath at 120 bits: y_i is the bf16 value nearest
+    x_i / sqrt(mean(x^2) + eps) * w_i (elements within 2^-40 of a tie aside,
+    where the float64 oracle's own rounding could decide)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 120
+    x, w = _bf16_values(xb), _bf16_values(wb)
+    y = O.rms_norm(x[None], w, eps)[0]
+    ms = mpmath.fsum(mpmath.mpf(float(v)) ** 2 for v in x) / len(x)
+    inv = 1 / mpmath.sqrt(ms + mpmath.mpf(float(np.float64(eps))))
+    for i in range(len(x)):
+        want, tie_dist = _mp_round_bf16(mpmath, mpmath.mpf(float(x[i])) * inv * mpmath.mpf(float(w[i])))
+        if tie_dist > 2.0 ** -40:
+            assert y[i] == want, (i, x[i], w[i], y[i], want)
+
+
+@settings(max_examples=60, deadline=None, derandomize=True)
+@given(row_bf16, st.integers(0, 2 ** 24 - 1), st.sampled_from([(1e4, 64), (1e6, 32)]))
+def test_rope_is_the_correctly_rounded_definition(xb, pos, theta_r):
+    """RoPE against mpmath at 200 bits on general vectors (head_dim 64): each
+    rotated element is the bf16 value nearest x_j cos(a) -/+ x_{j+R/2} sin(a),
+    a = pos * float64(theta^(-2j/64)); dims >= R unchanged."""
+    import math
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 200
+    theta, R = theta_r
+    x = _bf16_values(xb)
+    y = O.rope(x[None, None], np.array([pos]), theta, R)[0, 0]
+    half = R // 2
+    assert np.array_equal(y[R:], x[R:])
+    for j in range(half):
+        a = mpmath.mpf(pos) * mpmath.mpf(math.pow(theta, -(2.0 * j) / 64))
+        c, s = mpmath.cos(a), mpmath.sin(a)
+        x1, x2 = mpmath.mpf(float(x[j])), mpmath.mpf(float(x[j + half]))
+        for idx, v in ((j, x1 * c - x2 * s), (j + half, x2 * c + x1 * s)):
+            want, tie_dist = _mp_round_bf16(mpmath, v)
+            if tie_dist > 2.0 ** -40:
+                assert y[idx] == want, (pos, j, idx, y[idx], want)
