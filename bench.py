@@ -110,22 +110,20 @@ def source_hash(kernel: str) -> str | None:
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, workload: str, algorithmic_per_launch: float):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel sources.  An entry may instead give the
-    traffic/algorithmic ratio measured on a smaller case of the same kernel
-    (`scaled_from`), applied to this workload's algorithmic bytes."""
+def traffic_for(kernel: str, key: str, algorithmic_per_launch: float):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries, if
+    they were taken on the current kernel sources: the traffic/algorithmic
+    ratio measured on one launch (entry `key`, e.g. the cache bit width),
+    applied to this launch's algorithmic bytes."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    e = t.get(kernel, {}).get(workload)
+    e = t.get(kernel, {}).get(key)
     if not e or e.get("source_hash") is None or e.get("source_hash") != source_hash(kernel):
         return None
-    if e.get("dram_bytes_per_launch") is not None:
-        return float(e["dram_bytes_per_launch"])
     if e.get("traffic_over_algorithmic") is not None:
         return float(e["traffic_over_algorithmic"]) * algorithmic_per_launch
     return None
@@ -260,8 +258,12 @@ def build_workload(name: str, rank: int, device):
                                 "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64",
                     "n_seqs": wl.n_seqs, "layers": 42, "kv_donor_layers": 24}}
         return case, calls, info
-    if name in ("tiny", "sliding16", "full32k"):
-        wl = W.WORKLOADS[name]()
+    if name in ("tiny", "sliding16", "full32k", "full32k-8bit"):
+        if name == "full32k-8bit":          # the full32k shape with 8-bit caches
+            base = W.workload_full_keqv_decode()
+            wl = W.DecodeWorkload(base.name + "-8bit", base.seed, base.layer, base.filled, [8] * base.n_seqs)
+        else:
+            wl = W.WORKLOADS[name]()
         case = harness.DecodeCase(wl, device=device, out_f32=False)
         spec = wl.layer
         by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
@@ -316,25 +318,24 @@ def step_calls(calls, stream=None):
         c.attend(stream)
 
 
-def run_gpu(args):
+def call_bytes(c) -> int:
+    """Algorithmic KV bytes one attention call of a DecodeCase reads."""
+    spec = c.spec
+    return sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
+               for p, b in zip(c.wl.filled, c.wl.bits)) * spec.n_kv_heads
+
+
+def measure(workload, case, calls, info, K, warmup, device, world, with_breakdown=True):
+    """Warm-up, then K steps captured in one CUDA graph and replayed once
+    between CUDA events.  Events captured around each attention call of the
+    dominant kernel give its duration.  Returns a dict of timings."""
     import torch
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist_init(world, "nccl")
-    case, calls, info = build_workload(args.workload, rank, device)
+    for _ in range(warmup):
+        step_calls(calls)                      # eager (first calls also set kernel attributes)
     torch.cuda.synchronize()
-
-    # warm-up, eager (first calls also set kernel attributes)
-    for _ in range(args.warmup):
-        step_calls(calls)
-    torch.cuda.synchronize()
-
-    # capture K steps into one graph, with timing events around each attention
-    # call of the dominant kernel
     stream = torch.cuda.Stream(device=device)
-    K = args.steps
-    full_calls = [c for _, c in calls if c.spec.window == 0] if args.workload == "stack42" else [c for _, c in calls]
+    full_calls = [c for _, c in calls if c.spec.window == 0] if workload == "stack42" else [c for _, c in calls]
+
     def ev_pair():
         return (torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True))
@@ -346,11 +347,11 @@ def run_gpu(args):
         have_inner = True
     except TypeError:
         ev, ev_app, ev_oth, have_inner = None, None, None, False
-    graph = torch.cuda.CUDAGraph()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         step_calls(calls)                      # one more warm-up on the capture stream
     torch.cuda.synchronize()
+
     def capture(g, all_events):
         # all_events: time every call (the events break the launch overlap
         # between calls, so that graph is replayed apart from the timed one)
@@ -377,12 +378,12 @@ def run_gpu(args):
                         else:
                             jo += 1
         torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
     capture(graph, False)
-
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     replay_stream = torch.cuda.current_stream()     # graph.replay() launches here
-    with ClockSampler(local) as clk:
+    with ClockSampler(device.index) as clk:
         dist_barrier(world, device)
         torch.cuda.synchronize()
         t0.record(replay_stream)
@@ -390,8 +391,13 @@ def run_gpu(args):
         t1.record(replay_stream)
         torch.cuda.synchronize()
         dist_barrier(world, device)
-    value, ms_step = whole_job_rate(info["tokens"], t0.elapsed_time(t1), K, world, device)
-    serial_ms = None
+    res = {"ms_total": t0.elapsed_time(t1), "clocks": clk.summary(), "full_calls": full_calls}
+    if have_inner:
+        res["dom_ms"] = sum(x.elapsed_time(y) for row in ev for x, y in row) / K
+        # per dominant call (the same call in every step), for splits by bit width
+        res["dom_call_ms"] = [sum(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)) / K
+                              for j in range(len(full_calls))]
+    del graph
     if info.get("mixed"):
         # the same steps with every group as its own call on one stream
         # (with the same timing events around the attention calls as the
@@ -413,46 +419,107 @@ def run_gpu(args):
         g_ser.replay()
         a1.record(replay_stream)
         torch.cuda.synchronize()
-        serial_ms = a0.elapsed_time(a1) / K
+        res["serial_ms"] = a0.elapsed_time(a1) / K
         del g_ser
-
-    # dominant-kernel duration from the events inside the graph
-    dom_ms = None
-    breakdown = None
-    if have_inner:
-        dom_ms = sum(a.elapsed_time(b) for row in ev for a, b in row) / K
+    if have_inner and with_breakdown:
         # per-call breakdown from a separate replay with events around every call
         graph_bd = torch.cuda.CUDAGraph()
         capture(graph_bd, True)
         graph_bd.replay()
         torch.cuda.synchronize()
-        breakdown = {"dominant_calls_ms": sum(a.elapsed_time(b) for row in ev for a, b in row) / K,
-                     "other_attention_calls_ms": sum(a.elapsed_time(b) for row in ev_oth for a, b in row) / K,
-                     "append_calls_ms": sum(a.elapsed_time(b) for row in ev_app for a, b in row) / K}
+        res["breakdown"] = {"dominant_calls_ms": sum(x.elapsed_time(y) for row in ev for x, y in row) / K,
+                            "other_attention_calls_ms": sum(x.elapsed_time(y) for row in ev_oth for x, y in row) / K,
+                            "append_calls_ms": sum(x.elapsed_time(y) for row in ev_app for x, y in row) / K}
         del graph_bd
-    status_ok = all(all(w == 0 for w in (c.status_words() if hasattr(c, "status_words") else [c.status_word()]))
-                    for _, c in calls)
+    res["status_ok"] = all(all(w == 0 for w in (c.status_words() if hasattr(c, "status_words")
+                                                 else [c.status_word()])) for _, c in calls)
+    return res
+
+
+def roofline(workload, info, res, peaks):
+    """The dominant kernel's roofline object from the events inside the graph."""
+    dom_ms = res.get("dom_ms")
+    if not dom_ms:
+        return None
+    n_calls = max(1, len(res["full_calls"]))
+    if workload == "prefill":
+        achieved = info["flops"] / (dom_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": peaks["source"] + " bf16 burst (f16 runs at the bf16 rate)",
+                "kernel": info["dominant"], "launch_ms": dom_ms / n_calls}
+    achieved = info["dominant_bytes"] / (dom_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "frac_of_nominal_8000": achieved / 8000.0,
+            "traffic": None, "peak_source": peaks["source"], "kernel": info["dominant"],
+            "launch_ms": dom_ms / n_calls}
+    # DRAM traffic per launch from the committed ncu summaries, keyed by the
+    # kernel's sources and the cache bit width (weighted by each call's bytes)
+    calls = res["full_calls"]
+    if "512" in info["dominant"] and all(hasattr(c, "wl") for c in calls):
+        tr = 0.0
+        for c in calls:
+            t = traffic_for("decode_kernel_512", f"{c.wl.bits[0]}bit", call_bytes(c))
+            if t is None:
+                tr = None
+                break
+            tr += t
+        roof["traffic"] = None if tr is None else tr / n_calls
+    return roof
+
+
+def bit_split(res, peaks):
+    """The dominant calls' bytes, time and HBM fraction per cache bit width."""
+    out = {}
+    for c, ms in zip(res["full_calls"], res.get("dom_call_ms", [])):
+        b = c.wl.bits[0]
+        o = out.setdefault(f"{b}bit", {"calls": 0, "bytes": 0, "ms": 0.0})
+        o["calls"] += 1
+        o["bytes"] += call_bytes(c)
+        o["ms"] += ms
+    for o in out.values():
+        o["achieved_gbs"] = o["bytes"] / (o["ms"] / 1e3) / 1e9
+        o["frac"] = o["achieved_gbs"] / peaks["hbm_gbs"]
+        o["ms_per_call"] = o["ms"] / o["calls"]
+    return out
+
+
+def sub_result(name, K, warmup, device, peaks):
+    """One more workload timed in the same run (CUDA events on a graph of K
+    steps): its own rate and its dominant kernel's roofline."""
+    import torch
+    case, calls, info = build_workload(name, 0, device)
+    torch.cuda.synchronize()
+    res = measure(name, case, calls, info, K, warmup, device, 1, with_breakdown=False)
+    ms_step = res["ms_total"] / K
+    out = {"metric": METRIC.get(name, "decode-attention tokens/s"), "value": info["tokens"] / (ms_step / 1e3),
+           "unit": "tokens/s", "ms_per_step": ms_step, "workload": info["config"]["workload"],
+           "roofline": roofline(name, info, res, peaks), "device_status_clean": res["status_ok"],
+           "clocks": res["clocks"]}
+    if info["kv_bytes"]:
+        out["kv_bytes_per_step"] = info["kv_bytes"]
+    del case, calls
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    case, calls, info = build_workload(args.workload, rank, device)
+    torch.cuda.synchronize()
+    K = args.steps
+    res = measure(args.workload, case, calls, info, K, args.warmup, device, world)
+    value, ms_step = whole_job_rate(info["tokens"], res["ms_total"], K, world, device)
 
     # e2e through the binding with host buffers
     e2e = run_e2e(calls, K, device, info, world)
 
     peaks = load_peaks()
-    roof = None
-    if args.workload == "prefill":
-        if dom_ms:
-            achieved = info["flops"] / (dom_ms / 1e3) / 1e12
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                    "peak_source": peaks["source"] + " bf16 burst (f16 runs at the bf16 rate)",
-                    "kernel": info["dominant"]}
-    elif dom_ms:
-        achieved = info["dominant_bytes"] / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"],
-                "traffic": traffic_for("decode_kernel_512" if "512" in info["dominant"] else info["dominant"],
-                                       args.workload, info["dominant_bytes"] / max(1, len(full_calls))),
-                "peak_source": peaks["source"], "kernel": info["dominant"],
-                "launch_ms": dom_ms / max(1, len(full_calls))}
+    roof = roofline(args.workload, info, res, peaks)
     step_gbs = info["kv_bytes"] / (ms_step / 1e3) / 1e9 if info["kv_bytes"] else None
 
     cpu = None
@@ -463,18 +530,27 @@ def run_gpu(args):
     cfg.update({"l2": "inputs larger than L2" if info["kv_bytes"] > 129e6 else
                 "inputs smaller than L2 (launch-bound case)",
                 "kv_bytes_per_step": info["kv_bytes"], "step_kv_gbs": step_gbs,
-                "graph": f"{K} steps captured in one CUDA graph", "device_status_clean": status_ok})
-    if serial_ms is not None:
-        cfg["separate_calls_ms_per_step"] = serial_ms
-    if breakdown:
-        cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in breakdown.items()}
+                "graph": f"{K} steps captured in one CUDA graph", "device_status_clean": res["status_ok"],
+                "compute": "packed 4/8-bit codes; f16 tensor-core operands (codes exact), fp32 accumulation"})
+    if res.get("serial_ms") is not None:
+        cfg["separate_calls_ms_per_step"] = res["serial_ms"]
+    if res.get("breakdown"):
+        cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in res["breakdown"].items()}
         cfg["step_breakdown_note"] = "separate replay with events around every call (they slow it down)"
+    if args.workload == "stack42" and res.get("dom_call_ms"):
+        cfg["dominant_by_bits"] = bit_split(res, peaks)
+    del case, calls
+    if args.workload == "stack42" and world == 1 and not args.no_sub_results:
+        # the long-context and tensor-core workloads, timed in the same run
+        torch.cuda.empty_cache()
+        cfg["sub_results"] = {name: sub_result(name, K, args.warmup, device, peaks)
+                              for name in ("full32k", "prefill")}
     line = {"metric": METRIC.get(args.workload, "decode-attention tokens/s"),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16", "data": "synthetic (seeded N(0,1) bf16 inputs, norm weights 1+N(0,0.1))",
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 inputs, norm weights 1+N(0,0.1))",
             "config": cfg, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": info["launches"] * K, "clocks": clk.summary()}
+            "gpu_launches": info["launches"] * K, "clocks": res["clocks"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -581,22 +657,34 @@ def run_e2e(calls, K, device, info, world):
 # the CPU oracle (reference arm and cpu_baseline)
 # ----------------------------------------------------------------------------
 
-CPU_SAMPLE_SEQS = 2
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def run_cpu_baseline(workload: str, steps: int, warmup: int):
+    """The oracle as it stands on the host cores: one single-threaded worker
+    process per core, one sampled sequence per worker (sequences spread over
+    the workload's length distribution)."""
+    cores = host_cores()
+    n_all = {"stack42": 64, "tiny": 1, "sliding16": 16, "full32k": 8, "full32k-8bit": 8}.get(workload, 1)
+    nseq = max(1, min(cores, n_all))
+    procs = nseq if workload in ("stack42", "tiny", "sliding16", "full32k", "full32k-8bit") else 1
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.join(ROOT, "oracle", "timing.py"), workload, str(steps), str(warmup),
-           str(CPU_SAMPLE_SEQS)]
+           str(nseq), str(procs)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT, timeout=1800)
     if r.returncode != 0:
         return {"error": r.stderr[-500:]}
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": res["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": res["sample"], "ms_per_step": res["ms_per_step"]}
+    return {"value": res["tokens_per_s"], "unit": "tokens/s", "cores": res.get("procs", 1), "kind": "oracle",
+            "sample": res["sample"], "ms_per_step": res["ms_per_step"], "host_cores": cores,
+            "cpu_model": res.get("cpu_model")}
 
 
 def run_reference(args):
@@ -622,9 +710,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
-                    choices=["stack42", "tiny", "sliding16", "full32k", "prefill", "mixed"])
+                    choices=["stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "prefill", "mixed"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-results", action="store_true",
+                    help="stack42 only: skip timing full32k and prefill in the same run")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -71,6 +71,13 @@ typedef enum {
   KVQ_EWORKSPACE = 4     /* workspace smaller than the matching *_workspace_bytes() */
 } kvq_status;
 
+/* Bits of the device status word an attention call leaves in the first 4
+ * bytes of its workspace (attn_decode_static: read with kvq_static_status).
+ * Errors found while the kernels run cannot be returned by the (asynchronous)
+ * call itself; the kernels record them here instead and finish. */
+#define KVQ_STATUS_WAIT_TIMEOUT 0x2u  /* a bounded wait on a copy gave up (outputs of that work are not valid) */
+#define KVQ_STATUS_SEQ_SKIPPED 0x4u   /* a sequence with an invalid descriptor was skipped (its outputs are NaN) */
+
 /* One sequence's cache of one layer.  An array of these lives in DEVICE
  * memory (kernels read the pointers from it). */
 typedef struct {
@@ -152,8 +159,8 @@ kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, in
  *   out         device [n_seqs][n_q_heads][head_dim], fp32 if out_is_f32 else bf16
  *   q_prepped   NULL, or device bf16 [n_seqs][n_q_heads][head_dim] receiving q_hat
  *   workspace   device scratch of at least attn_decode_workspace_bytes(...) bytes;
- *               its first 4 bytes receive a device status word (0 = clean;
- *               bit 1: a bounded wait gave up; bit 2: a sequence was skipped)
+ *               its first 4 bytes receive a device status word (0 = clean,
+ *               else KVQ_STATUS_WAIT_TIMEOUT / KVQ_STATUS_SEQ_SKIPPED bits)
  */
 kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
                        const int32_t* pos, int32_t max_pos,
@@ -261,12 +268,29 @@ kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int3
  *     status word at its start is cleared by each call).  Calls whose work
  *     overlaps on the GPU (different streams, or different host threads on
  *     one device) race on it: serialise them.
+ *   - The device status word of the call (see KVQ_STATUS_*) stays in the
+ *     array until the next call on the device; kvq_static_status copies it out.
  */
 #define KVQ_STATIC_SCRATCH_BYTES (16u << 20)
 kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
                               const int32_t* pos, int32_t max_pos,
                               const uint16_t* q_raw, const uint16_t* q_norm_w,
                               void* out, int32_t out_is_f32, uint16_t* q_prepped, void* stream);
+
+/*
+ * kvq_static_status -- the device status word of the latest attn_decode_static
+ * call on the current device (0 = clean, else KVQ_STATUS_* bits), for the same
+ * callers: they have no workspace to read it from.  The pages have no
+ * counterpart of this call.
+ *
+ *   status   host or device memory for one uint32 (4-byte aligned).  The copy
+ *            is enqueued on `stream`, after the work enqueued there before; read
+ *            *status once the stream has synchronized (with pageable host
+ *            memory the call itself returns after the copy).  It allocates
+ *            nothing and, like attn_decode_static, races with static calls
+ *            whose work overlaps it on the GPU.
+ */
+kvq_status kvq_static_status(uint32_t* status, void* stream);
 
 /*
  * kvq_selftest_wait_timeout -- exercises the failure detection of the

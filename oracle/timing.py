@@ -1,15 +1,18 @@
 """Times the float64 oracle, as it stands, on a bounded sample of a workload.
 
 TEST INFRASTRUCTURE: run only by bench.py (its CPU baseline and its reference
-arm), in a fresh single-threaded process.
+arm), in a fresh process.
 
-    python oracle/timing.py WORKLOAD STEPS WARMUP NSEQ
+    python oracle/timing.py WORKLOAD STEPS WARMUP NSEQ [PROCS]
 
-Builds the oracle's caches for NSEQ seeded-sampled sequences of the workload
-(untimed), then times STEPS decode steps after WARMUP untimed ones.  A step is
-what the GPU step does for those sequences: for the 42-layer stack, every
-donor layer appends the new token and attends, every KV-shared layer attends
-its donor's cache.  Prints one JSON line.
+Builds the oracle's caches for NSEQ sequences of the workload (untimed),
+spread over its length distribution, then times STEPS decode steps after
+WARMUP untimed ones.  A step is what the GPU step does for those sequences:
+for the 42-layer stack, every donor layer appends the new token and attends,
+every KV-shared layer attends its donor's cache.  With PROCS > 1 the sampled
+sequences are dealt to PROCS single-threaded worker processes (one per host
+core) that start their timed steps together; the step time is the slowest
+worker's.  Prints one JSON line.
 """
 from __future__ import annotations
 
@@ -75,11 +78,24 @@ class Sharer:
         return O.attend_cache(q_hat, self.p, spec.window, spec.n_kv_heads, c.k_hat, c.v_hat)
 
 
-def build(workload: str, nseq: int):
-    """(steps callable list, tokens per step, sample description)."""
+def sample_indices(lengths, n: int) -> list:
+    """n sequences spread over the length distribution: sorted by length, the
+    middle one of each of n equal slices (their mean length is close to the
+    workload's mean)."""
+    order = np.argsort(np.asarray(lengths), kind="stable")
+    n = min(n, len(order))
+    return sorted({int(order[int((i + 0.5) * len(order) / n)]) for i in range(n)})
+
+
+def build(workload: str, nseq: int, part=None):
+    """(steps callable list, tokens per step, sample description).  `part` =
+    (i, P) keeps only the i-th of P interleaved shares of the sample."""
+    def share(idx):
+        return idx if part is None else idx[part[0]::part[1]]
     if workload == "stack42":
         wl = W.workload_stack_decode()
-        idx = sorted(np.random.default_rng(7).choice(wl.n_seqs, size=nseq, replace=False).tolist())
+        idx_all = sample_indices(wl.lengths, nseq)
+        idx = share(idx_all)
         units = []
         donors = {}
         for i in range(W.N_LAYERS):
@@ -93,13 +109,20 @@ def build(workload: str, nseq: int):
                     v = wl.decode_view(i)
                     vi = W.DecodeWorkload(v.name, wl.seed, v.layer, v.filled, v.bits, layer_id=i)
                     units.append(Sharer(vi, s, donors[(d, s)]))
-        lens = [wl.lengths[s] for s in idx]
-        return units, len(idx), f"{len(idx)} of {wl.n_seqs} sequences (indices {idx}, lengths {lens}), all 42 layers"
-    if workload in ("tiny", "sliding16", "full32k"):
-        wl = W.WORKLOADS[workload]()
-        n = min(nseq, wl.n_seqs)
-        idx = sorted(np.random.default_rng(7).choice(wl.n_seqs, size=n, replace=False).tolist())
-        return [SeqLayer(wl, s) for s in idx], n, f"{n} of {wl.n_seqs} sequences (indices {idx})"
+        lens = [wl.lengths[s] for s in idx_all]
+        return units, len(idx), (f"{len(idx_all)} of {wl.n_seqs} sequences spread over the length distribution "
+                                 f"(indices {idx_all}; mean length {np.mean(lens):.0f}, workload mean "
+                                 f"{np.mean(wl.lengths):.0f}), all 42 layers")
+    if workload in ("tiny", "sliding16", "full32k", "full32k-8bit"):
+        if workload == "full32k-8bit":
+            base = W.workload_full_keqv_decode()
+            wl = W.DecodeWorkload(base.name + "-8bit", base.seed, base.layer, base.filled, [8] * base.n_seqs)
+        else:
+            wl = W.WORKLOADS[workload]()
+        idx_all = sample_indices(wl.filled, nseq)
+        idx = share(idx_all)
+        return ([SeqLayer(wl, s) for s in idx], len(idx),
+                f"{len(idx_all)} of {wl.n_seqs} sequences (indices {idx_all})")
     if workload == "prefill":
         wl = W.workload_prefill_chunk()
         s = 0
@@ -134,19 +157,59 @@ def build(workload: str, nseq: int):
     raise SystemExit(f"unknown workload {workload}")
 
 
-def main():
-    workload, steps, warmup, nseq = sys.argv[1], int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4])
-    units, tokens, sample = build(workload, nseq)
+def run_steps(units, steps, warmup, barrier=None) -> float:
+    """Seconds per timed step (after `warmup` untimed ones)."""
     for _ in range(warmup):
         for u in units:
             u.decode()
+    if barrier is not None:
+        barrier.wait()
     t0 = time.perf_counter()
     for _ in range(max(1, steps)):
         for u in units:
             u.decode()
-    dt = (time.perf_counter() - t0) / max(1, steps)
+    return (time.perf_counter() - t0) / max(1, steps)
+
+
+def _worker(workload, nseq, part, steps, warmup, barrier, results):
+    units, tokens, sample = build(workload, nseq, part)
+    results.put((part[0], tokens, sample, run_steps(units, steps, warmup, barrier)))
+
+
+def cpu_model() -> str:
+    try:
+        out = os.popen("lscpu 2>/dev/null").read()
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def main():
+    workload, steps, warmup, nseq = sys.argv[1], int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4])
+    procs = int(sys.argv[5]) if len(sys.argv) > 5 else 1
+    if procs <= 1:
+        units, tokens, sample = build(workload, nseq)
+        dt = run_steps(units, steps, warmup)
+    else:
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        barrier, results = ctx.Barrier(procs), ctx.Queue()
+        ws = [ctx.Process(target=_worker, args=(workload, nseq, (i, procs), steps, warmup, barrier, results))
+              for i in range(procs)]
+        for w in ws:
+            w.start()
+        got = [results.get() for _ in ws]
+        for w in ws:
+            w.join()
+        tokens = sum(g[1] for g in got)
+        sample = got[0][2]
+        dt = max(g[3] for g in got)          # the workers ran their steps side by side
     print(json.dumps({"tokens_per_s": tokens / dt, "ms_per_step": dt * 1e3, "sample": sample,
-                      "tokens_per_step": tokens}))
+                      "tokens_per_step": tokens, "procs": procs, "cpu_model": cpu_model()}))
 
 
 if __name__ == "__main__":

@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libkvq.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kvq.h")
 
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECUDA, KVQ_EWORKSPACE = range(5)
+# bits of the device status word left in the first 4 bytes of a workspace
+KVQ_STATUS_WAIT_TIMEOUT, KVQ_STATUS_SEQ_SKIPPED = 0x2, 0x4
 
 
 class KvqLayer(ctypes.Structure):
@@ -74,6 +76,8 @@ def _load():
     lib.attn_prefill_workspace_bytes.restype = sz
     lib.attn_mixed.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
     lib.attn_mixed.restype = ctypes.c_int
+    lib.kvq_static_status.argtypes = [vp, vp]
+    lib.kvq_static_status.restype = ctypes.c_int
     lib.kvq_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.kvq_selftest_wait_timeout.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -157,6 +161,17 @@ def attn_decode_static(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_nor
 
 
 KVQ_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def kvq_static_status(status, stream=None):
+    """Copy the device status word of the latest attn_decode_static call into
+    `status` (one uint32 of host or device memory: a numpy array, a torch
+    tensor or an address); read it after the stream synchronizes."""
+    if hasattr(status, "ctypes") and hasattr(status, "dtype"):          # numpy array
+        addr = status.ctypes.data
+    else:
+        addr = _ptr(status)
+    _check(lib.kvq_static_status(addr, _stream(stream)))
 
 
 def attn_decode_workspace_bytes(layer: KvqLayer, n_seqs, max_pos) -> int:

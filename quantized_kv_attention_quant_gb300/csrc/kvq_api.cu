@@ -1,5 +1,6 @@
 // C ABI of libkvq.so: argument checks, rotary frequency tables, launches.
 // The operations and their page citations are documented in include/kvq.h.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -59,16 +60,18 @@ const kvq::RopeFreqs& rope_freqs(double theta, int D, int R) {
   return cache.emplace(key, f).first->second;
 }
 
+// SM count of the current device, looked up once per device (atomics: host
+// threads may make their first call on a device at the same time).
 int num_sms_current() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_release);
   }
-  return cached[dev];
+  return n;
 }
 
 kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
@@ -471,6 +474,14 @@ kvq_status attn_decode_static(const kvq_layer* layer, const kvq_seq_cache* seqs,
   if (!scratch) return KVQ_ECUDA;
   return attention_common(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, 0, q_raw, q_norm_w, out,
                           out_is_f32, q_prepped, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
+}
+
+kvq_status kvq_static_status(uint32_t* status, void* stream) {
+  if (!status || !aligned(status, 4)) return fail(KVQ_EINVAL, "status is NULL or not 4-byte aligned");
+  const cudaError_t e = cudaMemcpyFromSymbolAsync(status, g_static_scratch, sizeof(uint32_t), 0, cudaMemcpyDefault,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_static_status copy");
+  return KVQ_OK;
 }
 
 kvq_status kvq_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, void* stream) {

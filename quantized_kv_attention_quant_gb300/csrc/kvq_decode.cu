@@ -33,6 +33,8 @@
 #include "kvq_qprep.cuh"
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 namespace kvq {
 
@@ -905,16 +907,22 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
                 "the stream-K plan leaves two stages");
   cudaError_t e;
   const int smem = decode_smem_bytes<D>();
-  static bool attr_set[64] = {};
+  // the shared-memory opt-in, once per device (a lock: host threads may make
+  // their first call on a device at the same time)
+  static std::atomic<bool> attr_set[64];
+  static std::mutex attr_mu;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr_set[dev].store(true, std::memory_order_release);
+    }
   }
   int hpb = 1, nblk = 1;
   qprep_shape<D>(a.L.n_q, hpb, nblk);

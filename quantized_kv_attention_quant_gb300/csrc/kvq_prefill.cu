@@ -34,6 +34,8 @@
 #include "kvq_tc.cuh"
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 namespace kvq {
 
@@ -481,18 +483,24 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
   cudaError_t e;
   constexpr int smem = Pf<D>::BYTES;
   static_assert(smem <= 227 * 1024, "shared memory");
-  static bool attr_set[64] = {};
+  // the shared-memory opt-in, once per device (a lock: host threads may make
+  // their first call on a device at the same time)
+  static std::atomic<bool> attr_set[64];
+  static std::mutex attr_mu;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    // at most 512 / (2 D) CTAs may share an SM's tensor memory: ask for enough
-    // shared memory that no more fit
-    const int per_sm = 512 / Pf<D>::TMEM_COLS;
-    const int want = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+      // at most 512 / (2 D) CTAs may share an SM's tensor memory: ask for
+      // enough shared memory that no more fit
+      const int per_sm = 512 / Pf<D>::TMEM_COLS;
+      const int want = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);
+      e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+      if (e != cudaSuccess) return e;
+      attr_set[dev].store(true, std::memory_order_release);
+    }
   }
   const int per_sm = 512 / Pf<D>::TMEM_COLS;
   const int launch_smem = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);

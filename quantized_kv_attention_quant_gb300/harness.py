@@ -104,7 +104,7 @@ class DecodeCase:
     new token's K/V row, then attends with one query token."""
 
     def __init__(self, wl: W.DecodeWorkload, device="cuda", keep_prepped=False, out_f32=True,
-                 caches: LayerCaches | None = None, fill=True):
+                 caches: LayerCaches | None = None, fill=True, keep_fill=None):
         self.wl, self.spec, self.device = wl, wl.layer, device
         spec, n = wl.layer, wl.n_seqs
         self.lay = kvq_layer(spec)
@@ -120,7 +120,8 @@ class DecodeCase:
         self.fill_prepped = {}
         if fill:
             self.fill_prepped = fill_caches(self.caches, spec, wl.seed, wl.layer_id, wl.cached_positions,
-                                            self.k_w, device, keep_prepped=keep_prepped)
+                                            self.k_w, device,
+                                            keep_prepped=keep_prepped if keep_fill is None else keep_fill)
         self.pos = dev_i32(wl.filled, device)
         self.offs = dev_i32(np.arange(n + 1), device)
         self.max_pos = int(max(wl.filled))
@@ -266,22 +267,27 @@ class MixedCase:
 
 class StackCase:
     """Decode step over the 42-layer stack (StackWorkload): donors 0..23 append
-    and attend their own caches; layers 24..41 attend their donor's cache."""
+    and attend their own caches; layers 24..41 attend their donor's cache.
 
-    def __init__(self, wl: W.StackWorkload, device="cuda", out_f32=True):
+    Layers listed in `inspect` also write their prepped q rows and their new
+    K/V rows (not the cached rows of the fill) for comparison."""
+
+    def __init__(self, wl: W.StackWorkload, device="cuda", out_f32=True, inspect=()):
         self.wl = wl
         self.layers = []
         self.donor_case = {}
         for i in range(W.N_LAYERS):
             d = W.stack_cache_layer(i)
             view = wl.decode_view(i)
+            keep = i in inspect
             if i < W.N_DONORS:
-                case = DecodeCase(view, device, out_f32=out_f32)
+                case = DecodeCase(view, device, out_f32=out_f32, keep_prepped=keep, keep_fill=False)
                 self.donor_case[i] = case
             else:
                 # a sharer: its own q inputs, the donor's caches, no append
                 sv = W.DecodeWorkload(view.name, wl.seed, view.layer, view.filled, view.bits, layer_id=i)
-                case = DecodeCase(sv, device, out_f32=out_f32, caches=self.donor_case[d].caches, fill=False)
+                case = DecodeCase(sv, device, out_f32=out_f32, caches=self.donor_case[d].caches, fill=False,
+                                  keep_prepped=keep)
             self.layers.append((i, d, case))
 
     def step(self, stream=None):

@@ -25,7 +25,8 @@ static const any_fn kAll[] = {
     (any_fn)&kv_quant_append,        (any_fn)&attn_decode,
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
-    (any_fn)&attn_decode_static,     (any_fn)&kvq_selftest_wait_timeout,
+    (any_fn)&attn_decode_static,     (any_fn)&kvq_static_status,
+    (any_fn)&kvq_selftest_wait_timeout,
     (any_fn)&kvq_status_string,      (any_fn)&kvq_last_error,
     (any_fn)&kvq_version,
 };
@@ -69,6 +70,8 @@ int main(void) {
   CHECK(attn_mixed(&L, NULL, KVQ_MAX_MIXED_GROUPS + 1, NULL, 1, NULL) == KVQ_EINVAL);
   CHECK(attn_decode_static(&L, NULL, 1, NULL, -1, NULL, NULL, NULL, 1, NULL, NULL) == KVQ_EINVAL);
   CHECK(kvq_selftest_wait_timeout(NULL, 1000000, NULL) == KVQ_EINVAL);
+  CHECK(kvq_static_status(NULL, NULL) == KVQ_EINVAL);
+  CHECK((KVQ_STATUS_WAIT_TIMEOUT & KVQ_STATUS_SEQ_SKIPPED) == 0);
   /* nothing to do is not an error */
   CHECK(kv_quant_append(&L, NULL, 0, NULL, NULL, 0, NULL, NULL, NULL, NULL, NULL) == KVQ_OK);
   printf("all checks passed\n");

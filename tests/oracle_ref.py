@@ -61,6 +61,24 @@ def expect_decode(wl: W.DecodeWorkload, s: int) -> SeqExpect:
     return SeqExpect(cache, pos, kh, vh, np.arange(lo, p + 1), q_hat[None], k_new[None], v_new[None], {0: out})
 
 
+def expect_shared(donor: SeqExpect, wl: W.DecodeWorkload, layer_id: int, s: int):
+    """A KV-shared layer of the stack (gemma4-e4b.ts, LAYERS and the decode
+    loop: layers 24..41 attend the cache of the last donor of their attention
+    type, with no append): its own q inputs of layer `layer_id`, prepped at the
+    sequence's position, attend the donor's cache as the donor's step `donor`
+    (an expect_decode of the donor's workload `wl`) left it.
+    Returns (q_hat [Hq, D], out [Hq, D])."""
+    spec = wl.layer
+    L = oracle_layer(spec)
+    inp = W.layer_inputs(wl.seed, layer_id, spec, wl.n_seqs, wl.n_seqs)
+    f = O.bf16_to_f64
+    p = wl.filled[s]
+    q_hat = O.prep_q(f(inp["q"][s])[None], f(inp["q_w"]), np.array([p]), L.rope_theta, L.rope_dims,
+                     L.rms_eps)[0]
+    out = O.attend_cache(q_hat, p, L.window, L.n_kv_heads, donor.cache.k_hat, donor.cache.v_hat)
+    return q_hat, out
+
+
 def expect_prefill(wl: W.PrefillWorkload, s: int, rows=None) -> SeqExpect:
     spec = wl.layer
     L, cache, pos, kh, vh = _fill(wl, spec, s, wl.bits[s])

@@ -178,6 +178,9 @@ def test_bad_selftest_arguments(m):
     assert f(P + 2, 1000000, None) == 1           # status misaligned
     assert f(P, 10, None) == 1                    # limit below 1 us
     assert f(P, 2000000000, None) == 1            # limit above 1 s
+    g = m.lib.kvq_static_status
+    assert g(None, None) == 1                     # status NULL
+    assert g(P + 2, None) == 1                    # status misaligned
 
 
 def test_plain_c_program(m, tmp_path):

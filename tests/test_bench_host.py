@@ -51,21 +51,37 @@ def test_code_only_ignores_comments_and_layout():
     assert "/* kept */ // kept" in bench._code_only(a)
 
 
-def test_traffic_only_for_the_kernel_sources_it_was_taken_on():
+def test_traffic_only_for_the_kernel_sources_it_was_taken_on(tmp_path, monkeypatch):
     h = bench.source_hash("decode_kernel_512")
     assert h is not None and bench.source_hash("no_such_kernel") is None
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         t = json.load(f)
-    e = t["decode_kernel_512"]
-    current = e["full32k"]["source_hash"] == h
-    want = e["full32k"]["dram_bytes_per_launch"] if current else None
-    assert bench.traffic_for("decode_kernel_512", "full32k", 1.0) == want
-    got = bench.traffic_for("decode_kernel_512", "stack42", 1e9)
-    if e["stack42"]["source_hash"] == h:
-        assert got == pytest.approx(e["stack42"]["traffic_over_algorithmic"] * 1e9)
-    else:
-        assert got is None
+    for key, e in t.get("decode_kernel_512", {}).items():
+        got = bench.traffic_for("decode_kernel_512", key, 1e9)
+        if e["source_hash"] == h:
+            assert got == pytest.approx(e["traffic_over_algorithmic"] * 1e9)
+        else:
+            assert got is None
+    # a planted entry: used on the current sources only, keyed by bit width
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"decode_kernel_512": {
+        "8bit": {"source_hash": h, "traffic_over_algorithmic": 1.01},
+        "4bit": {"source_hash": "0" * 16, "traffic_over_algorithmic": 1.02}}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda k: h if k == "decode_kernel_512" else None)
+    assert bench.traffic_for("decode_kernel_512", "8bit", 2e9) == pytest.approx(2.02e9)
+    assert bench.traffic_for("decode_kernel_512", "4bit", 2e9) is None
     assert bench.traffic_for("decode_kernel_512", "prefill", 1.0) is None
+
+
+def test_cpu_sample_spreads_over_lengths():
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import timing
+    lengths = list(range(1000, 65000, 1000))
+    idx = timing.sample_indices(lengths, 16)
+    assert len(idx) == 16 and idx == sorted(idx)
+    mean = sum(lengths[i] for i in idx) / 16
+    assert abs(mean - sum(lengths) / len(lengths)) < 1000
 
 
 def test_reference_arm_line():

@@ -15,7 +15,7 @@ import pytest
 import oracle as O
 import workloads as W
 from oracle_ref import (EDGE_BITS, EDGE_SPEC, attn_errors, compare_cache, edge_inputs, expect_decode,
-                        expect_edge, expect_prefill, ring_slots)
+                        expect_edge, expect_prefill, expect_shared, ring_slots)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,7 @@ def _spec(n_q, n_kv, D, window, rope_dims, theta=1e4, k_eq_v=False):
 
 
 def check_decode(harness, wl, seqs=None, check_fill=True):
-    case = harness.DecodeCase(wl, keep_prepped=True)
+    case = harness.DecodeCase(wl, keep_prepped=True, keep_fill=check_fill)
     case.step()
     torch.cuda.synchronize()
     return case, verify_decode(case, wl, seqs, check_fill)
@@ -387,6 +387,76 @@ def test_workload_full32k(kvq):
 
 def test_workload_prefill(kvq):
     check_prefill(kvq[1], W.workload_prefill_chunk(), seqs=[2], rows=[0, 1, 255, 511])
+
+
+# layers of the 42-layer step compared with the oracle: full donors with an
+# 8-bit (23) and a 4-bit (11) cache, the full sharer 41 (reads 23), the
+# sliding donor 22 and the sliding sharer 24 (reads 22)
+STACK_LAYERS = (11, 22, 23, 24, 41)
+
+
+def test_workload_stack42(kvq):
+    """The 42-layer KV-shared decode step at full size, as the bench runs it:
+    64 ragged sequences of 1,798 .. 32,737 cached tokens, donors 0..23 append
+    and attend, sharers 24..41 attend the donor's cache without appending.  The
+    full layers take the stream-K schedule over 64 rows (8-bit on donor 23 and
+    its sharers).  On sampled sequences (every one of at least 32,000 keys, the
+    shortest and the one nearest the mean length) of the listed layers: the
+    prepped q rows and the new K/V rows bit-exact, every resident cache row of
+    the donors bit-exact (codes, scales, biases), outputs within the tolerance."""
+    _, harness = kvq
+    wl = W.workload_stack_decode()
+    assert (wl.donor_bits[23], wl.donor_bits[11], wl.donor_bits[22]) == (8, 4, 8)
+    case = harness.StackCase(wl, inspect=STACK_LAYERS)
+    case.step()
+    torch.cuda.synchronize()
+    L = np.asarray(wl.lengths)
+    seqs = sorted(set(np.flatnonzero(L >= 32000).tolist())
+                  | {int(np.argmin(L)), int(np.argmin(np.abs(L - L.mean())))})
+    assert len(seqs) >= 5
+    donors = {}
+    worst = {}
+    for i in STACK_LAYERS:
+        _, d, lc = case.layers[i]
+        assert lc.status_word() == 0, f"layer {i}: status"
+        view = wl.decode_view(i)
+        out = lc.out.cpu().numpy()
+        qp = lc.q_prepped.cpu().numpy().view(np.uint16)
+        kvp = lc.kv_prepped.cpu().numpy().view(np.uint16) if i == d else None
+        for s in seqs:
+            if (d, s) not in donors:
+                donors[(d, s)] = expect_decode(view, s)
+            e = donors[(d, s)]
+            if i == d:
+                q_hat, want = e.q_hat[0], e.out[0]
+                assert np.array_equal(kvp[0, s], O.f64_to_bf16(e.k_hat[0])), f"layer {i} seq {s}: k prep"
+                assert np.array_equal(kvp[1, s], O.f64_to_bf16(e.v_hat[0])), f"layer {i} seq {s}: v prep"
+                rows = lc.caches.host_rows(s, ring_slots(e.resident, view.capacity(s)))
+                assert compare_cache(rows, e.cache, e.resident) == 0, f"layer {i} seq {s}: cache bytes"
+            else:
+                q_hat, want = expect_shared(e, view, i, s)
+            assert np.array_equal(qp[s], O.f64_to_bf16(q_hat)), f"layer {i} seq {s}: q prep"
+            mx, mean = attn_errors(out[s], want)
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, f"layer {i} seq {s}: max {mx} mean {mean}"
+            w = worst.get(i, (0.0, 0.0))
+            worst[i] = (max(w[0], mx), max(w[1], mean))
+    print("stack42 worst per layer", worst)
+
+
+def test_stream_k_64_long_8bit_rows(kvq):
+    """Stream-K over 64 rows of a head_dim-512 K = V layer with 8-bit caches,
+    eight of them at 32,000 keys or more and the rest ragged: every CTA range
+    crosses units, pieces of the long rows are merged from many CTAs.  Checked
+    on the long rows, the shortest and two others."""
+    _, harness = kvq
+    rng = np.random.default_rng(94)
+    filled = [int(x) for x in rng.integers(100, 24000, size=64)]
+    for s in (0, 9, 21, 30, 31, 47, 58, 63):
+        filled[s] = 32000 + 97 * s
+    wl = W.DecodeWorkload("sk-64-long-8bit", 94, W.FULL_KEQV, filled=filled, bits=[8] * 64)
+    seqs = [0, 9, 21, 30, 31, 47, 58, 63, int(np.argmin(filled)), 5, 40]
+    _, worst = check_decode(harness, wl, seqs=sorted(set(seqs)), check_fill=False)
+    print("sk-64-long-8bit worst", worst)
 
 
 def test_workspace_contents_do_not_matter(kvq):

@@ -29,6 +29,20 @@ def _static_call(m, case, out):
                          out, 1)
 
 
+def _static_status(m) -> int:
+    word = np.full(1, 0xFFFFFFFF, np.uint32)      # pageable host memory: the copy is done on return
+    m.kvq_static_status(word)
+    torch.cuda.synchronize()
+    return int(word[0])
+
+
+def _device_memory():
+    """(free device bytes, torch allocations so far): a cudaMalloc of the
+    library moves the first, one through torch the second."""
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0], torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+
+
 @pytest.mark.parametrize("name,spec,filled,bits", [
     ("sliding-mixed-bits", W.LayerSpec(8, 2, 256, 512, 256, 1e4, False), [700, 40, 513], [4, 8, 4]),
     ("full-keqv", W.LayerSpec(16, 1, 512, 0, 128, 1e6, True), [2000, 65, 1], [4, 8, 4]),
@@ -42,13 +56,18 @@ def test_static_scratch_matches_workspace_call(kvq, name, spec, filled, bits):
     torch.cuda.synchronize()
     ref = case.out.cpu().numpy().copy()
     assert np.all(np.isfinite(ref))
-    for _ in range(2):                      # two calls in a row share the static scratch
-        out = torch.full_like(case.out, float("nan"))
+    outs = [torch.full_like(case.out, float("nan")) for _ in range(3)]
+    _static_call(m, case, outs[2])          # first use on this device: looks up the array, loads kernels
+    assert _static_status(m) == 0
+    before = _device_memory()
+    for out in outs[:2]:                    # two calls in a row share the static scratch
         _static_call(m, case, out)
         torch.cuda.synchronize()
+        assert _static_status(m) == 0
         got = out.cpu().numpy()
         d = np.abs(got.astype(np.float64) - ref)
         assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, (d.max(), d.mean())
+    assert _device_memory() == before, "a static call allocated device memory"
 
 
 def test_static_scratch_rejects_oversized_call(kvq):
