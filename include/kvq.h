@@ -93,9 +93,9 @@ typedef struct {
 
 /* One attention layer (host memory). */
 typedef struct {
-  int32_t n_q_heads;   /* q heads; a multiple of n_kv_heads */
+  int32_t n_q_heads;   /* q heads; a multiple of n_kv_heads, at most 16 per kv head */
   int32_t n_kv_heads;  /* kv heads; q head h reads kv head h / (n_q_heads / n_kv_heads) */
-  int32_t head_dim;    /* 64, 128, 256 or 512 (64: at most 8 q heads per kv head) */
+  int32_t head_dim;    /* 64, 128, 256 or 512 */
   int32_t group_size;  /* must be 64 */
   int32_t window;      /* 0 = full causal; W > 0: a query at p sees keys p-W+1 .. p */
   int32_t rope_dims;   /* even, 0..head_dim: dims 0..rope_dims-1 are rotated in pairs

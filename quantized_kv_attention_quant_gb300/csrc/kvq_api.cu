@@ -85,11 +85,6 @@ kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
   if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 256 && L->head_dim != 512)
     return fail(KVQ_EUNSUPPORTED, "head_dim %d not in {64, 128, 256, 512}", L->head_dim);
   if (L->group_size != 64) return fail(KVQ_EUNSUPPORTED, "group_size %d != 64", L->group_size);
-  // head_dim 64 with more than 8 q heads per kv head is outside the shapes the
-  // parity tests cover (the limit dates from an earlier CTA layout); refused
-  // until it is tested
-  if (L->head_dim == 64 && G > 8)
-    return fail(KVQ_EUNSUPPORTED, "head_dim 64 supports at most 8 q heads per kv head (got %d)", G);
   if (L->window < 0) return fail(KVQ_EINVAL, "window %d < 0", L->window);
   if (L->rope_dims < 0 || L->rope_dims > L->head_dim || (L->rope_dims & 1))
     return fail(KVQ_EINVAL, "rope_dims %d must be even and in [0, head_dim]", L->rope_dims);

@@ -57,7 +57,6 @@ def _layer(m, **kw):
     (dict(n_q_heads=34, n_kv_heads=2), 2),      # ratio 17 > 16
     (dict(head_dim=96), 2),
     (dict(head_dim=1024), 2),
-    (dict(head_dim=64, rope_dims=64, n_q_heads=32, n_kv_heads=2), 2),   # ratio 16 > 8 at head_dim 64
     (dict(window=-1), 1),
     (dict(rope_dims=3), 1),
     (dict(rope_dims=512), 1),

@@ -64,6 +64,11 @@ def test_designed_edges_are_hit():
     assert (c[1], c[2]) == (254, 127)
     c, _ = _k_codes(4, "bf16-scale-divides")
     assert (c[1], c[2]) == (15, 7)
+    # a bf16-subnormal scale: 17 * 2^-133 at 4 bits, 2^-133 at 8 bits
+    c, p = _k_codes(4, "subnormal-scale")
+    assert tuple(c[:4]) == (0, 15, 6, 2) and p[1][0, 0, 0] == 0x0011
+    c, p = _k_codes(8, "subnormal-scale")
+    assert tuple(c[:4]) == (0, 255, 100, 37) and p[1][0, 0, 0] == 0x0001
 
 
 def test_every_row_attends():

@@ -80,6 +80,8 @@ DECODE_CASES = {
     "gqa1-d512-window": (_spec(2, 2, 512, 64, 512), [130, 64], [8, 4]),
     # G = 3 (not a power of two), a large eps and a single rotated pair
     "gqa3-eps-half-rope2": (W.LayerSpec(6, 2, 256, 0, 2, 1e4, False, rms_eps=0.5), [100, 7], [4, 8]),
+    # 16 q heads per kv head at head_dim 64 (one warp per CTA)
+    "d64-gqa16": (_spec(32, 2, 64, 0, 64), [200, 5, 70], [4, 8, 4]),
 }
 
 
@@ -101,6 +103,7 @@ STREAM_K_CASES = {
     "sk-ragged-d256-full": (_spec(8, 2, 256, 0, 256), [3300, 100, 2000, 3999, 63], [8, 4, 4, 8, 8]),
     "sk-equal-rows-d512": (_spec(16, 1, 512, 0, 128, 1e6, True), [3500] * 4, [4, 8, 4, 8]),
     "sk-gqa8-d128": (_spec(8, 1, 128, 0, 128), [5000, 3072, 3073, 17], [8, 4, 8, 4]),
+    "sk-gqa16-d64": (_spec(16, 1, 64, 0, 32), [4000, 3300, 20, 3100], [8, 4, 4, 8]),
 }
 
 
@@ -166,6 +169,16 @@ def test_stream_k_bad_descriptor_is_nan(kvq):
     # the other rows' tiles are split at other points now: equal up to rounding
     assert np.allclose(out[0], good[0], atol=1e-4) and np.allclose(out[2], good[2], atol=1e-4)
     assert case.status_word() & (1 << 2)
+
+
+def test_rope_frequencies_on_this_host():
+    """The frequency table both sides derive from the platform pow is the
+    nearest-double table of tests/golden/rope_freqs.txt on the machine that
+    runs the GPU tests too (its libm may differ from the one the CPU pins ran
+    on)."""
+    from test_oracle_pins import read_rope_freqs
+    for (theta, D), want in read_rope_freqs().items():
+        assert [float(x) for x in O.rope_inv_freq(theta, D, D)] == want, (theta, D)
 
 
 def test_bounded_wait_gives_up(kvq):
@@ -312,7 +325,8 @@ def test_largest_positions(kvq):
 def test_quantizer_edge_rows(kvq):
     """Hand-designed groups (an fp32-quotient midpoint, exact ties, a constant
     group, a -0 minimum, a bf16 scale that is not (max - min) / (2^b - 1), a
-    nearly constant and an all-negative group) appended as one prompt chunk
+    nearly constant and an all-negative group, a bf16-subnormal scale whose
+    float32 reciprocal overflows) appended as one prompt chunk
     into a 4-bit and an 8-bit cache: prepped rows and cache bytes bit-exact
     with the oracle, the designed codes read back from the GPU cache, then the
     prompt path (every row) and the decode path (the last row) within the
@@ -361,6 +375,10 @@ def test_quantizer_edge_rows(kvq):
         assert (c[0], c[1], c[2]) == ((0, 15, 0) if bits == 4 else (0, 254, 0))
         assert rows["k_biases"][0, names.index("negative-zero-min"), 0] == 0x0000
         assert rows["k_scales"][0, names.index("constant"), 0] == 0
+        sub = names.index("subnormal-scale")
+        c = O.unpack(rows["k_codes"][0, sub], bits)
+        assert tuple(c[:4]) == ((0, 15, 6, 2) if bits == 4 else (0, 255, 100, 37))
+        assert rows["k_scales"][0, sub, 0] == (0x0011 if bits == 4 else 0x0001)
         for t in range(n):
             mx, mean = attn_errors(got[s * n + t], e.out[t])
             assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{bits}-bit row {t} ({names[t]}): max {mx} mean {mean}"
@@ -520,6 +538,7 @@ PREFILL_TC_CASES = {
     "g2-d128-window": (_spec(4, 2, 128, 96, 64, 1e6), [200, 0], [70, 45], [4, 8]),
     "g8-d256": (_spec(8, 1, 256, 0, 256), [31, 140], [40, 17], [8, 4]),
     "g16-d128-norope": (_spec(16, 1, 128, 0, 0), [64, 5], [24, 8], [4, 8]),
+    "g16-d64-window": (_spec(32, 2, 64, 48, 64), [90, 3], [40, 11], [8, 4]),
 }
 
 

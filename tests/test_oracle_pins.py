@@ -361,6 +361,30 @@ def test_rope():
     pin_rope_large_positions(O)
 
 
+def read_rope_freqs():
+    """{(theta, head_dim): [float64 frequencies]} from tests/golden/rope_freqs.txt
+    (written by make_rope_freqs.py with mpmath at 200 bits)."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "rope_freqs.txt")
+    table = {}
+    for ln in open(path):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        theta, D, j, v = ln.split()
+        table.setdefault((float(theta), int(D)), []).append((int(j), float.fromhex(v)))
+    return {k: [v for _, v in sorted(vs)] for k, vs in table.items()}
+
+
+def test_rope_frequencies_are_the_nearest_doubles():
+    """The oracle's float64 frequencies theta^(-2j/D) (platform pow) are the
+    doubles nearest to the exact values, for every j of every rotary layout
+    the workloads use: an independent evaluation pins the pow both sides
+    call."""
+    for (theta, D), want in read_rope_freqs().items():
+        got = O.rope_inv_freq(theta, D, D)
+        assert len(want) == D // 2
+        assert [float(x) for x in got] == want, (theta, D)
+
+
 # ----------------------------------------------------------------------------
 # attention read
 # ----------------------------------------------------------------------------

@@ -340,6 +340,10 @@ EDGE_GROUPS = {
     "nearly-constant": ({63: 1.0078125}, 1.0),
     # an all-negative group
     "all-negative": ({0: -2.0, 1: -0.015625, 2: -1.0, 3: -0.75}, -0.5),
+    # a range so small that the scale is a bf16 subnormal: min 0, max 2^-125
+    # (4 bits: scale 17 * 2^-133, 8 bits: scale 2^-133); the reciprocal of
+    # such a scale overflows float32
+    "subnormal-scale": ({1: 2.0 ** -125, 2: 100 * 2.0 ** -133, 3: 37 * 2.0 ** -133}, 0.0),
 }
 
 EDGE_HEAD_DIM = 128      # one designed group followed by one balancing group
