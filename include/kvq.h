@@ -103,6 +103,19 @@ typedef struct {
   double rope_theta;   /* > 0 */
   float rms_eps;       /* >= 0; RMSNorm: x / sqrt(mean(x^2) + eps) * w */
   int32_t k_eq_v;      /* 1: V is the un-scaled RMS norm of the raw k rows (no v input) */
+  /* NULL, or DEVICE int8[head_dim] of +1 / -1: the deferred TurboQuant read
+   * (model.ts, cacheLayers comment: full-attention caches keep their values
+   * rotated through the attention and the read un-rotates the output).  The
+   * rotation R = diag(rot_signs) H, H the Sylvester Hadamard matrix of order
+   * head_dim (entries +-1, H H^T = head_dim I), is taken from outside the
+   * pages (the randomized Hadamard transform).  kv_quant_append stores
+   * bf16(k_hat R) and bf16(v_hat R); the attention calls rotate q alike
+   * (bf16(q_hat R)), score (q R)(k R)^T / head_dim and return O' R^T / head_dim
+   * for the output O' over the rotated values.  kv_prepped and q_prepped
+   * receive the rotated rows.  The same signs must be given to the append and
+   * the attention calls of a cache.  q_hat R is at most head_dim |w| in size:
+   * norm weights |w| <= 64 keep the f16 operands finite. */
+  const int8_t* rot_signs;
 } kvq_layer;
 
 /*

@@ -43,6 +43,21 @@ Readings taken where the pages are silent:
   R-zero: a group whose minimum (maximum) is a zero stores +0 as its bias;
           zeros elsewhere keep their IEEE sign.
 
+TurboQuant deferred read of the full-attention caches (model.ts, the
+`cacheLayers` comment: the values stay rotated through the fused SDPA and the
+read un-rotates the output; `deferredTurboQuantKernels`).  The pages give only
+this outline; the rotation is taken from outside them:
+  R-rot:  R = diag(s) H, H the Sylvester Hadamard matrix of order head_dim
+          (entries +-1, H H^T = D I) and s a vector of +-1 signs drawn once
+          per layer (an input, like the norm weights): the randomized Hadamard
+          transform, the fast random rotation TurboQuant-style quantizers
+          apply before quantizing.  The prepped K and V rows are rotated and
+          rounded to bf16 before the quantizer (the same affine groups), q is
+          rotated and rounded alike (a zero of a rotated row is +0), the
+          scores are (q R)(k R)^T / D = q k^T
+          up to those roundings, and the output O' of the rotated values is
+          un-rotated: O = O' R^T / D.
+
 Values are carried as float64 arrays holding bf16-representable numbers.
 """
 from __future__ import annotations
@@ -246,18 +261,19 @@ def visible_keys(p: int, window: int) -> tuple:
     return lo, p
 
 
-def attend(q_hat: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray) -> np.ndarray:
-    """Softmax attention of G query heads over n keys of one KV head, scale 1.0.
+def attend(q_hat: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, scale: float = 1.0) -> np.ndarray:
+    """Softmax attention of G query heads over n keys of one KV head, scores
+    times `scale` (1.0: the SDPA scale of the pages; 1/D on rotated rows).
 
     q_hat [G, D], k_hat [n, D], v_hat [n, D] -> [G, D], in float64."""
-    s = q_hat @ k_hat.T                                  # [G, n], scale 1.0
+    s = (q_hat @ k_hat.T) * scale                        # [G, n]
     m = s.max(axis=-1, keepdims=True)
     p = np.exp(s - m)
     return (p @ v_hat) / p.sum(axis=-1, keepdims=True)
 
 
 def attend_cache(q_hat: np.ndarray, p: int, window: int, n_kv_heads: int,
-                 k_hat_at, v_hat_at) -> np.ndarray:
+                 k_hat_at, v_hat_at, scale: float = 1.0) -> np.ndarray:
     """Output [Hq, D] of one query token at position p.
 
     `k_hat_at(lo, hi)` / `v_hat_at(lo, hi)` return dequantized rows
@@ -270,8 +286,36 @@ def attend_cache(q_hat: np.ndarray, p: int, window: int, n_kv_heads: int,
     V = v_hat_at(lo, hi)
     out = np.empty((Hq, D), dtype=np.float64)
     for kvh in range(n_kv_heads):
-        out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh * G:(kvh + 1) * G], K[:, kvh], V[:, kvh])
+        out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh * G:(kvh + 1) * G], K[:, kvh], V[:, kvh], scale)
     return out
+
+
+# ----------------------------------------------------------------------------
+# the rotation of the deferred TurboQuant read (reading R-rot)
+# ----------------------------------------------------------------------------
+
+def hadamard(n: int) -> np.ndarray:
+    """Sylvester's Hadamard matrix of order n (a power of two): H_1 = [1],
+    H_2m = [[H_m, H_m], [H_m, -H_m]]; entries +-1 and H H^T = n I."""
+    if n < 1 or n & (n - 1):
+        raise ValueError("order must be a power of two")
+    H = np.ones((1, 1))
+    while H.shape[0] < n:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def rotate(x: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """x R = (x * s) H over the last axis (R = diag(s) H), in float64."""
+    s = np.asarray(signs, dtype=np.float64)
+    return (np.asarray(x, dtype=np.float64) * s) @ hadamard(s.shape[0])
+
+
+def unrotate(y: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """y R^T / D = ((y H^T) * s) / D over the last axis, the inverse of rotate."""
+    s = np.asarray(signs, dtype=np.float64)
+    D = s.shape[0]
+    return ((np.asarray(y, dtype=np.float64) @ hadamard(D).T) * s) / D
 
 
 # ----------------------------------------------------------------------------
@@ -366,35 +410,54 @@ def prep_kv(k_raw, v_raw, k_w, pos, theta, rope_dims, eps):
     return k_hat, v_hat
 
 
-def decode_step(layer, cache: OracleCache, p: int, q_raw, q_w, k_raw, v_raw, k_w):
+def rotate_rows(x: np.ndarray, signs) -> np.ndarray:
+    """Prepped bf16 rows rotated and rounded to bf16 (reading R-rot); the rows
+    themselves when there is no rotation (signs None)."""
+    return x if signs is None else rn_bf16(rotate(x, signs) + 0.0)
+
+
+def finish_read(out: np.ndarray, signs) -> np.ndarray:
+    """The read's output: un-rotated when the values were rotated."""
+    return out if signs is None else unrotate(out, signs)
+
+
+def decode_step(layer, cache: OracleCache, p: int, q_raw, q_w, k_raw, v_raw, k_w, signs=None):
     """One decode token of one sequence: append its K/V at position p, then
-    attend all q heads.  q_raw [Hq, D], k_raw/v_raw [Hkv, D] (bf16 values).
-    Returns (q_hat [Hq, D], k_hat, v_hat [Hkv, D], out [Hq, D])."""
+    attend all q heads.  q_raw [Hq, D], k_raw/v_raw [Hkv, D] (bf16 values);
+    signs [D] (+-1) selects the deferred TurboQuant read (None: plain).
+    Returns (q_hat [Hq, D], k_hat, v_hat [Hkv, D], out [Hq, D]); on a rotated
+    layer q_hat, k_hat and v_hat are the rotated rows."""
     pos = np.array([p])
     k_hat, v_hat = prep_kv(k_raw[None], None if v_raw is None else v_raw[None], k_w, pos,
                            layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    k_hat, v_hat = rotate_rows(k_hat, signs), rotate_rows(v_hat, signs)
     cache.append(pos, k_hat, v_hat)
-    q_hat = prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)[0]
-    out = attend_cache(q_hat, p, layer.window, layer.n_kv_heads, cache.k_hat, cache.v_hat)
-    return q_hat, k_hat[0], v_hat[0], out
+    q_hat = rotate_rows(prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps),
+                        signs)[0]
+    scale = 1.0 if signs is None else 1.0 / q_hat.shape[-1]
+    out = attend_cache(q_hat, p, layer.window, layer.n_kv_heads, cache.k_hat, cache.v_hat, scale)
+    return q_hat, k_hat[0], v_hat[0], finish_read(out, signs)
 
 
 def prefill_chunk(layer, cache: OracleCache, start: int, q_raw, q_w, k_raw, v_raw, k_w,
-                  rows=None):
+                  rows=None, signs=None):
     """A chunk of T tokens of one sequence at positions start .. start+T-1:
     append all T K/V rows, then every token attends the keys visible from its
     own position (the chunk's earlier rows included).
 
     q_raw [T, Hq, D]; `rows` optionally restricts which tokens' outputs are
-    computed.  Returns (q_hat [T, Hq, D], k_hat, v_hat, {t: out [Hq, D]})."""
+    computed; signs as for decode_step.  Returns (q_hat [T, Hq, D], k_hat,
+    v_hat, {t: out [Hq, D]})."""
     T = q_raw.shape[0]
     pos = np.arange(start, start + T)
     k_hat, v_hat = prep_kv(k_raw, v_raw, k_w, pos, layer.rope_theta, layer.rope_dims,
                            layer.rms_eps)
+    k_hat, v_hat = rotate_rows(k_hat, signs), rotate_rows(v_hat, signs)
     cache.append(pos, k_hat, v_hat)
-    q_hat = prep_q(q_raw, q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    q_hat = rotate_rows(prep_q(q_raw, q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps), signs)
+    scale = 1.0 if signs is None else 1.0 / q_hat.shape[-1]
     outs = {}
     for t in (range(T) if rows is None else rows):
-        outs[t] = attend_cache(q_hat[t], start + t, layer.window, layer.n_kv_heads,
-                               cache.k_hat, cache.v_hat)
+        outs[t] = finish_read(attend_cache(q_hat[t], start + t, layer.window, layer.n_kv_heads,
+                                           cache.k_hat, cache.v_hat, scale), signs)
     return q_hat, k_hat, v_hat, outs

@@ -27,7 +27,7 @@ class KvqLayer(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("rope_dims", ctypes.c_int32),
                 ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_float),
-                ("k_eq_v", ctypes.c_int32)]
+                ("k_eq_v", ctypes.c_int32), ("rot_signs", ctypes.c_void_p)]
 
 
 class KvqSeqCache(ctypes.Structure):
@@ -132,9 +132,11 @@ def _check(status: int):
 
 
 def layer(n_q_heads, n_kv_heads, head_dim, window, rope_dims, rope_theta, rms_eps=1e-6,
-          k_eq_v=False, group_size=64) -> KvqLayer:
+          k_eq_v=False, group_size=64, rot_signs=None) -> KvqLayer:
+    """rot_signs: None, or the device int8 [head_dim] signs of the deferred
+    TurboQuant read (a tensor or an address; see include/kvq.h)."""
     return KvqLayer(n_q_heads, n_kv_heads, head_dim, group_size, window, rope_dims,
-                    float(rope_theta), float(rms_eps), int(bool(k_eq_v)))
+                    float(rope_theta), float(rms_eps), int(bool(k_eq_v)), _ptr(rot_signs))
 
 
 def kv_quant_append(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_rows, k_raw, v_raw,

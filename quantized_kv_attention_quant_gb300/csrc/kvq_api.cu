@@ -100,6 +100,8 @@ kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
   out->rope_dims = L->rope_dims;
   out->k_eq_v = L->k_eq_v;
   out->eps = L->rms_eps;
+  out->rot = L->rot_signs;
+  out->qk_scale = L->rot_signs ? 1.0f / (float)L->head_dim : 1.0f;
   return KVQ_OK;
 }
 
@@ -501,6 +503,6 @@ const char* kvq_status_string(kvq_status s) {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }
 
-int32_t kvq_version(void) { return 100; }
+int32_t kvq_version(void) { return 110; }
 
 }  // extern "C"

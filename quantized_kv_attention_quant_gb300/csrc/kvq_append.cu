@@ -128,6 +128,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   __shared__ float4 cs[D / 2];            // (cos.hi, cos.lo, sin.hi, sin.lo) per pair
   __shared__ __align__(16) float freq[D / 2][3];   // rotary frequency triples
   __shared__ ff red[A::IPB][A::HW];
+  extern __shared__ double rot_rows[];    // [ipb][D], rotated layers only
   const int tid = threadIdx.x, il = tid / TH, tt = tid % TH, lane = tid & 31;
   const int R = a.L.rope_dims, half = R >> 1;
   const int Hkv = a.L.n_kv;
@@ -221,6 +222,8 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
       }
     }
   }
+  // ---- the deferred TurboQuant read's rotation: bf16((y * s) H) ----
+  if (a.L.rot) rotate_row_bf16<D, E, TH>(y, a.L.rot, rot_rows + il * D, tt, active);
   if (!active) return;
 
   if (a.prepped) {
@@ -244,7 +247,8 @@ cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t 
     const int items = 2 * a.L.n_kv;
     const int ipb = items < App<D>::IPB ? items : App<D>::IPB;
     const dim3 grid((unsigned)a.n_rows, (unsigned)((items + ipb - 1) / ipb));
-    append_kernel<D><<<grid, ipb * App<D>::TH, 0, st>>>(a, f, ipb);
+    const size_t dyn = a.L.rot ? (size_t)ipb * D * sizeof(double) : 0;   // rotation rows
+    append_kernel<D><<<grid, ipb * App<D>::TH, dyn, st>>>(a, f, ipb);
   };
   switch (a.L.D) {
     case 64: go(std::integral_constant<int, 64>{}); break;

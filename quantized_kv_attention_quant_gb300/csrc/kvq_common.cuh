@@ -89,6 +89,20 @@ __device__ __forceinline__ uint16_t ff_to_bf16_rn(ff v) {
   return uint16_t(away ? top + 1 : top);
 }
 
+// Correctly rounded bf16 of a double (ties to even).  f = d truncated toward
+// zero to fp32 and r = d - f (exact, zero or of d's sign): d lies strictly
+// above f's magnitude when r != 0, so a low half of f below the midpoint
+// 0x8000 rounds down, above it up, and at it up unless r == 0 (a tie).
+__device__ __forceinline__ uint16_t d_to_bf16_rn(double d) {
+  const float f = __double2float_rz(d);
+  const double r = d - (double)f;
+  const uint32_t u = __float_as_uint(f);
+  const uint32_t low = u & 0xFFFFu;
+  uint32_t top = u >> 16;
+  if (low > 0x8000u || (low == 0x8000u && (r != 0.0 || (top & 1u)))) ++top;
+  return uint16_t(top);
+}
+
 // ----------------------------------------------------------------------------
 // RMSNorm pieces (reading: y = x / sqrt(mean(x^2) + eps) * w, rounded once)
 // ----------------------------------------------------------------------------
@@ -265,6 +279,41 @@ __device__ __forceinline__ uint16_t rot_bf16(float x, float y, ff c, ff s) {
   ff a = ff_mul_f(c, x);
   ff b = ff_mul_f(s, y);
   return ff_to_bf16_rn(ff_add(a, ff_neg(b)));
+}
+
+// ----------------------------------------------------------------------------
+// The rotation of the deferred TurboQuant read: a bf16 row y of D values
+// (E per thread, thread t of the row's TH holding elements t*E .. t*E+E-1)
+// becomes bf16((y * s) H), H the Sylvester Hadamard matrix (H_ij =
+// (-1)^popcount(i & j)): sign flip, then the in-place Walsh-Hadamard butterflies
+// (u, v) -> (u + v, u - v) at strides 1, 2, .., D/2 in float64 shared memory,
+// then one correct rounding to bf16 (a zero becomes +0).  Every thread of the
+// block calls it (block barriers inside); `active` marks threads of real rows.
+// ----------------------------------------------------------------------------
+template <int D, int E, int TH>
+__device__ __forceinline__ void rotate_row_bf16(uint16_t (&y)[E], const int8_t* signs, double* row, int t,
+                                                bool active) {
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) row[t * E + i] = (double)bf16_to_f(y[i]) * (double)__ldg(signs + t * E + i);
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int h = 1; h < D; h <<= 1) {
+    if (active) {
+      for (int p = t; p < D / 2; p += TH) {
+        const int i = (p / h) * 2 * h + (p % h);
+        const double u = row[i], v = row[i + h];
+        row[i] = u + v;
+        row[i + h] = u - v;
+      }
+    }
+    __syncthreads();
+  }
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) y[i] = d_to_bf16_rn(row[t * E + i] + 0.0);
+  }
 }
 
 // ----------------------------------------------------------------------------

@@ -100,9 +100,16 @@ __device__ __forceinline__ float bf16_word_at(const uint32_t (&w)[(NG + 1) / 2],
   return (g & 1) ? bf16hi_to_f(w[g >> 1]) : bf16lo_to_f(w[g >> 1]);
 }
 
-// log2 of the power of two the PV A operand (P * scale) is multiplied by, so
-// that it stays clear of the f16 subnormal range; divided out at the end.
-template <int BITS> struct PvPrescale { static constexpr int log2 = BITS == 4 ? 2 : 6; };
+// The power of two the PV A operand (P * scale) is multiplied by, so that it
+// stays clear of the f16 subnormal range; divided out at the end.  V rows are
+// RMS-normalised without a weight (|v| <= sqrt(D), a group's range <= 2 sqrt(D)),
+// so with P <= e^8: 2^2 at 4 bits and 2^6 at 8 bits keep P * scale * 2^k below
+// f16's 65504.  A rotated layer's values v R reach D in size (range <= 2 D):
+// 2^-2 and 2^2 there.
+template <int BITS>
+__device__ __forceinline__ float pv_prescale(bool rotated) {
+  return rotated ? (BITS == 4 ? 0.25f : 4.f) : (BITS == 4 ? 4.f : 64.f);
+}
 
 // Key mapping inside a tile (key 16c + s: chunk c < 4, slot s < 16).
 //   QK n-tile j (0..7): column n is key 16*(n & 3) + 2j + (n >> 2), so the
@@ -149,7 +156,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   constexpr int SLB = slot_bytes(D, BITS);
   constexpr uint32_t TX = 64 * RB + 2 * SB;     // bytes of one slot
   constexpr float L2E = 1.4426950408889634f;
-  constexpr float PRESCALE = float(1 << PvPrescale<BITS>::log2);
+  const float PRESCALE = pv_prescale<BITS>(a.L.rot != nullptr);
   constexpr int GB = NG < 8 ? NG : 8;           // groups whose MMA chains run interleaved
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3, rq = lane >> 2;
@@ -161,6 +168,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   uint8_t* const slots_base = stages;
   const int cap_tiles = c.capacity / kTileKeys;
   const size_t head_row0 = (size_t)kvh * c.capacity;
+  const float ksc = kTwo24 * a.L.qk_scale;      // codes' units times the score scale (a power of two)
 
   // Copies of one stage: per side 4 code chunks, the scale block and the bias
   // block; K copies by copy ids 0..5, V copies by 6..11 (copy id j is lane
@@ -333,13 +341,14 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
           T[3] = fmaf(s1, acc[u][3], T[3]);
         }
       }
-      // the code products are in units of 2^-24
+      // the code products are in units of 2^-24 (times the score scale; the
+      // bias term arrives scaled)
       const int kp0 = tpos0 + kc0, kp1 = tpos0 + kc1;
       const bool v0 = kp0 >= tr.lo && kp0 <= tr.hi, v1 = kp1 >= tr.lo && kp1 <= tr.hi;
-      S[nt][0] = v0 ? fmaf(T[0], kTwo24, Sb[0]) : -INFINITY;
-      S[nt][1] = v1 ? fmaf(T[1], kTwo24, Sb[1]) : -INFINITY;
-      S[nt][2] = v0 ? fmaf(T[2], kTwo24, Sb[2]) : -INFINITY;
-      S[nt][3] = v1 ? fmaf(T[3], kTwo24, Sb[3]) : -INFINITY;
+      S[nt][0] = v0 ? fmaf(T[0], ksc, Sb[0]) : -INFINITY;
+      S[nt][1] = v1 ? fmaf(T[1], ksc, Sb[1]) : -INFINITY;
+      S[nt][2] = v0 ? fmaf(T[2], ksc, Sb[2]) : -INFINITY;
+      S[nt][3] = v1 ? fmaf(T[3], ksc, Sb[3]) : -INFINITY;
       tmax[0] = fmaxf(tmax[0], fmaxf(S[nt][0], S[nt][1]));
       tmax[1] = fmaxf(tmax[1], fmaxf(S[nt][2], S[nt][3]));
     }
@@ -562,11 +571,26 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
       *reinterpret_cast<float4*>(po + r * D + 4 * c4) = *reinterpret_cast<const float4*>(ps + r * PS + 4 * c4);
     }
   } else {
-    // the whole row in this run: out = o / l, as the merge of one partial
+    // the whole row in this run: out = o / l, as the merge of one partial;
+    // on a rotated layer the rows are un-rotated first: o R^T / D
+    if (a.L.rot) {
+#pragma unroll 1
+      for (int h = 1; h < D; h <<= 1) {
+        for (int p = threadIdx.x; p < G * (D / 2); p += NW * 32) {
+          const int r = p / (D / 2), q = p % (D / 2);
+          const int i = r * PS + (q / h) * 2 * h + (q % h);
+          const float u = ps[i], v = ps[i + h];
+          ps[i] = u + v;
+          ps[i + h] = u - v;
+        }
+        named_bar(1, NW * 32);
+      }
+    }
     const size_t ob = ((size_t)row * a.L.n_q + (size_t)kvh * G) * D;
     for (int i = threadIdx.x; i < G * D; i += NW * 32) {
       const int r = i / D, d = i % D;
-      const float o = ps[r * PS + d] * (1.f / lfin[r]);
+      float o = ps[r * PS + d] * (1.f / lfin[r]);
+      if (a.L.rot) o *= (float)__ldg(a.L.rot + d) * a.L.qk_scale;
       if (a.out_f32) reinterpret_cast<float*>(a.out)[ob + i] = o;
       else reinterpret_cast<uint16_t*>(a.out)[ob + i] = f_to_bf16_rn(o);
     }
@@ -764,13 +788,35 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
   }
 }
 
+// The output value of dim d = threadIdx.x of a row (blockDim == D) on a
+// rotated layer: o R^T / D = s_d (o H)_d / D, H the Sylvester Hadamard matrix,
+// by in-place butterflies in `buf` (D floats of shared memory, reused: the
+// caller is done with it).  Every thread of the block calls it.
+template <int D>
+__device__ __forceinline__ float unrotate_dim(float o, const int8_t* signs, float inv_d, float* buf) {
+  const int d = threadIdx.x;
+  __syncthreads();                               // every earlier read of buf is done
+  buf[d] = o;
+  __syncthreads();
+#pragma unroll 1
+  for (int h = 1; h < D; h <<= 1) {
+    if ((d & h) == 0) {
+      const float u = buf[d], v = buf[d + h];
+      buf[d] = u + v;
+      buf[d + h] = u - v;
+    }
+    __syncthreads();
+  }
+  return buf[d] * (float)__ldg(signs + d) * inv_d;
+}
+
 // ----------------------------------------------------------------------------
 // 3. merge split partials: out = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
 // ----------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(D)
 combine_kernel(const DecodeArgs a) {
-  __shared__ float wsm[256];
+  __shared__ float wsm[D > 256 ? D : 256];   // split weights, then (rotated layers) the output row
   __shared__ float inv_l;
   pdl_wait();
   const int row = blockIdx.x, hq = blockIdx.y;
@@ -816,7 +862,8 @@ combine_kernel(const DecodeArgs a) {
   }
   for (; i < S; ++i)
     if (wsm[i] != 0.f) acc0 = fmaf(wsm[i], po[(size_t)i * 16 * D], acc0);
-  const float o = ((acc0 + acc1) + (acc2 + acc3)) * inv_l;
+  float o = ((acc0 + acc1) + (acc2 + acc3)) * inv_l;
+  if (a.L.rot) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
   const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
@@ -886,7 +933,8 @@ combine_sk_kernel(const DecodeArgs a) {
     acc1 = fmaf(wsm[i + 1], o1, acc1);
   }
   if (i < S) acc0 = fmaf(wsm[i], a.ws.part_o[(piece(i) * 16 + r) * D + d], acc0);
-  const float o = (acc0 + acc1) * inv_l;
+  float o = (acc0 + acc1) * inv_l;
+  if (a.L.rot) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
 }
@@ -926,7 +974,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   }
   int hpb = 1, nblk = 1;
   qprep_shape<D>(a.L.n_q, hpb, nblk);
-  qprep_kernel<D, false><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH), 0, st>>>(a, f, hpb);
+  qprep_kernel<D, false><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH),
+                            a.L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(a, f, hpb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   cudaLaunchAttribute attr[1];

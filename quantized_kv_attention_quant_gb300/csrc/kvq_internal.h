@@ -19,6 +19,8 @@ struct alignas(16) RopeFreqs {
 struct LayerArgs {
   int n_q, n_kv, D, G, window, rope_dims, k_eq_v;
   float eps;
+  const int8_t* rot;    // signs of the deferred TurboQuant read (device), or nullptr
+  float qk_scale;       // score scale: 1, or 1/D on a rotated layer (a power of two)
 };
 
 struct AppendArgs {

@@ -518,7 +518,9 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
 }  // namespace
 
 bool prefill_tc_supported(const LayerArgs& L) {
-  return (L.D == 64 || L.D == 128 || L.D == 256) && L.G >= 1 && L.G <= kMaxG && (kRows % L.G) == 0;
+  // (a rotated layer takes the row path, whose merge un-rotates the output)
+  return (L.D == 64 || L.D == 128 || L.D == 256) && L.G >= 1 && L.G <= kMaxG && (kRows % L.G) == 0 &&
+         L.rot == nullptr;
 }
 
 size_t prefill_tc_ws_bytes(int n_rows, const LayerArgs& L) {

@@ -87,6 +87,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   __shared__ __align__(16) float freq[D / 2][3];
   __shared__ ff red[Q::HPB][Q::HW];
   __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
+  extern __shared__ double rot_rows[];     // [hpb][D], rotated layers only
   const int row = blockIdx.x;
   const int tid = threadIdx.x, hl = tid / TH, tt = tid % TH, lane = tid & 31;
   // the first kernel of an attention call clears its status word; the later
@@ -169,6 +170,8 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
     }
   }
   __syncthreads();                         // every read of the normed rows is done
+  // the deferred TurboQuant read: q_hat R, rounded to bf16 like K and V
+  if (a.L.rot) rotate_row_bf16<D, E, TH>(y, a.L.rot, rot_rows + (hl < Q::HPB ? hl : 0) * D, tt, active);
   float gs = 0.f;
   if (active) {
 #pragma unroll
@@ -223,7 +226,8 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int g = 2 * t4 + e;
-        const float xs = g < NG ? qs[hl][g] : 0.f;
+        // the bias term meets the scores' scale (1, or 1/D exactly on a rotated layer)
+        const float xs = g < NG ? qs[hl][g] * a.L.qk_scale : 0.f;
         const float hi = __half2float(__float2half_rn(xs));
         v[e] = lo_part ? xs - hi : hi;
       }

@@ -20,9 +20,16 @@ from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_work
 from .cache import LayerCaches
 
 
-def kvq_layer(spec: W.LayerSpec):
+def kvq_layer(spec: W.LayerSpec, rot_signs=None):
+    """The library's layer descriptor; rot_signs: the device int8 signs of a
+    rotated layer (spec.kv_rotation), else None."""
     return make_layer(spec.n_q_heads, spec.n_kv_heads, spec.head_dim, spec.window, spec.rope_dims,
-                      spec.rope_theta, spec.rms_eps, spec.k_eq_v)
+                      spec.rope_theta, spec.rms_eps, spec.k_eq_v, rot_signs=rot_signs)
+
+
+def dev_signs(inp, device):
+    """The layer's rotation signs on the device (int8), or None."""
+    return None if inp.get("rot") is None else torch.from_numpy(np.ascontiguousarray(inp["rot"])).to(device)
 
 
 def dev_bits(a: np.ndarray, device) -> torch.Tensor:
@@ -48,12 +55,12 @@ def _gen_pool():
 
 
 def fill_caches(caches: LayerCaches, spec: W.LayerSpec, seed: int, layer_id: int, positions_of,
-                k_w: torch.Tensor, device, max_rows_per_call: int = 1 << 20, keep_prepped=False):
+                k_w: torch.Tensor, device, max_rows_per_call: int = 1 << 20, keep_prepped=False, lay=None):
     """Append the raw rows of every cached position of every sequence.
 
     positions_of(s) -> int array of the positions resident before the step.
     Returns {s: prepped [2, n, Hkv, D] uint16} when keep_prepped, else {}."""
-    lay = kvq_layer(spec)
+    lay = lay if lay is not None else kvq_layer(spec)
     desc_size = 56
     kept = {}
     s = 0
@@ -107,8 +114,9 @@ class DecodeCase:
                  caches: LayerCaches | None = None, fill=True, keep_fill=None):
         self.wl, self.spec, self.device = wl, wl.layer, device
         spec, n = wl.layer, wl.n_seqs
-        self.lay = kvq_layer(spec)
         inp = W.layer_inputs(wl.seed, wl.layer_id, spec, n, n)
+        self.rot = dev_signs(inp, device)
+        self.lay = kvq_layer(spec, self.rot)
         self.host_inputs = inp
         self.q_w = dev_bits(inp["q_w"], device)
         self.k_w = dev_bits(inp["k_w"], device)
@@ -121,7 +129,8 @@ class DecodeCase:
         if fill:
             self.fill_prepped = fill_caches(self.caches, spec, wl.seed, wl.layer_id, wl.cached_positions,
                                             self.k_w, device,
-                                            keep_prepped=keep_prepped if keep_fill is None else keep_fill)
+                                            keep_prepped=keep_prepped if keep_fill is None else keep_fill,
+                                            lay=self.lay)
         self.pos = dev_i32(wl.filled, device)
         self.offs = dev_i32(np.arange(n + 1), device)
         self.max_pos = int(max(wl.filled))
@@ -159,7 +168,8 @@ class PrefillCase:
     def __init__(self, wl: W.PrefillWorkload, device="cuda", keep_prepped=False, out_f32=True, fill=True):
         self.wl, self.spec, self.device = wl, wl.layer, device
         spec, n = wl.layer, wl.n_seqs
-        self.lay = kvq_layer(spec)
+        self.rot = dev_signs(W.layer_inputs(wl.seed, wl.layer_id, spec, 0, 0), device)
+        self.lay = kvq_layer(spec, self.rot)
         rows = int(sum(wl.chunk))
         self.n_rows = rows
         self.host_inputs = []
@@ -181,7 +191,7 @@ class PrefillCase:
         self.fill_prepped = {}
         if fill:
             self.fill_prepped = fill_caches(self.caches, spec, wl.seed, wl.layer_id, wl.cached_positions,
-                                            self.k_w, device, keep_prepped=keep_prepped)
+                                            self.k_w, device, keep_prepped=keep_prepped, lay=self.lay)
         self.offs = dev_i32(np.concatenate([[0], np.cumsum(wl.chunk)]), device)
         self.start = dev_i32(wl.filled, device)
         self.max_rows = int(max(wl.chunk))

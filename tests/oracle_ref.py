@@ -32,6 +32,11 @@ class SeqExpect:
     out: dict                     # row -> [Hq, D]
 
 
+def signs_of(inp):
+    """The layer's rotation signs as float64, or None (no rotation)."""
+    return None if inp.get("rot") is None else inp["rot"].astype(np.float64)
+
+
 def _fill(wl, spec, s, bits):
     L = oracle_layer(spec)
     pos = wl.cached_positions(s)
@@ -42,6 +47,7 @@ def _fill(wl, spec, s, bits):
     if len(pos):
         kh, vh = O.prep_kv(O.bf16_to_f64(k_raw), None if v_raw is None else O.bf16_to_f64(v_raw), k_w,
                            pos, L.rope_theta, L.rope_dims, L.rms_eps)
+        kh, vh = O.rotate_rows(kh, signs_of(inp)), O.rotate_rows(vh, signs_of(inp))
         cache.append(pos, kh, vh)
     else:
         kh = vh = np.zeros((0, spec.n_kv_heads, spec.head_dim))
@@ -55,7 +61,8 @@ def expect_decode(wl: W.DecodeWorkload, s: int) -> SeqExpect:
     f = O.bf16_to_f64
     p = wl.filled[s]
     q_hat, k_new, v_new, out = O.decode_step(L, cache, p, f(inp["q"][s]), f(inp["q_w"]), f(inp["k"][s]),
-                                             None if inp["v"] is None else f(inp["v"][s]), f(inp["k_w"]))
+                                             None if inp["v"] is None else f(inp["v"][s]), f(inp["k_w"]),
+                                             signs=signs_of(inp))
     cap = wl.capacity(s)
     lo = max(0, p - cap + 1)
     return SeqExpect(cache, pos, kh, vh, np.arange(lo, p + 1), q_hat[None], k_new[None], v_new[None], {0: out})
@@ -87,7 +94,7 @@ def expect_prefill(wl: W.PrefillWorkload, s: int, rows=None) -> SeqExpect:
     start = wl.filled[s]
     q_hat, k_new, v_new, outs = O.prefill_chunk(L, cache, start, f(inp["q"]), f(inp["q_w"]), f(inp["k"]),
                                                 None if inp["v"] is None else f(inp["v"]), f(inp["k_w"]),
-                                                rows=rows)
+                                                rows=rows, signs=signs_of(inp))
     cap = wl.capacity(s)
     newest = start + wl.chunk[s] - 1
     lo = max(0, newest - cap + 1)

@@ -38,7 +38,8 @@ def test_status_strings_and_version(m):
 def test_struct_layout_matches_header(m):
     assert ctypes.sizeof(m.KvqSeqCache) == 56
     assert m.KvqSeqCache.bits.offset == 48 and m.KvqSeqCache.capacity.offset == 52
-    assert m.KvqLayer.rope_theta.offset == 24 and ctypes.sizeof(m.KvqLayer) == 40
+    assert m.KvqLayer.rope_theta.offset == 24 and m.KvqLayer.rot_signs.offset == 40
+    assert ctypes.sizeof(m.KvqLayer) == 48
 
 
 GOOD = dict(n_q_heads=8, n_kv_heads=2, head_dim=256, window=512, rope_dims=256, rope_theta=1e4)

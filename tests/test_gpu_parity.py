@@ -148,6 +148,52 @@ def test_many_rows_take_fixed_chunks(kvq):
     print("many-rows worst", worst)
 
 
+# the deferred TurboQuant read (rotated K/V, q rotated, output un-rotated):
+# fixed chunks, stream-K with rows merged and rows written by one CTA, a
+# window layer and a prompt chunk (the row path), 4- and 8-bit caches
+ROT = dict(kv_rotation=True)
+ROT_DECODE_CASES = {
+    "rot-full-keqv-short": (_spec(16, 1, 512, 0, 128, 1e6, True), [0, 63, 64, 900, 2000], [4, 8, 8, 4, 8]),
+    "rot-full-keqv-stream-k": (_spec(16, 1, 512, 0, 128, 1e6, True), [3300, 20, 5000, 4100, 700, 64],
+                               [8, 4, 4, 8, 8, 4]),
+    "rot-sliding-d256": (_spec(8, 2, 256, 512, 256), [600, 40, 1500], [4, 8, 8]),
+    "rot-d64-gqa16": (_spec(32, 2, 64, 0, 64), [300, 9], [8, 4]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROT_DECODE_CASES))
+def test_rotated_decode(kvq, name):
+    """Rotated rows (q, k, v and every cached row) bit-exact, caches bit-exact,
+    outputs within the tolerance of the oracle's rotated read."""
+    _, harness = kvq
+    spec, filled, bits = ROT_DECODE_CASES[name]
+    wl = W.DecodeWorkload(name, 96, dataclasses.replace(spec, **ROT), filled=filled, bits=bits)
+    _, worst = check_decode(harness, wl)
+    print(name, "worst", worst)
+
+
+def test_rotated_prompt_chunks_and_bf16_output(kvq):
+    """Prompt chunks and verify windows on rotated layers (the row path, which
+    the merge un-rotates), and the bf16 output of a rotated read is the
+    rounded fp32 one."""
+    _, harness = kvq
+    wl = W.PrefillWorkload("rot-chunk-d512", 97, dataclasses.replace(_spec(16, 1, 512, 0, 128, 1e6, True), **ROT),
+                           filled=[130, 5], chunk=[40, 9], bits=[4, 8])
+    check_prefill(harness, wl)
+    wl = W.PrefillWorkload("rot-chunk-d256", 97, dataclasses.replace(_spec(8, 2, 256, 64, 256), **ROT),
+                           filled=[150, 0], chunk=[30, 12], bits=[8, 4])
+    check_prefill(harness, wl)
+    spec, filled, bits = ROT_DECODE_CASES["rot-full-keqv-stream-k"]
+    wl = W.DecodeWorkload("rot-bf16", 98, dataclasses.replace(spec, **ROT), filled=filled, bits=bits)
+    a = harness.DecodeCase(wl)
+    a.step()
+    b = harness.DecodeCase(wl, out_f32=False)
+    b.step()
+    torch.cuda.synchronize()
+    f32 = a.out.cpu().numpy()
+    assert np.array_equal(b.out.cpu().numpy().view(np.uint16), O.f64_to_bf16(O.rn_bf16(f32.astype(np.float64))))
+
+
 def test_stream_k_bad_descriptor_is_nan(kvq):
     """A skipped sequence inside a stream-K batch: NaN rows, status bit set,
     the other rows unaffected."""

@@ -29,10 +29,10 @@ MUTANTS = {
     "pack-big-endian": ("words |= c[..., i] << np.uint64(i * bits)",
                         "words |= c[..., per - 1 - i] << np.uint64(i * bits)"),
     "window-off-by-one": ("max(0, p - window + 1)", "max(0, p - window)"),
-    "gqa-modulo-mapping": ("out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh * G:(kvh + 1) * G], K[:, kvh], V[:, kvh])",
-                           "out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh::n_kv_heads], K[:, kvh], V[:, kvh])"),
+    "gqa-modulo-mapping": ("out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh * G:(kvh + 1) * G], K[:, kvh], V[:, kvh], scale)",
+                           "out[kvh * G:(kvh + 1) * G] = attend(q_hat[kvh::n_kv_heads], K[:, kvh], V[:, kvh], scale)"),
     "softmax-unnormalised": ("return (p @ v_hat) / p.sum(axis=-1, keepdims=True)", "return (p @ v_hat)"),
-    "sdpa-scale-rsqrt-d": ("s = q_hat @ k_hat.T ", "s = q_hat @ k_hat.T / np.sqrt(q_hat.shape[-1]) "),
+    "sdpa-scale-rsqrt-d": ("s = (q_hat @ k_hat.T) * scale", "s = (q_hat @ k_hat.T) * scale / np.sqrt(q_hat.shape[-1])"),
     "dequant-no-bias": ("x = c * np.asarray(scales)[..., None] + np.asarray(biases)[..., None]",
                         "x = c * np.asarray(scales)[..., None]"),
     "v-norm-weighted": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
@@ -57,9 +57,8 @@ MUTANTS = {
     "query-excludes-itself": ("return lo, p\n", "return lo, max(lo, p - 1)\n"),
     "window-ignores-full-layer": ("lo = 0 if window <= 0 else max(0, p - window + 1)",
                                   "lo = max(0, p - window + 1)"),
-    "prefill-not-causal": ("outs[t] = attend_cache(q_hat[t], start + t,",
-                           "outs[t] = attend_cache(q_hat[t], start + T - 1,"),
-    "decode-q-norm-uses-k-weight": ("q_hat = prep_q(q_raw[None], q_w, pos,", "q_hat = prep_q(q_raw[None], k_w, pos,"),
+    "prefill-not-causal": ("attend_cache(q_hat[t], start + t,", "attend_cache(q_hat[t], start + T - 1,"),
+    "decode-q-norm-uses-k-weight": ("prep_q(q_raw[None], q_w, pos,", "prep_q(q_raw[None], k_w, pos,"),
     "keqv-v-from-roped-k": ("v_hat = prep_v(k_raw if v_raw is None else v_raw, eps)",
                             "v_hat = prep_v(k_hat if v_raw is None else v_raw, eps)"),
     "quant-scale-truncated": ("s = rn_bf16(s32.astype(np.float64)).astype(np.float32)",
@@ -77,12 +76,30 @@ MUTANTS = {
                           "parts = [(w >> np.uint64((per - 1 - i) * bits)) & mask for i in range(per)]"),
     "attend-values-reversed": ("return (p @ v_hat) / p.sum(axis=-1, keepdims=True)",
                                "return (p @ v_hat[::-1]) / p.sum(axis=-1, keepdims=True)"),
-    "decode-attends-before-append": ("    cache.append(pos, k_hat, v_hat)\n    q_hat = prep_q(q_raw[None], q_w, pos,",
-                                     "    q_hat = prep_q(q_raw[None], q_w, pos,"),
-    "prefill-window-grows-in-chunk": ("outs[t] = attend_cache(q_hat[t], start + t, layer.window,",
-                                      "outs[t] = attend_cache(q_hat[t], start + t, layer.window + t,"),
+    "decode-attends-before-append": ("    cache.append(pos, k_hat, v_hat)\n    q_hat = rotate_rows(prep_q(q_raw[None], q_w, pos,",
+                                     "    q_hat = rotate_rows(prep_q(q_raw[None], q_w, pos,"),
+    "prefill-window-grows-in-chunk": ("attend_cache(q_hat[t], start + t, layer.window,",
+                                      "attend_cache(q_hat[t], start + t, layer.window + t,"),
     "bf16-7-bits": ("q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
                     "q = np.ldexp(np.rint(np.ldexp(x, 7 - e)), e - 7)"),
+    # the rotation of the deferred TurboQuant read
+    "rot-signs-after-hadamard": ("return (np.asarray(x, dtype=np.float64) * s) @ hadamard(s.shape[0])",
+                                 "return (np.asarray(x, dtype=np.float64) @ hadamard(s.shape[0])) * s"),
+    "rot-no-signs": ("return (np.asarray(x, dtype=np.float64) * s) @ hadamard(s.shape[0])",
+                     "return np.asarray(x, dtype=np.float64) @ hadamard(s.shape[0])"),
+    "unrot-no-divide": ("return ((np.asarray(y, dtype=np.float64) @ hadamard(D).T) * s) / D",
+                        "return (np.asarray(y, dtype=np.float64) @ hadamard(D).T) * s"),
+    "unrot-no-signs": ("return ((np.asarray(y, dtype=np.float64) @ hadamard(D).T) * s) / D",
+                       "return (np.asarray(y, dtype=np.float64) @ hadamard(D).T) / D"),
+    "hadamard-other-block-order": ("H = np.block([[H, H], [H, -H]])", "H = np.block([[H, H], [-H, H]])"),
+    "rot-score-scale-missing": ("    scale = 1.0 if signs is None else 1.0 / q_hat.shape[-1]\n    out = attend_cache(",
+                                "    scale = 1.0\n    out = attend_cache("),
+    "rot-output-not-unrotated": ("return out if signs is None else unrotate(out, signs)", "return out"),
+    "rot-rows-not-rounded": ("return x if signs is None else rn_bf16(rotate(x, signs) + 0.0)",
+                             "return x if signs is None else rotate(x, signs) + 0.0"),
+    "rot-q-not-rotated": ("    q_hat = rotate_rows(prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps),\n"
+                          "                        signs)[0]",
+                          "    q_hat = prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)[0]"),
 }
 
 PINS = [
@@ -92,6 +109,7 @@ PINS = [
     lambda o: P.pin_quant_invariants(o, 4), lambda o: P.pin_quant_invariants(o, 8),
     P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants, P.pin_rope_large_positions,
     P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,
+    P.pin_hadamard, P.pin_rotation, P.pin_rotated_attention_identity, P.pin_rotated_step,
 ]
 
 

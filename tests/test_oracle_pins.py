@@ -578,3 +578,101 @@ def test_stack_matches_e4b_layer_table():
         assert W.stack_cache_layer(i) == int(cache)
         assert int(group) == W.GROUP == 64 and int(bits) in (4, 8)
     assert sum(1 for r in rows if int(r[0]) == int(r[2])) == W.N_DONORS == 24
+
+
+# ----------------------------------------------------------------------------
+# the deferred TurboQuant read: rotation R = diag(s) H (reading R-rot)
+# ----------------------------------------------------------------------------
+
+def _signs(D, seed=3):
+    return np.where(np.random.default_rng(seed).random(D) < 0.5, -1.0, 1.0)
+
+
+def pin_hadamard(o):
+    """Sylvester's matrix: H H^T = n I exactly, symmetric, and entry (i, j) is
+    (-1)^popcount(i & j), the closed form of the construction."""
+    for k in range(10):
+        n = 2 ** k
+        H = o.hadamard(n)
+        assert H.shape == (n, n)
+        assert np.array_equal(H @ H.T, n * np.eye(n)) and np.array_equal(H, H.T)
+    H = o.hadamard(64)
+    i, j = np.meshgrid(np.arange(64), np.arange(64), indexing="ij")
+    pop = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    assert np.array_equal(H, np.where(pop % 2 == 0, 1.0, -1.0))
+    with pytest.raises(ValueError):
+        o.hadamard(48)
+
+
+def pin_rotation(o):
+    """rotate against the definition written out as loops (sign flip, then
+    sum over i of x_i s_i (-1)^popcount(i & j)) on small integers (exact in
+    float64), the exact inverse, and the norm scaled by D."""
+    rng = np.random.default_rng(11)
+    for D in (8, 64):
+        s = _signs(D, D)
+        x = rng.integers(-9, 10, size=(3, D)).astype(np.float64)
+        want = np.zeros_like(x)
+        for r in range(x.shape[0]):
+            for j in range(D):
+                want[r, j] = sum(x[r, i] * s[i] * (-1.0) ** bin(i & j).count("1") for i in range(D))
+        y = o.rotate(x, s)
+        assert np.array_equal(y, want)
+        assert np.array_equal(o.unrotate(y, s), x)
+        assert np.array_equal((y * y).sum(-1), D * (x * x).sum(-1))
+
+
+def pin_rotated_attention_identity(o):
+    """With no rounding, attention over rotated q, K, V with scores / D, then
+    un-rotated, is plain attention (R R^T = D I)."""
+    rng = np.random.default_rng(12)
+    D, n, G = 64, 10, 3
+    s = _signs(D)
+    q, K, V = rng.standard_normal((G, D)), rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    got = o.unrotate(o.attend(o.rotate(q, s), o.rotate(K, s), o.rotate(V, s), 1.0 / D), s)
+    assert np.allclose(got, o.attend(q, K, V), atol=1e-12, rtol=0)
+
+
+def pin_rotated_step(o):
+    """A decode step and a prompt chunk on a rotated 8-bit layer: the rows it
+    stores are bf16 values whose un-rotation is the plain prepped row within
+    bf16 rounding, and the outputs, like the plain layer's, are within the
+    quantization error of exact attention over the unquantized plain rows
+    (the rotation changes only which values get rounded)."""
+    rng = np.random.default_rng(13)
+    layer = W.LayerSpec(4, 1, 64, 0, 64, 1e4, False, rms_eps=1e-6)
+    D = layer.head_dim
+    s = _signs(D, 5)
+    n = 40
+    kraw = o.rn_bf16(rng.standard_normal((n + 1, 1, D)))
+    vraw = o.rn_bf16(rng.standard_normal((n + 1, 1, D)))
+    qraw = o.rn_bf16(rng.standard_normal((3, 4, D)))
+    w = o.rn_bf16(1 + 0.1 * rng.standard_normal(D))
+    pos = np.arange(n + 1)
+    prep = lambda x: o.prep_kv(x, None, w, pos[:len(x)], layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    K = prep(kraw)[0][:, 0]                                  # plain prepped rows, exact reference
+    V = o.prep_v(vraw, layer.rms_eps)[:, 0]
+    qh = o.prep_q(qraw, w, np.array([n, 20, 21]), layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    for signs in (None, s):
+        kh, vh = o.prep_kv(kraw[:n], vraw[:n], w, pos[:n], layer.rope_theta, layer.rope_dims, layer.rms_eps)
+        kr, vr = o.rotate_rows(kh, signs), o.rotate_rows(vh, signs)
+        c = o.OracleCache(1, D, 8)
+        c.append(pos[:n], kr, vr)
+        q_hat, k_new, v_new, out = o.decode_step(layer, c, n, qraw[0], w, kraw[n], vraw[n], w, signs=signs)
+        for rows in (q_hat, k_new, v_new, kr, vr):
+            assert np.array_equal(o.rn_bf16(rows), rows)
+        if signs is not None:
+            assert np.max(np.abs(o.unrotate(kr, s) - kh)) <= 2.0 ** -8 * np.max(np.abs(kr)) / np.sqrt(D) * 2
+        assert np.max(np.abs(out - o.attend(qh[0], K[:n + 1], V[:n + 1]))) < 0.1
+        c2 = o.OracleCache(1, D, 8)
+        c2.append(pos[:20], kr[:20], vr[:20])
+        chunk = o.prefill_chunk(layer, c2, 20, qraw[1:3], w, kraw[20:22], vraw[20:22], w, signs=signs)[3]
+        for t, got in chunk.items():
+            assert np.max(np.abs(got - o.attend(qh[1 + t], K[:21 + t], V[:21 + t]))) < 0.1
+
+
+def test_rotation():
+    pin_hadamard(O)
+    pin_rotation(O)
+    pin_rotated_attention_identity(O)
+    pin_rotated_step(O)

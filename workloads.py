@@ -53,7 +53,7 @@ def normal_bf16(seed: int, key: tuple, shape, loc: float = 0.0, scale: float = 1
 
 
 # stream purposes
-P_Q, P_K, P_V, P_QW, P_KW, P_CACHE_K, P_CACHE_V, P_BITS, P_LEN = range(9)
+P_Q, P_K, P_V, P_QW, P_KW, P_CACHE_K, P_CACHE_V, P_BITS, P_LEN, P_ROT = range(10)
 
 
 # ----------------------------------------------------------------------------
@@ -70,6 +70,7 @@ class LayerSpec:
     rope_theta: float
     k_eq_v: bool
     rms_eps: float = 1e-6
+    kv_rotation: bool = False      # the deferred TurboQuant read (rotated K/V, signs from the seed)
 
     @property
     def group_ratio(self) -> int:
@@ -170,7 +171,15 @@ def layer_inputs(seed: int, layer_id: int, layer: LayerSpec, n_rows_q: int, n_ro
     }
     if not layer.k_eq_v:
         out["v"] = normal_bf16(seed, (P_V, layer_id, *sk), (n_rows_kv, layer.n_kv_heads, D))
+    out["rot"] = rotation_signs(seed, layer_id, D) if layer.kv_rotation else None
     return out
+
+
+def rotation_signs(seed: int, layer_id: int, head_dim: int) -> np.ndarray:
+    """int8 [head_dim] of +1 / -1, equally likely: the per-layer signs of the
+    rotated (deferred TurboQuant) read."""
+    g = _rng(seed, P_ROT, layer_id)
+    return np.where(g.random(head_dim) < 0.5, -1, 1).astype(np.int8)
 
 
 def cache_rows(seed: int, layer_id: int, seq: int, layer: LayerSpec, positions: np.ndarray):
