@@ -258,10 +258,12 @@ def build_workload(name: str, rank: int, device):
                                 "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64",
                     "n_seqs": wl.n_seqs, "layers": 42, "kv_donor_layers": 24}}
         return case, calls, info
-    if name in ("tiny", "sliding16", "full32k", "full32k-8bit"):
+    if name in ("tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot"):
         if name == "full32k-8bit":          # the full32k shape with 8-bit caches
             base = W.workload_full_keqv_decode()
             wl = W.DecodeWorkload(base.name + "-8bit", base.seed, base.layer, base.filled, [8] * base.n_seqs)
+        elif name == "full32k-rot":         # the full32k shape with the deferred TurboQuant read
+            wl = W.workload_full_keqv_rotated_decode()
         else:
             wl = W.WORKLOADS[name]()
         case = harness.DecodeCase(wl, device=device, out_f32=False)
@@ -544,7 +546,7 @@ def run_gpu(args):
         # the long-context and tensor-core workloads, timed in the same run
         torch.cuda.empty_cache()
         cfg["sub_results"] = {name: sub_result(name, K, args.warmup, device, peaks)
-                              for name in ("full32k", "prefill")}
+                              for name in ("full32k", "full32k-rot", "prefill")}
     line = {"metric": METRIC.get(args.workload, "decode-attention tokens/s"),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -669,9 +671,10 @@ def run_cpu_baseline(workload: str, steps: int, warmup: int):
     process per core, one sampled sequence per worker (sequences spread over
     the workload's length distribution)."""
     cores = host_cores()
-    n_all = {"stack42": 64, "tiny": 1, "sliding16": 16, "full32k": 8, "full32k-8bit": 8}.get(workload, 1)
+    n_all = {"stack42": 64, "tiny": 1, "sliding16": 16, "full32k": 8, "full32k-8bit": 8, "full32k-rot": 8}.get(
+        workload, 1)
     nseq = max(1, min(cores, n_all))
-    procs = nseq if workload in ("stack42", "tiny", "sliding16", "full32k", "full32k-8bit") else 1
+    procs = nseq if workload in ("stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot") else 1
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
@@ -710,7 +713,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
-                    choices=["stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "prefill", "mixed"])
+                    choices=["stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot", "prefill",
+                             "mixed"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-results", action="store_true",

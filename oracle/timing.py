@@ -48,17 +48,19 @@ class SeqLayer:
         pos = wl.cached_positions(s)
         k_raw, v_raw = W.cache_rows(wl.seed, wl.layer_id, s, spec, pos)
         inp = W.layer_inputs(wl.seed, wl.layer_id, spec, wl.n_seqs, wl.n_seqs)
+        self.signs = None if inp.get("rot") is None else inp["rot"].astype(np.float64)
         if len(pos):
             kh, vh = O.prep_kv(f(k_raw), None if v_raw is None else f(v_raw), f(inp["k_w"]), pos,
                                spec.rope_theta, spec.rope_dims, eps32(spec))
-            self.cache.append(pos, kh, vh)
+            self.cache.append(pos, O.rotate_rows(kh, self.signs), O.rotate_rows(vh, self.signs))
         self.p = wl.filled[s]
         self.q, self.q_w = f(inp["q"][s]), f(inp["q_w"])
         self.k, self.k_w = f(inp["k"][s]), f(inp["k_w"])
         self.v = None if inp["v"] is None else f(inp["v"][s])
 
     def decode(self):
-        return O.decode_step(self.spec, self.cache, self.p, self.q, self.q_w, self.k, self.v, self.k_w)[3]
+        return O.decode_step(self.spec, self.cache, self.p, self.q, self.q_w, self.k, self.v, self.k_w,
+                             signs=self.signs)[3]
 
 
 class Sharer:
@@ -113,10 +115,12 @@ def build(workload: str, nseq: int, part=None):
         return units, len(idx), (f"{len(idx_all)} of {wl.n_seqs} sequences spread over the length distribution "
                                  f"(indices {idx_all}; mean length {np.mean(lens):.0f}, workload mean "
                                  f"{np.mean(wl.lengths):.0f}), all 42 layers")
-    if workload in ("tiny", "sliding16", "full32k", "full32k-8bit"):
+    if workload in ("tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot"):
         if workload == "full32k-8bit":
             base = W.workload_full_keqv_decode()
             wl = W.DecodeWorkload(base.name + "-8bit", base.seed, base.layer, base.filled, [8] * base.n_seqs)
+        elif workload == "full32k-rot":
+            wl = W.workload_full_keqv_rotated_decode()
         else:
             wl = W.WORKLOADS[workload]()
         idx_all = sample_indices(wl.filled, nseq)

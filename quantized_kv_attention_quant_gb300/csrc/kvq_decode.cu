@@ -106,9 +106,9 @@ __device__ __forceinline__ float bf16_word_at(const uint32_t (&w)[(NG + 1) / 2],
 // so with P <= e^8: 2^2 at 4 bits and 2^6 at 8 bits keep P * scale * 2^k below
 // f16's 65504.  A rotated layer's values v R reach D in size (range <= 2 D):
 // 2^-2 and 2^2 there.
-template <int BITS>
-__device__ __forceinline__ float pv_prescale(bool rotated) {
-  return rotated ? (BITS == 4 ? 0.25f : 4.f) : (BITS == 4 ? 4.f : 64.f);
+template <int BITS, bool ROT>
+__host__ __device__ constexpr float pv_prescale() {
+  return ROT ? (BITS == 4 ? 0.25f : 4.f) : (BITS == 4 ? 4.f : 64.f);
 }
 
 // Key mapping inside a tile (key 16c + s: chunk c < 4, slot s < 16).
@@ -145,7 +145,7 @@ __device__ __forceinline__ float max_over_warps(const float* p) {
 // pipelined loop and the epilogue, which writes the run's (m, l, o) partial
 // to po / ml, or, when the run is the whole row (final_out), the normalised
 // output.  Returns true when a bounded wait gave up.
-template <int D, int BITS>
+template <int D, int BITS, bool ROT>
 __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_cache& c, uint8_t* smem,
                                             const int nst, const TileRange tr, const int row, const int kvh,
                                             float* po, float* ml, const bool final_out) {
@@ -156,7 +156,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   constexpr int SLB = slot_bytes(D, BITS);
   constexpr uint32_t TX = 64 * RB + 2 * SB;     // bytes of one slot
   constexpr float L2E = 1.4426950408889634f;
-  const float PRESCALE = pv_prescale<BITS>(a.L.rot != nullptr);
+  constexpr float PRESCALE = pv_prescale<BITS, ROT>();
   constexpr int GB = NG < 8 ? NG : 8;           // groups whose MMA chains run interleaved
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t4 = lane & 3, rq = lane >> 2;
@@ -168,7 +168,8 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   uint8_t* const slots_base = stages;
   const int cap_tiles = c.capacity / kTileKeys;
   const size_t head_row0 = (size_t)kvh * c.capacity;
-  const float ksc = kTwo24 * a.L.qk_scale;      // codes' units times the score scale (a power of two)
+  // codes' units times the score scale (1, or 1/D exactly on a rotated layer)
+  const float ksc = ROT ? kTwo24 * a.L.qk_scale : kTwo24;
 
   // Copies of one stage: per side 4 code chunks, the scale block and the bias
   // block; K copies by copy ids 0..5, V copies by 6..11 (copy id j is lane
@@ -573,7 +574,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   } else {
     // the whole row in this run: out = o / l, as the merge of one partial;
     // on a rotated layer the rows are un-rotated first: o R^T / D
-    if (a.L.rot) {
+    if constexpr (ROT) {
 #pragma unroll 1
       for (int h = 1; h < D; h <<= 1) {
         for (int p = threadIdx.x; p < G * (D / 2); p += NW * 32) {
@@ -590,7 +591,7 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
     for (int i = threadIdx.x; i < G * D; i += NW * 32) {
       const int r = i / D, d = i % D;
       float o = ps[r * PS + d] * (1.f / lfin[r]);
-      if (a.L.rot) o *= (float)__ldg(a.L.rot + d) * a.L.qk_scale;
+      if constexpr (ROT) o *= (float)__ldg(a.L.rot + d) * a.L.qk_scale;
       if (a.out_f32) reinterpret_cast<float*>(a.out)[ob + i] = o;
       else reinterpret_cast<uint16_t*>(a.out)[ob + i] = f_to_bf16_rn(o);
     }
@@ -636,7 +637,7 @@ __host__ __device__ constexpr int sk_plan_bytes(int n_rows) {
   return (((n_rows + 5) & ~1) * 4 + (int)sizeof(SkWalk) + 127) & ~127;
 }
 
-template <int D, bool SK>
+template <int D, bool SK, bool ROT>
 __global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
 decode_kernel(const DecodeArgs a, const int smem_total) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -767,8 +768,8 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
     }
     __syncthreads();
     const int nst = ring_slots(D, c.bits, ring_smem);
-    const bool dead = c.bits == 4 ? decode_body<D, 4>(a, c, smem, nst, tr, row, kvh, po, ml, final_out)
-                                  : decode_body<D, 8>(a, c, smem, nst, tr, row, kvh, po, ml, final_out);
+    const bool dead = c.bits == 4 ? decode_body<D, 4, ROT>(a, c, smem, nst, tr, row, kvh, po, ml, final_out)
+                                  : decode_body<D, 8, ROT>(a, c, smem, nst, tr, row, kvh, po, ml, final_out);
     if (!SK || dead) break;
     // every thread is past its reads of the walk (decode_body has block
     // barriers); thread 0 moves it to the next unit with tiles
@@ -813,7 +814,7 @@ __device__ __forceinline__ float unrotate_dim(float o, const int8_t* signs, floa
 // ----------------------------------------------------------------------------
 // 3. merge split partials: out = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
 // ----------------------------------------------------------------------------
-template <int D>
+template <int D, bool ROT>
 __global__ void __launch_bounds__(D)
 combine_kernel(const DecodeArgs a) {
   __shared__ float wsm[D > 256 ? D : 256];   // split weights, then (rotated layers) the output row
@@ -863,7 +864,7 @@ combine_kernel(const DecodeArgs a) {
   for (; i < S; ++i)
     if (wsm[i] != 0.f) acc0 = fmaf(wsm[i], po[(size_t)i * 16 * D], acc0);
   float o = ((acc0 + acc1) + (acc2 + acc3)) * inv_l;
-  if (a.L.rot) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
+  if constexpr (ROT) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
   const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
@@ -877,7 +878,7 @@ __device__ __forceinline__ long long sk_cta_of(long long x, long long T, long lo
   return ((x + 1) * nc - 1) / T;                 // the largest c with c*T/nc <= x
 }
 
-template <int D>
+template <int D, bool ROT>
 __global__ void __launch_bounds__(D)
 combine_sk_kernel(const DecodeArgs a) {
   __shared__ float wsm[1024];
@@ -934,7 +935,7 @@ combine_sk_kernel(const DecodeArgs a) {
   }
   if (i < S) acc0 = fmaf(wsm[i], a.ws.part_o[(piece(i) * 16 + r) * D + d], acc0);
   float o = (acc0 + acc1) * inv_l;
-  if (a.L.rot) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
+  if constexpr (ROT) o = unrotate_dim<D>(o, a.L.rot, a.L.qk_scale, wsm);
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
 }
@@ -965,9 +966,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   if (!attr_set[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(attr_mu);
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(decode_kernel<D, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(decode_kernel<D, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(decode_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(decode_kernel<D, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       attr_set[dev].store(true, std::memory_order_release);
     }
@@ -988,14 +993,23 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true>, a, smem)
-                    : cudaLaunchKernelEx(&cfg, decode_kernel<D, false>, a, smem);
+  if (a.L.rot)       // the deferred TurboQuant read: score scale, PV pre-scale, output un-rotation
+    e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, true>, a, smem)
+                      : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, true>, a, smem);
+  else
+    e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, false>, a, smem)
+                      : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, false>, a, smem);
   if (e != cudaSuccess) return e;
 
   cfg.gridDim = dim3(a.n_rows, a.L.n_q);
   cfg.blockDim = dim3(D);
   cfg.dynamicSmemBytes = 0;
-  e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D>, a) : cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
+  if (a.L.rot)
+    e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D, true>, a)
+                      : cudaLaunchKernelEx(&cfg, combine_kernel<D, true>, a);
+  else
+    e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D, false>, a)
+                      : cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, a);
   return e;
 }
 

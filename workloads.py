@@ -234,6 +234,14 @@ def workload_full_keqv_decode() -> DecodeWorkload:
                           filled=[32768] * 8, bits=[4] * 8)
 
 
+def workload_full_keqv_rotated_decode() -> DecodeWorkload:
+    """The full-attention K = V decode above with the deferred TurboQuant read
+    (K and V cached in the randomized Hadamard basis, the output rotated back)."""
+    base = workload_full_keqv_decode()
+    return DecodeWorkload(base.name + "-rotated", base.seed, dataclasses.replace(FULL_KEQV, kv_rotation=True),
+                          filled=list(base.filled), bits=list(base.bits))
+
+
 def workload_prefill_chunk() -> PrefillWorkload:
     """Prompt chunk: 4 sequences append 512 tokens each onto 8192 cached
     tokens of an 8-bit cache; 8 q / 2 kv heads, head_dim 256, window 1024."""
