@@ -58,6 +58,23 @@ this outline; the rotation is taken from outside them:
           up to those roundings, and the output O' of the rotated values is
           un-rotated: O = O' R^T / D.
 
+The training forward's stateless read (trainable.ts, `trainingCaches` and
+`prefixShared.prefixSharedHidden`; model.ts, the `attentionTraining` comment
+and `forwardTrainingHidden`): one training cache per donor layer stores
+nothing; it reads the plain (unquantized) prepped keys and values handed to it
+under the run's mask -- causal (windowed on sliding layers), or block-sparse
+with a logical-position window under a prefix-shared layout, whose blocks are
+roped block-wise.  A KV-sharing layer reads its donor's keys and values.  The
+pages do not print the layout type; the reading taken is
+  R-prefix: the packed rows of one training sequence are a prefix block (block
+          0, possibly empty) followed by branch blocks 1..n-1, given by block
+          offsets.  Prefix row i sits at logical position i, row j of a branch
+          at P + j (P = prefix rows).  Row r sees row k iff k is in r's own
+          block or in the prefix, lp(k) <= lp(r), and lp(k) > lp(r) - W on a
+          sliding layer.  A single block is the plain causal training read.
+  Each branch thus reads exactly what it would read as its own sequence
+  continuing the prefix.
+
 Values are carried as float64 arrays holding bf16-representable numbers.
 """
 from __future__ import annotations
@@ -461,3 +478,60 @@ def prefill_chunk(layer, cache: OracleCache, start: int, q_raw, q_w, k_raw, v_ra
         outs[t] = finish_read(attend_cache(q_hat[t], start + t, layer.window, layer.n_kv_heads,
                                            cache.k_hat, cache.v_hat, scale), signs)
     return q_hat, k_hat, v_hat, outs
+
+
+# ----------------------------------------------------------------------------
+# the training forward's stateless read (reading R-prefix)
+# ----------------------------------------------------------------------------
+
+def layout_positions(block_offsets):
+    """Block index and logical position of every packed row of a training
+    sequence whose blocks are [off[b], off[b+1]): block 0 is the prefix, the
+    others are branches continuing it at position P = off[1]."""
+    off = np.asarray(block_offsets, dtype=np.int64)
+    T = int(off[-1])
+    block = np.zeros(T, dtype=np.int64)
+    pos = np.zeros(T, dtype=np.int64)
+    P = int(off[1]) if len(off) > 1 else 0
+    for b in range(len(off) - 1):
+        lo, hi = int(off[b]), int(off[b + 1])
+        block[lo:hi] = b
+        pos[lo:hi] = np.arange(hi - lo) + (0 if b == 0 else P)
+    return block, pos
+
+
+def train_visible(block_offsets, r: int, window: int) -> np.ndarray:
+    """Packed indices of the rows that packed row r reads, in increasing order."""
+    block, pos = layout_positions(block_offsets)
+    same = (block == block[r]) | (block == 0)
+    causal = pos <= pos[r]
+    inside = pos > pos[r] - window if window > 0 else np.ones_like(causal)
+    return np.nonzero(same & causal & inside)[0]
+
+
+def train_kv(layer, k_raw, v_raw, k_w, block_offsets):
+    """A donor layer's plain keys and values for the packed rows [T, Hkv, D]:
+    kNorm + RoPE at each row's logical position, vNorm (K = V: of the raw k
+    rows); nothing is quantized."""
+    _, pos = layout_positions(block_offsets)
+    return prep_kv(k_raw, v_raw, k_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)
+
+
+def train_attend(layer, q_raw, q_w, k_hat, v_hat, block_offsets, rows=None):
+    """The stateless read of the training forward: every packed row's q heads
+    attend the rows it sees (train_visible) of k_hat / v_hat [T, Hkv, D] with
+    SDPA scale 1.0.  q_raw [T, Hq, D]; `rows` optionally restricts which rows'
+    outputs are computed.  Returns (q_hat [T, Hq, D], {r: out [Hq, D]})."""
+    _, pos = layout_positions(block_offsets)
+    q_hat = prep_q(q_raw, q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    Hq = q_hat.shape[1]
+    Hkv = k_hat.shape[1]
+    G = Hq // Hkv
+    outs = {}
+    for r in (range(q_hat.shape[0]) if rows is None else rows):
+        vis = train_visible(block_offsets, r, layer.window)
+        out = np.empty((Hq, q_hat.shape[2]), dtype=np.float64)
+        for kvh in range(Hkv):
+            out[kvh * G:(kvh + 1) * G] = attend(q_hat[r, kvh * G:(kvh + 1) * G], k_hat[vis, kvh], v_hat[vis, kvh])
+        outs[r] = out
+    return q_hat, outs

@@ -100,6 +100,16 @@ MUTANTS = {
     "rot-q-not-rotated": ("    q_hat = rotate_rows(prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps),\n"
                           "                        signs)[0]",
                           "    q_hat = prep_q(q_raw[None], q_w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)[0]"),
+    # the training forward's stateless read (reading R-prefix)
+    "train-branch-pos-from-zero": ("pos[lo:hi] = np.arange(hi - lo) + (0 if b == 0 else P)",
+                                   "pos[lo:hi] = np.arange(hi - lo)"),
+    "train-branch-pos-packed": ("pos[lo:hi] = np.arange(hi - lo) + (0 if b == 0 else P)",
+                                "pos[lo:hi] = np.arange(hi - lo) + lo"),
+    "train-branches-see-each-other": ("same = (block == block[r]) | (block == 0)",
+                                      "same = np.ones_like(block, dtype=bool)"),
+    "train-branch-no-prefix": ("same = (block == block[r]) | (block == 0)", "same = block == block[r]"),
+    "train-window-on-packed-index": ("inside = pos > pos[r] - window if window > 0",
+                                     "inside = np.arange(len(pos)) > r - window if window > 0"),
 }
 
 PINS = [
@@ -110,6 +120,7 @@ PINS = [
     P.pin_rms_hand, P.pin_rms_invariants, P.pin_rope_hand, P.pin_rope_invariants, P.pin_rope_large_positions,
     P.pin_attention, P.pin_brute_force_attention, P.pin_keqv, P.pin_prefill_matches_decode,
     P.pin_hadamard, P.pin_rotation, P.pin_rotated_attention_identity, P.pin_rotated_step,
+    P.pin_train_branches_read_as_own_sequences, P.pin_train_branch_independence,
 ]
 
 

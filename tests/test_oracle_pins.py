@@ -676,3 +676,88 @@ def test_rotation():
     pin_rotation(O)
     pin_rotated_attention_identity(O)
     pin_rotated_step(O)
+
+
+# ----------------------------------------------------------------------------
+# the training forward's stateless read (reading R-prefix)
+# ----------------------------------------------------------------------------
+
+def _train_case(rng, D=32, Hq=4, Hkv=2, lens=(13, 9, 1, 6), window=0, keqv=False, rope=16):
+    layer = W.LayerSpec(Hq, Hkv, D, window, rope, 1e4, keqv, rms_eps=1e-6)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(off[-1])
+    raw = lambda h: O.rn_bf16(rng.standard_normal((T, h, D)))
+    w = O.rn_bf16(1 + 0.1 * rng.standard_normal(D))
+    return layer, off, raw(Hq), raw(Hkv), (None if keqv else raw(Hkv)), w
+
+
+def _own_sequence(o, layer, q, k, v, w, rows):
+    """The rows `rows` (packed indices, in order) as a sequence of their own at
+    positions 0 .. n-1, read by the inference definitions (visible_keys /
+    attend_cache) over unquantized keys and values: (k_hat, v_hat, outs)."""
+    pos = np.arange(len(rows))
+    k_hat, v_hat = o.prep_kv(k[rows], None if v is None else v[rows], w, pos, layer.rope_theta,
+                             layer.rope_dims, layer.rms_eps)
+    q_hat = o.prep_q(q[rows], w, pos, layer.rope_theta, layer.rope_dims, layer.rms_eps)
+    at = lambda a: (lambda lo, hi: a[lo:hi + 1])
+    outs = [o.attend_cache(q_hat[t], t, layer.window, layer.n_kv_heads, at(k_hat), at(v_hat))
+            for t in range(len(rows))]
+    return k_hat, v_hat, outs
+
+
+def pin_train_branches_read_as_own_sequences(o):
+    """Under a prefix-shared layout every branch reads exactly what it reads as
+    its own sequence continuing the prefix, and the prefix what it reads
+    alone: the packed mask and positions against the plain causal read of each
+    unpacked sequence (full, windowed and K = V layers; an empty branch)."""
+    for seed, kw in ((21, {}), (22, dict(window=5)), (23, dict(keqv=True, lens=(7, 12, 0, 3))),
+                     (24, dict(lens=(0, 6, 4), window=3))):
+        rng = np.random.default_rng(seed)
+        layer, off, q, k, v, w = _train_case(rng, **kw)
+        k_hat, v_hat = o.train_kv(layer, k, v, w, off)
+        _, outs = o.train_attend(layer, q, w, k_hat, v_hat, off)
+        prefix = np.arange(off[0], off[1])
+        for b in range(len(off) - 1):
+            rows = np.arange(off[b], off[b + 1])
+            seq = prefix if b == 0 else np.concatenate([prefix, rows])
+            kk, vv, want = _own_sequence(o, layer, q, k, v, w, seq)
+            mine = np.arange(len(seq)) if b == 0 else np.arange(len(prefix), len(seq))
+            assert np.array_equal(k_hat[rows], kk[mine]) and np.array_equal(v_hat[rows], vv[mine])
+            for j, r in enumerate(rows):
+                assert np.allclose(outs[int(r)], want[mine[j]], rtol=0, atol=1e-12), (seed, b, j)
+
+
+def pin_train_branch_independence(o):
+    """A branch's outputs do not depend on another branch's rows, nor on the
+    order in which the branches are packed."""
+    rng = np.random.default_rng(25)
+    layer, off, q, k, v, w = _train_case(rng, window=6)
+    k_hat, v_hat = o.train_kv(layer, k, v, w, off)
+    _, base = o.train_attend(layer, q, w, k_hat, v_hat, off)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    for a in (q2, k2, v2):
+        a[off[1]:off[2]] = O.rn_bf16(rng.standard_normal(a[off[1]:off[2]].shape))   # branch 1 replaced
+    kh2, vh2 = o.train_kv(layer, k2, v2, w, off)
+    _, other = o.train_attend(layer, q2, w, kh2, vh2, off)
+    for r in list(range(off[0], off[1])) + list(range(off[2], off[-1])):
+        assert np.array_equal(base[r], other[r])
+    # branches 1 and 3 swapped in the packing
+    lens = np.diff(off)
+    order = [0, 3, 2, 1]
+    perm = np.concatenate([np.arange(off[b], off[b + 1]) for b in order])
+    off_p = np.concatenate([[0], np.cumsum(lens[order])])
+    khp, vhp = o.train_kv(layer, k[perm], v[perm], w, off_p)
+    _, swapped = o.train_attend(layer, q[perm], w, khp, vhp, off_p)
+    for new_r, old_r in enumerate(perm):
+        assert np.allclose(swapped[new_r], base[int(old_r)], rtol=0, atol=1e-12)
+
+
+def test_training_read():
+    pin_train_branches_read_as_own_sequences(O)
+    pin_train_branch_independence(O)
+    # hand case: prefix of 2, branches of 1 and 2 rows; row 4 (branch 2, row 1,
+    # logical position 3) reads the prefix and its own branch up to itself
+    assert list(O.train_visible([0, 2, 3, 5], 4, 0)) == [0, 1, 3, 4]
+    assert list(O.train_visible([0, 2, 3, 5], 4, 2)) == [3, 4]
+    assert list(O.train_visible([0, 2, 3, 5], 2, 0)) == [0, 1, 2]
+    assert list(O.layout_positions([0, 2, 3, 5])[1]) == [0, 1, 2, 2, 3]

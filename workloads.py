@@ -320,6 +320,36 @@ def workload_mixed_step(n_decode: int = 48, lo: int = 1024, hi: int = 8192):
     return dec, win
 
 
+@dataclasses.dataclass
+class TrainWorkload:
+    """One packed training sequence of a layer under a prefix-shared layout:
+    blocks[0] prefix rows (may be 0), blocks[1:] the rows of each branch.  A
+    single block is the plain causal training read.  Inputs come from
+    `layer_inputs(seed, layer_id, layer, T, T)`."""
+    name: str
+    seed: int
+    layer: LayerSpec
+    blocks: list
+
+    @property
+    def n_rows(self) -> int:
+        return int(sum(self.blocks))
+
+    def offsets(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.blocks)]).astype(np.int32)
+
+
+def workload_train_prefix_shared(prefix: int = 1024, branches: tuple = (256, 256, 256, 256)):
+    """The training forward's read over the 42-layer stack for one packed
+    sequence: a prefix of `prefix` rows shared by the given branches (the
+    prefix-shared layout of trainable.ts), sliding and full layers of the
+    stack's shapes.  Returns (sliding, full) workloads of one seed."""
+    seed = 1007
+    blocks = [prefix, *branches]
+    return (TrainWorkload("train-prefix-sliding", seed, SLIDING, list(blocks)),
+            TrainWorkload("train-prefix-full", seed, FULL_KEQV, list(blocks)))
+
+
 WORKLOADS = {
     "tiny": workload_tiny_decode,
     "sliding16": workload_sliding_decode_b16,
