@@ -259,6 +259,76 @@ kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int3
                       const uint16_t* q_norm_w, int32_t out_is_f32, void* stream);
 
 /*
+ * The training forward's stateless read (trainable.ts, trainingCaches and
+ * prefixShared.prefixSharedHidden; model.ts, the attentionTraining comment and
+ * forwardTrainingHidden).  A training cache stores nothing: each donor layer
+ * preps plain (unquantized) bf16 keys and values for the rows of the pass,
+ * and every layer -- a KV-sharing one with its donor's keys and values -- reads
+ * them under the pass's mask, block-sparse under a prefix-shared layout.
+ *
+ * Layout (the pages name the prefix-shared layout but do not print it; this
+ * is the plain reading): the n_rows packed rows of one training sequence form
+ * n_blocks blocks [block_offsets[b], block_offsets[b+1]).  Block 0 is the
+ * shared prefix (it may be empty) at positions 0, 1, ...; every other block is
+ * a branch continuing the prefix, its row j at position block_offsets[1] + j.
+ * A row reads the rows of the prefix and of its own block whose positions are
+ * at most its own (and, on a sliding layer, greater than its own - window).
+ * One block is the plain causal (or windowed) training read.
+ *
+ *   block_offsets   device int32[n_blocks + 1]: 0 = block_offsets[0] <= ... <=
+ *                   block_offsets[n_blocks] = n_rows (1 <= n_blocks <= 65535,
+ *                   n_rows < 2^24).  A layout that breaks this for some block is
+ *                   found by the kernels: that block's outputs are not written and
+ *                   KVQ_STATUS_SEQ_SKIPPED is set in the status word.
+ *   rot_signs of the layer must be NULL (KVQ_EUNSUPPORTED): the training read
+ *   has no quantized cache to rotate.
+ */
+
+/*
+ * kvq_train_kv_prep -- a donor layer's plain keys and values for the rows of
+ * the pass: k_hat = RoPE_p(bf16(RMSNorm(k_raw, k_norm_w))) and v_hat =
+ * bf16(RMSNorm(v_raw or k_raw if k_eq_v, no weight)), each row at its layout
+ * position p.  Nothing is quantized.
+ *
+ *   k_raw, v_raw      device bf16 [n_rows][n_kv_heads][head_dim]; v_raw NULL iff k_eq_v
+ *   k_norm_w          device bf16 [head_dim]
+ *   k_hat, v_hat      device bf16 [n_rows][n_kv_heads][head_dim] (16-byte aligned),
+ *                     the outputs
+ */
+kvq_status kvq_train_kv_prep(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets,
+                             int32_t n_rows, const uint16_t* k_raw, const uint16_t* v_raw,
+                             const uint16_t* k_norm_w, uint16_t* k_hat, uint16_t* v_hat, void* stream);
+
+/*
+ * attn_train_forward -- every row's q heads read the keys and values of the
+ * rows they see under the layout (above), with SDPA scale 1.0:
+ *   q_hat = RoPE_p(bf16(RMSNorm(q_raw, q_norm_w))),
+ *   out[r][h] = sum_j softmax_j(q_hat . k_hat_j) v_hat_j.
+ * It runs on the tcgen05 tensor cores, 128 (row, head) pairs of one block per
+ * CTA (head_dim 512: each CTA half of the output dims): QK with the bf16
+ * operands (exact products, fp32 accumulation), PV with P and v_hat as f16.
+ * n_q_heads / n_kv_heads must divide 128 (KVQ_EUNSUPPORTED otherwise).
+ *
+ *   max_block_rows   host upper bound of the rows of every block (sizes the grid),
+ *                    1 .. n_rows
+ *   q_raw            device bf16 [n_rows][n_q_heads][head_dim]
+ *   k_hat, v_hat     device bf16 [n_rows][n_kv_heads][head_dim] (16-byte aligned),
+ *                    as written by kvq_train_kv_prep of this layer or its donor
+ *   out              device [n_rows][n_q_heads][head_dim], fp32 if out_is_f32 else bf16
+ *   q_prepped        NULL or device bf16 [n_rows][n_q_heads][head_dim] receiving q_hat
+ *   workspace        device scratch of at least attn_train_workspace_bytes(layer,
+ *                    n_rows) bytes; its first 4 bytes receive the status word
+ */
+kvq_status attn_train_forward(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets,
+                              int32_t n_rows, int32_t max_block_rows,
+                              const uint16_t* q_raw, const uint16_t* q_norm_w,
+                              const uint16_t* k_hat, const uint16_t* v_hat,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+size_t attn_train_workspace_bytes(const kvq_layer* layer, int32_t n_rows);
+
+/*
  * attn_decode_static -- attn_decode without a caller-provided workspace, for
  * callers that cannot allocate device memory: code that only receives input
  * and output pointers from a host framework that owns every allocation (a

@@ -76,6 +76,12 @@ def _load():
     lib.attn_prefill_workspace_bytes.restype = sz
     lib.attn_mixed.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
     lib.attn_mixed.restype = ctypes.c_int
+    lib.kvq_train_kv_prep.argtypes = [lay, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.kvq_train_kv_prep.restype = ctypes.c_int
+    lib.attn_train_forward.argtypes = [lay, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
+    lib.attn_train_forward.restype = ctypes.c_int
+    lib.attn_train_workspace_bytes.argtypes = [lay, i32]
+    lib.attn_train_workspace_bytes.restype = sz
     lib.kvq_static_status.argtypes = [vp, vp]
     lib.kvq_static_status.restype = ctypes.c_int
     lib.kvq_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
@@ -191,6 +197,26 @@ def attn_prefill_chunk(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_
 
 def attn_prefill_workspace_bytes(layer: KvqLayer, n_seqs, n_rows, max_rows_per_seq) -> int:
     return lib.attn_prefill_workspace_bytes(ctypes.byref(layer), n_seqs, n_rows, max_rows_per_seq)
+
+
+def kvq_train_kv_prep(layer: KvqLayer, n_blocks, block_offsets, n_rows, k_raw, v_raw, k_norm_w, k_hat, v_hat,
+                      stream=None):
+    """A donor layer's plain keys and values of a training pass (see include/kvq.h)."""
+    _check(lib.kvq_train_kv_prep(ctypes.byref(layer), n_blocks, _ptr(block_offsets), n_rows, _ptr(k_raw),
+                                 _ptr(v_raw), _ptr(k_norm_w), _ptr(k_hat), _ptr(v_hat), _stream(stream)))
+
+
+def attn_train_forward(layer: KvqLayer, n_blocks, block_offsets, n_rows, max_block_rows, q_raw, q_norm_w,
+                       k_hat, v_hat, out, out_is_f32, q_prepped, workspace, workspace_bytes, stream=None):
+    """The training forward's read under a prefix-shared layout (see include/kvq.h)."""
+    _check(lib.attn_train_forward(ctypes.byref(layer), n_blocks, _ptr(block_offsets), n_rows, max_block_rows,
+                                  _ptr(q_raw), _ptr(q_norm_w), _ptr(k_hat), _ptr(v_hat), _ptr(out),
+                                  int(out_is_f32), _ptr(q_prepped), _ptr(workspace), workspace_bytes,
+                                  _stream(stream)))
+
+
+def attn_train_workspace_bytes(layer: KvqLayer, n_rows) -> int:
+    return lib.attn_train_workspace_bytes(ctypes.byref(layer), n_rows)
 
 
 def attn_group(phase, seqs, n_seqs, row_offsets, pos, n_rows, max_pos, max_rows_per_seq, q_raw, out,

@@ -224,7 +224,7 @@ kvq_status kv_quant_append(const kvq_layer* layer, const kvq_seq_cache* seqs, in
     REQUIRE_PTR(v_raw, "v_raw", 16);
   }
   if (kv_prepped && !aligned(kv_prepped, 2)) return fail(KVQ_EINVAL, "kv_prepped is not 2-byte aligned");
-  kvq::AppendArgs a;
+  kvq::AppendArgs a = {};
   a.L = L;
   a.seqs = seqs;
   a.n_seqs = n_seqs;
@@ -490,6 +490,110 @@ kvq_status kvq_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, void* 
   return KVQ_OK;
 }
 
+// ---------------------------------------------------------------------------
+// The training forward's stateless read: plain keys and values of a donor
+// layer, then the read of any layer under the prefix-shared block layout.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+kvq_status check_layout(int32_t n_blocks, const int32_t* block_offsets, int32_t n_rows) {
+  if (n_blocks < 1 || n_blocks > 65535) return fail(KVQ_EINVAL, "n_blocks %d not in [1, 65535]", n_blocks);
+  if (n_rows < 0 || n_rows >= (1 << 24)) return fail(KVQ_EINVAL, "n_rows %d not in [0, 2^24)", n_rows);
+  REQUIRE_PTR(block_offsets, "block_offsets", 4);
+  return KVQ_OK;
+}
+
+kvq_status check_train_layer(const kvq_layer* layer, kvq::LayerArgs* L) {
+  const kvq_status st = check_layer(layer, L);
+  if (st != KVQ_OK) return st;
+  if (L->rot) return fail(KVQ_EUNSUPPORTED, "the training read takes plain keys and values (rot_signs must be NULL)");
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_train_kv_prep(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets, int32_t n_rows,
+                             const uint16_t* k_raw, const uint16_t* v_raw, const uint16_t* k_norm_w,
+                             uint16_t* k_hat, uint16_t* v_hat, void* stream) {
+  kvq::LayerArgs L;
+  kvq_status st = check_train_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if ((st = check_layout(n_blocks, block_offsets, n_rows)) != KVQ_OK) return st;
+  if (n_rows == 0) return KVQ_OK;
+  REQUIRE_PTR(k_raw, "k_raw", 16);
+  REQUIRE_PTR(k_norm_w, "k_norm_w", 2);
+  if (L.k_eq_v) {
+    if (v_raw) return fail(KVQ_EINVAL, "v_raw must be NULL when k_eq_v = 1");
+  } else {
+    REQUIRE_PTR(v_raw, "v_raw", 16);
+  }
+  REQUIRE_PTR(k_hat, "k_hat", 16);
+  REQUIRE_PTR(v_hat, "v_hat", 16);
+  kvq::AppendArgs a = {};
+  a.L = L;
+  a.seqs = nullptr;
+  a.n_seqs = n_blocks;
+  a.row_offsets = block_offsets;
+  a.start_pos = nullptr;
+  a.n_rows = n_rows;
+  a.k_raw = k_raw;
+  a.v_raw = v_raw;
+  a.k_w = k_norm_w;
+  a.out_k = k_hat;
+  a.out_v = v_hat;
+  const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
+  const cudaError_t e = kvq::launch_append(a, f, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_train_kv_prep launch");
+  return KVQ_OK;
+}
+
+size_t attn_train_workspace_bytes(const kvq_layer* layer, int32_t n_rows) {
+  kvq::LayerArgs L;
+  if (check_layer(layer, &L) != KVQ_OK || n_rows < 0 || n_rows >= (1 << 24)) return 0;
+  return kvq::train_ws_bytes(n_rows, L);
+}
+
+kvq_status attn_train_forward(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets, int32_t n_rows,
+                              int32_t max_block_rows, const uint16_t* q_raw, const uint16_t* q_norm_w,
+                              const uint16_t* k_hat, const uint16_t* v_hat, void* out, int32_t out_is_f32,
+                              uint16_t* q_prepped, void* workspace, size_t workspace_bytes, void* stream) {
+  kvq::LayerArgs L;
+  kvq_status st = check_train_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if (!kvq::train_supported(L))
+    return fail(KVQ_EUNSUPPORTED, "training read: n_q_heads / n_kv_heads = %d must divide 128", L.G);
+  if ((st = check_layout(n_blocks, block_offsets, n_rows)) != KVQ_OK) return st;
+  if (n_rows == 0) return KVQ_OK;
+  if (max_block_rows < 1 || max_block_rows > n_rows)
+    return fail(KVQ_EINVAL, "max_block_rows %d not in [1, n_rows]", max_block_rows);
+  REQUIRE_PTR(q_raw, "q_raw", 16);
+  REQUIRE_PTR(q_norm_w, "q_norm_w", 2);
+  REQUIRE_PTR(k_hat, "k_hat", 16);
+  REQUIRE_PTR(v_hat, "v_hat", 16);
+  REQUIRE_PTR(out, "out", out_is_f32 ? 4 : 2);
+  REQUIRE_PTR(workspace, "workspace", 256);
+  if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
+  if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
+  const size_t need = kvq::train_ws_bytes(n_rows, L);
+  if (workspace_bytes < need) return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  kvq::TrainArgs t = {};
+  t.L = L;
+  t.n_rows = n_rows;
+  t.n_blocks = n_blocks;
+  t.off = block_offsets;
+  t.out = out;
+  t.out_f32 = out_is_f32;
+  const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
+  const cudaError_t e = kvq::launch_train(t, q_raw, q_norm_w, k_hat, v_hat, q_prepped, workspace, max_block_rows, f,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_train_forward launch");
+  return KVQ_OK;
+}
+
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
     case KVQ_OK: return "ok";
@@ -503,6 +607,6 @@ const char* kvq_status_string(kvq_status s) {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }
 
-int32_t kvq_version(void) { return 110; }
+int32_t kvq_version(void) { return 120; }
 
 }  // extern "C"

@@ -1,7 +1,8 @@
 // kv_quant_append: prep (norm, RoPE) and group-quantize new K/V rows into the
 // affine cache (model.ts attentionTraining: kNorm, vNorm, RoPE at the cache
 // offset, then cache.appendWindow(k, v); gemma4-e4b.ts Gemma4Layer.kv:
-// {bits, groupSize 64}).
+// {bits, groupSize 64}).  The same kernel preps the plain keys and values of
+// the training read (kvq_train_kv_prep), which are not quantized.
 //
 // One block handles one row (token) and a block of its (kv head, K-or-V)
 // items, TH threads of E contiguous elements per item: the row's RoPE angles
@@ -160,17 +161,21 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   const int s = find_seq(a.row_offsets, a.n_seqs, row);
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
   const int t_in = row - off0, rows_s = off1 - off0;
-  const int pos = __ldg(a.start_pos + s) + t_in;
-  const kvq_seq_cache c = a.seqs[s];
-  const bool ok = (c.bits == 4 || c.bits == 8) && c.capacity > 0 && (c.capacity % kTileKeys) == 0 &&
-                  c.k_codes && c.v_codes && c.k_scales && c.k_biases && c.v_scales && c.v_biases &&
-                  aligned16(c.k_codes) && aligned16(c.v_codes) && aligned16(c.k_scales) &&
-                  aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases) &&
+  // training read (no caches): block 0 of the layout starts at position 0,
+  // every later block (a branch) continues the prefix
+  const bool train = a.seqs == nullptr;
+  const int pos = (train ? (s == 0 ? 0 : __ldg(a.row_offsets + 1)) : __ldg(a.start_pos + s)) + t_in;
+  kvq_seq_cache c = {};
+  if (!train) c = a.seqs[s];
+  const bool ok = (train || ((c.bits == 4 || c.bits == 8) && c.capacity > 0 && (c.capacity % kTileKeys) == 0 &&
+                             c.k_codes && c.v_codes && c.k_scales && c.k_biases && c.v_scales && c.v_biases &&
+                             aligned16(c.k_codes) && aligned16(c.v_codes) && aligned16(c.k_scales) &&
+                             aligned16(c.k_biases) && aligned16(c.v_scales) && aligned16(c.v_biases))) &&
                   pos >= 0 && pos < (1 << 24);
   if (!ok) return;                       // uniform over the block
   // a row whose slot a newer row of this call overwrites is prepped (for
   // kv_prepped) but not stored
-  const bool store = t_in >= rows_s - c.capacity;
+  const bool store = !train && t_in >= rows_s - c.capacity;
 
   // ---- the row's rotation angles, once for all K heads ----
   if (R > 0) {
@@ -230,6 +235,13 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
     uint16_t* dst = a.prepped + (((size_t)kind * a.n_rows + row) * Hkv + head) * D + tt * E;
 #pragma unroll
     for (int i = 0; i < E; ++i) dst[i] = y[i];
+  }
+
+  if (train) {                           // the plain keys and values are the output
+    uint16_t* dst = (kind == 0 ? a.out_k : a.out_v) + ((size_t)row * Hkv + head) * D + tt * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) dst[i] = y[i];
+    return;
   }
 
   // ---- quantize the 64-element group, pack, store ----

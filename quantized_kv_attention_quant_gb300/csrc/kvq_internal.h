@@ -34,6 +34,10 @@ struct AppendArgs {
   const uint16_t* v_raw;
   const uint16_t* k_w;
   uint16_t* prepped;
+  // training read (seqs == nullptr): the prepped rows are the output, written
+  // to out_k / out_v [n_rows][n_kv][D], and nothing is quantized
+  uint16_t* out_k;
+  uint16_t* out_v;
 };
 
 // Workspace of the attention calls, carved from the caller's buffer.
@@ -48,13 +52,17 @@ struct DecodeWs {
   // prompt-chunk tensor-core path only
   uint16_t* q16;        // [n_rows][n_q][D] q_hat as f16
   float* qsum;          // [n_rows][n_q][D/64] per-group sums of those f16 values
+  // training-read path only
+  uint16_t* qhat;       // [n_rows][n_q][D] q_hat as bf16
 };
 
 // Query rows of an attention call.  Decode: row i is sequence i at position
 // pos[i] (row_offsets == nullptr).  Prompt chunk: row i belongs to the
 // sequence s with row_offsets[s] <= i < row_offsets[s+1] and sits at position
 // pos[s] + (i - row_offsets[s]); the sequence's newest cached position is its
-// last row's.
+// last row's.  Training read (pos == nullptr): the row_offsets are the blocks
+// of a prefix-shared layout, block 0 (the prefix) starting at position 0 and
+// every other block at position row_offsets[1].
 struct DecodeArgs {
   LayerArgs L;
   const kvq_seq_cache* seqs;
@@ -90,6 +98,21 @@ DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L);
 cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st);
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
+
+// The training forward's stateless read (tcgen05): q prep, then the read of
+// the plain bf16 keys and values under the prefix-shared block mask.
+struct TrainArgs {
+  LayerArgs L;
+  int n_rows, n_blocks;
+  const int32_t* off;   // block offsets [n_blocks + 1]
+  void* out;
+  int out_f32;
+};
+bool train_supported(const LayerArgs& L);
+size_t train_ws_bytes(int n_rows, const LayerArgs& L);
+cudaError_t launch_train(const TrainArgs& t, const uint16_t* q_raw, const uint16_t* q_w, const uint16_t* k_hat,
+                         const uint16_t* v_hat, uint16_t* q_prepped, void* ws, int max_block_rows,
+                         const RopeFreqs& f, cudaStream_t st);
 // One CTA whose bounded wait on an mbarrier that nothing completes gives up
 // after limit_ns and flags the timeout bit in *status.
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st);

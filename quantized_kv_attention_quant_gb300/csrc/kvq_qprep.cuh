@@ -44,7 +44,8 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
     if (__ldg(a.row_offsets + mid) <= row) lo = mid; else hi = mid - 1;
   }
   const int o0 = __ldg(a.row_offsets + lo), o1 = __ldg(a.row_offsets + lo + 1);
-  const int p0 = __ldg(a.pos + lo);
+  // training read: the prefix starts at 0, every branch continues it
+  const int p0 = a.pos ? __ldg(a.pos + lo) : (lo == 0 ? 0 : __ldg(a.row_offsets + 1));
   return {lo, p0 + (row - o0), p0 + (o1 - o0) - 1};
 }
 
@@ -58,7 +59,7 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
 //     32-bit fragment word holds two dims of ONE head, so heads write
 //     disjoint words.
 //   ROWS = true (prompt chunk): q_hat as f16 rows and per-group sums of
-//     those f16 values.
+//     those f16 values; (training read) q_hat as bf16 rows.
 // Both write q_hat (bf16) to q_prepped when it is given.
 // ----------------------------------------------------------------------------
 template <int D>
@@ -115,7 +116,7 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
 #pragma unroll
   for (int i = 0; i < E; ++i) wq[i] = bf16_to_f(a.q_w[tt * E + i]);
   const RowInfo ri = row_info(a, row);
-  const int bits = a.seqs[ri.s].bits;
+  const int bits = a.seqs ? a.seqs[ri.s].bits : 8;
   const int pc = min(max(ri.p, 0), (1 << 24) - 1);
 
   // ---- the row's rotation angles, once for all heads ----
@@ -191,7 +192,12 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
     }
   }
   if constexpr (ROWS) {
-    if (active) {
+    if (active && a.ws.qhat) {
+      uint16_t* dst = a.ws.qhat + ((size_t)row * a.L.n_q + hq) * D + tt * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) dst[i] = y[i];
+    }
+    if (active && a.ws.q16) {
       __half* dst = reinterpret_cast<__half*>(a.ws.q16) + ((size_t)row * a.L.n_q + hq) * D + tt * E;
 #pragma unroll
       for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(bf16_to_f(y[i]));

@@ -1,4 +1,5 @@
-// Blackwell tensor-core (tcgen05) building blocks for the prompt-chunk path:
+// Blackwell tensor-core (tcgen05) building blocks for the prompt-chunk and
+// training-read paths:
 // tensor-memory allocation, shared-memory matrix descriptors, the f16 MMA with
 // its commit to an mbarrier, and tensor-memory loads/stores.  Written from the
 // PTX ISA's description of tcgen05 (sm_100 family).
@@ -47,12 +48,28 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);        // M / 16
 }
 
+// the same with bf16 A and B (both operands must share their type)
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                            // D format: f32
+         | (1u << 7) | (1u << 10)             // A, B format: bf16
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         bool accumulate) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T: A's row i in lane i, K elements 2j and
+// 2j+1 of a 16-bit type packed in column j (8 columns per K step of 16)
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u) : "memory");
 }
 // the mbarrier receives one arrival when every MMA issued so far by this thread is complete
 __device__ __forceinline__ void commit(uint64_t* mbar) {
@@ -82,6 +99,21 @@ __device__ __forceinline__ void st_x16(uint32_t taddr, const float (&v)[16]) {
                   "r"(__float_as_uint(v[15]))
                : "memory");
 }
+__device__ __forceinline__ void ld_x4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void st_x1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(__float_as_uint(v)) : "memory");
+}
+__device__ __forceinline__ void st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -93,6 +125,17 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t smem_row_addr, uint32
                                                   uint32_t r3) {
   asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
                :: "r"(smem_row_addr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
+// ---- tensor memory accelerator: a 3-D tile global -> shared ----
+// `map` is the address of a CUtensorMap kernel parameter; coordinates are
+// elements, innermost first; completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+               : "memory");
 }
 
 // 16-byte chunk `chunk` of row `r` of a K-major 128-byte-swizzled tile whose

@@ -15,8 +15,8 @@ import torch
 import workloads as W
 
 from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_workspace_bytes, attn_group,
-               attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, kv_quant_append,
-               layer as make_layer)
+               attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, attn_train_forward,
+               attn_train_workspace_bytes, kv_quant_append, kvq_train_kv_prep, layer as make_layer)
 from .cache import LayerCaches
 
 
@@ -305,3 +305,86 @@ class StackCase:
             if i < W.N_DONORS:
                 case.append(stream)
             case.attend(stream)
+
+
+class TrainCase:
+    """The training forward's read of one layer over one packed sequence
+    (TrainWorkload): a donor layer preps its plain keys and values, then every
+    row attends under the prefix-shared layout.  With `kv` = (k_hat, v_hat) of
+    a donor the layer is a KV-sharing one: it reads those and preps none."""
+
+    def __init__(self, wl: W.TrainWorkload, device="cuda", out_f32=True, keep_prepped=False, kv=None,
+                 layer_id=0):
+        self.wl, self.spec, self.device = wl, wl.layer, device
+        spec, T = wl.layer, wl.n_rows
+        self.lay = kvq_layer(spec)
+        inp = W.layer_inputs(wl.seed, layer_id, spec, T, T)
+        self.host_inputs = inp
+        self.q_w = dev_bits(inp["q_w"], device)
+        self.k_w = dev_bits(inp["k_w"], device)
+        self.q = dev_bits(inp["q"], device)
+        self.donor = kv is None
+        if self.donor:
+            self.k = dev_bits(inp["k"], device)
+            self.v = dev_bits(inp["v"], device) if inp["v"] is not None else None
+            shape = (T, spec.n_kv_heads, spec.head_dim)
+            self.k_hat = torch.empty(shape, dtype=torch.int16, device=device)
+            self.v_hat = torch.empty(shape, dtype=torch.int16, device=device)
+        else:
+            self.k_hat, self.v_hat = kv
+        self.n_rows = T
+        self.n_blocks = len(wl.blocks)
+        self.offs = dev_i32(wl.offsets(), device)
+        self.max_rows = max(1, min(T, int(max(wl.blocks))))
+        self.ws_bytes = attn_train_workspace_bytes(self.lay, T)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.out_f32 = out_f32
+        self.out = torch.empty((T, spec.n_q_heads, spec.head_dim), dtype=torch.float32 if out_f32 else torch.int16,
+                               device=device)
+        self.q_prepped = torch.empty_like(self.q) if keep_prepped else None
+
+    @property
+    def kv(self):
+        return self.k_hat, self.v_hat
+
+    def prep_kv(self, stream=None):
+        kvq_train_kv_prep(self.lay, self.n_blocks, self.offs, self.n_rows, self.k, self.v, self.k_w, self.k_hat,
+                          self.v_hat, stream)
+
+    def attend(self, stream=None):
+        attn_train_forward(self.lay, self.n_blocks, self.offs, self.n_rows, self.max_rows, self.q, self.q_w,
+                           self.k_hat, self.v_hat, self.out, self.out_f32, self.q_prepped, self.ws, self.ws_bytes,
+                           stream)
+
+    def step(self, stream=None):
+        if self.donor:
+            self.prep_kv(stream)
+        self.attend(stream)
+
+    def status_word(self) -> int:
+        return int(self.ws[:4].cpu().numpy().view(np.uint32)[0])
+
+
+class TrainStackCase:
+    """The training forward's reads over the 42-layer stack for one packed
+    sequence: donors 0..23 prep their keys and values and attend, layers
+    24..41 attend the keys and values of the last donor of their type (as the
+    donors hand theirs to their sharers)."""
+
+    def __init__(self, blocks, seed=1007, device="cuda", out_f32=True, keep_prepped=(), name="train-stack"):
+        self.layers = []
+        donors = {}
+        for i in range(W.N_LAYERS):
+            spec = W.FULL_KEQV if W.stack_layer_kind(i) == "full" else W.SLIDING
+            wl = W.TrainWorkload(f"{name}-layer{i}", seed, spec, list(blocks))
+            d = W.stack_cache_layer(i)
+            kv = None if i < W.N_DONORS else donors[d].kv
+            case = TrainCase(wl, device, out_f32=out_f32, keep_prepped=i in keep_prepped, kv=kv, layer_id=i)
+            if i < W.N_DONORS:
+                donors[i] = case
+            self.layers.append((i, d, case))
+        self.n_rows = int(sum(blocks))
+
+    def step(self, stream=None):
+        for _, _, case in self.layers:
+            case.step(stream)

@@ -26,7 +26,8 @@ static const any_fn kAll[] = {
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
     (any_fn)&attn_decode_static,     (any_fn)&kvq_static_status,
-    (any_fn)&kvq_selftest_wait_timeout,
+    (any_fn)&kvq_selftest_wait_timeout, (any_fn)&kvq_train_kv_prep,
+    (any_fn)&attn_train_forward,     (any_fn)&attn_train_workspace_bytes,
     (any_fn)&kvq_status_string,      (any_fn)&kvq_last_error,
     (any_fn)&kvq_version,
 };
@@ -72,7 +73,12 @@ int main(void) {
   CHECK(kvq_selftest_wait_timeout(NULL, 1000000, NULL) == KVQ_EINVAL);
   CHECK(kvq_static_status(NULL, NULL) == KVQ_EINVAL);
   CHECK((KVQ_STATUS_WAIT_TIMEOUT & KVQ_STATUS_SEQ_SKIPPED) == 0);
+  CHECK(attn_train_workspace_bytes(&L, 100) == 256 + 100u * 8u * 256u * 2u);
+  CHECK(attn_train_forward(&L, 0, fake_offsets, 4, 4, NULL, NULL, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) ==
+        KVQ_EINVAL);
+  CHECK(kvq_train_kv_prep(&L, 1, NULL, 4, NULL, NULL, NULL, NULL, NULL, NULL) == KVQ_EINVAL);
   /* nothing to do is not an error */
+  CHECK(kvq_train_kv_prep(&L, 1, fake_offsets, 0, NULL, NULL, NULL, NULL, NULL, NULL) == KVQ_OK);
   CHECK(kv_quant_append(&L, NULL, 0, NULL, NULL, 0, NULL, NULL, NULL, NULL, NULL) == KVQ_OK);
   printf("all checks passed\n");
   return 0;

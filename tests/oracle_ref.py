@@ -147,3 +147,18 @@ def expect_edge(bits: int) -> SeqExpect:
     n = len(names)
     empty = np.zeros((0, 1, EDGE_SPEC.head_dim))
     return SeqExpect(cache, np.arange(0), empty, empty, np.arange(n), q_hat, k_hat, v_hat, outs)
+
+
+def expect_train(wl: W.TrainWorkload, layer_id: int = 0, rows=None, kv=None):
+    """The training read of one layer over the packed sequence of `wl`:
+    (k_hat, v_hat, q_hat, {row: out [Hq, D]}).  kv = (k_hat, v_hat) of a donor
+    makes it a KV-sharing layer's read (no prep of its own)."""
+    spec = oracle_layer(wl.layer)
+    T = wl.n_rows
+    inp = W.layer_inputs(wl.seed, layer_id, wl.layer, T, T)
+    f = O.bf16_to_f64
+    off = wl.offsets()
+    if kv is None:
+        kv = O.train_kv(spec, f(inp["k"]), None if inp["v"] is None else f(inp["v"]), f(inp["k_w"]), off)
+    q_hat, outs = O.train_attend(spec, f(inp["q"]), f(inp["q_w"]), kv[0], kv[1], off, rows=rows)
+    return kv[0], kv[1], q_hat, outs

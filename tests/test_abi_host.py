@@ -183,6 +183,46 @@ def test_bad_selftest_arguments(m):
     assert g(P + 2, None) == 1                    # status misaligned
 
 
+def test_bad_training_arguments(m):
+    lay = _layer(m)
+    L = ctypes.byref(lay)
+    f = m.lib.attn_train_forward
+    need = m.attn_train_workspace_bytes(lay, 100)
+    assert need == 256 + 100 * 8 * 256 * 2
+    big = 1 << 40
+    ok = (L, 2, P, 100, 60, P, P, P, P, P, 1, None, P, big, None)
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a1=0) == 1                                    # no block
+    assert call(a1=65536) == 1
+    assert call(a2=None) == 1                                 # block_offsets NULL
+    assert call(a3=1 << 24) == 1                              # rows past the position range
+    assert call(a4=0) == 1 and call(a4=101) == 1              # max_block_rows out of [1, n_rows]
+    assert call(a5=P + 8) == 1                                # q_raw not 16-aligned
+    assert call(a7=P + 2) == 1 and call(a8=P + 2) == 1        # k_hat, v_hat not 16-aligned
+    assert call(a9=P + 2) == 1                                # f32 out misaligned
+    assert call(a10=2) == 1                                   # out_is_f32 not 0/1
+    assert call(a12=P + 16) == 1                              # workspace not 256-aligned
+    assert call(a13=need - 1) == 4                            # workspace too small
+    rot = _layer(m, rot_signs=P)
+    assert f(ctypes.byref(rot), *ok[1:]) == 2                 # no rotated training read
+    g3 = _layer(m, n_q_heads=6, n_kv_heads=2)
+    assert f(ctypes.byref(g3), *ok[1:]) == 2                  # 3 q heads per kv head do not divide 128
+    assert call(a3=0) == 0                                    # no rows: nothing to do
+    p = m.lib.kvq_train_kv_prep
+    assert p(L, 2, P, 100, P, P, P, P + 2, P, None) == 1      # k_hat misaligned
+    assert p(L, 2, P, 100, P, None, P, P, P, None) == 1       # v_raw missing
+    keqv = _layer(m, k_eq_v=True)
+    assert p(ctypes.byref(keqv), 2, P, 100, P, P, P, P, P, None) == 1   # v_raw given with K = V
+    assert p(ctypes.byref(rot), 2, P, 100, P, P, P, P, P, None) == 2
+    assert p(L, 2, None, 100, P, P, P, P, P, None) == 1
+    assert p(L, 2, P, 0, P, P, P, P, P, None) == 0
+
+
 def test_plain_c_program(m, tmp_path):
     """include/kvq.h compiles as pedantic C11 and a C program links libkvq.so,
     resolves every declared function and gets the documented host-side
