@@ -307,10 +307,43 @@ def build_workload(name: str, rank: int, device):
                 "dominant": f"prefill_tc_kernel<{spec.head_dim}> (tcgen05)", "launches": 1 + 2,
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
+    if name == "train42":
+        sliding, _ = W.workload_train_prefix_shared()
+        blocks = sliding.blocks
+        case = harness.TrainStackCase(blocks, seed=sliding.seed, device=device, out_f32=False)
+        calls = [(i < W.N_DONORS, c) for i, _, c in case.layers]
+        flops = sum(4 * c.spec.n_q_heads * c.spec.head_dim * train_visible_total(blocks, c.spec.window)
+                    for _, c in calls)
+        info = {"tokens": case.n_rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
+                "dominant": "train_tc_kernel<256|512> with its q prep (tcgen05)", "launches": 24 + 42 * 2,
+                "config": {"workload": "training forward's stateless read over the 42-layer stack, one packed "
+                                       f"sequence of {case.n_rows} rows: a prefix of {blocks[0]} rows shared by "
+                                       f"{len(blocks) - 1} branches of {blocks[1]} (block-sparse mask), sliding "
+                                       "8q/2kv D256 W512 + full 16q/1kv D512 K=V; plain bf16 keys and values",
+                           "rows": case.n_rows, "layers": 42, "kv_donor_layers": 24,
+                           "l2": "keys and values of a layer (<= 8 MB) are L2-resident"}}
+        return case, calls, info
     raise SystemExit(f"unknown workload {name}")
 
 
-METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)"}
+def train_visible_total(blocks, window: int) -> int:
+    """Keys read by all rows of a prefix-shared layout: a prefix row t reads
+    the prefix up to itself, a branch row j the prefix and its branch up to
+    position P + j (windowed on sliding layers)."""
+    P = blocks[0]
+    total = 0
+    for t in range(P):
+        total += t + 1 - (max(0, t - window + 1) if window > 0 else 0)
+    for L in blocks[1:]:
+        for j in range(L):
+            lp = P + j
+            lo = max(0, lp - window + 1) if window > 0 else 0
+            total += max(0, P - lo) + (lp - max(lo, P) + 1)
+    return total
+
+
+METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)",
+          "train42": "training-read tokens/s"}
 
 
 def step_calls(calls, stream=None):
@@ -444,7 +477,7 @@ def roofline(workload, info, res, peaks):
     if not dom_ms:
         return None
     n_calls = max(1, len(res["full_calls"]))
-    if workload == "prefill":
+    if workload in ("prefill", "train42"):
         achieved = info["flops"] / (dom_ms / 1e3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None,
@@ -546,7 +579,7 @@ def run_gpu(args):
         # the long-context and tensor-core workloads, timed in the same run
         torch.cuda.empty_cache()
         cfg["sub_results"] = {name: sub_result(name, K, args.warmup, device, peaks)
-                              for name in ("full32k", "full32k-rot", "prefill")}
+                              for name in ("full32k", "full32k-rot", "prefill", "train42")}
     line = {"metric": METRIC.get(args.workload, "decode-attention tokens/s"),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -714,7 +747,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
                     choices=["stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot", "prefill",
-                             "mixed"])
+                             "mixed", "train42"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-results", action="store_true",

@@ -356,6 +356,10 @@ class TrainCase:
                            self.k_hat, self.v_hat, self.out, self.out_f32, self.q_prepped, self.ws, self.ws_bytes,
                            stream)
 
+    def append(self, stream=None):
+        """The donor's part of a step (the name the step drivers use)."""
+        self.prep_kv(stream)
+
     def step(self, stream=None):
         if self.donor:
             self.prep_kv(stream)

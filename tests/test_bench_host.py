@@ -6,6 +6,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -102,3 +103,14 @@ def test_warmup_below_three_is_refused():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
                        capture_output=True, text=True, cwd=ROOT, timeout=120)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_training_read_key_count_matches_the_oracle():
+    """The flop count of the training-read workload counts exactly the keys
+    the oracle's layout lets every row read."""
+    import oracle as O
+    for blocks in ([37, 20, 0, 9], [0, 5, 64], [70]):
+        off = np.concatenate([[0], np.cumsum(blocks)])
+        for window in (0, 1, 5, 100):
+            want = sum(len(O.train_visible(off, r, window)) for r in range(int(off[-1])))
+            assert bench.train_visible_total(blocks, window) == want
