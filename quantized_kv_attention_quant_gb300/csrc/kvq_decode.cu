@@ -979,8 +979,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   }
   int hpb = 1, nblk = 1;
   qprep_shape<D>(a.L.n_q, hpb, nblk);
-  qprep_kernel<D, false><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH),
-                            a.L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(a, f, hpb);
+  qprep_kernel<D><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH),
+                     a.L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(a, f, hpb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   cudaLaunchAttribute attr[1];

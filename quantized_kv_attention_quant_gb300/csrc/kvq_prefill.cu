@@ -31,6 +31,7 @@
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "kvq_qprep.cuh"
+#include "kvq_qrows.cuh"
 #include "kvq_tc.cuh"
 
 #include <algorithm>
@@ -504,10 +505,7 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
   }
   const int per_sm = 512 / Pf<D>::TMEM_COLS;
   const int launch_smem = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);
-  int hpb = 1, nblk = 1;
-  qprep_shape<D>(a.L.n_q, hpb, nblk);
-  qprep_kernel<D, true><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH), 0, st>>>(a, f, hpb);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_qprep_rows<D>(a, f, st)) != cudaSuccess) return e;
   const int TQ = kRows / a.L.G;
   if (a.n_seqs > 65535 || a.L.n_kv > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, a.L.n_kv);

@@ -50,17 +50,15 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs& a, int row) {
 }
 
 // ----------------------------------------------------------------------------
-// q prep: one block per (row, block of heads).  The block first evaluates
-// the row's RoPE angles once for all its heads (the float-float sine/cosine
-// is the costly part), then each head's TH threads of E elements RMS-normalise
-// and rotate it.  Outputs:
-//   ROWS = false (decode): the mma.sync A fragments of every head slot of the
-//     row's kv heads (slots >= G are zeros) and the bias-term fragment; each
-//     32-bit fragment word holds two dims of ONE head, so heads write
-//     disjoint words.
-//   ROWS = true (prompt chunk): q_hat as f16 rows and per-group sums of
-//     those f16 values; (training read) q_hat as bf16 rows.
-// Both write q_hat (bf16) to q_prepped when it is given.
+// q prep of the decode kernels: one block per (row, block of heads), laid
+// out for latency (few rows per call).  The block first evaluates the row's
+// RoPE angles once for all its heads (the float-float sine/cosine is the
+// costly part), then each head's TH threads of E elements RMS-normalise and
+// rotate it.  Outputs: the mma.sync A fragments of every head slot of the
+// row's kv heads (slots >= G are zeros) and the bias-term fragment (each
+// 32-bit fragment word holds two dims of ONE head, so heads write disjoint
+// words), and q_hat (bf16) in q_prepped when it is given.  Calls with many
+// rows use qprep_rows_kernel (kvq_qrows.cuh).
 // ----------------------------------------------------------------------------
 template <int D>
 struct Qp {
@@ -78,7 +76,7 @@ inline void qprep_shape(int n_q, int& hpb, int& nblk) {
   nblk = (n_q + hpb - 1) / hpb;
 }
 
-template <int D, bool ROWS>
+template <int D>
 __global__ void __launch_bounds__(1024)
 qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   using Q = Qp<D>;
@@ -190,20 +188,6 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
 #pragma unroll
       for (int i = 0; i < E; ++i) dst[i] = y[i];
     }
-  }
-  if constexpr (ROWS) {
-    if (active && a.ws.qhat) {
-      uint16_t* dst = a.ws.qhat + ((size_t)row * a.L.n_q + hq) * D + tt * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i) dst[i] = y[i];
-    }
-    if (active && a.ws.q16) {
-      __half* dst = reinterpret_cast<__half*>(a.ws.q16) + ((size_t)row * a.L.n_q + hq) * D + tt * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i) dst[i] = __float2half_rn(bf16_to_f(y[i]));
-      if (tt % Q::TPG == 0) a.ws.qsum[((size_t)row * a.L.n_q + hq) * NG + tt / Q::TPG] = gs;
-    }
-    return;
   }
   __syncthreads();                         // q_hat and the group sums complete
   if (!active) return;

@@ -1,0 +1,156 @@
+// q prep for calls with many query rows (prompt chunks on the tensor cores,
+// the training read): q RMSNorm and RoPE (model.ts attentionTraining: qNorm,
+// then RoPE at the row's position), the same arithmetic as qprep_kernel in
+// kvq_qprep.cuh, laid out for throughput instead of latency:
+//   - a block of 8 warps takes `rb` consecutive rows; it stages the rotary
+//     frequencies once and evaluates every (row, pair) angle of its rows once,
+//     spread over all its threads;
+//   - each warp then preps one (row, q head) at a time, D/32 elements per
+//     lane: the float-float sum of squares is a warp reduction (no block
+//     barrier), the rotation partners come from a per-warp shared row.
+// Outputs: q_hat as bf16 (q_prepped and/or ws.qhat) and, for the prompt
+// kernel, q_hat as f16 with the per-group sums of those f16 values (ws.q16,
+// ws.qsum).  Rotated layers do not come here.
+#pragma once
+#include <algorithm>
+
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+#include "kvq_qprep.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kQrWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kQrWarps * 32)
+qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
+  constexpr int E = D / 32;                 // elements per lane
+  constexpr int NG = D / 64, LPG = 64 / E;  // 64-dim groups; lanes per group
+  extern __shared__ __align__(16) uint8_t qr_smem[];
+  __shared__ int rpos[16];
+  const int R = a.L.rope_dims, half = R >> 1, Hq = a.L.n_q;
+  float4* cs = reinterpret_cast<float4*>(qr_smem);                        // [rb][half] (cos, sin) pairs
+  float (*freq)[3] = reinterpret_cast<float (*)[3]>(qr_smem + (size_t)rb * half * 16);
+  uint16_t* nrm = reinterpret_cast<uint16_t*>(qr_smem + (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row0 = blockIdx.x * rb;
+  if (blockIdx.x == 0 && tid == 0) *a.ws.status = 0u;    // the first kernel of the call
+
+  float wq[E];                                          // (the weights are only 2-byte aligned)
+#pragma unroll
+  for (int i = 0; i < E; ++i) wq[i] = bf16_to_f(__ldg(a.q_w + lane * E + i));
+  // ---- the rows' rotation angles, once per (row, pair) ----
+  if (R > 0) {
+    if (tid < rb) {
+      const int row = row0 + tid;
+      rpos[tid] = row < a.n_rows ? min(max(row_info(a, row).p, 0), (1 << 24) - 1) : 0;
+    }
+    stage_freqs(freqs.f, half, freq);
+    __syncthreads();
+    for (int idx = tid; idx < rb * half; idx += kQrWarps * 32) {
+      const int r = idx / half, j = idx - r * half;
+      ff cc, sn;
+      rope_cos_sin(rpos[r], freq[j][0], freq[j][1], freq[j][2], cc, sn);
+      cs[idx] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+    }
+    __syncthreads();
+  }
+
+  // ---- one (row, q head) per warp at a time ----
+  uint16_t* nr = nrm + warp * D;
+  for (int it = warp; it < rb * Hq; it += kQrWarps) {
+    const int r = it / Hq, hq = it - r * Hq;
+    const int row = row0 + r;
+    if (row >= a.n_rows) break;                         // later items are later rows
+    const size_t base = ((size_t)row * Hq + hq) * D + lane * E;
+    float x[E];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.q_raw + base);
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const uint32_t u = src[i / 2];
+      x[i] = bf16lo_to_f(u);
+      x[i + 1] = bf16hi_to_f(u);
+    }
+    ff ss = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
+    ss = ff_warp_sum(ss);
+    const ff inv = rms_inv(ss, D, a.L.eps);
+    uint16_t y[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) y[i] = norm_scale_bf16(x[i], wq[i], inv);
+    if (R > 0) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) nr[lane * E + i] = y[i];
+      __syncwarp();
+      const float4* csr = cs + r * half;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int e = lane * E + i;
+        if (e < R) {
+          const int j = e < half ? e : e - half;
+          const float4 cv = csr[j];
+          const ff cc = {cv.x, cv.y};
+          y[i] = e < half ? rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w})
+                          : rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
+        }
+      }
+      __syncwarp();                                     // the row is read before the next item writes it
+    }
+    uint32_t yw[E / 2];
+#pragma unroll
+    for (int i = 0; i < E; i += 2) yw[i / 2] = (uint32_t)y[i] | ((uint32_t)y[i + 1] << 16);
+    if (a.q_prepped) {                                  // (only 2-byte alignment is asked of it)
+      if ((reinterpret_cast<uintptr_t>(a.q_prepped) & 3u) == 0) {
+        uint32_t* d = reinterpret_cast<uint32_t*>(a.q_prepped + base);
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) d[i] = yw[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) a.q_prepped[base + i] = y[i];
+      }
+    }
+    if (a.ws.qhat) {
+      uint32_t* d = reinterpret_cast<uint32_t*>(a.ws.qhat + base);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) d[i] = yw[i];
+    }
+    if (a.ws.q16) {
+      uint32_t* d = reinterpret_cast<uint32_t*>(a.ws.q16 + base);
+      float gs = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; i += 2) {
+        const __half2 h = __floats2half2_rn(bf16_to_f(y[i]), bf16_to_f(y[i + 1]));
+        const float2 hf = __half22float2(h);
+        gs += hf.x + hf.y;                              // the f16 values the MMA multiplies
+        d[i / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+#pragma unroll
+      for (int m = 1; m < LPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
+      if (lane % LPG == 0) a.ws.qsum[((size_t)row * Hq + hq) * NG + lane / LPG] = gs;
+    }
+  }
+}
+
+// rows per block: enough (row, head) items for the 8 warps, angle tables of
+// at most 16 KB
+inline int qprep_rows_rb(const LayerArgs& L) {
+  int rb = std::max(1, std::min(16, 32 / L.n_q));
+  const int half = L.rope_dims / 2;
+  if (half > 0) rb = std::max(1, std::min(rb, 1024 / half));
+  return rb;
+}
+
+template <int D>
+cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
+  const int rb = qprep_rows_rb(a.L);
+  const int half = a.L.rope_dims / 2;
+  const size_t smem = (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * D * 2;
+  qprep_rows_kernel<D><<<(a.n_rows + rb - 1) / rb, kQrWarps * 32, smem, st>>>(a, f, rb);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace kvq

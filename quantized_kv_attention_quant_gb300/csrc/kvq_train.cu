@@ -38,6 +38,7 @@
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "kvq_qprep.cuh"
+#include "kvq_qrows.cuh"
 #include "kvq_tc.cuh"
 
 #include <cuda.h>
@@ -472,10 +473,7 @@ cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint
   qa.q_prepped = q_prepped;
   qa.ws.status = status;
   qa.ws.qhat = qhat;
-  int hpb = 1, nblk = 1;
-  qprep_shape<D>(L.n_q, hpb, nblk);
-  qprep_kernel<D, true><<<dim3(t.n_rows, nblk), dim3(hpb * Qp<D>::TH), 0, st>>>(qa, f, hpb);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_qprep_rows<D>(qa, f, st)) != cudaSuccess) return e;
   if (t.n_blocks > 65535 || L.n_kv * Tr<D>::NSPLIT > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_block_rows + TQ - 1) / TQ, t.n_blocks, L.n_kv * Tr<D>::NSPLIT);
   train_tc_kernel<D><<<grid, kThreads, smem, st>>>(t, status, mq, mk, mv);
