@@ -7,7 +7,8 @@
 //     spread over all its threads;
 //   - each warp then preps one (row, q head) at a time, D/32 elements per
 //     lane: the float-float sum of squares is a warp reduction (no block
-//     barrier), the rotation partners come from a per-warp shared row.
+//     barrier); the rotated dims (rope_dims of them, a share of the row under
+//     partial RoPE) are spread over all 32 lanes through a per-warp shared row.
 // Outputs: q_hat as bf16 (q_prepped and/or ws.qhat) and, for the prompt
 // kernel, q_hat as f16 with the per-group sums of those f16 values (ws.q16,
 // ws.qsum).  Rotated layers do not come here.
@@ -34,6 +35,7 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
   float4* cs = reinterpret_cast<float4*>(qr_smem);                        // [rb][half] (cos, sin) pairs
   float (*freq)[3] = reinterpret_cast<float (*)[3]>(qr_smem + (size_t)rb * half * 16);
   uint16_t* nrm = reinterpret_cast<uint16_t*>(qr_smem + (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4));
+  // per warp: the normed row, then the rotated dims
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * rb;
   if (blockIdx.x == 0 && tid == 0) *a.ws.status = 0u;    // the first kernel of the call
@@ -59,7 +61,8 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
   }
 
   // ---- one (row, q head) per warp at a time ----
-  uint16_t* nr = nrm + warp * D;
+  uint16_t* nr = nrm + warp * 2 * D;
+  uint16_t* rt = nr + D;
   for (int it = warp; it < rb * Hq; it += kQrWarps) {
     const int r = it / Hq, hq = it - r * Hq;
     const int row = row0 + r;
@@ -73,35 +76,58 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
       x[i] = bf16lo_to_f(u);
       x[i + 1] = bf16hi_to_f(u);
     }
-    ff ss = {0.f, 0.f};
+    // sum of squares in two independent float-float chains (more work in
+    // flight per warp), joined before the warp reduction
+    ff s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < E; ++i) ff_acc_sq(ss, x[i]);
-    ss = ff_warp_sum(ss);
+    for (int i = 0; i < E; i += 2) {
+      ff_acc_sq(s0, x[i]);
+      ff_acc_sq(s1, x[i + 1]);
+    }
+    const ff ss = ff_warp_sum(ff_add(s0, s1));
     const ff inv = rms_inv(ss, D, a.L.eps);
     uint16_t y[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) y[i] = norm_scale_bf16(x[i], wq[i], inv);
-    if (R > 0) {
-#pragma unroll
-      for (int i = 0; i < E; ++i) nr[lane * E + i] = y[i];
-      __syncwarp();
-      const float4* csr = cs + r * half;
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        const int e = lane * E + i;
-        if (e < R) {
-          const int j = e < half ? e : e - half;
-          const float4 cv = csr[j];
-          const ff cc = {cv.x, cv.y};
-          y[i] = e < half ? rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w})
-                          : rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
-        }
-      }
-      __syncwarp();                                     // the row is read before the next item writes it
-    }
     uint32_t yw[E / 2];
 #pragma unroll
     for (int i = 0; i < E; i += 2) yw[i / 2] = (uint32_t)y[i] | ((uint32_t)y[i + 1] << 16);
+    if (R > 0) {
+      // the normed row to shared memory; the rotated dims are then spread over
+      // all lanes (dim e = lane + 32 k), whatever share of the row they are
+      uint32_t* nw = reinterpret_cast<uint32_t*>(nr) + lane * (E / 2);
+      if constexpr (E % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < E / 2; i += 4)
+          *reinterpret_cast<uint4*>(nw + i) = make_uint4(yw[i], yw[i + 1], yw[i + 2], yw[i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) nw[i] = yw[i];
+      }
+      __syncwarp();
+      const float4* csr = cs + r * half;
+      for (int e = lane; e < R; e += 32) {
+        const int j = e < half ? e : e - half;
+        const float4 cv = csr[j];
+        const ff cc = {cv.x, cv.y};
+        rt[e] = e < half ? rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w})
+                         : rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
+      }
+      __syncwarp();
+      if (lane * E < R) {                               // this lane holds rotated dims
+#pragma unroll
+        for (int i = 0; i < E; i += 2) {
+          const int e = lane * E + i;                   // R is even: e and e + 1 on the same side
+          if (e < R) yw[i / 2] = (uint32_t)rt[e] | ((uint32_t)rt[e + 1] << 16);
+        }
+#pragma unroll
+        for (int i = 0; i < E; i += 2) {
+          y[i] = uint16_t(yw[i / 2] & 0xFFFFu);
+          y[i + 1] = uint16_t(yw[i / 2] >> 16);
+        }
+      }
+      __syncwarp();                                     // both rows read before the next item writes them
+    }
     if (a.q_prepped) {                                  // (only 2-byte alignment is asked of it)
       if ((reinterpret_cast<uintptr_t>(a.q_prepped) & 3u) == 0) {
         uint32_t* d = reinterpret_cast<uint32_t*>(a.q_prepped + base);
@@ -147,7 +173,7 @@ template <int D>
 cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
   const int rb = qprep_rows_rb(a.L);
   const int half = a.L.rope_dims / 2;
-  const size_t smem = (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * D * 2;
+  const size_t smem = (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * 2 * D * 2;
   qprep_rows_kernel<D><<<(a.n_rows + rb - 1) / rb, kQrWarps * 32, smem, st>>>(a, f, rb);
   return cudaGetLastError();
 }
