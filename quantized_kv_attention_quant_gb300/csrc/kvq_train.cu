@@ -62,18 +62,21 @@ struct Tr {
   static constexpr int NSPLIT = D / DO;                 // CTAs per row tile
   static constexpr int NG = D / 64;                     // 64-dim groups of q and K
   static constexpr int NO = DO / 64;                    // 64-dim groups of the CTA's output dims
+  static constexpr int KB = D <= 256 ? 2 : 1;           // K buffers (head_dim 512: no room for two)
+  static constexpr bool VSTAGE = D <= 256;              // V copied into a stage, then transposed apart
   // byte offsets from the 1024-aligned base
   static constexpr int Q_OFF = 0;                       // NG blocks [128 rows x 128 B]: q as bf16
-  static constexpr int K_OFF = Q_OFF + NG * 16384;      // NG blocks [64 keys x 128 B]: K as bf16
-  static constexpr int V_OFF = K_OFF + NG * 8192;       // NO blocks [64 keys x 128 B] of V (bf16), then
-                                                        // [DO dims x 128 B]: V^T as f16, in place
-  static constexpr int C_OFF = V_OFF + NO * 8192;       // 5 mbarriers and the tensor-memory address
-  static constexpr int BYTES = C_OFF + 64 + 1024;       // + room to align the base
+  static constexpr int K_OFF = Q_OFF + NG * 16384;      // KB x NG blocks [64 keys x 128 B]: K as bf16
+  static constexpr int V_OFF = K_OFF + KB * NG * 8192;  // [DO dims x 128 B]: V^T as f16 (in place of V
+                                                        // when there is no stage)
+  static constexpr int VS_OFF = V_OFF + NO * 8192;      // stage: NO blocks [64 keys x 128 B] of V (bf16)
+  static constexpr int C_OFF = VS_OFF + (VSTAGE ? NO * 8192 : 0);   // mbarriers, tensor-memory address
+  static constexpr int BYTES = C_OFF + 128 + 1024;      // + room to align the base
   // tensor-memory columns
   static constexpr int C_O = 0;                         // output accumulator, DO columns
-  static constexpr int C_S = DO;                        // scores, 64 columns
-  static constexpr int C_P = DO + 64;                   // P as f16 pairs, 32 columns (A of PV)
-  static constexpr int C_X = DO + 96;                   // row exchange, one column per share
+  static constexpr int C_S = DO;                        // two score slots of 64 columns
+  static constexpr int C_P = DO + 128;                  // P as f16 pairs, 32 columns (A of PV)
+  static constexpr int C_X = DO + 160;                  // row exchange, one column per share
   static constexpr int TMEM_COLS = C_X + kNQ <= 256 ? 256 : 512;
 };
 
@@ -85,12 +88,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
 // two bf16 values -> the same two values as f16 (round to nearest)
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) { return pack_h2(bf16lo_to_f(w), bf16hi_to_f(w)); }
 
+// the 16 softmax warps' own barrier (the MMA warp does not take part)
+__device__ __forceinline__ void softmax_sync() { named_bar(1, kThreads); }
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads + 32, 1)
 train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUtensorMap tmq,
                 const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using T = Tr<D>;
-  constexpr int NG = T::NG, NO = T::NO, DO = T::DO;
+  constexpr int NG = T::NG, NO = T::NO, DO = T::DO, KB = T::KB;
   constexpr float L2E = 1.4426950408889634f;
   constexpr float kSlack = 8.f;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -113,26 +119,17 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
   const int rows_b = off1 - off0;
   if (t0 >= rows_b) return;
   const int base = b == 0 ? 0 : P;                        // position of the block's first row
+  // mbarriers: q, K[2], V, S[2] (QK done), Sfree[2] (scores read), PV ready, O (PV done)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::C_OFF);
   uint64_t* bar_q = bars;
   uint64_t* bar_k = bars + 1;
-  uint64_t* bar_v = bars + 2;
-  uint64_t* bar_s = bars + 3;
-  uint64_t* bar_o = bars + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + T::C_OFF + 48);
+  uint64_t* bar_v = bars + 3;
+  uint64_t* bar_s = bars + 4;
+  uint64_t* bar_sfree = bars + 6;
+  uint64_t* bar_pv = bars + 8;
+  uint64_t* bar_o = bars + 9;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + T::C_OFF + 96);
   const uint32_t sbase = smem_u32(sm);
-
-  // ---- this thread's row and share ----
-  const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
-  constexpr int DPT = DO / kNQ;                           // output dims per thread
-  const int tq = r / G, h = r % G;
-  const int t = t0 + tq;
-  const bool row_valid = t < rows_b;
-  const int lp_r = base + t;                              // the row's position
-  const int lo_r = W > 0 ? lp_r - W + 1 : -(1 << 30);     // its oldest visible position
-  const int hq = kvh * G + h;
-  const int kk0 = kKPT * hf;
-  const int dd0 = DPT * hf;
 
   // ---- the keys of the CTA: the prefix segment, then its own block's ----
   const int t_last = min(t0 + TQ, rows_b) - 1;
@@ -154,230 +151,285 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
       pk_end = off0 + (bl_hi - P) + 1;
     }
   };
-
-  // 16-byte stores when the output allows them
-  const bool out_vec = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
-  auto write_row = [&](const float* v, int d0) {          // 16 values at dims d0..d0+15
-    const size_t oi = (((size_t)off0 + t) * a.L.n_q + hq) * D + d0;
-    if (!out_vec) {
+  auto issue_k = [&](int i) {                             // one thread: K rows of tile i
+    int pk0, lp0, pk_end;
+    tile_at(i, pk0, lp0, pk_end);
+    uint64_t* bk = bar_k + (i % KB);
+    mbar_arrive_expect_tx(bk, NG * 8192);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (a.out_f32) reinterpret_cast<float*>(a.out)[oi + i] = v[i];
-        else reinterpret_cast<uint16_t*>(a.out)[oi + i] = f_to_bf16_rn(v[i]);
-      }
-    } else if (a.out_f32) {
-      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi);
+    for (int g = 0; g < NG; ++g)
+      tc::tma_load_3d(sbase + T::K_OFF + ((i % KB) * NG + g) * 8192, &tmk, 64 * g, kvh, pk0, smem_u32(bk));
+  };
+  auto issue_v = [&](int i) {                             // one thread: V rows (the CTA's dims) of tile i
+    int pk0, lp0, pk_end;
+    tile_at(i, pk0, lp0, pk_end);
+    mbar_arrive_expect_tx(bar_v, NO * 8192);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    } else {
-      uint32_t w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = (uint32_t)f_to_bf16_rn(v[2 * i]) | ((uint32_t)f_to_bf16_rn(v[2 * i + 1]) << 16);
-      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + oi);
-      o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
+    for (int j = 0; j < NO; ++j)
+      tc::tma_load_3d(sbase + (T::VSTAGE ? T::VS_OFF : T::V_OFF) + j * 8192, &tmv, d_base + 64 * j, kvh, pk0,
+                      smem_u32(bar_v));
   };
 
-  // ---- setup: barriers, tensor memory, q and the first tile's copies ----
+  // ---- setup ----
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_k, 1);
+    mbar_init(bar_k + 1, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_s + 1, 1);
+    mbar_init(bar_sfree, kThreads / 32);
+    mbar_init(bar_sfree + 1, kThreads / 32);
+    mbar_init(bar_pv, 1);
+    mbar_init(bar_o, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
     tc::tmem_alloc(tslot, T::TMEM_COLS);
     tc::tmem_relinquish();
   }
-  auto issue_k = [&](int i) {                             // thread 0
-    int pk0, lp0, pk_end;
-    tile_at(i, pk0, lp0, pk_end);
-    mbar_arrive_expect_tx(bar_k, NG * 8192);
-#pragma unroll
-    for (int g = 0; g < NG; ++g)
-      tc::tma_load_3d(sbase + T::K_OFF + g * 8192, &tmk, 64 * g, kvh, pk0, smem_u32(bar_k));
-  };
-  auto issue_v = [&](int i) {                             // thread 0
-    int pk0, lp0, pk_end;
-    tile_at(i, pk0, lp0, pk_end);
-    mbar_arrive_expect_tx(bar_v, NO * 8192);
-#pragma unroll
-    for (int j = 0; j < NO; ++j)
-      tc::tma_load_3d(sbase + T::V_OFF + j * 8192, &tmv, d_base + 64 * j, kvh, pk0, smem_u32(bar_v));
-  };
   tc::fence_before_sync();
   __syncthreads();                                        // barriers initialised, tensor memory address written
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_q, NG * 16384);
-#pragma unroll
-    for (int g = 0; g < NG; ++g)
-      tc::tma_load_3d(sbase + T::Q_OFF + g * 16384, &tmq, 64 * g, kvh * G, off0 + t0, smem_u32(bar_q));
-    issue_k(0);
-    issue_v(0);
-  }
-
-  float m_ref = -INFINITY, l_part = 0.f;
-  int ph_q = 0, ph_k = 0, ph_v = 0, ph_s = 0, ph_o = 0;
   bool dead = false;
-  auto wait = [&](uint64_t* bar, int& ph) {
-    if (!dead && !mbar_wait(bar, ph)) {
+  auto wait = [&](uint64_t* bar, int parity) {
+    if (!dead && !mbar_wait(bar, parity)) {
       dead = true;
       flag_error(status, KVQ_DEV_TIMEOUT);
     }
-    ph ^= 1;
   };
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 64);
-  constexpr uint32_t ID_PV = tc::idesc_f16_f32(128, DO);
-  if (tid == 0) wait(bar_q, ph_q);                        // only the MMA issuer reads q
 
-  for (int ti = 0; ti < n_tiles; ++ti) {
-    int pk0, lp0, pk_end;
-    tile_at(ti, pk0, lp0, pk_end);
-    if (tid == 0) {
-      wait(bar_k, ph_k);
-      tc::fence_after_sync();
+  if (warp == kThreads / 32) {
+    // ================= the MMA warp: copies of q and K, QK and PV =================
+    const bool leader = lane == 0;
+    constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 64);
+    constexpr uint32_t ID_PV = tc::idesc_f16_f32(128, DO);
+    if (leader) {
+      mbar_arrive_expect_tx(bar_q, NG * 16384);
 #pragma unroll
       for (int g = 0; g < NG; ++g)
+        tc::tma_load_3d(sbase + T::Q_OFF + g * 16384, &tmq, 64 * g, kvh * G, off0 + t0, smem_u32(bar_q));
+      issue_k(0);
+      if (KB == 2 && n_tiles > 1) issue_k(1);
+      if (!T::VSTAGE) issue_v(0);
+    }
+    __syncwarp();
+    wait(bar_q, 0);
+    auto issue_pv = [&](int i) {                          // P(i) and V^T(i) are ready
+      wait(bar_pv, i & 1);
+      tc::fence_after_sync();
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_f16(tmem + T::C_S, tc::desc_kmajor_sw128(sbase + T::Q_OFF + g * 16384 + 32 * k, 1024),
-                      tc::desc_kmajor_sw128(sbase + T::K_OFF + g * 8192 + 32 * k, 1024), ID_QK, (g | k) != 0);
-      tc::commit(bar_s);
-    }
-    // PV(ti-1) done: the V buffer is free and the output accumulator settled
-    if (ti > 0) {
-      wait(bar_o, ph_o);
+          tc::mma_f16_ts(tmem + T::C_O, tmem + T::C_P + 8 * k,
+                         tc::desc_kmajor_sw128(sbase + T::V_OFF + 32 * k, 1024), ID_PV, i > 0 || k > 0);
+        tc::commit(bar_o);
+      }
+      __syncwarp();
+    };
+    for (int ti = 0; ti < n_tiles; ++ti) {
+      const int slot = ti & 1, kb = ti % KB;
+      wait(bar_k + kb, (ti / KB) & 1);                    // K(ti) landed
+      if (ti >= 2) wait(bar_sfree + slot, ((ti - 2) >> 1) & 1);   // scores of ti-2 read
       tc::fence_after_sync();
-      if (tid == 0) issue_v(ti);
-    }
-    wait(bar_s, ph_s);
-    tc::fence_after_sync();
-    if (tid == 0 && ti + 1 < n_tiles) issue_k(ti + 1);   // QK(ti) has read K
-    __syncwarp();                                         // the warp-wide tensor-memory loads below
-
-    // ---- scores of this thread's kKPT keys ----
-    float S[kKPT];
-    tc::ld_x16(lane_base + T::C_S + kk0, S);
-    tc::wait_ld();
-    const int lpk = lp0 + kk0, pkk = pk0 + kk0;
-    float mt = -INFINITY;
-    if (__all_sync(0xffffffffu, row_valid && lpk >= lo_r && lpk + kKPT - 1 <= lp_r && pkk + kKPT - 1 < pk_end)) {
+      if (leader) {
 #pragma unroll
-      for (int j = 0; j < kKPT; ++j) mt = fmaxf(mt, S[j]);
-    } else {
+        for (int g = 0; g < NG; ++g)
 #pragma unroll
-      for (int j = 0; j < kKPT; ++j) {
-        const bool vis = row_valid && lpk + j >= lo_r && lpk + j <= lp_r && pkk + j < pk_end;
-        S[j] = vis ? S[j] : -INFINITY;
-        mt = fmaxf(mt, S[j]);
+          for (int k = 0; k < 4; ++k)
+            tc::mma_f16(tmem + T::C_S + 64 * slot,
+                        tc::desc_kmajor_sw128(sbase + T::Q_OFF + g * 16384 + 32 * k, 1024),
+                        tc::desc_kmajor_sw128(sbase + T::K_OFF + (kb * NG + g) * 8192 + 32 * k, 1024), ID_QK,
+                        (g | k) != 0);
+        tc::commit(bar_s + slot);
+      }
+      __syncwarp();
+      if (ti > 0) issue_pv(ti - 1);
+      // K buffer kb is free once QK(ti) is done: the tile KB ahead goes there
+      if (ti + KB < n_tiles) {
+        wait(bar_s + slot, (ti >> 1) & 1);
+        if (leader) issue_k(ti + KB);
+        __syncwarp();
+      }
+      // no V stage: V(ti) replaces V^T(ti-1) once PV(ti-1) is done
+      if (!T::VSTAGE && ti > 0) {
+        wait(bar_o, (ti - 1) & 1);
+        if (leader) issue_v(ti);
+        __syncwarp();
       }
     }
-    // the row's maximum over its kNQ shares, through tensor memory
-    tc::st_x1(lane_base + T::C_X + hf, mt);
+    issue_pv(n_tiles - 1);
+  } else {
+    // ================= the softmax warps =================
+    const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
+    constexpr int DPT = DO / kNQ;                         // output dims per thread
+    const int tq = r / G, h = r % G;
+    const int t = t0 + tq;
+    const bool row_valid = t < rows_b;
+    const int lp_r = base + t;                            // the row's position
+    const int lo_r = W > 0 ? lp_r - W + 1 : -(1 << 30);   // its oldest visible position
+    const int hq = kvh * G + h;
+    const int kk0 = kKPT * hf;
+    const int dd0 = DPT * hf;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    if (T::VSTAGE && tid == 0) issue_v(0);
+    float m_ref = -INFINITY, l_part = 0.f;
+    for (int ti = 0; ti < n_tiles; ++ti) {
+      const int slot = ti & 1;
+      int pk0, lp0, pk_end;
+      tile_at(ti, pk0, lp0, pk_end);
+      wait(bar_s + slot, (ti >> 1) & 1);                  // QK(ti) done
+      tc::fence_after_sync();
+      __syncwarp();
+      float S[kKPT];
+      tc::ld_x16(lane_base + T::C_S + 64 * slot + kk0, S);
+      tc::wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree + slot);       // this warp's share of the slot is read
+      const int lpk = lp0 + kk0, pkk = pk0 + kk0;
+      float mt = -INFINITY;
+      if (__all_sync(0xffffffffu, row_valid && lpk >= lo_r && lpk + kKPT - 1 <= lp_r && pkk + kKPT - 1 < pk_end)) {
+#pragma unroll
+        for (int j = 0; j < kKPT; ++j) mt = fmaxf(mt, S[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKPT; ++j) {
+          const bool vis = row_valid && lpk + j >= lo_r && lpk + j <= lp_r && pkk + j < pk_end;
+          S[j] = vis ? S[j] : -INFINITY;
+          mt = fmaxf(mt, S[j]);
+        }
+      }
+      // the row's maximum over its kNQ shares, through tensor memory
+      tc::st_x1(lane_base + T::C_X + hf, mt);
+      tc::wait_st();
+      tc::fence_before_sync();
+      softmax_sync();
+      tc::fence_after_sync();
+      {
+        float xm[4];
+        tc::ld_x4(lane_base + T::C_X, xm);
+        tc::wait_ld();
+        mt = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3]));
+      }
+      const bool renew = mt > m_ref + kSlack;
+      const bool rescale_o = renew && m_ref != -INFINITY;
+      const float alpha = rescale_o ? exp2f((m_ref - mt) * L2E) : 1.f;
+      if (renew) {
+        l_part *= alpha;
+        m_ref = mt;
+      }
+      // PV(ti-1) done: the output is settled, P and V^T are free
+      if (ti > 0) {
+        wait(bar_o, (ti - 1) & 1);
+        tc::fence_after_sync();
+        __syncwarp();
+      }
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        for (int cc = 0; cc < DPT / 16; ++cc) {
+          float v[16];
+          tc::ld_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= alpha;
+          tc::st_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
+        }
+      }
+      // ---- P = e^(S - ref) as f16 pairs into tensor memory ----
+      {
+        uint32_t pw[kKPT / 2];
+#pragma unroll
+        for (int e = 0; e < kKPT / 2; ++e) {
+          float p0 = 0.f, p1 = 0.f;
+          if (m_ref != -INFINITY) {
+            p0 = exp2f((S[2 * e] - m_ref) * L2E);
+            p1 = exp2f((S[2 * e + 1] - m_ref) * L2E);
+          }
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          const float2 pf = __half22float2(hp);
+          l_part += pf.x + pf.y;
+          pw[e] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        tc::st_x8(lane_base + T::C_P + (kKPT / 2) * hf, pw);
+      }
+
+      // ---- V(ti) -> V^T as f16 ----
+      wait(bar_v, ti & 1);
+      __syncwarp();
+      constexpr int QPK = DO / 32;                        // groups of four 8x8 blocks per 8-key row
+      const uint32_t vsrc = sbase + (T::VSTAGE ? T::VS_OFF : T::V_OFF);
+      uint32_t vr[NO][4];
+#pragma unroll
+      for (int i = 0; i < NO; ++i) {
+        const int qd = warp * NO + i, kb8 = qd / QPK, db0 = 4 * (qd % QPK);
+        const int dch = db0 + (lane >> 3);                // 8-dim chunk of the CTA's dims
+        ldsm_x4(vsrc + (dch >> 3) * 8192 + tc::sw128_off(8 * kb8 + (lane & 7), dch & 7), vr[i]);
+      }
+      if (!T::VSTAGE) softmax_sync();                     // every V row read before any is overwritten
+#pragma unroll
+      for (int i = 0; i < NO; ++i) {
+        const int qd = warp * NO + i, kb8 = qd / QPK, db0 = 4 * (qd % QPK);
+        const int dim = 8 * (db0 + (lane >> 3)) + (lane & 7);
+        tc::stmatrix_x4_trans(sbase + T::V_OFF + tc::sw128_off(dim, kb8), bf2_to_h2(vr[i][0]),
+                              bf2_to_h2(vr[i][1]), bf2_to_h2(vr[i][2]), bf2_to_h2(vr[i][3]));
+      }
+      fence_proxy_async();
+      tc::wait_st();                                      // P and the rescaled output written
+      tc::fence_before_sync();
+      softmax_sync();
+      if (tid == 0) {
+        mbar_arrive(bar_pv);                              // PV(ti) may go
+        if (T::VSTAGE && ti + 1 < n_tiles) issue_v(ti + 1);   // the stage is read
+      }
+    }
+    wait(bar_o, (n_tiles - 1) & 1);                       // the last PV
+    tc::fence_after_sync();
+    __syncwarp();
+
+    // ---- output: O / l, each thread a quarter of its row's dims ----
+    tc::st_x1(lane_base + T::C_X + hf, l_part);
     tc::wait_st();
     tc::fence_before_sync();
-    __syncthreads();
+    softmax_sync();
     tc::fence_after_sync();
+    float l_row;
     {
-      float xm[4];
-      tc::ld_x4(lane_base + T::C_X, xm);
+      float xl[4];
+      tc::ld_x4(lane_base + T::C_X, xl);
       tc::wait_ld();
-      mt = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3]));
+      l_row = (xl[0] + xl[1]) + (xl[2] + xl[3]);
     }
-    const bool renew = mt > m_ref + kSlack;
-    const bool rescale_o = renew && m_ref != -INFINITY;
-    const float alpha = rescale_o ? exp2f((m_ref - mt) * L2E) : 1.f;
-    if (renew) {
-      l_part *= alpha;
-      m_ref = mt;
-    }
-    if (__any_sync(0xffffffffu, rescale_o)) {
-      for (int cc = 0; cc < DPT / 16; ++cc) {
-        float v[16];
-        tc::ld_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
-        tc::wait_ld();
+    const float inv = 1.f / l_row;
+    const bool out_vec = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
+    for (int cc = 0; cc < DPT / 16; ++cc) {
+      float v[16];
+      tc::ld_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
+      tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= alpha;
-        tc::st_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
-      }
-    }
-    // ---- P = e^(S - ref) as f16 pairs into tensor memory ----
-    {
-      uint32_t pw[kKPT / 2];
+      for (int i = 0; i < 16; ++i) v[i] *= inv;
+      if (!row_valid) continue;
+      const size_t oi = (((size_t)off0 + t) * a.L.n_q + hq) * D + d_base + dd0 + 16 * cc;
+      if (!out_vec) {
 #pragma unroll
-      for (int e = 0; e < kKPT / 2; ++e) {
-        float p0 = 0.f, p1 = 0.f;
-        if (m_ref != -INFINITY) {
-          p0 = exp2f((S[2 * e] - m_ref) * L2E);
-          p1 = exp2f((S[2 * e + 1] - m_ref) * L2E);
+        for (int i = 0; i < 16; ++i) {
+          if (a.out_f32) reinterpret_cast<float*>(a.out)[oi + i] = v[i];
+          else reinterpret_cast<uint16_t*>(a.out)[oi + i] = f_to_bf16_rn(v[i]);
         }
-        const __half2 hp = __floats2half2_rn(p0, p1);
-        const float2 pf = __half22float2(hp);
-        l_part += pf.x + pf.y;
-        pw[e] = *reinterpret_cast<const uint32_t*>(&hp);
+      } else if (a.out_f32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = (uint32_t)f_to_bf16_rn(v[2 * i]) | ((uint32_t)f_to_bf16_rn(v[2 * i + 1]) << 16);
+        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + oi);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      tc::st_x8(lane_base + T::C_P + (kKPT / 2) * hf, pw);
     }
-
-    // ---- V(ti) -> V^T as f16, in place ----
-    wait(bar_v, ph_v);
-    __syncwarp();
-    constexpr int QPK = DO / 32;                          // groups of four 8x8 blocks per 8-key row
-    uint32_t vr[NO][4];
-#pragma unroll
-    for (int i = 0; i < NO; ++i) {
-      const int qd = warp * NO + i, kb = qd / QPK, db0 = 4 * (qd % QPK);
-      const int dch = db0 + (lane >> 3);                  // 8-dim chunk of the CTA's dims
-      ldsm_x4(sbase + T::V_OFF + (dch >> 3) * 8192 + tc::sw128_off(8 * kb + (lane & 7), dch & 7), vr[i]);
-    }
-    __syncthreads();                                      // every V row read before any is overwritten
-#pragma unroll
-    for (int i = 0; i < NO; ++i) {
-      const int qd = warp * NO + i, kb = qd / QPK, db0 = 4 * (qd % QPK);
-      const int dim = 8 * (db0 + (lane >> 3)) + (lane & 7);
-      tc::stmatrix_x4_trans(sbase + T::V_OFF + tc::sw128_off(dim, kb), bf2_to_h2(vr[i][0]), bf2_to_h2(vr[i][1]),
-                            bf2_to_h2(vr[i][2]), bf2_to_h2(vr[i][3]));
-    }
-    fence_proxy_async();
-    tc::wait_st();                                        // P and the rescaled output written
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_f16_ts(tmem + T::C_O, tmem + T::C_P + 8 * k, tc::desc_kmajor_sw128(sbase + T::V_OFF + 32 * k, 1024),
-                       ID_PV, ti > 0 || k > 0);
-      tc::commit(bar_o);
-    }
-  }
-  wait(bar_o, ph_o);                                      // the last PV
-  tc::fence_after_sync();
-  __syncwarp();
-
-  // ---- output: O / l, each thread a quarter of its row's dims ----
-  tc::st_x1(lane_base + T::C_X + hf, l_part);
-  tc::wait_st();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  float l_row;
-  {
-    float xl[4];
-    tc::ld_x4(lane_base + T::C_X, xl);
-    tc::wait_ld();
-    l_row = (xl[0] + xl[1]) + (xl[2] + xl[3]);
-  }
-  const float inv = 1.f / l_row;
-  for (int cc = 0; cc < DPT / 16; ++cc) {
-    float v[16];
-    tc::ld_x16(lane_base + T::C_O + dd0 + 16 * cc, v);
-    tc::wait_ld();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] *= inv;
-    if (row_valid) write_row(v, d_base + dd0 + 16 * cc);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -476,7 +528,7 @@ cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint
   if ((e = launch_qprep_rows<D>(qa, f, st)) != cudaSuccess) return e;
   if (t.n_blocks > 65535 || L.n_kv * Tr<D>::NSPLIT > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_block_rows + TQ - 1) / TQ, t.n_blocks, L.n_kv * Tr<D>::NSPLIT);
-  train_tc_kernel<D><<<grid, kThreads, smem, st>>>(t, status, mq, mk, mv);
+  train_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(t, status, mq, mk, mv);
   return cudaGetLastError();
 }
 
