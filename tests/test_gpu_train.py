@@ -149,3 +149,23 @@ def test_workload_train_prefix_shared(kvq, kind):
     rows = sorted({int(x) for b in range(len(off) - 1) if off[b + 1] > off[b]
                    for x in (off[b], off[b] + 1, off[b] + 127, off[b] + 128, off[b + 1] - 1)})
     check_train(harness, wl, layer_id=5 if kind == "full" else 0, rows=rows)
+
+
+@pytest.mark.parametrize("blocks", [[1], [0, 1], [37, 0, 0], [5, 1, 1, 1]])
+def test_train_tiny_layouts(kvq, blocks):
+    """One row; a branch of one row and no prefix; a prefix whose branches are
+    all empty; one-row branches (D512 K = V and D128 window 3)."""
+    _, harness = kvq
+    for spec in (_spec(16, 1, 512, 0, 128, 1e6, True), _spec(4, 2, 128, 3, 128)):
+        check_train(harness, W.TrainWorkload("tiny", 75, spec, list(blocks)))
+
+
+def test_train_grid_larger_than_blocks(kvq):
+    """max_block_rows above every block (extra row tiles return at once)."""
+    _, harness = kvq
+    spec, blocks = TRAIN_CASES["d256-sliding-prefix"]
+    wl = W.TrainWorkload("grid", 76, spec, blocks)
+    case = harness.TrainCase(wl, keep_prepped=True)
+    case.max_rows = wl.n_rows
+    case.step()
+    verify_train(case, wl)
