@@ -20,7 +20,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
 
-SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_prefill.cu", "kvq_train.cu"]
+SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_prefill.cu", "kvq_prompt.cu", "kvq_train.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE]
 

@@ -11,6 +11,7 @@
 #include <tuple>
 
 #include "kvq_internal.h"
+#include "kvq_prompt.h"
 
 namespace {
 
@@ -114,13 +115,25 @@ kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
   } while (0)
 
 // One attention call, checked and planned, ready to launch.
+enum class Path { kDecode, kPrefillTc, kPromptTc };
 struct Prepared {
   kvq::DecodeArgs a;
   const kvq::RopeFreqs* f;
-  bool tc;
+  bool tc;              // a tensor-core path (launched first among attn_mixed's groups)
+  Path path;
+  void* workspace;
   int32_t max_rows_per_seq;
   bool empty;
 };
+
+// The path of a call: sliding-window prompt rows on the dequantize-once
+// tensor-core path, other prompt rows the tensor cores fit on the codes-in-MMA
+// tensor-core path, the rest on the decode kernels.
+Path choose_path(const kvq::LayerArgs& L, bool prompt) {
+  if (prompt && kvq::prompt_tc_supported(L)) return Path::kPromptTc;
+  if (prompt && kvq::prefill_tc_supported(L)) return Path::kPrefillTc;
+  return Path::kDecode;
+}
 
 // Every check of an attention call; enqueues nothing.
 kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
@@ -148,11 +161,14 @@ kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, 
   if (row_offsets) REQUIRE_PTR(row_offsets, "row_offsets", 4);
   if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
   if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
-  // prompt chunks whose head shape fits the tensor-core kernel take it
-  const bool tc = row_offsets != nullptr && kvq::prefill_tc_supported(L);
+  // prompt chunks whose head shape fits a tensor-core kernel take it
+  const Path path = choose_path(L, row_offsets != nullptr);
+  const bool tc = path != Path::kDecode;
   const kvq::DecodePlan plan = tc ? kvq::DecodePlan{1, 0, 0}
                                   : kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
-  const size_t need = tc ? kvq::prefill_tc_ws_bytes(n_rows, L) : kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan);
+  const size_t need = path == Path::kPromptTc ? kvq::prompt_tc_ws_bytes(n_seqs, n_rows, max_rows_per_seq, L)
+                      : path == Path::kPrefillTc ? kvq::prefill_tc_ws_bytes(n_rows, L)
+                                                 : kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan);
   if (workspace_bytes < need)
     return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
   kvq::DecodeArgs& a = p->a;
@@ -171,17 +187,26 @@ kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, 
   a.splits = plan.splits;
   a.chunk_tiles = plan.chunk_tiles;
   a.sk_ctas = plan.sk_ctas;
-  a.ws = tc ? kvq::prefill_tc_ws_carve(workspace, n_rows, L) : kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, plan);
+  if (path == Path::kPromptTc) {
+    a.ws = kvq::DecodeWs{};
+    a.ws.status = static_cast<uint32_t*>(workspace);
+  } else {
+    a.ws = tc ? kvq::prefill_tc_ws_carve(workspace, n_rows, L)
+              : kvq::decode_ws_carve(workspace, n_rows, L.n_kv, L.D, plan);
+  }
   p->f = &rope_freqs(layer->rope_theta, L.D, L.rope_dims);
   p->tc = tc;
+  p->path = path;
+  p->workspace = workspace;
   p->max_rows_per_seq = max_rows_per_seq;
   return KVQ_OK;
 }
 
 kvq_status attention_launch(const Prepared& p, cudaStream_t st) {
   if (p.empty) return KVQ_OK;
-  const cudaError_t e = p.tc ? kvq::launch_prefill_tc(p.a, *p.f, p.max_rows_per_seq, st)
-                             : kvq::launch_decode(p.a, *p.f, num_sms_current(), st);
+  const cudaError_t e = p.path == Path::kPromptTc   ? kvq::launch_prompt_tc(p.a, p.workspace, p.max_rows_per_seq, *p.f, st)
+                        : p.path == Path::kPrefillTc ? kvq::launch_prefill_tc(p.a, *p.f, p.max_rows_per_seq, st)
+                                                     : kvq::launch_decode(p.a, *p.f, num_sms_current(), st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return KVQ_OK;
 }
@@ -274,7 +299,9 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
                                     int32_t max_rows_per_seq) {
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || n_rows < 0 || max_rows_per_seq < 0) return 0;
-  if (kvq::prefill_tc_supported(L)) return kvq::prefill_tc_ws_bytes(n_rows, L);
+  const Path path = choose_path(L, true);
+  if (path == Path::kPromptTc) return kvq::prompt_tc_ws_bytes(n_seqs, n_rows, max_rows_per_seq, L);
+  if (path == Path::kPrefillTc) return kvq::prefill_tc_ws_bytes(n_rows, L);
   const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
   const kvq::DecodePlan plan = kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), false);
   return kvq::decode_ws_bytes(n_rows, L.n_kv, L.D, plan);

@@ -10,8 +10,8 @@
 //     barrier); the rotated dims (rope_dims of them, a share of the row under
 //     partial RoPE) are spread over all 32 lanes through a per-warp shared row.
 // Outputs: q_hat as bf16 (q_prepped and/or ws.qhat) and, for the prompt
-// kernel, q_hat as f16 with the per-group sums of those f16 values (ws.q16,
-// ws.qsum).  Rotated layers do not come here.
+// kernels, q_hat as f16 (ws.q16) with (when ws.qsum is given) the per-group
+// sums of those f16 values.  Rotated layers do not come here.
 #pragma once
 #include <algorithm>
 
@@ -155,7 +155,7 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
       }
 #pragma unroll
       for (int m = 1; m < LPG; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
-      if (lane % LPG == 0) a.ws.qsum[((size_t)row * Hq + hq) * NG + lane / LPG] = gs;
+      if (a.ws.qsum && lane % LPG == 0) a.ws.qsum[((size_t)row * Hq + hq) * NG + lane / LPG] = gs;
     }
   }
 }

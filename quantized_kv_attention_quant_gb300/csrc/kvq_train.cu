@@ -40,6 +40,7 @@
 #include "kvq_qprep.cuh"
 #include "kvq_qrows.cuh"
 #include "kvq_tc.cuh"
+#include "kvq_tma.cuh"
 
 #include <cuda.h>
 
@@ -441,36 +442,10 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
 
 // ---- host side ----
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 // A bf16 tensor [rows][heads][D] read in boxes of (64 dims, box_h heads,
-// box_r rows), 128-byte swizzled, rows past the end read as zeros.
+// box_r rows).
 bool bf16_rows_map(CUtensorMap* m, const void* base, int D, int heads, int rows, int box_h, int box_r) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  const cuuint32_t box[3] = {64u, (cuuint32_t)box_h, (cuuint32_t)box_r};
-  const cuuint32_t es[3] = {1u, 1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return rows_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, D, heads, rows, box_h, box_r);
 }
 
 template <int D>
