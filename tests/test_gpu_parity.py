@@ -585,6 +585,10 @@ PREFILL_TC_CASES = {
     "g8-d256": (_spec(8, 1, 256, 0, 256), [31, 140], [40, 17], [8, 4]),
     "g16-d128-norope": (_spec(16, 1, 128, 0, 0), [64, 5], [24, 8], [4, 8]),
     "g16-d64-window": (_spec(32, 2, 64, 48, 64), [90, 3], [40, 11], [8, 4]),
+    # the sliding-layer (dequantize-once) path at the other G and head_dim
+    "g1-d64-window": (_spec(2, 2, 64, 40, 64), [70, 3], [130, 9], [8, 4]),
+    "g8-d256-window": (_spec(8, 1, 256, 100, 256), [31, 140], [40, 17], [8, 4]),
+    "g16-d128-window-norope": (_spec(16, 1, 128, 30, 0), [64, 5], [24, 8], [4, 8]),
 }
 
 
