@@ -100,6 +100,7 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
   constexpr int NG = T::NG, NO = T::NO, DO = T::DO, KB = T::KB;
   constexpr float L2E = 1.4426950408889634f;
   constexpr float kSlack = 8.f;
+  constexpr float kHead = 6.f;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -314,12 +315,16 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
         tc::wait_ld();
         mt = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3]));
       }
+      // a new reference sits kHead above the tile's maximum, so that a later
+      // tile must exceed it by kSlack + kHead before the output is rescaled
+      // again (P stays below e^kSlack, the largest P after a renewal is
+      // e^-kHead, far from f16's limits at either end)
       const bool renew = mt > m_ref + kSlack;
       const bool rescale_o = renew && m_ref != -INFINITY;
-      const float alpha = rescale_o ? exp2f((m_ref - mt) * L2E) : 1.f;
+      const float alpha = rescale_o ? exp2f((m_ref - (mt + kHead)) * L2E) : 1.f;
       if (renew) {
         l_part *= alpha;
-        m_ref = mt;
+        m_ref = mt + kHead;
       }
       // PV(ti-1) done: the output is settled, P and V^T are free
       if (ti > 0) {
