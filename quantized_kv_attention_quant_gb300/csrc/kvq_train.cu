@@ -13,28 +13,30 @@
 //
 // One CTA takes 128 query rows of one block that share a kv head (128/G
 // consecutive rows times their G q heads, row r = token r / G, head r % G)
-// and DO <= 256 of the output dims (head_dim 512: two CTAs per row tile),
-// with kNQ = 4 threads per row (warps w, w + 4, w + 8, w + 12 reach the same
-// tensor-memory lanes; each takes a quarter of a tile's keys and of the
-// output dims).  It walks the keys it can see -- the prefix segment, then
-// its own block's segment -- in 64-key tiles:
-//   1. The tensor memory accelerator brings q (once), each tile's K rows (all
-//      dims) and V rows (the CTA's dims) into shared memory as bf16, in the
-//      128-byte-swizzled K-major layout the MMA reads; rows past the end of
-//      the sequence arrive as zeros.
-//   2. One thread issues QK (M = 128 rows, N = 64 keys, bf16 operands: the
-//      products of the bf16 values are exact in fp32) into tensor memory.
-//   3. Each thread reads its share of the scores, masks keys outside its row's
-//      view, exchanges the row maximum through tensor memory and writes
-//      P = e^(S - ref) as f16 into tensor memory, where ref is the row's running
-//      maximum; the output accumulator is rescaled only when a tile's maximum
-//      exceeds ref by more than 8.
-//   4. All threads transpose the V tile in place into (dims x keys) f16 rows
-//      (ldmatrix / stmatrix; bf16 -> f16 is exact for |v| in f16's normal
-//      range, and v_hat = vNorm(v) is at most sqrt(head_dim)).
-//   5. One thread issues PV (A = P from tensor memory, B = V^T, N = DO).
-// The next tile's K is loaded while the scores are formed, its V as soon as
-// PV has released the buffer.  The output is O / l per row.
+// and DO <= 256 of the output dims (head_dim 512: two CTAs per row tile).
+// It walks the keys it can see -- the prefix segment, then its own block's
+// segment -- in 64-key tiles, with two roles:
+//   - one MMA warp: the tensor memory accelerator copies of q (once) and of
+//     each tile's K rows (all dims) as bf16 in the 128-byte-swizzled K-major
+//     layout the MMA reads (rows past the end of the sequence arrive as
+//     zeros); QK (M = 128 rows, N = 64 keys, bf16 operands: the products of
+//     bf16 values are exact in fp32) into one of two score slots of tensor
+//     memory, so that the next tile's QK runs under this tile's softmax; and
+//     PV (A = P from tensor memory, B = V^T, N = DO) into the output
+//     accumulator;
+//   - 16 softmax warps, four threads per row (warps w, w + 4, w + 8, w + 12
+//     reach the same tensor-memory lanes; each takes a quarter of a tile's
+//     keys and of the output dims): mask the keys outside a row's view,
+//     exchange the row maximum through tensor memory, write P = e^(S - ref)
+//     as f16 into tensor memory (ref is a lazily renewed reference: the
+//     output is rescaled only when a tile's maximum exceeds it by more than
+//     8), and transpose the V tile, staged by the tensor memory accelerator,
+//     into (dims x keys) f16 rows (ldmatrix / stmatrix; bf16 -> f16 is exact
+//     for |v| in f16's normal range, and v_hat = vNorm(v) is at most
+//     sqrt(head_dim)).
+// Head_dim <= 256 keeps two K buffers and a V stage; head_dim 512 (128 KB of
+// q) has one K buffer and transposes V in place.  The output is O / l per
+// row.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "kvq_qprep.cuh"
