@@ -172,6 +172,25 @@ def test_bad_mixed_groups(m):
     assert "share workspace" in m.kvq_last_error()
 
 
+def test_prompt_workspace_holds_the_dequantized_window(m):
+    """Sliding layers' prompt calls keep k_hi, k_lo and v (f16) of window +
+    rows - 1 keys per sequence (whole 64-key tiles) besides q_hat as f16;
+    full layers' prompt calls keep no such scratch."""
+    lay = _layer(m)                                   # 8q/2kv, D256, window 512
+    def expect(n_seqs, n_rows, max_rows, window=512, hkv=2, hq=8, d=256):
+        ks = -(-(window + max_rows - 1) // 64) * 64
+        scratch = n_seqs * ks * hkv * d * 2
+        a256 = lambda x: (x + 255) & ~255
+        off = a256(256 + n_rows * hq * d * 2)
+        off = a256(off + scratch)
+        off = a256(off + scratch)
+        return off + scratch
+    for n_seqs, n_rows, max_rows in ((1, 1, 1), (4, 2048, 512), (3, 100, 64)):
+        assert m.attn_prefill_workspace_bytes(lay, n_seqs, n_rows, max_rows) == expect(n_seqs, n_rows, max_rows)
+    full = _layer(m, window=0)
+    assert m.attn_prefill_workspace_bytes(full, 4, 2048, 512) < expect(4, 2048, 512)
+
+
 def test_bad_selftest_arguments(m):
     f = m.lib.kvq_selftest_wait_timeout
     assert f(None, 1000000, None) == 1            # status NULL
