@@ -234,8 +234,8 @@ def whole_job_rate(tokens_per_rank_step: float, ms_local: float, steps: int, wor
 
 def build_workload(name: str, rank: int, device):
     from quantized_kv_attention_quant_gb300 import harness
-    if name == "stack42":
-        wl = W.workload_stack_decode()
+    if name in ("stack42", "stack42-e4b"):
+        wl = W.workload_stack_decode() if name == "stack42" else W.workload_stack_decode_e4b_bits()
         if rank:
             wl = W.StackWorkload(wl.name, wl.seed + 100 * rank, wl.lengths, wl.donor_bits)
         case = harness.StackCase(wl, device=device, out_f32=False)
@@ -255,7 +255,9 @@ def build_workload(name: str, rank: int, device):
                 "dominant": "decode_kernel<512> (full-attention layers)",
                 "launches": 24 + 42 * 3, "config": {
                     "workload": "42-layer mixed decode step, 64 ragged sequences (lengths U[1024,32768]), "
-                                "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64",
+                                "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64"
+                                + (" (per-donor bits from the seed)" if name == "stack42" else
+                                   " (per-donor bits of the e4b layer table: full-layer reads mostly 4-bit)"),
                     "n_seqs": wl.n_seqs, "layers": 42, "kv_donor_layers": 24}}
         return case, calls, info
     if name in ("tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot"):
@@ -369,7 +371,8 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
         step_calls(calls)                      # eager (first calls also set kernel attributes)
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=device)
-    full_calls = [c for _, c in calls if c.spec.window == 0] if workload == "stack42" else [c for _, c in calls]
+    full_calls = ([c for _, c in calls if c.spec.window == 0] if workload.startswith("stack42")
+                  else [c for _, c in calls])
 
     def ev_pair():
         return (torch.cuda.Event(enable_timing=True, external=True),
@@ -533,6 +536,8 @@ def sub_result(name, K, warmup, device, peaks):
            "clocks": res["clocks"]}
     if info["kv_bytes"]:
         out["kv_bytes_per_step"] = info["kv_bytes"]
+    if name.startswith("stack42") and res.get("dom_call_ms"):
+        out["dominant_by_bits"] = bit_split(res, peaks)
     del case, calls
     torch.cuda.empty_cache()
     return out
@@ -572,14 +577,14 @@ def run_gpu(args):
     if res.get("breakdown"):
         cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in res["breakdown"].items()}
         cfg["step_breakdown_note"] = "separate replay with events around every call (they slow it down)"
-    if args.workload == "stack42" and res.get("dom_call_ms"):
+    if args.workload.startswith("stack42") and res.get("dom_call_ms"):
         cfg["dominant_by_bits"] = bit_split(res, peaks)
     del case, calls
     if args.workload == "stack42" and world == 1 and not args.no_sub_results:
         # the long-context and tensor-core workloads, timed in the same run
         torch.cuda.empty_cache()
         cfg["sub_results"] = {name: sub_result(name, K, args.warmup, device, peaks)
-                              for name in ("full32k", "full32k-rot", "prefill", "train42")}
+                              for name in ("stack42-e4b", "full32k", "full32k-rot", "prefill", "train42")}
     line = {"metric": METRIC.get(args.workload, "decode-attention tokens/s"),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -704,10 +709,11 @@ def run_cpu_baseline(workload: str, steps: int, warmup: int):
     process per core, one sampled sequence per worker (sequences spread over
     the workload's length distribution)."""
     cores = host_cores()
-    n_all = {"stack42": 64, "tiny": 1, "sliding16": 16, "full32k": 8, "full32k-8bit": 8, "full32k-rot": 8}.get(
-        workload, 1)
+    n_all = {"stack42": 64, "stack42-e4b": 64, "tiny": 1, "sliding16": 16, "full32k": 8, "full32k-8bit": 8,
+             "full32k-rot": 8}.get(workload, 1)
     nseq = max(1, min(cores, n_all))
-    procs = nseq if workload in ("stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot") else 1
+    procs = nseq if workload in ("stack42", "stack42-e4b", "tiny", "sliding16", "full32k", "full32k-8bit",
+                                 "full32k-rot") else 1
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
@@ -746,8 +752,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
-                    choices=["stack42", "tiny", "sliding16", "full32k", "full32k-8bit", "full32k-rot", "prefill",
-                             "mixed", "train42"])
+                    choices=["stack42", "stack42-e4b", "tiny", "sliding16", "full32k", "full32k-8bit",
+                             "full32k-rot", "prefill", "mixed", "train42"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-results", action="store_true",

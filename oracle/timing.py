@@ -94,8 +94,8 @@ def build(workload: str, nseq: int, part=None):
     (i, P) keeps only the i-th of P interleaved shares of the sample."""
     def share(idx):
         return idx if part is None else idx[part[0]::part[1]]
-    if workload == "stack42":
-        wl = W.workload_stack_decode()
+    if workload in ("stack42", "stack42-e4b"):
+        wl = W.workload_stack_decode() if workload == "stack42" else W.workload_stack_decode_e4b_bits()
         idx_all = sample_indices(wl.lengths, nseq)
         idx = share(idx_all)
         units = []

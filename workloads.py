@@ -303,6 +303,20 @@ def workload_stack_decode(n_seqs: int = 64, lo: int = 1024, hi: int = 32768) -> 
     return StackWorkload("stack42-mixed-decode-64-ragged", seed, lengths, bits)
 
 
+# KV bit width of every cache-owning layer 0..23 in the e4b artifact's layer
+# table (gemma4-e4b.ts, `LAYERS`); the full-attention donors 5, 11, 17, 23
+# are 4, 8, 4, 4 bits, so the full-layer reads of a step are mostly 4-bit
+E4B_DONOR_BITS = [4, 4, 4, 8, 8, 4, 4, 4, 4, 8, 8, 8, 4, 4, 8, 4, 4, 4, 4, 4, 4, 4, 4, 4]
+
+
+def workload_stack_decode_e4b_bits() -> StackWorkload:
+    """The 42-layer step of workload_stack_decode with the per-donor bit widths
+    of the e4b layer table instead of drawn from the seed."""
+    wl = workload_stack_decode()
+    return StackWorkload("stack42-e4b-bits-decode-64-ragged", wl.seed, list(wl.lengths),
+                         {d: E4B_DONOR_BITS[d] for d in range(N_DONORS)})
+
+
 def workload_mixed_step(n_decode: int = 48, lo: int = 1024, hi: int = 8192):
     """A mixed step of one sliding layer (the 42-layer stack's sliding shape):
     a decode group of n_decode sequences with lengths uniform in [lo, hi] and
