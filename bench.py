@@ -288,13 +288,35 @@ def build_workload(name: str, rank: int, device):
                      rb_pair(spec.head_dim, pwl.bits[s]) for s in range(pwl.n_seqs)) * spec.n_kv_heads
         info = {"tokens": dwl.n_seqs + int(sum(pwl.chunk)), "kv_bytes": dec_by + win_by,
                 "dominant_bytes": dec_by + win_by,
-                "dominant": "attn_mixed call (decode group: decode_kernel<256>; window group: prefill_tc_kernel<256>)",
-                "launches": 2 + 3 + 2, "mixed": True,
+                "dominant": "attn_mixed call (decode group: decode_kernel<256>; window group: "
+                            "prompt_dequant_kernel<256> + prompt_tc_kernel<256>)",
+                "launches": 2 + 3 + 3, "mixed": True,
                 "config": {"workload": "mixed step of one sliding layer (8q/2kv D256 W512): decode group of "
                                        f"{dwl.n_seqs} sequences (lengths U[1024,8192]) + window group of 2 prompt "
                                        "chunks of 256 rows, one attn_mixed call",
                            "n_seqs": dwl.n_seqs + pwl.n_seqs, "decode_rows": dwl.n_seqs,
                            "window_rows": int(sum(pwl.chunk))}}
+        return case, [(True, case)], info
+    if name == "mixed-verify":
+        dwl, vwl = W.workload_mixed_verify()
+        case = harness.MixedCase([dwl, vwl], device=device, out_f32=False)
+        spec = dwl.layer
+        dec_by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
+                     for p, b in zip(dwl.filled, dwl.bits)) * spec.n_kv_heads
+        # every verify row reads its own window (the rows of a sequence share
+        # most of their keys, read once from HBM and again from L2)
+        ver_by = sum(sum(visible_keys(vwl.filled[s] + t, spec.window) for t in range(vwl.chunk[s])) *
+                     rb_pair(spec.head_dim, vwl.bits[s]) for s in range(vwl.n_seqs)) * spec.n_kv_heads
+        info = {"tokens": dwl.n_seqs + int(sum(vwl.chunk)), "kv_bytes": dec_by + ver_by,
+                "dominant_bytes": dec_by + ver_by,
+                "dominant": "attn_mixed call: both groups in one grouped launch of qprep_grouped_kernel<256>, "
+                            "decode_grouped_kernel<256>, combine_grouped_kernel<256>",
+                "launches": 2 + 3, "mixed": True,
+                "config": {"workload": "verify step of one sliding layer (8q/2kv D256 W512): decode group of "
+                                       f"{dwl.n_seqs} sequences + verify group of {vwl.n_seqs} sequences x "
+                                       f"{vwl.chunk[0]} drafted rows (lengths U[1024,8192]), one attn_mixed call",
+                           "n_seqs": dwl.n_seqs + vwl.n_seqs, "decode_rows": dwl.n_seqs,
+                           "window_rows": int(sum(vwl.chunk))}}
         return case, [(True, case)], info
     if name == "prefill":
         wl = W.workload_prefill_chunk()
@@ -345,6 +367,7 @@ def train_visible_total(blocks, window: int) -> int:
 
 
 METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)",
+          "mixed-verify": "mixed-step tokens/s (decode tokens + window rows)",
           "train42": "training-read tokens/s"}
 
 
@@ -753,7 +776,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
                     choices=["stack42", "stack42-e4b", "tiny", "sliding16", "full32k", "full32k-8bit",
-                             "full32k-rot", "prefill", "mixed", "train42"])
+                             "full32k-rot", "prefill", "mixed", "mixed-verify", "train42"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-results", action="store_true",

@@ -27,6 +27,8 @@
  *   - bf16 values are passed as their 16-bit patterns (uint16_t).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously; no call synchronizes the device.
+ *   - A call with no rows (n_rows == 0) enqueues nothing; its workspace,
+ *     status word included, is left as it was.
  *   - Arguments are checked on the host first; a bad argument returns a
  *     status other than KVQ_OK and enqueues nothing.  kvq_last_error()
  *     returns a message for the calling thread's last failure.
@@ -189,11 +191,16 @@ size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32
  * of the pages: prompt chunks and verify windows).  Row t of sequence s sits
  * at position p = start_pos[s] + (t - row_offsets[s]) and sees keys
  * max(0, p-window+1) .. p (0 .. p when window == 0), including the rows of
- * its own chunk up to itself.  With head_dim <= 256 and G dividing 128 the
- * rows run on the tcgen05 tensor cores, 128 (token, head) rows per block:
- * QK as on attn_decode (exact codes, fp32 per-group scale), PV on v_hat =
- * scale * code + bias rounded once to f16.  Other shapes use the attn_decode
- * kernels row by row.
+ * its own chunk up to itself.  Verify windows (max_rows_per_seq <= 16) run
+ * on the attn_decode kernels row by row.  Longer chunks with head_dim <= 256
+ * and G dividing 128 run on the tcgen05 tensor cores, 128 (token, head) rows
+ * per block.
+ * Sliding-window layers: every key the chunk sees is dequantized once into
+ * the workspace (k_hat as an f16 pair hi + lo, within ~2^-22 of k_hat; v_hat
+ * rounded once to f16), then QK and PV on those.  Full-attention layers: QK
+ * as on attn_decode (exact codes, fp32 per-group scale), PV on v_hat = scale
+ * * code + bias rounded once to f16.  Other shapes (head_dim 512, a rotated
+ * layer) use the attn_decode kernels row by row.
  *
  *   max_rows_per_seq must be >= the rows of every sequence (it sizes the grid).
  *
@@ -211,6 +218,8 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
                               void* out, int32_t out_is_f32, uint16_t* q_prepped,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes of an attn_prefill_chunk call (0 for an invalid layer or a
+ * negative count). */
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
                                     int32_t max_rows_per_seq);
 
@@ -219,9 +228,22 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
  * in its own phase, as in the mixed forward of the pages (serving-blocks.ts,
  * `#mixed`, and the Gemma `#mixed` scope: each group attends over its own
  * caches at its own positions, in decode or window mode, a verify group in
- * window mode).  A decode group is exactly the attn_decode call its
- * fields describe, a window group (prompt chunk or verify window) the
- * attn_prefill_chunk call.  The groups run concurrently on the GPU.
+ * window mode).  A decode group computes the attn_decode call its fields
+ * describe, a window group (prompt chunk or verify window) the
+ * attn_prefill_chunk call.
+ *
+ * Schedule: the groups the decode kernels serve -- decode groups, verify
+ * windows (at most 16 rows per sequence) and window groups of head shapes no
+ * tensor-core kernel takes -- run as ONE grouped launch of each decode-path
+ * kernel (q prep, attention, merge), whose grids cover the rows of all of
+ * them; each group keeps its own caches, bit widths, positions, q, output and
+ * workspace (its status word included), and its keys are cut into its own
+ * fixed chunks of a split plan shared by all groups (so its outputs can
+ * differ from the separate call's in the last bits, within the attention
+ * tolerance).  A group whose workspace holds not even one split of that plan
+ * runs on its own.  Prompt chunks on the tensor cores run beside the grouped
+ * launch, concurrently on the GPU.  attn_mixed_schedule (below) reports which
+ * groups a call would group.
  *
  *   groups      host array of n_groups descriptors (below), 0 <= n_groups <=
  *               KVQ_MAX_MIXED_GROUPS
@@ -257,6 +279,16 @@ typedef struct {
 
 kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
                       const uint16_t* q_norm_w, int32_t out_is_f32, void* stream);
+
+/*
+ * attn_mixed_schedule -- every check and plan of the same attn_mixed call,
+ * with nothing enqueued (host only, no device access): on KVQ_OK,
+ * *grouped_mask has bit i set for each group i that would run in the grouped
+ * launch (0 when fewer than two groups share it).  Returns what attn_mixed
+ * would return for its checks; grouped_mask must not be NULL.
+ */
+kvq_status attn_mixed_schedule(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
+                               const uint16_t* q_norm_w, int32_t out_is_f32, uint32_t* grouped_mask);
 
 /*
  * The training forward's stateless read (trainable.ts, trainingCaches and

@@ -76,6 +76,8 @@ def _load():
     lib.attn_prefill_workspace_bytes.restype = sz
     lib.attn_mixed.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
     lib.attn_mixed.restype = ctypes.c_int
+    lib.attn_mixed_schedule.argtypes = [lay, ctypes.POINTER(KvqAttnGroup), i32, vp, i32, vp]
+    lib.attn_mixed_schedule.restype = ctypes.c_int
     lib.kvq_train_kv_prep.argtypes = [lay, i32, vp, i32, vp, vp, vp, vp, vp, vp]
     lib.kvq_train_kv_prep.restype = ctypes.c_int
     lib.attn_train_forward.argtypes = [lay, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
@@ -231,6 +233,16 @@ def attn_mixed(layer: KvqLayer, groups, q_norm_w, out_is_f32, stream=None):
     arr = (KvqAttnGroup * max(1, len(groups)))(*groups)
     _check(lib.attn_mixed(ctypes.byref(layer), arr, len(groups), _ptr(q_norm_w), int(out_is_f32),
                           _stream(stream)))
+
+
+def attn_mixed_schedule(layer: KvqLayer, groups, q_norm_w, out_is_f32) -> int:
+    """Bit i set: group i of this attn_mixed call would run in the grouped
+    decode-kernel launch (see include/kvq.h).  Host only."""
+    arr = (KvqAttnGroup * max(1, len(groups)))(*groups)
+    mask = ctypes.c_uint32(0)
+    _check(lib.attn_mixed_schedule(ctypes.byref(layer), arr, len(groups), _ptr(q_norm_w), int(out_is_f32),
+                                   ctypes.byref(mask)))
+    return mask.value
 
 
 def kvq_selftest_wait_timeout(status, limit_ns, stream=None):

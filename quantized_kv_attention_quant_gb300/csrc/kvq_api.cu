@@ -1,5 +1,6 @@
 // C ABI of libkvq.so: argument checks, rotary frequency tables, launches.
 // The operations and their page citations are documented in include/kvq.h.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -122,16 +123,28 @@ struct Prepared {
   bool tc;              // a tensor-core path (launched first among attn_mixed's groups)
   Path path;
   void* workspace;
+  size_t workspace_bytes;
   int32_t max_rows_per_seq;
+  int32_t max_keys;     // the decode plan's bound on keys per row
+  bool fixed_chunks;
   bool empty;
 };
 
+// Windows of at most this many rows per sequence (verify windows) are read
+// by the decode kernels row by row.  Measured on GB300 (16 sequences of a
+// sliding layer, 8q/2kv D256 W512, lengths 1k-8k): the tensor-core prompt
+// path takes 42-44 us for 1..16 rows per sequence, the decode kernels 4-33 us
+// more than a 48-sequence decode group alone; at 32 rows the tensor cores win
+// (46 us against 75 us).
+constexpr int kRowPathWindowRows = 16;
+
 // The path of a call: sliding-window prompt rows on the dequantize-once
 // tensor-core path, other prompt rows the tensor cores fit on the codes-in-MMA
-// tensor-core path, the rest on the decode kernels.
-Path choose_path(const kvq::LayerArgs& L, bool prompt) {
-  if (prompt && kvq::prompt_tc_supported(L)) return Path::kPromptTc;
-  if (prompt && kvq::prefill_tc_supported(L)) return Path::kPrefillTc;
+// tensor-core path, verify windows and the rest on the decode kernels.
+Path choose_path(const kvq::LayerArgs& L, bool prompt, int max_rows_per_seq) {
+  if (!prompt || max_rows_per_seq <= kRowPathWindowRows) return Path::kDecode;
+  if (kvq::prompt_tc_supported(L)) return Path::kPromptTc;
+  if (kvq::prefill_tc_supported(L)) return Path::kPrefillTc;
   return Path::kDecode;
 }
 
@@ -162,7 +175,7 @@ kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, 
   if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
   if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
   // prompt chunks whose head shape fits a tensor-core kernel take it
-  const Path path = choose_path(L, row_offsets != nullptr);
+  const Path path = choose_path(L, row_offsets != nullptr, max_rows_per_seq);
   const bool tc = path != Path::kDecode;
   const kvq::DecodePlan plan = tc ? kvq::DecodePlan{1, 0, 0}
                                   : kvq::decode_plan(L, n_rows, max_keys, num_sms_current(), fixed_chunks);
@@ -198,7 +211,10 @@ kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, 
   p->tc = tc;
   p->path = path;
   p->workspace = workspace;
+  p->workspace_bytes = workspace_bytes;
   p->max_rows_per_seq = max_rows_per_seq;
+  p->max_keys = max_keys;
+  p->fixed_chunks = fixed_chunks;
   return KVQ_OK;
 }
 
@@ -299,7 +315,7 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
                                     int32_t max_rows_per_seq) {
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || n_rows < 0 || max_rows_per_seq < 0) return 0;
-  const Path path = choose_path(L, true);
+  const Path path = choose_path(L, true, max_rows_per_seq);
   if (path == Path::kPromptTc) return kvq::prompt_tc_ws_bytes(n_seqs, n_rows, max_rows_per_seq, L);
   if (path == Path::kPrefillTc) return kvq::prefill_tc_ws_bytes(n_rows, L);
   const int32_t max_keys = layer->window > 0 ? layer->window : (1 << 24);
@@ -308,12 +324,121 @@ size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int3
 }
 
 // ---------------------------------------------------------------------------
-// attn_mixed: the groups of one layer checked together, then forked from the
-// caller's stream onto library streams and joined back.
+// attn_mixed: the groups of one layer checked together; the groups the
+// decode kernels serve run as one grouped launch, every other group on its
+// own kernels, forked from the caller's stream onto library streams and
+// joined back.
 // ---------------------------------------------------------------------------
 }  // extern "C"
 
 namespace {
+
+// Everything attn_mixed does before it enqueues: every group checked and
+// planned (p), the members of the grouped launch (member) and, when two or
+// more groups share it, its arguments (*ga non-null).
+struct MixedPlan {
+  Prepared p[KVQ_MAX_MIXED_GROUPS];
+  bool member[KVQ_MAX_MIXED_GROUPS];
+  kvq::GroupedDecode ga_buf;
+  kvq::GroupedDecode* ga;
+  const kvq::RopeFreqs* gf;
+};
+
+kvq_status mixed_prepare(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
+                         const uint16_t* q_norm_w, int32_t out_is_f32, MixedPlan* mp) {
+  Prepared* p = mp->p;
+  bool* member = mp->member;
+  mp->ga = nullptr;
+  mp->gf = nullptr;
+  if (n_groups < 0 || n_groups > KVQ_MAX_MIXED_GROUPS)
+    return fail(KVQ_EINVAL, "n_groups %d not in [0, %d]", n_groups, KVQ_MAX_MIXED_GROUPS);
+  if (n_groups == 0) return KVQ_OK;
+  if (!groups) return fail(KVQ_EINVAL, "groups is NULL");
+  for (int i = 0; i < n_groups; ++i) {
+    const kvq_attn_group& g = groups[i];
+    kvq_status st;
+    if (g.phase == KVQ_PHASE_DECODE) {
+      if (!max_pos_ok(g.max_pos)) return fail(KVQ_EINVAL, "group %d: max_pos %d not in [0, 2^24)", i, g.max_pos);
+      st = attention_prepare(layer, g.seqs, g.n_seqs, nullptr, g.pos, g.n_seqs, g.max_pos + 1, true, 0, g.q_raw,
+                             q_norm_w, g.out, out_is_f32, g.q_prepped, g.workspace, g.workspace_bytes, &p[i]);
+    } else if (g.phase == KVQ_PHASE_WINDOW) {
+      if (g.n_rows > 0 && !g.row_offsets) return fail(KVQ_EINVAL, "group %d: row_offsets is NULL", i);
+      if (g.max_rows_per_seq < 1 && g.n_rows > 0) return fail(KVQ_EINVAL, "group %d: max_rows_per_seq < 1", i);
+      const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
+      st = attention_prepare(layer, g.seqs, g.n_seqs, g.row_offsets, g.pos, g.n_rows, max_keys, false,
+                             g.max_rows_per_seq, g.q_raw, q_norm_w, g.out, out_is_f32, g.q_prepped, g.workspace,
+                             g.workspace_bytes, &p[i]);
+    } else {
+      return fail(KVQ_EINVAL, "group %d: phase %d is neither decode nor window", i, g.phase);
+    }
+    if (st != KVQ_OK) {
+      g_last_error = "group " + std::to_string(i) + ": " + g_last_error;
+      return st;
+    }
+  }
+  for (int i = 0; i < n_groups; ++i)
+    for (int j = 0; j < i; ++j) {
+      if (p[i].empty || p[j].empty) continue;
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(groups[i].workspace), a1 = a0 + groups[i].workspace_bytes;
+      const uintptr_t b0 = reinterpret_cast<uintptr_t>(groups[j].workspace), b1 = b0 + groups[j].workspace_bytes;
+      if (a0 < b1 && b0 < a1) return fail(KVQ_EINVAL, "groups %d and %d share workspace memory", j, i);
+    }
+  // The grouped schedule: every group the decode kernels serve (decode
+  // groups, verify windows, window groups of shapes the tensor-core kernels
+  // do not take) runs in ONE launch of each decode-path kernel -- q prep,
+  // attention, merge -- whose grids cover all of them, each group with its own
+  // sequences, positions, bits, q, output and workspace.  A group whose
+  // workspace cannot hold even one split of the shared plan runs on its own.
+  int n_member = 0;
+  for (int i = 0; i < n_groups; ++i) {
+    member[i] = !p[i].empty && !p[i].tc;
+    n_member += member[i];
+  }
+  const kvq::LayerArgs* Lg = nullptr;
+  for (int i = 0; i < n_groups; ++i)
+    if (member[i]) Lg = &p[i].a.L;
+  while (n_member >= 2) {
+    int idx[KVQ_MAX_MIXED_GROUPS], rows[KVQ_MAX_MIXED_GROUPS], mk[KVQ_MAX_MIXED_GROUPS], cap[KVQ_MAX_MIXED_GROUPS];
+    bool fx[KVQ_MAX_MIXED_GROUPS];
+    int n = 0;
+    for (int i = 0; i < n_groups; ++i)
+      if (member[i]) {
+        idx[n] = i;
+        rows[n] = p[i].a.n_rows;
+        mk[n] = p[i].max_keys;
+        fx[n] = p[i].fixed_chunks;
+        cap[n] = kvq::decode_max_splits(rows[n], Lg->n_kv, Lg->D, p[i].workspace_bytes);
+        ++n;
+      }
+    bool dropped = false;
+    for (int k = 0; k < n; ++k)
+      if (cap[k] < 1) {
+        member[idx[k]] = false;
+        --n_member;
+        dropped = true;
+      }
+    if (dropped) continue;
+    kvq::DecodePlan plans[KVQ_MAX_MIXED_GROUPS];
+    kvq::decode_plan_grouped(*Lg, n, rows, mk, fx, cap, num_sms_current(), plans);
+    kvq::GroupedDecode* ga = &mp->ga_buf;
+    *ga = kvq::GroupedDecode{};
+    ga->n = n;
+    mp->ga = ga;
+    mp->gf = p[idx[0]].f;
+    for (int k = 0; k < n; ++k) {
+      kvq::DecodeArgs a = p[idx[k]].a;
+      a.splits = plans[k].splits;
+      a.chunk_tiles = plans[k].chunk_tiles;
+      a.sk_ctas = 0;
+      a.ws = kvq::decode_ws_carve(p[idx[k]].workspace, rows[k], a.L.n_kv, a.L.D, plans[k]);
+      ga->g[k] = a;
+      ga->row_base[k + 1] = ga->row_base[k] + rows[k];
+      ga->cta_base[k + 1] = ga->cta_base[k] + rows[k] * a.L.n_kv * a.splits;
+    }
+    break;
+  }
+  return KVQ_OK;
+}
 
 struct MixedPool {
   cudaStream_t s[KVQ_MAX_MIXED_GROUPS];
@@ -357,55 +482,33 @@ extern "C" {
 
 kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
                       const uint16_t* q_norm_w, int32_t out_is_f32, void* stream) {
-  if (n_groups < 0 || n_groups > KVQ_MAX_MIXED_GROUPS)
-    return fail(KVQ_EINVAL, "n_groups %d not in [0, %d]", n_groups, KVQ_MAX_MIXED_GROUPS);
-  if (n_groups == 0) return KVQ_OK;
-  if (!groups) return fail(KVQ_EINVAL, "groups is NULL");
-  Prepared p[KVQ_MAX_MIXED_GROUPS];
-  for (int i = 0; i < n_groups; ++i) {
-    const kvq_attn_group& g = groups[i];
-    kvq_status st;
-    if (g.phase == KVQ_PHASE_DECODE) {
-      if (!max_pos_ok(g.max_pos)) return fail(KVQ_EINVAL, "group %d: max_pos %d not in [0, 2^24)", i, g.max_pos);
-      st = attention_prepare(layer, g.seqs, g.n_seqs, nullptr, g.pos, g.n_seqs, g.max_pos + 1, true, 0, g.q_raw,
-                             q_norm_w, g.out, out_is_f32, g.q_prepped, g.workspace, g.workspace_bytes, &p[i]);
-    } else if (g.phase == KVQ_PHASE_WINDOW) {
-      if (g.n_rows > 0 && !g.row_offsets) return fail(KVQ_EINVAL, "group %d: row_offsets is NULL", i);
-      if (g.max_rows_per_seq < 1 && g.n_rows > 0) return fail(KVQ_EINVAL, "group %d: max_rows_per_seq < 1", i);
-      const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
-      st = attention_prepare(layer, g.seqs, g.n_seqs, g.row_offsets, g.pos, g.n_rows, max_keys, false,
-                             g.max_rows_per_seq, g.q_raw, q_norm_w, g.out, out_is_f32, g.q_prepped, g.workspace,
-                             g.workspace_bytes, &p[i]);
-    } else {
-      return fail(KVQ_EINVAL, "group %d: phase %d is neither decode nor window", i, g.phase);
-    }
-    if (st != KVQ_OK) {
-      g_last_error = "group " + std::to_string(i) + ": " + g_last_error;
-      return st;
-    }
-  }
-  for (int i = 0; i < n_groups; ++i)
-    for (int j = 0; j < i; ++j) {
-      if (p[i].empty || p[j].empty) continue;
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(groups[i].workspace), a1 = a0 + groups[i].workspace_bytes;
-      const uintptr_t b0 = reinterpret_cast<uintptr_t>(groups[j].workspace), b1 = b0 + groups[j].workspace_bytes;
-      if (a0 < b1 && b0 < a1) return fail(KVQ_EINVAL, "groups %d and %d share workspace memory", j, i);
-    }
-  // Launch order: the library streams' groups are enqueued first and the
-  // caller's stream's group last.  Window groups on the tensor cores go first:
+  static thread_local MixedPlan mp;
+  const kvq_status pst = mixed_prepare(layer, groups, n_groups, q_norm_w, out_is_f32, &mp);
+  if (pst != KVQ_OK || n_groups == 0) return pst;
+  const Prepared* p = mp.p;
+  const bool* member = mp.member;
+  const kvq::GroupedDecode* ga = mp.ga;
+  // Launch order: the library streams' units are enqueued first and the
+  // caller's stream's unit last.  Window groups on the tensor cores go first:
   // their one-wave grids of one CTA per SM then get the SMs, and the short,
   // latency-bound decode kernels fill in around them.  (Measured on GB300, a
   // 48-sequence decode group beside two 256-row prompt chunks of a sliding
   // layer: 0.078 ms per step this way, 0.090 with the decode group first,
-  // 0.087 as separate calls.)
-  int live[KVQ_MAX_MIXED_GROUPS], n_live = 0;
+  // 0.087 as separate calls.)  Unit -1 is the grouped launch.
+  int live[KVQ_MAX_MIXED_GROUPS + 1], n_live = 0;
+  if (ga) live[n_live++] = -1;
   for (int i = 0; i < n_groups; ++i)
-    if (!p[i].empty && !p[i].tc) live[n_live++] = i;
+    if (!p[i].empty && !p[i].tc && !(ga && member[i])) live[n_live++] = i;
   for (int i = 0; i < n_groups; ++i)
-    if (!p[i].empty && p[i].tc) live[n_live++] = i;
+    if (!p[i].empty && p[i].tc && !(ga && member[i])) live[n_live++] = i;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto launch_unit = [&](int u, cudaStream_t s) -> kvq_status {
+    if (u >= 0) return attention_launch(p[u], s);
+    const cudaError_t le = kvq::launch_decode_grouped(*ga, *mp.gf, s);
+    return le == cudaSuccess ? KVQ_OK : cuda_fail(le, "attn_mixed: grouped launch");
+  };
   if (n_live == 0) return KVQ_OK;
-  if (n_live == 1) return attention_launch(p[live[0]], st);
+  if (n_live == 1) return launch_unit(live[0], st);
   MixedPool* pool = mixed_pool();
   if (!pool) return KVQ_ECUDA;
   cudaError_t e = cudaEventRecord(pool->fork, st);
@@ -421,19 +524,33 @@ kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int3
       break;
     }
     forked = k;
-    const kvq_status ls = attention_launch(p[live[k]], pool->s[k]);
+    const kvq_status ls = launch_unit(live[k], pool->s[k]);
     if (ls != KVQ_OK) {
       result = ls;
       break;
     }
   }
-  if (result == KVQ_OK) result = attention_launch(p[live[0]], st);
+  if (result == KVQ_OK) result = launch_unit(live[0], st);
   for (int k = 1; k <= forked; ++k) {
     e = cudaEventRecord(pool->join[k], pool->s[k]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, pool->join[k], 0);
     if (e != cudaSuccess && result == KVQ_OK) result = cuda_fail(e, "attn_mixed: join");
   }
   return result;
+}
+
+kvq_status attn_mixed_schedule(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
+                               const uint16_t* q_norm_w, int32_t out_is_f32, uint32_t* grouped_mask) {
+  if (!grouped_mask) return fail(KVQ_EINVAL, "grouped_mask is NULL");
+  static thread_local MixedPlan mp;
+  const kvq_status st = mixed_prepare(layer, groups, n_groups, q_norm_w, out_is_f32, &mp);
+  if (st != KVQ_OK) return st;
+  uint32_t m = 0;
+  if (mp.ga)
+    for (int i = 0; i < n_groups; ++i)
+      if (mp.member[i]) m |= 1u << i;
+  *grouped_mask = m;
+  return KVQ_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -636,6 +753,6 @@ const char* kvq_status_string(kvq_status s) {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }
 
-int32_t kvq_version(void) { return 120; }
+int32_t kvq_version(void) { return 130; }
 
 }  // extern "C"

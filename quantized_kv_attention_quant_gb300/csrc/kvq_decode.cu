@@ -637,9 +637,11 @@ __host__ __device__ constexpr int sk_plan_bytes(int n_rows) {
   return (((n_rows + 5) & ~1) * 4 + (int)sizeof(SkWalk) + 127) & ~127;
 }
 
+// One CTA of the attention kernel.  Fixed chunks: (bx, by, bz) = (row, kv
+// head, split) of the call `a`; stream-K: bx is the CTA's index in the wave.
 template <int D, bool SK, bool ROT>
-__global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
-decode_kernel(const DecodeArgs a, const int smem_total) {
+__device__ __forceinline__ void decode_cta(const DecodeArgs& a, const int smem_total, const int bx, const int by,
+                                           const int bz) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool sk = SK;
   const int ring_smem = sk ? smem_total - sk_plan_bytes(a.n_rows) : smem_total;
@@ -653,8 +655,8 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
   int* pr = reinterpret_cast<int*>(smem + ring_smem);        // [n_rows + 1] row tile prefix (stream-K)
   SkWalk* wk = reinterpret_cast<SkWalk*>(pr + ((a.n_rows + 5) & ~1));
   if constexpr (!SK) {
-    row = blockIdx.x; kvh = blockIdx.y;
-    const int split = blockIdx.z;
+    row = bx; kvh = by;
+    const int split = bz;
     const RowInfo ri = row_info(a, row);
     c = a.seqs[ri.s];
     const RowWin rw = row_window(a, ri, c);
@@ -718,7 +720,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
     } else {
       nc = min(nc, max(1LL, T / kSkMinTiles));
     }
-    if (blockIdx.x == 0) {
+    if (bx == 0) {
       long long* plan = a.ws.plan;
       for (int r = tid; r <= n_rows; r += NT) plan[2 + r] = pr[r];
       if (tid == 0) { plan[0] = T; plan[1] = nc; }
@@ -727,7 +729,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
         flag_error(a.ws.status, KVQ_DEV_BADSEQ);
       }
     }
-    const long long cta = blockIdx.x;
+    const long long cta = bx;
     const long long b = sk_range_start(cta, T, nc), e = sk_range_start(cta + 1, T, nc);
     if (cta >= nc || b >= e) { pdl_launch(); return; }
     if (tid == 0) {
@@ -755,7 +757,7 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
     const RowWin rw = row_window(a, ri, c);
     tr = TileRange{rw.lo / kTileKeys + s0, s1 - s0, rw.lo, rw.hi};
     final_out = s0 == 0 && s1 == t;
-    const size_t pidx = (size_t)blockIdx.x * 2 + (pu > wk->b ? 1 : 0);
+    const size_t pidx = (size_t)bx * 2 + (pu > wk->b ? 1 : 0);
     po = a.ws.part_o + pidx * 16 * D;
     ml = a.ws.part_ml + pidx * 32;
     if (threadIdx.x == 0) wk->next = pu + s1;
@@ -789,6 +791,24 @@ decode_kernel(const DecodeArgs a, const int smem_total) {
   }
 }
 
+template <int D, bool SK, bool ROT>
+__global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
+decode_kernel(const DecodeArgs a, const int smem_total) {
+  decode_cta<D, SK, ROT>(a, smem_total, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// Grouped schedule: the fixed-chunk CTAs of every group in one 1-D grid.
+template <int D, bool ROT>
+__global__ void __launch_bounds__(Dec<D>::THREADS, Dec<D>::MIN_BLOCKS)
+decode_grouped_kernel(const GroupedDecode ga, const int smem_total) {
+  const int g = group_of(ga.cta_base, ga.n, blockIdx.x);
+  const DecodeArgs& a = ga.g[g];
+  const int local = blockIdx.x - ga.cta_base[g];
+  const int per_row = a.L.n_kv * a.splits;
+  const int row = local / per_row, rem = local - row * per_row;
+  decode_cta<D, false, ROT>(a, smem_total, row, rem / a.splits, rem % a.splits);
+}
+
 // The output value of dim d = threadIdx.x of a row (blockDim == D) on a
 // rotated layer: o R^T / D = s_d (o H)_d / D, H the Sylvester Hadamard matrix,
 // by in-place butterflies in `buf` (D floats of shared memory, reused: the
@@ -815,12 +835,10 @@ __device__ __forceinline__ float unrotate_dim(float o, const int8_t* signs, floa
 // 3. merge split partials: out = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
 // ----------------------------------------------------------------------------
 template <int D, bool ROT>
-__global__ void __launch_bounds__(D)
-combine_kernel(const DecodeArgs a) {
+__device__ __forceinline__ void combine_row(const DecodeArgs& a, const int row, const int hq) {
   __shared__ float wsm[D > 256 ? D : 256];   // split weights, then (rotated layers) the output row
   __shared__ float inv_l;
   pdl_wait();
-  const int row = blockIdx.x, hq = blockIdx.y;
   const int G = a.L.G, kvh = hq / G, r = hq % G;
   const int S = a.splits;
   const size_t base = ((size_t)row * a.L.n_kv + kvh) * S;
@@ -868,6 +886,19 @@ combine_kernel(const DecodeArgs a) {
   const size_t oi = ((size_t)row * a.L.n_q + hq) * D + d;
   if (a.out_f32) reinterpret_cast<float*>(a.out)[oi] = o;
   else reinterpret_cast<uint16_t*>(a.out)[oi] = f_to_bf16_rn(o);
+}
+
+template <int D, bool ROT>
+__global__ void __launch_bounds__(D)
+combine_kernel(const DecodeArgs a) {
+  combine_row<D, ROT>(a, blockIdx.x, blockIdx.y);
+}
+
+template <int D, bool ROT>
+__global__ void __launch_bounds__(D)
+combine_grouped_kernel(const GroupedDecode ga) {
+  const int g = group_of(ga.row_base, ga.n, blockIdx.x);
+  combine_row<D, ROT>(ga.g[g], blockIdx.x - ga.row_base[g], blockIdx.y);
 }
 
 // Stream-K merge: one block per (row, q head) of a unit whose tiles were
@@ -947,6 +978,36 @@ constexpr int decode_smem_bytes() {
   return D >= 512 ? 227 * 1024 : (D == 256 ? 110 * 1024 : 56 * 1024);
 }
 
+// The shared-memory opt-in of every attention kernel of head_dim D, once per
+// device (a lock: host threads may make their first call on a device at the
+// same time).
+template <int D>
+cudaError_t decode_attrs(int smem) {
+  static std::atomic<bool> attr_set[64];
+  static std::mutex attr_mu;
+  cudaError_t e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+      const void* fns[6] = {
+          reinterpret_cast<const void*>(decode_kernel<D, false, false>),
+          reinterpret_cast<const void*>(decode_kernel<D, true, false>),
+          reinterpret_cast<const void*>(decode_kernel<D, false, true>),
+          reinterpret_cast<const void*>(decode_kernel<D, true, true>),
+          reinterpret_cast<const void*>(decode_grouped_kernel<D, false>),
+          reinterpret_cast<const void*>(decode_grouped_kernel<D, true>)};
+      for (const void* fn : fns)
+        if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+          return e;
+      attr_set[dev].store(true, std::memory_order_release);
+    }
+  }
+  return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
   static_assert(D % 64 == 0, "");
@@ -956,27 +1017,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
                 "the stream-K plan leaves two stages");
   cudaError_t e;
   const int smem = decode_smem_bytes<D>();
-  // the shared-memory opt-in, once per device (a lock: host threads may make
-  // their first call on a device at the same time)
-  static std::atomic<bool> attr_set[64];
-  static std::mutex attr_mu;
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev].load(std::memory_order_acquire)) {
-    std::lock_guard<std::mutex> lock(attr_mu);
-    if (!attr_set[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(decode_kernel<D, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(decode_kernel<D, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(decode_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(decode_kernel<D, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr_set[dev].store(true, std::memory_order_release);
-    }
-  }
+  if ((e = decode_attrs<D>(smem)) != cudaSuccess) return e;
   int hpb = 1, nblk = 1;
   qprep_shape<D>(a.L.n_q, hpb, nblk);
   qprep_kernel<D><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH),
@@ -1011,6 +1052,41 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D, false>, a)
                       : cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, a);
   return e;
+}
+
+// The grouped schedule: the same three kernels, each grid over every group.
+template <int D>
+cudaError_t launch_decode_grouped_t(const GroupedDecode& ga, const RopeFreqs& f, cudaStream_t st) {
+  cudaError_t e;
+  const int smem = decode_smem_bytes<D>();
+  if ((e = decode_attrs<D>(smem)) != cudaSuccess) return e;
+  const LayerArgs& L = ga.g[0].L;
+  const int rows = ga.row_base[ga.n], ctas = ga.cta_base[ga.n];
+  int hpb = 1, nblk = 1;
+  qprep_shape<D>(L.n_q, hpb, nblk);
+  qprep_grouped_kernel<D><<<dim3(rows, nblk), dim3(hpb * Qp<D>::TH),
+                             L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(ga, f, hpb);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(Dec<D>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = L.rot ? cudaLaunchKernelEx(&cfg, decode_grouped_kernel<D, true>, ga, smem)
+            : cudaLaunchKernelEx(&cfg, decode_grouped_kernel<D, false>, ga, smem);
+  if (e != cudaSuccess) return e;
+
+  cfg.gridDim = dim3(rows, L.n_q);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  return L.rot ? cudaLaunchKernelEx(&cfg, combine_grouped_kernel<D, true>, ga)
+               : cudaLaunchKernelEx(&cfg, combine_grouped_kernel<D, false>, ga);
 }
 
 }  // namespace
@@ -1100,6 +1176,51 @@ DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms
     plan.chunk_tiles = 0;                                   // per row: ceil(row tiles / splits)
   }
   return plan;
+}
+
+void decode_plan_grouped(const LayerArgs& L, int n, const int* rows, const int* max_keys, const bool* fixed_chunks,
+                         const int* max_splits, int num_sms, DecodePlan* plans) {
+  const int per_sm = L.D >= 512 ? 1 : (L.D == 256 ? 2 : 4);
+  long base = 0;
+  for (int g = 0; g < n; ++g) base += (long)rows[g] * L.n_kv;
+  const long wave = std::max<long>(1, ((long)num_sms * per_sm) / std::max<long>(base, 1));
+  for (int g = 0; g < n; ++g) {
+    const long full_tiles = ((long)std::max(max_keys[g], 1) - 1) / kTileKeys + 1;
+    const int tiles = int(L.window > 0 ? std::min<long>(full_tiles, (L.window + kTileKeys - 2) / kTileKeys + 1)
+                                       : full_tiles);
+    DecodePlan& p = plans[g];
+    p.sk_ctas = 0;
+    const long cap = std::max(1, std::min(max_splits[g], 256));
+    if (fixed_chunks[g]) {
+      long splits = std::max<long>(wave, (tiles + kChunkTiles - 1) / kChunkTiles);
+      splits = std::max<long>(1, std::min<long>(splits, cap));
+      const int chunk = int((tiles + splits - 1) / splits);
+      p.chunk_tiles = chunk;
+      p.splits = (tiles + chunk - 1) / chunk;
+    } else {
+      p.splits = int(std::max<long>(1, std::min<long>(std::min<long>(wave, std::max(1, tiles / 2)), cap)));
+      p.chunk_tiles = 0;
+    }
+  }
+}
+
+int decode_max_splits(int n_rows, int n_kv, int D, size_t bytes) {
+  const DecodePlan one{1, 0, 0};
+  const size_t fixed = decode_ws_bytes(n_rows, n_kv, D, one) - (size_t)n_rows * n_kv * (16 * (size_t)D * 4 + 32 * 4);
+  if (bytes < fixed) return 0;
+  const size_t per_split = (size_t)n_rows * n_kv * (16 * (size_t)D * 4 + 32 * 4);
+  return (int)std::min<size_t>((bytes - fixed) / std::max<size_t>(per_split, 1), 256);
+}
+
+cudaError_t launch_decode_grouped(const GroupedDecode& ga, const RopeFreqs& f, cudaStream_t st) {
+  if (ga.n < 1 || ga.row_base[ga.n] == 0) return cudaSuccess;
+  switch (ga.g[0].L.D) {
+    case 64: return launch_decode_grouped_t<64>(ga, f, st);
+    case 128: return launch_decode_grouped_t<128>(ga, f, st);
+    case 256: return launch_decode_grouped_t<256>(ga, f, st);
+    case 512: return launch_decode_grouped_t<512>(ga, f, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int /*num_sms*/, cudaStream_t st) {

@@ -81,6 +81,20 @@ struct DecodeArgs {
   DecodeWs ws;
 };
 
+// Several calls of one layer in one launch of each decode-path kernel (q
+// prep, attention, merge): group g's rows are rows [row_base[g],
+// row_base[g+1]) of the q prep and merge grids, its fixed-chunk CTAs
+// [cta_base[g], cta_base[g+1]) of the attention grid, in (row, kv head,
+// split) order.  Every group keeps its own arguments (sequences, positions,
+// rows, q, output, workspace, plan); the layer is the same for all.
+constexpr int kMaxGroups = KVQ_MAX_MIXED_GROUPS;
+struct GroupedDecode {
+  int n;
+  int row_base[kMaxGroups + 1];
+  int cta_base[kMaxGroups + 1];
+  DecodeArgs g[kMaxGroups];
+};
+
 constexpr int kChunkTiles = 48;   // target tiles per split when the longest row is known
 // Stream-K decode: used for decode calls whose longest row spans several
 // chunks and whose row count fits the plan held in shared memory.
@@ -90,6 +104,15 @@ struct DecodePlan { int splits, chunk_tiles, sk_ctas; };
 size_t decode_ws_bytes(int n_rows, int n_kv, int D, const DecodePlan& plan);
 DecodeWs decode_ws_carve(void* base, int n_rows, int n_kv, int D, const DecodePlan& plan);
 DecodePlan decode_plan(const LayerArgs& L, int n_rows, int max_keys, int num_sms, bool fixed_chunks);
+// Fixed-chunk plans of the groups of a grouped launch (no stream-K): one
+// wave shared by every group's (row, kv head) units.  rows, max_keys and
+// fixed_chunks per group as for decode_plan; group g takes at most
+// max_splits[g] >= 1 splits (what its workspace holds).
+void decode_plan_grouped(const LayerArgs& L, int n, const int* rows, const int* max_keys, const bool* fixed_chunks,
+                         const int* max_splits, int num_sms, DecodePlan* plans);
+// The most splits of a fixed-chunk plan whose workspace for n_rows rows fits
+// in `bytes` (0 when not even one split fits).
+int decode_max_splits(int n_rows, int n_kv, int D, size_t bytes);
 
 // Prompt chunks on the tensor cores (tcgen05): head_dim <= 256 and G | 128.
 bool prefill_tc_supported(const LayerArgs& L);
@@ -117,5 +140,7 @@ cudaError_t launch_train(const TrainArgs& t, const uint16_t* q_raw, const uint16
 // after limit_ns and flags the timeout bit in *status.
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
+// The grouped launch (fixed-chunk plans in every group, ga.n >= 1).
+cudaError_t launch_decode_grouped(const GroupedDecode& ga, const RopeFreqs& f, cudaStream_t st);
 
 }  // namespace kvq

@@ -76,9 +76,10 @@ inline void qprep_shape(int n_q, int& hpb, int& nblk) {
   nblk = (n_q + hpb - 1) / hpb;
 }
 
+// One block: row `row` of the call `a`, heads hb*hpb .. hb*hpb + hpb - 1.
 template <int D>
-__global__ void __launch_bounds__(1024)
-qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
+__device__ __forceinline__ void qprep_block(const DecodeArgs& a, const RopeFreqs& freqs, const int hpb,
+                                            const int row, const int hb) {
   using Q = Qp<D>;
   constexpr int E = Q::E, NG = D / 64, TH = Q::TH;
   __shared__ uint16_t qn[Q::HPB * D];      // normed, then q_hat, per head of the block
@@ -87,13 +88,12 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
   __shared__ ff red[Q::HPB][Q::HW];
   __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
   extern __shared__ double rot_rows[];     // [hpb][D], rotated layers only
-  const int row = blockIdx.x;
   const int tid = threadIdx.x, hl = tid / TH, tt = tid % TH, lane = tid & 31;
   // the first kernel of an attention call clears its status word; the later
   // kernels flag errors only once this grid is complete
-  if (row == 0 && blockIdx.y == 0 && tid == 0) *a.ws.status = 0u;
+  if (row == 0 && hb == 0 && tid == 0) *a.ws.status = 0u;
   pdl_launch();
-  const int hq = blockIdx.y * hpb + hl;                   // q head of this thread
+  const int hq = hb * hpb + hl;                           // q head of this thread
   const bool active = hl < hpb && hq < a.L.n_q;
   const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
   // the raw row and the norm weight first: their latency overlaps the row
@@ -235,6 +235,28 @@ qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
       if (tt < 8) qb[(rq * 4 + (tt & 3)) * 4 + reg_lo + 2 * (tt >> 2)] = 0u;
     }
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(1024)
+qprep_kernel(const DecodeArgs a, const RopeFreqs freqs, const int hpb) {
+  qprep_block<D>(a, freqs, hpb, blockIdx.x, blockIdx.y);
+}
+
+// The group of block x of a grouped grid whose groups start at base[0..n).
+__device__ __forceinline__ int group_of(const int* base, int n, int x) {
+  int g = 0;
+  for (int i = 1; i < n; ++i)
+    if (x >= base[i]) g = i;
+  return g;
+}
+
+// Grouped schedule: the rows of every group in one grid (rows, head blocks).
+template <int D>
+__global__ void __launch_bounds__(1024)
+qprep_grouped_kernel(const GroupedDecode ga, const RopeFreqs freqs, const int hpb) {
+  const int g = group_of(ga.row_base, ga.n, blockIdx.x);
+  qprep_block<D>(ga.g[g], freqs, hpb, blockIdx.x - ga.row_base[g], blockIdx.y);
 }
 
 }  // namespace

@@ -25,6 +25,7 @@ static const any_fn kAll[] = {
     (any_fn)&kv_quant_append,        (any_fn)&attn_decode,
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
+    (any_fn)&attn_mixed_schedule,
     (any_fn)&attn_decode_static,     (any_fn)&kvq_static_status,
     (any_fn)&kvq_selftest_wait_timeout, (any_fn)&kvq_train_kv_prep,
     (any_fn)&attn_train_forward,     (any_fn)&attn_train_workspace_bytes,
@@ -69,6 +70,11 @@ int main(void) {
   CHECK(attn_prefill_chunk(&bad, NULL, 1, fake_offsets, NULL, 4, 4, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) ==
         KVQ_EUNSUPPORTED);
   CHECK(attn_mixed(&L, NULL, KVQ_MAX_MIXED_GROUPS + 1, NULL, 1, NULL) == KVQ_EINVAL);
+  {
+    uint32_t mask = 7;
+    CHECK(attn_mixed_schedule(&L, NULL, 0, NULL, 1, &mask) == KVQ_OK && mask == 0);
+    CHECK(attn_mixed_schedule(&L, NULL, 0, NULL, 1, NULL) == KVQ_EINVAL);
+  }
   CHECK(attn_decode_static(&L, NULL, 1, NULL, -1, NULL, NULL, NULL, 1, NULL, NULL) == KVQ_EINVAL);
   CHECK(kvq_selftest_wait_timeout(NULL, 1000000, NULL) == KVQ_EINVAL);
   CHECK(kvq_static_status(NULL, NULL) == KVQ_EINVAL);

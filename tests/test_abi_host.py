@@ -172,10 +172,61 @@ def test_bad_mixed_groups(m):
     assert "share workspace" in m.kvq_last_error()
 
 
+def test_mixed_grouped_schedule_membership(m):
+    """attn_mixed_schedule: decode groups, verify windows (at most 16 rows
+    per sequence, read by the decode kernels) and window groups no
+    tensor-core kernel takes share the grouped launch; larger prompt chunks on
+    the tensor cores, empty groups and groups whose workspace holds no split
+    of the shared plan run on their own."""
+    big = 1 << 36
+
+    def grp(k, phase, n_seqs, n_rows=0, max_pos=0, max_rows=0, ws=big):
+        base = P + k * (1 << 40)                  # disjoint workspaces
+        return m.attn_group(phase, P, n_seqs, P if phase == m.KVQ_PHASE_WINDOW else None, P, n_rows, max_pos,
+                            max_rows, P, P, None, base, ws)
+
+    def mask(lay, groups):
+        return m.attn_mixed_schedule(lay, groups, P, 1)
+
+    D, W_ = m.KVQ_PHASE_DECODE, m.KVQ_PHASE_WINDOW
+    sliding = _layer(m)                           # 8q/2kv D256 W512: prompt chunks on the tensor cores
+    assert mask(sliding, []) == 0
+    assert mask(sliding, [grp(0, D, 48, max_pos=8000)]) == 0
+    assert mask(sliding, [grp(0, D, 48, max_pos=8000), grp(1, D, 3, max_pos=10)]) == 0b11
+    verify, chunk = grp(1, W_, 8, 32, max_rows=4), grp(2, W_, 2, 512, max_rows=256)
+    assert mask(sliding, [grp(0, D, 48, max_pos=8000), verify, chunk]) == 0b011
+    assert mask(sliding, [grp(0, D, 48, max_pos=8000), chunk]) == 0      # one member: nothing to group
+    assert mask(sliding, [verify, grp(3, W_, 4, 64, max_rows=16), chunk]) == 0b011
+    assert mask(sliding, [verify, grp(3, W_, 4, 68, max_rows=17)]) == 0  # 17 rows: the tensor cores
+    empty = grp(3, W_, 1, 0, max_rows=0)
+    assert mask(sliding, [grp(0, D, 48, max_pos=8000), empty, verify]) == 0b101
+    full = _layer(m, window=0, head_dim=512, n_q_heads=16, n_kv_heads=1, rope_dims=128)
+    # head_dim 512: every window group is read by the decode kernels
+    assert mask(full, [grp(0, D, 8, max_pos=32767), grp(1, W_, 2, 512, max_rows=256)]) == 0b11
+    # a decode group sized for its own stream-K plan: 512 rows need 512 pieces
+    # even at one split, its workspace holds 2 per stream-K CTA
+    own = m.attn_decode_workspace_bytes(full, 512, 32767)
+    wide = grp(0, D, 512, max_pos=32767, ws=own)
+    assert mask(full, [wide, grp(1, D, 8, max_pos=100), grp(2, D, 4, max_pos=50)]) == 0b110
+    assert mask(full, [wide, grp(1, D, 8, max_pos=100)]) == 0
+    assert mask(full, [grp(0, D, 512, max_pos=32767), grp(1, D, 8, max_pos=100)]) == 0b11
+    # a verify window sized by attn_prefill_workspace_bytes joins (head_dim
+    # 128, GQA 16, full causal)
+    d128 = _layer(m, window=0, head_dim=128, n_q_heads=32, n_kv_heads=2, rope_dims=64)
+    vws = m.attn_prefill_workspace_bytes(d128, 2, 18, 16)
+    assert mask(d128, [grp(0, D, 4, max_pos=4000), grp(1, W_, 2, 18, max_rows=16, ws=vws)]) == 0b11
+    assert mask(d128, [grp(0, D, 4, max_pos=4000), grp(1, W_, 2, 34, max_rows=17)]) == 0
+    # the checks of attn_mixed come first
+    with pytest.raises(RuntimeError):
+        mask(sliding, [grp(0, D, 48, max_pos=8000), grp(0, D, 3, max_pos=10)])   # shared workspace
+    assert m.lib.attn_mixed_schedule(ctypes.byref(sliding), None, 0, P, 1, None) == 1
+
+
 def test_prompt_workspace_holds_the_dequantized_window(m):
-    """Sliding layers' prompt calls keep k_hi, k_lo and v (f16) of window +
-    rows - 1 keys per sequence (whole 64-key tiles) besides q_hat as f16;
-    full layers' prompt calls keep no such scratch."""
+    """Sliding layers' prompt calls (more than 16 rows per sequence) keep
+    k_hi, k_lo and v (f16) of window + rows - 1 keys per sequence (whole
+    64-key tiles) besides q_hat as f16; full layers' prompt calls keep no such
+    scratch."""
     lay = _layer(m)                                   # 8q/2kv, D256, window 512
     def expect(n_seqs, n_rows, max_rows, window=512, hkv=2, hq=8, d=256):
         ks = -(-(window + max_rows - 1) // 64) * 64
@@ -185,8 +236,11 @@ def test_prompt_workspace_holds_the_dequantized_window(m):
         off = a256(off + scratch)
         off = a256(off + scratch)
         return off + scratch
-    for n_seqs, n_rows, max_rows in ((1, 1, 1), (4, 2048, 512), (3, 100, 64)):
+    for n_seqs, n_rows, max_rows in ((1, 17, 17), (4, 2048, 512), (3, 100, 64)):
         assert m.attn_prefill_workspace_bytes(lay, n_seqs, n_rows, max_rows) == expect(n_seqs, n_rows, max_rows)
+    # verify windows (at most 16 rows per sequence) take the decode kernels'
+    # workspace (q fragments and split partials), not the dequantized window
+    assert m.attn_prefill_workspace_bytes(lay, 1, 16, 16) not in (0, expect(1, 16, 16))
     full = _layer(m, window=0)
     assert m.attn_prefill_workspace_bytes(full, 4, 2048, 512) < expect(4, 2048, 512)
 

@@ -541,12 +541,16 @@ def test_workspace_contents_do_not_matter(kvq):
 
 def test_verify_windows(kvq):
     """Short windows of 2..64 query rows per sequence (speculative verify):
-    the same call as a prompt chunk, on the tensor-core path (D256, G 4) and
-    on the row path (D512, G 16)."""
+    the same call as a prompt chunk, on the tensor-core path (D256, G 4, a
+    sequence of more than 16 rows), on the row path (D256 with at most 16 rows
+    per sequence) and on the row path (D512, G 16)."""
     _, harness = kvq
     spec = _spec(8, 2, 256, 512, 256)
     wl = W.PrefillWorkload("verify-sliding", 84, spec, filled=[100, 700, 5, 1030], chunk=[2, 7, 33, 64],
                            bits=[4, 8, 8, 4])
+    check_prefill(harness, wl)
+    wl = W.PrefillWorkload("verify-sliding-rows", 84, spec, filled=[100, 700, 5, 1030, 511], chunk=[2, 7, 16, 1, 4],
+                           bits=[4, 8, 8, 4, 8])
     check_prefill(harness, wl)
     spec = _spec(16, 1, 512, 0, 128, 1e6, True)
     wl = W.PrefillWorkload("verify-full", 85, spec, filled=[90, 3], chunk=[5, 17], bits=[8, 4])
@@ -560,7 +564,7 @@ def test_prefill_empty_sequences(kvq):
     oracle has them."""
     _, harness = kvq
     wl = W.PrefillWorkload("empty-seqs-tc", 91, _spec(8, 2, 256, 64, 256), filled=[10, 100, 0, 7],
-                           chunk=[0, 12, 0, 5], bits=[4, 8, 8, 4])
+                           chunk=[0, 20, 0, 5], bits=[4, 8, 8, 4])
     check_prefill(harness, wl)
     wl = W.PrefillWorkload("empty-seqs-rows", 92, _spec(16, 1, 512, 0, 128, 1e6, True), filled=[30, 5, 64],
                            chunk=[3, 0, 0], bits=[8, 4, 8])
@@ -623,23 +627,45 @@ def test_prefill_bf16_output_is_rounded_f32(kvq):
 # one attn_mixed call, each group checked against the oracle on its own
 # ----------------------------------------------------------------------------
 
+# Each case: the layer, its groups, and the groups attn_mixed_schedule puts in
+# the grouped decode-kernel launch (bit i = group i).
 MIXED_CASES = {
     "sliding-decode-and-chunk": (_spec(8, 2, 256, 512, 256), [
         ("decode", [700, 40, 1500, 3], [4, 8, 8, 4]),
         ("window", [300, 0], [37, 130], [8, 4]),
-    ]),
+    ], 0b00),
     "full-keqv-two-decode-one-verify": (_spec(16, 1, 512, 0, 128, 1e6, True), [
         ("decode", [3500, 10, 900], [8, 4, 4]),
         ("window", [200, 65], [5, 64], [4, 8]),
         ("decode", [64, 4000], [8, 8]),
-    ]),
+    ], 0b111),
+    # two decode groups and a verify window grouped; the prompt chunk on the
+    # tensor cores beside them; an empty window group
+    "sliding-grouped-decode-verify-beside-chunk": (_spec(8, 2, 256, 512, 256), [
+        ("decode", [700, 40, 1500, 3, 511, 512], [4, 8, 8, 4, 8, 4]),
+        ("window", [300, 5, 0], [4, 16, 1], [8, 4, 8]),
+        ("window", [200, 0], [37, 130], [8, 4]),
+        ("decode", [64, 900, 2000], [8, 4, 4]),
+        ("window", [10], [0], [4]),
+    ], 0b01011),
+    # GQA 16 at head_dim 128, full causal: long ragged decode rows (the
+    # standalone call would take stream-K) beside verify windows
+    "d128-gqa16-grouped": (_spec(32, 2, 128, 0, 64, 1e6), [
+        ("decode", [4000, 1, 64, 2500], [8, 4, 4, 8]),
+        ("window", [3000, 63], [16, 2], [4, 8]),
+    ], 0b11),
+    # the deferred TurboQuant read: the grouped merge un-rotates every group
+    "rot-full-keqv-grouped": (dataclasses.replace(_spec(16, 1, 512, 0, 128, 1e6, True), **ROT), [
+        ("decode", [1200, 64, 3000], [4, 8, 4]),
+        ("window", [100, 700], [3, 9], [8, 4]),
+    ], 0b11),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MIXED_CASES))
 def test_mixed_groups(kvq, name):
-    _, harness = kvq
-    spec, groups = MIXED_CASES[name]
+    m, harness = kvq
+    spec, groups, grouped = MIXED_CASES[name]
     wls = []
     for i, g in enumerate(groups):
         if g[0] == "decode":
@@ -647,25 +673,30 @@ def test_mixed_groups(kvq, name):
         else:
             wls.append(W.PrefillWorkload(f"{name}-{i}", 91, spec, filled=g[1], chunk=g[2], bits=g[3]))
     case = harness.MixedCase(wls, keep_prepped=True)
+    assert m.attn_mixed_schedule(case.lay, case.groups(), case.q_w, case.out_f32) == grouped
     case.step()
     torch.cuda.synchronize()
     for c, wl in zip(case.cases, wls):
         if isinstance(wl, W.DecodeWorkload):
             worst = verify_decode(c, wl, check_fill=False)
         else:
-            assert c.status_word() == 0
+            if c.n_rows:                # a group with no rows enqueues nothing
+                assert c.status_word() == 0
             worst = verify_prefill(c, wl)
         print(name, wl.name, "worst", worst)
 
 
 def test_mixed_equals_separate_calls(kvq):
-    """The groups of one attn_mixed call give the same bytes as the separate
-    attn_decode / attn_prefill_chunk calls."""
-    _, harness = kvq
+    """Groups of an attn_mixed call that run on their own kernels (here a
+    decode group beside a prompt chunk on the tensor cores: nothing to group)
+    give the same bytes as the separate attn_decode / attn_prefill_chunk
+    calls."""
+    m, harness = kvq
     spec = _spec(8, 2, 256, 512, 256)
     wls = [W.DecodeWorkload("eq-d", 92, spec, filled=[900, 33], bits=[4, 8]),
            W.PrefillWorkload("eq-w", 92, spec, filled=[128], chunk=[70], bits=[8])]
     case = harness.MixedCase(wls)
+    assert m.attn_mixed_schedule(case.lay, case.groups(), case.q_w, case.out_f32) == 0
     case.append()
     case.attend()
     torch.cuda.synchronize()

@@ -334,6 +334,24 @@ def workload_mixed_step(n_decode: int = 48, lo: int = 1024, hi: int = 8192):
     return dec, win
 
 
+def workload_mixed_verify(n_decode: int = 48, n_verify: int = 16, rows: int = 4, lo: int = 1024,
+                          hi: int = 8192):
+    """A serving step of one sliding layer with speculative verification: a
+    decode group of n_decode sequences and a verify group of n_verify other
+    sequences, each checking `rows` drafted tokens (a window of `rows` query
+    rows); lengths uniform in [lo, hi], per-sequence bits from the seed."""
+    seed = 1008
+    g = _rng(seed, P_LEN)
+    lengths = [int(x) for x in g.integers(lo, hi + 1, size=n_decode + n_verify)]
+    gb = _rng(seed, P_BITS)
+    bits = [int(gb.choice([4, 8])) for _ in range(n_decode + n_verify)]
+    dec = DecodeWorkload(f"verify-decode-{n_decode}-ragged", seed, SLIDING, filled=lengths[:n_decode],
+                         bits=bits[:n_decode])
+    win = PrefillWorkload(f"verify-window-{n_verify}x{rows}", seed, SLIDING, filled=lengths[n_decode:],
+                          chunk=[rows] * n_verify, bits=bits[n_decode:])
+    return dec, win
+
+
 @dataclasses.dataclass
 class TrainWorkload:
     """One packed training sequence of a layer under a prefix-shared layout:
