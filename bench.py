@@ -328,7 +328,8 @@ def build_workload(name: str, rank: int, device):
             for t in range(wl.chunk[s]):
                 flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
         info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
-                "dominant": f"prefill_tc_kernel<{spec.head_dim}> (tcgen05)", "launches": 1 + 2,
+                "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05) with its q prep and key "
+                            "dequantization", "launches": 1 + 3,
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     if name == "train42":
