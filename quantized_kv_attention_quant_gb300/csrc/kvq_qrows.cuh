@@ -7,8 +7,10 @@
 //     spread over all its threads;
 //   - each warp then preps one (row, q head) at a time, D/32 elements per
 //     lane: the float-float sum of squares is a warp reduction (no block
-//     barrier); the rotated dims (rope_dims of them, a share of the row under
-//     partial RoPE) are spread over all 32 lanes through a per-warp shared row.
+//     barrier); under full RoPE the partner of element e (e +- D/2) sits in
+//     lane ^ 16 at the same index, one shuffle away; under partial RoPE the
+//     rotated dims (a share of the row) are spread over all 32 lanes through
+//     a per-warp shared row.
 // Outputs: q_hat as bf16 (q_prepped and/or ws.qhat) and, for the prompt
 // kernels, q_hat as f16 (ws.q16) with (when ws.qsum is given) the per-group
 // sums of those f16 values.  Rotated layers do not come here.
@@ -33,6 +35,8 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
   __shared__ int rpos[16];
   const int R = a.L.rope_dims, half = R >> 1, Hq = a.L.n_q;
   float4* cs = reinterpret_cast<float4*>(qr_smem);                        // [rb][half] (cos, sin) pairs
+  // under full RoPE pair j = 16 * (j % E) + j / E of a row's table: the 16
+  // lanes of a half read consecutive entries
   float (*freq)[3] = reinterpret_cast<float (*)[3]>(qr_smem + (size_t)rb * half * 16);
   uint16_t* nrm = reinterpret_cast<uint16_t*>(qr_smem + (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4));
   // per warp: the normed row, then the rotated dims
@@ -55,7 +59,7 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
       const int r = idx / half, j = idx - r * half;
       ff cc, sn;
       rope_cos_sin(rpos[r], freq[j][0], freq[j][1], freq[j][2], cc, sn);
-      cs[idx] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
+      cs[R == D ? r * half + (j % E) * 16 + j / E : idx] = make_float4(cc.hi, cc.lo, sn.hi, sn.lo);
     }
     __syncthreads();
   }
@@ -92,7 +96,20 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
     uint32_t yw[E / 2];
 #pragma unroll
     for (int i = 0; i < E; i += 2) yw[i / 2] = (uint32_t)y[i] | ((uint32_t)y[i + 1] << 16);
-    if (R > 0) {
+    if (R == D) {
+      // x_e c - x_(e+D/2) s in lanes 0..15, x_e c + x_(e-D/2) s in lanes 16..31
+      const float4* csr = cs + r * half + (lane & 15);
+      const bool upper = lane >= 16;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const float xe = bf16_to_f(y[i]);
+        const float xp = __shfl_xor_sync(0xffffffffu, xe, 16);
+        const float4 cv = csr[i * 16];
+        y[i] = rot_bf16(xe, xp, ff{cv.x, cv.y}, upper ? ff{-cv.z, -cv.w} : ff{cv.z, cv.w});
+      }
+#pragma unroll
+      for (int i = 0; i < E; i += 2) yw[i / 2] = (uint32_t)y[i] | ((uint32_t)y[i + 1] << 16);
+    } else if (R > 0) {
       // the normed row to shared memory; the rotated dims are then spread over
       // all lanes (dim e = lane + 32 k), whatever share of the row they are
       uint32_t* nw = reinterpret_cast<uint32_t*>(nr) + lane * (E / 2);
