@@ -139,6 +139,13 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
   const int kind = item & 1;             // 0: K, 1: V
   const int head = item >> 1;
 
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // until that grid is complete only the library's own frequency table is
+  // read; every caller buffer is touched after the wait.
+  if (R > 0) stage_freqs(freqs.f, half, freq);
+  pdl_wait();
+  pdl_launch();
+
   // the raw row and the norm weight first: their latency overlaps the
   // sequence lookup and the angles
   float x[E], wk[E];
@@ -179,8 +186,7 @@ append_kernel(const AppendArgs a, const RopeFreqs freqs, const int ipb) {
 
   // ---- the row's rotation angles, once for all K heads ----
   if (R > 0) {
-    stage_freqs(freqs.f, half, freq);
-    __syncthreads();
+    __syncthreads();                     // the staged frequencies
     for (int j = tid; j < half; j += blockDim.x) {
       ff cc, sn;
       rope_cos_sin(pos, freq[j][0], freq[j][1], freq[j][2], cc, sn);
@@ -258,18 +264,25 @@ cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t 
     constexpr int D = decltype(tag)::value;
     const int items = 2 * a.L.n_kv;
     const int ipb = items < App<D>::IPB ? items : App<D>::IPB;
-    const dim3 grid((unsigned)a.n_rows, (unsigned)((items + ipb - 1) / ipb));
-    const size_t dyn = a.L.rot ? (size_t)ipb * D * sizeof(double) : 0;   // rotation rows
-    append_kernel<D><<<grid, ipb * App<D>::TH, dyn, st>>>(a, f, ipb);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_rows, (unsigned)((items + ipb - 1) / ipb));
+    cfg.blockDim = dim3(ipb * App<D>::TH);
+    cfg.dynamicSmemBytes = a.L.rot ? (size_t)ipb * D * sizeof(double) : 0;   // rotation rows
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel<D>, a, f, ipb);
   };
   switch (a.L.D) {
-    case 64: go(std::integral_constant<int, 64>{}); break;
-    case 128: go(std::integral_constant<int, 128>{}); break;
-    case 256: go(std::integral_constant<int, 256>{}); break;
-    case 512: go(std::integral_constant<int, 512>{}); break;
+    case 64: return go(std::integral_constant<int, 64>{});
+    case 128: return go(std::integral_constant<int, 128>{});
+    case 256: return go(std::integral_constant<int, 256>{});
+    case 512: return go(std::integral_constant<int, 512>{});
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace kvq

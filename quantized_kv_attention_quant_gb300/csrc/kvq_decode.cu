@@ -838,6 +838,7 @@ template <int D, bool ROT>
 __device__ __forceinline__ void combine_row(const DecodeArgs& a, const int row, const int hq) {
   __shared__ float wsm[D > 256 ? D : 256];   // split weights, then (rotated layers) the output row
   __shared__ float inv_l;
+  pdl_launch();                              // the next call's first kernel waits for this grid itself
   pdl_wait();
   const int G = a.L.G, kvh = hq / G, r = hq % G;
   const int S = a.splits;
@@ -915,6 +916,7 @@ combine_sk_kernel(const DecodeArgs a) {
   __shared__ float wsm[1024];
   __shared__ int pid[1024];
   __shared__ float inv_l;
+  pdl_launch();                              // the next call's first kernel waits for this grid itself
   pdl_wait();
   const int row = blockIdx.x, hq = blockIdx.y;
   const int G = a.L.G, kvh = hq / G, r = hq % G, n_kv = a.L.n_kv;
@@ -1020,20 +1022,21 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
   if ((e = decode_attrs<D>(smem)) != cudaSuccess) return e;
   int hpb = 1, nblk = 1;
   qprep_shape<D>(a.L.n_q, hpb, nblk);
-  qprep_kernel<D><<<dim3(a.n_rows, nblk), dim3(hpb * Qp<D>::TH),
-                     a.L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(a, f, hpb);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = a.sk_ctas > 0 ? dim3(a.sk_ctas) : dim3(a.n_rows, a.L.n_kv, a.splits);
-  cfg.blockDim = dim3(Dec<D>::THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(a.n_rows, nblk);
+  cfg.blockDim = dim3(hpb * Qp<D>::TH);
+  cfg.dynamicSmemBytes = a.L.rot ? (size_t)hpb * D * sizeof(double) : 0;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, qprep_kernel<D>, a, f, hpb)) != cudaSuccess) return e;
+
+  cfg.gridDim = a.sk_ctas > 0 ? dim3(a.sk_ctas) : dim3(a.n_rows, a.L.n_kv, a.splits);
+  cfg.blockDim = dim3(Dec<D>::THREADS);
+  cfg.dynamicSmemBytes = smem;
   if (a.L.rot)       // the deferred TurboQuant read: score scale, PV pre-scale, output un-rotation
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, true>, a, smem)
                       : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, true>, a, smem);
@@ -1064,20 +1067,21 @@ cudaError_t launch_decode_grouped_t(const GroupedDecode& ga, const RopeFreqs& f,
   const int rows = ga.row_base[ga.n], ctas = ga.cta_base[ga.n];
   int hpb = 1, nblk = 1;
   qprep_shape<D>(L.n_q, hpb, nblk);
-  qprep_grouped_kernel<D><<<dim3(rows, nblk), dim3(hpb * Qp<D>::TH),
-                             L.rot ? (size_t)hpb * D * sizeof(double) : 0, st>>>(ga, f, hpb);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(Dec<D>::THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(rows, nblk);
+  cfg.blockDim = dim3(hpb * Qp<D>::TH);
+  cfg.dynamicSmemBytes = L.rot ? (size_t)hpb * D * sizeof(double) : 0;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, qprep_grouped_kernel<D>, ga, f, hpb)) != cudaSuccess) return e;
+
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(Dec<D>::THREADS);
+  cfg.dynamicSmemBytes = smem;
   e = L.rot ? cudaLaunchKernelEx(&cfg, decode_grouped_kernel<D, true>, ga, smem)
             : cudaLaunchKernelEx(&cfg, decode_grouped_kernel<D, false>, ga, smem);
   if (e != cudaSuccess) return e;

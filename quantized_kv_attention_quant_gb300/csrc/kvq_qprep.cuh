@@ -89,13 +89,20 @@ __device__ __forceinline__ void qprep_block(const DecodeArgs& a, const RopeFreqs
   __shared__ float qs[Q::HPB][8];          // per-group sums of the f16 q values
   extern __shared__ double rot_rows[];     // [hpb][D], rotated layers only
   const int tid = threadIdx.x, hl = tid / TH, tt = tid % TH, lane = tid & 31;
+  const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // until that grid is complete only the library's own frequency table is
+  // read; every caller buffer (q, positions, descriptors, the workspace) is
+  // touched after the wait.  The attention kernel may launch only after it
+  // too, so that its ring reads caches an earlier append has finished.
+  if (R > 0) stage_freqs(freqs.f, half, freq);
+  pdl_wait();
   // the first kernel of an attention call clears its status word; the later
   // kernels flag errors only once this grid is complete
   if (row == 0 && hb == 0 && tid == 0) *a.ws.status = 0u;
   pdl_launch();
   const int hq = hb * hpb + hl;                           // q head of this thread
   const bool active = hl < hpb && hq < a.L.n_q;
-  const int G = a.L.G, R = a.L.rope_dims, half = R >> 1;
   // the raw row and the norm weight first: their latency overlaps the row
   // lookup and the angles
   float x[E], wq[E];
@@ -119,8 +126,7 @@ __device__ __forceinline__ void qprep_block(const DecodeArgs& a, const RopeFreqs
 
   // ---- the row's rotation angles, once for all heads ----
   if (R > 0) {
-    stage_freqs(freqs.f, half, freq);
-    __syncthreads();
+    __syncthreads();                       // the staged frequencies
     for (int j = tid; j < half; j += blockDim.x) {
       ff cc, sn;
       rope_cos_sin(pc, freq[j][0], freq[j][1], freq[j][2], cc, sn);
