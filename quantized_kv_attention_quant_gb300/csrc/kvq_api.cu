@@ -420,6 +420,12 @@ kvq_status mixed_prepare(const kvq_layer* layer, const kvq_attn_group* groups, i
     if (dropped) continue;
     kvq::DecodePlan plans[KVQ_MAX_MIXED_GROUPS];
     kvq::decode_plan_grouped(*Lg, n, rows, mk, fx, cap, num_sms_current(), plans);
+    long long total_rows = 0, total_ctas = 0;
+    for (int k = 0; k < n; ++k) {
+      total_rows += rows[k];
+      total_ctas += (long long)rows[k] * Lg->n_kv * plans[k].splits;
+    }
+    if (total_rows > INT32_MAX || total_ctas > INT32_MAX) break;   // past one 1-D grid: run them apart
     kvq::GroupedDecode* ga = &mp->ga_buf;
     *ga = kvq::GroupedDecode{};
     ga->n = n;
