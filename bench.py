@@ -253,7 +253,7 @@ def build_workload(name: str, rank: int, device):
                 full_bytes += by
         info = {"tokens": wl.n_seqs, "kv_bytes": kv_bytes, "dominant_bytes": full_bytes,
                 "dominant": "decode_kernel<512> (full-attention layers)",
-                "launches": 24 + 42 * 3, "config": {
+                "launches": 42 * 3, "config": {              # 24 donor calls fused with their append
                     "workload": "42-layer mixed decode step, 64 ragged sequences (lengths U[1024,32768]), "
                                 "sliding 8q/2kv D256 W512 + full 16q/1kv D512 K=V rope 128, 4/8-bit group 64"
                                 + (" (per-donor bits from the seed)" if name == "stack42" else
@@ -273,7 +273,7 @@ def build_workload(name: str, rank: int, device):
         by = sum(visible_keys(p, spec.window) * rb_pair(spec.head_dim, b)
                  for p, b in zip(wl.filled, wl.bits)) * spec.n_kv_heads
         info = {"tokens": wl.n_seqs, "kv_bytes": by, "dominant_bytes": by,
-                "dominant": f"decode_kernel<{spec.head_dim}>", "launches": 1 + 3,
+                "dominant": f"decode_kernel<{spec.head_dim}>", "launches": 3,    # one fused append + read
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs}}
         return case, [(True, case)], info
     if name == "mixed":
@@ -372,11 +372,23 @@ METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode t
           "train42": "training-read tokens/s"}
 
 
-def step_calls(calls, stream=None):
+def fusable(donor, c) -> bool:
+    """A decode donor's append and attention run as one attn_decode_append."""
+    return donor and hasattr(c, "append_attend")
+
+
+def run_call(donor, c, stream=None, fused=True):
+    if fused and fusable(donor, c):
+        c.append_attend(stream)
+        return
+    if donor:
+        c.append(stream)
+    c.attend(stream)
+
+
+def step_calls(calls, stream=None, fused=True):
     for donor, c in calls:
-        if donor:
-            c.append(stream)
-        c.attend(stream)
+        run_call(donor, c, stream, fused)
 
 
 def call_bytes(c) -> int:
@@ -403,8 +415,9 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
                 torch.cuda.Event(enable_timing=True, external=True))
     try:
         ev = [[ev_pair() for _ in full_calls] for _ in range(K)]
-        # every other call too, for the step breakdown (appends, other attention calls)
-        ev_app = [[ev_pair() for donor, _ in calls if donor] for _ in range(K)]
+        # every other call too, for the step breakdown (appends outside a fused
+        # call, other attention calls)
+        ev_app = [[ev_pair() for donor, c in calls if donor and not fusable(donor, c)] for _ in range(K)]
         ev_oth = [[ev_pair() for _, c in calls if c not in full_calls] for _ in range(K)]
         have_inner = True
     except TypeError:
@@ -421,7 +434,8 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
             for k in range(K):
                 j = ja = jo = 0
                 for donor, c in calls:
-                    if donor:
+                    fused = fusable(donor, c)
+                    if donor and not fused:
                         if all_events:
                             ev_app[k][ja][0].record()
                         c.append()
@@ -432,7 +446,10 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
                     pair = ev[k][j] if inner else (ev_oth[k][jo] if all_events else None)
                     if pair:
                         pair[0].record()
-                    c.attend()
+                    if fused:
+                        c.append_attend()
+                    else:
+                        c.attend()
                     if pair:
                         pair[1].record()
                         if inner:
@@ -460,6 +477,33 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
         res["dom_call_ms"] = [sum(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)) / K
                               for j in range(len(full_calls))]
     del graph
+    if any(fusable(d, c) for d, c in calls) and workload.startswith("stack42"):
+        # the same steps with every donor's append as its own kv_quant_append
+        # call before its attn_decode (the same timing events around the
+        # dominant calls as the timed graph)
+        g_sep = torch.cuda.CUDAGraph()
+        ev_sep = [[ev_pair() for _ in full_calls] for _ in range(K)] if have_inner else None
+        with torch.cuda.graph(g_sep, stream=stream):
+            for k in range(K):
+                j = 0
+                for donor, c in calls:
+                    if donor:
+                        c.append()
+                    pair = ev_sep[k][j] if (ev_sep and c in full_calls) else None
+                    if pair:
+                        pair[0].record()
+                    c.attend()
+                    if pair:
+                        pair[1].record()
+                        j += 1
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(replay_stream)
+        g_sep.replay()
+        a1.record(replay_stream)
+        torch.cuda.synchronize()
+        res["separate_append_ms"] = a0.elapsed_time(a1) / K
+        del g_sep
     if info.get("mixed"):
         # the same steps with every group as its own call on one stream
         # (with the same timing events around the attention calls as the
@@ -558,6 +602,8 @@ def sub_result(name, K, warmup, device, peaks):
            "unit": "tokens/s", "ms_per_step": ms_step, "workload": info["config"]["workload"],
            "roofline": roofline(name, info, res, peaks), "device_status_clean": res["status_ok"],
            "clocks": res["clocks"]}
+    if res.get("separate_append_ms") is not None:
+        out["separate_append_ms_per_step"] = res["separate_append_ms"]
     if info["kv_bytes"]:
         out["kv_bytes_per_step"] = info["kv_bytes"]
     if name.startswith("stack42") and res.get("dom_call_ms"):
@@ -598,9 +644,15 @@ def run_gpu(args):
                 "compute": "packed 4/8-bit codes; f16 tensor-core operands (codes exact), fp32 accumulation"})
     if res.get("serial_ms") is not None:
         cfg["separate_calls_ms_per_step"] = res["serial_ms"]
+    if any(fusable(d, c) for d, c in calls):
+        cfg["donor_calls"] = ("attn_decode_append (each donor's K/V append and its attention read in one "
+                              "call; the first kernel preps q and appends K/V side by side)")
+    if res.get("separate_append_ms") is not None:
+        cfg["separate_append_ms_per_step"] = res["separate_append_ms"]
     if res.get("breakdown"):
         cfg["step_breakdown_ms"] = {k: round(v, 4) for k, v in res["breakdown"].items()}
-        cfg["step_breakdown_note"] = "separate replay with events around every call (they slow it down)"
+        cfg["step_breakdown_note"] = ("separate replay with events around every call (they slow it down); "
+                                      "fused donor appends count with the attention calls")
     if args.workload.startswith("stack42") and res.get("dom_call_ms"):
         cfg["dominant_by_bits"] = bit_split(res, peaks)
     del case, calls
@@ -674,9 +726,7 @@ def run_e2e(calls, K, device, info, world):
                 s.wait_event(ready[L])
                 if read[L] is not None:
                     s.wait_event(read[L])
-                if donor:
-                    c.append()
-                c.attend()
+                run_call(donor, c)
                 ev = torch.cuda.Event()
                 ev.record(s)
                 done[L] = ev

@@ -186,6 +186,33 @@ kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_
 size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos);
 
 /*
+ * attn_decode_append -- a donor layer's decode step in one call: each
+ * sequence's new K/V row is prepped and quantize-appended at position pos[s]
+ * (kv_quant_append with one row per sequence, row s of k_raw / v_raw being
+ * sequence s's, start_pos = pos), then query row s attends its cache up to
+ * and including that row (attn_decode).  model.ts attentionTraining in the
+ * decode phase: cache.appendWindow(k, v), then read.attend(q, 1.0).
+ *
+ * The outputs are those of the two separate calls, bit for bit: the q prep
+ * and the K/V append run side by side in the call's first kernel, and the
+ * attention kernel copies the tile holding a sequence's new row only once
+ * that kernel is complete.
+ *
+ *   k_raw, v_raw, k_norm_w, kv_prepped   as for kv_quant_append, with n_rows
+ *                                        = n_seqs ([n_seqs][n_kv_heads][head_dim])
+ *   kv_prepped                           NULL or device bf16 [2][n_seqs][n_kv_heads][head_dim]
+ *   every other argument                 as for attn_decode; the workspace is
+ *                                        attn_decode_workspace_bytes(layer, n_seqs, max_pos)
+ * Arguments of both halves are checked before anything is enqueued.
+ */
+kvq_status attn_decode_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* pos, int32_t max_pos,
+                              const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v_raw,
+                              const uint16_t* q_norm_w, const uint16_t* k_norm_w,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped, uint16_t* kv_prepped,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_prefill_chunk -- a chunk of new query rows per sequence attends the
  * cache after kv_quant_append stored the chunk's K/V rows (the "window" phase
  * of the pages: prompt chunks and verify windows).  Row t of sequence s sits

@@ -66,6 +66,8 @@ def _load():
     lib.kv_quant_append.restype = ctypes.c_int
     lib.attn_decode.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp, sz, vp]
     lib.attn_decode.restype = ctypes.c_int
+    lib.attn_decode_append.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.attn_decode_append.restype = ctypes.c_int
     lib.attn_decode_static.argtypes = [lay, vp, i32, vp, i32, vp, vp, vp, i32, vp, vp]
     lib.attn_decode_static.restype = ctypes.c_int
     lib.attn_decode_workspace_bytes.argtypes = [lay, i32, i32]
@@ -159,6 +161,16 @@ def attn_decode(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, ou
     _check(lib.attn_decode(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(pos), max_pos, _ptr(q_raw),
                            _ptr(q_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
                            _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def attn_decode_append(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, k_raw, v_raw, q_norm_w, k_norm_w,
+                       out, out_is_f32, q_prepped, kv_prepped, workspace, workspace_bytes, stream=None):
+    """kv_quant_append of one row per sequence at pos, then attn_decode, in one
+    call (see include/kvq.h)."""
+    _check(lib.attn_decode_append(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(pos), max_pos, _ptr(q_raw),
+                                  _ptr(k_raw), _ptr(v_raw), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
+                                  int(out_is_f32), _ptr(q_prepped), _ptr(kv_prepped), _ptr(workspace),
+                                  workspace_bytes, _stream(stream)))
 
 
 def attn_decode_static(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, out, out_is_f32,

@@ -291,6 +291,42 @@ kvq_status attn_decode(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_
                           out_is_f32, q_prepped, workspace, workspace_bytes, stream);
 }
 
+kvq_status attn_decode_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                              const int32_t* pos, int32_t max_pos, const uint16_t* q_raw, const uint16_t* k_raw,
+                              const uint16_t* v_raw, const uint16_t* q_norm_w, const uint16_t* k_norm_w,
+                              void* out, int32_t out_is_f32, uint16_t* q_prepped, uint16_t* kv_prepped,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!max_pos_ok(max_pos)) return fail(KVQ_EINVAL, "max_pos %d not in [0, 2^24)", max_pos);
+  Prepared p;
+  kvq_status st = attention_prepare(layer, seqs, n_seqs, nullptr, pos, n_seqs, max_pos + 1, true, 0, q_raw,
+                                    q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes, &p);
+  if (st != KVQ_OK || p.empty) return st;
+  // the append's own checks (the layer, sequences and positions passed above)
+  REQUIRE_PTR(k_raw, "k_raw", 16);
+  REQUIRE_PTR(k_norm_w, "k_norm_w", 2);
+  if (p.a.L.k_eq_v) {
+    if (v_raw) return fail(KVQ_EINVAL, "v_raw must be NULL when k_eq_v = 1");
+  } else {
+    REQUIRE_PTR(v_raw, "v_raw", 16);
+  }
+  if (kv_prepped && !aligned(kv_prepped, 2)) return fail(KVQ_EINVAL, "kv_prepped is not 2-byte aligned");
+  kvq::AppendArgs ap = {};
+  ap.L = p.a.L;
+  ap.seqs = seqs;
+  ap.n_seqs = n_seqs;
+  ap.row_offsets = nullptr;                 // one row per sequence
+  ap.start_pos = pos;
+  ap.n_rows = n_seqs;
+  ap.k_raw = k_raw;
+  ap.v_raw = v_raw;
+  ap.k_w = k_norm_w;
+  ap.prepped = kv_prepped;
+  p.a.fused_append = 1;
+  const cudaError_t e = kvq::launch_decode_append(p.a, ap, *p.f, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_append launch");
+  return KVQ_OK;
+}
+
 size_t attn_decode_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t max_pos) {
   kvq::LayerArgs L;
   if (check_layer(layer, &L) != KVQ_OK || n_seqs < 0 || !max_pos_ok(max_pos)) return 0;

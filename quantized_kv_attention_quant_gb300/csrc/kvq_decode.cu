@@ -30,6 +30,7 @@
 //   3. combine_kernel / combine_sk_kernel (rows, n_q): merge the partials.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
+#include "kvq_append.cuh"
 #include "kvq_qprep.cuh"
 
 #include <algorithm>
@@ -195,13 +196,16 @@ __device__ __forceinline__ bool decode_body(const DecodeArgs& a, const kvq_seq_c
   int issued = 0, issue_st = 0, issue_slot = tr.t_begin % cap_tiles;
   auto refill = [&]() {
     if (issued < tr.n_my) {
+      // a key the call's first kernel is still appending: wait for that grid
+      if (a.fused_append && tr.t_begin + issued == tr.hi / kTileKeys) pdl_wait();
       issue(issue_st, issue_slot);
       if (++issue_st == nst) issue_st = 0;
       if (++issue_slot == cap_tiles) issue_slot = 0;
       ++issued;
     }
   };
-  // prologue: fill the ring (the cache was written before this launch)
+  // prologue: fill the ring (the cache was written before this launch, but
+  // for the newest keys of an attn_decode_append call: see refill)
   for (int i = 0; i < nst; ++i) refill();
 
   pdl_wait();                                   // q fragments come from qprep_kernel
@@ -980,6 +984,17 @@ constexpr int decode_smem_bytes() {
   return D >= 512 ? 227 * 1024 : (D == 256 ? 110 * 1024 : 56 * 1024);
 }
 
+// attn_decode_append's first kernel: blocks y < nq_blocks prep q (as
+// qprep_kernel), the others append the rows' new K/V (as append_kernel); the
+// two halves share nothing and run side by side.
+template <int D>
+__global__ void __launch_bounds__(1024)
+prep_append_kernel(const DecodeArgs a, const AppendArgs ap, const RopeFreqs freqs, const int hpb,
+                   const int nq_blocks, const int ipb) {
+  if ((int)blockIdx.y < nq_blocks) qprep_block<D>(a, freqs, hpb, blockIdx.x, blockIdx.y);
+  else append_block<D>(ap, freqs, ipb, blockIdx.x, blockIdx.y - nq_blocks);
+}
+
 // The shared-memory opt-in of every attention kernel of head_dim D, once per
 // device (a lock: host threads may make their first call on a device at the
 // same time).
@@ -1004,39 +1019,33 @@ cudaError_t decode_attrs(int smem) {
       for (const void* fn : fns)
         if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
           return e;
+      // the fused q + K/V prep of a rotated layer: one float64 row per head
+      // or item beside the static shared memory of both halves
+      if ((e = cudaFuncSetAttribute(prep_append_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (1024 / Qp<D>::TH) * D * (int)sizeof(double))) != cudaSuccess)
+        return e;
       attr_set[dev].store(true, std::memory_order_release);
     }
   }
   return cudaSuccess;
 }
 
+// The attention and merge launches of a call, programmatic dependents of the
+// call's first kernel.
 template <int D>
-cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
-  static_assert(D % 64 == 0, "");
-  static_assert(ring_slots(D, 8, decode_smem_bytes<D>()) >= 2 && ring_slots(D, 4, decode_smem_bytes<D>()) >= 2,
-                "the pipeline needs at least two stages");
-  static_assert(ring_slots(D, 8, decode_smem_bytes<D>() - sk_plan_bytes(kSkMaxRows)) >= 2,
-                "the stream-K plan leaves two stages");
-  cudaError_t e;
+cudaError_t launch_read_merge_t(const DecodeArgs& a, cudaStream_t st) {
   const int smem = decode_smem_bytes<D>();
-  if ((e = decode_attrs<D>(smem)) != cudaSuccess) return e;
-  int hpb = 1, nblk = 1;
-  qprep_shape<D>(a.L.n_q, hpb, nblk);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_rows, nblk);
-  cfg.blockDim = dim3(hpb * Qp<D>::TH);
-  cfg.dynamicSmemBytes = a.L.rot ? (size_t)hpb * D * sizeof(double) : 0;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg, qprep_kernel<D>, a, f, hpb)) != cudaSuccess) return e;
-
   cfg.gridDim = a.sk_ctas > 0 ? dim3(a.sk_ctas) : dim3(a.n_rows, a.L.n_kv, a.splits);
   cfg.blockDim = dim3(Dec<D>::THREADS);
   cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (a.L.rot)       // the deferred TurboQuant read: score scale, PV pre-scale, output un-rotation
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, true>, a, smem)
                       : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, true>, a, smem);
@@ -1055,6 +1064,55 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, combine_sk_kernel<D, false>, a)
                       : cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, a);
   return e;
+}
+
+template <int D>
+cudaError_t launch_decode_t(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
+  static_assert(D % 64 == 0, "");
+  static_assert(ring_slots(D, 8, decode_smem_bytes<D>()) >= 2 && ring_slots(D, 4, decode_smem_bytes<D>()) >= 2,
+                "the pipeline needs at least two stages");
+  static_assert(ring_slots(D, 8, decode_smem_bytes<D>() - sk_plan_bytes(kSkMaxRows)) >= 2,
+                "the stream-K plan leaves two stages");
+  cudaError_t e;
+  if ((e = decode_attrs<D>(decode_smem_bytes<D>())) != cudaSuccess) return e;
+  int hpb = 1, nblk = 1;
+  qprep_shape<D>(a.L.n_q, hpb, nblk);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_rows, nblk);
+  cfg.blockDim = dim3(hpb * Qp<D>::TH);
+  cfg.dynamicSmemBytes = a.L.rot ? (size_t)hpb * D * sizeof(double) : 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, qprep_kernel<D>, a, f, hpb)) != cudaSuccess) return e;
+  return launch_read_merge_t<D>(a, st);
+}
+
+template <int D>
+cudaError_t launch_decode_append_t(const DecodeArgs& a, const AppendArgs& ap, const RopeFreqs& f, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = decode_attrs<D>(decode_smem_bytes<D>())) != cudaSuccess) return e;
+  int hpb = 1, nblk = 1;
+  qprep_shape<D>(a.L.n_q, hpb, nblk);
+  const int items = 2 * a.L.n_kv;
+  const int ipb = std::min(items, App<D>::IPB);
+  const int ablk = (items + ipb - 1) / ipb;
+  const int per = std::max(hpb, ipb);            // Qp<D>::TH == App<D>::TH threads per head or item
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_rows, nblk + ablk);
+  cfg.blockDim = dim3(per * Qp<D>::TH);
+  cfg.dynamicSmemBytes = a.L.rot ? (size_t)per * D * sizeof(double) : 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, prep_append_kernel<D>, a, ap, f, hpb, nblk, ipb)) != cudaSuccess) return e;
+  return launch_read_merge_t<D>(a, st);
 }
 
 // The grouped schedule: the same three kernels, each grid over every group.
@@ -1223,6 +1281,18 @@ cudaError_t launch_decode_grouped(const GroupedDecode& ga, const RopeFreqs& f, c
     case 128: return launch_decode_grouped_t<128>(ga, f, st);
     case 256: return launch_decode_grouped_t<256>(ga, f, st);
     case 512: return launch_decode_grouped_t<512>(ga, f, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_append(const DecodeArgs& a, const AppendArgs& ap, const RopeFreqs& f, cudaStream_t st) {
+  if (a.n_rows == 0) return cudaSuccess;
+  static_assert(Qp<64>::TH == App<64>::TH && Qp<512>::TH == App<512>::TH, "one block shape for both halves");
+  switch (a.L.D) {
+    case 64: return launch_decode_append_t<64>(a, ap, f, st);
+    case 128: return launch_decode_append_t<128>(a, ap, f, st);
+    case 256: return launch_decode_append_t<256>(a, ap, f, st);
+    case 512: return launch_decode_append_t<512>(a, ap, f, st);
     default: return cudaErrorInvalidValue;
   }
 }

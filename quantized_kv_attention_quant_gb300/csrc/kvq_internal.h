@@ -27,7 +27,7 @@ struct AppendArgs {
   LayerArgs L;
   const kvq_seq_cache* seqs;
   int n_seqs;
-  const int32_t* row_offsets;
+  const int32_t* row_offsets;   // nullptr: one row per sequence (row s is sequence s)
   const int32_t* start_pos;
   int n_rows;
   const uint16_t* k_raw;
@@ -78,6 +78,10 @@ struct DecodeArgs {
   int splits;
   int chunk_tiles;      // > 0: every split covers this many tiles; 0: ceil(row tiles / splits)
   int sk_ctas;          // > 0: stream-K schedule over this many CTAs (splits / chunk_tiles unused)
+  // 1: the call's first kernel also appends each row's new K/V (the row's
+  // position is its newest key), so the tile holding a row's newest key is
+  // copied only once that kernel is complete
+  int fused_append;
   DecodeWs ws;
 };
 
@@ -142,5 +146,9 @@ cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, 
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
 // The grouped launch (fixed-chunk plans in every group, ga.n >= 1).
 cudaError_t launch_decode_grouped(const GroupedDecode& ga, const RopeFreqs& f, cudaStream_t st);
+// attn_decode_append: one kernel preps q and appends each sequence's new K/V
+// row (ap: one row per sequence, ap.start_pos == a.pos), then the attention
+// and merge kernels of launch_decode (a.fused_append == 1).
+cudaError_t launch_decode_append(const DecodeArgs& a, const AppendArgs& ap, const RopeFreqs& f, cudaStream_t st);
 
 }  // namespace kvq

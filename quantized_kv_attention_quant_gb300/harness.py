@@ -14,8 +14,8 @@ import torch
 
 import workloads as W
 
-from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_workspace_bytes, attn_group,
-               attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, attn_train_forward,
+from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_append, attn_decode_workspace_bytes,
+               attn_group, attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, attn_train_forward,
                attn_train_workspace_bytes, kv_quant_append, kvq_train_kv_prep, layer as make_layer)
 from .cache import LayerCaches
 
@@ -152,6 +152,12 @@ class DecodeCase:
         c = caches or self.caches
         attn_decode(self.lay, c.desc, self.wl.n_seqs, self.pos, self.max_pos, self.q, self.q_w, self.out,
                     self.out_f32, self.q_prepped, self.ws, self.ws_bytes, stream)
+
+    def append_attend(self, stream=None):
+        """append + attend as one attn_decode_append call."""
+        attn_decode_append(self.lay, self.caches.desc, self.wl.n_seqs, self.pos, self.max_pos, self.q, self.k,
+                           self.v, self.q_w, self.k_w, self.out, self.out_f32, self.q_prepped, self.kv_prepped,
+                           self.ws, self.ws_bytes, stream)
 
     def step(self, stream=None):
         self.append(stream)
@@ -300,8 +306,13 @@ class StackCase:
                                   keep_prepped=keep)
             self.layers.append((i, d, case))
 
-    def step(self, stream=None):
+    def step(self, stream=None, fused=True):
+        """One step: each donor's append and read as one attn_decode_append
+        (fused) or as kv_quant_append + attn_decode; sharers read only."""
         for i, d, case in self.layers:
+            if i < W.N_DONORS and fused:
+                case.append_attend(stream)
+                continue
             if i < W.N_DONORS:
                 case.append(stream)
             case.attend(stream)

@@ -23,6 +23,7 @@
 typedef void (*any_fn)(void);
 static const any_fn kAll[] = {
     (any_fn)&kv_quant_append,        (any_fn)&attn_decode,
+    (any_fn)&attn_decode_append,
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
     (any_fn)&attn_mixed_schedule,
@@ -59,6 +60,8 @@ int main(void) {
   CHECK(attn_decode(&L, NULL, 1, NULL, 10, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) == KVQ_EINVAL);
   CHECK(strlen(kvq_last_error()) > 0);
   CHECK(attn_decode(NULL, NULL, 1, NULL, 10, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) == KVQ_EINVAL);
+  CHECK(attn_decode_append(&L, NULL, 1, NULL, -1, NULL, NULL, NULL, NULL, NULL, NULL, 1, NULL, NULL, NULL, 0,
+                           NULL) == KVQ_EINVAL);
   kvq_layer bad = L;
   bad.head_dim = 96;
   CHECK(kv_quant_append(&bad, NULL, 1, NULL, NULL, 1, NULL, NULL, NULL, NULL, NULL) == KVQ_EUNSUPPORTED);

@@ -120,6 +120,28 @@ def test_bad_pointers_decode(m):
     assert f(L, P, 0, P, 10, P, P, P, 1, None, P, 0, None) == 0           # no sequences: no work
 
 
+def test_bad_pointers_decode_append(m):
+    """attn_decode_append checks the decode half and the append half before
+    enqueueing anything."""
+    lay = _layer(m)
+    f = m.lib.attn_decode_append
+    L = ctypes.byref(lay)
+    big = 1 << 40
+    # (layer, seqs, n, pos, max_pos, q, k, v, q_w, k_w, out, f32, q_prepped, kv_prepped, ws, ws_bytes, stream)
+    assert f(L, P, 1, P, -1, P, P, P, P, P, P, 1, None, None, P, big, None) == 1     # max_pos < 0
+    assert f(L, P, 1, P, 10, P + 8, P, P, P, P, P, 1, None, None, P, big, None) == 1  # q_raw misaligned
+    assert f(L, P, 1, P, 10, P, None, P, P, P, P, 1, None, None, P, big, None) == 1   # k_raw NULL
+    assert f(L, P, 1, P, 10, P, P + 8, P, P, P, P, 1, None, None, P, big, None) == 1  # k_raw misaligned
+    assert f(L, P, 1, P, 10, P, P, None, P, P, P, 1, None, None, P, big, None) == 1   # v_raw missing
+    assert f(L, P, 1, P, 10, P, P, P, P, None, P, 1, None, None, P, big, None) == 1   # k_norm_w NULL
+    assert f(L, P, 1, P, 10, P, P, P, P, P, P, 1, None, P + 1, P, big, None) == 1     # kv_prepped odd
+    keqv = _layer(m, k_eq_v=True)
+    assert f(ctypes.byref(keqv), P, 1, P, 10, P, P, P, P, P, P, 1, None, None, P, big, None) == 1  # v_raw with K=V
+    need = m.attn_decode_workspace_bytes(lay, 1, 10)
+    assert f(L, P, 1, P, 10, P, P, P, P, P, P, 1, None, None, P, need - 1, None) == 4  # workspace too small
+    assert f(L, P, 0, P, 10, P, P, P, P, P, P, 1, None, None, P, 0, None) == 0        # no sequences
+
+
 def test_bad_pointers_prefill(m):
     lay = _layer(m)
     f = m.lib.attn_prefill_chunk

@@ -148,6 +148,73 @@ def test_many_rows_take_fixed_chunks(kvq):
     print("many-rows worst", worst)
 
 
+# attn_decode_append: one call for a donor's append and read, bit-equal to
+# kv_quant_append + attn_decode.  Cases: a window ring that is exactly the
+# window (row 611 of a 512-slot ring sees keys 100..611, whose first and last
+# tiles share a ring tile: the first is copied early, the last after the
+# append), fresh caches (position 0: the first tile is the new one), ragged
+# stream-K rows, GQA 16 at D64, a rotated layer, a skipped sequence.
+FUSED_CASES = {
+    "sliding-ring-exact": (_spec(8, 2, 256, 512, 256), [611, 512, 511, 0, 1000, 63], [4, 8, 8, 4, 4, 8]),
+    "full-keqv-stream-k": STREAM_K_CASES["sk-ragged-d512-keqv"],
+    "d64-gqa16": DECODE_CASES["d64-gqa16"],
+    "rot-full-keqv": (dataclasses.replace(_spec(16, 1, 512, 0, 128, 1e6, True), kv_rotation=True),
+                      [900, 0, 64, 2000], [4, 8, 8, 4]),
+}
+
+
+def _fused_pair(harness, wl):
+    """The same step twice on identical caches: separate calls, then the fused
+    call.  Returns the two cases after the steps."""
+    a = harness.DecodeCase(wl, keep_prepped=True)
+    b = harness.DecodeCase(wl, keep_prepped=True)
+    a.step()
+    b.append_attend()
+    torch.cuda.synchronize()
+    return a, b
+
+
+@pytest.mark.parametrize("name", sorted(FUSED_CASES))
+def test_decode_append_equals_separate_calls(kvq, name):
+    _, harness = kvq
+    spec, filled, bits = FUSED_CASES[name]
+    wl = W.DecodeWorkload("fused-" + name, 96, spec, filled=filled, bits=bits)
+    a, b = _fused_pair(harness, wl)
+    assert a.status_word() == b.status_word() == 0
+    for x, y in ((a.out, b.out), (a.q_prepped, b.q_prepped), (a.kv_prepped, b.kv_prepped)):
+        assert torch.equal(x, y)
+    for s in range(wl.n_seqs):
+        slots = ring_slots(wl.filled[s] + 1, wl.capacity(s))
+        assert np.array_equal(a.caches.host_rows(s, slots)["k_codes"], b.caches.host_rows(s, slots)["k_codes"])
+    worst = verify_decode(b, wl, check_fill=False)
+    print(name, "worst", worst)
+
+
+def test_decode_append_skips_a_bad_sequence(kvq):
+    """A sequence with an invalid descriptor inside a fused call: nothing of
+    it is written, its output is NaN, the status word says so, and the other
+    sequences are as the oracle has them."""
+    _, harness = kvq
+    spec = _spec(8, 2, 256, 512, 256)
+    wl = W.DecodeWorkload("fused-bad", 97, spec, filled=[300, 40, 700], bits=[8, 4, 4])
+    c = harness.DecodeCase(wl, keep_prepped=True)
+    torch.cuda.synchronize()
+    before = c.caches.seqs[1]["k_codes"].clone()
+    bad = c.caches.desc.cpu().numpy().copy()
+    bad[56 + 48:56 + 52] = np.frombuffer(np.int32(5).tobytes(), np.uint8)      # seq 1: bits = 5
+    c.caches.desc.copy_(torch.from_numpy(bad))
+    c.append_attend()
+    torch.cuda.synchronize()
+    assert c.status_word() & (1 << 2)
+    out = c.out.cpu().numpy()
+    assert np.all(np.isnan(out[1]))
+    assert torch.equal(before, c.caches.seqs[1]["k_codes"])
+    good = harness.DecodeCase(wl, keep_prepped=True)
+    good.step()
+    torch.cuda.synchronize()
+    assert torch.equal(c.out[[0, 2]], good.out[[0, 2]])
+
+
 # the deferred TurboQuant read (rotated K/V, q rotated, output un-rotated):
 # fixed chunks, stream-K with rows merged and rows written by one CTA, a
 # window layer and a prompt chunk (the row path), 4- and 8-bit caches
@@ -462,7 +529,8 @@ STACK_LAYERS = (11, 22, 23, 24, 41)
 def test_workload_stack42(kvq):
     """The 42-layer KV-shared decode step at full size, as the bench runs it:
     64 ragged sequences of 1,798 .. 32,737 cached tokens, donors 0..23 append
-    and attend, sharers 24..41 attend the donor's cache without appending.  The
+    and attend (one attn_decode_append call each), sharers 24..41 attend the
+    donor's cache without appending.  The
     full layers take the stream-K schedule over 64 rows (8-bit on donor 23 and
     its sharers).  On sampled sequences (every one of at least 32,000 keys, the
     shortest and the one nearest the mean length) of the listed layers: the
