@@ -82,6 +82,7 @@ KERNEL_SOURCES = {
                           "quantized_kv_attention_quant_gb300/csrc/rope_consts.h",
                           "quantized_kv_attention_quant_gb300/csrc/kvq_internal.h",
                           "quantized_kv_attention_quant_gb300/csrc/kvq_qprep.cuh",
+                          "quantized_kv_attention_quant_gb300/csrc/kvq_append.cuh",
                           "include/kvq.h"],
 }
 
