@@ -330,7 +330,7 @@ def build_workload(name: str, rank: int, device):
                 flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
         info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
                 "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05) with its q prep and key "
-                            "dequantization", "launches": 1 + 3,
+                            "dequantization", "launches": 3,     # the append runs in the q prep's grid
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     if name == "train42":
@@ -341,7 +341,8 @@ def build_workload(name: str, rank: int, device):
         flops = sum(4 * c.spec.n_q_heads * c.spec.head_dim * train_visible_total(blocks, c.spec.window)
                     for _, c in calls)
         info = {"tokens": case.n_rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
-                "dominant": "train_tc_kernel<256|512> with its q prep (tcgen05)", "launches": 24 + 42 * 2,
+                "dominant": "train_tc_kernel<256|512> with its q prep (tcgen05)",
+                "launches": 42 * 2,                   # donors' K/V prep in the q prep's grid
                 "config": {"workload": "training forward's stateless read over the 42-layer stack, one packed "
                                        f"sequence of {case.n_rows} rows: a prefix of {blocks[0]} rows shared by "
                                        f"{len(blocks) - 1} branches of {blocks[1]} (block-sparse mask), sliding "
@@ -371,6 +372,10 @@ def train_visible_total(blocks, window: int) -> int:
 METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)",
           "mixed-verify": "mixed-step tokens/s (decode tokens + window rows)",
           "train42": "training-read tokens/s"}
+
+
+FUSED_CALL = {"DecodeCase": "attn_decode_append", "PrefillCase": "attn_prefill_append",
+              "TrainCase": "attn_train_donor_forward"}
 
 
 def fusable(donor, c) -> bool:
@@ -478,7 +483,7 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
         res["dom_call_ms"] = [sum(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)) / K
                               for j in range(len(full_calls))]
     del graph
-    if any(fusable(d, c) for d, c in calls) and workload.startswith("stack42"):
+    if any(fusable(d, c) for d, c in calls) and not info.get("mixed"):
         # the same steps with every donor's append as its own kv_quant_append
         # call before its attn_decode (the same timing events around the
         # dominant calls as the timed graph)
@@ -645,9 +650,10 @@ def run_gpu(args):
                 "compute": "packed 4/8-bit codes; f16 tensor-core operands (codes exact), fp32 accumulation"})
     if res.get("serial_ms") is not None:
         cfg["separate_calls_ms_per_step"] = res["serial_ms"]
-    if any(fusable(d, c) for d, c in calls):
-        cfg["donor_calls"] = ("attn_decode_append (each donor's K/V append and its attention read in one "
-                              "call; the first kernel preps q and appends K/V side by side)")
+    fused_calls = sorted({FUSED_CALL[type(c).__name__] for d, c in calls if fusable(d, c)})
+    if fused_calls:
+        cfg["donor_calls"] = (", ".join(fused_calls) + " (each donor's K/V append and its attention read in one "
+                              "call; the append runs beside the q prep in the call's first kernel)")
     if res.get("separate_append_ms") is not None:
         cfg["separate_append_ms_per_step"] = res["separate_append_ms"]
     if res.get("breakdown"):

@@ -245,6 +245,26 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
                               void* out, int32_t out_is_f32, uint16_t* q_prepped,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * attn_prefill_append -- a prompt chunk's (or verify window's) K/V append and
+ * its read in one call: kv_quant_append of the chunk rows (row_offsets,
+ * start_pos, n_rows as given), then attn_prefill_chunk of the same rows, bit
+ * for bit.  On the tensor-core paths the append runs in the grid of the
+ * call's q prep (the two share nothing), and the read follows; on the row
+ * path (verify windows, head_dim 512, a rotated layer) the append comes
+ * first.  k_raw / v_raw / k_norm_w / kv_prepped as for kv_quant_append
+ * (kv_prepped: NULL or device bf16 [2][n_rows][n_kv_heads][head_dim]); every
+ * other argument as for attn_prefill_chunk, whose workspace size it takes.
+ * Arguments of both halves are checked before anything is enqueued.
+ */
+kvq_status attn_prefill_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                               const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                               int32_t max_rows_per_seq,
+                               const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v_raw,
+                               const uint16_t* q_norm_w, const uint16_t* k_norm_w,
+                               void* out, int32_t out_is_f32, uint16_t* q_prepped, uint16_t* kv_prepped,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of an attn_prefill_chunk call (0 for an invalid layer or a
  * negative count). */
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
@@ -384,6 +404,21 @@ kvq_status attn_train_forward(const kvq_layer* layer, int32_t n_blocks, const in
                               const uint16_t* k_hat, const uint16_t* v_hat,
                               void* out, int32_t out_is_f32, uint16_t* q_prepped,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_train_donor_forward -- a donor layer's training read in one call:
+ * kvq_train_kv_prep of the pass's rows into k_hat / v_hat, then
+ * attn_train_forward over them, bit for bit.  The K/V prep runs in the grid
+ * of the read's q prep (the two share nothing).  Arguments as for those two
+ * calls; k_hat / v_hat are written and kept (the layer's sharers read them).
+ */
+kvq_status attn_train_donor_forward(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets,
+                                    int32_t n_rows, int32_t max_block_rows,
+                                    const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v_raw,
+                                    const uint16_t* q_norm_w, const uint16_t* k_norm_w,
+                                    uint16_t* k_hat, uint16_t* v_hat,
+                                    void* out, int32_t out_is_f32, uint16_t* q_prepped,
+                                    void* workspace, size_t workspace_bytes, void* stream);
 
 size_t attn_train_workspace_bytes(const kvq_layer* layer, int32_t n_rows);
 

@@ -84,6 +84,12 @@ def _load():
     lib.kvq_train_kv_prep.restype = ctypes.c_int
     lib.attn_train_forward.argtypes = [lay, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
     lib.attn_train_forward.restype = ctypes.c_int
+    lib.attn_prefill_append.argtypes = [lay, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp,
+                                        sz, vp]
+    lib.attn_prefill_append.restype = ctypes.c_int
+    lib.attn_train_donor_forward.argtypes = [lay, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
+                                             sz, vp]
+    lib.attn_train_donor_forward.restype = ctypes.c_int
     lib.attn_train_workspace_bytes.argtypes = [lay, i32]
     lib.attn_train_workspace_bytes.restype = sz
     lib.kvq_static_status.argtypes = [vp, vp]
@@ -171,6 +177,27 @@ def attn_decode_append(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, k_raw
                                   _ptr(k_raw), _ptr(v_raw), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
                                   int(out_is_f32), _ptr(q_prepped), _ptr(kv_prepped), _ptr(workspace),
                                   workspace_bytes, _stream(stream)))
+
+
+def attn_prefill_append(layer: KvqLayer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_rows_per_seq, q_raw,
+                        k_raw, v_raw, q_norm_w, k_norm_w, out, out_is_f32, q_prepped, kv_prepped, workspace,
+                        workspace_bytes, stream=None):
+    """kv_quant_append of a chunk's rows, then attn_prefill_chunk, in one call
+    (see include/kvq.h)."""
+    _check(lib.attn_prefill_append(ctypes.byref(layer), _ptr(seqs), n_seqs, _ptr(row_offsets), _ptr(start_pos),
+                                   n_rows, max_rows_per_seq, _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                                   _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out), int(out_is_f32), _ptr(q_prepped),
+                                   _ptr(kv_prepped), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def attn_train_donor_forward(layer: KvqLayer, n_blocks, block_offsets, n_rows, max_block_rows, q_raw, k_raw,
+                             v_raw, q_norm_w, k_norm_w, k_hat, v_hat, out, out_is_f32, q_prepped, workspace,
+                             workspace_bytes, stream=None):
+    """kvq_train_kv_prep, then attn_train_forward, in one call (see include/kvq.h)."""
+    _check(lib.attn_train_donor_forward(ctypes.byref(layer), n_blocks, _ptr(block_offsets), n_rows,
+                                        max_block_rows, _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_norm_w),
+                                        _ptr(k_norm_w), _ptr(k_hat), _ptr(v_hat), _ptr(out), int(out_is_f32),
+                                        _ptr(q_prepped), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def attn_decode_static(layer: KvqLayer, seqs, n_seqs, pos, max_pos, q_raw, q_norm_w, out, out_is_f32,

@@ -218,11 +218,19 @@ kvq_status attention_prepare(const kvq_layer* layer, const kvq_seq_cache* seqs, 
   return KVQ_OK;
 }
 
-kvq_status attention_launch(const Prepared& p, cudaStream_t st) {
+// ap: NULL, or the call's K/V append, run in the grid of the tensor-core
+// paths' q prep (the row path appends first, then reads)
+kvq_status attention_launch(const Prepared& p, cudaStream_t st, const kvq::AppendArgs* ap = nullptr) {
   if (p.empty) return KVQ_OK;
-  const cudaError_t e = p.path == Path::kPromptTc   ? kvq::launch_prompt_tc(p.a, p.workspace, p.max_rows_per_seq, *p.f, st)
-                        : p.path == Path::kPrefillTc ? kvq::launch_prefill_tc(p.a, *p.f, p.max_rows_per_seq, st)
-                                                     : kvq::launch_decode(p.a, *p.f, num_sms_current(), st);
+  cudaError_t e = cudaSuccess;
+  if (p.path == Path::kPromptTc) {
+    e = kvq::launch_prompt_tc(p.a, p.workspace, p.max_rows_per_seq, *p.f, st, ap);
+  } else if (p.path == Path::kPrefillTc) {
+    e = kvq::launch_prefill_tc(p.a, *p.f, p.max_rows_per_seq, st, ap);
+  } else {
+    if (ap) e = kvq::launch_append(*ap, *p.f, st);
+    if (e == cudaSuccess) e = kvq::launch_decode(p.a, *p.f, num_sms_current(), st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return KVQ_OK;
 }
@@ -345,6 +353,42 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
   const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
   return attention_common(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, false, max_rows_per_seq,
                           q_raw, q_norm_w, out, out_is_f32, q_prepped, workspace, workspace_bytes, stream);
+}
+
+kvq_status attn_prefill_append(const kvq_layer* layer, const kvq_seq_cache* seqs, int32_t n_seqs,
+                               const int32_t* row_offsets, const int32_t* start_pos, int32_t n_rows,
+                               int32_t max_rows_per_seq, const uint16_t* q_raw, const uint16_t* k_raw,
+                               const uint16_t* v_raw, const uint16_t* q_norm_w, const uint16_t* k_norm_w,
+                               void* out, int32_t out_is_f32, uint16_t* q_prepped, uint16_t* kv_prepped,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_rows > 0 && !row_offsets) return fail(KVQ_EINVAL, "row_offsets is NULL");
+  if (max_rows_per_seq < 1 && n_rows > 0) return fail(KVQ_EINVAL, "max_rows_per_seq < 1");
+  const int32_t max_keys = layer && layer->window > 0 ? layer->window : (1 << 24);
+  Prepared p;
+  kvq_status st = attention_prepare(layer, seqs, n_seqs, row_offsets, start_pos, n_rows, max_keys, false,
+                                    max_rows_per_seq, q_raw, q_norm_w, out, out_is_f32, q_prepped, workspace,
+                                    workspace_bytes, &p);
+  if (st != KVQ_OK || p.empty) return st;
+  REQUIRE_PTR(k_raw, "k_raw", 16);
+  REQUIRE_PTR(k_norm_w, "k_norm_w", 2);
+  if (p.a.L.k_eq_v) {
+    if (v_raw) return fail(KVQ_EINVAL, "v_raw must be NULL when k_eq_v = 1");
+  } else {
+    REQUIRE_PTR(v_raw, "v_raw", 16);
+  }
+  if (kv_prepped && !aligned(kv_prepped, 2)) return fail(KVQ_EINVAL, "kv_prepped is not 2-byte aligned");
+  kvq::AppendArgs ap = {};
+  ap.L = p.a.L;
+  ap.seqs = seqs;
+  ap.n_seqs = n_seqs;
+  ap.row_offsets = row_offsets;
+  ap.start_pos = start_pos;
+  ap.n_rows = n_rows;
+  ap.k_raw = k_raw;
+  ap.v_raw = v_raw;
+  ap.k_w = k_norm_w;
+  ap.prepped = kv_prepped;
+  return attention_launch(p, static_cast<cudaStream_t>(stream), &ap);
 }
 
 size_t attn_prefill_workspace_bytes(const kvq_layer* layer, int32_t n_seqs, int32_t n_rows,
@@ -779,6 +823,64 @@ kvq_status attn_train_forward(const kvq_layer* layer, int32_t n_blocks, const in
   const cudaError_t e = kvq::launch_train(t, q_raw, q_norm_w, k_hat, v_hat, q_prepped, workspace, max_block_rows, f,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_train_forward launch");
+  return KVQ_OK;
+}
+
+kvq_status attn_train_donor_forward(const kvq_layer* layer, int32_t n_blocks, const int32_t* block_offsets,
+                                    int32_t n_rows, int32_t max_block_rows, const uint16_t* q_raw,
+                                    const uint16_t* k_raw, const uint16_t* v_raw, const uint16_t* q_norm_w,
+                                    const uint16_t* k_norm_w, uint16_t* k_hat, uint16_t* v_hat, void* out,
+                                    int32_t out_is_f32, uint16_t* q_prepped, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  kvq::LayerArgs L;
+  kvq_status st = check_train_layer(layer, &L);
+  if (st != KVQ_OK) return st;
+  if (!kvq::train_supported(L))
+    return fail(KVQ_EUNSUPPORTED, "training read: n_q_heads / n_kv_heads = %d must divide 128", L.G);
+  if ((st = check_layout(n_blocks, block_offsets, n_rows)) != KVQ_OK) return st;
+  if (n_rows == 0) return KVQ_OK;
+  if (max_block_rows < 1 || max_block_rows > n_rows)
+    return fail(KVQ_EINVAL, "max_block_rows %d not in [1, n_rows]", max_block_rows);
+  REQUIRE_PTR(q_raw, "q_raw", 16);
+  REQUIRE_PTR(q_norm_w, "q_norm_w", 2);
+  REQUIRE_PTR(k_raw, "k_raw", 16);
+  REQUIRE_PTR(k_norm_w, "k_norm_w", 2);
+  if (L.k_eq_v) {
+    if (v_raw) return fail(KVQ_EINVAL, "v_raw must be NULL when k_eq_v = 1");
+  } else {
+    REQUIRE_PTR(v_raw, "v_raw", 16);
+  }
+  REQUIRE_PTR(k_hat, "k_hat", 16);
+  REQUIRE_PTR(v_hat, "v_hat", 16);
+  REQUIRE_PTR(out, "out", out_is_f32 ? 4 : 2);
+  REQUIRE_PTR(workspace, "workspace", 256);
+  if (q_prepped && !aligned(q_prepped, 2)) return fail(KVQ_EINVAL, "q_prepped is not 2-byte aligned");
+  if (out_is_f32 != 0 && out_is_f32 != 1) return fail(KVQ_EINVAL, "out_is_f32 must be 0 or 1");
+  const size_t need = kvq::train_ws_bytes(n_rows, L);
+  if (workspace_bytes < need) return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  kvq::AppendArgs ap = {};
+  ap.L = L;
+  ap.seqs = nullptr;
+  ap.n_seqs = n_blocks;
+  ap.row_offsets = block_offsets;
+  ap.start_pos = nullptr;
+  ap.n_rows = n_rows;
+  ap.k_raw = k_raw;
+  ap.v_raw = v_raw;
+  ap.k_w = k_norm_w;
+  ap.out_k = k_hat;
+  ap.out_v = v_hat;
+  kvq::TrainArgs t = {};
+  t.L = L;
+  t.n_rows = n_rows;
+  t.n_blocks = n_blocks;
+  t.off = block_offsets;
+  t.out = out;
+  t.out_f32 = out_is_f32;
+  const kvq::RopeFreqs& f = rope_freqs(layer->rope_theta, L.D, L.rope_dims);
+  const cudaError_t e = kvq::launch_train(t, q_raw, q_norm_w, k_hat, v_hat, q_prepped, workspace, max_block_rows, f,
+                                          static_cast<cudaStream_t>(stream), &ap);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_train_donor_forward launch");
   return KVQ_OK;
 }
 

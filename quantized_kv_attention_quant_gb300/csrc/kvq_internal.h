@@ -122,7 +122,10 @@ int decode_max_splits(int n_rows, int n_kv, int D, size_t bytes);
 bool prefill_tc_supported(const LayerArgs& L);
 size_t prefill_tc_ws_bytes(int n_rows, const LayerArgs& L);
 DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L);
-cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st);
+// ap: NULL, or the rows' K/V append, run in the q prep's grid (the read that
+// follows reads the appended rows)
+cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st,
+                              const AppendArgs* ap = nullptr);
 
 cudaError_t launch_append(const AppendArgs& a, const RopeFreqs& f, cudaStream_t st);
 
@@ -137,9 +140,11 @@ struct TrainArgs {
 };
 bool train_supported(const LayerArgs& L);
 size_t train_ws_bytes(int n_rows, const LayerArgs& L);
+// ap: NULL, or the donor's K/V prep of the pass (writing k_hat / v_hat), run
+// in the q prep's grid
 cudaError_t launch_train(const TrainArgs& t, const uint16_t* q_raw, const uint16_t* q_w, const uint16_t* k_hat,
                          const uint16_t* v_hat, uint16_t* q_prepped, void* ws, int max_block_rows,
-                         const RopeFreqs& f, cudaStream_t st);
+                         const RopeFreqs& f, cudaStream_t st, const AppendArgs* ap = nullptr);
 // One CTA whose bounded wait on an mbarrier that nothing completes gives up
 // after limit_ns and flags the timeout bit in *status.
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st);

@@ -480,7 +480,8 @@ prefill_tc_kernel(const DecodeArgs a) {
 }
 
 template <int D>
-cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_rows, cudaStream_t st) {
+cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_rows, cudaStream_t st,
+                             const AppendArgs* ap) {
   cudaError_t e;
   constexpr int smem = Pf<D>::BYTES;
   static_assert(smem <= 227 * 1024, "shared memory");
@@ -505,7 +506,7 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
   }
   const int per_sm = 512 / Pf<D>::TMEM_COLS;
   const int launch_smem = per_sm >= 3 ? smem : std::max(smem, (228 * 1024) / (per_sm + 1) + 1024);
-  if ((e = launch_qprep_rows<D>(a, f, st)) != cudaSuccess) return e;
+  if ((e = launch_qprep_rows<D>(a, f, st, ap)) != cudaSuccess) return e;
   const int TQ = kRows / a.L.G;
   if (a.n_seqs > 65535 || a.L.n_kv > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, a.L.n_kv);
@@ -541,13 +542,14 @@ DecodeWs prefill_tc_ws_carve(void* base, int n_rows, const LayerArgs& L) {
   return w;
 }
 
-cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const DecodeArgs& a, const RopeFreqs& f, int max_rows_per_seq, cudaStream_t st,
+                              const AppendArgs* ap) {
   if (a.n_rows == 0) return cudaSuccess;
   // the status word is cleared by q prep, the first kernel of the call
   switch (a.L.D) {
-    case 64: return launch_prefill_t<64>(a, f, max_rows_per_seq, st);
-    case 128: return launch_prefill_t<128>(a, f, max_rows_per_seq, st);
-    case 256: return launch_prefill_t<256>(a, f, max_rows_per_seq, st);
+    case 64: return launch_prefill_t<64>(a, f, max_rows_per_seq, st, ap);
+    case 128: return launch_prefill_t<128>(a, f, max_rows_per_seq, st, ap);
+    case 256: return launch_prefill_t<256>(a, f, max_rows_per_seq, st, ap);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -558,7 +558,8 @@ PromptWs prompt_ws_carve(void* base, int n_seqs, int n_rows, int max_rows, const
 }
 
 template <int D>
-cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const RopeFreqs& f, cudaStream_t st) {
+cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const RopeFreqs& f, cudaStream_t st,
+                            const AppendArgs* ap) {
   static_assert(Pr<D>::BYTES <= 227 * 1024, "shared memory");
   cudaError_t e;
   static std::atomic<bool> attr_set[64];
@@ -590,7 +591,7 @@ cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const R
   qa.ws = DecodeWs{};
   qa.ws.status = w.status;
   qa.ws.q16 = w.q16;
-  if ((e = launch_qprep_rows<D>(qa, f, st)) != cudaSuccess) return e;
+  if ((e = launch_qprep_rows<D>(qa, f, st, ap)) != cudaSuccess) return e;
   PromptArgs pa;
   pa.L = L;
   pa.seqs = a.seqs;
@@ -630,12 +631,12 @@ size_t prompt_tc_ws_bytes(int n_seqs, int n_rows, int max_rows, const LayerArgs&
 }
 
 cudaError_t launch_prompt_tc(const DecodeArgs& a, void* ws, int max_rows_per_seq, const RopeFreqs& f,
-                             cudaStream_t st) {
+                             cudaStream_t st, const AppendArgs* ap) {
   if (a.n_rows == 0) return cudaSuccess;
   switch (a.L.D) {
-    case 64: return launch_prompt_t<64>(a, ws, max_rows_per_seq, f, st);
-    case 128: return launch_prompt_t<128>(a, ws, max_rows_per_seq, f, st);
-    case 256: return launch_prompt_t<256>(a, ws, max_rows_per_seq, f, st);
+    case 64: return launch_prompt_t<64>(a, ws, max_rows_per_seq, f, st, ap);
+    case 128: return launch_prompt_t<128>(a, ws, max_rows_per_seq, f, st, ap);
+    case 256: return launch_prompt_t<256>(a, ws, max_rows_per_seq, f, st, ap);
     default: return cudaErrorInvalidValue;
   }
 }

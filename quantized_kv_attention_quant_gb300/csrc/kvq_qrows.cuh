@@ -17,6 +17,7 @@
 #pragma once
 #include <algorithm>
 
+#include "kvq_append.cuh"
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "kvq_qprep.cuh"
@@ -26,9 +27,10 @@ namespace {
 
 constexpr int kQrWarps = 8;
 
+// One block: rows bx*rb .. bx*rb + rb - 1 of the call `a`.
 template <int D>
-__global__ void __launch_bounds__(kQrWarps * 32)
-qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
+__device__ __forceinline__ void qprep_rows_block(const DecodeArgs& a, const RopeFreqs& freqs, const int rb,
+                                                 const int bx) {
   constexpr int E = D / 32;                 // elements per lane
   constexpr int NG = D / 64, LPG = 64 / E;  // 64-dim groups; lanes per group
   extern __shared__ __align__(16) uint8_t qr_smem[];
@@ -41,8 +43,8 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
   uint16_t* nrm = reinterpret_cast<uint16_t*>(qr_smem + (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4));
   // per warp: the normed row, then the rotated dims
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row0 = blockIdx.x * rb;
-  if (blockIdx.x == 0 && tid == 0) *a.ws.status = 0u;    // the first kernel of the call
+  const int row0 = bx * rb;
+  if (bx == 0 && tid == 0) *a.ws.status = 0u;            // the first kernel of the call
 
   float wq[E];                                          // (the weights are only 2-byte aligned)
 #pragma unroll
@@ -177,6 +179,28 @@ qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
   }
 }
 
+template <int D>
+__global__ void __launch_bounds__(kQrWarps * 32)
+qprep_rows_kernel(const DecodeArgs a, const RopeFreqs freqs, const int rb) {
+  qprep_rows_block<D>(a, freqs, rb, blockIdx.x);
+}
+
+// The q prep of a call together with the K/V prep of its rows (the append of
+// attn_prefill_append, the donor's K/V of attn_train_donor_forward) in one
+// grid: blocks below nq prep q, the others each take one row's block of ipb
+// append items (ablk blocks per row).  The halves share nothing.
+template <int D>
+__global__ void __launch_bounds__(kQrWarps * 32)
+qprep_rows_append_kernel(const DecodeArgs a, const AppendArgs ap, const RopeFreqs freqs, const int rb,
+                         const int nq, const int ipb, const int ablk) {
+  if ((int)blockIdx.x < nq) {
+    qprep_rows_block<D>(a, freqs, rb, blockIdx.x);
+  } else {
+    const int b = blockIdx.x - nq;
+    append_block<D>(ap, freqs, ipb, b / ablk, b % ablk);
+  }
+}
+
 // rows per block: enough (row, head) items for the 8 warps, angle tables of
 // at most 16 KB
 inline int qprep_rows_rb(const LayerArgs& L) {
@@ -186,12 +210,25 @@ inline int qprep_rows_rb(const LayerArgs& L) {
   return rb;
 }
 
+// ap: NULL, or the append whose blocks share the q prep's grid (its rows
+// need not be the q rows: the training read's K/V rows are those of the pass)
 template <int D>
-cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st) {
+cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st,
+                              const AppendArgs* ap = nullptr) {
   const int rb = qprep_rows_rb(a.L);
   const int half = a.L.rope_dims / 2;
   const size_t smem = (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * 2 * D * 2;
-  qprep_rows_kernel<D><<<(a.n_rows + rb - 1) / rb, kQrWarps * 32, smem, st>>>(a, f, rb);
+  const int nq = (a.n_rows + rb - 1) / rb;
+  if (!ap || ap->n_rows == 0) {
+    qprep_rows_kernel<D><<<nq, kQrWarps * 32, smem, st>>>(a, f, rb);
+    return cudaGetLastError();
+  }
+  const int items = 2 * ap->L.n_kv;
+  const int ipb = std::min(items, kQrWarps * 32 / App<D>::TH);
+  const int ablk = (items + ipb - 1) / ipb;
+  const long long blocks = (long long)nq + (long long)ap->n_rows * ablk;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  qprep_rows_append_kernel<D><<<(unsigned)blocks, kQrWarps * 32, smem, st>>>(a, *ap, f, rb, nq, ipb, ablk);
   return cudaGetLastError();
 }
 

@@ -467,7 +467,7 @@ int train_launch_smem() {
 template <int D>
 cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint16_t* q_w, const uint16_t* k_hat,
                            const uint16_t* v_hat, uint16_t* q_prepped, void* ws, int max_block_rows,
-                           const RopeFreqs& f, cudaStream_t st) {
+                           const RopeFreqs& f, cudaStream_t st, const AppendArgs* ap) {
   static_assert(Tr<D>::BYTES <= 227 * 1024, "shared memory");
   cudaError_t e;
   static std::atomic<bool> attr_set[64];
@@ -507,7 +507,7 @@ cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint
   qa.q_prepped = q_prepped;
   qa.ws.status = status;
   qa.ws.qhat = qhat;
-  if ((e = launch_qprep_rows<D>(qa, f, st)) != cudaSuccess) return e;
+  if ((e = launch_qprep_rows<D>(qa, f, st, ap)) != cudaSuccess) return e;
   if (t.n_blocks > 65535 || L.n_kv * Tr<D>::NSPLIT > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_block_rows + TQ - 1) / TQ, t.n_blocks, L.n_kv * Tr<D>::NSPLIT);
   train_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(t, status, mq, mk, mv);
@@ -527,13 +527,13 @@ size_t train_ws_bytes(int n_rows, const LayerArgs& L) {
 
 cudaError_t launch_train(const TrainArgs& t, const uint16_t* q_raw, const uint16_t* q_w, const uint16_t* k_hat,
                          const uint16_t* v_hat, uint16_t* q_prepped, void* ws, int max_block_rows,
-                         const RopeFreqs& f, cudaStream_t st) {
+                         const RopeFreqs& f, cudaStream_t st, const AppendArgs* ap) {
   if (t.n_rows == 0) return cudaSuccess;
   switch (t.L.D) {
-    case 64: return launch_train_t<64>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st);
-    case 128: return launch_train_t<128>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st);
-    case 256: return launch_train_t<256>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st);
-    case 512: return launch_train_t<512>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st);
+    case 64: return launch_train_t<64>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st, ap);
+    case 128: return launch_train_t<128>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st, ap);
+    case 256: return launch_train_t<256>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st, ap);
+    case 512: return launch_train_t<512>(t, q_raw, q_w, k_hat, v_hat, q_prepped, ws, max_block_rows, f, st, ap);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,8 +15,9 @@ import torch
 import workloads as W
 
 from . import (KVQ_PHASE_DECODE, KVQ_PHASE_WINDOW, attn_decode, attn_decode_append, attn_decode_workspace_bytes,
-               attn_group, attn_mixed, attn_prefill_chunk, attn_prefill_workspace_bytes, attn_train_forward,
-               attn_train_workspace_bytes, kv_quant_append, kvq_train_kv_prep, layer as make_layer)
+               attn_group, attn_mixed, attn_prefill_append, attn_prefill_chunk, attn_prefill_workspace_bytes,
+               attn_train_donor_forward, attn_train_forward, attn_train_workspace_bytes, kv_quant_append,
+               kvq_train_kv_prep, layer as make_layer)
 from .cache import LayerCaches
 
 
@@ -219,6 +220,12 @@ class PrefillCase:
                            self.max_rows, self.q, self.q_w, self.out, self.out_f32, self.q_prepped, self.ws,
                            self.ws_bytes, stream)
 
+    def append_attend(self, stream=None):
+        """append + attend as one attn_prefill_append call."""
+        attn_prefill_append(self.lay, self.caches.desc, self.wl.n_seqs, self.offs, self.start, self.n_rows,
+                            self.max_rows, self.q, self.k, self.v, self.q_w, self.k_w, self.out, self.out_f32,
+                            self.q_prepped, self.kv_prepped, self.ws, self.ws_bytes, stream)
+
     def step(self, stream=None):
         self.append(stream)
         self.attend(stream)
@@ -371,7 +378,16 @@ class TrainCase:
         """The donor's part of a step (the name the step drivers use)."""
         self.prep_kv(stream)
 
-    def step(self, stream=None):
+    def append_attend(self, stream=None):
+        """A donor's K/V prep and read as one attn_train_donor_forward call."""
+        attn_train_donor_forward(self.lay, self.n_blocks, self.offs, self.n_rows, self.max_rows, self.q, self.k,
+                                 self.v, self.q_w, self.k_w, self.k_hat, self.v_hat, self.out, self.out_f32,
+                                 self.q_prepped, self.ws, self.ws_bytes, stream)
+
+    def step(self, stream=None, fused=False):
+        if self.donor and fused:
+            self.append_attend(stream)
+            return
         if self.donor:
             self.prep_kv(stream)
         self.attend(stream)
@@ -400,6 +416,6 @@ class TrainStackCase:
             self.layers.append((i, d, case))
         self.n_rows = int(sum(blocks))
 
-    def step(self, stream=None):
+    def step(self, stream=None, fused=True):
         for _, _, case in self.layers:
-            case.step(stream)
+            case.step(stream, fused=fused)

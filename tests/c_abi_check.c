@@ -23,7 +23,8 @@
 typedef void (*any_fn)(void);
 static const any_fn kAll[] = {
     (any_fn)&kv_quant_append,        (any_fn)&attn_decode,
-    (any_fn)&attn_decode_append,
+    (any_fn)&attn_decode_append,     (any_fn)&attn_prefill_append,
+    (any_fn)&attn_train_donor_forward,
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
     (any_fn)&attn_mixed_schedule,

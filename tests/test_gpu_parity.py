@@ -675,6 +675,49 @@ def test_prefill_tc_shapes(kvq, name):
     print(name, "worst", worst)
 
 
+def _bits32(t):
+    """A tensor's bytes as int32 (NaN rows compare equal bit for bit)."""
+    return t.contiguous().view(torch.int32) if t.element_size() == 4 else t.contiguous().view(torch.int16)
+
+
+# attn_prefill_append: the chunk's append and read in one call, bit-equal to
+# kv_quant_append + attn_prefill_chunk on each path: the dequantize-once
+# tensor-core path (sliding), the codes-in-MMA tensor-core path (full, D128),
+# the row path (D512; verify windows of at most 16 rows), and a chunk longer
+# than its window ring (rows whose window reaches an overwritten key: NaN).
+PREFILL_FUSED_CASES = {
+    "sliding-prompt-tc": (_spec(8, 2, 256, 512, 256), [300, 0, 1000], [37, 130, 64], [8, 4, 4]),
+    "full-d128-prefill-tc": (_spec(8, 1, 128, 0, 128, 1e6), [200, 5], [40, 17], [4, 8]),
+    "full-keqv-d512-rows": (_spec(16, 1, 512, 0, 128, 1e6, True), [90, 3], [5, 17], [8, 4]),
+    "verify-sliding-rows": (_spec(8, 2, 256, 512, 256), [100, 700, 0], [4, 16, 1], [4, 8, 8]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_FUSED_CASES) + ["ring-overflow"])
+def test_prefill_append_equals_separate_calls(kvq, name):
+    _, harness = kvq
+    if name == "ring-overflow":
+        wl = W.PrefillWorkload("fused-overflow", 98, _spec(4, 1, 128, 64, 128), filled=[10], chunk=[300], bits=[4])
+        wl.capacity = lambda s: 192
+        wl.cached_positions = lambda s: np.arange(0, 10)
+    else:
+        spec, filled, chunk, bits = PREFILL_FUSED_CASES[name]
+        wl = W.PrefillWorkload("fused-" + name, 98, spec, filled=filled, chunk=chunk, bits=bits)
+    a = harness.PrefillCase(wl, keep_prepped=True)
+    b = harness.PrefillCase(wl, keep_prepped=True)
+    a.step()
+    b.append_attend()
+    torch.cuda.synchronize()
+    assert a.status_word() == b.status_word()
+    for x, y in ((a.out, b.out), (a.q_prepped, b.q_prepped), (a.kv_prepped, b.kv_prepped)):
+        assert torch.equal(_bits32(x), _bits32(y))
+    for s_ in range(wl.n_seqs):
+        for key in a.caches.seqs[s_]:
+            assert torch.equal(a.caches.seqs[s_][key], b.caches.seqs[s_][key]), (s_, key)
+    if name != "ring-overflow":
+        verify_prefill(b, wl)
+
+
 def test_prefill_bf16_output_is_rounded_f32(kvq):
     _, harness = kvq
     spec = _spec(8, 2, 256, 64, 256)

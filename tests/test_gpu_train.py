@@ -91,6 +91,24 @@ def test_train_small(kvq, name):
     check_train(harness, W.TrainWorkload(name, 71, spec, blocks))
 
 
+@pytest.mark.parametrize("name", ["d256-sliding-prefix", "d512-keqv-full", "d64-gqa16-no-prefix"])
+def test_train_donor_forward_equals_separate_calls(kvq, name):
+    """attn_train_donor_forward (the donor's K/V prep in the grid of the read's
+    q prep) gives the bytes of kvq_train_kv_prep + attn_train_forward."""
+    _, harness = kvq
+    spec, blocks = TRAIN_CASES[name]
+    wl = W.TrainWorkload("fused-" + name, 75, spec, blocks)
+    a = harness.TrainCase(wl, keep_prepped=True, layer_id=5)
+    b = harness.TrainCase(wl, keep_prepped=True, layer_id=5)
+    a.step()
+    b.step(fused=True)
+    torch.cuda.synchronize()
+    assert a.status_word() == b.status_word() == 0
+    for x, y in ((a.out, b.out), (a.q_prepped, b.q_prepped), (a.k_hat, b.k_hat), (a.v_hat, b.v_hat)):
+        assert torch.equal(x, y)
+    verify_train(b, wl, 5)
+
+
 def test_train_sharer_reads_donor_kv(kvq):
     """A KV-sharing layer (its own q rows and weights) reads the donor's plain
     keys and values."""
