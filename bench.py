@@ -329,8 +329,8 @@ def build_workload(name: str, rank: int, device):
             for t in range(wl.chunk[s]):
                 flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
         info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
-                "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05) with its q prep and key "
-                            "dequantization", "launches": 3,     # the append runs in the q prep's grid
+                "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05)",
+                "launches": 3,                        # the append runs in the q prep's grid
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     if name == "train42":
@@ -341,7 +341,7 @@ def build_workload(name: str, rank: int, device):
         flops = sum(4 * c.spec.n_q_heads * c.spec.head_dim * train_visible_total(blocks, c.spec.window)
                     for _, c in calls)
         info = {"tokens": case.n_rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
-                "dominant": "train_tc_kernel<256|512> with its q prep (tcgen05)",
+                "dominant": "train_tc_kernel<256|512> (tcgen05)",
                 "launches": 42 * 2,                   # donors' K/V prep in the q prep's grid
                 "config": {"workload": "training forward's stateless read over the 42-layer stack, one packed "
                                        f"sequence of {case.n_rows} rows: a prefix of {blocks[0]} rows shared by "
@@ -483,6 +483,35 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
         res["dom_call_ms"] = [sum(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)) / K
                               for j in range(len(full_calls))]
     del graph
+    if have_inner and not info.get("mixed"):
+        # the dominant kernel alone: the same steps, with the library recording
+        # an event pair right around each dominant call's attention kernel
+        # (kvq_profile_next_read; these records remove that kernel's overlap
+        # with its neighbours, so this graph is replayed apart from the timed one)
+        from quantized_kv_attention_quant_gb300 import kvq_profile_next_read
+        evk = [[ev_pair() for _ in full_calls] for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for row in evk:
+                for x, y in row:                 # create the events before the capture
+                    x.record()
+                    y.record()
+        torch.cuda.synchronize()
+        g_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_k, stream=stream):
+            for k in range(K):
+                j = 0
+                for donor, c in calls:
+                    if c in full_calls:
+                        kvq_profile_next_read(*evk[k][j])
+                        j += 1
+                    run_call(donor, c)
+        torch.cuda.synchronize()
+        g_k.replay()
+        torch.cuda.synchronize()
+        res["kern_call_ms"] = [sum(evk[k][j][0].elapsed_time(evk[k][j][1]) for k in range(K)) / K
+                               for j in range(len(full_calls))]
+        res["kern_ms"] = sum(res["kern_call_ms"])
+        del g_k
     if any(fusable(d, c) for d, c in calls) and not info.get("mixed"):
         # the same steps with every donor's append as its own kv_quant_append
         # call before its attn_decode (the same timing events around the
@@ -549,22 +578,31 @@ def measure(workload, case, calls, info, K, warmup, device, world, with_breakdow
 
 
 def roofline(workload, info, res, peaks):
-    """The dominant kernel's roofline object from the events inside the graph."""
+    """The dominant kernel's roofline object: algorithmic work over the
+    kernel's own launch durations (event pairs the library records right
+    around it, `kern_ms`), and beside it the same over the whole calls (q
+    prep, the donor's append, the kernel and the merge: events around each
+    call inside the timed graph, `dom_ms`)."""
     dom_ms = res.get("dom_ms")
     if not dom_ms:
         return None
+    kern_ms = res.get("kern_ms") or dom_ms
     n_calls = max(1, len(res["full_calls"]))
     if workload in ("prefill", "train42"):
-        achieved = info["flops"] / (dom_ms / 1e3) / 1e12
+        achieved = info["flops"] / (kern_ms / 1e3) / 1e12
+        call = info["flops"] / (dom_ms / 1e3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                 "peak_source": peaks["source"] + " bf16 burst (f16 runs at the bf16 rate)",
-                "kernel": info["dominant"], "launch_ms": dom_ms / n_calls}
-    achieved = info["dominant_bytes"] / (dom_ms / 1e3) / 1e9
+                "kernel": info["dominant"], "launch_ms": kern_ms / n_calls,
+                "call": {"achieved": call, "frac": call / peaks["bf16_tflops"], "ms": dom_ms / n_calls}}
+    achieved = info["dominant_bytes"] / (kern_ms / 1e3) / 1e9
+    call = info["dominant_bytes"] / (dom_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "frac_of_nominal_8000": achieved / 8000.0,
             "traffic": None, "peak_source": peaks["source"], "kernel": info["dominant"],
-            "launch_ms": dom_ms / n_calls}
+            "launch_ms": kern_ms / n_calls,
+            "call": {"achieved": call, "frac": call / peaks["hbm_gbs"], "ms": dom_ms / n_calls}}
     # DRAM traffic per launch from the committed ncu summaries, keyed by the
     # kernel's sources and the cache bit width (weighted by each call's bytes)
     calls = res["full_calls"]
@@ -581,18 +619,22 @@ def roofline(workload, info, res, peaks):
 
 
 def bit_split(res, peaks):
-    """The dominant calls' bytes, time and HBM fraction per cache bit width."""
+    """The dominant kernel's bytes, time and HBM fraction per cache bit width
+    (kernel alone; `call_*`: the whole calls)."""
     out = {}
-    for c, ms in zip(res["full_calls"], res.get("dom_call_ms", [])):
+    kern = res.get("kern_call_ms") or res.get("dom_call_ms", [])
+    for c, ms, cms in zip(res["full_calls"], kern, res.get("dom_call_ms", [])):
         b = c.wl.bits[0]
-        o = out.setdefault(f"{b}bit", {"calls": 0, "bytes": 0, "ms": 0.0})
+        o = out.setdefault(f"{b}bit", {"calls": 0, "bytes": 0, "ms": 0.0, "call_ms": 0.0})
         o["calls"] += 1
         o["bytes"] += call_bytes(c)
         o["ms"] += ms
+        o["call_ms"] += cms
     for o in out.values():
         o["achieved_gbs"] = o["bytes"] / (o["ms"] / 1e3) / 1e9
         o["frac"] = o["achieved_gbs"] / peaks["hbm_gbs"]
         o["ms_per_call"] = o["ms"] / o["calls"]
+        o["call_frac"] = o["bytes"] / (o["call_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"]
     return out
 
 

@@ -486,6 +486,19 @@ kvq_status kvq_selftest_wait_timeout(uint32_t* status, uint64_t limit_ns, void* 
 
 /* Static message for a status code. */
 const char* kvq_status_string(kvq_status status);
+/*
+ * kvq_profile_next_read -- profiling: the calling host thread's next call
+ * that reads attention (attn_decode, attn_decode_append, attn_prefill_chunk,
+ * attn_prefill_append, attn_train_forward, attn_train_donor_forward; not
+ * attn_mixed) records start_event on its stream right before launching its
+ * attention kernel and stop_event right after, so that
+ * cudaEventElapsedTime gives that kernel's time alone.  Both are
+ * cudaEvent_t created with timing enabled, or both NULL (clears).  Inside a
+ * stream capture they are recorded as external event nodes.  Recording an
+ * event between two kernels of a call removes their programmatic overlap.
+ */
+kvq_status kvq_profile_next_read(void* start_event, void* stop_event);
+
 /* Message of the calling thread's most recent failing call ("" if none). */
 const char* kvq_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */

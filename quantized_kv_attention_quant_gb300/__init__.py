@@ -96,6 +96,8 @@ def _load():
     lib.kvq_static_status.restype = ctypes.c_int
     lib.kvq_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.kvq_selftest_wait_timeout.restype = ctypes.c_int
+    lib.kvq_profile_next_read.argtypes = [vp, vp]
+    lib.kvq_profile_next_read.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_last_error.argtypes = []
@@ -288,6 +290,15 @@ def kvq_selftest_wait_timeout(status, limit_ns, stream=None):
     """Run the kernels' bounded wait on an mbarrier nothing completes (see
     include/kvq.h); bit 1 of the device uint32 `status` is set when it gives up."""
     _check(lib.kvq_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)))
+
+
+def kvq_profile_next_read(start_event, stop_event):
+    """The next attention-reading call of this thread records the two events
+    (torch.cuda.Event with timing, already created, or raw cudaEvent_t
+    handles) around its attention kernel (see include/kvq.h)."""
+    def handle(e):
+        return None if e is None else int(getattr(e, "cuda_event", e))
+    _check(lib.kvq_profile_next_read(handle(start_event), handle(stop_event)))
 
 
 def kvq_status_string(status: int) -> str:

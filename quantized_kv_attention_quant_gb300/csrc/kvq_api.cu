@@ -76,6 +76,18 @@ int num_sms_current() {
   return n;
 }
 
+// kvq_profile_next_read's events for this host thread
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+cudaError_t prof_record(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  // inside a stream capture the record becomes a graph node that times the replay
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, st);
+}
+
 kvq_status check_layer(const kvq_layer* L, kvq::LayerArgs* out) {
   if (!L) return fail(KVQ_EINVAL, "layer is NULL");
   if (L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->n_q_heads % L->n_kv_heads)
@@ -249,6 +261,15 @@ kvq_status attention_common(const kvq_layer* layer, const kvq_seq_cache* seqs, i
 }
 
 }  // namespace
+
+namespace kvq {
+cudaError_t prof_before(cudaStream_t st) { return g_prof_start ? prof_record(g_prof_start, st) : cudaSuccess; }
+cudaError_t prof_after(cudaStream_t st) {
+  const cudaEvent_t ev = g_prof_stop;
+  g_prof_start = g_prof_stop = nullptr;
+  return ev ? prof_record(ev, st) : cudaSuccess;
+}
+}  // namespace kvq
 
 extern "C" {
 
@@ -569,6 +590,7 @@ extern "C" {
 kvq_status attn_mixed(const kvq_layer* layer, const kvq_attn_group* groups, int32_t n_groups,
                       const uint16_t* q_norm_w, int32_t out_is_f32, void* stream) {
   static thread_local MixedPlan mp;
+  g_prof_start = g_prof_stop = nullptr;           // not a call kvq_profile_next_read times
   const kvq_status pst = mixed_prepare(layer, groups, n_groups, q_norm_w, out_is_f32, &mp);
   if (pst != KVQ_OK || n_groups == 0) return pst;
   const Prepared* p = mp.p;
@@ -881,6 +903,14 @@ kvq_status attn_train_donor_forward(const kvq_layer* layer, int32_t n_blocks, co
   const cudaError_t e = kvq::launch_train(t, q_raw, q_norm_w, k_hat, v_hat, q_prepped, workspace, max_block_rows, f,
                                           static_cast<cudaStream_t>(stream), &ap);
   if (e != cudaSuccess) return cuda_fail(e, "attn_train_donor_forward launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_profile_next_read(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(KVQ_EINVAL, "give both events or neither");
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
   return KVQ_OK;
 }
 

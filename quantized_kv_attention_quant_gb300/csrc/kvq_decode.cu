@@ -1046,6 +1046,7 @@ cudaError_t launch_read_merge_t(const DecodeArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
+  if ((e = prof_before(st)) != cudaSuccess) return e;
   if (a.L.rot)       // the deferred TurboQuant read: score scale, PV pre-scale, output un-rotation
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, true>, a, smem)
                       : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, true>, a, smem);
@@ -1053,6 +1054,7 @@ cudaError_t launch_read_merge_t(const DecodeArgs& a, cudaStream_t st) {
     e = a.sk_ctas > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, true, false>, a, smem)
                       : cudaLaunchKernelEx(&cfg, decode_kernel<D, false, false>, a, smem);
   if (e != cudaSuccess) return e;
+  if ((e = prof_after(st)) != cudaSuccess) return e;
 
   cfg.gridDim = dim3(a.n_rows, a.L.n_q);
   cfg.blockDim = dim3(D);

@@ -149,6 +149,11 @@ cudaError_t launch_train(const TrainArgs& t, const uint16_t* q_raw, const uint16
 // after limit_ns and flags the timeout bit in *status.
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, const RopeFreqs& f, int num_sms, cudaStream_t st);
+// Profiling (kvq_profile_next_read): the events the calling host thread's
+// next attention call records on its stream right before and right after
+// launching its attention kernel; prof_after also clears them.
+cudaError_t prof_before(cudaStream_t st);
+cudaError_t prof_after(cudaStream_t st);
 // The grouped launch (fixed-chunk plans in every group, ga.n >= 1).
 cudaError_t launch_decode_grouped(const GroupedDecode& ga, const RopeFreqs& f, cudaStream_t st);
 // attn_decode_append: one kernel preps q and appends each sequence's new K/V

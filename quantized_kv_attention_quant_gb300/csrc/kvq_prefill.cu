@@ -510,8 +510,10 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const RopeFreqs& f, int max_ro
   const int TQ = kRows / a.L.G;
   if (a.n_seqs > 65535 || a.L.n_kv > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, a.L.n_kv);
+  if ((e = prof_before(st)) != cudaSuccess) return e;
   prefill_tc_kernel<D><<<grid, kThreads, launch_smem, st>>>(a);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return prof_after(st);
 }
 
 }  // namespace

@@ -610,8 +610,10 @@ cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const R
   prompt_dequant_kernel<D><<<dim3(w.ks / kDqKeys, a.n_seqs, L.n_kv), 256, 0, st>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, L.n_kv);
+  if ((e = prof_before(st)) != cudaSuccess) return e;
   prompt_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(pa, mq, mkh, mkl, mv);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return prof_after(st);
 }
 
 }  // namespace

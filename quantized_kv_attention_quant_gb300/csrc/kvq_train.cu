@@ -510,7 +510,10 @@ cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint
   if ((e = launch_qprep_rows<D>(qa, f, st, ap)) != cudaSuccess) return e;
   if (t.n_blocks > 65535 || L.n_kv * Tr<D>::NSPLIT > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_block_rows + TQ - 1) / TQ, t.n_blocks, L.n_kv * Tr<D>::NSPLIT);
+  if ((e = prof_before(st)) != cudaSuccess) return e;
   train_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(t, status, mq, mk, mv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = prof_after(st)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -24,7 +24,7 @@ typedef void (*any_fn)(void);
 static const any_fn kAll[] = {
     (any_fn)&kv_quant_append,        (any_fn)&attn_decode,
     (any_fn)&attn_decode_append,     (any_fn)&attn_prefill_append,
-    (any_fn)&attn_train_donor_forward,
+    (any_fn)&attn_train_donor_forward, (any_fn)&kvq_profile_next_read,
     (any_fn)&attn_decode_workspace_bytes, (any_fn)&attn_prefill_chunk,
     (any_fn)&attn_prefill_workspace_bytes, (any_fn)&attn_mixed,
     (any_fn)&attn_mixed_schedule,
@@ -82,6 +82,8 @@ int main(void) {
   CHECK(attn_decode_static(&L, NULL, 1, NULL, -1, NULL, NULL, NULL, 1, NULL, NULL) == KVQ_EINVAL);
   CHECK(kvq_selftest_wait_timeout(NULL, 1000000, NULL) == KVQ_EINVAL);
   CHECK(kvq_static_status(NULL, NULL) == KVQ_EINVAL);
+  CHECK(kvq_profile_next_read((void*)&L, NULL) == KVQ_EINVAL);
+  CHECK(kvq_profile_next_read(NULL, NULL) == KVQ_OK);
   CHECK((KVQ_STATUS_WAIT_TIMEOUT & KVQ_STATUS_SEQ_SKIPPED) == 0);
   CHECK(attn_train_workspace_bytes(&L, 100) == 256 + 100u * 8u * 256u * 2u);
   CHECK(attn_train_forward(&L, 0, fake_offsets, 4, 4, NULL, NULL, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL) ==

@@ -190,6 +190,36 @@ def test_decode_append_equals_separate_calls(kvq, name):
     print(name, "worst", worst)
 
 
+def test_profile_events_time_the_attention_kernel(kvq):
+    """kvq_profile_next_read: the next call records the event pair around its
+    attention kernel (inside the call's own span); its outputs are those of a
+    plain call; the call after it records nothing."""
+    m, harness = kvq
+    spec, filled, bits = STREAM_K_CASES["sk-ragged-d512-keqv"]
+    wl = W.DecodeWorkload("profile", 95, spec, filled=filled, bits=bits)
+    case = harness.DecodeCase(wl)
+    case.step()
+    torch.cuda.synchronize()
+    want = case.out.clone()
+    k0, k1, c0, c1 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    k0.record()
+    k1.record()
+    torch.cuda.synchronize()
+    c0.record()
+    m.kvq_profile_next_read(k0, k1)
+    case.attend()
+    c1.record()
+    torch.cuda.synchronize()
+    kern, call = k0.elapsed_time(k1), c0.elapsed_time(c1)
+    assert 0 < kern <= call
+    assert torch.equal(case.out, want)
+    case.attend()                     # the pair is spent: the kernel's events stay as they were
+    torch.cuda.synchronize()
+    assert k0.elapsed_time(k1) == kern
+    with pytest.raises(m.KvqError):
+        m.kvq_profile_next_read(k0, None)
+
+
 def test_decode_append_skips_a_bad_sequence(kvq):
     """A sequence with an invalid descriptor inside a fused call: nothing of
     it is written, its output is NaN, the status word says so, and the other
