@@ -220,13 +220,12 @@ __device__ __forceinline__ void append_block(const AppendArgs& a, const RopeFreq
       for (int i = 0; i < E; ++i) {
         const int e = tt * E + i;
         if (e < R) {
-          const int j = e < half ? e : e - half;
+          // x_j cos - x_{j+h} sin below half, x_{j+h} cos + x_j sin above: one call
+          const bool lo = e < half;
+          const int j = lo ? e : e - half;
           const float4 cv = cs[j];
-          const ff cc = {cv.x, cv.y};
-          if (e < half)        // x_j cos - x_{j+h} sin
-            y[i] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w});
-          else                 // x_{j+h} cos + x_j sin
-            y[i] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
+          y[i] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[lo ? e + half : j]), ff{cv.x, cv.y},
+                          lo ? ff{cv.z, cv.w} : ff{-cv.z, -cv.w});
         }
       }
     }

@@ -166,11 +166,12 @@ __device__ __forceinline__ void qprep_block(const DecodeArgs& a, const RopeFreqs
     for (int i = 0; i < E; ++i) {
       const int e = tt * E + i;
       if (e < R) {
-        const int j = e < half ? e : e - half;
+        // x_e c - x_(e+h) s below half, x_e c + x_(e-h) s above: one call
+        const bool lo = e < half;
+        const int j = lo ? e : e - half;
         const float4 cv = cs[j];
-        const ff cc = {cv.x, cv.y};
-        y[i] = e < half ? rot_bf16(bf16_to_f(qh[e]), bf16_to_f(qh[e + half]), cc, ff{cv.z, cv.w})
-                        : rot_bf16(bf16_to_f(qh[e]), bf16_to_f(qh[j]), cc, ff{-cv.z, -cv.w});
+        y[i] = rot_bf16(bf16_to_f(qh[e]), bf16_to_f(qh[lo ? e + half : j]), ff{cv.x, cv.y},
+                        lo ? ff{cv.z, cv.w} : ff{-cv.z, -cv.w});
       }
     }
   }

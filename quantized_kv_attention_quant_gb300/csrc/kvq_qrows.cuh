@@ -126,11 +126,11 @@ __device__ __forceinline__ void qprep_rows_block(const DecodeArgs& a, const Rope
       __syncwarp();
       const float4* csr = cs + r * half;
       for (int e = lane; e < R; e += 32) {
-        const int j = e < half ? e : e - half;
+        const bool lo = e < half;
+        const int j = lo ? e : e - half;
         const float4 cv = csr[j];
-        const ff cc = {cv.x, cv.y};
-        rt[e] = e < half ? rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[e + half]), cc, ff{cv.z, cv.w})
-                         : rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[j]), cc, ff{-cv.z, -cv.w});
+        rt[e] = rot_bf16(bf16_to_f(nr[e]), bf16_to_f(nr[lo ? e + half : j]), ff{cv.x, cv.y},
+                         lo ? ff{cv.z, cv.w} : ff{-cv.z, -cv.w});
       }
       __syncwarp();
       if (lane * E < R) {                               // this lane holds rotated dims
