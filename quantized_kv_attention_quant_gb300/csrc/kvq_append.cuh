@@ -46,10 +46,15 @@ __device__ __forceinline__ int quant_code(float d, float s, float rcp) {
 }
 
 // Quantize this thread's E prepped values (one slice of a 64-group), pack the
-// codes little-endian and store them, the group's scale and its bias.
+// codes little-endian and store them, the group's scale and its bias.  With
+// shi non-null the dequantized values scale * code + bias (fp32, one
+// rounding) also go to shi as f16 and, with slo non-null, their remainders
+// v - f16(v) to slo as f16: the prompt read's scratch, as its dequantization
+// writes it from the stored codes, scale and bias.
 template <int D, int BITS>
 __device__ __forceinline__ void quantize_store(const uint16_t (&y)[App<D>::E], const kvq_seq_cache& c,
-                                               int kind, int head, int pos, int t) {
+                                               int kind, int head, int pos, int t, uint16_t* shi,
+                                               uint16_t* slo) {
   constexpr int E = App<D>::E;
   constexpr int TPG = App<D>::TPG;
   constexpr int NG = D / 64;
@@ -76,6 +81,19 @@ __device__ __forceinline__ void quantize_store(const uint16_t (&y)[App<D>::E], c
     int q = 0;
     if (sf != 0.f) q = min(max(quant_code(__fsub_rn(v[i], mn), sf, rcp), 0), TOP);
     code[i] = uint32_t(q);
+  }
+  if (shi) {                              // mn is a bf16 value: the stored bias exactly
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const float v0 = __fmaf_rn(sf, (float)code[i], mn), v1 = __fmaf_rn(sf, (float)code[i + 1], mn);
+      const __half2 h = __floats2half2_rn(v0, v1);
+      reinterpret_cast<uint32_t*>(shi)[i / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      if (slo) {
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(__fsub_rn(v0, hf.x), __fsub_rn(v1, hf.y));
+        reinterpret_cast<uint32_t*>(slo)[i / 2] = *reinterpret_cast<const uint32_t*>(&l);
+      }
+    }
   }
   const int slot = pos % c.capacity;
   const size_t rowi = (size_t)head * c.capacity + slot;
@@ -249,8 +267,25 @@ __device__ __forceinline__ void append_block(const AppendArgs& a, const RopeFreq
 
   // ---- quantize the 64-element group, pack, store ----
   if (!store) return;
-  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, tt);
-  else quantize_store<D, 8>(y, c, kind, head, pos, tt);
+  // the prompt read's scratch row of this position (rows of a sequence the
+  // read flags, and rows past the scratch slot, are not written)
+  uint16_t* shi = nullptr;
+  uint16_t* slo = nullptr;
+  if (a.sk_hi) {
+    const int start = pos - t_in, W = a.L.window;
+    const int q = pos - (W > 0 ? max(0, start - W + 1) : 0);
+    if (start >= 0 && start + rows_s - 1 < (1 << 24) && q < a.sks) {
+      const size_t o = (((size_t)s * a.sks + q) * Hkv + head) * D + tt * E;
+      if (kind == 0) {
+        shi = a.sk_hi + o;
+        slo = a.sk_lo + o;
+      } else {
+        shi = a.sv + o;
+      }
+    }
+  }
+  if (c.bits == 4) quantize_store<D, 4>(y, c, kind, head, pos, tt, shi, slo);
+  else quantize_store<D, 8>(y, c, kind, head, pos, tt, shi, slo);
 }
 
 }  // namespace

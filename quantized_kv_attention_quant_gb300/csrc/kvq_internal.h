@@ -38,6 +38,14 @@ struct AppendArgs {
   // to out_k / out_v [n_rows][n_kv][D], and nothing is quantized
   uint16_t* out_k;
   uint16_t* out_v;
+  // prompt chunks read on the dequantize-once tensor-core path (sk_hi
+  // non-null): each stored row's dequantized key (as k_hi + k_lo f16) or
+  // value (f16) also goes to the read's scratch [n_seqs * sks][n_kv][D],
+  // whose row 0 of sequence s is position max(0, start_pos[s] - window + 1)
+  uint16_t* sk_hi;
+  uint16_t* sk_lo;
+  uint16_t* sv;
+  int sks;
 };
 
 // Workspace of the attention calls, carved from the caller's buffer.

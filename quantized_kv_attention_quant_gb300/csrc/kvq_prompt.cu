@@ -92,11 +92,15 @@ struct PromptArgs {
 // ---------------------------------------------------------------------------
 constexpr int kDqKeys = 16;             // keys per block of the dequantization
 
+// Scratch rows bx * kDqKeys .. + kDqKeys - 1 of sequence s, kv head kvh.
+// appended: the call's append writes the rows of its own stored positions
+// (the chunk's rows a later row of the chunk does not overwrite) in the same
+// grid, so only the older keys are read here; they sit in ring slots the
+// append does not write.
 template <int D>
-__global__ void __launch_bounds__(256)
-prompt_dequant_kernel(const PromptArgs a) {
+__device__ __forceinline__ void prompt_dequant_block(const PromptArgs& a, const int bx, const int s, const int kvh,
+                                                     const bool appended) {
   constexpr int NG = D / 64;
-  const int s = blockIdx.y, kvh = blockIdx.z;
   const kvq_seq_cache c = a.seqs[s];
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
   const int rows_s = off1 - off0;
@@ -114,9 +118,10 @@ prompt_dequant_kernel(const PromptArgs a) {
   // the tiles that reach them (masked out of the scores) multiply finite values
   for (int i = threadIdx.x; i < kDqKeys * (D / 8); i += blockDim.x) {
     const int key = i / (D / 8), ch = i % (D / 8), g = ch / 8;
-    const int q = blockIdx.x * kDqKeys + key;             // scratch row in the slot
+    const int q = bx * kDqKeys + key;                     // scratch row in the slot
     const int p = kbase + q;
     const size_t o = (((size_t)s * a.ks + q) * a.L.n_kv + kvh) * D + ch * 8;
+    if (appended && p >= start && p >= klo && p <= khi) continue;   // the append's row
     if (p < klo || p > khi) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(a.k_hi + o) = z;
@@ -164,6 +169,28 @@ prompt_dequant_kernel(const PromptArgs a) {
   }
 }
 
+// The read's first kernel: the q prep of the chunk's rows (blocks below nq),
+// the call's K/V append (the next nap blocks, ablk per row, writing the
+// appended rows' scratch too) and the dequantization of the scratch (the
+// rest: slot blocks x sequences x kv heads), which share nothing.  (The
+// dequantization blocks placed among the others, every other block index,
+// made the prompt step slower: 0.093 -> 0.095 ms.)
+template <int D, bool APPEND>
+__global__ void __launch_bounds__(kQrWarps * 32, APPEND ? 5 : 1)
+prompt_prep_kernel(const DecodeArgs a, const AppendArgs ap, const PromptArgs pa, const RopeFreqs freqs,
+                   const int rb, const int nq, const int ipb, const int ablk, const int nap) {
+  const int b = blockIdx.x;
+  pdl_launch();                                           // the read may launch (it waits for this grid)
+  if (b < nq) {
+    qprep_rows_block<D>(a, freqs, rb, b);
+  } else if (APPEND && b < nq + nap) {
+    append_block<D>(ap, freqs, ipb, (b - nq) / ablk, (b - nq) % ablk);
+  } else {
+    const int x = b - nq - nap, nx = pa.ks / kDqKeys;
+    prompt_dequant_block<D>(pa, x % nx, (x / nx) % pa.n_seqs, x / (nx * pa.n_seqs), APPEND);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 2. the read
 // ---------------------------------------------------------------------------
@@ -208,6 +235,7 @@ prompt_tc_kernel(const PromptArgs a, const __grid_constant__ CUtensorMap tmq,
     }
   };
   if (!ok) {
+    pdl_wait();                                           // the prep grid clears the status word
     if (t0 == 0 && kvh == 0 && tid == 0) flag_error(a.status, KVQ_DEV_BADSEQ);
     write_nan_rows(false, [](int) { return true; });
     return;
@@ -277,6 +305,9 @@ prompt_tc_kernel(const PromptArgs a, const __grid_constant__ CUtensorMap tmq,
   __syncthreads();                                        // barriers initialised, tensor memory address written
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  // launched as a programmatic dependent of the prep grid: q, the scratch and
+  // the status word are read or written only after it is complete
+  pdl_wait();
   bool dead = false;
   auto wait = [&](uint64_t* bar, int parity) {
     if (!dead && !mbar_wait(bar, parity)) {
@@ -586,12 +617,12 @@ cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const R
       !rows_map(&mkl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w.k_lo, D, L.n_kv, srows, 1, kTileKeys) ||
       !rows_map(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w.v, D, L.n_kv, srows, 1, kTileKeys))
     return cudaErrorInvalidValue;
-  // q prep: q_hat as f16 rows (it also clears the status word)
+  // q prep (q_hat as f16 rows; it also clears the status word), the append
+  // and the dequantization in one grid
   DecodeArgs qa = a;
   qa.ws = DecodeWs{};
   qa.ws.status = w.status;
   qa.ws.q16 = w.q16;
-  if ((e = launch_qprep_rows<D>(qa, f, st, ap)) != cudaSuccess) return e;
   PromptArgs pa;
   pa.L = L;
   pa.seqs = a.seqs;
@@ -607,12 +638,44 @@ cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const R
   pa.k_lo = w.k_lo;
   pa.v = w.v;
   if (a.n_seqs > 65535 || L.n_kv > 65535) return cudaErrorInvalidValue;
-  prompt_dequant_kernel<D><<<dim3(w.ks / kDqKeys, a.n_seqs, L.n_kv), 256, 0, st>>>(pa);
+  AppendArgs apx = {};
+  int ipb = 1, ablk = 1;
+  long long nap = 0;
+  if (ap && ap->n_rows > 0) {
+    apx = *ap;
+    apx.sk_hi = w.k_hi;
+    apx.sk_lo = w.k_lo;
+    apx.sv = w.v;
+    apx.sks = w.ks;
+    const int items = 2 * L.n_kv;
+    ipb = std::min(items, kQrWarps * 32 / App<D>::TH);
+    ablk = (items + ipb - 1) / ipb;
+    nap = (long long)ap->n_rows * ablk;
+  }
+  const int rb = qprep_rows_rb(L);
+  const long long nq = (a.n_rows + rb - 1) / rb;
+  const long long ndq = (long long)(w.ks / kDqKeys) * a.n_seqs * L.n_kv;
+  if (nq + nap + ndq > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (nap > 0)
+    prompt_prep_kernel<D, true><<<(unsigned)(nq + nap + ndq), kQrWarps * 32, qprep_rows_smem(L, rb), st>>>(
+        qa, apx, pa, f, rb, (int)nq, ipb, ablk, (int)nap);
+  else
+    prompt_prep_kernel<D, false><<<(unsigned)(nq + ndq), kQrWarps * 32, qprep_rows_smem(L, rb), st>>>(
+        qa, apx, pa, f, rb, (int)nq, ipb, ablk, 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, L.n_kv);
   if ((e = prof_before(st)) != cudaSuccess) return e;
-  prompt_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(pa, mq, mkh, mkl, mv);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads + 32);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, prompt_tc_kernel<D>, pa, mq, mkh, mkl, mv)) != cudaSuccess) return e;
   return prof_after(st);
 }
 

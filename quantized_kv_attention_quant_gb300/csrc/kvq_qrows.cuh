@@ -210,14 +210,20 @@ inline int qprep_rows_rb(const LayerArgs& L) {
   return rb;
 }
 
+// dynamic shared memory of a q-prep block of rb rows: the angle table, the
+// frequencies, two rows per warp
+inline size_t qprep_rows_smem(const LayerArgs& L, int rb) {
+  const int half = L.rope_dims / 2;
+  return (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * 2 * L.D * 2;
+}
+
 // ap: NULL, or the append whose blocks share the q prep's grid (its rows
 // need not be the q rows: the training read's K/V rows are those of the pass)
 template <int D>
 cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStream_t st,
                               const AppendArgs* ap = nullptr) {
   const int rb = qprep_rows_rb(a.L);
-  const int half = a.L.rope_dims / 2;
-  const size_t smem = (size_t)rb * half * 16 + 16 * ((3 * half + 3) / 4) + (size_t)kQrWarps * 2 * D * 2;
+  const size_t smem = qprep_rows_smem(a.L, rb);
   const int nq = (a.n_rows + rb - 1) / rb;
   if (!ap || ap->n_rows == 0) {
     qprep_rows_kernel<D><<<nq, kQrWarps * 32, smem, st>>>(a, f, rb);
