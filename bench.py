@@ -290,8 +290,8 @@ def build_workload(name: str, rank: int, device):
         info = {"tokens": dwl.n_seqs + int(sum(pwl.chunk)), "kv_bytes": dec_by + win_by,
                 "dominant_bytes": dec_by + win_by,
                 "dominant": "attn_mixed call (decode group: decode_kernel<256>; window group: "
-                            "prompt_dequant_kernel<256> + prompt_tc_kernel<256>)",
-                "launches": 2 + 3 + 3, "mixed": True,
+                            "prompt_prep_kernel<256> + prompt_tc_kernel<256>)",
+                "launches": 2 + 3 + 2, "mixed": True,
                 "config": {"workload": "mixed step of one sliding layer (8q/2kv D256 W512): decode group of "
                                        f"{dwl.n_seqs} sequences (lengths U[1024,8192]) + window group of 2 prompt "
                                        "chunks of 256 rows, one attn_mixed call",
@@ -330,7 +330,7 @@ def build_workload(name: str, rank: int, device):
                 flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
         info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
                 "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05)",
-                "launches": 3,                        # the append runs in the q prep's grid
+                "launches": 2,                        # q prep, append, dequantization in one grid; the read
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     if name == "train42":
