@@ -180,12 +180,13 @@ __global__ void __launch_bounds__(kQrWarps * 32, APPEND ? 5 : 1)
 prompt_prep_kernel(const DecodeArgs a, const AppendArgs ap, const PromptArgs pa, const RopeFreqs freqs,
                    const int rb, const int nq, const int ipb, const int ablk, const int nap) {
   const int b = blockIdx.x;
-  pdl_launch();                                           // the read may launch (it waits for this grid)
   if (b < nq) {
     qprep_rows_block<D>(a, freqs, rb, b);
   } else if (APPEND && b < nq + nap) {
     append_block<D>(ap, freqs, ipb, (b - nq) / ablk, (b - nq) % ablk);
   } else {
+    pdl_wait();                                           // (launched as a programmatic dependent)
+    pdl_launch();
     const int x = b - nq - nap, nx = pa.ks / kDqKeys;
     prompt_dequant_block<D>(pa, x % nx, (x / nx) % pa.n_seqs, x / (nx * pa.n_seqs), APPEND);
   }
@@ -219,6 +220,7 @@ prompt_tc_kernel(const PromptArgs a, const __grid_constant__ CUtensorMap tmq,
   const int off0 = __ldg(a.row_offsets + s), off1 = __ldg(a.row_offsets + s + 1);
   const int rows_s = off1 - off0;
   const int t0 = blockIdx.x * TQ;
+  pdl_launch();                                           // the next call's first kernel waits for this grid
   if (t0 >= rows_s) return;
   const int start = __ldg(a.pos + s);
   const kvq_seq_cache c = a.seqs[s];
@@ -656,26 +658,16 @@ cudaError_t launch_prompt_t(const DecodeArgs& a, void* ws, int max_rows, const R
   const long long nq = (a.n_rows + rb - 1) / rb;
   const long long ndq = (long long)(w.ks / kDqKeys) * a.n_seqs * L.n_kv;
   if (nq + nap + ndq > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (nap > 0)
-    prompt_prep_kernel<D, true><<<(unsigned)(nq + nap + ndq), kQrWarps * 32, qprep_rows_smem(L, rb), st>>>(
-        qa, apx, pa, f, rb, (int)nq, ipb, ablk, (int)nap);
-  else
-    prompt_prep_kernel<D, false><<<(unsigned)(nq + ndq), kQrWarps * 32, qprep_rows_smem(L, rb), st>>>(
-        qa, apx, pa, f, rb, (int)nq, ipb, ablk, 0);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = nap > 0 ? launch_pdl(prompt_prep_kernel<D, true>, dim3((unsigned)(nq + nap + ndq)), dim3(kQrWarps * 32),
+                           qprep_rows_smem(L, rb), st, qa, apx, pa, f, rb, (int)nq, ipb, ablk, (int)nap)
+              : launch_pdl(prompt_prep_kernel<D, false>, dim3((unsigned)(nq + ndq)), dim3(kQrWarps * 32),
+                           qprep_rows_smem(L, rb), st, qa, apx, pa, f, rb, (int)nq, ipb, ablk, 0);
+  if (e != cudaSuccess) return e;
   const dim3 grid((max_rows + TQ - 1) / TQ, a.n_seqs, L.n_kv);
   if ((e = prof_before(st)) != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads + 32);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg, prompt_tc_kernel<D>, pa, mq, mkh, mkl, mv)) != cudaSuccess) return e;
+  if ((e = launch_pdl(prompt_tc_kernel<D>, grid, dim3(kThreads + 32), (size_t)smem, st, pa, mq, mkh, mkl, mv)) !=
+      cudaSuccess)
+    return e;
   return prof_after(st);
 }
 

@@ -44,7 +44,12 @@ __device__ __forceinline__ void qprep_rows_block(const DecodeArgs& a, const Rope
   // per warp: the normed row, then the rotated dims
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = bx * rb;
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // until that grid is complete only the library's frequency table is read
+  if (R > 0) stage_freqs(freqs.f, half, freq);
+  pdl_wait();
   if (bx == 0 && tid == 0) *a.ws.status = 0u;            // the first kernel of the call
+  pdl_launch();
 
   float wq[E];                                          // (the weights are only 2-byte aligned)
 #pragma unroll
@@ -55,7 +60,6 @@ __device__ __forceinline__ void qprep_rows_block(const DecodeArgs& a, const Rope
       const int row = row0 + tid;
       rpos[tid] = row < a.n_rows ? min(max(row_info(a, row).p, 0), (1 << 24) - 1) : 0;
     }
-    stage_freqs(freqs.f, half, freq);
     __syncthreads();
     for (int idx = tid; idx < rb * half; idx += kQrWarps * 32) {
       const int r = idx / half, j = idx - r * half;
@@ -225,17 +229,14 @@ cudaError_t launch_qprep_rows(const DecodeArgs& a, const RopeFreqs& f, cudaStrea
   const int rb = qprep_rows_rb(a.L);
   const size_t smem = qprep_rows_smem(a.L, rb);
   const int nq = (a.n_rows + rb - 1) / rb;
-  if (!ap || ap->n_rows == 0) {
-    qprep_rows_kernel<D><<<nq, kQrWarps * 32, smem, st>>>(a, f, rb);
-    return cudaGetLastError();
-  }
+  if (!ap || ap->n_rows == 0) return launch_pdl(qprep_rows_kernel<D>, dim3(nq), dim3(kQrWarps * 32), smem, st, a, f, rb);
   const int items = 2 * ap->L.n_kv;
   const int ipb = std::min(items, kQrWarps * 32 / App<D>::TH);
   const int ablk = (items + ipb - 1) / ipb;
   const long long blocks = (long long)nq + (long long)ap->n_rows * ablk;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  qprep_rows_append_kernel<D><<<(unsigned)blocks, kQrWarps * 32, smem, st>>>(a, *ap, f, rb, nq, ipb, ablk);
-  return cudaGetLastError();
+  return launch_pdl(qprep_rows_append_kernel<D>, dim3((unsigned)blocks), dim3(kQrWarps * 32), smem, st, a, *ap, f,
+                    rb, nq, ipb, ablk);
 }
 
 }  // namespace

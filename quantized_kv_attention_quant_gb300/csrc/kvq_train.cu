@@ -113,10 +113,12 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
   const int off0 = __ldg(a.off + b), off1 = __ldg(a.off + b + 1);
   const int P = __ldg(a.off + 1);                         // prefix rows
   const int t0 = blockIdx.x * TQ;
+  pdl_launch();                                           // the next call's first kernel waits for this grid
   // the layout as the rows of this block need it (uniform over the CTA)
   const bool ok = off0 >= 0 && off0 <= off1 && off1 <= a.n_rows && P >= 0 && P <= a.n_rows &&
                   (b == 0 ? off0 == 0 : off0 >= P) && (b + 1 < a.n_blocks || off1 == a.n_rows);
   if (!ok) {
+    pdl_wait();                                           // the q prep clears the status word
     if (blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) flag_error(status, KVQ_DEV_BADSEQ);
     return;
   }
@@ -196,6 +198,9 @@ train_tc_kernel(const TrainArgs a, uint32_t* status, const __grid_constant__ CUt
   __syncthreads();                                        // barriers initialised, tensor memory address written
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  // launched as a programmatic dependent of the q prep grid: q, the donor's
+  // keys and values and the status word are touched only after it is complete
+  pdl_wait();
   bool dead = false;
   auto wait = [&](uint64_t* bar, int parity) {
     if (!dead && !mbar_wait(bar, parity)) {
@@ -511,10 +516,10 @@ cudaError_t launch_train_t(const TrainArgs& t, const uint16_t* q_raw, const uint
   if (t.n_blocks > 65535 || L.n_kv * Tr<D>::NSPLIT > 65535) return cudaErrorInvalidValue;
   const dim3 grid((max_block_rows + TQ - 1) / TQ, t.n_blocks, L.n_kv * Tr<D>::NSPLIT);
   if ((e = prof_before(st)) != cudaSuccess) return e;
-  train_tc_kernel<D><<<grid, kThreads + 32, smem, st>>>(t, status, mq, mk, mv);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = prof_after(st)) != cudaSuccess) return e;
-  return cudaGetLastError();
+  if ((e = launch_pdl(train_tc_kernel<D>, grid, dim3(kThreads + 32), (size_t)smem, st, t, status, mq, mk, mv)) !=
+      cudaSuccess)
+    return e;
+  return prof_after(st);
 }
 
 }  // namespace
