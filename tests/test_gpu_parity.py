@@ -748,6 +748,33 @@ def test_prefill_append_equals_separate_calls(kvq, name):
         verify_prefill(b, wl)
 
 
+def test_prefill_append_skips_a_bad_sequence(kvq):
+    """attn_prefill_append on the dequantize-once tensor-core path with one
+    sequence whose descriptor is invalid: its cache and its rows' scratch are
+    not written, its output rows are NaN, the status word says so, and the
+    other sequences' outputs are those of the same call without it."""
+    _, harness = kvq
+    spec, filled, chunk, bits = PREFILL_FUSED_CASES["sliding-prompt-tc"]
+    wl = W.PrefillWorkload("fused-prefill-bad", 99, spec, filled=filled, chunk=chunk, bits=bits)
+    c = harness.PrefillCase(wl)
+    good = harness.PrefillCase(wl)
+    torch.cuda.synchronize()
+    before = c.caches.seqs[1]["k_codes"].clone()
+    bad = c.caches.desc.cpu().numpy().copy()
+    bad[56 + 48:56 + 52] = np.frombuffer(np.int32(5).tobytes(), np.uint8)      # seq 1: bits = 5
+    c.caches.desc.copy_(torch.from_numpy(bad))
+    c.append_attend()
+    good.append_attend()
+    torch.cuda.synchronize()
+    assert c.status_word() & (1 << 2)
+    assert torch.equal(before, c.caches.seqs[1]["k_codes"])
+    r0, r1 = chunk[0], chunk[0] + chunk[1]
+    out = c.out.cpu().numpy()
+    assert np.all(np.isnan(out[r0:r1]))
+    keep = list(range(r0)) + list(range(r1, sum(chunk)))
+    assert torch.equal(_bits32(c.out[keep]), _bits32(good.out[keep]))
+
+
 def test_prefill_bf16_output_is_rounded_f32(kvq):
     _, harness = kvq
     spec = _spec(8, 2, 256, 64, 256)
