@@ -8,7 +8,9 @@ The default workload is the 42-layer mixed decode step: 64 ragged sequences
 the e4b layer table, per-donor 4/8-bit caches, KV-shared layers 24..41.  Per
 step: 24 quantize-appends (q/k/v prep, quantize, pack) and 42 attention reads
 (split-K decode, combine), 64 decode tokens.  Other workloads (--workload):
-tiny, sliding16, full32k, prefill.
+stack42-e4b, tiny, sliding16, full32k (and its 8-bit and rotated forms),
+prefill, prefill-full (a head_dim-512 prompt chunk, row path), mixed,
+mixed-verify, train42.
 
 The timed region replays a CUDA graph holding K steps (inputs resident in
 HBM); `e2e` repeats K steps through the Python binding with inputs copied
@@ -319,8 +321,8 @@ def build_workload(name: str, rank: int, device):
                            "n_seqs": dwl.n_seqs + vwl.n_seqs, "decode_rows": dwl.n_seqs,
                            "window_rows": int(sum(vwl.chunk))}}
         return case, [(True, case)], info
-    if name == "prefill":
-        wl = W.workload_prefill_chunk()
+    if name in ("prefill", "prefill-full"):
+        wl = W.workload_prefill_chunk() if name == "prefill" else W.workload_prefill_full()
         case = harness.PrefillCase(wl, device=device, out_f32=False)
         spec = wl.layer
         rows = sum(wl.chunk)
@@ -328,9 +330,13 @@ def build_workload(name: str, rank: int, device):
         for s in range(wl.n_seqs):
             for t in range(wl.chunk[s]):
                 flops += 4 * spec.n_q_heads * spec.head_dim * visible_keys(wl.filled[s] + t, spec.window)
+        # head_dim 512 takes the row path: the append, then q prep, the
+        # decode kernel over every row and the merge
+        row_path = spec.head_dim > 256
         info = {"tokens": rows, "flops": flops, "kv_bytes": 0, "dominant_bytes": 0,
-                "dominant": f"prompt_tc_kernel<{spec.head_dim}> (tcgen05)",
-                "launches": 2,                        # q prep, append, dequantization in one grid; the read
+                "dominant": (f"decode_kernel<{spec.head_dim}> (row path)" if row_path
+                             else f"prompt_tc_kernel<{spec.head_dim}> (tcgen05)"),
+                "launches": 4 if row_path else 2,     # sliding: q prep, append, dequantization in one grid; the read
                 "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "rows": rows}}
         return case, [(True, case)], info
     if name == "train42":
@@ -369,7 +375,7 @@ def train_visible_total(blocks, window: int) -> int:
     return total
 
 
-METRIC = {"prefill": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)",
+METRIC = {"prefill": "prefill tokens/s", "prefill-full": "prefill tokens/s", "mixed": "mixed-step tokens/s (decode tokens + window rows)",
           "mixed-verify": "mixed-step tokens/s (decode tokens + window rows)",
           "train42": "training-read tokens/s"}
 
@@ -588,7 +594,7 @@ def roofline(workload, info, res, peaks):
         return None
     kern_ms = res.get("kern_ms") or dom_ms
     n_calls = max(1, len(res["full_calls"]))
-    if workload in ("prefill", "train42"):
+    if workload in ("prefill", "prefill-full", "train42"):
         achieved = info["flops"] / (kern_ms / 1e3) / 1e12
         call = info["flops"] / (dom_ms / 1e3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -876,7 +882,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="stack42",
                     choices=["stack42", "stack42-e4b", "tiny", "sliding16", "full32k", "full32k-8bit",
-                             "full32k-rot", "prefill", "mixed", "mixed-verify", "train42"])
+                             "full32k-rot", "prefill", "prefill-full", "mixed", "mixed-verify", "train42"])
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-results", action="store_true",

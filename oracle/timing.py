@@ -127,8 +127,8 @@ def build(workload: str, nseq: int, part=None):
         idx = share(idx_all)
         return ([SeqLayer(wl, s) for s in idx], len(idx),
                 f"{len(idx_all)} of {wl.n_seqs} sequences (indices {idx_all})")
-    if workload == "prefill":
-        wl = W.workload_prefill_chunk()
+    if workload in ("prefill", "prefill-full"):
+        wl = W.workload_prefill_chunk() if workload == "prefill" else W.workload_prefill_full()
         s = 0
         spec = wl.layer
         rows = 32

@@ -550,6 +550,11 @@ def test_workload_prefill(kvq):
     check_prefill(kvq[1], W.workload_prefill_chunk(), seqs=[2], rows=[0, 1, 255, 511])
 
 
+def test_workload_prefill_full(kvq):
+    """The head_dim-512 prompt chunk at full size (the row path)."""
+    check_prefill(kvq[1], W.workload_prefill_full(), seqs=[1], rows=[0, 1, 255, 511])
+
+
 # layers of the 42-layer step compared with the oracle: full donors with an
 # 8-bit (23) and a 4-bit (11) cache, the full sharer 41 (reads 23), the
 # sliding donor 22 and the sliding sharer 24 (reads 22)

@@ -250,6 +250,14 @@ def workload_prefill_chunk() -> PrefillWorkload:
                            filled=[8192] * 4, chunk=[512] * 4, bits=[8] * 4)
 
 
+def workload_prefill_full() -> PrefillWorkload:
+    """Prompt chunk on a full-attention layer: 4 sequences append 512 tokens
+    each onto 8192 cached tokens of a 4-bit cache; 16 q / 1 kv head, head_dim
+    512, K = V, partial RoPE on 128 dims."""
+    return PrefillWorkload("prefill-full-b4x512-8k-d512", 1009, FULL_KEQV,
+                           filled=[8192] * 4, chunk=[512] * 4, bits=[4] * 4)
+
+
 N_LAYERS = 42
 N_DONORS = 24
 
