@@ -250,7 +250,10 @@ kvq_status attn_prefill_chunk(const kvq_layer* layer, const kvq_seq_cache* seqs,
  * its read in one call: kv_quant_append of the chunk rows (row_offsets,
  * start_pos, n_rows as given), then attn_prefill_chunk of the same rows, bit
  * for bit.  On the tensor-core paths the append runs in the grid of the
- * call's q prep (the two share nothing), and the read follows; on the row
+ * call's q prep (the two share nothing; on sliding-window layers the append
+ * also writes the dequantized keys and values of the rows it stores into the
+ * read's workspace scratch, and the key dequantization in the same grid
+ * covers only the older keys), and the read follows; on the row
  * path (verify windows, head_dim 512, a rotated layer) the append comes
  * first.  k_raw / v_raw / k_norm_w / kv_prepped as for kv_quant_append
  * (kv_prepped: NULL or device bf16 [2][n_rows][n_kv_heads][head_dim]); every
